@@ -1,0 +1,489 @@
+"""Benchmark of the KDA operator on one GB300 (or N independent replicas under torchrun).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Default workload: the single-sequence prefill (B=1, H=32, T=8192, d_k=d_v=128, bf16 q/k/v, fp32
+gates and state).  One step is one kda_prefill call over that batch; `value` is prefill tokens/s
+with the inputs resident in HBM.  The same JSON line carries the batched decode workload
+(512 sequences x 32 heads of 128x128 fp32 state, 256 steps) as the `decode` object: steps/s and
+achieved state-HBM GB/s against the measured copy bandwidth.
+
+Other workloads (`--workload`): varlen_64 (64 packed sequences, ~291K tokens), append_1m (a
+1,032,192-token prefill followed by a 16,384-token append, H=8), decode_512x32.
+
+`--impl reference` times the float64 CPU oracle (a deliberately slow baseline) on the host cores on
+the same workload, metric and unit.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from kda_gated_delta_03_gb300 import inputs as I  # noqa: E402
+
+PREFILL_KERNEL_SRC = ["kda_gated_delta_03_gb300/csrc/kda_prefill_cc.cu"]
+DECODE_KERNEL_SRC = ["kda_gated_delta_03_gb300/csrc/kda_decode.cu"]
+METRIC = "KDA prefill tokens/s (H=32,d=128); decode steps/s and state HBM GB/s vs peak"
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# ----------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("gloo")
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (timing of the slowest replica)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# measurement helpers
+# ----------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def source_sha(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kind: str, paths):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    entry = json.load(open(path)).get(kind)
+    if not entry or entry.get("source_sha") != source_sha(paths):
+        return None
+    return entry.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------
+# workloads on the GPU
+# ----------------------------------------------------------------------------
+def to_dev(a, bf16=False, dev=None, pin=False):
+    import torch
+    a = np.ascontiguousarray(a)
+    t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if bf16 else torch.from_numpy(a)
+    if pin:
+        return t.pin_memory()
+    return t.to(dev)
+
+
+def prefill_bytes(tokens: int, H: int, dk: int, dv: int, esize: int, n_states_in: int, n_states_out: int) -> int:
+    """Algorithmic HBM bytes of one prefill: q, k, v, o in the storage dtype, fp32 alpha and beta, fp32 states."""
+    per_token_head = (2 * dk + dv) * esize + 4 * dk + 4 + dv * esize
+    return tokens * H * per_token_head + (n_states_in + n_states_out) * H * dk * dv * 4
+
+
+def decode_bytes_per_step(B: int, H: int, d: int, esize: int) -> int:
+    """Algorithmic HBM bytes of one decode step: state read + write, q, k, v, o, alpha, beta."""
+    return B * H * (2 * d * d * 4 + 4 * d * esize + 4 * d + 4)
+
+
+def gpu_prefill(inp, steps, warmup, dev, e2e_steps):
+    import torch
+    import kda_gated_delta_03_gb300 as kda
+    bf = inp["dtype"] == "bf16"
+    names = ("q", "k", "v", "beta", "alpha", "cu_seqlens")
+    host = {n: to_dev(inp[n], bf and n in ("q", "k", "v"), pin=True) for n in names}
+    d = {n: host[n].to(dev) for n in names}
+    s_in = None if inp["state_in"] is None else to_dev(inp["state_in"], dev=dev)
+    T, H, dv = inp["v"].shape
+    N = len(inp["cu_seqlens"]) - 1
+    dk = inp["dk"]
+    o = torch.empty((T, H, dv), dtype=d["q"].dtype, device=dev)
+    st = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    ws_bytes = kda.kda_prefill_workspace_size(N, T, H, dk, dv, d["q"].dtype)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    launches_per_call = 1 + (1 if ws_bytes > 0 else 0)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        kda.kda_prefill(d["q"], d["k"], d["v"], d["beta"], d["alpha"], d["cu_seqlens"], s_in, state_out=st, o=o,
+                        workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    # end to end: pinned host inputs -> device, the C-ABI call, outputs -> pinned host
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    st_h = torch.empty(st.shape, dtype=st.dtype).pin_memory()
+    s_in_h = None if s_in is None else s_in.cpu().pin_memory()
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names) + (
+        0 if s_in_h is None else s_in_h.numel() * 4)
+    d2h = o.numel() * o.element_size() + st.numel() * 4
+
+    def e2e_call():
+        for n in names:
+            d[n].copy_(host[n], non_blocking=True)
+        if s_in is not None:
+            s_in.copy_(s_in_h, non_blocking=True)
+        call()
+        o_h.copy_(o, non_blocking=True)
+        st_h.copy_(st, non_blocking=True)
+
+    for _ in range(2):
+        e2e_call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    return dict(total_ms=total_ms, ms_per_step=total_ms / steps, kernel_ms=kernel_ms, e2e_ms=e2e_ms, h2d=h2d,
+                d2h=d2h, launches=steps * launches_per_call, T=T, H=H, N=N)
+
+
+def gpu_decode(w, steps, warmup, dev, distinct=16):
+    """Batched decode: `steps` fused steps over the resident pool; step s uses input set s mod `distinct`."""
+    import torch
+    import kda_gated_delta_03_gb300 as kda
+    B, H, d, dt = w["B"], w["H"], w["dk"], w["dtype"]
+    bf = dt == "bf16"
+    pool = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    for b0 in range(0, B, 64):   # seeded N(0, 0.02) states, generated in slices to bound host memory
+        pool[b0:b0 + 64] = to_dev(I.random_state(min(64, B - b0), H, d, d, (w["seed"], b0)), dev=dev)
+    sets = []
+    for s in range(distinct):
+        st = I.decode_step_inputs(B, H, d, d, dt, w["seed"], s)
+        sets.append({n: to_dev(st[n], bf and n in ("q", "k", "v"), dev=dev) for n in ("q", "k", "v", "beta", "alpha")})
+    o = torch.empty((B, H, d), dtype=sets[0]["q"].dtype, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(i):
+        x = sets[i % distinct]
+        kda.kda_decode_step(x["q"], x["k"], x["v"], x["beta"], x["alpha"], pool, o=o)
+
+    for i in range(warmup):
+        call(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        call(i)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return dict(total_ms=total_ms, ms_per_step=total_ms / steps, kernel_ms=kernel_ms, launches=steps,
+                bytes_per_step=decode_bytes_per_step(B, H, d, 2 if bf else 4))
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle leg
+# ----------------------------------------------------------------------------
+def oracle_prefill_time(inp, threads):
+    from oracle import oracle as O
+    t0 = time.perf_counter()
+    O.prefill(inp, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_threads():
+    return max(1, os.cpu_count() or 1)
+
+
+# ----------------------------------------------------------------------------
+# main
+# ----------------------------------------------------------------------------
+def prefill_workload_inputs(name):
+    w = I.workload(name)
+    return w, I.prefill_inputs(w["seqlens"], w["H"], w["dk"], w["dv"], w["dtype"], w["seed"], state=w["state"])
+
+
+def roofline_obj(alg_bytes, kernel_ms, peaks, kind, src):
+    achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(kind, src),
+            "alg_bytes_per_launch": int(alg_bytes), "kernel_ms": round(kernel_ms, 4),
+            "peak_source": peaks["source"]}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import kda_gated_delta_03_gb300 as kda
+    from kda_gated_delta_03_gb300 import build
+    build.build()
+    kda.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    name = args.workload
+    line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic"}
+    if name == "decode_512x32":
+        w = I.workload(name)
+        barrier(world)
+        with ClockSampler(local_rank) as clk:
+            r = gpu_decode(w, args.steps, args.warmup, dev)
+        ms = max_over_ranks(r["ms_per_step"], world)
+        steps_s = world * 1e3 / ms
+        line.update(metric="KDA decode steps/s (512 seqs x 32 heads, d=128)", value=round(steps_s, 2),
+                    unit="steps/s", ms_per_step=round(ms, 4), dtype="f32",
+                    config={"workload": name, "B": w["B"], "H": w["H"], "d": w["dk"], "qkv": w["dtype"],
+                            "l2": "state pool (1 GiB) larger than L2"},
+                    roofline=roofline_obj(r["bytes_per_step"], r["kernel_ms"], peaks, "decode", DECODE_KERNEL_SRC),
+                    gpu_launches=r["launches"], clocks=clk.summary())
+        return line
+
+    if name == "append_1m":
+        return run_append(args, I.workload(name), dev, peaks, line, world, local_rank)
+    w, inp = prefill_workload_inputs(name)
+    barrier(world)
+    with ClockSampler(local_rank) as clk:
+        r = gpu_prefill(inp, args.steps, args.warmup, dev, args.e2e_steps)
+    ms = max_over_ranks(r["ms_per_step"], world)
+    e2e_ms = max_over_ranks(r["e2e_ms"], world)
+    tokens = r["T"]
+    esize = 2 if inp["dtype"] == "bf16" else 4
+    alg = prefill_bytes(tokens, r["H"], inp["dk"], inp["dv"], esize, 0 if inp["state_in"] is None else r["N"], r["N"])
+    line.update(value=round(world * tokens * 1e3 / ms, 1), unit="tokens/s", ms_per_step=round(ms, 4), dtype="f32",
+                config={"workload": name, "seqs": r["N"], "tokens": tokens, "H": r["H"], "d": inp["dk"],
+                        "qkv": inp["dtype"], "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{world}"},
+                roofline=roofline_obj(alg, r["kernel_ms"], peaks, "prefill", PREFILL_KERNEL_SRC),
+                e2e={"value": round(world * tokens * 1e3 / e2e_ms, 1), "unit": "tokens/s",
+                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+                gpu_launches=r["launches"], clocks=clk.summary())
+    if name == "prefill_8k" and not args.no_decode:
+        wd = I.workload("decode_512x32")
+        rd = gpu_decode(wd, wd["steps"], 3, dev)
+        dms = max_over_ranks(rd["ms_per_step"], world)
+        roof = roofline_obj(rd["bytes_per_step"], rd["kernel_ms"], peaks, "decode", DECODE_KERNEL_SRC)
+        line["decode"] = {"workload": "decode_512x32", "steps": wd["steps"], "steps_per_s": round(world * 1e3 / dms, 2),
+                          "tokens_per_s": round(world * wd["B"] * 1e3 / dms, 1), "ms_per_step": round(dms, 4),
+                          "state_hbm_gbs": roof["achieved"], "roofline": roof, "gpu_launches": rd["launches"]}
+        line["gpu_launches"] += rd["launches"]
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = cpu_threads()
+        secs = oracle_prefill_time(inp, threads)
+        line["cpu_baseline"] = {"value": round(tokens / secs, 1), "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle", "sample": f"the whole {name} workload once ({tokens} tokens x "
+                                                            f"{r['H']} heads), float64, {threads} threads"}
+    return line
+
+
+def run_append(args, w, dev, peaks, line, world, local_rank):
+    import torch
+    T1, T2 = w["seqlens"][0], w["append"]
+    full = I.prefill_inputs([T1 + T2], w["H"], w["dk"], w["dv"], w["dtype"], w["seed"])
+
+    def part(t0, t1):
+        d = dict(full)
+        for k in ("q", "k", "v", "beta", "alpha"):
+            d[k] = full[k][t0:t1]
+        d["cu_seqlens"] = I.cu_seqlens_of([t1 - t0])
+        return d
+
+    p1 = part(0, T1)
+    barrier(world)
+    with ClockSampler(local_rank) as clk:
+        r1 = gpu_prefill(p1, args.steps, args.warmup, dev, 1)
+    p2 = part(T1, T1 + T2)
+    p2["state_in"] = np.zeros((1, w["H"], w["dk"], w["dv"]), np.float32)
+    r2 = gpu_prefill(p2, args.steps, args.warmup, dev, 1)
+    ms1 = max_over_ranks(r1["ms_per_step"], world)
+    ms2 = max_over_ranks(r2["ms_per_step"], world)
+    alg1 = prefill_bytes(T1, w["H"], w["dk"], w["dv"], 2, 0, 1)
+    line.update(metric="KDA append-prefill tokens/s (H=8, d=128): 1,032,192-token prefill",
+                value=round(world * T1 * 1e3 / ms1, 1), unit="tokens/s", ms_per_step=round(ms1, 4), dtype="f32",
+                config={"workload": "append_1m", "prefill_tokens": T1, "append_tokens": T2, "H": w["H"],
+                        "d": w["dk"], "l2": "inputs larger than L2 (no flush)"},
+                roofline=roofline_obj(alg1, r1["kernel_ms"], peaks, "prefill", PREFILL_KERNEL_SRC),
+                e2e={"value": round(world * T1 * 1e3 / r1["e2e_ms"], 1), "unit": "tokens/s",
+                     "h2d_bytes_per_step": r1["h2d"], "d2h_bytes_per_step": r1["d2h"]},
+                append={"tokens_per_s": round(world * T2 * 1e3 / ms2, 1), "ms_per_step": round(ms2, 4),
+                        "roofline": roofline_obj(prefill_bytes(T2, w["H"], w["dk"], w["dv"], 2, 1, 1),
+                                                 r2["kernel_ms"], peaks, "prefill", PREFILL_KERNEL_SRC)},
+                gpu_launches=r1["launches"] + r2["launches"], clocks=clk.summary())
+    return line
+
+
+def run_reference(args, rank, world):
+    """The float64 CPU oracle on the host cores, one bounded sample of the workload per step."""
+    if rank != 0:
+        return None
+    name = args.workload
+    threads = cpu_threads()
+    if name == "decode_512x32":
+        from oracle import oracle as O
+        w = I.workload(name)
+        rows = 16          # bounded sample: 16 of the 512 sequences (all 32 heads) per step
+        pool = I.random_state(rows, w["H"], w["dk"], w["dv"], (w["seed"], 0)).astype(np.float64)
+        st = I.decode_step_inputs(rows, w["H"], w["dk"], w["dv"], w["dtype"], w["seed"], 0)
+        times = []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            O.decode_step(st, pool, threads=threads)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        per_step = statistics.mean(times) * w["B"] / rows
+        value = 1.0 / per_step
+        unit, metric = "steps/s", "KDA decode steps/s (512 seqs x 32 heads, d=128)"
+        sample = f"{rows} of {w['B']} sequences x {w['H']} heads per step, scaled to the full batch"
+        ms = per_step * 1e3
+    else:
+        w, inp = prefill_workload_inputs("prefill_8k" if name == "append_1m" else name)
+        tokens = int(inp["cu_seqlens"][-1])
+        times = []
+        for i in range(args.warmup + args.steps):
+            s = oracle_prefill_time(inp, threads)
+            if i >= args.warmup:
+                times.append(s)
+        secs = statistics.mean(times)
+        value, unit, metric = tokens / secs, "tokens/s", METRIC
+        sample = f"the whole {w['kind']} workload ({tokens} tokens x {w['H']} heads) per step"
+        ms = secs * 1e3
+    return {"impl": "reference", "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": name},
+            "cpu_baseline": {"value": round(value, 3), "unit": unit, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill_8k",
+                    choices=["prefill_8k", "varlen_64", "decode_512x32", "append_1m"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    rank, world, local_rank = dist_env()
+    dist_init(world)
+    line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world, local_rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,150 @@
+/*
+ * kda.h -- C ABI of libkda, a single-GPU (sm_103a) implementation of the Kimi
+ * Delta Attention (KDA) operator.
+ *
+ * The operator ("Kimi K3, explained", section "The math", and section "How
+ * Kimi Delta Attention works, step by step"): per head a fixed state S is
+ * decayed channel by channel, the delta rule erases what S returns for the key
+ * and writes the new value, and the query reads the result.  The page writes S
+ * as d_v x d_k with o_t = S_t q_t; this library stores the transpose,
+ * S[d_k][d_v] (d_v contiguous), so that
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * which is the same operator.  alpha_t in (0,1]^{d_k} is the per-channel decay
+ * (one value per key channel, which is what KDA adds over Gated DeltaNet),
+ * beta_t in [0,1] the write strength.  q and k are expected L2-normalised by the
+ * caller; the library does not renormalise.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major arrays,
+ *    owned by the caller.  The library never allocates, frees or retains them,
+ *    and keeps no state between calls except one 32-bit error word per device
+ *    (a static device variable, see kda_get_device_error).
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) on the current device.  Arguments are validated on
+ *    the host before anything is launched; a validation failure launches
+ *    nothing and returns the status.  Conditions only visible on the device
+ *    (inconsistent cu_seqlens contents, out-of-range state slots) make the
+ *    kernels skip the affected work and set bits of the device error word.
+ *  - Alignment: q, k, v, o, alpha, states 16 bytes; beta, cu_seqlens,
+ *    state_idx 4 bytes; workspace 256 bytes.
+ *  - dtype (kda_dtype) applies to q, k, v and o.  beta, alpha and the states
+ *    are always float32.
+ *  - Supported sizes: d_k == d_v in {16, 64, 128}.  Other sizes return
+ *    KDA_ERR_UNSUPPORTED.
+ *  - Numerics: log2(alpha) is clamped below at -15 per token (alpha >= 2^-15
+ *    ~= 3.1e-5 per token and channel); smaller alphas, including alpha = 0,
+ *    decay as if alpha were 2^-15.  Intermediates are float32 (bf16 tensor-core
+ *    operands only for the raw bf16 q, k, v).
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, bad scale        */
+    KDA_ERR_UNSUPPORTED = 2,  /* head size or dtype this build has no kernel for           */
+    KDA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the required size       */
+    KDA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed                      */
+    KDA_ERR_DEVICE = 5        /* kda_get_device_error found device-detected errors         */
+} kda_status;
+
+typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
+
+/* Bits of the device error word. */
+#define KDA_DEVERR_CU_SEQLENS 0x1u  /* cu_seqlens not monotone / cu[0] != 0 / cu[N] != total  */
+#define KDA_DEVERR_STATE_IDX 0x2u   /* decode state_idx entry outside [0, num_slots)          */
+
+/*
+ * Bytes of device workspace kda_prefill needs for this problem (0 is a valid
+ * answer).  Pure host function; never fails (returns 0 for invalid sizes).
+ */
+KDA_API size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                                  int32_t d_v, kda_dtype dt);
+
+/*
+ * Chunkwise-parallel prefill over packed variable-length sequences, with state
+ * in and state out ("Kimi K3, explained", section "Training in chunks": the
+ * sequence is split into chunks, the per-token decay-and-erase products inside
+ * a chunk are rewritten in WY form so most of the work becomes matrix
+ * products, and only the state is carried from chunk to chunk).  Results equal
+ * the token-by-token recurrence above up to rounding.  Append-prefill (the
+ * agentic workload of the hex-index review, where new context continues a long
+ * history) is this call with state_in set to an earlier call's state_out.
+ *
+ *   q, k        [total_tokens, H, d_k]  dtype dt
+ *   v           [total_tokens, H, d_v]  dtype dt
+ *   beta        [total_tokens, H]       float32, write strength in [0,1]
+ *   alpha       [total_tokens, H, d_k]  float32, per-channel decay in (0,1]
+ *   cu_seqlens  [num_seqs + 1]          int32 device array, cu[0] = 0,
+ *               non-decreasing, cu[num_seqs] = total_tokens; sequence n owns
+ *               tokens [cu[n], cu[n+1]).  Zero-length sequences are allowed:
+ *               their state_out is their state_in (or zero).
+ *   state_in    [num_seqs, H, d_k, d_v] float32, or NULL for zero states
+ *   state_out   [num_seqs, H, d_k, d_v] float32 (may equal state_in, in place)
+ *   o           [total_tokens, H, d_v]  dtype dt, o_t = scale * S_t^T q_t
+ *   workspace   device scratch of at least kda_prefill_workspace_size(...)
+ *               bytes (may be NULL when that size is 0); contents need not be
+ *               initialised and are clobbered.
+ * Returns KDA_OK once the work is enqueued.  Bad cu_seqlens contents are
+ * reported through the device error word (KDA_DEVERR_CU_SEQLENS); the
+ * sequences they affect are skipped.
+ */
+KDA_API kda_status kda_prefill(const void* q, const void* k, const void* v, const float* beta,
+                       const float* alpha, const int32_t* cu_seqlens, int32_t num_seqs,
+                       int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                       float scale, const float* state_in, float* state_out, void* o,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One fused decode step for B sequences, each with H resident states
+ * ("Kimi K3, explained", section "How Kimi Delta Attention works, step by
+ * step", and the question on constant-cost decode: one fixed-size state update
+ * and read per generated token, independent of context length).  Each state is
+ * read once, decayed, delta-corrected, written back in place, and queried.
+ *
+ *   q, k        [B, H, d_k]  dtype dt;  v [B, H, d_v] dtype dt
+ *   beta        [B, H] float32;  alpha [B, H, d_k] float32
+ *   state       [num_slots, H, d_k, d_v] float32 pool, updated in place
+ *   state_idx   [B] int32 device array: row b uses slot state_idx[b]; NULL
+ *               means slot b (then num_slots >= B).  Slots must be distinct
+ *               within one call.  Out-of-range entries skip the row and set
+ *               KDA_DEVERR_STATE_IDX.
+ *   o           [B, H, d_v] dtype dt
+ */
+KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* beta,
+                           const float* alpha, float* state, const int32_t* state_idx,
+                           int32_t num_slots, void* o, int32_t B, int32_t H, int32_t d_k,
+                           int32_t d_v, kda_dtype dt, float scale, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  *bits (may be NULL) receives the KDA_DEVERR_* bits that were set.
+ * Returns KDA_OK if none were set, KDA_ERR_DEVICE if some were, KDA_ERR_CUDA if
+ * a CUDA call failed.
+ */
+KDA_API kda_status kda_get_device_error(void* stream, uint32_t* bits);
+
+/* Static, human-readable name of a status code. */
+KDA_API const char* kda_status_string(kda_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

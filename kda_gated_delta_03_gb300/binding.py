@@ -1,0 +1,170 @@
+"""Thin Python binding of libkda (``include/kda.h``), through ctypes.
+
+Argument marshalling only: shape/dtype checks, pointer extraction, default
+output allocation through PyTorch, and the caller's current CUDA stream.  Every
+step of the operator runs in the CUDA kernels behind the C ABI; when the library
+is missing or fails to load, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_DEVICE = range(6)
+KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
+KDA_DEVERR_CU_SEQLENS, KDA_DEVERR_STATE_IDX = 0x1, 0x2
+
+# Every function include/kda.h declares, with its ctypes signature.
+_vp, _i32, _i64, _sz, _f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+SIGNATURES = {
+    "kda_prefill_workspace_size": (_sz, [_i32, _i64, _i32, _i32, _i32, ctypes.c_int]),
+    "kda_prefill": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, ctypes.c_int,
+                                   _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "kda_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                       ctypes.c_int, _f32, _vp]),
+    "kda_get_device_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
+    "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {kda_status_string(code)} ({code})")
+        self.code = code
+
+
+_LIB = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libkda (built in-tree by ``build.build()``); raises if it is missing."""
+    global _LIB
+    if _LIB is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libkda is not built ({path} missing); run kda_gated_delta_03_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _LIB = L
+    return _LIB
+
+
+def kda_status_string(code: int) -> str:
+    return load().kda_status_string(int(code)).decode()
+
+
+def _dt(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return KDA_DTYPE_BF16
+    if t == torch.float32:
+        return KDA_DTYPE_F32
+    raise TypeError(f"unsupported q/k/v dtype {t}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(name, t, dtype, shape, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def kda_prefill_workspace_size(num_seqs: int, total_tokens: int, H: int, d_k: int, d_v: int,
+                               dtype: torch.dtype = torch.bfloat16) -> int:
+    return int(load().kda_prefill_workspace_size(num_seqs, total_tokens, H, d_k, d_v, _dt(dtype)))
+
+
+def kda_prefill(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float = 1.0, state_out=None,
+                o=None, workspace=None, stream=None):
+    """Chunkwise prefill over packed sequences; returns (o, state_out).
+
+    q, k [T, H, d_k], v [T, H, d_v] (bf16 or f32); beta [T, H] f32; alpha [T, H, d_k] f32;
+    cu_seqlens [N + 1] int32 (device); state_in [N, H, d_k, d_v] f32 or None.
+    """
+    L = load()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dev = q.device
+    N = cu_seqlens.shape[0] - 1
+    _check("q", q, q.dtype, (T, H, dk), dev)
+    _check("k", k, q.dtype, (T, H, dk), dev)
+    _check("v", v, q.dtype, (T, H, dv), dev)
+    _check("beta", beta, torch.float32, (T, H), dev)
+    _check("alpha", alpha, torch.float32, (T, H, dk), dev)
+    _check("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
+    if state_in is not None:
+        _check("state_in", state_in, torch.float32, (N, H, dk, dv), dev)
+    if state_out is None:
+        state_out = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check("state_out", state_out, torch.float32, (N, H, dk, dv), dev)
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    _check("o", o, q.dtype, (T, H, dv), dev)
+    need = int(L.kda_prefill_workspace_size(N, T, H, dk, dv, _dt(q.dtype)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = L.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(cu_seqlens), N, T, H, dk, dv,
+                       _dt(q.dtype), float(scale), _ptr(state_in), _ptr(state_out), _ptr(o), _ptr(workspace),
+                       wbytes, _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError("kda_prefill", rc)
+    return o, state_out
+
+
+def kda_decode_step(q, k, v, beta, alpha, state, state_idx=None, *, scale: float = 1.0, o=None, stream=None):
+    """One fused decode step; updates `state` ([P, H, d_k, d_v] f32) in place and returns o [B, H, d_v]."""
+    L = load()
+    B, H, dk = q.shape
+    dv = v.shape[2]
+    dev = q.device
+    P = state.shape[0]
+    _check("q", q, q.dtype, (B, H, dk), dev)
+    _check("k", k, q.dtype, (B, H, dk), dev)
+    _check("v", v, q.dtype, (B, H, dv), dev)
+    _check("beta", beta, torch.float32, (B, H), dev)
+    _check("alpha", alpha, torch.float32, (B, H, dk), dev)
+    _check("state", state, torch.float32, (P, H, dk, dv), dev)
+    if state_idx is not None:
+        _check("state_idx", state_idx, torch.int32, (B,), dev)
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=q.dtype, device=dev)
+    _check("o", o, q.dtype, (B, H, dv), dev)
+    rc = L.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(state), _ptr(state_idx), P,
+                           _ptr(o), B, H, dk, dv, _dt(q.dtype), float(scale), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError("kda_decode_step", rc)
+    return o
+
+
+def kda_get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error bits."""
+    bits = ctypes.c_uint32(0)
+    rc = load().kda_get_device_error(_stream(stream), ctypes.byref(bits))
+    if rc not in (KDA_OK, KDA_ERR_DEVICE):
+        raise KdaError("kda_get_device_error", rc)
+    return int(bits.value)

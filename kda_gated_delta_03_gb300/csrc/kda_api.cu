@@ -1,0 +1,154 @@
+// C ABI of libkda: host-side validation, scheduling and dispatch.
+//
+// Every entry point validates its arguments completely on the host before it
+// touches the CUDA runtime, so a rejected call launches nothing.  The only
+// state the library keeps is one 32-bit error word per device (a file-scope
+// __device__ variable), which kernels set when they detect inconsistent
+// device-side inputs and kda_get_device_error reads back and clears.
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+__device__ unsigned g_kda_device_error = 0u;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mutex;
+unsigned* g_err_addr[kMaxDevices] = {};
+
+kda_status error_word(unsigned** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_err_mutex);
+    if (!g_err_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_kda_device_error) != cudaSuccess) return KDA_ERR_CUDA;
+        g_err_addr[dev] = static_cast<unsigned*>(p);
+    }
+    *out = g_err_addr[dev];
+    return KDA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_head(int32_t dk, int32_t dv) { return dk == dv && (dk == 16 || dk == 64 || dk == 128); }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_DEVICE: return "KDA_ERR_DEVICE";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                                  int32_t d_v, kda_dtype dt) {
+    (void)total_tokens; (void)H; (void)d_k; (void)d_v; (void)dt;
+    if (num_seqs <= 1) return 0;
+    // longest-first schedule of the sequences
+    return align_up(sizeof(int32_t) * (size_t)num_seqs, 256);
+}
+
+kda_status kda_prefill(const void* q, const void* k, const void* v, const float* beta,
+                       const float* alpha, const int32_t* cu_seqlens, int32_t num_seqs,
+                       int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                       float scale, const float* state_in, float* state_out, void* o,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    // ---- host-side validation (no CUDA call before this block ends) ----
+    if (num_seqs < 0 || total_tokens < 0 || total_tokens > INT32_MAX || H <= 0 || d_k <= 0 ||
+        d_v <= 0 || !std::isfinite(scale))
+        return KDA_ERR_INVALID_ARG;
+    if (dt != KDA_DTYPE_F32 && dt != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
+    if (!supported_head(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !state_out || !aligned(cu_seqlens, 4) || !aligned(state_out, 16))
+        return KDA_ERR_INVALID_ARG;
+    if (state_in && !aligned(state_in, 16)) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0) {
+        if (!q || !k || !v || !beta || !alpha || !o) return KDA_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+            !aligned(alpha, 16) || !aligned(beta, 4))
+            return KDA_ERR_INVALID_ARG;
+    }
+    const size_t need = kda_prefill_workspace_size(num_seqs, total_tokens, H, d_k, d_v, dt);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+        return KDA_ERR_WORKSPACE;
+
+    // ---- launch ----
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned* err = nullptr;
+    if (error_word(&err) != KDA_OK) return KDA_ERR_CUDA;
+
+    kda::PrefillParams p{};
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.alpha = alpha;
+    p.cu_seqlens = cu_seqlens;
+    p.order = nullptr;
+    p.num_seqs = num_seqs;
+    p.total_tokens = static_cast<int32_t>(total_tokens);
+    p.H = H; p.dk = d_k; p.dv = d_v;
+    p.scale = scale;
+    p.state_in = state_in; p.state_out = state_out; p.o = o;
+    p.err = err;
+    if (need > 0) {
+        int32_t* order = static_cast<int32_t*>(workspace);
+        if (kda::launch_order(cu_seqlens, num_seqs, order, s) != cudaSuccess) return KDA_ERR_CUDA;
+        p.order = order;
+    }
+    p.slices = kda::prefill_cc_slices(d_v);
+    if (kda::launch_prefill_cc(p, dt, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* beta,
+                           const float* alpha, float* state, const int32_t* state_idx,
+                           int32_t num_slots, void* o, int32_t B, int32_t H, int32_t d_k,
+                           int32_t d_v, kda_dtype dt, float scale, void* stream) {
+    if (B < 0 || H <= 0 || d_k <= 0 || d_v <= 0 || num_slots < 0 || !std::isfinite(scale))
+        return KDA_ERR_INVALID_ARG;
+    if (dt != KDA_DTYPE_F32 && dt != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
+    if (!supported_head(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !beta || !alpha || !state || !o) return KDA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+        !aligned(alpha, 16) || !aligned(beta, 4) || !aligned(state, 16))
+        return KDA_ERR_INVALID_ARG;
+    if (state_idx ? !aligned(state_idx, 4) : num_slots < B) return KDA_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned* err = nullptr;
+    if (error_word(&err) != KDA_OK) return KDA_ERR_CUDA;
+    kda::DecodeParams p{};
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.alpha = alpha;
+    p.state = state; p.state_idx = state_idx; p.num_slots = num_slots;
+    p.o = o; p.B = B; p.H = H; p.d = d_k; p.scale = scale; p.err = err;
+    if (kda::launch_decode(p, dt, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_get_device_error(void* stream, uint32_t* bits) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned* err = nullptr;
+    if (error_word(&err) != KDA_OK) return KDA_ERR_CUDA;
+    unsigned host = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaMemcpy(&host, err, sizeof host, cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
+    if (host != 0u && cudaMemset(err, 0, sizeof host) != cudaSuccess) return KDA_ERR_CUDA;
+    if (bits) *bits = host;
+    return host ? KDA_ERR_DEVICE : KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Internal interfaces between the C-ABI host code (kda_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr int kChunk = 64;             // tokens per chunk of the chunkwise prefill
+constexpr float kLog2AlphaMin = -15.f; // clamp of log2(alpha) per token
+
+// Everything a prefill kernel needs, already validated on the host.
+struct PrefillParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* beta;
+    const float* alpha;
+    const int32_t* cu_seqlens;   // [num_seqs + 1], device
+    const int32_t* order;        // [num_seqs] sequences longest first (device), or nullptr
+    int32_t num_seqs;
+    int32_t total_tokens;
+    int32_t H;
+    int32_t dk;
+    int32_t dv;
+    int32_t slices;              // d_v slices per (sequence, head)
+    float scale;
+    const float* state_in;       // may be nullptr
+    float* state_out;
+    void* o;
+    unsigned* err;               // device error word
+};
+
+struct DecodeParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* beta;
+    const float* alpha;
+    float* state;
+    const int32_t* state_idx;    // may be nullptr
+    int32_t num_slots;
+    void* o;
+    int32_t B;
+    int32_t H;
+    int32_t d;
+    float scale;
+    unsigned* err;
+};
+
+// Launchers (return the launch error, if any).
+cudaError_t launch_decode(const DecodeParams& p, kda_dtype dt, cudaStream_t s);
+cudaError_t launch_prefill_cc(const PrefillParams& p, kda_dtype dt, cudaStream_t s);
+cudaError_t launch_order(const int32_t* cu_seqlens, int32_t num_seqs, int32_t* order, cudaStream_t s);
+
+// Number of CUDA-core prefill d_v slices for a head size.
+int prefill_cc_slices(int dv);
+
+__device__ __forceinline__ float load_as_float(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float load_as_float(const __nv_bfloat16* p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void store_from_float(float* p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void store_from_float(__nv_bfloat16* p, int64_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+}  // namespace kda

@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI: the library builds for sm_103a, exports every symbol the header
+declares, and rejects bad arguments on the host before touching the CUDA runtime (no GPU needed)."""
+
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+from kda_gated_delta_03_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", text)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert set(names) == set(binding.SIGNATURES), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_library_targets_sm103a():
+    assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
+
+
+def test_status_strings(lib):
+    assert binding.kda_status_string(0) == "KDA_OK"
+    assert binding.kda_status_string(3) == "KDA_ERR_WORKSPACE"
+    assert binding.kda_status_string(99) == "KDA_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 1) == 0
+    assert lib.kda_prefill_workspace_size(64, 300000, 32, 128, 128, 1) == 256
+    assert lib.kda_prefill_workspace_size(65, 300000, 32, 128, 128, 1) == 512
+
+
+# Fake, suitably aligned device addresses: every call below must be rejected before any CUDA call.
+P = ctypes.c_void_p(0x10000)
+
+
+def prefill(lib, **over):
+    a = dict(q=P, k=P, v=P, beta=P, alpha=P, cu=P, N=1, T=64, H=2, dk=16, dv=16, dt=0, scale=1.0, s_in=None,
+             s_out=P, o=P, ws=None, wsb=0, stream=None)
+    a.update(over)
+    return lib.kda_prefill(a["q"], a["k"], a["v"], a["beta"], a["alpha"], a["cu"], a["N"], a["T"], a["H"], a["dk"],
+                           a["dv"], a["dt"], a["scale"], a["s_in"], a["s_out"], a["o"], a["ws"], a["wsb"],
+                           a["stream"])
+
+
+def decode(lib, **over):
+    a = dict(q=P, k=P, v=P, beta=P, alpha=P, state=P, idx=None, slots=4, o=P, B=4, H=2, dk=16, dv=16, dt=1,
+             scale=1.0, stream=None)
+    a.update(over)
+    return lib.kda_decode_step(a["q"], a["k"], a["v"], a["beta"], a["alpha"], a["state"], a["idx"], a["slots"],
+                               a["o"], a["B"], a["H"], a["dk"], a["dv"], a["dt"], a["scale"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(H=0), binding.KDA_ERR_INVALID_ARG),
+    (dict(N=-1), binding.KDA_ERR_INVALID_ARG),
+    (dict(T=-5), binding.KDA_ERR_INVALID_ARG),
+    (dict(T=2**31), binding.KDA_ERR_INVALID_ARG),
+    (dict(dk=32, dv=32), binding.KDA_ERR_UNSUPPORTED),
+    (dict(dk=128, dv=64), binding.KDA_ERR_UNSUPPORTED),
+    (dict(dt=7), binding.KDA_ERR_INVALID_ARG),
+    (dict(q=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(alpha=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(cu=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(s_out=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(q=ctypes.c_void_p(0x10008)), binding.KDA_ERR_INVALID_ARG),
+    (dict(cu=ctypes.c_void_p(0x10002)), binding.KDA_ERR_INVALID_ARG),
+    (dict(s_in=ctypes.c_void_p(0x10004)), binding.KDA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.KDA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), binding.KDA_ERR_INVALID_ARG),
+    (dict(N=4), binding.KDA_ERR_WORKSPACE),
+    (dict(N=4, ws=P, wsb=255), binding.KDA_ERR_WORKSPACE),
+    (dict(N=4, ws=ctypes.c_void_p(0x10010), wsb=4096), binding.KDA_ERR_WORKSPACE),
+    (dict(N=0, T=5), binding.KDA_ERR_INVALID_ARG),
+    (dict(N=0, T=0), binding.KDA_OK),
+])
+def test_prefill_host_validation(lib, over, code):
+    assert prefill(lib, **over) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(H=0), binding.KDA_ERR_INVALID_ARG),
+    (dict(B=-1), binding.KDA_ERR_INVALID_ARG),
+    (dict(dk=48, dv=48), binding.KDA_ERR_UNSUPPORTED),
+    (dict(state=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(o=ctypes.c_void_p(0x10001)), binding.KDA_ERR_INVALID_ARG),
+    (dict(slots=3), binding.KDA_ERR_INVALID_ARG),
+    (dict(idx=ctypes.c_void_p(0x10002)), binding.KDA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.KDA_ERR_INVALID_ARG),
+    (dict(B=0), binding.KDA_OK),
+])
+def test_decode_host_validation(lib, over, code):
+    assert decode(lib, **over) == code

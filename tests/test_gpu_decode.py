@@ -1,0 +1,75 @@
+"""Parity of kda_decode_step (CUDA, through the C ABI) with the float64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from kda_gated_delta_03_gb300 import inputs as I
+from oracle import oracle as O
+from kda_testutil import TOL, rel_frob, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_steps(B, H, d, dtype, steps, seed, P=None, idx=None, decay="config"):
+    import kda_gated_delta_03_gb300 as kda
+    P = P or B
+    pool = I.random_state(P, H, d, d, seed)
+    pool_d = to_dev(pool)
+    pool64 = pool.astype(np.float64)
+    idx_d = None if idx is None else to_dev(np.asarray(idx, np.int32))
+    bf = dtype == "bf16"
+    os_gpu, os_ref = [], []
+    for s in range(steps):
+        st = I.decode_step_inputs(B, H, d, d, dtype, seed, s, decay=decay)
+        o = kda.kda_decode_step(*(to_dev(st[n], bf) for n in ("q", "k", "v")), to_dev(st["beta"]),
+                                to_dev(st["alpha"]), pool_d, idx_d)
+        os_gpu.append(o.double().cpu().numpy())
+        os_ref.append(O.decode_step(st, pool64, idx))
+    torch.cuda.synchronize()
+    return np.stack(os_gpu), np.stack(os_ref), pool_d.double().cpu().numpy(), pool64
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 64, 128])
+@pytest.mark.parametrize("decay", ["config", "slow"])
+def test_decode_steps(dtype, d, decay):
+    o, o_ref, pool, pool_ref = run_steps(5, 3, d, dtype, 6, 40 + d, decay=decay)
+    assert rel_frob(o, o_ref) <= TOL[dtype]
+    assert rel_frob(pool, pool_ref) <= TOL[dtype]
+
+
+def test_decode_state_idx_and_untouched_slots():
+    idx = [6, 1, 3, 0]
+    o, o_ref, pool, pool_ref = run_steps(4, 2, 128, "bf16", 3, 50, P=8, idx=idx)
+    assert rel_frob(o, o_ref) <= 3e-3
+    assert rel_frob(pool, pool_ref) <= 3e-3
+    untouched = [2, 4, 5, 7]
+    assert np.array_equal(pool[untouched], pool_ref[untouched])
+
+
+def test_decode_bad_slot_is_reported_not_faulted():
+    import kda_gated_delta_03_gb300 as kda
+    pool = to_dev(I.random_state(4, 2, 16, 16, 1))
+    before = pool.clone()
+    st = I.decode_step_inputs(2, 2, 16, 16, "f32", 1, 0)
+    idx = to_dev(np.array([1, 9], np.int32))
+    kda.kda_decode_step(*(to_dev(st[n]) for n in ("q", "k", "v", "beta", "alpha")), pool, idx)
+    assert kda.kda_get_device_error() & 0x2
+    assert torch.equal(pool[[0, 2, 3]], before[[0, 2, 3]])
+    assert not torch.equal(pool[1], before[1])
+
+
+def test_decode_equals_prefill_of_one_token():
+    """A decode step is one token of the recurrence: it matches kda_prefill with T = 1 per sequence."""
+    import kda_gated_delta_03_gb300 as kda
+    B, H, d = 3, 2, 128
+    st = I.decode_step_inputs(B, H, d, d, "f32", 60, 0, decay="slow")
+    pool = I.random_state(B, H, d, d, 61)
+    pool_d = to_dev(pool)
+    o_dec = kda.kda_decode_step(*(to_dev(st[n]) for n in ("q", "k", "v", "beta", "alpha")), pool_d)
+    cu = to_dev(np.arange(B + 1, dtype=np.int32))
+    o_pre, s_pre = kda.kda_prefill(*(to_dev(st[n]) for n in ("q", "k", "v", "beta", "alpha")), cu, to_dev(pool))
+    torch.cuda.synchronize()
+    assert rel_frob(o_dec.cpu().numpy(), o_pre.cpu().numpy()) <= 1e-5
+    assert rel_frob(pool_d.cpu().numpy(), s_pre.cpu().numpy()) <= 1e-5

@@ -1,0 +1,151 @@
+"""Parity of kda_prefill (CUDA, through the C ABI) with the float64 oracle, element by element,
+on seeded inputs that span several chunks, ragged tails and the degenerate cases."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from kda_gated_delta_03_gb300 import inputs as I
+from oracle import oracle as O
+from kda_testutil import TOL, prefill_gpu, rel_frob, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import kda_gated_delta_03_gb300 as kda
+    from kda_gated_delta_03_gb300 import build
+    build.build()
+    kda.load()
+    yield
+    assert kda.kda_get_device_error() == 0
+
+
+def check(inp, tol=None, scale=1.0):
+    tol = tol or TOL[inp["dtype"]]
+    o, st = prefill_gpu(inp, scale=scale)
+    o_ref, st_ref = O.prefill(inp, scale=scale)
+    e_o, e_s = rel_frob(o, o_ref), rel_frob(st, st_ref)
+    assert e_o <= tol and e_s <= tol, (e_o, e_s)
+    return e_o, e_s
+
+
+def test_tiny_fp32_workload():
+    """B=1, H=2, T=64, d=16, fp32 throughout, zero initial state (the tiny correctness workload)."""
+    w = I.workload("tiny_fp32")
+    inp = I.prefill_inputs(w["seqlens"], w["H"], w["dk"], w["dv"], w["dtype"], w["seed"], state=w["state"])
+    check(inp, 1e-4)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 64, 128])
+@pytest.mark.parametrize("decay", ["config", "slow", "one", "scalar"])
+def test_ragged_varlen(dtype, d, decay):
+    """Lengths 1, 63, 64, 65, 0 and 200 packed together, random initial states."""
+    inp = I.prefill_inputs([1, 63, 64, 65, 0, 200], 3, d, d, dtype, 100 + d, decay=decay, state="randn")
+    check(inp)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_long_carry_slow_decay(dtype):
+    """Slow decay over 1000 tokens, so the carried state matters across many chunks."""
+    inp = I.prefill_inputs([1000], 2, 128, 128, dtype, 7, decay="slow", state="randn")
+    check(inp)
+
+
+def test_scale_and_zero_state():
+    inp = I.prefill_inputs([130, 7], 2, 64, 64, "f32", 8, decay="slow")
+    check(inp, scale=0.125)
+
+
+def test_worked_overwrite_on_gpu(golden_dir):
+    """The page's overwrite example (write (k, a) then (k, b), beta = 1, no decay) at d = 16 with zero
+    padding: reading k returns b."""
+    g = json.load(open(os.path.join(golden_dir, "overwrite_example.json")))
+    d = 16
+    key = np.zeros(d, np.float32)
+    key[g["key_index"]] = 1.0
+    a = np.zeros(d, np.float32)
+    b = np.zeros(d, np.float32)
+    a[:4], b[:4] = g["a"], g["b"]
+    inp = dict(q=np.stack([key, key])[:, None, :].copy(), k=np.stack([key, key])[:, None, :].copy(),
+               v=np.stack([a, b])[:, None, :].copy(), beta=np.ones((2, 1), np.float32),
+               alpha=np.ones((2, 1, d), np.float32), cu_seqlens=I.cu_seqlens_of([2]), state_in=None,
+               dtype="f32", H=1, dk=d, dv=d)
+    o, _ = prefill_gpu(inp)
+    np.testing.assert_allclose(o[0, 0, :4], g["a"], rtol=0, atol=1e-5)
+    np.testing.assert_allclose(o[1, 0, :4], g["delta_read_after_both_writes"], rtol=0, atol=1e-5)
+
+
+def test_packing_independence():
+    """Each sequence's results do not depend on which other sequences share the batch."""
+    inp = I.prefill_inputs([70, 150, 33], 2, 128, 128, "bf16", 9, decay="slow", state="randn")
+    o, st = prefill_gpu(inp)
+    cu = inp["cu_seqlens"]
+    for n in range(3):
+        sub = dict(inp)
+        for key in ("q", "k", "v", "beta", "alpha"):
+            sub[key] = np.ascontiguousarray(inp[key][cu[n]:cu[n + 1]])
+        sub["cu_seqlens"] = I.cu_seqlens_of([cu[n + 1] - cu[n]])
+        sub["state_in"] = np.ascontiguousarray(inp["state_in"][n:n + 1])
+        o1, st1 = prefill_gpu(sub)
+        assert np.array_equal(o1, o[cu[n]:cu[n + 1]])
+        assert np.array_equal(st1[0], st[n])
+
+
+def test_append_equals_one_shot():
+    """prefill(T1) then prefill(T2) from the carried state equals prefill(T1 + T2) when T1 is a whole
+    number of chunks (identical chunking), and matches the oracle otherwise."""
+    inp = I.prefill_inputs([320], 2, 128, 128, "bf16", 10, decay="slow", state="randn")
+    o_full, s_full = prefill_gpu(inp)
+    for cut in (192, 100):
+        a, b = dict(inp), dict(inp)
+        for key in ("q", "k", "v", "beta", "alpha"):
+            a[key] = np.ascontiguousarray(inp[key][:cut])
+            b[key] = np.ascontiguousarray(inp[key][cut:])
+        a["cu_seqlens"], b["cu_seqlens"] = I.cu_seqlens_of([cut]), I.cu_seqlens_of([320 - cut])
+        o1, s1 = prefill_gpu(a)
+        o2, s2 = prefill_gpu(b, state_in=s1.astype(np.float32))
+        if cut % 64 == 0:
+            assert np.array_equal(np.concatenate([o1, o2]), o_full)
+            assert np.array_equal(s2, s_full.astype(np.float32).astype(np.float64))
+        else:
+            o_ref, s_ref = O.prefill(inp)
+            assert rel_frob(np.concatenate([o1, o2]), o_ref) <= 3e-3
+            assert rel_frob(s2, s_ref) <= 3e-3
+
+
+def test_in_place_state():
+    import kda_gated_delta_03_gb300 as kda
+    inp = I.prefill_inputs([90, 40], 2, 64, 64, "f32", 11, decay="slow", state="randn")
+    st = to_dev(inp["state_in"])
+    kda.kda_prefill(*(to_dev(inp[n]) for n in ("q", "k", "v", "beta", "alpha", "cu_seqlens")), st, state_out=st)
+    torch.cuda.synchronize()
+    _, s_ref = O.prefill(inp)
+    assert rel_frob(st.cpu().numpy(), s_ref) <= 1e-4
+
+
+def test_empty_and_all_zero_length():
+    import kda_gated_delta_03_gb300 as kda
+    inp = I.prefill_inputs([0, 0], 2, 16, 16, "f32", 12, state="randn")
+    o, st = prefill_gpu(inp)
+    assert o.shape == (0, 2, 16)
+    assert np.array_equal(st, inp["state_in"].astype(np.float64))
+    o, st = prefill_gpu(I.prefill_inputs([0], 2, 16, 16, "f32", 12))
+    assert np.all(st == 0)
+    assert kda.kda_get_device_error() == 0
+
+
+def test_bad_cu_seqlens_is_reported_not_faulted():
+    """Inconsistent cu_seqlens contents are caught on the device: the affected sequences are skipped and
+    the error word says so; nothing reads or writes out of bounds."""
+    import kda_gated_delta_03_gb300 as kda
+    inp = I.prefill_inputs([10, 20, 30], 1, 16, 16, "f32", 13)
+    inp["cu_seqlens"] = np.array([0, 25, 20, 60], np.int32)
+    prefill_gpu(inp)
+    assert kda.kda_get_device_error() & 0x1
+    assert kda.kda_get_device_error() == 0
