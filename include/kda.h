@@ -69,6 +69,7 @@ typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 /* Bits of the device error word. */
 #define KDA_DEVERR_CU_SEQLENS 0x1u  /* cu_seqlens not monotone / cu[0] != 0 / cu[N] != total  */
 #define KDA_DEVERR_STATE_IDX 0x2u   /* decode state_idx entry outside [0, num_slots)          */
+#define KDA_DEVERR_TIMEOUT 0x4u     /* a bounded wait inside a kernel gave up (work abandoned) */
 
 /*
  * Bytes of device workspace kda_prefill needs for this problem (0 is a valid

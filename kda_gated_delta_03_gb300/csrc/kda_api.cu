@@ -108,8 +108,13 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
         if (kda::launch_order(cu_seqlens, num_seqs, order, s) != cudaSuccess) return KDA_ERR_CUDA;
         p.order = order;
     }
-    p.slices = kda::prefill_cc_slices(d_v);
-    if (kda::launch_prefill_cc(p, dt, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::prefill_tc_supported(p, dt)) {
+        p.slices = kda::prefill_tc_slices(d_v);
+        if (kda::launch_prefill_tc(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+    } else {
+        p.slices = kda::prefill_cc_slices(d_v);
+        if (kda::launch_prefill_cc(p, dt, s) != cudaSuccess) return KDA_ERR_CUDA;
+    }
     return KDA_OK;
 }
 
