@@ -35,7 +35,7 @@ if ROOT not in sys.path:
 
 from kda_gated_delta_03_gb300 import inputs as I  # noqa: E402
 
-PREFILL_KERNEL_SRC = ["kda_gated_delta_03_gb300/csrc/kda_prefill_cc.cu"]
+PREFILL_KERNEL_SRC = ["kda_gated_delta_03_gb300/csrc/kda_prefill_tc.cu"]
 DECODE_KERNEL_SRC = ["kda_gated_delta_03_gb300/csrc/kda_decode.cu"]
 METRIC = "KDA prefill tokens/s (H=32,d=128); decode steps/s and state HBM GB/s vs peak"
 
