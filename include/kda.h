@@ -61,7 +61,8 @@ typedef enum {
     KDA_ERR_UNSUPPORTED = 2,  /* head size or dtype this build has no kernel for           */
     KDA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the required size       */
     KDA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed                      */
-    KDA_ERR_DEVICE = 5        /* kda_get_device_error found device-detected errors         */
+    KDA_ERR_DEVICE = 5,       /* kda_get_device_error found device-detected errors         */
+    KDA_ERR_TOO_LARGE = 6     /* problem exceeds the fixed scratch of kda_prefill_noalloc  */
 } kda_status;
 
 typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
@@ -132,6 +133,35 @@ KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, 
                            const float* alpha, float* state, const int32_t* state_idx,
                            int32_t num_slots, void* o, int32_t B, int32_t H, int32_t d_k,
                            int32_t d_v, kda_dtype dt, float scale, void* stream);
+
+/*
+ * kda_prefill without a workspace argument, for callers that cannot allocate
+ * device memory.  (The pages have no counterpart; this is an interface
+ * convenience.)  Typical callers: a serving process whose memory manager has
+ * reserved the GPU's memory up front and hands out no scratch buffers, or a
+ * host program that reaches this library only through the C ABI and has no
+ * device allocator of its own.  Arguments, results and errors are those of
+ * kda_prefill, except:
+ *  - The scratch kda_prefill takes as `workspace` (the longest-first order of
+ *    the sequences) lives in a fixed static device array of
+ *    KDA_NOALLOC_MAX_SEQS int32 entries (64 KiB), which every GPU that loads
+ *    libkda holds until the process exits.  num_seqs > KDA_NOALLOC_MAX_SEQS
+ *    returns KDA_ERR_TOO_LARGE before anything is launched.
+ *  - The function allocates and frees nothing.  The first call on a device
+ *    looks up the array's device address (cudaGetSymbolAddress, with that
+ *    device current) and caches it; make that first call on each device before
+ *    any stream capture.
+ *  - Every call shares the one array, which keeps the last call's contents;
+ *    each call rewrites every entry it reads, so nothing needs clearing.  Calls
+ *    whose work overlaps on the GPU (for example on two unordered streams)
+ *    race on the array and must be serialised by the caller.
+ */
+#define KDA_NOALLOC_MAX_SEQS 16384
+KDA_API kda_status kda_prefill_noalloc(const void* q, const void* k, const void* v, const float* beta,
+                                       const float* alpha, const int32_t* cu_seqlens, int32_t num_seqs,
+                                       int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                       kda_dtype dt, float scale, const float* state_in,
+                                       float* state_out, void* o, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error

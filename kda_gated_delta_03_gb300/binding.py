@@ -16,6 +16,8 @@ import torch
 from . import build as _build
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_DEVICE = range(6)
+KDA_ERR_TOO_LARGE = 6
+KDA_NOALLOC_MAX_SEQS = 16384
 KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
 KDA_DEVERR_CU_SEQLENS, KDA_DEVERR_STATE_IDX = 0x1, 0x2
 
@@ -27,6 +29,8 @@ SIGNATURES = {
                                    _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "kda_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                        ctypes.c_int, _f32, _vp]),
+    "kda_prefill_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
+                                           ctypes.c_int, _f32, _vp, _vp, _vp, _vp]),
     "kda_get_device_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -133,6 +137,41 @@ def kda_prefill(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float
                        wbytes, _stream(stream))
     if rc != KDA_OK:
         raise KdaError("kda_prefill", rc)
+    return o, state_out
+
+
+def kda_prefill_noalloc(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float = 1.0, state_out=None,
+                        o=None, stream=None):
+    """kda_prefill for callers that cannot allocate device memory: no workspace argument; the library
+    uses a fixed static device array (at most KDA_NOALLOC_MAX_SEQS sequences) and allocates nothing.
+
+    Pass preallocated `state_out` and `o` to keep the whole call allocation-free; when they are None,
+    this wrapper allocates them through PyTorch.  Returns (o, state_out).
+    """
+    L = load()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dev = q.device
+    N = cu_seqlens.shape[0] - 1
+    _check("q", q, q.dtype, (T, H, dk), dev)
+    _check("k", k, q.dtype, (T, H, dk), dev)
+    _check("v", v, q.dtype, (T, H, dv), dev)
+    _check("beta", beta, torch.float32, (T, H), dev)
+    _check("alpha", alpha, torch.float32, (T, H, dk), dev)
+    _check("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
+    if state_in is not None:
+        _check("state_in", state_in, torch.float32, (N, H, dk, dv), dev)
+    if state_out is None:
+        state_out = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check("state_out", state_out, torch.float32, (N, H, dk, dv), dev)
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    _check("o", o, q.dtype, (T, H, dv), dev)
+    rc = L.kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(cu_seqlens), N, T, H, dk,
+                               dv, _dt(q.dtype), float(scale), _ptr(state_in), _ptr(state_out), _ptr(o),
+                               _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError("kda_prefill_noalloc", rc)
     return o, state_out
 
 

@@ -39,6 +39,27 @@ bool supported_head(int32_t dk, int32_t dv) { return dk == dv && (dk == 16 || dk
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Scratch of kda_prefill_noalloc: the longest-first sequence order, in a fixed
+// static device array so that the entry point never allocates.  Host code must
+// not pass the array's name to a kernel (on the host it is only a stand-in);
+// the device address is looked up once per device and cached.
+static __device__ __align__(256) int32_t g_kda_noalloc_order[KDA_NOALLOC_MAX_SEQS];
+std::mutex g_noalloc_mutex;
+int32_t* g_noalloc_addr[kMaxDevices] = {};
+
+kda_status noalloc_scratch(int32_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        int32_t* ptr = nullptr;
+        if (cudaGetSymbolAddress((void**)&ptr, g_kda_noalloc_order) != cudaSuccess || !ptr) return KDA_ERR_CUDA;
+        g_noalloc_addr[dev] = ptr;
+    }
+    *out = g_noalloc_addr[dev];
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -51,6 +72,7 @@ const char* kda_status_string(kda_status s) {
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
         case KDA_ERR_DEVICE: return "KDA_ERR_DEVICE";
+        case KDA_ERR_TOO_LARGE: return "KDA_ERR_TOO_LARGE";
     }
     return "KDA_ERR_UNKNOWN";
 }
@@ -141,6 +163,58 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const fl
     p.state = state; p.state_idx = state_idx; p.num_slots = num_slots;
     p.o = o; p.B = B; p.H = H; p.d = d_k; p.scale = scale; p.err = err;
     if (kda::launch_decode(p, dt, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_prefill_noalloc(const void* q, const void* k, const void* v, const float* beta,
+                               const float* alpha, const int32_t* cu_seqlens, int32_t num_seqs,
+                               int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                               float scale, const float* state_in, float* state_out, void* o, void* stream) {
+    // ---- host-side validation, as kda_prefill, plus the fixed scratch limit ----
+    if (num_seqs < 0 || total_tokens < 0 || total_tokens > INT32_MAX || H <= 0 || d_k <= 0 ||
+        d_v <= 0 || !std::isfinite(scale))
+        return KDA_ERR_INVALID_ARG;
+    if (dt != KDA_DTYPE_F32 && dt != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
+    if (!supported_head(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs > KDA_NOALLOC_MAX_SEQS) return KDA_ERR_TOO_LARGE;
+    if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !state_out || !aligned(cu_seqlens, 4) || !aligned(state_out, 16))
+        return KDA_ERR_INVALID_ARG;
+    if (state_in && !aligned(state_in, 16)) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0) {
+        if (!q || !k || !v || !beta || !alpha || !o) return KDA_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+            !aligned(alpha, 16) || !aligned(beta, 4))
+            return KDA_ERR_INVALID_ARG;
+    }
+
+    // ---- launch, with the static scratch in place of a workspace ----
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned* err = nullptr;
+    if (error_word(&err) != KDA_OK) return KDA_ERR_CUDA;
+    kda::PrefillParams p{};
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.alpha = alpha;
+    p.cu_seqlens = cu_seqlens;
+    p.order = nullptr;
+    p.num_seqs = num_seqs;
+    p.total_tokens = static_cast<int32_t>(total_tokens);
+    p.H = H; p.dk = d_k; p.dv = d_v;
+    p.scale = scale;
+    p.state_in = state_in; p.state_out = state_out; p.o = o;
+    p.err = err;
+    if (num_seqs > 1) {
+        int32_t* order = nullptr;
+        if (noalloc_scratch(&order) != KDA_OK) return KDA_ERR_CUDA;
+        if (kda::launch_order(cu_seqlens, num_seqs, order, s) != cudaSuccess) return KDA_ERR_CUDA;
+        p.order = order;
+    }
+    if (kda::prefill_tc_supported(p, dt)) {
+        p.slices = kda::prefill_tc_slices(d_v);
+        if (kda::launch_prefill_tc(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+    } else {
+        p.slices = kda::prefill_cc_slices(d_v);
+        if (kda::launch_prefill_cc(p, dt, s) != cudaSuccess) return KDA_ERR_CUDA;
+    }
     return KDA_OK;
 }
 
