@@ -19,10 +19,10 @@
 // tcgen05 with float32 operands read as TF32 from shared memory (K-major, no
 // swizzle: 8-row x 16-byte core matrices) and float32 accumulators in TMEM.
 // Derived operands stay TF32/FP32 (only q, k, v are bf16), and the state is
-// kept in float32 registers, one key row per thread.
+// kept in float32 registers, one key row per pair of threads.
 //
-// One CTA = (sequence, head, 32 value columns); 128 threads; thread 0 issues
-// the tcgen05 MMAs.  The next chunk's inputs are fetched with cp.async while
+// One CTA = (sequence, head, 32 value columns); 256 threads (two threads per
+// TMEM lane, splitting the columns); thread 0 issues the tcgen05 MMAs.  The next chunk's inputs are fetched with cp.async while
 // the current chunk runs its state-dependent GEMMs.  Every wait on an MMA
 // completion is bounded; on timeout the CTA records KDA_DEVERR_TIMEOUT, frees
 // its TMEM and stops.
@@ -35,7 +35,7 @@ namespace {
 constexpr int C = 64;
 constexpr int DK = 128;
 constexpr int NV = 32;
-constexpr int NT = 128;
+constexpr int NT = 256;
 constexpr long long kWaitLimit = 4000000000LL;   // clock cycles (about 2 s)
 
 // ---- shared memory map (bytes) ----
@@ -53,7 +53,7 @@ constexpr int OFF_Y = OFF_X + 65536;             // 138496 region Y, 56 KiB
 constexpr int OFF_P = OFF_Y + 57344;             // 195840 P operand
 constexpr int OFF_S = OFF_P + 16384;             // 212224 S^T operand
 constexpr int OFF_MISC = OFF_S + 16384;          // 228608
-constexpr int SMEM_BYTES = OFF_MISC + 64;
+constexpr int SMEM_BYTES = OFF_MISC + 64 + DK * 4;
 // region X: G1 factors -> solve tiles -> W, Gamma.Q operands
 constexpr int X_R = 0, X_LK = C * F_LD * 4, X_LQ = X_LK + 16 * F_LD * 4;
 constexpr int X_A = 0, X_T = C * AT_LD * 4, X_SCR = 2 * C * AT_LD * 4;
@@ -62,7 +62,7 @@ constexpr int X_W = 0, X_QT = 32768;
 constexpr int Y_T = 0, Y_KV = 16384;
 constexpr int Y_KH = 0, Y_U = 32768;
 // misc
-constexpr int M_MBAR = 0, M_TMEM = 8, M_ABORT = 12;
+constexpr int M_MBAR = 0, M_TMEM = 8, M_ABORT = 12, M_GAMC = 64;
 // TMEM columns
 constexpr uint32_t TM_WU = 0, TM_X = 160, TM_O = 192, TM_S = 224, TM_COLS = 256;
 
@@ -140,6 +140,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Hardware base-2 exponential and logarithm (PTX ex2.approx / lg2.approx, relative error ~2^-22,
+// denormal results flushed to zero: an underflowed decay factor is an exact zero here).
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2f(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -213,6 +240,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
+    const int quad = warp & 3;             // TMEM lane quadrant this warp may access
+    const int half = warp >> 2;            // which 16 of the 32 value columns this thread takes in epilogues
+    const int ch = tid & (DK - 1);         // key channel of the per-channel stages
+    const int rh = tid >> 7;               // row half of the per-channel stages
 
     // ---- work item ----
     const int item = blockIdx.x;
@@ -239,8 +270,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
     __nv_bfloat16* vraw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_V);
     float* G = reinterpret_cast<float*>(sm + OFF_G);
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
+    float* sgam = reinterpret_cast<float*>(sm + OFF_MISC + M_GAMC);
     unsigned char* X = sm + OFF_X;
     unsigned char* Y = sm + OFF_Y;
+    unsigned char* opP = sm + OFF_P;
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + OFF_MISC + M_ABORT);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + OFF_MISC + M_TMEM);
     const uint32_t mbar = saddr(sm + OFF_MISC + M_MBAR);
@@ -259,11 +292,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
     }
     if (t_begin < t_end) issue_chunk_loads(sm, g, t_begin, min(C, t_end - t_begin), tid);
 
-    // state row `tid` of this slice, float32 in registers
-    const int64_t state_off = ((int64_t)n * H + h) * DK * (int64_t)p.dv + (int64_t)tid * p.dv + j0;
-    float S[NV];
+    // state: key row srow, value columns 16*half .. 16*half+15 of this slice, float32 in registers
+    const int srow = 32 * quad + lane;
+    const int64_t state_off = (((int64_t)n * H + h) * DK + srow) * (int64_t)p.dv + j0 + 16 * half;
+    float S[16];
 #pragma unroll
-    for (int j = 0; j < NV; j += 4) {
+    for (int j = 0; j < 16; j += 4) {
         float4 v4 = p.state_in ? *reinterpret_cast<const float4*>(p.state_in + state_off + j)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
         S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
@@ -272,14 +306,14 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t tlane = (uint32_t)(warp * 32) << 16;   // this warp's TMEM lane quadrant
+    const uint32_t tlane = (uint32_t)(quad * 32) << 16;   // this warp's TMEM lane quadrant
     uint32_t phase = 0;
     bool aborted = false;
 
     auto write_state_operand = [&]() {
 #pragma unroll
-        for (int j = 0; j < NV; ++j)
-            *reinterpret_cast<float*>(sm + OFF_S + op_off(j, tid, DK)) = S[j];
+        for (int j = 0; j < 16; ++j)
+            *reinterpret_cast<float*>(sm + OFF_S + op_off(16 * half + j, srow, DK)) = S[j];
     };
     auto wait_mma = [&]() -> bool {
         if (!mbar_wait(mbar, phase)) {
@@ -299,59 +333,77 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
         cp_async_wait_all();
         __syncthreads();
 
-        // ---- 1. g = running sum of clamped log2 alpha, per key channel (thread = channel) ----
-        float gamC;
+        // ---- 1. g = running sum of clamped log2 alpha per key channel: each thread scans 32 rows,
+        //         then the upper half adds the lower half's total ----
         {
+            float la[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) la[x] = G[(32 * rh + x) * G_LD + ch];
             float acc = 0.f;
-            for (int r = 0; r < C; ++r) {
-                float* gp = G + r * G_LD + tid;
-                if (r < L) acc += fmaxf(log2f(*gp), kLog2AlphaMin);
-                *gp = acc;
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                acc += (32 * rh + x < L) ? fmaxf(lg2f(la[x]), kLog2AlphaMin) : 0.f;
+                la[x] = acc;
             }
-            gamC = exp2f(acc);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) G[(32 * rh + x) * G_LD + ch] = la[x];
+            __syncthreads();
+            if (rh == 1) {
+                const float base = G[31 * G_LD + ch];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) G[(32 + x) * G_LD + ch] = la[x] + base;
+                sgam[ch] = ex2f(la[31] + base);
+            }
         }
         __syncthreads();
 
-        // ---- 2. A and P by 16-row blocks (warp-level TF32 MMA) ----
+        // ---- 2. A and P by 16-row blocks (warp-level TF32 MMA, two accumulator chains each) ----
         float* R = reinterpret_cast<float*>(X + X_R);
         float* Lk = reinterpret_cast<float*>(X + X_LK);
         float* Lq = reinterpret_cast<float*>(X + X_LQ);
-        float res[10][4];
+        float res[6][4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            {   // factors for block b; thread = key channel
-                const int i = tid;
-                const float ref = G[(16 * b + 7) * G_LD + i];
+            {   // factors of block b: thread (channel, row half)
+                const float ref = G[(16 * b + 7) * G_LD + ch];
                 if (b > 0) {
-                    const float f = exp2f(ref - G[(16 * b - 9) * G_LD + i]);
-                    for (int s = 0; s < 16 * b; ++s) R[s * F_LD + i] *= f;
+                    const float f = ex2f(ref - G[(16 * b - 9) * G_LD + ch]);
+                    for (int s = rh; s < 16 * b; s += 2) R[s * F_LD + ch] *= f;
                 }
-#pragma unroll 4
-                for (int rr = 0; rr < 16; ++rr) {
-                    const int r = 16 * b + rr;
-                    const float gr = G[r * G_LD + i];
-                    const float kv = bf(kraw + r * KQ_LD + i);
-                    R[r * F_LD + i] = kv * exp2f(ref - gr);
-                    const float f = exp2f(gr - ref);
-                    Lk[rr * F_LD + i] = kv * f;
-                    Lq[rr * F_LD + i] = bf(qraw + r * KQ_LD + i) * f;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const int rr = 8 * rh + x, r = 16 * b + rr;
+                    const float gr = G[r * G_LD + ch];
+                    const float kv = bf(kraw + r * KQ_LD + ch);
+                    R[r * F_LD + ch] = kv * ex2f(ref - gr);
+                    const float f = ex2f(gr - ref);
+                    Lk[rr * F_LD + ch] = kv * f;
+                    Lq[rr * F_LD + ch] = bf(qraw + r * KQ_LD + ch) * f;
                 }
             }
             __syncthreads();
+            const int base = b == 0 ? 0 : (b == 1 ? 1 : (b == 2 ? 2 : 4));
 #pragma unroll
-            for (int m = 0; m <= b; ++m) {
-                const int cidx = warp + 4 * m;            // (which, n-tile) combination
-                const int ntiles = 2 * (b + 1);
-                const float* Lf = cidx < ntiles ? Lk : Lq;
-                const int nt = cidx < ntiles ? cidx : cidx - ntiles;
-                float(&d)[4] = res[b * (b + 1) / 2 + m];
-                d[0] = d[1] = d[2] = d[3] = 0.f;
+            for (int m = 0; m < 2; ++m) {
+                const int cidx = warp + 8 * m;             // (which, n-tile) combination
+                if (m <= (b >= 2 ? 1 : 0) && cidx < 4 * (b + 1)) {
+                    const int ntiles = 2 * (b + 1);
+                    const float* Lf = cidx < ntiles ? Lk : Lq;
+                    const int nt = cidx < ntiles ? cidx : cidx - ntiles;
+                    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                    const float* la0 = Lf + gid * F_LD + tig;
+                    const float* la1 = Lf + (gid + 8) * F_LD + tig;
+                    const float* rb = R + (8 * nt + gid) * F_LD + tig;
 #pragma unroll 4
-                for (int kk = 0; kk < DK / 8; ++kk) {
-                    const int k0 = kk * 8 + tig;
-                    mma_16x8x8(d, to_tf32(Lf[gid * F_LD + k0]), to_tf32(Lf[(gid + 8) * F_LD + k0]),
-                               to_tf32(Lf[gid * F_LD + k0 + 4]), to_tf32(Lf[(gid + 8) * F_LD + k0 + 4]),
-                               to_tf32(R[(8 * nt + gid) * F_LD + k0]), to_tf32(R[(8 * nt + gid) * F_LD + k0 + 4]));
+                    for (int kk = 0; kk < DK / 8; kk += 2) {
+                        const int k0 = kk * 8, k1 = k0 + 8;
+                        mma_16x8x8(d0, to_tf32(la0[k0]), to_tf32(la1[k0]), to_tf32(la0[k0 + 4]), to_tf32(la1[k0 + 4]),
+                                   to_tf32(rb[k0]), to_tf32(rb[k0 + 4]));
+                        mma_16x8x8(d1, to_tf32(la0[k1]), to_tf32(la1[k1]), to_tf32(la0[k1 + 4]), to_tf32(la1[k1 + 4]),
+                                   to_tf32(rb[k1]), to_tf32(rb[k1 + 4]));
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) res[base + m][e] = d0[e] + d1[e];
                 }
             }
             __syncthreads();
@@ -360,24 +412,26 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
         float* Ab = reinterpret_cast<float*>(X + X_A);
         float* Tb = reinterpret_cast<float*>(X + X_T);
         float* scr = reinterpret_cast<float*>(X + X_SCR);
-        unsigned char* opP = sm + OFF_P;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
+            const int base = b == 0 ? 0 : (b == 1 ? 1 : (b == 2 ? 2 : 4));
 #pragma unroll
-            for (int m = 0; m <= b; ++m) {
-                const int cidx = warp + 4 * m;
-                const int ntiles = 2 * (b + 1);
-                const bool isk = cidx < ntiles;
-                const int nt = isk ? cidx : cidx - ntiles;
-                const float* d = res[b * (b + 1) / 2 + m];
+            for (int m = 0; m < 2; ++m) {
+                const int cidx = warp + 8 * m;
+                if (m <= (b >= 2 ? 1 : 0) && cidx < 4 * (b + 1)) {
+                    const int ntiles = 2 * (b + 1);
+                    const bool isk = cidx < ntiles;
+                    const int nt = isk ? cidx : cidx - ntiles;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = 16 * b + gid + ((e & 2) ? 8 : 0);
-                    const int s = 8 * nt + 2 * tig + (e & 1);
-                    if (isk)
-                        Ab[r * AT_LD + s] = s < r ? sbeta[r] * d[e] : 0.f;
-                    else
-                        *reinterpret_cast<float*>(opP + op_off(r, s, C)) = s <= r ? d[e] : 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = 16 * b + gid + ((e & 2) ? 8 : 0);
+                        const int s = 8 * nt + 2 * tig + (e & 1);
+                        const float d = res[base + m][e];
+                        if (isk)
+                            Ab[r * AT_LD + s] = s < r ? sbeta[r] * d : 0.f;
+                        else
+                            *reinterpret_cast<float*>(opP + op_off(r, s, C)) = s <= r ? d : 0.f;
+                    }
                 }
             }
         }
@@ -411,22 +465,28 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
             for (int e = tid; e < nblk * 256; e += NT) {   // Z = sum_{c<=m<b} A_bm T_mc
                 const int c = e >> 8, row = (e >> 4) & 15, col = e & 15;
                 const int b = c + d;
-                float acc = 0.f;
-                for (int mb = c; mb < b; ++mb)
+                float acc0 = 0.f, acc1 = 0.f;
+                for (int mb = c; mb < b; ++mb) {
 #pragma unroll
-                    for (int x = 0; x < 16; ++x)
-                        acc = fmaf(Ab[(16 * b + row) * AT_LD + 16 * mb + x], Tb[(16 * mb + x) * AT_LD + 16 * c + col], acc);
-                scr[e] = acc;
+                    for (int x = 0; x < 16; x += 2) {
+                        acc0 = fmaf(Ab[(16 * b + row) * AT_LD + 16 * mb + x], Tb[(16 * mb + x) * AT_LD + 16 * c + col], acc0);
+                        acc1 = fmaf(Ab[(16 * b + row) * AT_LD + 16 * mb + x + 1],
+                                    Tb[(16 * mb + x + 1) * AT_LD + 16 * c + col], acc1);
+                    }
+                }
+                scr[e] = acc0 + acc1;
             }
             __syncthreads();
             for (int e = tid; e < nblk * 256; e += NT) {   // T_bc = -T_bb Z
                 const int c = e >> 8, row = (e >> 4) & 15, col = e & 15;
                 const int b = c + d;
-                float acc = 0.f;
+                float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-                for (int x = 0; x < 16; ++x)
-                    acc = fmaf(Tb[(16 * b + row) * AT_LD + 16 * b + x], scr[(c << 8) + (x << 4) + col], acc);
-                Tb[(16 * b + row) * AT_LD + 16 * c + col] = -acc;
+                for (int x = 0; x < 16; x += 2) {
+                    acc0 = fmaf(Tb[(16 * b + row) * AT_LD + 16 * b + x], scr[(c << 8) + (x << 4) + col], acc0);
+                    acc1 = fmaf(Tb[(16 * b + row) * AT_LD + 16 * b + x + 1], scr[(c << 8) + ((x + 1) << 4) + col], acc1);
+                }
+                Tb[(16 * b + row) * AT_LD + 16 * c + col] = -(acc0 + acc1);
             }
             __syncthreads();
         }
@@ -448,10 +508,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
             float4 v;
             if (nrow < DK) {
                 const int i = nrow;
-                v.x = exp2f(G[(m0 + 0) * G_LD + i]) * bf(kraw + (m0 + 0) * KQ_LD + i);
-                v.y = exp2f(G[(m0 + 1) * G_LD + i]) * bf(kraw + (m0 + 1) * KQ_LD + i);
-                v.z = exp2f(G[(m0 + 2) * G_LD + i]) * bf(kraw + (m0 + 2) * KQ_LD + i);
-                v.w = exp2f(G[(m0 + 3) * G_LD + i]) * bf(kraw + (m0 + 3) * KQ_LD + i);
+                v.x = ex2f(G[(m0 + 0) * G_LD + i]) * bf(kraw + (m0 + 0) * KQ_LD + i);
+                v.y = ex2f(G[(m0 + 1) * G_LD + i]) * bf(kraw + (m0 + 1) * KQ_LD + i);
+                v.z = ex2f(G[(m0 + 2) * G_LD + i]) * bf(kraw + (m0 + 2) * KQ_LD + i);
+                v.w = ex2f(G[(m0 + 3) * G_LD + i]) * bf(kraw + (m0 + 3) * KQ_LD + i);
             } else {
                 const int j = nrow - DK;
                 v.x = bf(vraw + (m0 + 0) * NV + j);
@@ -473,31 +533,32 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
         if (!wait_mma()) { aborted = true; break; }
 
         // ---- 5. operands of the state-dependent GEMMs ----
-        float Ut[NV];
-        const int myrow = 16 * warp + lane;                 // M=64 accumulator row held by this lane (lane < 16)
+        float Ut[16];
+        const int myrow = 16 * quad + lane;                // M=64 accumulator row of this lane (lane < 16)
         {
             float v[32];
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                tmem_ld32(tmem + tlane + TM_WU + 32 * cb, v);
+            for (int cb = 0; cb < 2; ++cb) {
+                const int c0 = 64 * half + 32 * cb;
+                tmem_ld32(tmem + tlane + TM_WU + c0, v);
                 if (lane < 16) {
 #pragma unroll
                     for (int x = 0; x < 32; x += 4)
-                        *reinterpret_cast<float4*>(X + X_W + op_off(myrow, 32 * cb + x, DK)) =
+                        *reinterpret_cast<float4*>(X + X_W + op_off(myrow, c0 + x, DK)) =
                             make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
                 }
             }
-            tmem_ld32(tmem + tlane + TM_WU + 128, Ut);
+            tmem_ld16(tmem + tlane + TM_WU + DK + 16 * half, Ut);
         }
         for (int e = tid; e < C * 32; e += NT) {            // Gamma . Q  (M=64, K=128)
             const int r = ((e >> 8) << 3) | (e & 7), q4 = (e >> 3) & 31;
             const int i0 = 4 * q4;
             const float4 gg = *reinterpret_cast<const float4*>(G + r * G_LD + i0);
             float4 v;
-            v.x = exp2f(gg.x) * bf(qraw + r * KQ_LD + i0 + 0);
-            v.y = exp2f(gg.y) * bf(qraw + r * KQ_LD + i0 + 1);
-            v.z = exp2f(gg.z) * bf(qraw + r * KQ_LD + i0 + 2);
-            v.w = exp2f(gg.w) * bf(qraw + r * KQ_LD + i0 + 3);
+            v.x = ex2f(gg.x) * bf(qraw + r * KQ_LD + i0 + 0);
+            v.y = ex2f(gg.y) * bf(qraw + r * KQ_LD + i0 + 1);
+            v.z = ex2f(gg.z) * bf(qraw + r * KQ_LD + i0 + 2);
+            v.w = ex2f(gg.w) * bf(qraw + r * KQ_LD + i0 + 3);
             *reinterpret_cast<float4*>(X + X_QT + op_off(r, i0, DK)) = v;
         }
         for (int e = tid; e < DK * 16; e += NT) {           // Khat^T  (M=128 rows i, K=64 time)
@@ -505,10 +566,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
             const int s0 = 4 * q4;
             const float gl = G[(C - 1) * G_LD + i];
             float4 v;
-            v.x = exp2f(gl - G[(s0 + 0) * G_LD + i]) * bf(kraw + (s0 + 0) * KQ_LD + i);
-            v.y = exp2f(gl - G[(s0 + 1) * G_LD + i]) * bf(kraw + (s0 + 1) * KQ_LD + i);
-            v.z = exp2f(gl - G[(s0 + 2) * G_LD + i]) * bf(kraw + (s0 + 2) * KQ_LD + i);
-            v.w = exp2f(gl - G[(s0 + 3) * G_LD + i]) * bf(kraw + (s0 + 3) * KQ_LD + i);
+            v.x = ex2f(gl - G[(s0 + 0) * G_LD + i]) * bf(kraw + (s0 + 0) * KQ_LD + i);
+            v.y = ex2f(gl - G[(s0 + 1) * G_LD + i]) * bf(kraw + (s0 + 1) * KQ_LD + i);
+            v.z = ex2f(gl - G[(s0 + 2) * G_LD + i]) * bf(kraw + (s0 + 2) * KQ_LD + i);
+            v.w = ex2f(gl - G[(s0 + 3) * G_LD + i]) * bf(kraw + (s0 + 3) * KQ_LD + i);
             *reinterpret_cast<float4*>(Y + Y_KH + op_off(i, s0, C)) = v;
         }
         fence_async_smem();
@@ -528,12 +589,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
 
         // ---- 7. U = Utilde - X  ->  U^T operand (N=32 rows j, K=64 time) ----
         {
-            float xv[32];
-            tmem_ld32(tmem + tlane + TM_X, xv);
+            float xv[16];
+            tmem_ld16(tmem + tlane + TM_X + 16 * half, xv);
             if (lane < 16) {
 #pragma unroll
-                for (int j = 0; j < NV; ++j)
-                    *reinterpret_cast<float*>(Y + Y_U + op_off(j, myrow, C)) = Ut[j] - xv[j];
+                for (int j = 0; j < 16; ++j)
+                    *reinterpret_cast<float*>(Y + Y_U + op_off(16 * half + j, myrow, C)) = Ut[j] - xv[j];
             }
         }
         fence_async_smem();
@@ -551,22 +612,23 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
 
         // ---- 9. outputs and the carried state ----
         {
-            float ov[32];
-            tmem_ld32(tmem + tlane + TM_O, ov);
+            float ov[16];
+            tmem_ld16(tmem + tlane + TM_O + 16 * half, ov);
             if (lane < 16 && myrow < L) {
-                __nv_bfloat16* dst = go + ((int64_t)(t0 + myrow) * H + h) * p.dv + j0;
+                __nv_bfloat16* dst = go + ((int64_t)(t0 + myrow) * H + h) * p.dv + j0 + 16 * half;
 #pragma unroll
-                for (int x = 0; x < NV; x += 8) {
+                for (int x = 0; x < 16; x += 8) {
                     __align__(16) __nv_bfloat16 pk[8];
 #pragma unroll
                     for (int y = 0; y < 8; ++y) pk[y] = __float2bfloat16_rn(p.scale * ov[x + y]);
                     *reinterpret_cast<uint4*>(dst + x) = *reinterpret_cast<const uint4*>(pk);
                 }
             }
-            float dsv[32];
-            tmem_ld32(tmem + tlane + TM_S, dsv);
+            float dsv[16];
+            tmem_ld16(tmem + tlane + TM_S + 16 * half, dsv);
+            const float gamC = sgam[srow];
 #pragma unroll
-            for (int j = 0; j < NV; ++j) S[j] = fmaf(gamC, S[j], dsv[j]);
+            for (int j = 0; j < 16; ++j) S[j] = fmaf(gamC, S[j], dsv[j]);
             write_state_operand();
         }
         fence_async_smem();
@@ -577,7 +639,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
     // ---- state out, TMEM release ----
     if (!aborted) {
 #pragma unroll
-        for (int j = 0; j < NV; j += 4)
+        for (int j = 0; j < 16; j += 4)
             *reinterpret_cast<float4*>(p.state_out + state_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
     cp_async_wait_all();
