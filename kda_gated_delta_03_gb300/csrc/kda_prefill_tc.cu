@@ -22,10 +22,16 @@
 // kept in float32 registers, one key row per pair of threads.
 //
 // One CTA = (sequence, head, 32 value columns); 256 threads (two threads per
-// TMEM lane, splitting the columns); thread 0 issues the tcgen05 MMAs.  The next chunk's inputs are fetched with cp.async while
-// the current chunk runs its state-dependent GEMMs.  Every wait on an MMA
+// TMEM lane, splitting the columns); thread 0 issues the tcgen05 MMAs.  The next chunk's rows are fetched with bulk copies (one per row,
+// completing on an mbarrier) while the current chunk runs its state-dependent GEMMs.  Every wait on an MMA
 // completion is bounded; on timeout the CTA records KDA_DEVERR_TIMEOUT, frees
 // its TMEM and stops.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
 
 #include "kda_internal.cuh"
 
@@ -39,20 +45,21 @@ constexpr int NT = 256;
 constexpr long long kWaitLimit = 4000000000LL;   // clock cycles (about 2 s)
 
 // ---- shared memory map (bytes) ----
-constexpr int KQ_LD = 136;                       // bf16 per raw k / q row (272 B)
-constexpr int G_LD = 132;                        // floats per log-decay row
 constexpr int F_LD = 132;                        // floats per A/P factor row
 constexpr int AT_LD = 68;                        // floats per row of the 64x64 solve tiles
+// raw tiles, written by TMA: k, q as two 128B-swizzled boxes of 64 rows x 64 bf16, alpha (then g) as
+// four 128B-swizzled boxes of 64 rows x 32 fp32, the v slice dense (64 rows x 32 bf16)
 constexpr int OFF_K = 0;
-constexpr int OFF_Q = OFF_K + C * KQ_LD * 2;     // 17408
-constexpr int OFF_G = OFF_Q + C * KQ_LD * 2;     // 34816
-constexpr int OFF_BETA = OFF_G + C * G_LD * 4;   // 68608
-constexpr int OFF_V = OFF_BETA + 256;            // 68864
-constexpr int OFF_X = OFF_V + C * NV * 2;        // 72960  region X, 64 KiB
-constexpr int OFF_Y = OFF_X + 65536;             // 138496 region Y, 56 KiB
-constexpr int OFF_P = OFF_Y + 57344;             // 195840 P operand
-constexpr int OFF_S = OFF_P + 16384;             // 212224 S^T operand
-constexpr int OFF_MISC = OFF_S + 16384;          // 228608
+constexpr int OFF_Q = 16384;
+constexpr int OFF_G = 32768;
+constexpr int OFF_V = 65536;
+constexpr int OFF_BETA = 69632;
+constexpr int OFF_X = 70656;                     // region X, 64 KiB
+constexpr int OFF_Y = OFF_X + 65536;             // region Y, 56 KiB
+constexpr int OFF_P = OFF_Y + 57344;             // P operand
+constexpr int OFF_S = OFF_P + 16384;             // S^T operand
+constexpr int OFF_MISC = OFF_S + 16384;
+constexpr uint32_t kChunkTxBytes = 2 * 16384 + 32768 + C * NV * 2;   // bytes the TMA loads of one chunk deliver
 constexpr int SMEM_BYTES = OFF_MISC + 64 + DK * 4;
 // region X: G1 factors -> solve tiles -> W, Gamma.Q operands
 constexpr int X_R = 0, X_LK = C * F_LD * 4, X_LQ = X_LK + 16 * F_LD * 4;
@@ -62,7 +69,7 @@ constexpr int X_W = 0, X_QT = 32768;
 constexpr int Y_T = 0, Y_KV = 16384;
 constexpr int Y_KH = 0, Y_U = 32768;
 // misc
-constexpr int M_MBAR = 0, M_TMEM = 8, M_ABORT = 12, M_GAMC = 64;
+constexpr int M_MBAR = 0, M_TMEM = 8, M_ABORT = 12, M_LBAR = 16, M_GAMC = 64;
 // TMEM columns
 constexpr uint32_t TM_WU = 0, TM_X = 160, TM_O = 192, TM_S = 224, TM_COLS = 256;
 
@@ -76,6 +83,14 @@ __device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cv
 // core matrices of 8 rows x 16 B, K-adjacent ones 128 B apart, 8-row groups K*32 B apart.
 __device__ __forceinline__ uint32_t op_off(int row, int k, int K) {
     return (uint32_t)((row >> 3) * (K * 32) + (k >> 2) * 128 + (row & 7) * 16 + (k & 3) * 4);
+}
+
+// Byte offsets inside the raw tiles (128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7)).
+__device__ __forceinline__ int g_off(int r, int i) {      // fp32 [64][128] as four 32-column boxes
+    return ((i >> 5) << 13) + (r << 7) + ((((i & 31) >> 2) ^ (r & 7)) << 4) + ((i & 3) << 2);
+}
+__device__ __forceinline__ int kq_off(int r, int i) {     // bf16 [64][128] as two 64-column boxes
+    return ((i >> 6) << 13) + (r << 7) + ((((i & 63) >> 3) ^ (r & 7)) << 4) + ((i & 7) << 1);
 }
 
 __device__ __forceinline__ uint64_t op_desc(uint32_t addr, int K) {
@@ -182,10 +197,27 @@ __device__ __forceinline__ void mma_16x8x8(float (&d)[4], uint32_t a0, uint32_t 
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
+__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(to_tf32(x)); }
+
+// Four 8x8 b16 matrices = four 8-row x 4-column fp32 tiles; lane l supplies the row address of tile l/8.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
 }
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+
+// TMA tile load of box (x, y, z) of a 3-D tensor map into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
+        : "memory");
+}
+
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0)
                  : "memory");
@@ -195,38 +227,33 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 __device__ __forceinline__ float bf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
+// Tensor maps of the raw inputs: k, q [T, H, 128] bf16 (64-column boxes), alpha [T, H, 128] fp32
+// (32-column boxes), v [T, H, d_v] bf16 (32-column box); each box is 64 tokens of one head.
+struct TcMaps {
+    CUtensorMap k, q, a, v;
+};
+
 struct Tile {
-    const __nv_bfloat16* k;
-    const __nv_bfloat16* q;
-    const __nv_bfloat16* v;
-    const float* alpha;
     const float* beta;
     int H;
     int h;
     int j0;
-    int dv;
 };
 
-// Fetch the raw inputs of the chunk starting at token t0 (L valid rows; the rest zero-filled).
-__device__ __forceinline__ void issue_chunk_loads(unsigned char* sm, const Tile& g, int32_t t0, int L, int tid) {
-    for (int e = tid; e < C * 16; e += NT) {
-        const int r = e >> 4, c = e & 15;
-        const bool ok = r < L;
-        const int64_t row = ok ? ((int64_t)(t0 + r) * g.H + g.h) : 0;
-        cp_async16(saddr(sm + OFF_K + r * KQ_LD * 2 + c * 16), g.k + row * DK + c * 8, ok);
-        cp_async16(saddr(sm + OFF_Q + r * KQ_LD * 2 + c * 16), g.q + row * DK + c * 8, ok);
-    }
-    for (int e = tid; e < C * 32; e += NT) {
-        const int r = e >> 5, c = e & 31;
-        const bool ok = r < L;
-        const int64_t row = ok ? ((int64_t)(t0 + r) * g.H + g.h) : 0;
-        cp_async16(saddr(sm + OFF_G + (r * G_LD + c * 4) * 4), g.alpha + row * DK + c * 4, ok);
-    }
-    for (int e = tid; e < C * 4; e += NT) {
-        const int r = e >> 2, c = e & 3;
-        const bool ok = r < L;
-        const int64_t row = ok ? ((int64_t)(t0 + r) * g.H + g.h) : 0;
-        cp_async16(saddr(sm + OFF_V + r * NV * 2 + c * 16), g.v + row * g.dv + g.j0 + c * 8, ok);
+// Fetch the raw rows of the chunk starting at token t0: one thread issues the 9 TMA box loads
+// (completing on `lbar`); beta (strided by H) goes through 4-byte cp.async with zero fill.  Rows at
+// or past the sequence end are zeroed by the consumer.
+__device__ __forceinline__ void issue_chunk_loads(unsigned char* sm, const TcMaps& m, const Tile& g, int32_t t0,
+                                                  int L, int tid, uint32_t lbar) {
+    if (tid == 32) {
+        mbar_expect_tx(lbar, kChunkTxBytes);
+        tma_load_3d(saddr(sm + OFF_K), &m.k, 0, g.h, t0, lbar);
+        tma_load_3d(saddr(sm + OFF_K + 8192), &m.k, 64, g.h, t0, lbar);
+        tma_load_3d(saddr(sm + OFF_Q), &m.q, 0, g.h, t0, lbar);
+        tma_load_3d(saddr(sm + OFF_Q + 8192), &m.q, 64, g.h, t0, lbar);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) tma_load_3d(saddr(sm + OFF_G + b * 8192), &m.a, 32 * b, g.h, t0, lbar);
+        tma_load_3d(saddr(sm + OFF_V), &m.v, g.j0, g.h, t0, lbar);
     }
     for (int r = tid; r < C; r += NT) {
         const bool ok = r < L;
@@ -236,7 +263,7 @@ __device__ __forceinline__ void issue_chunk_loads(unsigned char* sm, const Tile&
     cp_async_commit();
 }
 
-__global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) {
+__global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, const __grid_constant__ TcMaps maps) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
@@ -261,14 +288,13 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
         return;
     }
     const int H = p.H;
-    Tile g{static_cast<const __nv_bfloat16*>(p.k), static_cast<const __nv_bfloat16*>(p.q),
-           static_cast<const __nv_bfloat16*>(p.v), p.alpha, p.beta, H, h, j0, p.dv};
+    Tile g{p.beta, H, h, j0};
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(p.o);
 
-    __nv_bfloat16* kraw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_K);
-    __nv_bfloat16* qraw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_Q);
     __nv_bfloat16* vraw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_V);
-    float* G = reinterpret_cast<float*>(sm + OFF_G);
+    auto Gat = [&](int r, int i) -> float& { return *reinterpret_cast<float*>(sm + OFF_G + g_off(r, i)); };
+    auto kat = [&](int r, int i) { return bf(reinterpret_cast<const __nv_bfloat16*>(sm + OFF_K + kq_off(r, i))); };
+    auto qat = [&](int r, int i) { return bf(reinterpret_cast<const __nv_bfloat16*>(sm + OFF_Q + kq_off(r, i))); };
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* sgam = reinterpret_cast<float*>(sm + OFF_MISC + M_GAMC);
     unsigned char* X = sm + OFF_X;
@@ -277,10 +303,17 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + OFF_MISC + M_ABORT);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + OFF_MISC + M_TMEM);
     const uint32_t mbar = saddr(sm + OFF_MISC + M_MBAR);
+    const uint32_t lbar = saddr(sm + OFF_MISC + M_LBAR);
+
+    if (saddr(sm) & 1023u) {                          // the swizzled tiles need a 1 KiB-aligned base
+        if (tid == 0) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
+        return;
+    }
 
     // ---- set-up: barrier, TMEM, first loads ----
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(lbar) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *s_abort = 0;
     }
@@ -290,7 +323,6 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (t_begin < t_end) issue_chunk_loads(sm, g, t_begin, min(C, t_end - t_begin), tid);
 
     // state: key row srow, value columns 16*half .. 16*half+15 of this slice, float32 in registers
     const int srow = 32 * quad + lane;
@@ -307,8 +339,13 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t tlane = (uint32_t)(quad * 32) << 16;   // this warp's TMEM lane quadrant
-    uint32_t phase = 0;
+    uint32_t phase = 0, lphase = 0;
     bool aborted = false;
+    bool loads_pending = false;
+    if (t_begin < t_end) {
+        issue_chunk_loads(sm, maps, g, t_begin, min(C, t_end - t_begin), tid, lbar);
+        loads_pending = true;
+    }
 
     auto write_state_operand = [&]() {
 #pragma unroll
@@ -327,18 +364,39 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
         return true;
     };
     write_state_operand();
+    for (int e = tid; e < C * C; e += NT) {             // P beyond each row block's columns is always zero
+        const int r = e >> 6, s = e & 63;
+        if (s >= 16 * ((r >> 4) + 1)) *reinterpret_cast<float*>(opP + op_off(r, s, C)) = 0.f;
+    }
 
     for (int32_t t0 = t_begin; t0 < t_end && !aborted; t0 += C) {
         const int L = min(C, t_end - t0);
         cp_async_wait_all();
+        if (!mbar_wait(lbar, lphase)) {
+            atomicOr(p.err, KDA_DEVERR_TIMEOUT);
+            *s_abort = 1;
+        }
+        lphase ^= 1u;
+        loads_pending = false;
         __syncthreads();
+        if (*s_abort) { aborted = true; break; }
+        if (L < C) {                                    // zero the rows past the sequence end
+            for (int e = tid; e < (C - L) * 16; e += NT) {
+                const int r = L + (e >> 4), c = e & 15;      // 16-byte chunk c of row r (two boxes of 8)
+                const int off = ((c >> 3) << 13) + (r << 7) + ((c & 7) << 4);
+                *reinterpret_cast<uint4*>(sm + OFF_K + off) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(sm + OFF_Q + off) = make_uint4(0, 0, 0, 0);
+                if (c < 4) *reinterpret_cast<uint4*>(sm + OFF_V + r * NV * 2 + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+            __syncthreads();
+        }
 
         // ---- 1. g = running sum of clamped log2 alpha per key channel: each thread scans 32 rows,
         //         then the upper half adds the lower half's total ----
         {
             float la[32];
 #pragma unroll
-            for (int x = 0; x < 32; ++x) la[x] = G[(32 * rh + x) * G_LD + ch];
+            for (int x = 0; x < 32; ++x) la[x] = Gat(32 * rh + x, ch);
             float acc = 0.f;
 #pragma unroll
             for (int x = 0; x < 32; ++x) {
@@ -346,12 +404,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
                 la[x] = acc;
             }
 #pragma unroll
-            for (int x = 0; x < 32; ++x) G[(32 * rh + x) * G_LD + ch] = la[x];
+            for (int x = 0; x < 32; ++x) Gat(32 * rh + x, ch) = la[x];
             __syncthreads();
             if (rh == 1) {
-                const float base = G[31 * G_LD + ch];
+                const float base = Gat(31, ch);
 #pragma unroll
-                for (int x = 0; x < 32; ++x) G[(32 + x) * G_LD + ch] = la[x] + base;
+                for (int x = 0; x < 32; ++x) Gat(32 + x, ch) = la[x] + base;
                 sgam[ch] = ex2f(la[31] + base);
             }
         }
@@ -364,46 +422,71 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
         float res[6][4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            {   // factors of block b: thread (channel, row half)
-                const float ref = G[(16 * b + 7) * G_LD + ch];
+            {   // factors of block b: thread (channel, row half); all loads first, then math, then stores
+                const float ref = Gat(16 * b + 7, ch);
+                float gr[8], kv[8], qv[8];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const int r = 16 * b + 8 * rh + x;
+                    gr[x] = Gat(r, ch);
+                    kv[x] = kat(r, ch);
+                    qv[x] = qat(r, ch);
+                }
                 if (b > 0) {
-                    const float f = ex2f(ref - G[(16 * b - 9) * G_LD + ch]);
-                    for (int s = rh; s < 16 * b; s += 2) R[s * F_LD + ch] *= f;
+                    const float f = ex2f(ref - Gat(16 * b - 9, ch));
+                    float old[24];
+#pragma unroll
+                    for (int x = 0; x < 8 * b; ++x) old[x] = R[(rh + 2 * x) * F_LD + ch];
+#pragma unroll
+                    for (int x = 0; x < 8 * b; ++x) R[(rh + 2 * x) * F_LD + ch] = tf32r(old[x] * f);
                 }
 #pragma unroll
                 for (int x = 0; x < 8; ++x) {
                     const int rr = 8 * rh + x, r = 16 * b + rr;
-                    const float gr = G[r * G_LD + ch];
-                    const float kv = bf(kraw + r * KQ_LD + ch);
-                    R[r * F_LD + ch] = kv * ex2f(ref - gr);
-                    const float f = ex2f(gr - ref);
-                    Lk[rr * F_LD + ch] = kv * f;
-                    Lq[rr * F_LD + ch] = bf(qraw + r * KQ_LD + ch) * f;
+                    const float f = ex2f(gr[x] - ref);
+                    R[r * F_LD + ch] = tf32r(kv[x] * ex2f(ref - gr[x]));
+                    Lk[rr * F_LD + ch] = tf32r(kv[x] * f);
+                    Lq[rr * F_LD + ch] = tf32r(qv[x] * f);
                 }
             }
             __syncthreads();
             const int base = b == 0 ? 0 : (b == 1 ? 1 : (b == 2 ? 2 : 4));
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int cidx = warp + 8 * m;             // (which, n-tile) combination
-                if (m <= (b >= 2 ? 1 : 0) && cidx < 4 * (b + 1)) {
-                    const int ntiles = 2 * (b + 1);
+            const int ntiles = 2 * (b + 1);
+            const bool has0 = warp < 4 * (b + 1);                 // combination (which, n-tile) = warp
+            const bool has1 = b >= 2 && warp + 8 < 4 * (b + 1);    // second combination = warp + 8
+            if (has0) {
+                auto addrs = [&](int cidx, uint32_t& a_addr, uint32_t& b_addr) {
                     const float* Lf = cidx < ntiles ? Lk : Lq;
                     const int nt = cidx < ntiles ? cidx : cidx - ntiles;
-                    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-                    const float* la0 = Lf + gid * F_LD + tig;
-                    const float* la1 = Lf + (gid + 8) * F_LD + tig;
-                    const float* rb = R + (8 * nt + gid) * F_LD + tig;
-#pragma unroll 4
-                    for (int kk = 0; kk < DK / 8; kk += 2) {
-                        const int k0 = kk * 8, k1 = k0 + 8;
-                        mma_16x8x8(d0, to_tf32(la0[k0]), to_tf32(la1[k0]), to_tf32(la0[k0 + 4]), to_tf32(la1[k0 + 4]),
-                                   to_tf32(rb[k0]), to_tf32(rb[k0 + 4]));
-                        mma_16x8x8(d1, to_tf32(la0[k1]), to_tf32(la1[k1]), to_tf32(la0[k1 + 4]), to_tf32(la1[k1 + 4]),
-                                   to_tf32(rb[k1]), to_tf32(rb[k1 + 4]));
+                    a_addr = saddr(Lf + ((lane & 7) + ((lane >> 3) & 1) * 8) * F_LD + (lane >> 4) * 4);
+                    b_addr = saddr(R + (8 * nt + (lane & 7)) * F_LD + (lane >> 3) * 4);
+                };
+                uint32_t a0a, b0a, a1a = 0, b1a = 0;
+                addrs(warp, a0a, b0a);
+                if (has1) addrs(warp + 8, a1a, b1a);
+                float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+                for (int kk = 0; kk < DK / 8; kk += 2) {
+                    const uint32_t off = kk * 32;                   // 8 fp32 per k-step
+                    uint32_t fa[4], fa2[4], fb[4];
+                    ldsm_x4(a0a + off, fa);
+                    ldsm_x4(a0a + off + 32, fa2);
+                    ldsm_x4(b0a + off, fb);
+                    mma_16x8x8(d0, fa[0], fa[1], fa[2], fa[3], fb[0], fb[1]);
+                    mma_16x8x8(d1, fa2[0], fa2[1], fa2[2], fa2[3], fb[2], fb[3]);
+                    if (has1) {
+                        ldsm_x4(a1a + off, fa);
+                        ldsm_x4(a1a + off + 32, fa2);
+                        ldsm_x4(b1a + off, fb);
+                        mma_16x8x8(e0, fa[0], fa[1], fa[2], fa[3], fb[0], fb[1]);
+                        mma_16x8x8(e1, fa2[0], fa2[1], fa2[2], fa2[3], fb[2], fb[3]);
                     }
+                }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) res[base + m][e] = d0[e] + d1[e];
+                for (int e = 0; e < 4; ++e) {
+                    res[base][e] = d0[e] + d1[e];
+                    if (b >= 2) res[base + 1][e] = e0[e] + e1[e];
                 }
             }
             __syncthreads();
@@ -434,10 +517,6 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
                     }
                 }
             }
-        }
-        for (int e = tid; e < C * C; e += NT) {        // P beyond each row block's columns is zero
-            const int r = e >> 6, s = e & 63;
-            if (s >= 16 * ((r >> 4) + 1)) *reinterpret_cast<float*>(opP + op_off(r, s, C)) = 0.f;
         }
         __syncthreads();
 
@@ -501,25 +580,20 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
             v.w = m0 + 3 <= r ? Tb[r * AT_LD + m0 + 3] * sbeta[m0 + 3] : 0.f;
             *reinterpret_cast<float4*>(Y + Y_T + op_off(r, m0, C)) = v;
         }
-        // [Gamma.K | V]^T -> operand (N=160 rows, K=64 time)
-        for (int e = tid; e < 160 * 16; e += NT) {
-            const int nrow = ((e >> 7) << 3) | (e & 7), q4 = (e >> 3) & 15;
-            const int m0 = 4 * q4;
-            float4 v;
-            if (nrow < DK) {
-                const int i = nrow;
-                v.x = ex2f(G[(m0 + 0) * G_LD + i]) * bf(kraw + (m0 + 0) * KQ_LD + i);
-                v.y = ex2f(G[(m0 + 1) * G_LD + i]) * bf(kraw + (m0 + 1) * KQ_LD + i);
-                v.z = ex2f(G[(m0 + 2) * G_LD + i]) * bf(kraw + (m0 + 2) * KQ_LD + i);
-                v.w = ex2f(G[(m0 + 3) * G_LD + i]) * bf(kraw + (m0 + 3) * KQ_LD + i);
-            } else {
-                const int j = nrow - DK;
-                v.x = bf(vraw + (m0 + 0) * NV + j);
-                v.y = bf(vraw + (m0 + 1) * NV + j);
-                v.z = bf(vraw + (m0 + 2) * NV + j);
-                v.w = bf(vraw + (m0 + 3) * NV + j);
-            }
-            *reinterpret_cast<float4*>(Y + Y_KV + op_off(nrow, m0, C)) = v;
+        // [Gamma.K | V]^T -> operand (N=160 rows, K=64 time); lanes run over channels
+        for (int e = tid; e < DK * 16; e += NT) {
+            const int i = e & (DK - 1), m0 = 4 * (e >> 7);
+            float gg[4], kk4[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) { gg[x] = Gat(m0 + x, i); kk4[x] = kat(m0 + x, i); }
+            *reinterpret_cast<float4*>(Y + Y_KV + op_off(i, m0, C)) =
+                make_float4(ex2f(gg[0]) * kk4[0], ex2f(gg[1]) * kk4[1], ex2f(gg[2]) * kk4[2], ex2f(gg[3]) * kk4[3]);
+        }
+        for (int e = tid; e < NV * 16; e += NT) {
+            const int j = e & (NV - 1), m0 = 4 * (e >> 5);
+            *reinterpret_cast<float4*>(Y + Y_KV + op_off(DK + j, m0, C)) =
+                make_float4(bf(vraw + (m0 + 0) * NV + j), bf(vraw + (m0 + 1) * NV + j), bf(vraw + (m0 + 2) * NV + j),
+                            bf(vraw + (m0 + 3) * NV + j));
         }
         fence_async_smem();
         __syncthreads();
@@ -553,30 +627,32 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
         for (int e = tid; e < C * 32; e += NT) {            // Gamma . Q  (M=64, K=128)
             const int r = ((e >> 8) << 3) | (e & 7), q4 = (e >> 3) & 31;
             const int i0 = 4 * q4;
-            const float4 gg = *reinterpret_cast<const float4*>(G + r * G_LD + i0);
-            float4 v;
-            v.x = ex2f(gg.x) * bf(qraw + r * KQ_LD + i0 + 0);
-            v.y = ex2f(gg.y) * bf(qraw + r * KQ_LD + i0 + 1);
-            v.z = ex2f(gg.z) * bf(qraw + r * KQ_LD + i0 + 2);
-            v.w = ex2f(gg.w) * bf(qraw + r * KQ_LD + i0 + 3);
-            *reinterpret_cast<float4*>(X + X_QT + op_off(r, i0, DK)) = v;
+            const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(r, i0));
+            const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(r, i0));
+            const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162*>(&qq.x);
+            const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162*>(&qq.y);
+            *reinterpret_cast<float4*>(X + X_QT + op_off(r, i0, DK)) =
+                make_float4(ex2f(gg.x) * __low2float(q01), ex2f(gg.y) * __high2float(q01),
+                            ex2f(gg.z) * __low2float(q23), ex2f(gg.w) * __high2float(q23));
         }
         for (int e = tid; e < DK * 16; e += NT) {           // Khat^T  (M=128 rows i, K=64 time)
-            const int i = ((e >> 7) << 3) | (e & 7), q4 = (e >> 3) & 15;
-            const int s0 = 4 * q4;
-            const float gl = G[(C - 1) * G_LD + i];
-            float4 v;
-            v.x = ex2f(gl - G[(s0 + 0) * G_LD + i]) * bf(kraw + (s0 + 0) * KQ_LD + i);
-            v.y = ex2f(gl - G[(s0 + 1) * G_LD + i]) * bf(kraw + (s0 + 1) * KQ_LD + i);
-            v.z = ex2f(gl - G[(s0 + 2) * G_LD + i]) * bf(kraw + (s0 + 2) * KQ_LD + i);
-            v.w = ex2f(gl - G[(s0 + 3) * G_LD + i]) * bf(kraw + (s0 + 3) * KQ_LD + i);
-            *reinterpret_cast<float4*>(Y + Y_KH + op_off(i, s0, C)) = v;
+            const int i = e & (DK - 1), s0 = 4 * (e >> 7);
+            const float gl = Gat(C - 1, i);
+            float gg[4], kk4[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) { gg[x] = Gat(s0 + x, i); kk4[x] = kat(s0 + x, i); }
+            *reinterpret_cast<float4*>(Y + Y_KH + op_off(i, s0, C)) =
+                make_float4(ex2f(gl - gg[0]) * kk4[0], ex2f(gl - gg[1]) * kk4[1], ex2f(gl - gg[2]) * kk4[2],
+                            ex2f(gl - gg[3]) * kk4[3]);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         // the raw tiles are free: fetch the next chunk while the state GEMMs run
-        if (t0 + C < t_end) issue_chunk_loads(sm, g, t0 + C, min(C, t_end - t0 - C), tid);
+        if (t0 + C < t_end) {
+            issue_chunk_loads(sm, maps, g, t0 + C, min(C, t_end - t0 - C), tid, lbar);
+            loads_pending = true;
+        }
 
         // ---- 6. X = W S, O = (Gamma.Q) S ----
         if (tid == 0) {
@@ -643,6 +719,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p) 
             *reinterpret_cast<float4*>(p.state_out + state_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
     cp_async_wait_all();
+    if (loads_pending) mbar_wait(lbar, lphase);         // bounded: never leave copies in flight
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -659,13 +736,58 @@ bool prefill_tc_supported(const PrefillParams& p, kda_dtype dt) {
 
 int prefill_tc_slices(int dv) { return dv / NV; }
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 3-D map over [T][H][cols] with a box of (box_cols, 1 head, 64 tokens).
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, CUtensorMapDataType dt, const void* base,
+                 int esize, int cols, int H, int T, int box_cols, CUtensorMapSwizzle sw) {
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * esize, (cuuint64_t)cols * esize * H};
+    const cuuint32_t box[3] = {(cuuint32_t)box_cols, 1u, (cuuint32_t)C};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s) {
+    TcMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    if (p.total_tokens > 0) {                        // with no tokens no CTA loads anything
+        auto enc = tensor_map_encoder();
+        if (!enc) return cudaErrorNotSupported;
+        const int T = p.total_tokens;
+        if (!encode_rows(enc, &maps.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, 2, DK, p.H, T, 64,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_rows(enc, &maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, 2, DK, p.H, T, 64,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_rows(enc, &maps.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.alpha, 4, DK, p.H, T, 32,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_rows(enc, &maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, 2, p.dv, p.H, T, NV,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
     cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t blocks = (int64_t)p.num_seqs * p.H * p.slices;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 2147483647LL) return cudaErrorInvalidValue;
-    kda_prefill_tc_kernel<<<(unsigned)blocks, NT, SMEM_BYTES, s>>>(p);
+    kda_prefill_tc_kernel<<<(unsigned)blocks, NT, SMEM_BYTES, s>>>(p, maps);
     return cudaGetLastError();
 }
 
