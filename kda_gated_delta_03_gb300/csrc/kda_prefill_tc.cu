@@ -464,29 +464,34 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
                 uint32_t a0a, b0a, a1a = 0, b1a = 0;
                 addrs(warp, a0a, b0a);
                 if (has1) addrs(warp + 8, a1a, b1a);
-                float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-                float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-                for (int kk = 0; kk < DK / 8; kk += 2) {
-                    const uint32_t off = kk * 32;                   // 8 fp32 per k-step
-                    uint32_t fa[4], fa2[4], fb[4];
-                    ldsm_x4(a0a + off, fa);
-                    ldsm_x4(a0a + off + 32, fa2);
-                    ldsm_x4(b0a + off, fb);
-                    mma_16x8x8(d0, fa[0], fa[1], fa[2], fa[3], fb[0], fb[1]);
-                    mma_16x8x8(d1, fa2[0], fa2[1], fa2[2], fa2[3], fb[2], fb[3]);
+                float d[4][4] = {}, e4[4][4] = {};
+#pragma unroll
+                for (int kk = 0; kk < DK / 8; kk += 4) {            // 4 k-steps, 4 independent chains
+                    const uint32_t off = kk * 32;                     // 8 fp32 per k-step
+                    uint32_t fa[4][4], fb0[4], fb1[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) ldsm_x4(a0a + off + 32 * t, fa[t]);
+                    ldsm_x4(b0a + off, fb0);
+                    ldsm_x4(b0a + off + 64, fb1);
+                    mma_16x8x8(d[0], fa[0][0], fa[0][1], fa[0][2], fa[0][3], fb0[0], fb0[1]);
+                    mma_16x8x8(d[1], fa[1][0], fa[1][1], fa[1][2], fa[1][3], fb0[2], fb0[3]);
+                    mma_16x8x8(d[2], fa[2][0], fa[2][1], fa[2][2], fa[2][3], fb1[0], fb1[1]);
+                    mma_16x8x8(d[3], fa[3][0], fa[3][1], fa[3][2], fa[3][3], fb1[2], fb1[3]);
                     if (has1) {
-                        ldsm_x4(a1a + off, fa);
-                        ldsm_x4(a1a + off + 32, fa2);
-                        ldsm_x4(b1a + off, fb);
-                        mma_16x8x8(e0, fa[0], fa[1], fa[2], fa[3], fb[0], fb[1]);
-                        mma_16x8x8(e1, fa2[0], fa2[1], fa2[2], fa2[3], fb[2], fb[3]);
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) ldsm_x4(a1a + off + 32 * t, fa[t]);
+                        ldsm_x4(b1a + off, fb0);
+                        ldsm_x4(b1a + off + 64, fb1);
+                        mma_16x8x8(e4[0], fa[0][0], fa[0][1], fa[0][2], fa[0][3], fb0[0], fb0[1]);
+                        mma_16x8x8(e4[1], fa[1][0], fa[1][1], fa[1][2], fa[1][3], fb0[2], fb0[3]);
+                        mma_16x8x8(e4[2], fa[2][0], fa[2][1], fa[2][2], fa[2][3], fb1[0], fb1[1]);
+                        mma_16x8x8(e4[3], fa[3][0], fa[3][1], fa[3][2], fa[3][3], fb1[2], fb1[3]);
                     }
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    res[base][e] = d0[e] + d1[e];
-                    if (b >= 2) res[base + 1][e] = e0[e] + e1[e];
+                    res[base][e] = (d[0][e] + d[1][e]) + (d[2][e] + d[3][e]);
+                    if (b >= 2) res[base + 1][e] = (e4[0][e] + e4[1][e]) + (e4[2][e] + e4[3][e]);
                 }
             }
             __syncthreads();
@@ -537,35 +542,46 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
             for (int r = 0; r < 16; ++r) Tb[(16 * b + r) * AT_LD + 16 * b + c] = tc[r];
         }
         __syncthreads();
-        // off-diagonal blocks, by distance d = b - c
+        // off-diagonal blocks, by distance d = b - c:  Z = sum_{c<=m<b} A_bm T_mc,  T_bc = -T_bb Z
 #pragma unroll
         for (int d = 1; d < 4; ++d) {
             const int nblk = 4 - d;
-            for (int e = tid; e < nblk * 256; e += NT) {   // Z = sum_{c<=m<b} A_bm T_mc
+            for (int e = tid; e < nblk * 256; e += NT) {
                 const int c = e >> 8, row = (e >> 4) & 15, col = e & 15;
-                const int b = c + d;
-                float acc0 = 0.f, acc1 = 0.f;
-                for (int mb = c; mb < b; ++mb) {
+                const float* arow = Ab + (16 * (c + d) + row) * AT_LD + 16 * c;   // A_{b, c..b-1}, 16d entries
+                const float* tcol = Tb + (16 * c) * AT_LD + 16 * c + col;          // T_{c..b-1, c}, column col
+                float tv[48];
 #pragma unroll
-                    for (int x = 0; x < 16; x += 2) {
-                        acc0 = fmaf(Ab[(16 * b + row) * AT_LD + 16 * mb + x], Tb[(16 * mb + x) * AT_LD + 16 * c + col], acc0);
-                        acc1 = fmaf(Ab[(16 * b + row) * AT_LD + 16 * mb + x + 1],
-                                    Tb[(16 * mb + x + 1) * AT_LD + 16 * c + col], acc1);
-                    }
+                for (int x = 0; x < 16 * d; ++x) tv[x] = tcol[x * AT_LD];
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int x = 0; x < 16 * d; x += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(arow + x);
+                    acc[0] = fmaf(a4.x, tv[x], acc[0]);
+                    acc[1] = fmaf(a4.y, tv[x + 1], acc[1]);
+                    acc[2] = fmaf(a4.z, tv[x + 2], acc[2]);
+                    acc[3] = fmaf(a4.w, tv[x + 3], acc[3]);
                 }
-                scr[e] = acc0 + acc1;
+                scr[e] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             }
             __syncthreads();
-            for (int e = tid; e < nblk * 256; e += NT) {   // T_bc = -T_bb Z
+            for (int e = tid; e < nblk * 256; e += NT) {
                 const int c = e >> 8, row = (e >> 4) & 15, col = e & 15;
                 const int b = c + d;
-                float acc0 = 0.f, acc1 = 0.f;
+                const float* trow = Tb + (16 * b + row) * AT_LD + 16 * b;
+                float zv[16];
 #pragma unroll
-                for (int x = 0; x < 16; x += 2) {
-                    acc0 = fmaf(Tb[(16 * b + row) * AT_LD + 16 * b + x], scr[(c << 8) + (x << 4) + col], acc0);
-                    acc1 = fmaf(Tb[(16 * b + row) * AT_LD + 16 * b + x + 1], scr[(c << 8) + ((x + 1) << 4) + col], acc1);
+                for (int x = 0; x < 16; ++x) zv[x] = scr[(c << 8) + (x << 4) + col];
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int x = 0; x < 16; x += 4) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(trow + x);
+                    acc[0] = fmaf(t4.x, zv[x], acc[0]);
+                    acc[1] = fmaf(t4.y, zv[x + 1], acc[1]);
+                    acc[2] = fmaf(t4.z, zv[x + 2], acc[2]);
+                    acc[3] = fmaf(t4.w, zv[x + 3], acc[3]);
                 }
-                Tb[(16 * b + row) * AT_LD + 16 * c + col] = -(acc0 + acc1);
+                Tb[(16 * b + row) * AT_LD + 16 * c + col] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
             }
             __syncthreads();
         }
@@ -581,13 +597,18 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
             *reinterpret_cast<float4*>(Y + Y_T + op_off(r, m0, C)) = v;
         }
         // [Gamma.K | V]^T -> operand (N=160 rows, K=64 time); lanes run over channels
-        for (int e = tid; e < DK * 16; e += NT) {
-            const int i = e & (DK - 1), m0 = 4 * (e >> 7);
-            float gg[4], kk4[4];
+        for (int e = tid; e < DK * 16; e += 2 * NT) {       // two items per iteration
+            const int i = e & (DK - 1), m0 = 4 * (e >> 7), m1 = m0 + 4 * (NT >> 7);
+            float gg[8], kk8[8];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) { gg[x] = Gat(m0 + x, i); kk4[x] = kat(m0 + x, i); }
+            for (int x = 0; x < 4; ++x) {
+                gg[x] = Gat(m0 + x, i); kk8[x] = kat(m0 + x, i);
+                gg[4 + x] = Gat(m1 + x, i); kk8[4 + x] = kat(m1 + x, i);
+            }
             *reinterpret_cast<float4*>(Y + Y_KV + op_off(i, m0, C)) =
-                make_float4(ex2f(gg[0]) * kk4[0], ex2f(gg[1]) * kk4[1], ex2f(gg[2]) * kk4[2], ex2f(gg[3]) * kk4[3]);
+                make_float4(ex2f(gg[0]) * kk8[0], ex2f(gg[1]) * kk8[1], ex2f(gg[2]) * kk8[2], ex2f(gg[3]) * kk8[3]);
+            *reinterpret_cast<float4*>(Y + Y_KV + op_off(i, m1, C)) =
+                make_float4(ex2f(gg[4]) * kk8[4], ex2f(gg[5]) * kk8[5], ex2f(gg[6]) * kk8[6], ex2f(gg[7]) * kk8[7]);
         }
         for (int e = tid; e < NV * 16; e += NT) {
             const int j = e & (NV - 1), m0 = 4 * (e >> 5);
@@ -624,26 +645,42 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
             }
             tmem_ld16(tmem + tlane + TM_WU + DK + 16 * half, Ut);
         }
-        for (int e = tid; e < C * 32; e += NT) {            // Gamma . Q  (M=64, K=128)
-            const int r = ((e >> 8) << 3) | (e & 7), q4 = (e >> 3) & 31;
-            const int i0 = 4 * q4;
-            const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(r, i0));
-            const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(r, i0));
-            const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162*>(&qq.x);
-            const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162*>(&qq.y);
-            *reinterpret_cast<float4*>(X + X_QT + op_off(r, i0, DK)) =
-                make_float4(ex2f(gg.x) * __low2float(q01), ex2f(gg.y) * __high2float(q01),
-                            ex2f(gg.z) * __low2float(q23), ex2f(gg.w) * __high2float(q23));
-        }
-        for (int e = tid; e < DK * 16; e += NT) {           // Khat^T  (M=128 rows i, K=64 time)
-            const int i = e & (DK - 1), s0 = 4 * (e >> 7);
-            const float gl = Gat(C - 1, i);
-            float gg[4], kk4[4];
+        for (int e = tid; e < C * 32; e += 2 * NT) {        // Gamma . Q  (M=64, K=128), two items
+            float4 gg[2];
+            uint2 qq[2];
+            int rr[2], ii[2];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) { gg[x] = Gat(s0 + x, i); kk4[x] = kat(s0 + x, i); }
+            for (int u = 0; u < 2; ++u) {
+                const int f = e + u * NT;
+                rr[u] = ((f >> 8) << 3) | (f & 7);
+                ii[u] = 4 * ((f >> 3) & 31);
+                gg[u] = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(rr[u], ii[u]));
+                qq[u] = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(rr[u], ii[u]));
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162*>(&qq[u].x);
+                const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162*>(&qq[u].y);
+                *reinterpret_cast<float4*>(X + X_QT + op_off(rr[u], ii[u], DK)) =
+                    make_float4(ex2f(gg[u].x) * __low2float(q01), ex2f(gg[u].y) * __high2float(q01),
+                                ex2f(gg[u].z) * __low2float(q23), ex2f(gg[u].w) * __high2float(q23));
+            }
+        }
+        for (int e = tid; e < DK * 16; e += 2 * NT) {       // Khat^T  (M=128 rows i, K=64 time), two items
+            const int i = e & (DK - 1), s0 = 4 * (e >> 7), s1 = s0 + 4 * (NT >> 7);
+            const float gl = Gat(C - 1, i);
+            float gg[8], kk8[8];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                gg[x] = Gat(s0 + x, i); kk8[x] = kat(s0 + x, i);
+                gg[4 + x] = Gat(s1 + x, i); kk8[4 + x] = kat(s1 + x, i);
+            }
             *reinterpret_cast<float4*>(Y + Y_KH + op_off(i, s0, C)) =
-                make_float4(ex2f(gl - gg[0]) * kk4[0], ex2f(gl - gg[1]) * kk4[1], ex2f(gl - gg[2]) * kk4[2],
-                            ex2f(gl - gg[3]) * kk4[3]);
+                make_float4(ex2f(gl - gg[0]) * kk8[0], ex2f(gl - gg[1]) * kk8[1], ex2f(gl - gg[2]) * kk8[2],
+                            ex2f(gl - gg[3]) * kk8[3]);
+            *reinterpret_cast<float4*>(Y + Y_KH + op_off(i, s1, C)) =
+                make_float4(ex2f(gl - gg[4]) * kk8[4], ex2f(gl - gg[5]) * kk8[5], ex2f(gl - gg[6]) * kk8[6],
+                            ex2f(gl - gg[7]) * kk8[7]);
         }
         fence_async_smem();
         tc_fence_before();
