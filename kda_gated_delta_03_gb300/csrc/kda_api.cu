@@ -131,7 +131,7 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
         p.order = order;
     }
     if (kda::prefill_tc_supported(p, dt)) {
-        p.slices = kda::prefill_tc_slices(d_v);
+        p.slices = kda::prefill_tc_slices(num_seqs, H, d_v);
         if (kda::launch_prefill_tc(p, s) != cudaSuccess) return KDA_ERR_CUDA;
     } else {
         p.slices = kda::prefill_cc_slices(d_v);
@@ -209,7 +209,7 @@ kda_status kda_prefill_noalloc(const void* q, const void* k, const void* v, cons
         p.order = order;
     }
     if (kda::prefill_tc_supported(p, dt)) {
-        p.slices = kda::prefill_tc_slices(d_v);
+        p.slices = kda::prefill_tc_slices(num_seqs, H, d_v);
         if (kda::launch_prefill_tc(p, s) != cudaSuccess) return KDA_ERR_CUDA;
     } else {
         p.slices = kda::prefill_cc_slices(d_v);

@@ -56,7 +56,7 @@ cudaError_t launch_decode(const DecodeParams& p, kda_dtype dt, cudaStream_t s);
 cudaError_t launch_prefill_cc(const PrefillParams& p, kda_dtype dt, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s);
 bool prefill_tc_supported(const PrefillParams& p, kda_dtype dt);
-int prefill_tc_slices(int dv);
+int prefill_tc_slices(int32_t num_seqs, int32_t H, int32_t dv);
 cudaError_t launch_order(const int32_t* cu_seqlens, int32_t num_seqs, int32_t* order, cudaStream_t s);
 
 // Number of CUDA-core prefill d_v slices for a head size.

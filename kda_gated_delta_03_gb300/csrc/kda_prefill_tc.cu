@@ -40,7 +40,6 @@ namespace {
 
 constexpr int C = 64;
 constexpr int DK = 128;
-constexpr int NV = 32;
 constexpr int NT = 256;
 constexpr long long kWaitLimit = 4000000000LL;   // clock cycles (about 2 s)
 
@@ -48,33 +47,46 @@ constexpr long long kWaitLimit = 4000000000LL;   // clock cycles (about 2 s)
 constexpr int F_LD = 132;                        // floats per A/P factor row
 constexpr int AT_LD = 68;                        // floats per row of the 64x64 solve tiles
 // raw tiles, written by TMA: k, q as two 128B-swizzled boxes of 64 rows x 64 bf16, alpha (then g) as
-// four 128B-swizzled boxes of 64 rows x 32 fp32, the v slice dense (64 rows x 32 bf16)
+// four 128B-swizzled boxes of 64 rows x 32 fp32, then the v slice dense (64 rows x NV bf16)
 constexpr int OFF_K = 0;
 constexpr int OFF_Q = 16384;
 constexpr int OFF_G = 32768;
 constexpr int OFF_V = 65536;
-constexpr int OFF_BETA = 69632;
-constexpr int OFF_X = 70656;                     // region X, 64 KiB
-constexpr int OFF_Y = OFF_X + 65536;             // region Y, 56 KiB
-constexpr int OFF_P = OFF_Y + 57344;             // P operand
-constexpr int OFF_S = OFF_P + 16384;             // S^T operand
-constexpr int OFF_MISC = OFF_S + 16384;
-constexpr uint32_t kChunkTxBytes = 2 * 16384 + 32768 + C * NV * 2;   // bytes the TMA loads of one chunk deliver
-constexpr int SMEM_BYTES = OFF_MISC + 64 + DK * 4;
-// region X: G1 factors -> solve tiles -> W, Gamma.Q operands
+// region X: G1 factors -> solve tiles -> bf16 W and Gamma.Q operands
 constexpr int X_R = 0, X_LK = C * F_LD * 4, X_LQ = X_LK + 16 * F_LD * 4;
 constexpr int X_A = 0, X_T = C * AT_LD * 4, X_SCR = 2 * C * AT_LD * 4;
-constexpr int X_W = 0, X_QT = 32768;
+constexpr int X_W = 0, X_QT = 16384;
+constexpr int X_BYTES = 51200;
 // region Y: T' and [Gamma.K | V]^T operands -> Khat^T and U^T operands
 constexpr int Y_T = 0, Y_KV = 16384;
 constexpr int Y_KH = 0, Y_U = 32768;
 // misc
 constexpr int M_MBAR = 0, M_TMEM = 8, M_ABORT = 12, M_LBAR = 16, M_GAMC = 64;
-// TMEM columns
-constexpr uint32_t TM_WU = 0, TM_X = 160, TM_O = 192, TM_S = 224, TM_COLS = 256;
 
-static_assert(X_LQ + 16 * F_LD * 4 <= 65536 && X_SCR + 3 * 256 * 4 <= 65536, "region X");
-static_assert(SMEM_BYTES <= 232448, "shared memory");
+constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
+
+// Everything that depends on the number NV of value columns a CTA carries (32 or 64).
+template <int NV>
+struct Cfg {
+    static constexpr int CPT = NV / 2;                                   // columns per thread in epilogues
+    static constexpr int OFF_BETA = OFF_V + C * NV * 2;
+    static constexpr int OFF_X = align1k(OFF_BETA + 256);
+    static constexpr int Y_BYTES = (16384 + (DK + NV) * 256) > (32768 + NV * 256) ? (16384 + (DK + NV) * 256)
+                                                                                 : (32768 + NV * 256);
+    static constexpr int OFF_Y = OFF_X + X_BYTES;
+    static constexpr int OFF_P = OFF_Y + Y_BYTES;                        // P operand (TF32, 64 x 64)
+    static constexpr int OFF_S = OFF_P + 16384;                          // S^T operand (bf16, NV x 128)
+    static constexpr int OFF_MISC = OFF_S + NV * DK * 2;
+    static constexpr int SMEM_BYTES = OFF_MISC + 64 + DK * 4;
+    static constexpr uint32_t TX_BYTES = 2 * 16384 + 32768 + C * NV * 2; // bytes one chunk's TMA loads deliver
+    // TMEM columns: [W | Utilde] (M=64), X and O (M=64), the state update (M=128)
+    static constexpr uint32_t TM_WU = 0, TM_X = DK + NV, TM_O = TM_X + NV, TM_S = TM_O + NV;
+    static constexpr uint32_t TM_COLS = (TM_S + NV) <= 256 ? 256 : 512;
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(OFF_V % 1024 == 0 && OFF_X % 1024 == 0, "alignment");
+};
+
+static_assert(X_LQ + 16 * F_LD * 4 <= X_BYTES && X_SCR + 3 * 256 * 4 <= X_BYTES && X_QT + 16384 <= X_BYTES, "region X");
 
 // ---- small PTX helpers ----
 __device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -93,9 +105,22 @@ __device__ __forceinline__ int kq_off(int r, int i) {     // bf16 [64][128] as t
     return ((i >> 6) << 13) + (r << 7) + ((((i & 63) >> 3) ^ (r & 7)) << 4) + ((i & 7) << 1);
 }
 
-__device__ __forceinline__ uint64_t op_desc(uint32_t addr, int K) {
-    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)(128u >> 4) << 16) |
-           ((uint64_t)(((uint32_t)K * 32u >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+// Byte offset of element (row, k) of a K-major bf16 operand with K columns (core matrices of 8 rows x
+// 8 elements; 8-row groups K*16 B apart).
+__device__ __forceinline__ uint32_t op_off_h(int row, int k, int K) {
+    return (uint32_t)((row >> 3) * (K * 16) + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
+}
+
+// Shared-memory matrix descriptor: K-major, no swizzle, K-adjacent core matrices 128 B apart,
+// 8-row groups `sbo` bytes apart.
+__device__ __forceinline__ uint64_t desc_sbo(uint32_t addr, uint32_t sbo) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+           (1ull << 46);
+}
+__device__ __forceinline__ uint64_t op_desc(uint32_t addr, int K) { return desc_sbo(addr, (uint32_t)K * 32u); }
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
@@ -111,6 +136,19 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint32_t a_addr, uint
         asm volatile(
             "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
             "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(acc));
+    }
+}
+
+// D (+)= A B^T with bf16 K-major operands (16 elements per instruction).
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, int K, uint32_t idesc,
+                                          bool accumulate) {
+    for (int ks = 0; ks < K / 16; ++ks) {
+        const uint64_t a = desc_sbo(a_addr + ks * 256, (uint32_t)K * 16u), b = desc_sbo(b_addr + ks * 256, (uint32_t)K * 16u);
+        const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
             "l"(a), "l"(b), "r"(idesc), "r"(acc));
     }
 }
@@ -182,6 +220,21 @@ __device__ __forceinline__ float lg2f(float x) {
     return y;
 }
 
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v) {
+    if constexpr (N == 16) {
+        tmem_ld16(taddr, v);
+    } else {
+        static_assert(N == 32, "16 or 32 columns");
+        tmem_ld32(taddr, v);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -243,10 +296,11 @@ struct Tile {
 // Fetch the raw rows of the chunk starting at token t0: one thread issues the 9 TMA box loads
 // (completing on `lbar`); beta (strided by H) goes through 4-byte cp.async with zero fill.  Rows at
 // or past the sequence end are zeroed by the consumer.
+template <int NV>
 __device__ __forceinline__ void issue_chunk_loads(unsigned char* sm, const TcMaps& m, const Tile& g, int32_t t0,
                                                   int L, int tid, uint32_t lbar) {
     if (tid == 32) {
-        mbar_expect_tx(lbar, kChunkTxBytes);
+        mbar_expect_tx(lbar, Cfg<NV>::TX_BYTES);
         tma_load_3d(saddr(sm + OFF_K), &m.k, 0, g.h, t0, lbar);
         tma_load_3d(saddr(sm + OFF_K + 8192), &m.k, 64, g.h, t0, lbar);
         tma_load_3d(saddr(sm + OFF_Q), &m.q, 0, g.h, t0, lbar);
@@ -258,12 +312,18 @@ __device__ __forceinline__ void issue_chunk_loads(unsigned char* sm, const TcMap
     for (int r = tid; r < C; r += NT) {
         const bool ok = r < L;
         const int64_t row = ok ? ((int64_t)(t0 + r) * g.H + g.h) : 0;
-        cp_async4(saddr(sm + OFF_BETA + r * 4), g.beta + row, ok);
+        cp_async4(saddr(sm + Cfg<NV>::OFF_BETA + r * 4), g.beta + row, ok);
     }
     cp_async_commit();
 }
 
+template <int NV>
 __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, const __grid_constant__ TcMaps maps) {
+    using CF = Cfg<NV>;
+    constexpr int CPT = CF::CPT;
+    constexpr int OFF_BETA = CF::OFF_BETA, OFF_X = CF::OFF_X, OFF_Y = CF::OFF_Y, OFF_P = CF::OFF_P,
+                  OFF_S = CF::OFF_S, OFF_MISC = CF::OFF_MISC;
+    constexpr uint32_t TM_WU = CF::TM_WU, TM_X = CF::TM_X, TM_O = CF::TM_O, TM_S = CF::TM_S, TM_COLS = CF::TM_COLS;
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
@@ -324,12 +384,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 
-    // state: key row srow, value columns 16*half .. 16*half+15 of this slice, float32 in registers
+    // state: key row srow, value columns CPT*half .. CPT*half+CPT-1 of this slice, float32 in registers
     const int srow = 32 * quad + lane;
-    const int64_t state_off = (((int64_t)n * H + h) * DK + srow) * (int64_t)p.dv + j0 + 16 * half;
-    float S[16];
+    const int64_t state_off = (((int64_t)n * H + h) * DK + srow) * (int64_t)p.dv + j0 + CPT * half;
+    float S[CPT];
 #pragma unroll
-    for (int j = 0; j < 16; j += 4) {
+    for (int j = 0; j < CPT; j += 4) {
         float4 v4 = p.state_in ? *reinterpret_cast<const float4*>(p.state_in + state_off + j)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
         S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
@@ -343,14 +403,17 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
     bool aborted = false;
     bool loads_pending = false;
     if (t_begin < t_end) {
-        issue_chunk_loads(sm, maps, g, t_begin, min(C, t_end - t_begin), tid, lbar);
+        issue_chunk_loads<NV>(sm, maps, g, t_begin, min(C, t_end - t_begin), tid, lbar);
         loads_pending = true;
     }
 
-    auto write_state_operand = [&]() {
+    auto write_state_operand = [&]() {           // S^T as a bf16 operand; even lanes store key pairs
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            *reinterpret_cast<float*>(sm + OFF_S + op_off(16 * half + j, srow, DK)) = S[j];
+        for (int j = 0; j < CPT; ++j) {
+            const float partner = __shfl_xor_sync(0xffffffffu, S[j], 1);
+            if (!(lane & 1))
+                *reinterpret_cast<uint32_t*>(sm + OFF_S + op_off_h(CPT * half + j, srow, DK)) = pack_bf16x2(S[j], partner);
+        }
     };
     auto wait_mma = [&]() -> bool {
         if (!mbar_wait(mbar, phase)) {
@@ -386,7 +449,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
                 const int off = ((c >> 3) << 13) + (r << 7) + ((c & 7) << 4);
                 *reinterpret_cast<uint4*>(sm + OFF_K + off) = make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4*>(sm + OFF_Q + off) = make_uint4(0, 0, 0, 0);
-                if (c < 4) *reinterpret_cast<uint4*>(sm + OFF_V + r * NV * 2 + c * 16) = make_uint4(0, 0, 0, 0);
+                if (c < NV / 8) *reinterpret_cast<uint4*>(sm + OFF_V + r * NV * 2 + c * 16) = make_uint4(0, 0, 0, 0);
             }
             __syncthreads();
         }
@@ -611,7 +674,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
                 make_float4(ex2f(gg[4]) * kk8[4], ex2f(gg[5]) * kk8[5], ex2f(gg[6]) * kk8[6], ex2f(gg[7]) * kk8[7]);
         }
         for (int e = tid; e < NV * 16; e += NT) {
-            const int j = e & (NV - 1), m0 = 4 * (e >> 5);
+            const int j = e & (NV - 1), m0 = 4 * (e / NV);
             *reinterpret_cast<float4*>(Y + Y_KV + op_off(DK + j, m0, C)) =
                 make_float4(bf(vraw + (m0 + 0) * NV + j), bf(vraw + (m0 + 1) * NV + j), bf(vraw + (m0 + 2) * NV + j),
                             bf(vraw + (m0 + 3) * NV + j));
@@ -622,13 +685,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
         // ---- 4. [W | Utilde] = T' [Gamma.K | V]  (M=64, N=160, K=64) ----
         if (tid == 0) {
             tc_fence_after();
-            umma_tf32(tmem + TM_WU, saddr(Y + Y_T), saddr(Y + Y_KV), C, idesc_tf32(64, 160), false);
+            umma_tf32(tmem + TM_WU, saddr(Y + Y_T), saddr(Y + Y_KV), C, idesc_tf32(64, DK + NV), false);
             umma_commit(mbar);
         }
         if (!wait_mma()) { aborted = true; break; }
 
         // ---- 5. operands of the state-dependent GEMMs ----
-        float Ut[16];
         const int myrow = 16 * quad + lane;                // M=64 accumulator row of this lane (lane < 16)
         {
             float v[32];
@@ -638,33 +700,24 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
                 tmem_ld32(tmem + tlane + TM_WU + c0, v);
                 if (lane < 16) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 4)
-                        *reinterpret_cast<float4*>(X + X_W + op_off(myrow, c0 + x, DK)) =
-                            make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+                    for (int x = 0; x < 32; x += 8)
+                        *reinterpret_cast<uint4*>(X + X_W + op_off_h(myrow, c0 + x, DK)) =
+                            make_uint4(pack_bf16x2(v[x], v[x + 1]), pack_bf16x2(v[x + 2], v[x + 3]),
+                                       pack_bf16x2(v[x + 4], v[x + 5]), pack_bf16x2(v[x + 6], v[x + 7]));
                 }
             }
-            tmem_ld16(tmem + tlane + TM_WU + DK + 16 * half, Ut);
         }
-        for (int e = tid; e < C * 32; e += 2 * NT) {        // Gamma . Q  (M=64, K=128), two items
-            float4 gg[2];
-            uint2 qq[2];
-            int rr[2], ii[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int f = e + u * NT;
-                rr[u] = ((f >> 8) << 3) | (f & 7);
-                ii[u] = 4 * ((f >> 3) & 31);
-                gg[u] = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(rr[u], ii[u]));
-                qq[u] = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(rr[u], ii[u]));
-            }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162*>(&qq[u].x);
-                const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162*>(&qq[u].y);
-                *reinterpret_cast<float4*>(X + X_QT + op_off(rr[u], ii[u], DK)) =
-                    make_float4(ex2f(gg[u].x) * __low2float(q01), ex2f(gg[u].y) * __high2float(q01),
-                                ex2f(gg[u].z) * __low2float(q23), ex2f(gg[u].w) * __high2float(q23));
-            }
+        for (int e = tid; e < C * 16; e += NT) {            // Gamma . Q as bf16 (M=64, K=128), 8 channels per item
+            const int r = ((e >> 7) << 3) | (e & 7), i0 = 8 * ((e >> 3) & 15);
+            const float4 ga = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(r, i0));
+            const float4 gb = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(r, i0 + 4));
+            const uint4 qq = *reinterpret_cast<const uint4*>(sm + OFF_Q + kq_off(r, i0));
+            const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
+            *reinterpret_cast<uint4*>(X + X_QT + op_off_h(r, i0, DK)) =
+                make_uint4(pack_bf16x2(ex2f(ga.x) * __low2float(q2[0]), ex2f(ga.y) * __high2float(q2[0])),
+                           pack_bf16x2(ex2f(ga.z) * __low2float(q2[1]), ex2f(ga.w) * __high2float(q2[1])),
+                           pack_bf16x2(ex2f(gb.x) * __low2float(q2[2]), ex2f(gb.y) * __high2float(q2[2])),
+                           pack_bf16x2(ex2f(gb.z) * __low2float(q2[3]), ex2f(gb.w) * __high2float(q2[3])));
         }
         for (int e = tid; e < DK * 16; e += 2 * NT) {       // Khat^T  (M=128 rows i, K=64 time), two items
             const int i = e & (DK - 1), s0 = 4 * (e >> 7), s1 = s0 + 4 * (NT >> 7);
@@ -687,27 +740,28 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
         __syncthreads();
         // the raw tiles are free: fetch the next chunk while the state GEMMs run
         if (t0 + C < t_end) {
-            issue_chunk_loads(sm, maps, g, t0 + C, min(C, t_end - t0 - C), tid, lbar);
+            issue_chunk_loads<NV>(sm, maps, g, t0 + C, min(C, t_end - t0 - C), tid, lbar);
             loads_pending = true;
         }
 
         // ---- 6. X = W S, O = (Gamma.Q) S ----
         if (tid == 0) {
             tc_fence_after();
-            umma_tf32(tmem + TM_X, saddr(X + X_W), saddr(sm + OFF_S), DK, idesc_tf32(64, NV), false);
-            umma_tf32(tmem + TM_O, saddr(X + X_QT), saddr(sm + OFF_S), DK, idesc_tf32(64, NV), false);
+            umma_bf16(tmem + TM_X, saddr(X + X_W), saddr(sm + OFF_S), DK, idesc_bf16(64, NV), false);
+            umma_bf16(tmem + TM_O, saddr(X + X_QT), saddr(sm + OFF_S), DK, idesc_bf16(64, NV), false);
             umma_commit(mbar);
         }
         if (!wait_mma()) { aborted = true; break; }
 
         // ---- 7. U = Utilde - X  ->  U^T operand (N=32 rows j, K=64 time) ----
         {
-            float xv[16];
-            tmem_ld16(tmem + tlane + TM_X + 16 * half, xv);
+            float ut[CPT], xv[CPT];
+            tmem_ld<CPT>(tmem + tlane + TM_WU + DK + CPT * half, ut);     // Utilde stays in TMEM until here
+            tmem_ld<CPT>(tmem + tlane + TM_X + CPT * half, xv);
             if (lane < 16) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    *reinterpret_cast<float*>(Y + Y_U + op_off(16 * half + j, myrow, C)) = Ut[j] - xv[j];
+                for (int j = 0; j < CPT; ++j)
+                    *reinterpret_cast<float*>(Y + Y_U + op_off(CPT * half + j, myrow, C)) = ut[j] - xv[j];
             }
         }
         fence_async_smem();
@@ -725,23 +779,23 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
 
         // ---- 9. outputs and the carried state ----
         {
-            float ov[16];
-            tmem_ld16(tmem + tlane + TM_O + 16 * half, ov);
+            float ov[CPT];
+            tmem_ld<CPT>(tmem + tlane + TM_O + CPT * half, ov);
             if (lane < 16 && myrow < L) {
-                __nv_bfloat16* dst = go + ((int64_t)(t0 + myrow) * H + h) * p.dv + j0 + 16 * half;
+                __nv_bfloat16* dst = go + ((int64_t)(t0 + myrow) * H + h) * p.dv + j0 + CPT * half;
 #pragma unroll
-                for (int x = 0; x < 16; x += 8) {
+                for (int x = 0; x < CPT; x += 8) {
                     __align__(16) __nv_bfloat16 pk[8];
 #pragma unroll
                     for (int y = 0; y < 8; ++y) pk[y] = __float2bfloat16_rn(p.scale * ov[x + y]);
                     *reinterpret_cast<uint4*>(dst + x) = *reinterpret_cast<const uint4*>(pk);
                 }
             }
-            float dsv[16];
-            tmem_ld16(tmem + tlane + TM_S + 16 * half, dsv);
+            float dsv[CPT];
+            tmem_ld<CPT>(tmem + tlane + TM_S + CPT * half, dsv);
             const float gamC = sgam[srow];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) S[j] = fmaf(gamC, S[j], dsv[j]);
+            for (int j = 0; j < CPT; ++j) S[j] = fmaf(gamC, S[j], dsv[j]);
             write_state_operand();
         }
         fence_async_smem();
@@ -752,7 +806,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
     // ---- state out, TMEM release ----
     if (!aborted) {
 #pragma unroll
-        for (int j = 0; j < 16; j += 4)
+        for (int j = 0; j < CPT; j += 4)
             *reinterpret_cast<float4*>(p.state_out + state_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
     cp_async_wait_all();
@@ -771,7 +825,10 @@ bool prefill_tc_supported(const PrefillParams& p, kda_dtype dt) {
     return dt == KDA_DTYPE_BF16 && p.dk == DK && p.dv == DK;
 }
 
-int prefill_tc_slices(int dv) { return dv / NV; }
+int prefill_tc_slices(int32_t num_seqs, int32_t H, int32_t dv) {
+    // 64 value columns per CTA when there are enough (sequence, head) units to fill the GPU, otherwise 32
+    return (int64_t)num_seqs * H >= 148 ? dv / 64 : dv / 32;
+}
 
 namespace {
 
@@ -802,7 +859,8 @@ bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, CUtensor
 
 }  // namespace
 
-cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s) {
+template <int NV>
+cudaError_t launch_tc(const PrefillParams& p, cudaStream_t s) {
     TcMaps maps;
     std::memset(&maps, 0, sizeof maps);
     if (p.total_tokens > 0) {                        // with no tokens no CTA loads anything
@@ -819,13 +877,21 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s) {
                          CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    constexpr int SMEM_BYTES = Cfg<NV>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t blocks = (int64_t)p.num_seqs * p.H * p.slices;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 2147483647LL) return cudaErrorInvalidValue;
-    kda_prefill_tc_kernel<<<(unsigned)blocks, NT, SMEM_BYTES, s>>>(p, maps);
+    kda_prefill_tc_kernel<NV><<<(unsigned)blocks, NT, SMEM_BYTES, s>>>(p, maps);
     return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s) {
+    const int nv = p.dv / p.slices;
+    if (nv == 64) return launch_tc<64>(p, s);
+    if (nv == 32) return launch_tc<32>(p, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace kda

@@ -57,6 +57,14 @@ def test_long_carry_slow_decay(dtype):
     check(inp)
 
 
+def test_many_units_wide_slices():
+    """At least 148 (sequence, head) units: the bf16 d=128 path carries 64 value columns per CTA."""
+    rng = np.random.default_rng(77)
+    seqlens = [int(x) for x in rng.integers(1, 200, size=40)]
+    inp = I.prefill_inputs(seqlens, 4, 128, 128, "bf16", 78, decay="slow", state="randn")
+    check(inp)
+
+
 def test_scale_and_zero_state():
     inp = I.prefill_inputs([130, 7], 2, 64, 64, "f32", 8, decay="slow")
     check(inp, scale=0.125)
