@@ -605,48 +605,51 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
             for (int r = 0; r < 16; ++r) Tb[(16 * b + r) * AT_LD + 16 * b + c] = tc[r];
         }
         __syncthreads();
-        // off-diagonal blocks, by distance d = b - c:  Z = sum_{c<=m<b} A_bm T_mc,  T_bc = -T_bb Z
+        // off-diagonal blocks, by distance d = b - c:  Z = sum_{c<=m<b} A_bm T_mc,  T_bc = -T_bb Z.
+        // One warp per (block, 8-column tile), warp-level TF32 MMA; Z is staged per warp to become the
+        // B operand of the second product.
+        {
+            float* zs = scr + warp * 128;
 #pragma unroll
-        for (int d = 1; d < 4; ++d) {
-            const int nblk = 4 - d;
-            for (int e = tid; e < nblk * 256; e += NT) {
-                const int c = e >> 8, row = (e >> 4) & 15, col = e & 15;
-                const float* arow = Ab + (16 * (c + d) + row) * AT_LD + 16 * c;   // A_{b, c..b-1}, 16d entries
-                const float* tcol = Tb + (16 * c) * AT_LD + 16 * c + col;          // T_{c..b-1, c}, column col
-                float tv[48];
+            for (int d = 1; d < 4; ++d) {
+                if (warp < 2 * (4 - d)) {
+                    const int c = warp >> 1, b = c + d, col0 = 16 * c + 8 * (warp & 1);
+                    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 4;
+                    float z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int x = 0; x < 16 * d; ++x) tv[x] = tcol[x * AT_LD];
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int t = 0; t < d; ++t) {
+                        const int m = c + t;
 #pragma unroll
-                for (int x = 0; x < 16 * d; x += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(arow + x);
-                    acc[0] = fmaf(a4.x, tv[x], acc[0]);
-                    acc[1] = fmaf(a4.y, tv[x + 1], acc[1]);
-                    acc[2] = fmaf(a4.z, tv[x + 2], acc[2]);
-                    acc[3] = fmaf(a4.w, tv[x + 3], acc[3]);
+                        for (int ks = 0; ks < 2; ++ks) {
+                            uint32_t a[4];
+                            ldsm_x4(saddr(Ab + (16 * b + arow) * AT_LD + 16 * m + 8 * ks + acol), a);
+                            const uint32_t b0 = __float_as_uint(Tb[(16 * m + 8 * ks + tig) * AT_LD + col0 + gid]);
+                            const uint32_t b1 = __float_as_uint(Tb[(16 * m + 8 * ks + tig + 4) * AT_LD + col0 + gid]);
+                            mma_16x8x8(z, a[0], a[1], a[2], a[3], b0, b1);
+                        }
+                    }
+                    zs[gid * 8 + 2 * tig] = z[0];
+                    zs[gid * 8 + 2 * tig + 1] = z[1];
+                    zs[(gid + 8) * 8 + 2 * tig] = z[2];
+                    zs[(gid + 8) * 8 + 2 * tig + 1] = z[3];
+                    __syncwarp();
+                    float tv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        uint32_t a[4];
+                        ldsm_x4(saddr(Tb + (16 * b + arow) * AT_LD + 16 * b + 8 * ks + acol), a);
+                        const uint32_t b0 = __float_as_uint(zs[(8 * ks + tig) * 8 + gid]);
+                        const uint32_t b1 = __float_as_uint(zs[(8 * ks + tig + 4) * 8 + gid]);
+                        mma_16x8x8(tv, a[0], a[1], a[2], a[3], b0, b1);
+                    }
+                    Tb[(16 * b + gid) * AT_LD + col0 + 2 * tig] = -tv[0];
+                    Tb[(16 * b + gid) * AT_LD + col0 + 2 * tig + 1] = -tv[1];
+                    Tb[(16 * b + gid + 8) * AT_LD + col0 + 2 * tig] = -tv[2];
+                    Tb[(16 * b + gid + 8) * AT_LD + col0 + 2 * tig + 1] = -tv[3];
+                    __syncwarp();
                 }
-                scr[e] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                __syncthreads();
             }
-            __syncthreads();
-            for (int e = tid; e < nblk * 256; e += NT) {
-                const int c = e >> 8, row = (e >> 4) & 15, col = e & 15;
-                const int b = c + d;
-                const float* trow = Tb + (16 * b + row) * AT_LD + 16 * b;
-                float zv[16];
-#pragma unroll
-                for (int x = 0; x < 16; ++x) zv[x] = scr[(c << 8) + (x << 4) + col];
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int x = 0; x < 16; x += 4) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(trow + x);
-                    acc[0] = fmaf(t4.x, zv[x], acc[0]);
-                    acc[1] = fmaf(t4.y, zv[x + 1], acc[1]);
-                    acc[2] = fmaf(t4.z, zv[x + 2], acc[2]);
-                    acc[3] = fmaf(t4.w, zv[x + 3], acc[3]);
-                }
-                Tb[(16 * b + row) * AT_LD + 16 * c + col] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
-            }
-            __syncthreads();
         }
         // T' = T Diag(beta) -> operand (M=64 rows r, K=64 cols m)
         for (int e = tid; e < C * 16; e += NT) {
