@@ -65,19 +65,29 @@ constexpr int M_MBAR = 0, M_TMEM = 8, M_ABORT = 12, M_LBAR = 16, M_GAMC = 64;
 
 constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
 
+// tcgen05 A/P operands (offsets from region X): R_b at the running row offset 16*b*(b+1)/2 rows, each
+// row 512 B of TF32 in K-major canonical layout; [Lk_b; Lq_b] (32 rows) after all R_b.
+__host__ __device__ constexpr int g1_r_off(int b) { return 8192 * (b * (b + 1) / 2); }
+constexpr int G1_L_OFF = 81920;
+constexpr int G1_BYTES = G1_L_OFF + 4 * 16384;
+
 // Everything that depends on the number NV of value columns a CTA carries (32 or 64).
 template <int NV>
 struct Cfg {
     static constexpr int CPT = NV / 2;                                   // columns per thread in epilogues
     static constexpr int OFF_BETA = OFF_V + C * NV * 2;
-    static constexpr int OFF_X = align1k(OFF_BETA + 256);
+    static constexpr int OFF_S = align1k(OFF_BETA + 256);               // S^T operand (bf16, NV x 128)
+    static constexpr int OFF_MISC = OFF_S + NV * DK * 2;
+    static constexpr int OFF_X = align1k(OFF_MISC + 64 + DK * 4);
     static constexpr int Y_BYTES = (16384 + (DK + NV) * 256) > (32768 + NV * 256) ? (16384 + (DK + NV) * 256)
                                                                                  : (32768 + NV * 256);
     static constexpr int OFF_Y = OFF_X + X_BYTES;
     static constexpr int OFF_P = OFF_Y + Y_BYTES;                        // P operand (TF32, 64 x 64)
-    static constexpr int OFF_S = OFF_P + 16384;                          // S^T operand (bf16, NV x 128)
-    static constexpr int OFF_MISC = OFF_S + NV * DK * 2;
-    static constexpr int SMEM_BYTES = OFF_MISC + 64 + DK * 4;
+    // With 32 value columns the A/P products run on tcgen05: their TF32 operands (per row block b,
+    // R_b with 16(b+1) rows and [Lk_b; Lq_b] with 32 rows) span X, Y and P while they are live.
+    static constexpr bool TC_AP = (NV == 32);
+    static constexpr int SMEM_BYTES =
+        (TC_AP && OFF_X + G1_BYTES > OFF_P + 16384) ? OFF_X + G1_BYTES : OFF_P + 16384;
     static constexpr uint32_t TX_BYTES = 2 * 16384 + 32768 + C * NV * 2; // bytes one chunk's TMA loads deliver
     // TMEM columns: [W | Utilde] (M=64), X and O (M=64), the state update (M=128)
     static constexpr uint32_t TM_WU = 0, TM_X = DK + NV, TM_O = TM_X + NV, TM_S = TM_O + NV;
@@ -127,30 +137,39 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D (+)= A B^T with A [M x K] and B [N x K] K-major TF32 operands in shared memory.
-__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, int K, uint32_t idesc,
-                                          bool accumulate) {
-    for (int ks = 0; ks < K / 8; ++ks) {
-        const uint64_t a = op_desc(a_addr + ks * 256, K), b = op_desc(b_addr + ks * 256, K);
-        const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
-        asm volatile(
-            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-            "l"(a), "l"(b), "r"(idesc), "r"(acc));
-    }
+// One tcgen05.mma; the descriptors of successive k-steps differ only in the start-address field, so
+// callers advance them by adding (bytes >> 4).
+__device__ __forceinline__ void umma_tf32_1(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void umma_bf16_1(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
-// D (+)= A B^T with bf16 K-major operands (16 elements per instruction).
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, int K, uint32_t idesc,
+// D (+)= A B^T with A [M x K] and B [N x K] K-major TF32 operands in shared memory (8 elements per step).
+template <int K>
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t idesc,
                                           bool accumulate) {
-    for (int ks = 0; ks < K / 16; ++ks) {
-        const uint64_t a = desc_sbo(a_addr + ks * 256, (uint32_t)K * 16u), b = desc_sbo(b_addr + ks * 256, (uint32_t)K * 16u);
-        const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
-        asm volatile(
-            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-            "l"(a), "l"(b), "r"(idesc), "r"(acc));
-    }
+    const uint64_t a = op_desc(a_addr, K), b = op_desc(b_addr, K);
+#pragma unroll
+    for (int ks = 0; ks < K / 8; ++ks)
+        umma_tf32_1(d_tmem, a + (uint64_t)(ks * 16), b + (uint64_t)(ks * 16), idesc, (accumulate || ks > 0) ? 1u : 0u);
+}
+
+// D (+)= A B^T with bf16 K-major operands (16 elements per step).
+template <int K>
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t idesc,
+                                          bool accumulate) {
+    const uint64_t a = desc_sbo(a_addr, (uint32_t)K * 16u), b = desc_sbo(b_addr, (uint32_t)K * 16u);
+#pragma unroll
+    for (int ks = 0; ks < K / 16; ++ks)
+        umma_bf16_1(d_tmem, a + (uint64_t)(ks * 16), b + (uint64_t)(ks * 16), idesc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t mbar) {
@@ -478,7 +497,99 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
         }
         __syncthreads();
 
-        // ---- 2. A and P by 16-row blocks (warp-level TF32 MMA, two accumulator chains each) ----
+        // ---- 2. A and P by 16-row blocks ----
+        float* Ab = reinterpret_cast<float*>(X + X_A);
+        float* Tb = reinterpret_cast<float*>(X + X_T);
+        float* scr = reinterpret_cast<float*>(X + X_SCR);
+        if constexpr (CF::TC_AP) {
+            // Factors in one pass: thread (channel quad cq, row j within each 8-row group) keeps its rows'
+            // k_s 2^(ref_b - g_s) across blocks (rescaled by 2^(ref_b - ref_{b-1}), never re-exponentiated)
+            // and writes R_b (rows < 16(b+1)) and [Lk_b; Lq_b] as TF32 operands.
+            const int cq = 4 * warp + (lane >> 3), j = lane & 7, i0 = 4 * cq;
+            float4 rv[8];
+            float4 refp = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const float4 ref = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(16 * b + 7, i0));
+                if (b > 0) {
+                    const float4 f = make_float4(ex2f(ref.x - refp.x), ex2f(ref.y - refp.y), ex2f(ref.z - refp.z),
+                                                 ex2f(ref.w - refp.w));
+#pragma unroll
+                    for (int gi = 0; gi < 2 * b; ++gi)
+                        rv[gi] = make_float4(rv[gi].x * f.x, rv[gi].y * f.y, rv[gi].z * f.z, rv[gi].w * f.w);
+                }
+                refp = ref;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {                 // the two new rows of this thread in block b
+                    const int gi = 2 * b + u, fr = 8 * gi + j;
+                    const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(fr, i0));
+                    const uint2 kk = *reinterpret_cast<const uint2*>(sm + OFF_K + kq_off(fr, i0));
+                    const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(fr, i0));
+                    const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kk);
+                    const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
+                    const float kx = __low2float(k2[0]), ky = __high2float(k2[0]), kz = __low2float(k2[1]),
+                                kw = __high2float(k2[1]);
+                    rv[gi] = make_float4(kx * ex2f(ref.x - gg.x), ky * ex2f(ref.y - gg.y), kz * ex2f(ref.z - gg.z),
+                                         kw * ex2f(ref.w - gg.w));
+                    const float fx = ex2f(gg.x - ref.x), fy = ex2f(gg.y - ref.y), fz = ex2f(gg.z - ref.z),
+                                fw = ex2f(gg.w - ref.w);
+                    unsigned char* lb = X + G1_L_OFF + b * 16384;
+                    *reinterpret_cast<float4*>(lb + op_off(8 * u + j, i0, DK)) =
+                        make_float4(tf32r(kx * fx), tf32r(ky * fy), tf32r(kz * fz), tf32r(kw * fw));
+                    *reinterpret_cast<float4*>(lb + op_off(16 + 8 * u + j, i0, DK)) =
+                        make_float4(tf32r(__low2float(q2[0]) * fx), tf32r(__high2float(q2[0]) * fy),
+                                    tf32r(__low2float(q2[1]) * fz), tf32r(__high2float(q2[1]) * fw));
+                }
+                unsigned char* rb = X + g1_r_off(b);
+#pragma unroll
+                for (int gi = 0; gi < 2 * (b + 1); ++gi)
+                    *reinterpret_cast<float4*>(rb + op_off(8 * gi + j, i0, DK)) =
+                        make_float4(tf32r(rv[gi].x), tf32r(rv[gi].y), tf32r(rv[gi].z), tf32r(rv[gi].w));
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            // D_b = R_b [Lk_b; Lq_b]^T (M=64 rows s, N=32, K=128), the four blocks interleaved by k-step
+            if (tid == 0) {
+                tc_fence_after();
+                constexpr uint32_t id = idesc_tf32(64, 32);
+                uint64_t ad[4], bdsc[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    ad[b] = op_desc(saddr(X + g1_r_off(b)), DK);
+                    bdsc[b] = op_desc(saddr(X + G1_L_OFF + b * 16384), DK);
+                }
+#pragma unroll
+                for (int ks = 0; ks < DK / 8; ++ks) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        umma_tf32_1(tmem + TM_WU + 32 * b, ad[b] + (uint64_t)(ks * 16), bdsc[b] + (uint64_t)(ks * 16), id,
+                                    ks > 0 ? 1u : 0u);
+                }
+                umma_commit(mbar);
+            }
+            if (!wait_mma()) { aborted = true; break; }
+            // scatter: A (fp32, for the solve) and P (TF32 operand); lane row s = 16*quad + lane
+            {
+                const int sr = 16 * quad + lane;
+                float v[32];
+#pragma unroll
+                for (int bb = 0; bb < 2; ++bb) {
+                    const int b = 2 * half + bb;
+                    tmem_ld32(tmem + tlane + TM_WU + 32 * b, v);
+                    if (lane < 16) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int r = 16 * b + c;
+                            Ab[r * AT_LD + sr] = sr < r ? sbeta[r] * v[c] : 0.f;
+                            *reinterpret_cast<float*>(opP + op_off(r, sr, C)) = sr <= r ? v[16 + c] : 0.f;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncthreads();
+        } else {
         float* R = reinterpret_cast<float*>(X + X_R);
         float* Lk = reinterpret_cast<float*>(X + X_LK);
         float* Lq = reinterpret_cast<float*>(X + X_LQ);
@@ -560,9 +671,6 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
             __syncthreads();
         }
         // scatter: A (fp32, for the solve) and P (TF32 operand)
-        float* Ab = reinterpret_cast<float*>(X + X_A);
-        float* Tb = reinterpret_cast<float*>(X + X_T);
-        float* scr = reinterpret_cast<float*>(X + X_SCR);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             const int base = b == 0 ? 0 : (b == 1 ? 1 : (b == 2 ? 2 : 4));
@@ -587,6 +695,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
             }
         }
         __syncthreads();
+
+        }
 
         // ---- 3. T = (I + A)^-1 by 16x16 blocks ----
         if (tid < 64) {
@@ -688,7 +798,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
         // ---- 4. [W | Utilde] = T' [Gamma.K | V]  (M=64, N=160, K=64) ----
         if (tid == 0) {
             tc_fence_after();
-            umma_tf32(tmem + TM_WU, saddr(Y + Y_T), saddr(Y + Y_KV), C, idesc_tf32(64, DK + NV), false);
+            umma_tf32<C>(tmem + TM_WU, saddr(Y + Y_T), saddr(Y + Y_KV), idesc_tf32(64, DK + NV), false);
             umma_commit(mbar);
         }
         if (!wait_mma()) { aborted = true; break; }
@@ -750,8 +860,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
         // ---- 6. X = W S, O = (Gamma.Q) S ----
         if (tid == 0) {
             tc_fence_after();
-            umma_bf16(tmem + TM_X, saddr(X + X_W), saddr(sm + OFF_S), DK, idesc_bf16(64, NV), false);
-            umma_bf16(tmem + TM_O, saddr(X + X_QT), saddr(sm + OFF_S), DK, idesc_bf16(64, NV), false);
+            umma_bf16<DK>(tmem + TM_X, saddr(X + X_W), saddr(sm + OFF_S), idesc_bf16(64, NV), false);
+            umma_bf16<DK>(tmem + TM_O, saddr(X + X_QT), saddr(sm + OFF_S), idesc_bf16(64, NV), false);
             umma_commit(mbar);
         }
         if (!wait_mma()) { aborted = true; break; }
@@ -774,8 +884,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
         // ---- 8. O += P U,  D = Khat^T U ----
         if (tid == 0) {
             tc_fence_after();
-            umma_tf32(tmem + TM_O, saddr(opP), saddr(Y + Y_U), C, idesc_tf32(64, NV), true);
-            umma_tf32(tmem + TM_S, saddr(Y + Y_KH), saddr(Y + Y_U), C, idesc_tf32(128, NV), false);
+            umma_tf32<C>(tmem + TM_O, saddr(opP), saddr(Y + Y_U), idesc_tf32(64, NV), true);
+            umma_tf32<C>(tmem + TM_S, saddr(Y + Y_KH), saddr(Y + Y_U), idesc_tf32(128, NV), false);
             umma_commit(mbar);
         }
         if (!wait_mma()) { aborted = true; break; }
