@@ -75,6 +75,12 @@ typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 /*
  * Bytes of device workspace kda_prefill needs for this problem (0 is a valid
  * answer).  Pure host function; never fails (returns 0 for invalid sizes).
+ *  - Several sequences: the longest-first schedule, 4 bytes per sequence.
+ *  - One bf16 sequence with d_k = d_v = 128: the per-chunk records of the
+ *    two-phase path (115,200 bytes per chunk and head, for up to 512 MiB of
+ *    chunks per window).  kda_prefill also accepts less, down to the size
+ *    returned for total_tokens = 64 (one chunk per window); it then walks the
+ *    sequence in more windows, with identical results.
  */
 KDA_API size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                                   int32_t d_v, kda_dtype dt);
@@ -142,8 +148,11 @@ KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, 
  * host program that reaches this library only through the C ABI and has no
  * device allocator of its own.  Arguments, results and errors are those of
  * kda_prefill, except:
- *  - The scratch kda_prefill takes as `workspace` (the longest-first order of
- *    the sequences) lives in a fixed static device array of
+ *  - The one-sequence bf16 d = 128 case runs the single-kernel chunkwise path
+ *    (kda_prefill's two-phase path needs its workspace for per-chunk records);
+ *    results agree with kda_prefill within rounding.
+ *  - The scratch kda_prefill takes as `workspace` for several sequences (their
+ *    longest-first order) lives in a fixed static device array of
  *    KDA_NOALLOC_MAX_SEQS int32 entries (64 KiB), which every GPU that loads
  *    libkda holds until the process exits.  num_seqs > KDA_NOALLOC_MAX_SEQS
  *    returns KDA_ERR_TOO_LARGE before anything is launched.

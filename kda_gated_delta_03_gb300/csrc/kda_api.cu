@@ -79,7 +79,8 @@ const char* kda_status_string(kda_status s) {
 
 size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                                   int32_t d_v, kda_dtype dt) {
-    (void)total_tokens; (void)H; (void)d_k; (void)d_v; (void)dt;
+    if (kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt))
+        return align_up(kda::prefill_2p_workspace(total_tokens, H), 256);   // per-chunk records
     if (num_seqs <= 1) return 0;
     // longest-first schedule of the sequences
     return align_up(sizeof(int32_t) * (size_t)num_seqs, 256);
@@ -106,7 +107,10 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
             !aligned(alpha, 16) || !aligned(beta, 4))
             return KDA_ERR_INVALID_ARG;
     }
-    const size_t need = kda_prefill_workspace_size(num_seqs, total_tokens, H, d_k, d_v, dt);
+    const bool two_phase = kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt);
+    // the two-phase path takes any workspace down to one chunk's records and uses more windows
+    const size_t need = two_phase ? kda::prefill_2p_min_workspace(H)
+                                  : kda_prefill_workspace_size(num_seqs, total_tokens, H, d_k, d_v, dt);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
         return KDA_ERR_WORKSPACE;
 
@@ -125,6 +129,11 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
     p.scale = scale;
     p.state_in = state_in; p.state_out = state_out; p.o = o;
     p.err = err;
+    if (two_phase) {
+        p.slices = 1;
+        if (kda::launch_prefill_2p(p, workspace, workspace_bytes, s) != cudaSuccess) return KDA_ERR_CUDA;
+        return KDA_OK;
+    }
     if (need > 0) {
         int32_t* order = static_cast<int32_t*>(workspace);
         if (kda::launch_order(cu_seqlens, num_seqs, order, s) != cudaSuccess) return KDA_ERR_CUDA;

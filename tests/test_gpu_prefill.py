@@ -89,20 +89,69 @@ def test_worked_overwrite_on_gpu(golden_dir):
     np.testing.assert_allclose(o[1, 0, :4], g["delta_read_after_both_writes"], rtol=0, atol=1e-5)
 
 
-def test_packing_independence():
-    """Each sequence's results do not depend on which other sequences share the batch."""
-    inp = I.prefill_inputs([70, 150, 33], 2, 128, 128, "bf16", 9, decay="slow", state="randn")
+def _sub_batch(inp, seqs):
+    cu = inp["cu_seqlens"]
+    sub = dict(inp)
+    for key in ("q", "k", "v", "beta", "alpha"):
+        sub[key] = np.ascontiguousarray(np.concatenate([inp[key][cu[n]:cu[n + 1]] for n in seqs]))
+    sub["cu_seqlens"] = I.cu_seqlens_of([int(cu[n + 1] - cu[n]) for n in seqs])
+    sub["state_in"] = np.ascontiguousarray(inp["state_in"][list(seqs)])
+    return sub
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_packing_independence(dtype, d):
+    """Each sequence's results do not depend on which other sequences share the batch (or where in it)."""
+    inp = I.prefill_inputs([70, 150, 33], 2, d, d, dtype, 9, decay="slow", state="randn")
     o, st = prefill_gpu(inp)
     cu = inp["cu_seqlens"]
-    for n in range(3):
-        sub = dict(inp)
-        for key in ("q", "k", "v", "beta", "alpha"):
-            sub[key] = np.ascontiguousarray(inp[key][cu[n]:cu[n + 1]])
-        sub["cu_seqlens"] = I.cu_seqlens_of([cu[n + 1] - cu[n]])
-        sub["state_in"] = np.ascontiguousarray(inp["state_in"][n:n + 1])
-        o1, st1 = prefill_gpu(sub)
-        assert np.array_equal(o1, o[cu[n]:cu[n + 1]])
-        assert np.array_equal(st1[0], st[n])
+    for pair in ((1, 0), (2, 1), (0, 2)):
+        o1, st1 = prefill_gpu(_sub_batch(inp, pair))
+        c1 = cu[pair[0] + 1] - cu[pair[0]]
+        for part, n in ((slice(0, c1), pair[0]), (slice(c1, None), pair[1])):
+            assert np.array_equal(o1[part], o[cu[n]:cu[n + 1]])
+        assert np.array_equal(st1, st[list(pair)])
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 700])
+@pytest.mark.parametrize("decay", ["config", "slow", "one", "scalar"])
+def test_single_sequence_two_phase(T, decay):
+    """One bf16 d=128 sequence takes the two-phase path (per-chunk records, then the state chain)."""
+    inp = I.prefill_inputs([T], 3, 128, 128, "bf16", 300 + T, decay=decay, state="randn")
+    check(inp)
+
+
+def test_two_phase_windows_give_identical_results():
+    """A workspace smaller than the recommended size walks the sequence in more windows of chunks, the
+    state passing between windows through state_out; the results are bit-identical, in place too."""
+    import kda_gated_delta_03_gb300 as kda
+    inp = I.prefill_inputs([1000], 2, 128, 128, "bf16", 15, decay="slow", state="randn")
+    args = [to_dev(inp[n], n in ("q", "k", "v")) for n in ("q", "k", "v", "beta", "alpha", "cu_seqlens")]
+    s0 = to_dev(inp["state_in"])
+    rec = 2 * 115200                                          # one chunk of records for H = 2
+    assert kda.kda_prefill_workspace_size(1, 1000, 2, 128, 128, torch.bfloat16) == 16 * rec
+    runs = []
+    for chunks in (16, 5, 1):
+        ws = torch.empty(chunks * rec, dtype=torch.uint8, device="cuda:0")
+        runs.append(kda.kda_prefill(*args, s0, workspace=ws))
+    st = s0.clone()
+    ws = torch.empty(3 * rec, dtype=torch.uint8, device="cuda:0")
+    o_ip, _ = kda.kda_prefill(*args, st, state_out=st, workspace=ws)
+    torch.cuda.synchronize()
+    for o, s in runs[1:] + [(o_ip, st)]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(s, runs[0][1])
+    o_ref, s_ref = O.prefill(inp)
+    assert rel_frob(runs[0][0].double().cpu().numpy(), o_ref) <= 3e-3
+    assert rel_frob(runs[0][1].double().cpu().numpy(), s_ref) <= 3e-3
+
+
+def test_two_phase_bad_cu_seqlens_is_reported():
+    import kda_gated_delta_03_gb300 as kda
+    inp = I.prefill_inputs([100], 2, 128, 128, "bf16", 16)
+    inp["cu_seqlens"] = np.array([0, 90], np.int32)
+    prefill_gpu(inp)
+    assert kda.kda_get_device_error() & 0x1
+    assert kda.kda_get_device_error() == 0
 
 
 def test_append_equals_one_shot():
