@@ -77,7 +77,7 @@ typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
  * answer).  Pure host function; never fails (returns 0 for invalid sizes).
  *  - Several sequences: the longest-first schedule, 4 bytes per sequence.
  *  - One bf16 sequence with d_k = d_v = 128: the per-chunk records of the
- *    two-phase path (115,200 bytes per chunk and head, for up to 512 MiB of
+ *    two-phase path (197,120 bytes per chunk and head, for up to 512 MiB of
  *    chunks per window).  kda_prefill also accepts less, down to the size
  *    returned for total_tokens = 64 (one chunk per window); it then walks the
  *    sequence in more windows, with identical results.

@@ -1,17 +1,23 @@
 // Two-phase chunkwise prefill for a single long sequence: bf16 q/k/v, d_k = d_v = 128.
 //
-// The chunk algebra is the fused kernel's ("Kimi K3, explained", section "Training in chunks": WY form
-// inside a chunk, only the state carried across chunks).  Everything of a chunk that does not depend
-// on the state -- g, the decayed A and P blocks, T' = (I + A)^-1 Diag(beta), [W | Utilde], Gamma . Q,
-// Khat and Gamma_C -- is computed once per (head, chunk) by phase 1, in parallel over every chunk of a
-// window and every head, and stored as a record in the workspace in the exact byte layout of the
-// shared-memory operands.  Phase 2 walks the window's chunks in order, one CTA per (head, 32 value
-// columns), bulk-loading each record one chunk ahead and running only the state recurrence:
+// The chunk algebra is that of the single-kernel path ("Kimi K3, explained", section "Training in
+// chunks": WY form inside a chunk, only the state carried across chunks).  With U = Utilde - W S the
+// chunk's output and state update are affine in the chunk-start state S:
 //
-//   X = W S,  O = (Gamma . Q) S          tcgen05 kind::f16 (bf16 operands), M=64 N=32 K=128
-//   U = Utilde - X                       CUDA cores
-//   O += P U,  dS = Khat^T U             tcgen05 kind::tf32, M=64 / M=128, N=32, K=64
-//   S <- Diag(Gamma_C) S + dS,  o = scale O
+//   O     = (Gamma.Q) S + P U            = Q' S + P Utilde,         Q' = Gamma.Q - P W
+//   S_new = Diag(Gamma_C) S + Khat^T U   = Diag(Gamma_C) S + B - M S,  M = Khat^T W,  B = Khat^T Utilde
+//
+// Phase 1 computes, for every (head, chunk) of a window in parallel, everything that does not depend
+// on S -- g, A and P, T' = (I + A)^-1 Diag(beta), [W | Utilde], and from them Q', M, B and P Utilde --
+// and stores it as a record in the workspace, Q' and M already in the byte layout of a tensor-core
+// operand.  Phase 2 walks the chunks in order, one CTA per (head, 32 value columns), bulk-loading each
+// record one chunk ahead; per chunk it issues a single batch of tensor-core products,
+//
+//   [Q'; M_top] S  and  M S              tcgen05 kind::tf32, M=128, N=32, K=128
+//
+// followed by the fp32 update S <- Gamma_C . S + B - M S and o = scale (Q' S + P Utilde).  Folding W
+// into M and Q' doubles phase 1's work on W but leaves one round trip through the tensor core on the
+// sequential path instead of two, and no U tile to build between them.
 //
 // Long sequences are processed in windows of chunks so that the workspace stays bounded; the state
 // passes between windows through state_out.  Every wait is bounded (KDA_DEVERR_TIMEOUT on expiry).
@@ -22,15 +28,16 @@ namespace kda {
 namespace {
 
 // ---- one (head, chunk) record in the workspace ----
-constexpr int REC_WQ = 0;          // [W ; Gamma.Q]: two 64 x 128 bf16 K-major operands (32 KiB)
-constexpr int REC_KH = 32768;      // Khat^T: 128 x 64 TF32 K-major operand (32 KiB)
-constexpr int REC_P = 65536;       // P: 64 x 64 TF32 K-major operand (16 KiB)
-constexpr int REC_U = 81920;       // Utilde: fp32 [4 slices][64 rows][32 columns] (32 KiB)
-constexpr int REC_G = 114688;      // Gamma_C: fp32 [128]
-constexpr int REC_BYTES = 115200;
+constexpr int REC_QM = 0;          // [Q'; M]: 192 x 128 TF32 K-major operand (96 KiB)
+constexpr int REC_B = 98304;       // B = Khat^T Utilde: fp32 [32 column quads][128 rows][4] (64 KiB)
+constexpr int REC_O = 163840;      // P Utilde: fp32 [32 column quads][64 rows][4] (32 KiB)
+constexpr int REC_G = 196608;      // Gamma_C: fp32 [128]
+constexpr int REC_BYTES = 197120;
+constexpr int QM_BYTES = (C + DK) * DK * 4;
 constexpr int SNV = 32;            // value columns per chain CTA
 constexpr int SLICES = DK / SNV;
 constexpr size_t kWindowBudget = size_t(512) << 20;   // workspace bytes the records of one window may use
+static_assert(QM_BYTES == REC_B && REC_B + DK * DK * 4 == REC_O && REC_O + C * DK * 4 == REC_G, "record layout");
 
 // ---- phase 1 shared memory ----
 constexpr int P_OFF_V = OFF_V;                     // v tile, dense 64 x 128 bf16
@@ -40,30 +47,23 @@ constexpr int P_OFF_S = align1k(P_OFF_MISC + 64 + DK * 4);   // scratch, 144 KiB
 // scratch sub-regions (offsets from P_OFF_S)
 constexpr int PS_A = 0, PS_T = C * AT_LD * 4, PS_SCR = 2 * C * AT_LD * 4;   // solve tiles
 constexpr int PS_OPT = 38912, PS_KV = PS_OPT + 16384;                     // T' and [Gamma.K | V]^T (N = 256)
-constexpr int PS_P = 122880;                                               // P operand staging
-constexpr int PS_WQ = 0, PS_KH = 32768, PS_U = 65536, PS_G = 98304;       // record staging after [W | Utilde]
+constexpr int PS_P = 122880;                                               // P operand
+constexpr int PS_WU = 0, PS_KH = 65536;                                    // fold operands, after [W | Utilde]
 constexpr int P_SMEM = P_OFF_S + G1_BYTES;
 static_assert(PS_KV + (DK + DK) * 256 <= PS_P && PS_P + 16384 <= G1_BYTES, "phase-1 scratch");
+static_assert(PS_KH + DK * C * 4 <= PS_P, "phase-1 fold operands");
 static_assert(P_SMEM <= 232448, "phase-1 shared memory");
 
 // ---- phase 2 shared memory ----
-constexpr int BUF_BYTES = 90624;                   // WQ + KH (64 KiB) | P (16 KiB) | Utilde slice (8 KiB) | Gamma_C
-constexpr int B_P = 65536, B_U = 81920, B_G = 90112;
-constexpr uint32_t BUF_TX = 65536 + 16384 + 8192 + 512;
-constexpr int C_OFF_S = 2 * BUF_BYTES;             // S^T operand, bf16 32 x 128
-constexpr int C_OFF_U = C_OFF_S + SNV * DK * 2;    // U^T operand, TF32 32 x 64
-constexpr int C_OFF_MISC = C_OFF_U + SNV * C * 4;
+constexpr int C_OFF_S = 2 * QM_BYTES;              // S^T operand: TF32 32 x 128, 128-byte swizzle
+constexpr int C_OFF_MISC = C_OFF_S + SNV * DK * 4;
 constexpr int C_SMEM = C_OFF_MISC + 64;
-static_assert(C_SMEM <= 232448, "phase-2 shared memory");
+static_assert(C_OFF_S % 1024 == 0 && C_SMEM <= 232448, "phase-2 shared memory");
 
 struct PrepMaps {
     CUtensorMap k, q, a, v;   // v with a 128-column box
 };
 
-__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
-}
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(mbar)
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(NT, 1)
         *s_abort = 0;
     }
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(s_tmem)), "r"(256)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(s_tmem)), "r"(512)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(NT, 1)
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (warp == 0 && elect_one()) {
             tc_fence_after();
             constexpr uint32_t id = idesc_tf32(64, 32);
             uint64_t ad[4], bdsc[4];
@@ -371,74 +371,115 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
 
         // ---- 4. [W | Utilde] = T' [Gamma.K | V]  (M=64, N=256, K=64) ----
-        if (tid == 0) {
+        if (warp == 0 && elect_one()) {
             tc_fence_after();
             umma_tf32<C>(tmem, saddr(X + PS_OPT), saddr(X + PS_KV), idesc_tf32(64, 2 * DK), false);
             umma_commit(mbar);
         }
         if (!wait_mma()) { ok = false; break; }
 
-        // ---- 5. the record: W and Gamma.Q (bf16), Khat^T (TF32), Utilde (fp32, by slice), Gamma_C ----
-        const int myrow = 16 * quad + lane;
+        // ---- 5. fold operands: [W | Utilde]^T (N=256, K=64, 128-byte swizzle) and Khat^T (M=128, K=64) ----
+        unsigned char* opWU = X + PS_WU;
+        unsigned char* opKH = X + PS_KH;
         {
+            const int sr = 16 * quad + lane;                     // time row of this lane (lanes < 16)
             float v[32];
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {                     // W: this half's 64 columns
-                const int c0 = 64 * half + 32 * cb;
+            for (int cb = 0; cb < 4; ++cb) {
+                const int c0 = 128 * half + 32 * cb;
                 tmem_ld32(tmem + tlane + c0, v);
                 if (lane < 16) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 8)
-                        *reinterpret_cast<uint4*>(X + PS_WQ + op_off_h(myrow, c0 + x, DK)) =
-                            make_uint4(pack_bf16x2(v[x], v[x + 1]), pack_bf16x2(v[x + 2], v[x + 3]),
-                                       pack_bf16x2(v[x + 4], v[x + 5]), pack_bf16x2(v[x + 6], v[x + 7]));
-                }
-            }
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {                     // Utilde: value columns 64*half .. +63
-                const int c0 = 64 * half + 32 * cb;              // = slice 2*half + cb
-                tmem_ld32(tmem + tlane + DK + c0, v);
-                if (lane < 16) {
-                    float* dst = reinterpret_cast<float*>(X + PS_U) + ((c0 >> 5) * C + myrow) * SNV;
-#pragma unroll
-                    for (int x = 0; x < 32; x += 4)
-                        *reinterpret_cast<float4*>(dst + x) = make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+                    for (int x = 0; x < 32; ++x)
+                        *reinterpret_cast<float*>(opWU + sw128_off(c0 + x, sr, 2 * DK)) = tf32r(v[x]);
                 }
             }
         }
-        for (int e = tid; e < C * 16; e += NT) {                  // Gamma . Q as bf16 (rows 64..127 of [W; Q])
-            const int r = ((e >> 7) << 3) | (e & 7), i0 = 8 * ((e >> 3) & 15);
-            const float4 ga = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(r, i0));
-            const float4 gb = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(r, i0 + 4));
-            const uint4 qq = *reinterpret_cast<const uint4*>(sm + OFF_Q + kq_off(r, i0));
-            const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
-            *reinterpret_cast<uint4*>(X + PS_WQ + 16384 + op_off_h(r, i0, DK)) =
-                make_uint4(pack_bf16x2(ex2f(ga.x) * __low2float(q2[0]), ex2f(ga.y) * __high2float(q2[0])),
-                           pack_bf16x2(ex2f(ga.z) * __low2float(q2[1]), ex2f(ga.w) * __high2float(q2[1])),
-                           pack_bf16x2(ex2f(gb.x) * __low2float(q2[2]), ex2f(gb.y) * __high2float(q2[2])),
-                           pack_bf16x2(ex2f(gb.z) * __low2float(q2[3]), ex2f(gb.w) * __high2float(q2[3])));
-        }
-        for (int e = tid; e < DK * 16; e += NT) {                 // Khat^T (M=128 rows i, K=64 time)
+        for (int e = tid; e < DK * 16; e += NT) {
             const int i = e & (DK - 1), s0 = 4 * (e >> 7);
             const float gl = Gat(C - 1, i);
             float gg[4], kk4[4];
 #pragma unroll
             for (int x = 0; x < 4; ++x) { gg[x] = Gat(s0 + x, i); kk4[x] = kat(s0 + x, i); }
-            *reinterpret_cast<float4*>(X + PS_KH + op_off(i, s0, C)) =
-                make_float4(ex2f(gl - gg[0]) * kk4[0], ex2f(gl - gg[1]) * kk4[1], ex2f(gl - gg[2]) * kk4[2],
-                            ex2f(gl - gg[3]) * kk4[3]);
+            *reinterpret_cast<float4*>(opKH + op_off(i, s0, C)) =
+                make_float4(tf32r(ex2f(gl - gg[0]) * kk4[0]), tf32r(ex2f(gl - gg[1]) * kk4[1]),
+                            tf32r(ex2f(gl - gg[2]) * kk4[2]), tf32r(ex2f(gl - gg[3]) * kk4[3]));
         }
-        if (tid < DK) reinterpret_cast<float*>(X + PS_G)[tid] = sgam[tid];
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
-            bulk_s2g(rec + REC_WQ, saddr(X + PS_WQ), 65536);      // [W; Gamma.Q] and Khat^T are adjacent
-            bulk_s2g(rec + REC_P, saddr(opP), 16384);
-            bulk_s2g(rec + REC_U, saddr(X + PS_U), 32768);
-            bulk_s2g(rec + REC_G, saddr(X + PS_G), 512);
-            asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
-            asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+
+        // ---- 6. [M | B] = Khat^T [W | Utilde] (M=128) and [PW | P Utilde] = P [W | Utilde] (M=64); N=256, K=64 ----
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                const uint64_t ak = op_desc(saddr(opKH), C), ap = op_desc(saddr(opP), C);
+                const uint32_t wb = saddr(opWU);
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks) {
+                    const uint64_t bd = desc_sw128(wb + (ks >> 2) * (2 * DK * 128) + (ks & 3) * 32);
+                    umma_tf32_1(tmem, ak + (uint64_t)(ks * 16), bd, idesc_tf32(128, 2 * DK), ks > 0 ? 1u : 0u);
+                    umma_tf32_1(tmem + 2 * DK, ap + (uint64_t)(ks * 16), bd, idesc_tf32(64, 2 * DK), ks > 0 ? 1u : 0u);
+                }
+                umma_commit(mbar);
+            }
+            __syncwarp();
+        }
+        if (!wait_mma()) { ok = false; break; }
+
+        // ---- 7. the record, from TMEM straight to global memory ----
+        {
+            const int i = 32 * quad + lane;                      // M=128 accumulator row
+            const int r = 16 * quad + lane;                      // M=64 accumulator row (lanes < 16)
+            float v[32];
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {                     // M = Khat^T W -> rows 64.. of [Q'; M]
+                const int c0 = 64 * half + 32 * cb;
+                tmem_ld32(tmem + tlane + c0, v);
+#pragma unroll
+                for (int x = 0; x < 32; x += 4)
+                    *reinterpret_cast<float4*>(rec + REC_QM + op_off(C + i, c0 + x, DK)) =
+                        make_float4(tf32r(v[x]), tf32r(v[x + 1]), tf32r(v[x + 2]), tf32r(v[x + 3]));
+            }
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {                     // B = Khat^T Utilde
+                const int c0 = 64 * half + 32 * cb;
+                tmem_ld32(tmem + tlane + DK + c0, v);
+#pragma unroll
+                for (int x = 0; x < 32; x += 4)
+                    *reinterpret_cast<float4*>(rec + REC_B + (((c0 + x) >> 2) * DK + i) * 16) =
+                        make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+            }
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {                     // Q' = Gamma.Q - P W -> rows 0..63 of [Q'; M]
+                const int c0 = 64 * half + 32 * cb;
+                tmem_ld32(tmem + tlane + 2 * DK + c0, v);
+                if (lane < 16) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 4) {
+                        const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(r, c0 + x));
+                        const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(r, c0 + x));
+                        const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
+                        *reinterpret_cast<float4*>(rec + REC_QM + op_off(r, c0 + x, DK)) =
+                            make_float4(tf32r(ex2f(gg.x) * __low2float(q2[0]) - v[x]),
+                                        tf32r(ex2f(gg.y) * __high2float(q2[0]) - v[x + 1]),
+                                        tf32r(ex2f(gg.z) * __low2float(q2[1]) - v[x + 2]),
+                                        tf32r(ex2f(gg.w) * __high2float(q2[1]) - v[x + 3]));
+                    }
+                }
+            }
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {                     // P Utilde
+                const int c0 = 64 * half + 32 * cb;
+                tmem_ld32(tmem + tlane + 3 * DK + c0, v);
+                if (lane < 16) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 4)
+                        *reinterpret_cast<float4*>(rec + REC_O + (((c0 + x) >> 2) * C + r) * 16) =
+                            make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+                }
+            }
+            if (tid < DK) reinterpret_cast<float*>(rec + REC_G)[tid] = sgam[tid];
         }
     } while (false);
 
@@ -446,7 +487,7 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
     }
 }
 
@@ -459,11 +500,15 @@ __global__ void __launch_bounds__(NT, 1)
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2;
-    constexpr int CPT = SNV / 2;
+    constexpr int CPT = SNV / 2;                      // value columns per thread
     const int H = p.H;
     const int h = blockIdx.x / SLICES, slice = blockIdx.x % SLICES, j0 = slice * SNV;
     if (!valid_single_sequence(p)) {
         if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
+        return;
+    }
+    if (saddr(sm) & 1023u) {
+        if (tid == 0) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
         return;
     }
     const int32_t T = p.total_tokens;
@@ -472,7 +517,8 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + C_OFF_MISC + 8);
     const uint32_t mbar = saddr(sm + C_OFF_MISC);
     const uint32_t lbar0 = saddr(sm + C_OFF_MISC + 16), lbar1 = saddr(sm + C_OFF_MISC + 24);
-    constexpr uint32_t TM_X = 0, TM_O = 32, TM_S = 64;
+    unsigned char* sop = sm + C_OFF_S;
+    constexpr uint32_t TM_O = 0, TM_S = 32;           // [Q'; M_top] S and M S accumulators
 
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar) : "memory");
@@ -482,12 +528,13 @@ __global__ void __launch_bounds__(NT, 1)
         *s_abort = 0;
     }
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(s_tmem)), "r"(128)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(s_tmem)), "r"(64)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    const int srow = 32 * quad + lane;
-    const int64_t state_off = (((int64_t)h) * DK + srow) * (int64_t)p.dv + j0 + CPT * half;
+    const int srow = 32 * quad + lane;                // state row (key channel) of this thread
+    const int jc = j0 + CPT * half;                   // first value column of this thread
+    const int64_t state_off = (((int64_t)h) * DK + srow) * (int64_t)p.dv + jc;
     float S[CPT];
 #pragma unroll
     for (int j = 0; j < CPT; j += 4) {
@@ -504,39 +551,20 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t pend = 0;
     bool aborted = false;
 
-    auto issue = [&](int ci) {                        // bulk-load the record of chunk ci into buffer ci & 1
+    auto issue = [&](int ci) {                        // bulk-load [Q'; M] of chunk ci into buffer ci & 1
         if (tid == 32) {
             const int b = ci & 1;
             const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
-            unsigned char* buf = sm + b * BUF_BYTES;
             const uint32_t lb = b ? lbar1 : lbar0;
-            mbar_expect_tx(lb, BUF_TX);
-            bulk_g2s(saddr(buf), rec + REC_WQ, 65536, lb);
-            bulk_g2s(saddr(buf + B_P), rec + REC_P, 16384, lb);
-            bulk_g2s(saddr(buf + B_U), rec + REC_U + slice * (C * SNV * 4), C * SNV * 4, lb);
-            bulk_g2s(saddr(buf + B_G), rec + REC_G, 512, lb);
+            mbar_expect_tx(lb, QM_BYTES);
+            bulk_g2s(saddr(sm + b * QM_BYTES), rec + REC_QM, QM_BYTES, lb);
         }
         pend |= 1u << (ci & 1);
     };
-    auto write_state_operand = [&]() {
+    auto write_state_operand = [&]() {                // S^T as a TF32 operand: row = value column, K = srow
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-            const float partner = __shfl_xor_sync(0xffffffffu, S[j], 1);
-            if (!(lane & 1))
-                *reinterpret_cast<uint32_t*>(sm + C_OFF_S + op_off_h(CPT * half + j, srow, DK)) =
-                    pack_bf16x2(S[j], partner);
-        }
-    };
-    auto wait_mma = [&]() -> bool {
-        if (!mbar_wait(mbar, phase)) {
-            atomicOr(p.err, KDA_DEVERR_TIMEOUT);
-            *s_abort = 1;
-        }
-        phase ^= 1u;
-        __syncthreads();
-        if (*s_abort) return false;
-        tc_fence_after();
-        return true;
+        for (int j = 0; j < CPT; ++j)
+            *reinterpret_cast<float*>(sop + sw128_off(CPT * half + j, srow, SNV)) = tf32r(S[j]);
     };
     write_state_operand();
     if (n_chunks > 0) issue(0);
@@ -546,7 +574,8 @@ __global__ void __launch_bounds__(NT, 1)
 
     for (int ci = 0; ci < n_chunks && !aborted; ++ci) {
         const int b = ci & 1;
-        unsigned char* buf = sm + b * BUF_BYTES;
+        const uint32_t abuf = saddr(sm + b * QM_BYTES);
+        const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
         const int32_t t0 = (c_begin + ci) * C;
         const int L = min(C, T - t0);
         if (!mbar_wait(b ? lbar1 : lbar0, (lph >> b) & 1u)) {
@@ -558,57 +587,68 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         if (*s_abort) { aborted = true; break; }
 
-        // X = W S, O = (Gamma.Q) S  (bf16)
-        if (tid == 0) {
-            tc_fence_after();
-            umma_bf16<DK>(tmem + TM_X, saddr(buf), saddr(sm + C_OFF_S), idesc_bf16(64, SNV), false);
-            umma_bf16<DK>(tmem + TM_O, saddr(buf + 16384), saddr(sm + C_OFF_S), idesc_bf16(64, SNV), false);
-            umma_commit(mbar);
-        }
-        if (!wait_mma()) { aborted = true; break; }
-        // U = Utilde - X -> U^T operand
-        const int myrow = 16 * quad + lane;
-        {
-            float xv[CPT];
-            tmem_ld<CPT>(tmem + tlane + TM_X + CPT * half, xv);
-            if (lane < 16) {
-                const float* ut = reinterpret_cast<const float*>(buf + B_U) + myrow * SNV + CPT * half;
+        // [Q'; M_top] S and M S: 2 x 16 TF32 steps, one commit
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                constexpr uint32_t id = idesc_tf32(128, SNV);
+                const uint64_t a_o = op_desc(abuf, DK), a_s = op_desc(abuf + C * DK * 4, DK);
+                const uint32_t sb = saddr(sop);
 #pragma unroll
-                for (int j = 0; j < CPT; ++j)
-                    *reinterpret_cast<float*>(sm + C_OFF_U + op_off(CPT * half + j, myrow, C)) = ut[j] - xv[j];
+                for (int ks = 0; ks < DK / 8; ++ks) {
+                    const uint64_t bd = desc_sw128(sb + (ks >> 2) * (SNV * 128) + (ks & 3) * 32);
+                    umma_tf32_1(tmem + TM_O, a_o + (uint64_t)(ks * 16), bd, id, ks > 0 ? 1u : 0u);
+                    umma_tf32_1(tmem + TM_S, a_s + (uint64_t)(ks * 16), bd, id, ks > 0 ? 1u : 0u);
+                }
+                umma_commit(mbar);
             }
+            __syncwarp();
         }
-        fence_async_smem();
-        tc_fence_before();
+        // the chunk's B, P Utilde and Gamma_C, loaded while the products run
+        float4 bq[CPT / 4], oq[CPT / 4];
+#pragma unroll
+        for (int m = 0; m < CPT / 4; ++m)
+            bq[m] = __ldg(reinterpret_cast<const float4*>(rec + REC_B + (((jc + 4 * m) >> 2) * DK + srow) * 16));
+        if (quad < 2) {
+#pragma unroll
+            for (int m = 0; m < CPT / 4; ++m)
+                oq[m] = __ldg(reinterpret_cast<const float4*>(rec + REC_O + (((jc + 4 * m) >> 2) * C + srow) * 16));
+        }
+        const float gamC = __ldg(reinterpret_cast<const float*>(rec + REC_G) + srow);
+        if (!mbar_wait(mbar, phase)) {
+            atomicOr(p.err, KDA_DEVERR_TIMEOUT);
+            *s_abort = 1;
+        }
+        phase ^= 1u;
         __syncthreads();
-        // O += P U, dS = Khat^T U  (TF32)
-        if (tid == 0) {
-            tc_fence_after();
-            umma_tf32<C>(tmem + TM_O, saddr(buf + B_P), saddr(sm + C_OFF_U), idesc_tf32(64, SNV), true);
-            umma_tf32<C>(tmem + TM_S, saddr(buf + 32768), saddr(sm + C_OFF_U), idesc_tf32(128, SNV), false);
-            umma_commit(mbar);
-        }
-        if (!wait_mma()) { aborted = true; break; }
-        // outputs and the carried state
+        if (*s_abort) { aborted = true; break; }
+        tc_fence_after();
         {
-            float ov[CPT];
-            tmem_ld<CPT>(tmem + tlane + TM_O + CPT * half, ov);
-            if (lane < 16 && myrow < L) {
-                __nv_bfloat16* dst = go + ((int64_t)(t0 + myrow) * H + h) * p.dv + j0 + CPT * half;
+            float d[CPT];
+            tmem_ld16(tmem + tlane + TM_S + CPT * half, d);
 #pragma unroll
-                for (int x = 0; x < CPT; x += 8) {
-                    __align__(16) __nv_bfloat16 pk[8];
+            for (int m = 0; m < CPT / 4; ++m) {
+                S[4 * m + 0] = fmaf(gamC, S[4 * m + 0], bq[m].x - d[4 * m + 0]);
+                S[4 * m + 1] = fmaf(gamC, S[4 * m + 1], bq[m].y - d[4 * m + 1]);
+                S[4 * m + 2] = fmaf(gamC, S[4 * m + 2], bq[m].z - d[4 * m + 2]);
+                S[4 * m + 3] = fmaf(gamC, S[4 * m + 3], bq[m].w - d[4 * m + 3]);
+            }
+            write_state_operand();
+            if (quad < 2) {                           // output rows 0..63 live in lanes 0..63
+                tmem_ld16(tmem + tlane + TM_O + CPT * half, d);
+                if (srow < L) {
+                    __nv_bfloat16* dst = go + ((int64_t)(t0 + srow) * H + h) * p.dv + jc;
 #pragma unroll
-                    for (int y = 0; y < 8; ++y) pk[y] = __float2bfloat16_rn(p.scale * ov[x + y]);
-                    *reinterpret_cast<uint4*>(dst + x) = *reinterpret_cast<const uint4*>(pk);
+                    for (int x = 0; x < CPT; x += 8) {
+                        const float4 o0 = oq[x / 4], o1 = oq[x / 4 + 1];
+                        *reinterpret_cast<uint4*>(dst + x) =
+                            make_uint4(pack_bf16x2(p.scale * (d[x] + o0.x), p.scale * (d[x + 1] + o0.y)),
+                                       pack_bf16x2(p.scale * (d[x + 2] + o0.z), p.scale * (d[x + 3] + o0.w)),
+                                       pack_bf16x2(p.scale * (d[x + 4] + o1.x), p.scale * (d[x + 5] + o1.y)),
+                                       pack_bf16x2(p.scale * (d[x + 6] + o1.z), p.scale * (d[x + 7] + o1.w)));
+                    }
                 }
             }
-            float dsv[CPT];
-            tmem_ld<CPT>(tmem + tlane + TM_S + CPT * half, dsv);
-            const float gamC = reinterpret_cast<const float*>(buf + B_G)[srow];
-#pragma unroll
-            for (int j = 0; j < CPT; ++j) S[j] = fmaf(gamC, S[j], dsv[j]);
-            write_state_operand();
         }
         fence_async_smem();
         tc_fence_before();
@@ -627,7 +667,7 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64) : "memory");
     }
 }
 

@@ -65,6 +65,26 @@ __device__ __forceinline__ uint64_t desc_sbo(uint32_t addr, uint32_t sbo) {
 }
 __device__ __forceinline__ uint64_t op_desc(uint32_t addr, int K) { return desc_sbo(addr, (uint32_t)K * 32u); }
 
+// K-major TF32 operand with 128-byte swizzle: atoms of 8 rows x 128 B (32 elements of K) on 1 KiB
+// boundaries, 16-byte chunk c of atom row r stored at chunk c ^ r; row-groups 1 KiB apart, K-atoms
+// N * 128 B apart.  A warp writing one row, K = 32 consecutive lanes, hits 32 distinct banks.
+__device__ __forceinline__ uint32_t sw128_off(int row, int k, int N) {
+    return (uint32_t)((k >> 5) * (N * 128) + (row >> 3) * 1024 + (row & 7) * 128 + ((((k & 31) >> 2) ^ (row & 7)) << 4) +
+                      (k & 3) * 4);
+}
+// Descriptor of one 8-element K-step of such an operand: `addr` = base + K-atom offset + (k % 32) * 4.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+
+// One lane of a converged warp (for issuing tcgen05 work from a warp that stays converged).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile("{\n.reg .pred p;\nelect.sync _|p, 0xffffffff;\nselp.u32 %0, 1, 0, p;\n}\n" : "=r"(pred));
+    return pred != 0;
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
