@@ -196,7 +196,7 @@ def gpu_prefill(inp, steps, warmup, dev, e2e_steps):
     st = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     ws_bytes = kda.kda_prefill_workspace_size(N, T, H, dk, dv, d["q"].dtype)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-    launches_per_call = 1 + (1 if ws_bytes > 0 else 0)
+    launches_per_call = kda.kda_prefill_launch_count(N, T, H, dk, dv, d["q"].dtype, ws_bytes)
     stream = torch.cuda.current_stream()
 
     def call():

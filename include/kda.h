@@ -86,6 +86,17 @@ KDA_API size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens
                                   int32_t d_v, kda_dtype dt);
 
 /*
+ * Number of kernel launches a kda_prefill call with these arguments makes on the
+ * current device (diagnostics: launch budgets, profiler capture ranges), or -1
+ * for arguments kda_prefill would reject on the host.  The two-phase path makes
+ * two launches per window of chunks, and its window count depends on
+ * workspace_bytes and on the device's SM count.  Calls cudaGetDevice and
+ * cudaDeviceGetAttribute; enqueues nothing.
+ */
+KDA_API int64_t kda_prefill_launch_count(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                                         int32_t d_v, kda_dtype dt, size_t workspace_bytes);
+
+/*
  * Chunkwise-parallel prefill over packed variable-length sequences, with state
  * in and state out ("Kimi K3, explained", section "Training in chunks": the
  * sequence is split into chunks, the per-token decay-and-erase products inside

@@ -25,6 +25,7 @@ KDA_DEVERR_CU_SEQLENS, KDA_DEVERR_STATE_IDX = 0x1, 0x2
 _vp, _i32, _i64, _sz, _f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 SIGNATURES = {
     "kda_prefill_workspace_size": (_sz, [_i32, _i64, _i32, _i32, _i32, ctypes.c_int]),
+    "kda_prefill_launch_count": (_i64, [_i32, _i64, _i32, _i32, _i32, ctypes.c_int, _sz]),
     "kda_prefill": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, ctypes.c_int,
                                    _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "kda_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
@@ -100,6 +101,14 @@ def _check(name, t, dtype, shape, device):
 def kda_prefill_workspace_size(num_seqs: int, total_tokens: int, H: int, d_k: int, d_v: int,
                                dtype: torch.dtype = torch.bfloat16) -> int:
     return int(load().kda_prefill_workspace_size(num_seqs, total_tokens, H, d_k, d_v, _dt(dtype)))
+
+
+def kda_prefill_launch_count(num_seqs: int, total_tokens: int, H: int, d_k: int, d_v: int,
+                             dtype: torch.dtype = torch.bfloat16, workspace_bytes: int = None) -> int:
+    """Kernel launches of one kda_prefill call (with the recommended workspace when none is given)."""
+    if workspace_bytes is None:
+        workspace_bytes = kda_prefill_workspace_size(num_seqs, total_tokens, H, d_k, d_v, dtype)
+    return int(load().kda_prefill_launch_count(num_seqs, total_tokens, H, d_k, d_v, _dt(dtype), workspace_bytes))
 
 
 def kda_prefill(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float = 1.0, state_out=None,

@@ -86,6 +86,24 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
     return align_up(sizeof(int32_t) * (size_t)num_seqs, 256);
 }
 
+int64_t kda_prefill_launch_count(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                 kda_dtype dt, size_t workspace_bytes) {
+    if (num_seqs < 0 || total_tokens < 0 || total_tokens > INT32_MAX || H <= 0 || d_k <= 0 || d_v <= 0) return -1;
+    if ((dt != KDA_DTYPE_F32 && dt != KDA_DTYPE_BF16) || !supported_head(d_k, d_v)) return -1;
+    if (num_seqs == 0) return total_tokens == 0 ? 0 : -1;
+    if (kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt)) {
+        if (workspace_bytes < kda::prefill_2p_min_workspace(H)) return -1;
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return -1;
+        const int64_t chunks = (total_tokens + kda::kChunk - 1) / kda::kChunk;
+        const kda::WindowPlan plan = kda::prefill_2p_plan(chunks, H, workspace_bytes, sms);
+        return 2 * ((chunks + plan.window - 1) / plan.window);
+    }
+    return num_seqs > 1 ? 2 : 1;                      // longest-first order, then the chunkwise kernel
+}
+
 kda_status kda_prefill(const void* q, const void* k, const void* v, const float* beta,
                        const float* alpha, const int32_t* cu_seqlens, int32_t num_seqs,
                        int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,

@@ -36,7 +36,7 @@ constexpr int REC_BYTES = 197120;
 constexpr int QM_BYTES = (C + DK) * DK * 4;
 constexpr int SNV = 32;            // value columns per chain CTA
 constexpr int SLICES = DK / SNV;
-constexpr size_t kWindowBudget = size_t(512) << 20;   // workspace bytes the records of one window may use
+constexpr size_t kBufBudget = size_t(256) << 20;      // record bytes per window buffer (two buffers at most)
 static_assert(QM_BYTES == REC_B && REC_B + DK * DK * 4 == REC_O && REC_O + C * DK * 4 == REC_G, "record layout");
 
 // ---- phase 1 shared memory ----
@@ -54,20 +54,30 @@ static_assert(PS_KV + (DK + DK) * 256 <= PS_P && PS_P + 16384 <= G1_BYTES, "phas
 static_assert(PS_KH + DK * C * 4 <= PS_P, "phase-1 fold operands");
 static_assert(P_SMEM <= 232448, "phase-1 shared memory");
 
-// ---- phase 2 shared memory ----
-constexpr int C_OFF_S = 2 * QM_BYTES;              // S^T operand: TF32 32 x 128, 128-byte swizzle
-constexpr int C_OFF_MISC = C_OFF_S + SNV * DK * 4;
-constexpr int C_SMEM = C_OFF_MISC + 64;
+// ---- phase 2 shared memory and threads ----
+constexpr int SOP_BYTES = SNV * DK * 4;            // S^T operand: TF32 32 x 128, 128-byte swizzle
+constexpr int C_OFF_S = 2 * QM_BYTES;              // two record buffers, then two S^T operands
+constexpr int C_OFF_MISC = C_OFF_S + 2 * SOP_BYTES;
+constexpr int C_SMEM = C_OFF_MISC + 128;
+constexpr int C_NT = NT + 6 * 32;                  // 8 state warps, 2 MMA-issue warps, 2 idle, 2 output warps
 static_assert(C_OFF_S % 1024 == 0 && C_SMEM <= 232448, "phase-2 shared memory");
 
 struct PrepMaps {
     CUtensorMap k, q, a, v;   // v with a 128-column box
 };
 
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(mbar)
                  : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
 }
 
 __device__ __forceinline__ bool valid_single_sequence(const PrefillParams& p) {
@@ -75,30 +85,27 @@ __device__ __forceinline__ bool valid_single_sequence(const PrefillParams& p) {
 }
 
 // ============================================================================================
-// Phase 1: one CTA per (head, chunk) of the window [c_begin, c_begin + n_chunks).
+// Phase 1: persistent CTAs over the units (chunk-major: unit = window chunk * H + head) of the window
+// starting at chunk c_begin.  The raw tiles of a CTA's next unit are loaded while it stores the
+// current unit's record.
 // ============================================================================================
 __global__ void __launch_bounds__(NT, 1)
     kda_prefill_prep_kernel(PrefillParams p, const __grid_constant__ PrepMaps maps, unsigned char* records,
-                            int c_begin) {
+                            int c_begin, int n_units) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const int quad = warp & 3, half = warp >> 2;
     const int ch = tid & (DK - 1), rh = tid >> 7;
     const int H = p.H;
-    const int h = blockIdx.x % H, cw = blockIdx.x / H;
-    const int32_t t0 = (int32_t)(c_begin + cw) * C;
     if (!valid_single_sequence(p)) {
         if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
         return;
     }
-    if (t0 >= p.total_tokens) return;
     if (saddr(sm) & 1023u) {
         if (tid == 0) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
         return;
     }
-    const int L = min(C, p.total_tokens - t0);
-    unsigned char* rec = records + (size_t)(cw * H + h) * REC_BYTES;
 
     const __nv_bfloat16* vraw = reinterpret_cast<const __nv_bfloat16*>(sm + P_OFF_V);
     float* sbeta = reinterpret_cast<float*>(sm + P_OFF_BETA);
@@ -127,26 +134,7 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t tmem = *s_tmem;
     const uint32_t tlane = (uint32_t)(quad * 32) << 16;
     uint32_t phase = 0;
-    bool ok = true;
 
-    // ---- raw tiles by TMA (v with one 128-column box), beta by plain loads ----
-    if (tid == 32) {
-        mbar_expect_tx(lbar, 2 * 16384 + 32768 + C * DK * 2);
-        tma_load_3d(saddr(sm + OFF_K), &maps.k, 0, h, t0, lbar);
-        tma_load_3d(saddr(sm + OFF_K + 8192), &maps.k, 64, h, t0, lbar);
-        tma_load_3d(saddr(sm + OFF_Q), &maps.q, 0, h, t0, lbar);
-        tma_load_3d(saddr(sm + OFF_Q + 8192), &maps.q, 64, h, t0, lbar);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) tma_load_3d(saddr(sm + OFF_G + b * 8192), &maps.a, 32 * b, h, t0, lbar);
-        tma_load_3d(saddr(sm + P_OFF_V), &maps.v, 0, h, t0, lbar);
-    }
-    if (tid < C) sbeta[tid] = tid < L ? p.beta[(int64_t)(t0 + tid) * H + h] : 0.f;
-    if (!mbar_wait(lbar, 0)) {
-        atomicOr(p.err, KDA_DEVERR_TIMEOUT);
-        *s_abort = 1;
-    }
-    __syncthreads();
-    if (*s_abort) ok = false;
     auto wait_mma = [&]() -> bool {
         if (!mbar_wait(mbar, phase)) {
             atomicOr(p.err, KDA_DEVERR_TIMEOUT);
@@ -158,8 +146,46 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_after();
         return true;
     };
-    do {
-        if (!ok) break;
+    // raw tiles of unit u by TMA (v with one 128-column box)
+    auto issue_loads = [&](int u) {
+        if (tid == 32) {
+            const int hu = u % H;
+            const int32_t tu = (int32_t)(c_begin + u / H) * C;
+            mbar_expect_tx(lbar, 2 * 16384 + 32768 + C * DK * 2);
+            tma_load_3d(saddr(sm + OFF_K), &maps.k, 0, hu, tu, lbar);
+            tma_load_3d(saddr(sm + OFF_K + 8192), &maps.k, 64, hu, tu, lbar);
+            tma_load_3d(saddr(sm + OFF_Q), &maps.q, 0, hu, tu, lbar);
+            tma_load_3d(saddr(sm + OFF_Q + 8192), &maps.q, 64, hu, tu, lbar);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) tma_load_3d(saddr(sm + OFF_G + b * 8192), &maps.a, 32 * b, hu, tu, lbar);
+            tma_load_3d(saddr(sm + P_OFF_V), &maps.v, 0, hu, tu, lbar);
+        }
+    };
+    uint32_t lph = 0;
+    bool load_pending = (int)blockIdx.x < n_units;
+    float beta_next = 0.f;
+    if (load_pending) {
+        issue_loads(blockIdx.x);
+        const int32_t tn = (int32_t)(c_begin + (int)blockIdx.x / H) * C;
+        if (tid < C && tn + tid < p.total_tokens) beta_next = p.beta[(int64_t)(tn + tid) * H + (int)blockIdx.x % H];
+    }
+
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const int h = u % H, cw = u / H;
+        const int32_t t0 = (int32_t)(c_begin + cw) * C;
+        const int L = min(C, p.total_tokens - t0);
+        unsigned char* rec = records + (size_t)u * REC_BYTES;
+        if (tid < C) sbeta[tid] = beta_next;
+        if (!mbar_wait(lbar, lph)) {
+            atomicOr(p.err, KDA_DEVERR_TIMEOUT);
+            *s_abort = 1;
+        }
+        lph ^= 1u;
+        load_pending = false;
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");   // staging is free
+        tc_fence_before();
+        __syncthreads();
+        if (*s_abort) break;
         if (L < C) {                                    // rows past the sequence end read as zero
             for (int e = tid; e < (C - L) * 16; e += NT) {
                 const int r = L + (e >> 4), c = e & 15;
@@ -263,7 +289,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
             umma_commit(mbar);
         }
-        if (!wait_mma()) { ok = false; break; }
+        if (!wait_mma()) break;
         {                                               // scatter: A (fp32) and P (TF32 operand)
             const int sr = 16 * quad + lane;
             float v[32];
@@ -370,29 +396,34 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_before();
         __syncthreads();
 
-        // ---- 4. [W | Utilde] = T' [Gamma.K | V]  (M=64, N=256, K=64) ----
+        // ---- 4. [W | Utilde]^T = [Gamma.K | V]^T T'^T  (two M=128 halves, N=64, K=64) ----
         if (warp == 0 && elect_one()) {
             tc_fence_after();
-            umma_tf32<C>(tmem, saddr(X + PS_OPT), saddr(X + PS_KV), idesc_tf32(64, 2 * DK), false);
+            constexpr uint32_t id = idesc_tf32(128, C);
+            const uint64_t aw = op_desc(saddr(X + PS_KV), C), au = op_desc(saddr(X + PS_KV + DK * C * 4), C);
+            const uint64_t bt = op_desc(saddr(X + PS_OPT), C);
+#pragma unroll
+            for (int ks = 0; ks < C / 8; ++ks) {
+                umma_tf32_1(tmem, aw + (uint64_t)(ks * 16), bt + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
+                umma_tf32_1(tmem + C, au + (uint64_t)(ks * 16), bt + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
+            }
             umma_commit(mbar);
         }
-        if (!wait_mma()) { ok = false; break; }
+        if (!wait_mma()) break;
 
-        // ---- 5. fold operands: [W | Utilde]^T (N=256, K=64, 128-byte swizzle) and Khat^T (M=128, K=64) ----
+        // ---- 5. fold operands: [W | Utilde]^T (N=256, K=64) and Khat^T (M=128, K=64) ----
         unsigned char* opWU = X + PS_WU;
         unsigned char* opKH = X + PS_KH;
         {
-            const int sr = 16 * quad + lane;                     // time row of this lane (lanes < 16)
+            const int n = DK * half + 32 * quad + lane;          // row of [W | Utilde]^T held by this lane
             float v[32];
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                const int c0 = 128 * half + 32 * cb;
-                tmem_ld32(tmem + tlane + c0, v);
-                if (lane < 16) {
+            for (int cb = 0; cb < 2; ++cb) {
+                tmem_ld32(tmem + tlane + C * half + 32 * cb, v);
 #pragma unroll
-                    for (int x = 0; x < 32; ++x)
-                        *reinterpret_cast<float*>(opWU + sw128_off(c0 + x, sr, 2 * DK)) = tf32r(v[x]);
-                }
+                for (int x = 0; x < 32; x += 4)
+                    *reinterpret_cast<float4*>(opWU + op_off(n, 32 * cb + x, C)) =
+                        make_float4(tf32r(v[x]), tf32r(v[x + 1]), tf32r(v[x + 2]), tf32r(v[x + 3]));
             }
         }
         for (int e = tid; e < DK * 16; e += NT) {
@@ -414,10 +445,10 @@ __global__ void __launch_bounds__(NT, 1)
             if (elect_one()) {
                 tc_fence_after();
                 const uint64_t ak = op_desc(saddr(opKH), C), ap = op_desc(saddr(opP), C);
-                const uint32_t wb = saddr(opWU);
+                const uint64_t bw = op_desc(saddr(opWU), C);
 #pragma unroll
                 for (int ks = 0; ks < C / 8; ++ks) {
-                    const uint64_t bd = desc_sw128(wb + (ks >> 2) * (2 * DK * 128) + (ks & 3) * 32);
+                    const uint64_t bd = bw + (uint64_t)(ks * 16);
                     umma_tf32_1(tmem, ak + (uint64_t)(ks * 16), bd, idesc_tf32(128, 2 * DK), ks > 0 ? 1u : 0u);
                     umma_tf32_1(tmem + 2 * DK, ap + (uint64_t)(ks * 16), bd, idesc_tf32(64, 2 * DK), ks > 0 ? 1u : 0u);
                 }
@@ -425,64 +456,84 @@ __global__ void __launch_bounds__(NT, 1)
             }
             __syncwarp();
         }
-        if (!wait_mma()) { ok = false; break; }
+        if (!wait_mma()) break;
 
         // ---- 7. the record, from TMEM straight to global memory ----
-        {
-            const int i = 32 * quad + lane;                      // M=128 accumulator row
-            const int r = 16 * quad + lane;                      // M=64 accumulator row (lanes < 16)
-            float v[32];
+        const int i = 32 * quad + lane;                          // M=128 accumulator row
+        const int r = 16 * quad + lane;                          // M=64 accumulator row (lanes < 16)
+        float v[32];
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {                     // M = Khat^T W -> rows 64.. of [Q'; M]
-                const int c0 = 64 * half + 32 * cb;
-                tmem_ld32(tmem + tlane + c0, v);
+        for (int cb = 0; cb < 2; ++cb) {                         // Q' = Gamma.Q - P W -> rows 0..63 of [Q'; M]
+            const int c0 = 64 * half + 32 * cb;
+            tmem_ld32(tmem + tlane + 2 * DK + c0, v);
+            if (lane < 16) {
 #pragma unroll
-                for (int x = 0; x < 32; x += 4)
-                    *reinterpret_cast<float4*>(rec + REC_QM + op_off(C + i, c0 + x, DK)) =
-                        make_float4(tf32r(v[x]), tf32r(v[x + 1]), tf32r(v[x + 2]), tf32r(v[x + 3]));
+                for (int x = 0; x < 32; x += 4) {
+                    const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(r, c0 + x));
+                    const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(r, c0 + x));
+                    const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
+                    *reinterpret_cast<float4*>(rec + REC_QM + op_off(r, c0 + x, DK)) =
+                        make_float4(tf32r(ex2f(gg.x) * __low2float(q2[0]) - v[x]),
+                                    tf32r(ex2f(gg.y) * __high2float(q2[0]) - v[x + 1]),
+                                    tf32r(ex2f(gg.z) * __low2float(q2[1]) - v[x + 2]),
+                                    tf32r(ex2f(gg.w) * __high2float(q2[1]) - v[x + 3]));
+                }
             }
+        }
+        if (tid < DK) reinterpret_cast<float*>(rec + REC_G)[tid] = sgam[tid];
+        // M and B are staged in the scratch (free once the fold products are done) in their record byte
+        // layout and written by two bulk copies, which drain while the next unit starts
+        unsigned char* stage = X;                                // [M rows of [Q'; M] (64 KiB) | B (64 KiB)]
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {                     // B = Khat^T Utilde
-                const int c0 = 64 * half + 32 * cb;
-                tmem_ld32(tmem + tlane + DK + c0, v);
+        for (int cb = 0; cb < 2; ++cb) {                         // M = Khat^T W -> rows 64.. of [Q'; M]
+            const int c0 = 64 * half + 32 * cb;
+            tmem_ld32(tmem + tlane + c0, v);
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+                *reinterpret_cast<float4*>(stage + op_off(C + i, c0 + x, DK) - C * DK * 4) =
+                    make_float4(tf32r(v[x]), tf32r(v[x + 1]), tf32r(v[x + 2]), tf32r(v[x + 3]));
+        }
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {                         // B = Khat^T Utilde
+            const int c0 = 64 * half + 32 * cb;
+            tmem_ld32(tmem + tlane + DK + c0, v);
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+                *reinterpret_cast<float4*>(stage + DK * DK * 4 + (((c0 + x) >> 2) * DK + i) * 16) =
+                    make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+        }
+        fence_async_smem();
+        __syncthreads();                                         // staged; the raw tiles are free
+        const int un = u + (int)gridDim.x;
+        if (un < n_units) {                                      // fetch the next unit's tiles and beta
+            issue_loads(un);
+            load_pending = true;
+            if (tid < C) {
+                const int32_t tn = (int32_t)(c_begin + un / H) * C;
+                beta_next = tn + tid < p.total_tokens ? p.beta[(int64_t)(tn + tid) * H + un % H] : 0.f;
+            }
+        }
+        if (tid == 0) {
+            bulk_s2g(rec + REC_QM + C * DK * 4, saddr(stage), DK * DK * 4);
+            bulk_s2g(rec + REC_B, saddr(stage + DK * DK * 4), DK * DK * 4);
+            asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+        }
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {                         // P Utilde
+            const int c0 = 64 * half + 32 * cb;
+            tmem_ld32(tmem + tlane + 3 * DK + c0, v);
+            if (lane < 16) {
 #pragma unroll
                 for (int x = 0; x < 32; x += 4)
-                    *reinterpret_cast<float4*>(rec + REC_B + (((c0 + x) >> 2) * DK + i) * 16) =
+                    *reinterpret_cast<float4*>(rec + REC_O + (((c0 + x) >> 2) * C + r) * 16) =
                         make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
             }
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {                     // Q' = Gamma.Q - P W -> rows 0..63 of [Q'; M]
-                const int c0 = 64 * half + 32 * cb;
-                tmem_ld32(tmem + tlane + 2 * DK + c0, v);
-                if (lane < 16) {
-#pragma unroll
-                    for (int x = 0; x < 32; x += 4) {
-                        const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(r, c0 + x));
-                        const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(r, c0 + x));
-                        const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
-                        *reinterpret_cast<float4*>(rec + REC_QM + op_off(r, c0 + x, DK)) =
-                            make_float4(tf32r(ex2f(gg.x) * __low2float(q2[0]) - v[x]),
-                                        tf32r(ex2f(gg.y) * __high2float(q2[0]) - v[x + 1]),
-                                        tf32r(ex2f(gg.z) * __low2float(q2[1]) - v[x + 2]),
-                                        tf32r(ex2f(gg.w) * __high2float(q2[1]) - v[x + 3]));
-                    }
-                }
-            }
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {                     // P Utilde
-                const int c0 = 64 * half + 32 * cb;
-                tmem_ld32(tmem + tlane + 3 * DK + c0, v);
-                if (lane < 16) {
-#pragma unroll
-                    for (int x = 0; x < 32; x += 4)
-                        *reinterpret_cast<float4*>(rec + REC_O + (((c0 + x) >> 2) * C + r) * 16) =
-                            make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
-                }
-            }
-            if (tid < DK) reinterpret_cast<float*>(rec + REC_G)[tid] = sgam[tid];
         }
-    } while (false);
+        tc_fence_before();
+    }
 
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+    if (load_pending) mbar_wait(lbar, lph);              // bounded: never leave copies in flight
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -493,14 +544,28 @@ __global__ void __launch_bounds__(NT, 1)
 
 // ============================================================================================
 // Phase 2: one CTA per (head, 32 value columns), chunks [c_begin, c_begin + n_chunks) in order.
+//
+// Warps 0-7 hold the state (thread = one key channel, 16 value columns) and run the fp32 update;
+// warp 8 issues the products, warp 9 the record loads; warps 12-13 (TMEM lanes 0..63: the chunk's 64
+// output rows) run the output epilogue.  Per chunk c:
+//   warp 8:      wait record c, sbar ("S_c written") and ofree (output of c-2 read); issue M S_c -> dbar,
+//                then [Q'; M_top] S_c -> obar (issued while the state warps update S)
+//   warp 9:      wait obar, load record c+2 into the freed buffer
+//   warps 0-7:   wait dbar; S_{c+1} = Gamma_C S_c + B - M S_c; write the S^T operand of c+1; arrive on sbar
+//   warps 12-13: wait obar; o = scale ([Q'; M_top] S_c + P Utilde) for rows 0..63; arrive on ofree
+// so the output products and epilogue of one chunk overlap the state products of the next, and the
+// state warps' proxy fence never waits on output traffic.  The S^T operand and the output accumulator
+// are double-buffered; M S uses one accumulator (it is read before the arrival on sbar).  Every barrier
+// can run at most one phase ahead of each of its waiters.  Warps 10-11 exist only so that the output
+// warps sit on TMEM lanes 0..63 (warp w reaches lanes 32 (w mod 4) .. +31).
 // ============================================================================================
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(C_NT, 1)
     kda_prefill_chain_kernel(PrefillParams p, const unsigned char* records, int c_begin, int n_chunks,
                              const float* state_in) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;
-    constexpr int CPT = SNV / 2;                      // value columns per thread
+    const int quad = warp & 3, half = (warp >> 2) & 1;
+    constexpr int CPT = SNV / 2;                      // value columns per epilogue thread
     const int H = p.H;
     const int h = blockIdx.x / SLICES, slice = blockIdx.x % SLICES, j0 = slice * SNV;
     if (!valid_single_sequence(p)) {
@@ -513,117 +578,174 @@ __global__ void __launch_bounds__(NT, 1)
     }
     const int32_t T = p.total_tokens;
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(p.o);
-    volatile int* s_abort = reinterpret_cast<volatile int*>(sm + C_OFF_MISC + 12);
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + C_OFF_MISC + 8);
-    const uint32_t mbar = saddr(sm + C_OFF_MISC);
-    const uint32_t lbar0 = saddr(sm + C_OFF_MISC + 16), lbar1 = saddr(sm + C_OFF_MISC + 24);
-    unsigned char* sop = sm + C_OFF_S;
-    constexpr uint32_t TM_O = 0, TM_S = 32;           // [Q'; M_top] S and M S accumulators
+    unsigned char* misc = sm + C_OFF_MISC;
+    volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 100);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + 96);
+    const uint32_t lbar = saddr(misc), dbar = saddr(misc + 16), obar = saddr(misc + 32), sbar = saddr(misc + 48);
+    const uint32_t ofree = saddr(misc + 64);
+    constexpr uint32_t TM_S = 0, TM_O = 32;           // M S accumulator; two [Q'; M_top] S accumulators
 
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(lbar0) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(lbar1) : "memory");
+        for (int b = 0; b < 2; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(lbar + 8 * b) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(dbar + 8 * b) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(obar + 8 * b) : "memory");
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sbar), "r"(NT) : "memory");
+        for (int b = 0; b < 2; ++b)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(ofree + 8 * b), "r"(64) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *s_abort = 0;
     }
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(s_tmem)), "r"(64)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(s_tmem)), "r"(128)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    const int srow = 32 * quad + lane;                // state row (key channel) of this thread
-    const int jc = j0 + CPT * half;                   // first value column of this thread
-    const int64_t state_off = (((int64_t)h) * DK + srow) * (int64_t)p.dv + jc;
-    float S[CPT];
-#pragma unroll
-    for (int j = 0; j < CPT; j += 4) {
-        const float4 v4 = state_in ? *reinterpret_cast<const float4*>(state_in + state_off + j)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-        S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t tlane = (uint32_t)(quad * 32) << 16;
-    uint32_t phase = 0, lph = 0;      // lph bit b: parity of buffer b's next load;  pend bit b: a load in flight
-    uint32_t pend = 0;
-    bool aborted = false;
+    auto fail = [&]() {
+        atomicOr(p.err, KDA_DEVERR_TIMEOUT);
+        *s_abort = 1;
+    };
 
-    auto issue = [&](int ci) {                        // bulk-load [Q'; M] of chunk ci into buffer ci & 1
-        if (tid == 32) {
+    const uint32_t sop0 = saddr(sm + C_OFF_S);
+    if (warp == 8) {
+        // ---------------- products: M S_c (sequential path), then [Q'; M_top] S_c ----------------
+        const uint64_t a_s0 = op_desc(saddr(sm) + C * DK * 4, DK), a_o0 = op_desc(saddr(sm), DK);
+        const uint64_t b_s0 = desc_sw128(sop0);
+        int issued = 0;                               // chunks whose products were issued
+        for (int ci = 0; ci < n_chunks; ++ci) {
             const int b = ci & 1;
-            const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
-            const uint32_t lb = b ? lbar1 : lbar0;
-            mbar_expect_tx(lb, QM_BYTES);
-            bulk_g2s(saddr(sm + b * QM_BYTES), rec + REC_QM, QM_BYTES, lb);
-        }
-        pend |= 1u << (ci & 1);
-    };
-    auto write_state_operand = [&]() {                // S^T as a TF32 operand: row = value column, K = srow
-#pragma unroll
-        for (int j = 0; j < CPT; ++j)
-            *reinterpret_cast<float*>(sop + sw128_off(CPT * half + j, srow, SNV)) = tf32r(S[j]);
-    };
-    write_state_operand();
-    if (n_chunks > 0) issue(0);
-    if (n_chunks > 1) issue(1);
-    fence_async_smem();
-    __syncthreads();
-
-    for (int ci = 0; ci < n_chunks && !aborted; ++ci) {
-        const int b = ci & 1;
-        const uint32_t abuf = saddr(sm + b * QM_BYTES);
-        const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
-        const int32_t t0 = (c_begin + ci) * C;
-        const int L = min(C, T - t0);
-        if (!mbar_wait(b ? lbar1 : lbar0, (lph >> b) & 1u)) {
-            atomicOr(p.err, KDA_DEVERR_TIMEOUT);
-            *s_abort = 1;
-        }
-        lph ^= 1u << b;
-        pend &= ~(1u << b);
-        __syncthreads();
-        if (*s_abort) { aborted = true; break; }
-
-        // [Q'; M_top] S and M S: 2 x 16 TF32 steps, one commit
-        if (warp == 0) {
+            const uint32_t par = (uint32_t)(ci >> 1) & 1u;
+            if (!mbar_wait(lbar + 8 * b, par)) fail();
+            if (!mbar_wait(sbar, (uint32_t)ci & 1u)) fail();
+            // the output accumulator of chunk ci was last read by the output warps for chunk ci - 2
+            if (ci >= 2 && !mbar_wait(ofree + 8 * b, par ^ 1u)) fail();
+            if (*s_abort) break;
+            tc_fence_after();
             if (elect_one()) {
-                tc_fence_after();
-                constexpr uint32_t id = idesc_tf32(128, SNV);
-                const uint64_t a_o = op_desc(abuf, DK), a_s = op_desc(abuf + C * DK * 4, DK);
-                const uint32_t sb = saddr(sop);
+                const uint64_t bs = b_s0 + (uint64_t)((b * SOP_BYTES) >> 4);
+                const uint64_t as = a_s0 + (uint64_t)((b * QM_BYTES) >> 4), ao = a_o0 + (uint64_t)((b * QM_BYTES) >> 4);
 #pragma unroll
-                for (int ks = 0; ks < DK / 8; ++ks) {
-                    const uint64_t bd = desc_sw128(sb + (ks >> 2) * (SNV * 128) + (ks & 3) * 32);
-                    umma_tf32_1(tmem + TM_O, a_o + (uint64_t)(ks * 16), bd, id, ks > 0 ? 1u : 0u);
-                    umma_tf32_1(tmem + TM_S, a_s + (uint64_t)(ks * 16), bd, id, ks > 0 ? 1u : 0u);
-                }
-                umma_commit(mbar);
+                for (int ks = 0; ks < DK / 8; ++ks)
+                    umma_tf32_1(tmem + TM_S, as + (uint64_t)(ks * 16),
+                                bs + (uint64_t)(((ks >> 2) * (SNV * 128) + (ks & 3) * 32) >> 4), idesc_tf32(128, SNV),
+                                ks > 0 ? 1u : 0u);
+                umma_commit(dbar + 8 * b);
+#pragma unroll
+                for (int ks = 0; ks < DK / 8; ++ks)
+                    umma_tf32_1(tmem + TM_O + SNV * b, ao + (uint64_t)(ks * 16),
+                                bs + (uint64_t)(((ks >> 2) * (SNV * 128) + (ks & 3) * 32) >> 4), idesc_tf32(128, SNV),
+                                ks > 0 ? 1u : 0u);
+                umma_commit(obar + 8 * b);
             }
             __syncwarp();
+            issued = ci + 1;
         }
-        // the chunk's B, P Utilde and Gamma_C, loaded while the products run
-        float4 bq[CPT / 4], oq[CPT / 4];
+        // never leave products in flight
+        if (issued > 0) mbar_wait(obar + 8 * ((issued - 1) & 1), (uint32_t)((issued - 1) >> 1) & 1u);
+    } else if (warp == 9) {
+        // ---------------- record loads: [Q'; M] of chunk c + 2 once the products of c are done ----------------
+        auto load = [&](int ci) {                     // [Q'; M] of chunk ci into buffer ci & 1
+            if (lane == 0) {
+                const uint32_t lb = lbar + 8 * (ci & 1);
+                mbar_expect_tx(lb, QM_BYTES);
+                bulk_g2s(saddr(sm + (ci & 1) * QM_BYTES), records + (size_t)(ci * H + h) * REC_BYTES + REC_QM,
+                         QM_BYTES, lb);
+            }
+        };
+        if (n_chunks > 0) load(0);
+        if (n_chunks > 1) load(1);
+        int loaded = n_chunks < 2 ? n_chunks : 2;
+        for (int ci = 0; ci + 2 < n_chunks; ++ci) {
+            if (*s_abort) break;
+            if (!mbar_wait(obar + 8 * (ci & 1), (uint32_t)(ci >> 1) & 1u)) { fail(); break; }
+            load(ci + 2);
+            loaded = ci + 3;
+        }
+        // never leave copies in flight: every issued load completes (bounded waits)
+        for (int ci = loaded - 2 < 0 ? 0 : loaded - 2; ci < loaded; ++ci)
+            mbar_wait(lbar + 8 * (ci & 1), (uint32_t)(ci >> 1) & 1u);
+    } else if (warp >= 12) {
+        // ---------------- output warps: rows 0..63 of chunk c ----------------
+        const int orow = 32 * (warp - 12) + lane;
+        const uint32_t tlane = (uint32_t)(32 * (warp - 12)) << 16;
+        float4 oq[SNV / 4];
+        auto fetch_o = [&](int ci) {                  // the chunk's P Utilde for this row and slice
+            const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
 #pragma unroll
-        for (int m = 0; m < CPT / 4; ++m)
-            bq[m] = __ldg(reinterpret_cast<const float4*>(rec + REC_B + (((jc + 4 * m) >> 2) * DK + srow) * 16));
-        if (quad < 2) {
+            for (int m = 0; m < SNV / 4; ++m)
+                oq[m] = __ldg(reinterpret_cast<const float4*>(rec + REC_O + (((j0 + 4 * m) >> 2) * C + orow) * 16));
+        };
+        if (n_chunks > 0) fetch_o(0);
+        for (int ci = 0; ci < n_chunks; ++ci) {
+            const int b = ci & 1;
+            if (*s_abort) break;
+            if (!mbar_wait(obar + 8 * b, (uint32_t)(ci >> 1) & 1u)) { fail(); break; }
+            tc_fence_after();
+            float d[SNV];
+            tmem_ld32(tmem + tlane + TM_O + SNV * b, d);
+            tc_fence_before();
+            mbar_arrive(ofree + 8 * b);
+            const int32_t t0 = (c_begin + ci) * C;
+            if (orow < min(C, T - t0)) {
+                __nv_bfloat16* dst = go + ((int64_t)(t0 + orow) * H + h) * p.dv + j0;
+#pragma unroll
+                for (int x = 0; x < SNV; x += 8) {
+                    const float4 o0 = oq[x / 4], o1 = oq[x / 4 + 1];
+                    *reinterpret_cast<uint4*>(dst + x) =
+                        make_uint4(pack_bf16x2(p.scale * (d[x] + o0.x), p.scale * (d[x + 1] + o0.y)),
+                                   pack_bf16x2(p.scale * (d[x + 2] + o0.z), p.scale * (d[x + 3] + o0.w)),
+                                   pack_bf16x2(p.scale * (d[x + 4] + o1.x), p.scale * (d[x + 5] + o1.y)),
+                                   pack_bf16x2(p.scale * (d[x + 6] + o1.z), p.scale * (d[x + 7] + o1.w)));
+                }
+            }
+            if (ci + 1 < n_chunks) fetch_o(ci + 1);
+        }
+    } else if (warp < 8) {
+        // ---------------- state warps ----------------
+        const uint32_t tlane = (uint32_t)(quad * 32) << 16;
+        const int srow = 32 * quad + lane;            // state row (key channel)
+        const int jc = j0 + CPT * half;               // first value column of this thread
+        const int64_t state_off = (((int64_t)h) * DK + srow) * (int64_t)p.dv + jc;
+        float S[CPT];
+#pragma unroll
+        for (int j = 0; j < CPT; j += 4) {
+            const float4 v4 = state_in ? *reinterpret_cast<const float4*>(state_in + state_off + j)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
+        }
+        auto write_state_operand = [&](int b) {      // S^T: row = value column, K = srow
+            unsigned char* sop = sm + C_OFF_S + b * SOP_BYTES;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j)
+                *reinterpret_cast<float*>(sop + sw128_off(CPT * half + j, srow, SNV)) = tf32r(S[j]);
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(sbar);
+        };
+        // the chunk's B and Gamma_C, fetched one chunk ahead (after the proxy fence, which would wait on them)
+        float4 bq[CPT / 4];
+        float gamC = 0.f;
+        auto fetch_b = [&](int ci) {
+            const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
 #pragma unroll
             for (int m = 0; m < CPT / 4; ++m)
-                oq[m] = __ldg(reinterpret_cast<const float4*>(rec + REC_O + (((jc + 4 * m) >> 2) * C + srow) * 16));
-        }
-        const float gamC = __ldg(reinterpret_cast<const float*>(rec + REC_G) + srow);
-        if (!mbar_wait(mbar, phase)) {
-            atomicOr(p.err, KDA_DEVERR_TIMEOUT);
-            *s_abort = 1;
-        }
-        phase ^= 1u;
-        __syncthreads();
-        if (*s_abort) { aborted = true; break; }
-        tc_fence_after();
-        {
+                bq[m] = __ldg(reinterpret_cast<const float4*>(rec + REC_B + (((jc + 4 * m) >> 2) * DK + srow) * 16));
+            gamC = __ldg(reinterpret_cast<const float*>(rec + REC_G) + srow);
+        };
+        write_state_operand(0);
+        if (n_chunks > 0) fetch_b(0);
+        bool ok = true;
+        for (int ci = 0; ci < n_chunks; ++ci) {
+            const int b = ci & 1;
+            const uint32_t par = (uint32_t)(ci >> 1) & 1u;
+            if (*s_abort) { ok = false; break; }
+            if (!mbar_wait(dbar + 8 * b, par)) { fail(); ok = false; break; }
+            tc_fence_after();
             float d[CPT];
             tmem_ld16(tmem + tlane + TM_S + CPT * half, d);
 #pragma unroll
@@ -633,47 +755,61 @@ __global__ void __launch_bounds__(NT, 1)
                 S[4 * m + 2] = fmaf(gamC, S[4 * m + 2], bq[m].z - d[4 * m + 2]);
                 S[4 * m + 3] = fmaf(gamC, S[4 * m + 3], bq[m].w - d[4 * m + 3]);
             }
-            write_state_operand();
-            if (quad < 2) {                           // output rows 0..63 live in lanes 0..63
-                tmem_ld16(tmem + tlane + TM_O + CPT * half, d);
-                if (srow < L) {
-                    __nv_bfloat16* dst = go + ((int64_t)(t0 + srow) * H + h) * p.dv + jc;
-#pragma unroll
-                    for (int x = 0; x < CPT; x += 8) {
-                        const float4 o0 = oq[x / 4], o1 = oq[x / 4 + 1];
-                        *reinterpret_cast<uint4*>(dst + x) =
-                            make_uint4(pack_bf16x2(p.scale * (d[x] + o0.x), p.scale * (d[x + 1] + o0.y)),
-                                       pack_bf16x2(p.scale * (d[x + 2] + o0.z), p.scale * (d[x + 3] + o0.w)),
-                                       pack_bf16x2(p.scale * (d[x + 4] + o1.x), p.scale * (d[x + 5] + o1.y)),
-                                       pack_bf16x2(p.scale * (d[x + 6] + o1.z), p.scale * (d[x + 7] + o1.w)));
-                    }
+            if (ci + 1 < n_chunks) {
+                // the operand buffer of S_{c+1} was last read by the products of chunk c-1 (obar)
+                if (ci > 0 && !mbar_wait(obar + 8 * (b ^ 1), (uint32_t)((ci - 1) >> 1) & 1u)) {
+                    fail(); ok = false; break;
                 }
+                write_state_operand(b ^ 1);
+                fetch_b(ci + 1);
             }
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (ci + 2 < n_chunks) issue(ci + 2);          // this buffer is free again
-    }
-
-    if (!aborted) {
+        if (ok && !*s_abort) {
 #pragma unroll
-        for (int j = 0; j < CPT; j += 4)
-            *reinterpret_cast<float4*>(p.state_out + state_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            for (int j = 0; j < CPT; j += 4)
+                *reinterpret_cast<float4*>(p.state_out + state_off + j) =
+                    make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
     }
-    if (pend & 1u) mbar_wait(lbar0, lph & 1u);         // bounded: never leave copies in flight
-    if (pend & 2u) mbar_wait(lbar1, (lph >> 1) & 1u);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128) : "memory");
     }
 }
 
-int64_t window_chunks(int32_t H) {
-    const int64_t w = (int64_t)(kWindowBudget / ((size_t)H * REC_BYTES));
+int64_t buffer_chunks(int32_t H) {                   // chunks of records one 256 MiB buffer holds
+    const int64_t w = (int64_t)(kBufBudget / ((size_t)H * REC_BYTES));
     return w < 1 ? 1 : w;
+}
+
+// Side stream and events of the overlapped schedule, created once per device and kept for the life of
+// the process.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, prep_done[2] = {nullptr, nullptr}, chain_done[2] = {nullptr, nullptr};
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_side_mutex;
+SideStream g_side[kMaxDevices];
+std::mutex g_enqueue_mutex[kMaxDevices];
+
+cudaError_t side_stream(int dev, SideStream** out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_side_mutex);
+    SideStream& ss = g_side[dev];
+    if (!ss.stream) {
+        SideStream t;
+        cudaError_t e = cudaStreamCreateWithFlags(&t.stream, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return e;
+        cudaEvent_t* evs[5] = {&t.fork, &t.prep_done[0], &t.prep_done[1], &t.chain_done[0], &t.chain_done[1]};
+        for (cudaEvent_t* ev : evs)
+            if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+        ss = t;
+    }
+    *out = &ss;
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -686,11 +822,30 @@ bool prefill_2p_supported(int32_t num_seqs, int64_t total_tokens, int32_t H, int
 size_t prefill_2p_min_workspace(int32_t H) { return (size_t)H * REC_BYTES; }
 
 size_t prefill_2p_workspace(int64_t total_tokens, int32_t H) {
-    const int64_t chunks = (total_tokens + C - 1) / C;
-    const int64_t w = chunks < window_chunks(H) ? chunks : window_chunks(H);
-    return (size_t)w * H * REC_BYTES;
+    const int64_t chunks = (total_tokens + C - 1) / C, cap = 2 * buffer_chunks(H);
+    return (size_t)(chunks < cap ? chunks : cap) * H * REC_BYTES;
 }
 
+WindowPlan prefill_2p_plan(int64_t chunks, int32_t H, size_t workspace_bytes, int sms) {
+    const int64_t cap = (int64_t)(workspace_bytes / prefill_2p_min_workspace(H));   // records that fit
+    const int64_t one = buffer_chunks(H);
+    const bool overlap_ok = 2 * H * SLICES <= sms;   // the chain leaves at least half the SMs to phase 1
+    WindowPlan w;
+    if (chunks <= cap && chunks <= 2 * one) {
+        w.window = chunks; w.buffers = 1;             // one window
+    } else if (overlap_ok && cap >= 2) {
+        w.window = cap / 2 < one ? cap / 2 : one; w.buffers = 2;
+    } else {
+        w.window = cap < 2 * one ? cap : 2 * one; w.buffers = 1;
+    }
+    if (w.window < 1) w.window = 1;
+    return w;
+}
+
+// Phase 1 of window w+1 runs on a side stream while phase 2 of window w runs on the caller's stream,
+// with the records double-buffered, when the chain leaves SMs free (few heads); otherwise the windows
+// run back to back on the caller's stream.  Ordering is by events only, and every side-stream launch is
+// joined back into the caller's stream before the call returns.
 cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t workspace_bytes, cudaStream_t s) {
     auto enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
@@ -707,18 +862,43 @@ cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t wo
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kda_prefill_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C_SMEM);
     if (e != cudaSuccess) return e;
-    unsigned char* rec = static_cast<unsigned char*>(workspace);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int64_t chunks = (T + C - 1) / C;
-    int64_t wmax = (int64_t)(workspace_bytes / prefill_2p_min_workspace(p.H));   // records the workspace holds
-    if (wmax > window_chunks(p.H)) wmax = window_chunks(p.H);
-    if (wmax < 1) return cudaErrorInvalidValue;
-    for (int64_t c0 = 0; c0 < chunks; c0 += wmax) {
-        const int64_t n = chunks - c0 < wmax ? chunks - c0 : wmax;
-        kda_prefill_prep_kernel<<<(unsigned)(n * p.H), NT, P_SMEM, s>>>(p, maps, rec, (int)c0);
+    const WindowPlan plan = prefill_2p_plan(chunks, p.H, workspace_bytes, sms);
+    if ((size_t)plan.window * plan.buffers * prefill_2p_min_workspace(p.H) > workspace_bytes) return cudaErrorInvalidValue;
+    const int chain_ctas = p.H * SLICES;
+    const size_t buf_bytes = (size_t)plan.window * prefill_2p_min_workspace(p.H);
+    SideStream* ss = nullptr;
+    std::unique_lock<std::mutex> enqueue;             // concurrent callers must not interleave event records
+    if (plan.buffers == 2) {
+        if ((e = side_stream(dev, &ss)) != cudaSuccess) return e;
+        enqueue = std::unique_lock<std::mutex>(g_enqueue_mutex[dev]);
+        if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(ss->stream, ss->fork, 0)) != cudaSuccess) return e;
+    }
+    int w = 0;
+    for (int64_t c0 = 0; c0 < chunks; c0 += plan.window, ++w) {
+        const int64_t n = chunks - c0 < plan.window ? chunks - c0 : plan.window;
+        const int units = (int)(n * p.H);
+        const int buf = w % plan.buffers;
+        unsigned char* rec = static_cast<unsigned char*>(workspace) + buf * buf_bytes;
+        cudaStream_t ps = ss ? ss->stream : s;
+        // phase 1 shares the GPU with the previous window's chain when overlapped
+        int grid = (ss && w > 0) ? sms - chain_ctas : sms;
+        if (grid > units) grid = units;
+        if (ss && w >= 2 && (e = cudaStreamWaitEvent(ps, ss->chain_done[buf], 0)) != cudaSuccess) return e;
+        kda_prefill_prep_kernel<<<(unsigned)grid, NT, P_SMEM, ps>>>(p, maps, rec, (int)c0, units);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        kda_prefill_chain_kernel<<<(unsigned)(p.H * SLICES), NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n,
-                                                                               c0 == 0 ? p.state_in : p.state_out);
+        if (ss) {
+            if ((e = cudaEventRecord(ss->prep_done[buf], ps)) != cudaSuccess) return e;
+            if ((e = cudaStreamWaitEvent(s, ss->prep_done[buf], 0)) != cudaSuccess) return e;
+        }
+        kda_prefill_chain_kernel<<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n,
+                                                                            c0 == 0 ? p.state_in : p.state_out);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (ss && (e = cudaEventRecord(ss->chain_done[buf], s)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

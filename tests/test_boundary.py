@@ -54,13 +54,23 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     # one bf16 d=128 sequence: 197,120 bytes of records per (chunk, head), windows of at most 512 MiB
-    assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 1) == 85 * 32 * 197120
+    assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 1) == 84 * 32 * 197120
     assert lib.kda_prefill_workspace_size(1, 1_032_192, 8, 128, 128, 1) == 340 * 8 * 197120
     assert lib.kda_prefill_workspace_size(1, 65, 4, 128, 128, 1) == 2 * 4 * 197120
     assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 0) == 0      # fp32: single-kernel path
     assert lib.kda_prefill_workspace_size(1, 8192, 32, 64, 64, 1) == 0
     assert lib.kda_prefill_workspace_size(64, 300000, 32, 128, 128, 1) == 256
     assert lib.kda_prefill_workspace_size(65, 300000, 32, 128, 128, 1) == 512
+
+
+def test_launch_count_host_paths(lib):
+    """Launch counts that need no device: rejected arguments, the single-kernel paths."""
+    assert lib.kda_prefill_launch_count(0, 0, 2, 16, 16, 0, 0) == 0
+    assert lib.kda_prefill_launch_count(0, 5, 2, 16, 16, 0, 0) == -1
+    assert lib.kda_prefill_launch_count(1, 64, 2, 32, 32, 0, 0) == -1
+    assert lib.kda_prefill_launch_count(1, 64, 2, 16, 16, 0, 0) == 1
+    assert lib.kda_prefill_launch_count(3, 640, 2, 64, 64, 1, 256) == 2
+    assert lib.kda_prefill_launch_count(1, 640, 2, 128, 128, 1, 100) == -1      # below one chunk's records
 
 
 # Fake, suitably aligned device addresses: every call below must be rejected before any CUDA call.
