@@ -35,8 +35,21 @@ if ROOT not in sys.path:
 
 from kda_gated_delta_03_gb300 import inputs as I  # noqa: E402
 
-PREFILL_KERNEL_SRC = ["kda_gated_delta_03_gb300/csrc/kda_prefill_tc.cu"]
-DECODE_KERNEL_SRC = ["kda_gated_delta_03_gb300/csrc/kda_decode.cu"]
+CSRC = "kda_gated_delta_03_gb300/csrc/"
+# sources of each path: the DRAM traffic in profiles/traffic.json is used only while they are unchanged
+PREFILL_2P_SRC = [CSRC + "kda_prefill_2p.cu", CSRC + "kda_tc_util.cuh"]
+PREFILL_TC_SRC = [CSRC + "kda_prefill_tc.cu", CSRC + "kda_tc_util.cuh"]
+DECODE_KERNEL_SRC = [CSRC + "kda_decode.cu"]
+PREFILL_2P_LABEL = "kda_prefill_prep_kernel + kda_prefill_chain_kernel (one call, all windows)"
+PREFILL_TC_LABEL = "kda_order_kernel + kda_prefill_tc_kernel (one call)"
+DECODE_LABEL = "kda_decode_kernel"
+
+
+def prefill_path(N, dtype, dk):
+    """(traffic key, sources, label) of the kernels one kda_prefill call of this shape launches."""
+    if N == 1 and dtype == "bf16" and dk == 128:
+        return "prefill_2p", PREFILL_2P_SRC, PREFILL_2P_LABEL
+    return "prefill_tc", PREFILL_TC_SRC, PREFILL_TC_LABEL
 METRIC = "KDA prefill tokens/s (H=32,d=128); decode steps/s and state HBM GB/s vs peak"
 
 
@@ -92,13 +105,14 @@ def source_sha(paths) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kind: str, paths):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+def ncu_traffic(kind: str, paths, workload: str):
+    """DRAM bytes per timed launch from the committed ncu summary, if it was taken on the current kernel
+    source and on this workload."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     entry = json.load(open(path)).get(kind)
-    if not entry or entry.get("source_sha") != source_sha(paths):
+    if not entry or entry.get("source_sha") != source_sha(paths) or entry.get("workload_key") != workload:
         return None
     return entry.get("bytes_per_launch")
 
@@ -309,11 +323,12 @@ def prefill_workload_inputs(name):
     return w, I.prefill_inputs(w["seqlens"], w["H"], w["dk"], w["dv"], w["dtype"], w["seed"], state=w["state"])
 
 
-def roofline_obj(alg_bytes, kernel_ms, peaks, kind, src):
+def roofline_obj(alg_bytes, kernel_ms, peaks, kind, src, label, workload):
+    """HBM roofline of the timed launch sequence: algorithmic bytes / CUDA-event time per call."""
     achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(kind, src),
-            "alg_bytes_per_launch": int(alg_bytes), "kernel_ms": round(kernel_ms, 4),
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(kind, src, workload),
+            "kernel": label, "alg_bytes_per_launch": int(alg_bytes), "kernel_ms": round(kernel_ms, 4),
             "peak_source": peaks["source"]}
 
 
@@ -340,7 +355,8 @@ def run_ours(args, rank, world, local_rank):
                     unit="steps/s", ms_per_step=round(ms, 4), dtype="f32",
                     config={"workload": name, "B": w["B"], "H": w["H"], "d": w["dk"], "qkv": w["dtype"],
                             "l2": "state pool (1 GiB) larger than L2"},
-                    roofline=roofline_obj(r["bytes_per_step"], r["kernel_ms"], peaks, "decode", DECODE_KERNEL_SRC),
+                    roofline=roofline_obj(r["bytes_per_step"], r["kernel_ms"], peaks, "decode", DECODE_KERNEL_SRC,
+                                          DECODE_LABEL, name),
                     gpu_launches=r["launches"], clocks=clk.summary())
         return line
 
@@ -358,7 +374,7 @@ def run_ours(args, rank, world, local_rank):
     line.update(value=round(world * tokens * 1e3 / ms, 1), unit="tokens/s", ms_per_step=round(ms, 4), dtype="f32",
                 config={"workload": name, "seqs": r["N"], "tokens": tokens, "H": r["H"], "d": inp["dk"],
                         "qkv": inp["dtype"], "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{world}"},
-                roofline=roofline_obj(alg, r["kernel_ms"], peaks, "prefill", PREFILL_KERNEL_SRC),
+                roofline=roofline_obj(alg, r["kernel_ms"], peaks, *prefill_path(r["N"], inp["dtype"], inp["dk"]), name),
                 e2e={"value": round(world * tokens * 1e3 / e2e_ms, 1), "unit": "tokens/s",
                      "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
                 gpu_launches=r["launches"], clocks=clk.summary())
@@ -366,7 +382,8 @@ def run_ours(args, rank, world, local_rank):
         wd = I.workload("decode_512x32")
         rd = gpu_decode(wd, wd["steps"], 3, dev)
         dms = max_over_ranks(rd["ms_per_step"], world)
-        roof = roofline_obj(rd["bytes_per_step"], rd["kernel_ms"], peaks, "decode", DECODE_KERNEL_SRC)
+        roof = roofline_obj(rd["bytes_per_step"], rd["kernel_ms"], peaks, "decode", DECODE_KERNEL_SRC, DECODE_LABEL,
+                            "decode_512x32")
         line["decode"] = {"workload": "decode_512x32", "steps": wd["steps"], "steps_per_s": round(world * 1e3 / dms, 2),
                           "tokens_per_s": round(world * wd["B"] * 1e3 / dms, 1), "ms_per_step": round(dms, 4),
                           "state_hbm_gbs": roof["achieved"], "roofline": roof, "gpu_launches": rd["launches"]}
@@ -406,12 +423,13 @@ def run_append(args, w, dev, peaks, line, world, local_rank):
                 value=round(world * T1 * 1e3 / ms1, 1), unit="tokens/s", ms_per_step=round(ms1, 4), dtype="f32",
                 config={"workload": "append_1m", "prefill_tokens": T1, "append_tokens": T2, "H": w["H"],
                         "d": w["dk"], "l2": "inputs larger than L2 (no flush)"},
-                roofline=roofline_obj(alg1, r1["kernel_ms"], peaks, "prefill", PREFILL_KERNEL_SRC),
+                roofline=roofline_obj(alg1, r1["kernel_ms"], peaks, *prefill_path(1, "bf16", w["dk"]), "append_1m"),
                 e2e={"value": round(world * T1 * 1e3 / r1["e2e_ms"], 1), "unit": "tokens/s",
                      "h2d_bytes_per_step": r1["h2d"], "d2h_bytes_per_step": r1["d2h"]},
                 append={"tokens_per_s": round(world * T2 * 1e3 / ms2, 1), "ms_per_step": round(ms2, 4),
                         "roofline": roofline_obj(prefill_bytes(T2, w["H"], w["dk"], w["dv"], 2, 1, 1),
-                                                 r2["kernel_ms"], peaks, "prefill", PREFILL_KERNEL_SRC)},
+                                                 r2["kernel_ms"], peaks, *prefill_path(1, "bf16", w["dk"]),
+                                                 "append_1m/append")},
                 gpu_launches=r1["launches"] + r2["launches"], clocks=clk.summary())
     return line
 
