@@ -190,9 +190,9 @@ def prefill_bytes(tokens: int, H: int, dk: int, dv: int, esize: int, n_states_in
     return tokens * H * per_token_head + (n_states_in + n_states_out) * H * dk * dv * 4
 
 
-def decode_bytes_per_step(B: int, H: int, d: int, esize: int) -> int:
+def decode_bytes_per_step(B: int, H: int, d: int, esize: int, state_esize: int = 4) -> int:
     """Algorithmic HBM bytes of one decode step: state read + write, q, k, v, o, alpha, beta."""
-    return B * H * (2 * d * d * 4 + 4 * d * esize + 4 * d + 4)
+    return B * H * (2 * d * d * state_esize + 4 * d * esize + 4 * d + 4)
 
 
 def gpu_prefill(inp, steps, warmup, dev, e2e_steps):
@@ -263,13 +263,14 @@ def gpu_prefill(inp, steps, warmup, dev, e2e_steps):
                 d2h=d2h, launches=steps * launches_per_call, T=T, H=H, N=N)
 
 
-def gpu_decode(w, steps, warmup, dev, distinct=16):
-    """Batched decode: `steps` fused steps over the resident pool; step s uses input set s mod `distinct`."""
+def gpu_decode(w, steps, warmup, dev, distinct=16, state_dtype="f32"):
+    """Batched decode: `steps` fused steps over the resident pool; step s uses input set s mod `distinct`.
+    state_dtype "bf16" runs the bf16-stored state (kda_decode_step_bf16_state)."""
     import torch
     import kda_gated_delta_03_gb300 as kda
     B, H, d, dt = w["B"], w["H"], w["dk"], w["dtype"]
     bf = dt == "bf16"
-    pool = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    pool = torch.empty((B, H, d, d), dtype=torch.bfloat16 if state_dtype == "bf16" else torch.float32, device=dev)
     for b0 in range(0, B, 64):   # seeded N(0, 0.02) states, generated in slices to bound host memory
         pool[b0:b0 + 64] = to_dev(I.random_state(min(64, B - b0), H, d, d, (w["seed"], b0)), dev=dev)
     sets = []
@@ -298,7 +299,7 @@ def gpu_decode(w, steps, warmup, dev, distinct=16):
     total_ms = start.elapsed_time(end)
     kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     return dict(total_ms=total_ms, ms_per_step=total_ms / steps, kernel_ms=kernel_ms, launches=steps,
-                bytes_per_step=decode_bytes_per_step(B, H, d, 2 if bf else 4))
+                bytes_per_step=decode_bytes_per_step(B, H, d, 2 if bf else 4, 2 if state_dtype == "bf16" else 4))
 
 
 # ----------------------------------------------------------------------------
@@ -344,17 +345,19 @@ def run_ours(args, rank, world, local_rank):
     name = args.workload
     line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic"}
-    if name == "decode_512x32":
-        w = I.workload(name)
+    if name in ("decode_512x32", "decode_512x32_bf16_state"):
+        sdt = "bf16" if name.endswith("bf16_state") else "f32"
+        w = I.workload("decode_512x32")
         barrier(world)
         with ClockSampler(local_rank) as clk:
-            r = gpu_decode(w, args.steps, args.warmup, dev)
+            r = gpu_decode(w, args.steps, args.warmup, dev, state_dtype=sdt)
         ms = max_over_ranks(r["ms_per_step"], world)
         steps_s = world * 1e3 / ms
         line.update(metric="KDA decode steps/s (512 seqs x 32 heads, d=128)", value=round(steps_s, 2),
                     unit="steps/s", ms_per_step=round(ms, 4), dtype="f32",
                     config={"workload": name, "B": w["B"], "H": w["H"], "d": w["dk"], "qkv": w["dtype"],
-                            "l2": "state pool (1 GiB) larger than L2"},
+                            "state": "bf16" if sdt == "bf16" else "f32",
+                            "l2": f"state pool ({'0.5' if sdt == 'bf16' else '1'} GiB) larger than L2"},
                     roofline=roofline_obj(r["bytes_per_step"], r["kernel_ms"], peaks, "decode", DECODE_KERNEL_SRC,
                                           DECODE_LABEL, name),
                     gpu_launches=r["launches"], clocks=clk.summary())
@@ -388,6 +391,16 @@ def run_ours(args, rank, world, local_rank):
                           "tokens_per_s": round(world * wd["B"] * 1e3 / dms, 1), "ms_per_step": round(dms, 4),
                           "state_hbm_gbs": roof["achieved"], "roofline": roof, "gpu_launches": rd["launches"]}
         line["gpu_launches"] += rd["launches"]
+        rb = gpu_decode(wd, wd["steps"], 3, dev, state_dtype="bf16")
+        bms = max_over_ranks(rb["ms_per_step"], world)
+        roofb = roofline_obj(rb["bytes_per_step"], rb["kernel_ms"], peaks, "decode_bf16", DECODE_KERNEL_SRC,
+                             DECODE_LABEL + " (bf16 state)", "decode_512x32_bf16_state")
+        line["decode_bf16_state"] = {"workload": "decode_512x32, state stored in bf16", "steps": wd["steps"],
+                                     "steps_per_s": round(world * 1e3 / bms, 2),
+                                     "tokens_per_s": round(world * wd["B"] * 1e3 / bms, 1),
+                                     "ms_per_step": round(bms, 4), "state_hbm_gbs": roofb["achieved"],
+                                     "roofline": roofb, "gpu_launches": rb["launches"]}
+        line["gpu_launches"] += rb["launches"]
     if rank == 0 and not args.no_cpu_baseline:
         threads = cpu_threads()
         secs = oracle_prefill_time(inp, threads)
@@ -486,7 +499,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_8k",
-                    choices=["prefill_8k", "varlen_64", "decode_512x32", "append_1m"])
+                    choices=["prefill_8k", "varlen_64", "decode_512x32", "decode_512x32_bf16_state", "append_1m"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -152,6 +152,21 @@ KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, 
                            int32_t d_v, kda_dtype dt, float scale, void* stream);
 
 /*
+ * kda_decode_step on a state pool stored in bf16 ([num_slots, H, d_k, d_v]
+ * bf16, updated in place): each state is read as bf16, updated in float32 and
+ * written back rounded to nearest-even bf16.  The pages size the recurrent
+ * state at 2 bytes per element ("Kimi K3 changed the memory math for agentic
+ * AI forever", section "Linear Attention's Promise"), which halves the decode
+ * step's state traffic.  Every other argument, result and error is kda_decode_step's.  The
+ * state carries bf16 rounding from step to step, so results agree with the
+ * float32-state step only to bf16 precision.
+ */
+KDA_API kda_status kda_decode_step_bf16_state(const void* q, const void* k, const void* v, const float* beta,
+                                      const float* alpha, void* state, const int32_t* state_idx,
+                                      int32_t num_slots, void* o, int32_t B, int32_t H, int32_t d_k,
+                                      int32_t d_v, kda_dtype dt, float scale, void* stream);
+
+/*
  * kda_prefill without a workspace argument, for callers that cannot allocate
  * device memory.  (The pages have no counterpart; this is an interface
  * convenience.)  Typical callers: a serving process whose memory manager has

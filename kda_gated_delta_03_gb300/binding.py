@@ -30,6 +30,8 @@ SIGNATURES = {
                                    _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "kda_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                        ctypes.c_int, _f32, _vp]),
+    "kda_decode_step_bf16_state": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
+                                                  _i32, ctypes.c_int, _f32, _vp]),
     "kda_prefill_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
                                            ctypes.c_int, _f32, _vp, _vp, _vp, _vp]),
     "kda_get_device_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
@@ -185,7 +187,8 @@ def kda_prefill_noalloc(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scal
 
 
 def kda_decode_step(q, k, v, beta, alpha, state, state_idx=None, *, scale: float = 1.0, o=None, stream=None):
-    """One fused decode step; updates `state` ([P, H, d_k, d_v] f32) in place and returns o [B, H, d_v]."""
+    """One fused decode step; updates `state` ([P, H, d_k, d_v] f32, or bf16 for the bf16-stored state) in
+    place and returns o [B, H, d_v]."""
     L = load()
     B, H, dk = q.shape
     dv = v.shape[2]
@@ -196,16 +199,18 @@ def kda_decode_step(q, k, v, beta, alpha, state, state_idx=None, *, scale: float
     _check("v", v, q.dtype, (B, H, dv), dev)
     _check("beta", beta, torch.float32, (B, H), dev)
     _check("alpha", alpha, torch.float32, (B, H, dk), dev)
-    _check("state", state, torch.float32, (P, H, dk, dv), dev)
+    bf16_state = state.dtype == torch.bfloat16
+    _check("state", state, torch.bfloat16 if bf16_state else torch.float32, (P, H, dk, dv), dev)
     if state_idx is not None:
         _check("state_idx", state_idx, torch.int32, (B,), dev)
     if o is None:
         o = torch.empty((B, H, dv), dtype=q.dtype, device=dev)
     _check("o", o, q.dtype, (B, H, dv), dev)
-    rc = L.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(state), _ptr(state_idx), P,
-                           _ptr(o), B, H, dk, dv, _dt(q.dtype), float(scale), _stream(stream))
+    name = "kda_decode_step_bf16_state" if bf16_state else "kda_decode_step"
+    rc = getattr(L, name)(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(state), _ptr(state_idx), P,
+                          _ptr(o), B, H, dk, dv, _dt(q.dtype), float(scale), _stream(stream))
     if rc != KDA_OK:
-        raise KdaError("kda_decode_step", rc)
+        raise KdaError(name, rc)
     return o
 
 

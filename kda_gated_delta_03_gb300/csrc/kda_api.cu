@@ -167,10 +167,13 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
     return KDA_OK;
 }
 
-kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* beta,
-                           const float* alpha, float* state, const int32_t* state_idx,
-                           int32_t num_slots, void* o, int32_t B, int32_t H, int32_t d_k,
-                           int32_t d_v, kda_dtype dt, float scale, void* stream) {
+}  // extern "C"
+
+namespace {
+
+kda_status decode_impl(const void* q, const void* k, const void* v, const float* beta, const float* alpha,
+                       void* state, bool state_bf16, const int32_t* state_idx, int32_t num_slots, void* o, int32_t B,
+                       int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, float scale, void* stream) {
     if (B < 0 || H <= 0 || d_k <= 0 || d_v <= 0 || num_slots < 0 || !std::isfinite(scale))
         return KDA_ERR_INVALID_ARG;
     if (dt != KDA_DTYPE_F32 && dt != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
@@ -187,10 +190,30 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const fl
     if (error_word(&err) != KDA_OK) return KDA_ERR_CUDA;
     kda::DecodeParams p{};
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.alpha = alpha;
-    p.state = state; p.state_idx = state_idx; p.num_slots = num_slots;
+    p.state = state; p.state_bf16 = state_bf16; p.state_idx = state_idx; p.num_slots = num_slots;
     p.o = o; p.B = B; p.H = H; p.d = d_k; p.scale = scale; p.err = err;
     if (kda::launch_decode(p, dt, s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* beta,
+                           const float* alpha, float* state, const int32_t* state_idx,
+                           int32_t num_slots, void* o, int32_t B, int32_t H, int32_t d_k,
+                           int32_t d_v, kda_dtype dt, float scale, void* stream) {
+    return decode_impl(q, k, v, beta, alpha, state, false, state_idx, num_slots, o, B, H, d_k, d_v, dt, scale,
+                       stream);
+}
+
+kda_status kda_decode_step_bf16_state(const void* q, const void* k, const void* v, const float* beta,
+                                      const float* alpha, void* state, const int32_t* state_idx,
+                                      int32_t num_slots, void* o, int32_t B, int32_t H, int32_t d_k,
+                                      int32_t d_v, kda_dtype dt, float scale, void* stream) {
+    return decode_impl(q, k, v, beta, alpha, state, true, state_idx, num_slots, o, B, H, d_k, d_v, dt, scale,
+                       stream);
 }
 
 kda_status kda_prefill_noalloc(const void* q, const void* k, const void* v, const float* beta,

@@ -10,9 +10,9 @@
 //   S_ij <- alpha_i S_ij + k_i delta_j     (decay + erase + write, in place)
 //   o_j = scale (y_j + (q . k) delta_j)    (= scale * S_new^T q)
 //
-// The state is read from HBM once and written once.  Each CTA owns one
-// (sequence, head) state: a warp reads whole 512-byte rows with 128-bit
-// streaming loads, so every thread holds D*D/NT floats in registers across the
+// The state is read from HBM once and written once, as float32 or (kda_decode_step_bf16_state) as
+// bf16.  Each CTA owns one (sequence, head) state: a warp reads whole rows with 128-bit
+// streaming loads, so every thread holds D*D/NT values in registers across the
 // two reductions over the key channels (partial sums in registers, then across
 // row groups through shared memory), and writes the updated rows back with
 // streaming stores.
@@ -22,9 +22,40 @@
 namespace kda {
 namespace {
 
-template <int D, int NT, typename TIn>
+// State storage: float, or bf16 (read as bf16, updated in fp32, rounded to nearest-even on the way back).
+// One 16-byte access holds VEC state elements of a row.
+template <typename TS> struct StateIO;
+template <> struct StateIO<float> {
+    static constexpr int VEC = 4;
+    __device__ static void load(const float* p, float* v) {
+        const float4 t = __ldcs(reinterpret_cast<const float4*>(p));
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    }
+    __device__ static void store(float* p, const float* v) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+    }
+};
+template <> struct StateIO<__nv_bfloat16> {
+    static constexpr int VEC = 8;
+    __device__ static void load(const __nv_bfloat16* p, float* v) {
+        const uint4 t = __ldcs(reinterpret_cast<const uint4*>(p));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&t);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { v[2 * i] = __low2float(h[i]); v[2 * i + 1] = __high2float(h[i]); }
+    }
+    __device__ static void store(__nv_bfloat16* p, const float* v) {
+        uint4 t;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&t);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        __stcs(reinterpret_cast<uint4*>(p), t);
+    }
+};
+
+template <int D, int NT, typename TIn, typename TS>
 __global__ void __launch_bounds__(NT, (D == 128 ? 2 : 4)) kda_decode_kernel(DecodeParams p) {
-    constexpr int LPR = D / 4;          // float4 column groups per row
+    constexpr int VEC = StateIO<TS>::VEC;
+    constexpr int LPR = D / VEC;        // 16-byte column groups per row
     constexpr int RPP = NT / LPR;       // rows per pass
     constexpr int PASSES = D / RPP;     // passes over the rows
     static_assert(NT % LPR == 0 && D % RPP == 0, "bad decode tiling");
@@ -42,15 +73,14 @@ __global__ void __launch_bounds__(NT, (D == 128 ? 2 : 4)) kda_decode_kernel(Deco
         if (tid == 0) atomicOr(p.err, KDA_DEVERR_STATE_IDX);
         return;
     }
-    float* S = p.state + ((int64_t)slot * p.H + h) * (int64_t)(D * D);
+    TS* S = static_cast<TS*>(p.state) + ((int64_t)slot * p.H + h) * (int64_t)(D * D);
     const int cg = tid % LPR;
     const int rg = tid / LPR;
 
     // 1. issue every state load of this thread before anything else
-    float4 s[PASSES];
+    float s[PASSES][VEC];
 #pragma unroll
-    for (int m = 0; m < PASSES; ++m)
-        s[m] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rg + RPP * m) * D) + cg);
+    for (int m = 0; m < PASSES; ++m) StateIO<TS>::load(S + (int64_t)(rg + RPP * m) * D + cg * VEC, s[m]);
 
     // 2. stage q, k, alpha of this (sequence, head)
     const int64_t row = (int64_t)b * p.H + h;
@@ -64,18 +94,24 @@ __global__ void __launch_bounds__(NT, (D == 128 ? 2 : 4)) kda_decode_kernel(Deco
     __syncthreads();
 
     // 3. partial reductions over this thread's rows
-    float4 px = make_float4(0.f, 0.f, 0.f, 0.f), py = px;
+    float px[VEC], py[VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) px[c] = py[c] = 0.f;
 #pragma unroll
     for (int m = 0; m < PASSES; ++m) {
         const int r = rg + RPP * m;
         const float ak = sa[r] * sk[r], aq = sa[r] * sq[r];
-        px.x = fmaf(ak, s[m].x, px.x); px.y = fmaf(ak, s[m].y, px.y);
-        px.z = fmaf(ak, s[m].z, px.z); px.w = fmaf(ak, s[m].w, px.w);
-        py.x = fmaf(aq, s[m].x, py.x); py.y = fmaf(aq, s[m].y, py.y);
-        py.z = fmaf(aq, s[m].z, py.z); py.w = fmaf(aq, s[m].w, py.w);
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+            px[c] = fmaf(ak, s[m][c], px[c]);
+            py[c] = fmaf(aq, s[m][c], py[c]);
+        }
     }
-    reinterpret_cast<float4*>(sx[rg])[cg] = px;
-    reinterpret_cast<float4*>(sy[rg])[cg] = py;
+#pragma unroll
+    for (int c = 0; c < VEC; c += 4) {
+        reinterpret_cast<float4*>(sx[rg] + cg * VEC)[c / 4] = make_float4(px[c], px[c + 1], px[c + 2], px[c + 3]);
+        reinterpret_cast<float4*>(sy[rg] + cg * VEC)[c / 4] = make_float4(py[c], py[c + 1], py[c + 2], py[c + 3]);
+    }
     if (tid < 32) {
         float acc = 0.f;
         for (int i = tid; i < D; i += 32) acc = fmaf(sq[i], sk[i], acc);
@@ -100,27 +136,137 @@ __global__ void __launch_bounds__(NT, (D == 128 ? 2 : 4)) kda_decode_kernel(Deco
     __syncthreads();
 
     // 5. decay + erase + write, streamed back in place
-    const float4 d4 = reinterpret_cast<const float4*>(sdelta)[cg];
+    float dl[VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) dl[c] = sdelta[cg * VEC + c];
 #pragma unroll
     for (int m = 0; m < PASSES; ++m) {
         const int r = rg + RPP * m;
         const float a = sa[r], kk = sk[r];
-        float4 n;
-        n.x = fmaf(kk, d4.x, a * s[m].x);
-        n.y = fmaf(kk, d4.y, a * s[m].y);
-        n.z = fmaf(kk, d4.z, a * s[m].z);
-        n.w = fmaf(kk, d4.w, a * s[m].w);
-        __stcs(reinterpret_cast<float4*>(S + (int64_t)r * D) + cg, n);
+        float n[VEC];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) n[c] = fmaf(kk, dl[c], a * s[m][c]);
+        StateIO<TS>::store(S + (int64_t)r * D + cg * VEC, n);
     }
 }
 
-template <typename TIn>
+// bf16-stored state: the same step with the state kept packed (two bf16 per 32-bit register) between
+// the reductions and the write-back, so that one thread can hold twice the elements and a CTA of 128
+// threads covers a 128 x 128 state (three CTAs per SM keep enough loads in flight).
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int D, int NT, typename TIn>
+__global__ void __launch_bounds__(NT, 3) kda_decode_bf16s_kernel(DecodeParams p) {
+    constexpr int LPR = D / 8;          // 16-byte (8-element) column groups per row
+    constexpr int RPP = NT / LPR;       // rows per pass
+    constexpr int PASSES = D / RPP;
+    static_assert(NT % LPR == 0 && D % RPP == 0, "bad decode tiling");
+
+    __shared__ float sq[D], sk[D], sa[D], sdelta[D];
+    __shared__ float sx[RPP][D], sy[RPP][D];
+    __shared__ float s_qk;
+
+    const int tid = threadIdx.x;
+    const int bh = blockIdx.x;
+    const int b = bh / p.H;
+    const int h = bh - b * p.H;
+    const int slot = p.state_idx ? p.state_idx[b] : b;
+    if (slot < 0 || slot >= p.num_slots) {
+        if (tid == 0) atomicOr(p.err, KDA_DEVERR_STATE_IDX);
+        return;
+    }
+    __nv_bfloat16* S = static_cast<__nv_bfloat16*>(p.state) + ((int64_t)slot * p.H + h) * (int64_t)(D * D);
+    const int cg = tid % LPR;
+    const int rg = tid / LPR;
+
+    uint4 s[PASSES];
+#pragma unroll
+    for (int m = 0; m < PASSES; ++m)
+        s[m] = __ldcs(reinterpret_cast<const uint4*>(S + (int64_t)(rg + RPP * m) * D) + cg);
+
+    const int64_t row = (int64_t)b * p.H + h;
+    const TIn* q = static_cast<const TIn*>(p.q);
+    const TIn* k = static_cast<const TIn*>(p.k);
+    for (int i = tid; i < D; i += NT) {
+        sq[i] = load_as_float(q, row * D + i);
+        sk[i] = load_as_float(k, row * D + i);
+        sa[i] = p.alpha[row * D + i];
+    }
+    __syncthreads();
+
+    float px[8], py[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) px[c] = py[c] = 0.f;
+#pragma unroll
+    for (int m = 0; m < PASSES; ++m) {
+        const int r = rg + RPP * m;
+        const float ak = sa[r] * sk[r], aq = sa[r] * sq[r];
+        const uint32_t w[4] = {s[m].x, s[m].y, s[m].z, s[m].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float lo = bf_lo(w[c]), hi = bf_hi(w[c]);
+            px[2 * c] = fmaf(ak, lo, px[2 * c]);
+            px[2 * c + 1] = fmaf(ak, hi, px[2 * c + 1]);
+            py[2 * c] = fmaf(aq, lo, py[2 * c]);
+            py[2 * c + 1] = fmaf(aq, hi, py[2 * c + 1]);
+        }
+    }
+    reinterpret_cast<float4*>(sx[rg] + cg * 8)[0] = make_float4(px[0], px[1], px[2], px[3]);
+    reinterpret_cast<float4*>(sx[rg] + cg * 8)[1] = make_float4(px[4], px[5], px[6], px[7]);
+    reinterpret_cast<float4*>(sy[rg] + cg * 8)[0] = make_float4(py[0], py[1], py[2], py[3]);
+    reinterpret_cast<float4*>(sy[rg] + cg * 8)[1] = make_float4(py[4], py[5], py[6], py[7]);
+    if (tid < 32) {
+        float acc = 0.f;
+        for (int i = tid; i < D; i += 32) acc = fmaf(sq[i], sk[i], acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (tid == 0) s_qk = acc;
+    }
+    __syncthreads();
+
+    const float beta = p.beta[row];
+    const TIn* v = static_cast<const TIn*>(p.v);
+    TIn* o = static_cast<TIn*>(p.o);
+    for (int j = tid; j < D; j += NT) {
+        float x = 0.f, y = 0.f;
+#pragma unroll
+        for (int g = 0; g < RPP; ++g) { x += sx[g][j]; y += sy[g][j]; }
+        const float delta = beta * (load_as_float(v, row * D + j) - x);
+        sdelta[j] = delta;
+        store_from_float(o, row * D + j, p.scale * fmaf(s_qk, delta, y));
+    }
+    __syncthreads();
+
+    float dl[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) dl[c] = sdelta[cg * 8 + c];
+#pragma unroll
+    for (int m = 0; m < PASSES; ++m) {
+        const int r = rg + RPP * m;
+        const float a = sa[r], kk = sk[r];
+        const uint32_t w[4] = {s[m].x, s[m].y, s[m].z, s[m].w};
+        uint32_t n[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const __nv_bfloat162 t = __floats2bfloat162_rn(fmaf(kk, dl[2 * c], a * bf_lo(w[c])),
+                                                           fmaf(kk, dl[2 * c + 1], a * bf_hi(w[c])));
+            n[c] = *reinterpret_cast<const uint32_t*>(&t);
+        }
+        __stcs(reinterpret_cast<uint4*>(S + (int64_t)r * D) + cg, make_uint4(n[0], n[1], n[2], n[3]));
+    }
+}
+
+template <typename TIn, typename TS>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
     const unsigned grid = (unsigned)((int64_t)p.B * p.H);
     switch (p.d) {
-        case 128: kda_decode_kernel<128, 256, TIn><<<grid, 256, 0, s>>>(p); break;
-        case 64: kda_decode_kernel<64, 64, TIn><<<grid, 64, 0, s>>>(p); break;
-        case 16: kda_decode_kernel<16, 32, TIn><<<grid, 32, 0, s>>>(p); break;
+        case 128:
+            if (p.state_bf16) kda_decode_bf16s_kernel<128, 128, TIn><<<grid, 128, 0, s>>>(p);
+            else kda_decode_kernel<128, 256, TIn, TS><<<grid, 256, 0, s>>>(p);
+            break;
+        case 64: kda_decode_kernel<64, 64, TIn, TS><<<grid, 64, 0, s>>>(p); break;
+        case 16: kda_decode_kernel<16, 32, TIn, TS><<<grid, 32, 0, s>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -129,7 +275,10 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, kda_dtype dt, cudaStream_t s) {
-    return dt == KDA_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16>(p, s) : launch_decode_t<float>(p, s);
+    if (p.state_bf16)
+        return dt == KDA_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16, __nv_bfloat16>(p, s)
+                                    : launch_decode_t<float, __nv_bfloat16>(p, s);
+    return dt == KDA_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16, float>(p, s) : launch_decode_t<float, float>(p, s);
 }
 
 }  // namespace kda

@@ -40,7 +40,8 @@ struct DecodeParams {
     const void* v;
     const float* beta;
     const float* alpha;
-    float* state;
+    void* state;                 // float, or bf16 when state_bf16
+    bool state_bf16;
     const int32_t* state_idx;    // may be nullptr
     int32_t num_slots;
     void* o;

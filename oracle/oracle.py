@@ -134,9 +134,23 @@ def prefill(inp: dict, scale: float = 1.0, erase: bool = True, threads: int | No
     return o, st
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Nearest bf16 number (ties to even) of each float64 value, as float64.  The value is first rounded to
+    float32 (nearest); bf16 keeps the top 16 bits of a float32, so the low 16 bits are rounded away with
+    the usual add-half-minus-one-plus-lsb carry."""
+    f = np.ascontiguousarray(x, dtype=np.float64).astype(np.float32)
+    bits = f.view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x7FFF + ((bits >> 16) & 1)) & 0xFFFF0000
+    return bits.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def decode_step(step: dict, pool: np.ndarray, state_idx=None, scale: float = 1.0,
-                threads: int | None = None, mutant: int | None = None) -> np.ndarray:
-    """One decode step on a float64 state pool [P, H, d_k, d_v], updated in place; returns o [B, H, d_v]."""
+                threads: int | None = None, mutant: int | None = None, state_dtype: str = "f32") -> np.ndarray:
+    """One decode step on a float64 state pool [P, H, d_k, d_v], updated in place; returns o [B, H, d_v].
+
+    state_dtype "bf16" models a pool stored in bf16: after the step each updated state is rounded to the
+    nearest bf16 (ties to even), as storing it in 2 bytes per element does ("Kimi K3 changed the memory
+    math for agentic AI forever", section "Linear Attention's Promise", sizes the state at 2 bytes)."""
     _check_token_arrays(step)
     if pool.dtype != np.float64 or not pool.flags["C_CONTIGUOUS"]:
         raise ValueError("pool must be a C-contiguous float64 array")
@@ -161,4 +175,9 @@ def decode_step(step: dict, pool: np.ndarray, state_idx=None, scale: float = 1.0
     else:
         with ThreadPoolExecutor(nt) as ex:
             list(ex.map(run, range(nt)))
+    if state_dtype == "bf16":
+        slots = np.arange(B) if idx is None else idx
+        pool[slots] = round_bf16(pool[slots])
+    elif state_dtype != "f32":
+        raise ValueError("state_dtype must be f32 or bf16")
     return o

@@ -86,12 +86,12 @@ def prefill(lib, **over):
                            a["stream"])
 
 
-def decode(lib, **over):
+def decode(lib, fn="kda_decode_step", **over):
     a = dict(q=P, k=P, v=P, beta=P, alpha=P, state=P, idx=None, slots=4, o=P, B=4, H=2, dk=16, dv=16, dt=1,
              scale=1.0, stream=None)
     a.update(over)
-    return lib.kda_decode_step(a["q"], a["k"], a["v"], a["beta"], a["alpha"], a["state"], a["idx"], a["slots"],
-                               a["o"], a["B"], a["H"], a["dk"], a["dv"], a["dt"], a["scale"], a["stream"])
+    return getattr(lib, fn)(a["q"], a["k"], a["v"], a["beta"], a["alpha"], a["state"], a["idx"], a["slots"],
+                            a["o"], a["B"], a["H"], a["dk"], a["dv"], a["dt"], a["scale"], a["stream"])
 
 
 @pytest.mark.parametrize("over,code", [
@@ -138,3 +138,15 @@ def test_prefill_host_validation(lib, over, code):
 ])
 def test_decode_host_validation(lib, over, code):
     assert decode(lib, **over) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(H=0), binding.KDA_ERR_INVALID_ARG),
+    (dict(dk=48, dv=48), binding.KDA_ERR_UNSUPPORTED),
+    (dict(state=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(state=ctypes.c_void_p(0x10008)), binding.KDA_ERR_INVALID_ARG),
+    (dict(slots=3), binding.KDA_ERR_INVALID_ARG),
+    (dict(B=0), binding.KDA_OK),
+])
+def test_decode_bf16_state_host_validation(lib, over, code):
+    assert decode(lib, "kda_decode_step_bf16_state", **over) == code

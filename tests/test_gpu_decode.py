@@ -11,11 +11,15 @@ from kda_testutil import TOL, rel_frob, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def run_steps(B, H, d, dtype, steps, seed, P=None, idx=None, decay="config"):
+def run_steps(B, H, d, dtype, steps, seed, P=None, idx=None, decay="config", state_dtype="f32"):
     import kda_gated_delta_03_gb300 as kda
     P = P or B
     pool = I.random_state(P, H, d, d, seed)
-    pool_d = to_dev(pool)
+    if state_dtype == "bf16":                         # a bf16 pool: the same seeded values, stored in 2 bytes
+        pool = I.bf16_bits_to_f32(I.f32_to_bf16_bits(pool))
+        pool_d = to_dev(I.f32_to_bf16_bits(pool), True)
+    else:
+        pool_d = to_dev(pool)
     pool64 = pool.astype(np.float64)
     idx_d = None if idx is None else to_dev(np.asarray(idx, np.int32))
     bf = dtype == "bf16"
@@ -25,7 +29,7 @@ def run_steps(B, H, d, dtype, steps, seed, P=None, idx=None, decay="config"):
         o = kda.kda_decode_step(*(to_dev(st[n], bf) for n in ("q", "k", "v")), to_dev(st["beta"]),
                                 to_dev(st["alpha"]), pool_d, idx_d)
         os_gpu.append(o.double().cpu().numpy())
-        os_ref.append(O.decode_step(st, pool64, idx))
+        os_ref.append(O.decode_step(st, pool64, idx, state_dtype=state_dtype))
     torch.cuda.synchronize()
     return np.stack(os_gpu), np.stack(os_ref), pool_d.double().cpu().numpy(), pool64
 
@@ -73,3 +77,24 @@ def test_decode_equals_prefill_of_one_token():
     torch.cuda.synchronize()
     assert rel_frob(o_dec.cpu().numpy(), o_pre.cpu().numpy()) <= 1e-5
     assert rel_frob(pool_d.cpu().numpy(), s_pre.cpu().numpy()) <= 1e-5
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 64, 128])
+def test_decode_steps_bf16_state(dtype, d):
+    """kda_decode_step_bf16_state against the oracle's bf16-stored state (rounded to nearest-even bf16
+    after every step), over 8 steps."""
+    o, o_ref, pool, pool_ref = run_steps(5, 3, d, dtype, 8, 80 + d, decay="slow", state_dtype="bf16")
+    assert rel_frob(o, o_ref) <= 3e-3
+    assert rel_frob(pool, pool_ref) <= 3e-3
+    low = pool.astype(np.float32).view(np.uint32) & 0xFFFF
+    assert not low.any()
+
+
+def test_decode_bf16_state_idx_and_untouched_slots():
+    idx = [6, 1, 3, 0]
+    o, o_ref, pool, pool_ref = run_steps(4, 2, 128, "bf16", 3, 51, P=8, idx=idx, state_dtype="bf16")
+    assert rel_frob(o, o_ref) <= 3e-3
+    assert rel_frob(pool, pool_ref) <= 3e-3
+    untouched = [2, 4, 5, 7]
+    assert np.array_equal(pool[untouched], pool_ref[untouched])

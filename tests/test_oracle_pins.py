@@ -273,3 +273,52 @@ def test_decode_entry_matches_one_token_prefill():
         assert np.array_equal(sb[0], pool2[idx[b]])
     untouched = sorted(set(range(P)) - set(idx.tolist()))
     assert np.array_equal(pool2[untouched], pool[untouched])
+
+
+# ---- bf16-stored decode state ----
+
+def test_round_bf16_is_nearest_even_at_eight_significant_bits():
+    """bf16 keeps 8 significant bits: spacing 2^-7 at 1.0.  Halfway cases go to the even neighbour."""
+    x = np.array([1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -8 + 2 ** -20, -(1 + 2 ** -8), 3.0, 2 ** -130,
+                  65504.0, 1 + 2 ** -7])
+    want = np.array([1.0, 1.0, 1 + 2 ** -6, 1 + 2 ** -7, -1.0, 3.0, 0.0, 65536.0, 1 + 2 ** -7])
+    got = O.round_bf16(x)
+    assert np.array_equal(got[np.arange(9) != 6], want[np.arange(9) != 6])
+    assert abs(got[6]) < 2 ** -125                     # below bf16's (and float32's) normal range
+
+
+def test_bf16_state_overwrite_example(golden_dir):
+    """The page's overwrite example with the state stored in bf16: writing (k, a) then (k, b) at beta = 1
+    leaves the key's row equal to b exactly (b is a bf16 number) and the read returns b."""
+    g = json.load(open(os.path.join(golden_dir, "overwrite_example.json")))
+    d = 16
+    pool = np.zeros((1, 1, d, d))
+    for vec in (g["a"], g["b"]):
+        key = np.zeros(d, np.float32)
+        key[g["key_index"]] = 1.0
+        v = np.zeros(d, np.float32)
+        v[:4] = vec
+        step = dict(q=key[None, None].copy(), k=key[None, None].copy(), v=v[None, None].copy(),
+                    beta=np.ones((1, 1), np.float32), alpha=np.ones((1, 1, d), np.float32), dtype="f32", H=1, dk=d,
+                    dv=d)
+        o = O.decode_step(step, pool, state_dtype="bf16")
+    assert np.array_equal(pool[0, 0, g["key_index"], :4], g["b"])
+    assert np.array_equal(o[0, 0, :4], g["delta_read_after_both_writes"])
+
+
+def test_bf16_state_is_stored_in_bf16_and_unchanged_without_a_write():
+    rng = np.random.default_rng(36)
+    B, H, d = 3, 2, 16
+    pool = O.round_bf16(0.3 * rng.standard_normal((B, H, d, d)))
+    step = I.decode_step_inputs(B, H, d, d, "bf16", 37, 0, decay="slow")
+    frozen = dict(step, beta=np.zeros_like(step["beta"]), alpha=np.ones_like(step["alpha"]))
+    p0 = pool.copy()
+    O.decode_step(frozen, p0, state_dtype="bf16")
+    assert np.array_equal(p0, pool)                   # no decay, no write: bit-identical
+    p1 = pool.copy()
+    O.decode_step(step, p1, state_dtype="bf16")
+    low = p1.astype(np.float32).view(np.uint32) & 0xFFFF
+    assert not low.any()                              # every stored value is a bf16 number
+    p2 = pool.copy()
+    O.decode_step(step, p2)                           # the same step with an f64 state
+    assert np.max(np.abs(p1 - p2)) <= 2 ** -8 * np.max(np.abs(p2))
