@@ -71,6 +71,7 @@ typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 #define KDA_DEVERR_CU_SEQLENS 0x1u  /* cu_seqlens not monotone / cu[0] != 0 / cu[N] != total  */
 #define KDA_DEVERR_STATE_IDX 0x2u   /* decode state_idx entry outside [0, num_slots)          */
 #define KDA_DEVERR_TIMEOUT 0x4u     /* a bounded wait inside a kernel gave up (work abandoned) */
+#define KDA_DEVERR_SNAPSHOTS 0x8u   /* snapshot_offsets disagree with the sequence lengths       */
 
 /*
  * Bytes of device workspace kda_prefill needs for this problem (0 is a valid
@@ -129,6 +130,44 @@ KDA_API kda_status kda_prefill(const void* q, const void* k, const void* v, cons
                        int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
                        float scale, const float* state_in, float* state_out, void* o,
                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Options of kda_prefill_ex.  Zero-initialise and set what is used.
+ *
+ * State snapshots ("Kimi K3 changed the memory math for agentic AI forever",
+ * section "But KDA State Is Not Additive": the recurrent state depends on the
+ * whole prefix, so restartable checkpoints and prefix reuse keep copies of it
+ * at fixed token intervals): with snapshot_every > 0, the state of sequence n after its
+ * first (m + 1) * snapshot_every tokens is written to
+ * snapshots[snapshot_offsets[n] + m] for m = 0 .. floor(len_n /
+ * snapshot_every) - 1 (a snapshot at len_n equals that sequence's
+ * state_out).
+ *   snapshot_every    tokens between snapshots: 0, or a positive multiple of 64
+ *   snapshots         [snapshot_offsets[num_seqs], H, d_k, d_v] float32 device
+ *                     buffer, 16-byte aligned
+ *   snapshot_offsets  [num_seqs + 1] int32 device array, non-decreasing, with
+ *                     snapshot_offsets[n + 1] - snapshot_offsets[n] =
+ *                     floor(len_n / snapshot_every); a sequence whose count
+ *                     disagrees gets no snapshots and sets
+ *                     KDA_DEVERR_SNAPSHOTS.
+ */
+typedef struct kda_prefill_options {
+    int32_t snapshot_every;
+    float* snapshots;
+    const int32_t* snapshot_offsets;
+} kda_prefill_options;
+
+/*
+ * kda_prefill with options (NULL options = kda_prefill).  Snapshots add only
+ * their own writes (64 KiB per snapshot and head at d = 128); outputs and
+ * state_out are those of kda_prefill.
+ */
+KDA_API kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const float* beta,
+                          const float* alpha, const int32_t* cu_seqlens, int32_t num_seqs,
+                          int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                          float scale, const float* state_in, float* state_out, void* o,
+                          void* workspace, size_t workspace_bytes, void* stream,
+                          const kda_prefill_options* options);
 
 /*
  * One fused decode step for B sequences, each with H resident states

@@ -21,6 +21,12 @@ KDA_NOALLOC_MAX_SEQS = 16384
 KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
 KDA_DEVERR_CU_SEQLENS, KDA_DEVERR_STATE_IDX = 0x1, 0x2
 
+class PrefillOptions(ctypes.Structure):
+    """kda_prefill_options (include/kda.h)."""
+    _fields_ = [("snapshot_every", ctypes.c_int32), ("snapshots", ctypes.c_void_p),
+                ("snapshot_offsets", ctypes.c_void_p)]
+
+
 # Every function include/kda.h declares, with its ctypes signature.
 _vp, _i32, _i64, _sz, _f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 SIGNATURES = {
@@ -28,6 +34,8 @@ SIGNATURES = {
     "kda_prefill_launch_count": (_i64, [_i32, _i64, _i32, _i32, _i32, ctypes.c_int, _sz]),
     "kda_prefill": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, ctypes.c_int,
                                    _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "kda_prefill_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, ctypes.c_int,
+                                      _f32, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "kda_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                        ctypes.c_int, _f32, _vp]),
     "kda_decode_step_bf16_state": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
@@ -114,11 +122,14 @@ def kda_prefill_launch_count(num_seqs: int, total_tokens: int, H: int, d_k: int,
 
 
 def kda_prefill(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float = 1.0, state_out=None,
-                o=None, workspace=None, stream=None):
+                o=None, workspace=None, stream=None, snapshot_every: int = 0, snapshots=None, snapshot_offsets=None):
     """Chunkwise prefill over packed sequences; returns (o, state_out).
 
     q, k [T, H, d_k], v [T, H, d_v] (bf16 or f32); beta [T, H] f32; alpha [T, H, d_k] f32;
     cu_seqlens [N + 1] int32 (device); state_in [N, H, d_k, d_v] f32 or None.
+    With snapshot_every > 0 (a multiple of 64): snapshots [S, H, d_k, d_v] f32 and snapshot_offsets
+    [N + 1] int32 (device) receive the state of sequence n after each multiple of snapshot_every tokens
+    (kda_prefill_ex).
     """
     L = load()
     T, H, dk = q.shape
@@ -143,11 +154,20 @@ def kda_prefill(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = L.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(cu_seqlens), N, T, H, dk, dv,
-                       _dt(q.dtype), float(scale), _ptr(state_in), _ptr(state_out), _ptr(o), _ptr(workspace),
-                       wbytes, _stream(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(cu_seqlens), N, T, H, dk, dv, _dt(q.dtype),
+            float(scale), _ptr(state_in), _ptr(state_out), _ptr(o), _ptr(workspace), wbytes, _stream(stream))
+    if snapshot_every:
+        S = snapshots.shape[0]
+        _check("snapshots", snapshots, torch.float32, (S, H, dk, dv), dev)
+        _check("snapshot_offsets", snapshot_offsets, torch.int32, (N + 1,), dev)
+        opts = PrefillOptions(int(snapshot_every), _ptr(snapshots), _ptr(snapshot_offsets))
+        rc = L.kda_prefill_ex(*args, ctypes.byref(opts))
+        name = "kda_prefill_ex"
+    else:
+        rc = L.kda_prefill(*args)
+        name = "kda_prefill"
     if rc != KDA_OK:
-        raise KdaError("kda_prefill", rc)
+        raise KdaError(name, rc)
     return o, state_out
 
 

@@ -109,7 +109,22 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
                        int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
                        float scale, const float* state_in, float* state_out, void* o,
                        void* workspace, size_t workspace_bytes, void* stream) {
+    return kda_prefill_ex(q, k, v, beta, alpha, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, dt, scale, state_in,
+                          state_out, o, workspace, workspace_bytes, stream, nullptr);
+}
+
+kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const float* beta,
+                          const float* alpha, const int32_t* cu_seqlens, int32_t num_seqs,
+                          int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                          float scale, const float* state_in, float* state_out, void* o,
+                          void* workspace, size_t workspace_bytes, void* stream,
+                          const kda_prefill_options* options) {
     // ---- host-side validation (no CUDA call before this block ends) ----
+    const int32_t snap_every = options ? options->snapshot_every : 0;
+    if (snap_every < 0 || snap_every % kda::kChunk != 0) return KDA_ERR_INVALID_ARG;
+    if (snap_every > 0 && (!options->snapshots || !options->snapshot_offsets || !aligned(options->snapshots, 16) ||
+                           !aligned(options->snapshot_offsets, 4)))
+        return KDA_ERR_INVALID_ARG;
     if (num_seqs < 0 || total_tokens < 0 || total_tokens > INT32_MAX || H <= 0 || d_k <= 0 ||
         d_v <= 0 || !std::isfinite(scale))
         return KDA_ERR_INVALID_ARG;
@@ -147,6 +162,9 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
     p.scale = scale;
     p.state_in = state_in; p.state_out = state_out; p.o = o;
     p.err = err;
+    p.snap_every = snap_every;
+    p.snapshots = snap_every > 0 ? options->snapshots : nullptr;
+    p.snap_offsets = snap_every > 0 ? options->snapshot_offsets : nullptr;
     if (two_phase) {
         p.slices = 1;
         if (kda::launch_prefill_2p(p, workspace, workspace_bytes, s) != cudaSuccess) return KDA_ERR_CUDA;

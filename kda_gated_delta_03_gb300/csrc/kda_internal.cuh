@@ -32,6 +32,10 @@ struct PrefillParams {
     float* state_out;
     void* o;
     unsigned* err;               // device error word
+    // optional state snapshots: the state after every snap_every tokens of each sequence
+    int32_t snap_every;          // tokens (a multiple of kChunk), 0 = none
+    float* snapshots;            // [snap_offsets[num_seqs], H, dk, dv]
+    const int32_t* snap_offsets; // device [num_seqs + 1]
 };
 
 struct DecodeParams {
@@ -73,6 +77,23 @@ cudaError_t launch_order(const int32_t* cu_seqlens, int32_t num_seqs, int32_t* o
 
 // Number of CUDA-core prefill d_v slices for a head size.
 int prefill_cc_slices(int dv);
+
+// Whether snap_offsets fails to give sequence n (length len) floor(len / snap_every) slots.
+__device__ __forceinline__ bool snapshot_offsets_bad(const PrefillParams& p, int n, int32_t len) {
+    if (p.snap_every <= 0) return false;
+    const int32_t base = p.snap_offsets[n], cnt = p.snap_offsets[n + 1] - base;
+    return base < 0 || cnt != len / p.snap_every;
+}
+
+// Snapshot slot of the state after token t_rel (counted from the start of sequence n, whose length is
+// len), -1 if that point takes none, -2 if snap_offsets is inconsistent for sequence n (nothing is
+// written; snapshot_offsets_bad reports it).
+__device__ __forceinline__ int64_t snapshot_slot(const PrefillParams& p, int n, int32_t t_rel, int32_t len) {
+    if (p.snap_every <= 0 || t_rel <= 0 || t_rel % p.snap_every != 0) return -1;
+    const int32_t base = p.snap_offsets[n], cnt = p.snap_offsets[n + 1] - base;
+    if (base < 0 || cnt != len / p.snap_every) return -2;
+    return (int64_t)base + t_rel / p.snap_every - 1;
+}
 
 __device__ __forceinline__ float load_as_float(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float load_as_float(const __nv_bfloat16* p, int64_t i) {

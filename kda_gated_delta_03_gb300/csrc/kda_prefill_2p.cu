@@ -577,6 +577,7 @@ __global__ void __launch_bounds__(C_NT, 1)
         return;
     }
     const int32_t T = p.total_tokens;
+    if (blockIdx.x == 0 && tid == 0 && c_begin == 0 && snapshot_offsets_bad(p, 0, T)) atomicOr(p.err, KDA_DEVERR_SNAPSHOTS);
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(p.o);
     unsigned char* misc = sm + C_OFF_MISC;
     volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 100);
@@ -754,6 +755,15 @@ __global__ void __launch_bounds__(C_NT, 1)
                 S[4 * m + 1] = fmaf(gamC, S[4 * m + 1], bq[m].y - d[4 * m + 1]);
                 S[4 * m + 2] = fmaf(gamC, S[4 * m + 2], bq[m].z - d[4 * m + 2]);
                 S[4 * m + 3] = fmaf(gamC, S[4 * m + 3], bq[m].w - d[4 * m + 3]);
+            }
+            if (p.snap_every > 0) {                  // the state after this chunk, if a snapshot is due
+                const int64_t slot = snapshot_slot(p, 0, min(T, (c_begin + ci + 1) * C), T);
+                if (slot >= 0) {
+                    float* dst = p.snapshots + ((slot * H + h) * DK + srow) * (int64_t)p.dv + jc;
+#pragma unroll
+                    for (int x = 0; x < CPT; x += 4)
+                        *reinterpret_cast<float4*>(dst + x) = make_float4(S[x], S[x + 1], S[x + 2], S[x + 3]);
+                }
             }
             if (ci + 1 < n_chunks) {
                 // the operand buffer of S_{c+1} was last read by the products of chunk c-1 (obar)

@@ -76,6 +76,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_cc_kernel(PrefillParams p) 
         if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
         return;
     }
+    if (tid == 0 && h == 0 && slice == 0 && snapshot_offsets_bad(p, n, t_end - t_begin))
+        atomicOr(p.err, KDA_DEVERR_SNAPSHOTS);
     const int H = p.H;
     const TIn* gq = static_cast<const TIn*>(p.q);
     const TIn* gk = static_cast<const TIn*>(p.k);
@@ -246,6 +248,17 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_cc_kernel(PrefillParams p) 
         for (int m = 0; m < PER; ++m) {
             const int e = tid + m * NT;
             if (e < DK * NV) sm.S[e] = snew[m];
+        }
+        if (p.snap_every > 0) {                      // the state after this chunk, if a snapshot is due
+            const int64_t slot = snapshot_slot(p, n, t0 + L - t_begin, t_end - t_begin);
+            if (slot >= 0) {
+                float* dst = p.snapshots + (slot * H + h) * DK * (int64_t)p.dv + j0;
+#pragma unroll
+                for (int m = 0; m < PER; ++m) {
+                    const int e = tid + m * NT;
+                    if (e < DK * NV) dst[(int64_t)(e / NV) * p.dv + e % NV] = snew[m];
+                }
+            }
         }
     }
     __syncthreads();

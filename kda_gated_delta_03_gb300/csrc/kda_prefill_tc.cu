@@ -131,6 +131,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
         if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
         return;
     }
+    if (tid == 0 && h == 0 && slice == 0 && snapshot_offsets_bad(p, n, t_end - t_begin))
+        atomicOr(p.err, KDA_DEVERR_SNAPSHOTS);
     const int H = p.H;
     Tile g{p.beta, H, h, j0};
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(p.o);
@@ -675,6 +677,15 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
 #pragma unroll
             for (int j = 0; j < CPT; ++j) S[j] = fmaf(gamC, S[j], dsv[j]);
             write_state_operand();
+            if (p.snap_every > 0) {                  // the state after this chunk, if a snapshot is due
+                const int64_t slot = snapshot_slot(p, n, t0 + L - t_begin, t_end - t_begin);
+                if (slot >= 0) {
+                    float* dst = p.snapshots + ((slot * H + h) * DK + srow) * (int64_t)p.dv + j0 + CPT * half;
+#pragma unroll
+                    for (int j = 0; j < CPT; j += 4)
+                        *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                }
+            }
         }
         fence_async_smem();
         tc_fence_before();

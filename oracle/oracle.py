@@ -181,3 +181,31 @@ def decode_step(step: dict, pool: np.ndarray, state_idx=None, scale: float = 1.0
     elif state_dtype != "f32":
         raise ValueError("state_dtype must be f32 or bf16")
     return o
+
+
+def prefill_snapshots(inp: dict, every: int, scale: float = 1.0, threads: int | None = None):
+    """State snapshots of a prefill: for each sequence n, the state after its first (m + 1) * every tokens,
+    m = 0 .. floor(len_n / every) - 1, in order; returns (snapshots [S, H, d_k, d_v] float64, offsets
+    [N + 1]).  Each snapshot is the prefill of that prefix, taken segment by segment: the recurrence is
+    sequential, so continuing from a segment's final state is the prefix's state ("Kimi K3 changed the
+    memory math for agentic AI forever", section "But KDA State Is Not Additive", restartable checkpoints
+    at fixed token intervals)."""
+    cu = inp["cu_seqlens"]
+    N = len(cu) - 1
+    H, dk, dv = inp["H"], inp["dk"], inp["dv"]
+    snaps, offsets = [], [0]
+    for n in range(N):
+        t0, t1 = int(cu[n]), int(cu[n + 1])
+        state = None if inp["state_in"] is None else np.ascontiguousarray(inp["state_in"][n:n + 1])
+        for a in range(t0, t1 - (t1 - t0) % every, every):
+            seg = dict(inp)
+            for key in ("q", "k", "v", "beta", "alpha"):
+                seg[key] = np.ascontiguousarray(inp[key][a:a + every])
+            seg["cu_seqlens"] = np.array([0, every], np.int32)
+            seg["state_in"] = state                  # the previous segment's final state (or the initial one)
+            _, st = prefill(seg, scale=scale, threads=threads)
+            state = st
+            snaps.append(st[0])
+        offsets.append(len(snaps))
+    out = np.stack(snaps) if snaps else np.zeros((0, H, dk, dv))
+    return out, np.array(offsets, np.int32)

@@ -150,3 +150,15 @@ def test_decode_host_validation(lib, over, code):
 ])
 def test_decode_bf16_state_host_validation(lib, over, code):
     assert decode(lib, "kda_decode_step_bf16_state", **over) == code
+
+
+def test_prefill_ex_validates_snapshot_options(lib):
+    """kda_prefill_ex rejects bad snapshot options on the host; NULL options is kda_prefill."""
+    def call(opts):
+        return lib.kda_prefill_ex(P, P, P, P, P, P, 1, 64, 2, 16, 16, 0, 1.0, None, P, P, None, 0, None,
+                                  None if opts is None else ctypes.byref(opts))
+    assert call(binding.PrefillOptions(100, P, P)) == binding.KDA_ERR_INVALID_ARG     # not a multiple of 64
+    assert call(binding.PrefillOptions(-64, P, P)) == binding.KDA_ERR_INVALID_ARG
+    assert call(binding.PrefillOptions(64, None, P)) == binding.KDA_ERR_INVALID_ARG
+    assert call(binding.PrefillOptions(64, ctypes.c_void_p(0x10004), P)) == binding.KDA_ERR_INVALID_ARG
+    assert call(binding.PrefillOptions(64, P, None)) == binding.KDA_ERR_INVALID_ARG

@@ -322,3 +322,24 @@ def test_bf16_state_is_stored_in_bf16_and_unchanged_without_a_write():
     p2 = pool.copy()
     O.decode_step(step, p2)                           # the same step with an f64 state
     assert np.max(np.abs(p1 - p2)) <= 2 ** -8 * np.max(np.abs(p2))
+
+
+# ---- state snapshots ----
+
+def test_snapshots_are_prefix_states_and_the_last_is_state_out():
+    """A snapshot after m tokens is the final state of the prefill of the first m tokens (computed here by
+    a separate one-shot prefill of that prefix), and one at the sequence end equals state_out."""
+    inp = I.prefill_inputs([256, 100, 128, 0], 2, 16, 16, "f32", 38, decay="slow", state="randn")
+    snaps, offs = O.prefill_snapshots(inp, 64)
+    assert offs.tolist() == [0, 4, 5, 7, 7]
+    _, st = O.prefill(inp)
+    cu = inp["cu_seqlens"]
+    for n, m in ((0, 3), (2, 1)):                     # snapshots at the sequence ends
+        assert np.allclose(snaps[offs[n] + m], st[n], rtol=1e-12, atol=1e-12)
+    pre = dict(inp)                                   # sequence 0's first 128 tokens in one shot
+    for key in ("q", "k", "v", "beta", "alpha"):
+        pre[key] = np.ascontiguousarray(inp[key][cu[0]:cu[0] + 128])
+    pre["cu_seqlens"] = I.cu_seqlens_of([128])
+    pre["state_in"] = np.ascontiguousarray(inp["state_in"][0:1])
+    _, s128 = O.prefill(pre)
+    assert np.allclose(snaps[1], s128[0], rtol=1e-12, atol=1e-12)
