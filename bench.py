@@ -195,7 +195,7 @@ def decode_bytes_per_step(B: int, H: int, d: int, esize: int, state_esize: int =
     return B * H * (2 * d * d * state_esize + 4 * d * esize + 4 * d + 4)
 
 
-def gpu_prefill(inp, steps, warmup, dev, e2e_steps):
+def gpu_prefill(inp, steps, warmup, dev, e2e_steps, snapshot_every=0):
     import torch
     import kda_gated_delta_03_gb300 as kda
     bf = inp["dtype"] == "bf16"
@@ -212,10 +212,16 @@ def gpu_prefill(inp, steps, warmup, dev, e2e_steps):
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     launches_per_call = kda.kda_prefill_launch_count(N, T, H, dk, dv, d["q"].dtype, ws_bytes)
     stream = torch.cuda.current_stream()
+    snap = {}
+    if snapshot_every:                                # one sequence: floor(T / every) snapshots
+        cnt = T // snapshot_every
+        snap = dict(snapshot_every=snapshot_every,
+                    snapshots=torch.empty((max(cnt, 1), H, dk, dv), dtype=torch.float32, device=dev),
+                    snapshot_offsets=torch.tensor([0, cnt], dtype=torch.int32, device=dev))
 
     def call():
         kda.kda_prefill(d["q"], d["k"], d["v"], d["beta"], d["alpha"], d["cu_seqlens"], s_in, state_out=st, o=o,
-                        workspace=ws)
+                        workspace=ws, **snap)
 
     for _ in range(warmup):
         call()
@@ -429,6 +435,9 @@ def run_append(args, w, dev, peaks, line, world, local_rank):
     p2 = part(T1, T1 + T2)
     p2["state_in"] = np.zeros((1, w["H"], w["dk"], w["dv"]), np.float32)
     r2 = gpu_prefill(p2, args.steps, args.warmup, dev, 1)
+    every = 312 * 64                                  # restartable checkpoints about every 20,000 tokens
+    r3 = gpu_prefill(p1, args.steps, args.warmup, dev, 1, snapshot_every=every)
+    ms3 = max_over_ranks(r3["ms_per_step"], world)
     ms1 = max_over_ranks(r1["ms_per_step"], world)
     ms2 = max_over_ranks(r2["ms_per_step"], world)
     alg1 = prefill_bytes(T1, w["H"], w["dk"], w["dv"], 2, 0, 1)
@@ -443,6 +452,10 @@ def run_append(args, w, dev, peaks, line, world, local_rank):
                         "roofline": roofline_obj(prefill_bytes(T2, w["H"], w["dk"], w["dv"], 2, 1, 1),
                                                  r2["kernel_ms"], peaks, *prefill_path(1, "bf16", w["dk"]),
                                                  "append_1m/append")},
+                snapshots={"every_tokens": every, "count": T1 // every,
+                           "bytes": (T1 // every) * w["H"] * w["dk"] * w["dv"] * 4,
+                           "tokens_per_s": round(world * T1 * 1e3 / ms3, 1), "ms_per_step": round(ms3, 4),
+                           "overhead": round(ms3 / ms1 - 1.0, 4)},
                 gpu_launches=r1["launches"] + r2["launches"], clocks=clk.summary())
     return line
 

@@ -67,6 +67,17 @@ typedef enum {
 
 typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 
+/*
+ * Layout of alpha (the forget gate).  "Kimi K3, explained", section "The math":
+ * with every alpha equal to 1 the update is DeltaNet's delta rule, with one
+ * alpha per head it is Gated DeltaNet, and KDA gives every key channel its own.
+ */
+typedef enum {
+    KDA_ALPHA_PER_CHANNEL = 0,  /* KDA: alpha [tokens, H, d_k] float32, 16-byte aligned       */
+    KDA_ALPHA_PER_HEAD = 1,     /* Gated DeltaNet: alpha [tokens, H] float32, 4-byte aligned */
+    KDA_ALPHA_NONE = 2          /* DeltaNet: no decay; alpha is not read and may be NULL     */
+} kda_alpha_mode;
+
 /* Bits of the device error word. */
 #define KDA_DEVERR_CU_SEQLENS 0x1u  /* cu_seqlens not monotone / cu[0] != 0 / cu[N] != total  */
 #define KDA_DEVERR_STATE_IDX 0x2u   /* decode state_idx entry outside [0, num_slots)          */
@@ -134,6 +145,10 @@ KDA_API kda_status kda_prefill(const void* q, const void* k, const void* v, cons
 /*
  * Options of kda_prefill_ex.  Zero-initialise and set what is used.
  *
+ * alpha_mode selects the layout of `alpha` (kda_alpha_mode): per key channel
+ * (KDA, the default), one value per token and head (Gated DeltaNet: 4 bytes per
+ * token-head instead of 4 * d_k), or none (DeltaNet).
+ *
  * State snapshots ("Kimi K3 changed the memory math for agentic AI forever",
  * section "But KDA State Is Not Additive": the recurrent state depends on the
  * whole prefix, so restartable checkpoints and prefix reuse keep copies of it
@@ -155,6 +170,7 @@ typedef struct kda_prefill_options {
     int32_t snapshot_every;
     float* snapshots;
     const int32_t* snapshot_offsets;
+    int32_t alpha_mode;             /* kda_alpha_mode; 0 = KDA_ALPHA_PER_CHANNEL */
 } kda_prefill_options;
 
 /*
@@ -204,6 +220,23 @@ KDA_API kda_status kda_decode_step_bf16_state(const void* q, const void* k, cons
                                       const float* alpha, void* state, const int32_t* state_idx,
                                       int32_t num_slots, void* o, int32_t B, int32_t H, int32_t d_k,
                                       int32_t d_v, kda_dtype dt, float scale, void* stream);
+
+/*
+ * Options of kda_decode_step_ex.  Zero-initialise and set what is used.
+ *   alpha_mode   kda_alpha_mode: layout of alpha ([B, H, d_k], [B, H], or not read)
+ *   state_dtype  KDA_DTYPE_F32 (default) or KDA_DTYPE_BF16 (the pool is bf16, as
+ *                kda_decode_step_bf16_state)
+ */
+typedef struct kda_decode_options {
+    int32_t alpha_mode;
+    int32_t state_dtype;
+} kda_decode_options;
+
+/* kda_decode_step with options (NULL options = kda_decode_step); `state` is float32 or bf16. */
+KDA_API kda_status kda_decode_step_ex(const void* q, const void* k, const void* v, const float* beta,
+                              const float* alpha, void* state, const int32_t* state_idx, int32_t num_slots,
+                              void* o, int32_t B, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                              float scale, void* stream, const kda_decode_options* options);
 
 /*
  * kda_prefill without a workspace argument, for callers that cannot allocate

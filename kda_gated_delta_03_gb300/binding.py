@@ -24,7 +24,15 @@ KDA_DEVERR_CU_SEQLENS, KDA_DEVERR_STATE_IDX = 0x1, 0x2
 class PrefillOptions(ctypes.Structure):
     """kda_prefill_options (include/kda.h)."""
     _fields_ = [("snapshot_every", ctypes.c_int32), ("snapshots", ctypes.c_void_p),
-                ("snapshot_offsets", ctypes.c_void_p)]
+                ("snapshot_offsets", ctypes.c_void_p), ("alpha_mode", ctypes.c_int32)]
+
+
+class DecodeOptions(ctypes.Structure):
+    """kda_decode_options (include/kda.h)."""
+    _fields_ = [("alpha_mode", ctypes.c_int32), ("state_dtype", ctypes.c_int32)]
+
+
+KDA_ALPHA_PER_CHANNEL, KDA_ALPHA_PER_HEAD, KDA_ALPHA_NONE = 0, 1, 2
 
 
 # Every function include/kda.h declares, with its ctypes signature.
@@ -38,6 +46,8 @@ SIGNATURES = {
                                       _f32, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "kda_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                        ctypes.c_int, _f32, _vp]),
+    "kda_decode_step_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                          ctypes.c_int, _f32, _vp, _vp]),
     "kda_decode_step_bf16_state": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
                                                   _i32, ctypes.c_int, _f32, _vp]),
     "kda_prefill_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
@@ -121,15 +131,21 @@ def kda_prefill_launch_count(num_seqs: int, total_tokens: int, H: int, d_k: int,
     return int(load().kda_prefill_launch_count(num_seqs, total_tokens, H, d_k, d_v, _dt(dtype), workspace_bytes))
 
 
+def _alpha_shape(mode, lead, dk):
+    return {KDA_ALPHA_PER_CHANNEL: (*lead, dk), KDA_ALPHA_PER_HEAD: tuple(lead)}.get(mode)
+
+
 def kda_prefill(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float = 1.0, state_out=None,
-                o=None, workspace=None, stream=None, snapshot_every: int = 0, snapshots=None, snapshot_offsets=None):
+                o=None, workspace=None, stream=None, snapshot_every: int = 0, snapshots=None, snapshot_offsets=None,
+                alpha_mode: int = KDA_ALPHA_PER_CHANNEL):
     """Chunkwise prefill over packed sequences; returns (o, state_out).
 
     q, k [T, H, d_k], v [T, H, d_v] (bf16 or f32); beta [T, H] f32; alpha [T, H, d_k] f32;
     cu_seqlens [N + 1] int32 (device); state_in [N, H, d_k, d_v] f32 or None.
     With snapshot_every > 0 (a multiple of 64): snapshots [S, H, d_k, d_v] f32 and snapshot_offsets
     [N + 1] int32 (device) receive the state of sequence n after each multiple of snapshot_every tokens
-    (kda_prefill_ex).
+    (kda_prefill_ex).  alpha_mode: KDA_ALPHA_PER_CHANNEL (alpha [T, H, d_k]), KDA_ALPHA_PER_HEAD (Gated
+    DeltaNet, alpha [T, H]) or KDA_ALPHA_NONE (DeltaNet, alpha may be None).
     """
     L = load()
     T, H, dk = q.shape
@@ -140,7 +156,8 @@ def kda_prefill(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float
     _check("k", k, q.dtype, (T, H, dk), dev)
     _check("v", v, q.dtype, (T, H, dv), dev)
     _check("beta", beta, torch.float32, (T, H), dev)
-    _check("alpha", alpha, torch.float32, (T, H, dk), dev)
+    if alpha_mode != KDA_ALPHA_NONE or alpha is not None:
+        _check("alpha", alpha, torch.float32, _alpha_shape(alpha_mode, (T, H), dk), dev)
     _check("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
     if state_in is not None:
         _check("state_in", state_in, torch.float32, (N, H, dk, dv), dev)
@@ -156,11 +173,12 @@ def kda_prefill(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(cu_seqlens), N, T, H, dk, dv, _dt(q.dtype),
             float(scale), _ptr(state_in), _ptr(state_out), _ptr(o), _ptr(workspace), wbytes, _stream(stream))
-    if snapshot_every:
-        S = snapshots.shape[0]
-        _check("snapshots", snapshots, torch.float32, (S, H, dk, dv), dev)
-        _check("snapshot_offsets", snapshot_offsets, torch.int32, (N + 1,), dev)
-        opts = PrefillOptions(int(snapshot_every), _ptr(snapshots), _ptr(snapshot_offsets))
+    if snapshot_every or alpha_mode != KDA_ALPHA_PER_CHANNEL:
+        if snapshot_every:
+            S = snapshots.shape[0]
+            _check("snapshots", snapshots, torch.float32, (S, H, dk, dv), dev)
+            _check("snapshot_offsets", snapshot_offsets, torch.int32, (N + 1,), dev)
+        opts = PrefillOptions(int(snapshot_every), _ptr(snapshots), _ptr(snapshot_offsets), int(alpha_mode))
         rc = L.kda_prefill_ex(*args, ctypes.byref(opts))
         name = "kda_prefill_ex"
     else:
@@ -206,7 +224,8 @@ def kda_prefill_noalloc(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scal
     return o, state_out
 
 
-def kda_decode_step(q, k, v, beta, alpha, state, state_idx=None, *, scale: float = 1.0, o=None, stream=None):
+def kda_decode_step(q, k, v, beta, alpha, state, state_idx=None, *, scale: float = 1.0, o=None, stream=None,
+                    alpha_mode: int = KDA_ALPHA_PER_CHANNEL):
     """One fused decode step; updates `state` ([P, H, d_k, d_v] f32, or bf16 for the bf16-stored state) in
     place and returns o [B, H, d_v]."""
     L = load()
@@ -218,7 +237,8 @@ def kda_decode_step(q, k, v, beta, alpha, state, state_idx=None, *, scale: float
     _check("k", k, q.dtype, (B, H, dk), dev)
     _check("v", v, q.dtype, (B, H, dv), dev)
     _check("beta", beta, torch.float32, (B, H), dev)
-    _check("alpha", alpha, torch.float32, (B, H, dk), dev)
+    if alpha_mode != KDA_ALPHA_NONE or alpha is not None:
+        _check("alpha", alpha, torch.float32, _alpha_shape(alpha_mode, (B, H), dk), dev)
     bf16_state = state.dtype == torch.bfloat16
     _check("state", state, torch.bfloat16 if bf16_state else torch.float32, (P, H, dk, dv), dev)
     if state_idx is not None:
@@ -226,9 +246,14 @@ def kda_decode_step(q, k, v, beta, alpha, state, state_idx=None, *, scale: float
     if o is None:
         o = torch.empty((B, H, dv), dtype=q.dtype, device=dev)
     _check("o", o, q.dtype, (B, H, dv), dev)
-    name = "kda_decode_step_bf16_state" if bf16_state else "kda_decode_step"
-    rc = getattr(L, name)(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(state), _ptr(state_idx), P,
-                          _ptr(o), B, H, dk, dv, _dt(q.dtype), float(scale), _stream(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(state), _ptr(state_idx), P, _ptr(o), B, H,
+            dk, dv, _dt(q.dtype), float(scale), _stream(stream))
+    if alpha_mode != KDA_ALPHA_PER_CHANNEL:
+        name = "kda_decode_step_ex"
+        rc = L.kda_decode_step_ex(*args, ctypes.byref(DecodeOptions(int(alpha_mode), int(bf16_state))))
+    else:
+        name = "kda_decode_step_bf16_state" if bf16_state else "kda_decode_step"
+        rc = getattr(L, name)(*args)
     if rc != KDA_OK:
         raise KdaError(name, rc)
     return o

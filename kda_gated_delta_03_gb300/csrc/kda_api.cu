@@ -39,6 +39,13 @@ bool supported_head(int32_t dk, int32_t dv) { return dk == dv && (dk == 16 || dk
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// alpha's pointer requirements under its layout (DeltaNet reads none).
+bool alpha_ok(const float* alpha, int32_t mode) {
+    if (mode == KDA_ALPHA_NONE) return true;
+    if (mode == KDA_ALPHA_PER_HEAD) return alpha && aligned(alpha, 4);
+    return mode == KDA_ALPHA_PER_CHANNEL && alpha && aligned(alpha, 16);
+}
+
 // Scratch of kda_prefill_noalloc: the longest-first sequence order, in a fixed
 // static device array so that the entry point never allocates.  Host code must
 // not pass the array's name to a kernel (on the host it is only a stand-in);
@@ -134,10 +141,12 @@ kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const flo
     if (!cu_seqlens || !state_out || !aligned(cu_seqlens, 4) || !aligned(state_out, 16))
         return KDA_ERR_INVALID_ARG;
     if (state_in && !aligned(state_in, 16)) return KDA_ERR_INVALID_ARG;
+    const int32_t alpha_mode = options ? options->alpha_mode : KDA_ALPHA_PER_CHANNEL;
+    if (alpha_mode != KDA_ALPHA_PER_CHANNEL && alpha_mode != KDA_ALPHA_PER_HEAD && alpha_mode != KDA_ALPHA_NONE)
+        return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0) {
-        if (!q || !k || !v || !beta || !alpha || !o) return KDA_ERR_INVALID_ARG;
-        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
-            !aligned(alpha, 16) || !aligned(beta, 4))
+        if (!q || !k || !v || !beta || !o || !alpha_ok(alpha, alpha_mode)) return KDA_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(beta, 4))
             return KDA_ERR_INVALID_ARG;
     }
     const bool two_phase = kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt);
@@ -162,6 +171,7 @@ kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const flo
     p.scale = scale;
     p.state_in = state_in; p.state_out = state_out; p.o = o;
     p.err = err;
+    p.alpha_mode = alpha_mode;
     p.snap_every = snap_every;
     p.snapshots = snap_every > 0 ? options->snapshots : nullptr;
     p.snap_offsets = snap_every > 0 ? options->snapshot_offsets : nullptr;
@@ -190,16 +200,19 @@ kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const flo
 namespace {
 
 kda_status decode_impl(const void* q, const void* k, const void* v, const float* beta, const float* alpha,
-                       void* state, bool state_bf16, const int32_t* state_idx, int32_t num_slots, void* o, int32_t B,
-                       int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, float scale, void* stream) {
+                       void* state, bool state_bf16, int32_t alpha_mode, const int32_t* state_idx, int32_t num_slots,
+                       void* o, int32_t B, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, float scale,
+                       void* stream) {
     if (B < 0 || H <= 0 || d_k <= 0 || d_v <= 0 || num_slots < 0 || !std::isfinite(scale))
         return KDA_ERR_INVALID_ARG;
     if (dt != KDA_DTYPE_F32 && dt != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
+    if (alpha_mode != KDA_ALPHA_PER_CHANNEL && alpha_mode != KDA_ALPHA_PER_HEAD && alpha_mode != KDA_ALPHA_NONE)
+        return KDA_ERR_INVALID_ARG;
     if (!supported_head(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
     if (B == 0) return KDA_OK;
-    if (!q || !k || !v || !beta || !alpha || !state || !o) return KDA_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
-        !aligned(alpha, 16) || !aligned(beta, 4) || !aligned(state, 16))
+    if (!q || !k || !v || !beta || !alpha_ok(alpha, alpha_mode) || !state || !o) return KDA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(beta, 4) ||
+        !aligned(state, 16))
         return KDA_ERR_INVALID_ARG;
     if (state_idx ? !aligned(state_idx, 4) : num_slots < B) return KDA_ERR_INVALID_ARG;
 
@@ -208,7 +221,8 @@ kda_status decode_impl(const void* q, const void* k, const void* v, const float*
     if (error_word(&err) != KDA_OK) return KDA_ERR_CUDA;
     kda::DecodeParams p{};
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.alpha = alpha;
-    p.state = state; p.state_bf16 = state_bf16; p.state_idx = state_idx; p.num_slots = num_slots;
+    p.state = state; p.state_bf16 = state_bf16; p.alpha_mode = alpha_mode;
+    p.state_idx = state_idx; p.num_slots = num_slots;
     p.o = o; p.B = B; p.H = H; p.d = d_k; p.scale = scale; p.err = err;
     if (kda::launch_decode(p, dt, s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
@@ -222,16 +236,27 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const fl
                            const float* alpha, float* state, const int32_t* state_idx,
                            int32_t num_slots, void* o, int32_t B, int32_t H, int32_t d_k,
                            int32_t d_v, kda_dtype dt, float scale, void* stream) {
-    return decode_impl(q, k, v, beta, alpha, state, false, state_idx, num_slots, o, B, H, d_k, d_v, dt, scale,
-                       stream);
+    return decode_impl(q, k, v, beta, alpha, state, false, KDA_ALPHA_PER_CHANNEL, state_idx, num_slots, o, B, H,
+                       d_k, d_v, dt, scale, stream);
 }
 
 kda_status kda_decode_step_bf16_state(const void* q, const void* k, const void* v, const float* beta,
                                       const float* alpha, void* state, const int32_t* state_idx,
                                       int32_t num_slots, void* o, int32_t B, int32_t H, int32_t d_k,
                                       int32_t d_v, kda_dtype dt, float scale, void* stream) {
-    return decode_impl(q, k, v, beta, alpha, state, true, state_idx, num_slots, o, B, H, d_k, d_v, dt, scale,
-                       stream);
+    return decode_impl(q, k, v, beta, alpha, state, true, KDA_ALPHA_PER_CHANNEL, state_idx, num_slots, o, B, H,
+                       d_k, d_v, dt, scale, stream);
+}
+
+kda_status kda_decode_step_ex(const void* q, const void* k, const void* v, const float* beta, const float* alpha,
+                              void* state, const int32_t* state_idx, int32_t num_slots, void* o, int32_t B,
+                              int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, float scale, void* stream,
+                              const kda_decode_options* options) {
+    const int32_t sdt = options ? options->state_dtype : KDA_DTYPE_F32;
+    if (sdt != KDA_DTYPE_F32 && sdt != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
+    return decode_impl(q, k, v, beta, alpha, state, sdt == KDA_DTYPE_BF16,
+                       options ? options->alpha_mode : KDA_ALPHA_PER_CHANNEL, state_idx, num_slots, o, B, H, d_k,
+                       d_v, dt, scale, stream);
 }
 
 kda_status kda_prefill_noalloc(const void* q, const void* k, const void* v, const float* beta,
@@ -270,6 +295,7 @@ kda_status kda_prefill_noalloc(const void* q, const void* k, const void* v, cons
     p.scale = scale;
     p.state_in = state_in; p.state_out = state_out; p.o = o;
     p.err = err;
+    p.alpha_mode = KDA_ALPHA_PER_CHANNEL;
     if (num_seqs > 1) {
         int32_t* order = nullptr;
         if (noalloc_scratch(&order) != KDA_OK) return KDA_ERR_CUDA;

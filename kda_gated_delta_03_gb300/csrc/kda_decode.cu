@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(NT, (D == 128 ? 2 : 4)) kda_decode_kernel(Deco
     for (int i = tid; i < D; i += NT) {
         sq[i] = load_as_float(q, row * D + i);
         sk[i] = load_as_float(k, row * D + i);
-        sa[i] = p.alpha[row * D + i];
+        sa[i] = alpha_at(p.alpha, p.alpha_mode, row, D, i);
     }
     __syncthreads();
 
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(NT, 3) kda_decode_bf16s_kernel(DecodeParams p)
     for (int i = tid; i < D; i += NT) {
         sq[i] = load_as_float(q, row * D + i);
         sk[i] = load_as_float(k, row * D + i);
-        sa[i] = p.alpha[row * D + i];
+        sa[i] = alpha_at(p.alpha, p.alpha_mode, row, D, i);
     }
     __syncthreads();
 

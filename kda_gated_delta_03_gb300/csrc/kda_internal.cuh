@@ -32,6 +32,7 @@ struct PrefillParams {
     float* state_out;
     void* o;
     unsigned* err;               // device error word
+    int32_t alpha_mode;          // KDA_ALPHA_PER_CHANNEL [T,H,dk], KDA_ALPHA_PER_HEAD [T,H], KDA_ALPHA_NONE
     // optional state snapshots: the state after every snap_every tokens of each sequence
     int32_t snap_every;          // tokens (a multiple of kChunk), 0 = none
     float* snapshots;            // [snap_offsets[num_seqs], H, dk, dv]
@@ -46,6 +47,7 @@ struct DecodeParams {
     const float* alpha;
     void* state;                 // float, or bf16 when state_bf16
     bool state_bf16;
+    int32_t alpha_mode;          // as in PrefillParams
     const int32_t* state_idx;    // may be nullptr
     int32_t num_slots;
     void* o;
@@ -93,6 +95,11 @@ __device__ __forceinline__ int64_t snapshot_slot(const PrefillParams& p, int n, 
     const int32_t base = p.snap_offsets[n], cnt = p.snap_offsets[n + 1] - base;
     if (base < 0 || cnt != len / p.snap_every) return -2;
     return (int64_t)base + t_rel / p.snap_every - 1;
+}
+
+// The decay of key channel i at token-head row `row` (= t * H + h) under the given alpha layout.
+__device__ __forceinline__ float alpha_at(const float* alpha, int mode, int64_t row, int dk, int i) {
+    return mode == KDA_ALPHA_PER_CHANNEL ? alpha[row * dk + i] : mode == KDA_ALPHA_PER_HEAD ? alpha[row] : 1.f;
 }
 
 __device__ __forceinline__ float load_as_float(const float* p, int64_t i) { return p[i]; }

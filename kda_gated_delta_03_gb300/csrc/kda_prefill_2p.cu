@@ -43,7 +43,8 @@ static_assert(QM_BYTES == REC_B && REC_B + DK * DK * 4 == REC_O && REC_O + C * D
 constexpr int P_OFF_V = OFF_V;                     // v tile, dense 64 x 128 bf16
 constexpr int P_OFF_BETA = OFF_V + C * DK * 2;     // 81920
 constexpr int P_OFF_MISC = P_OFF_BETA + 256;
-constexpr int P_OFF_S = align1k(P_OFF_MISC + 64 + DK * 4);   // scratch, 144 KiB
+constexpr int P_OFF_ASC = P_OFF_MISC + 64 + DK * 4;         // per-head alpha of the unit's rows (256 B)
+constexpr int P_OFF_S = align1k(P_OFF_ASC + 256);           // scratch, 144 KiB
 // scratch sub-regions (offsets from P_OFF_S)
 constexpr int PS_A = 0, PS_T = C * AT_LD * 4, PS_SCR = 2 * C * AT_LD * 4;   // solve tiles
 constexpr int PS_OPT = 38912, PS_KV = PS_OPT + 16384;                     // T' and [Gamma.K | V]^T (N = 256)
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(NT, 1)
     const __nv_bfloat16* vraw = reinterpret_cast<const __nv_bfloat16*>(sm + P_OFF_V);
     float* sbeta = reinterpret_cast<float*>(sm + P_OFF_BETA);
     float* sgam = reinterpret_cast<float*>(sm + P_OFF_MISC + 64);
+    float* sasc = reinterpret_cast<float*>(sm + P_OFF_ASC);  // per-head alpha of the unit's token rows
     unsigned char* X = sm + P_OFF_S;
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + P_OFF_MISC + 12);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P_OFF_MISC + 8);
@@ -151,23 +153,32 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid == 32) {
             const int hu = u % H;
             const int32_t tu = (int32_t)(c_begin + u / H) * C;
-            mbar_expect_tx(lbar, 2 * 16384 + 32768 + C * DK * 2);
+            const bool per_channel = p.alpha_mode == KDA_ALPHA_PER_CHANNEL;
+            mbar_expect_tx(lbar, 2 * 16384 + (per_channel ? 32768 : 0) + C * DK * 2);
             tma_load_3d(saddr(sm + OFF_K), &maps.k, 0, hu, tu, lbar);
             tma_load_3d(saddr(sm + OFF_K + 8192), &maps.k, 64, hu, tu, lbar);
             tma_load_3d(saddr(sm + OFF_Q), &maps.q, 0, hu, tu, lbar);
             tma_load_3d(saddr(sm + OFF_Q + 8192), &maps.q, 64, hu, tu, lbar);
+            if (per_channel) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b) tma_load_3d(saddr(sm + OFF_G + b * 8192), &maps.a, 32 * b, hu, tu, lbar);
+                for (int b = 0; b < 4; ++b)
+                    tma_load_3d(saddr(sm + OFF_G + b * 8192), &maps.a, 32 * b, hu, tu, lbar);
+            }
             tma_load_3d(saddr(sm + P_OFF_V), &maps.v, 0, hu, tu, lbar);
         }
     };
     uint32_t lph = 0;
     bool load_pending = (int)blockIdx.x < n_units;
-    float beta_next = 0.f;
+    float beta_next = 0.f, alpha_next = 1.f;          // this thread's token row of the next unit
+    const bool per_head = p.alpha_mode == KDA_ALPHA_PER_HEAD;
     if (load_pending) {
         issue_loads(blockIdx.x);
         const int32_t tn = (int32_t)(c_begin + (int)blockIdx.x / H) * C;
-        if (tid < C && tn + tid < p.total_tokens) beta_next = p.beta[(int64_t)(tn + tid) * H + (int)blockIdx.x % H];
+        if (tid < C && tn + tid < p.total_tokens) {
+            const int64_t row = (int64_t)(tn + tid) * H + (int)blockIdx.x % H;
+            beta_next = p.beta[row];
+            if (per_head) alpha_next = p.alpha[row];
+        }
     }
 
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -175,7 +186,10 @@ __global__ void __launch_bounds__(NT, 1)
         const int32_t t0 = (int32_t)(c_begin + cw) * C;
         const int L = min(C, p.total_tokens - t0);
         unsigned char* rec = records + (size_t)u * REC_BYTES;
-        if (tid < C) sbeta[tid] = beta_next;
+        if (tid < C) {
+            sbeta[tid] = beta_next;
+            sasc[tid] = alpha_next;
+        }
         if (!mbar_wait(lbar, lph)) {
             atomicOr(p.err, KDA_DEVERR_TIMEOUT);
             *s_abort = 1;
@@ -201,7 +215,8 @@ __global__ void __launch_bounds__(NT, 1)
         {
             float la[32];
 #pragma unroll
-            for (int x = 0; x < 32; ++x) la[x] = Gat(32 * rh + x, ch);
+            for (int x = 0; x < 32; ++x)
+                la[x] = p.alpha_mode == KDA_ALPHA_PER_CHANNEL ? Gat(32 * rh + x, ch) : sasc[32 * rh + x];
             float acc = 0.f;
 #pragma unroll
             for (int x = 0; x < 32; ++x) {
@@ -510,7 +525,9 @@ __global__ void __launch_bounds__(NT, 1)
             load_pending = true;
             if (tid < C) {
                 const int32_t tn = (int32_t)(c_begin + un / H) * C;
-                beta_next = tn + tid < p.total_tokens ? p.beta[(int64_t)(tn + tid) * H + un % H] : 0.f;
+                const int64_t row = (int64_t)(tn + tid) * H + un % H;
+                beta_next = tn + tid < p.total_tokens ? p.beta[row] : 0.f;
+                alpha_next = per_head && tn + tid < p.total_tokens ? p.alpha[row] : 1.f;
             }
         }
         if (tid == 0) {
@@ -864,8 +881,9 @@ cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t wo
     const int T = p.total_tokens;
     if (!encode_rows(enc, &maps.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, 2, DK, p.H, T, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_rows(enc, &maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, 2, DK, p.H, T, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_rows(enc, &maps.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.alpha, 4, DK, p.H, T, 32,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        (p.alpha_mode == KDA_ALPHA_PER_CHANNEL &&
+         !encode_rows(enc, &maps.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.alpha, 4, DK, p.H, T, 32,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) ||
         !encode_rows(enc, &maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, 2, p.dv, p.H, T, DK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kda_prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);

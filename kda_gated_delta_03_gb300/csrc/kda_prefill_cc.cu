@@ -104,7 +104,9 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_cc_kernel(PrefillParams p) 
         }
         for (int e = tid; e < C * DK; e += NT) {
             const int r = e / DK, i = e % DK;
-            sm.G[e] = r < L ? fmaxf(log2f(p.alpha[((int64_t)(t0 + r) * H + h) * DK + i]), kLog2AlphaMin) : 0.f;
+            sm.G[e] = r < L ? fmaxf(log2f(alpha_at(p.alpha, p.alpha_mode, (int64_t)(t0 + r) * H + h, DK, i)),
+                                    kLog2AlphaMin)
+                            : 0.f;
         }
         for (int r = tid; r < C; r += NT) sm.beta[r] = r < L ? p.beta[(int64_t)(t0 + r) * H + h] : 0.f;
         __syncthreads();

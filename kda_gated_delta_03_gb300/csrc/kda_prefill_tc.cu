@@ -48,7 +48,8 @@ template <int NV>
 struct Cfg {
     static constexpr int CPT = NV / 2;                                   // columns per thread in epilogues
     static constexpr int OFF_BETA = OFF_V + C * NV * 2;
-    static constexpr int OFF_S = align1k(OFF_BETA + 256);               // S^T operand (bf16, NV x 128)
+    static constexpr int OFF_ASC = OFF_BETA + 256;                      // per-head alpha of the chunk's rows
+    static constexpr int OFF_S = align1k(OFF_ASC + 256);                // S^T operand (bf16, NV x 128)
     static constexpr int OFF_MISC = OFF_S + NV * DK * 2;
     static constexpr int OFF_X = align1k(OFF_MISC + 64 + DK * 4);
     static constexpr int Y_BYTES = (16384 + (DK + NV) * 256) > (32768 + NV * 256) ? (16384 + (DK + NV) * 256)
@@ -72,6 +73,8 @@ static_assert(X_LQ + 16 * F_LD * 4 <= X_BYTES && X_SCR + 3 * 256 * 4 <= X_BYTES 
 
 struct Tile {
     const float* beta;
+    const float* alpha;   // per-head alpha (KDA_ALPHA_PER_HEAD), else unused
+    int alpha_mode;
     int H;
     int h;
     int j0;
@@ -83,20 +86,24 @@ struct Tile {
 template <int NV>
 __device__ __forceinline__ void issue_chunk_loads(unsigned char* sm, const TcMaps& m, const Tile& g, int32_t t0,
                                                   int L, int tid, uint32_t lbar) {
+    const bool per_channel = g.alpha_mode == KDA_ALPHA_PER_CHANNEL;
     if (tid == 32) {
-        mbar_expect_tx(lbar, Cfg<NV>::TX_BYTES);
+        mbar_expect_tx(lbar, Cfg<NV>::TX_BYTES - (per_channel ? 0u : 32768u));
         tma_load_3d(saddr(sm + OFF_K), &m.k, 0, g.h, t0, lbar);
         tma_load_3d(saddr(sm + OFF_K + 8192), &m.k, 64, g.h, t0, lbar);
         tma_load_3d(saddr(sm + OFF_Q), &m.q, 0, g.h, t0, lbar);
         tma_load_3d(saddr(sm + OFF_Q + 8192), &m.q, 64, g.h, t0, lbar);
+        if (per_channel) {
 #pragma unroll
-        for (int b = 0; b < 4; ++b) tma_load_3d(saddr(sm + OFF_G + b * 8192), &m.a, 32 * b, g.h, t0, lbar);
+            for (int b = 0; b < 4; ++b) tma_load_3d(saddr(sm + OFF_G + b * 8192), &m.a, 32 * b, g.h, t0, lbar);
+        }
         tma_load_3d(saddr(sm + OFF_V), &m.v, g.j0, g.h, t0, lbar);
     }
     for (int r = tid; r < C; r += NT) {
         const bool ok = r < L;
         const int64_t row = ok ? ((int64_t)(t0 + r) * g.H + g.h) : 0;
         cp_async4(saddr(sm + Cfg<NV>::OFF_BETA + r * 4), g.beta + row, ok);
+        if (g.alpha_mode == KDA_ALPHA_PER_HEAD) cp_async4(saddr(sm + Cfg<NV>::OFF_ASC + r * 4), g.alpha + row, ok);
     }
     cp_async_commit();
 }
@@ -134,7 +141,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
     if (tid == 0 && h == 0 && slice == 0 && snapshot_offsets_bad(p, n, t_end - t_begin))
         atomicOr(p.err, KDA_DEVERR_SNAPSHOTS);
     const int H = p.H;
-    Tile g{p.beta, H, h, j0};
+    Tile g{p.beta, p.alpha, p.alpha_mode, H, h, j0};
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(p.o);
 
     __nv_bfloat16* vraw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_V);
@@ -244,8 +251,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
         //         then the upper half adds the lower half's total ----
         {
             float la[32];
+            const float* sasc = reinterpret_cast<const float*>(sm + CF::OFF_ASC);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) la[x] = Gat(32 * rh + x, ch);
+            for (int x = 0; x < 32; ++x)
+                la[x] = p.alpha_mode == KDA_ALPHA_PER_CHANNEL ? Gat(32 * rh + x, ch)
+                        : p.alpha_mode == KDA_ALPHA_PER_HEAD  ? sasc[32 * rh + x]
+                                                              : 1.f;
             float acc = 0.f;
 #pragma unroll
             for (int x = 0; x < 32; ++x) {
@@ -731,8 +742,9 @@ cudaError_t launch_tc(const PrefillParams& p, cudaStream_t s) {
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_rows(enc, &maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, 2, DK, p.H, T, 64,
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_rows(enc, &maps.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.alpha, 4, DK, p.H, T, 32,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+            (p.alpha_mode == KDA_ALPHA_PER_CHANNEL &&
+             !encode_rows(enc, &maps.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.alpha, 4, DK, p.H, T, 32,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) ||
             !encode_rows(enc, &maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, 2, p.dv, p.H, T, NV,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;

@@ -81,6 +81,25 @@ def _check_token_arrays(inp: dict):
             raise ValueError(f"{name} dtype {inp[name].dtype} does not match storage dtype {dt}")
 
 
+def alpha_per_channel(inp: dict) -> dict:
+    """The inputs with alpha in the per-channel layout.  "Kimi K3, explained", section "The math": Gated
+    DeltaNet's one forget value per head (alpha_mode 1, alpha [T, H]) decays every key channel by it, and
+    DeltaNet (alpha_mode 2) has no decay, alpha = 1."""
+    mode = inp.get("alpha_mode", 0)
+    if mode == 0:
+        return inp
+    out = dict(inp)
+    lead = inp["beta"].shape
+    if mode == 1:
+        out["alpha"] = np.ascontiguousarray(np.repeat(np.asarray(inp["alpha"], np.float32)[..., None], inp["dk"], -1))
+    elif mode == 2:
+        out["alpha"] = np.ones((*lead, inp["dk"]), np.float32)
+    else:
+        raise ValueError("alpha_mode must be 0, 1 or 2")
+    out["alpha_mode"] = 0
+    return out
+
+
 def prefill_units(inp: dict, units, scale: float = 1.0, erase: bool = True, want_o: bool = True,
                   threads: int | None = None, mutant: int | None = None, state_in=None):
     """Run selected (sequence, head) units of a packed varlen prefill.
@@ -88,6 +107,7 @@ def prefill_units(inp: dict, units, scale: float = 1.0, erase: bool = True, want
     Returns {(n, h): (o [T_n, d_v] float64 or None, state_out [d_k, d_v] float64)}.
     ``state_in`` overrides ``inp['state_in']`` (float32 or float64, [N, H, d_k, d_v]).
     """
+    inp = alpha_per_channel(inp)
     _check_token_arrays(inp)
     lib = _lib(mutant)
     H, dk, dv = inp["H"], inp["dk"], inp["dv"]
@@ -151,6 +171,7 @@ def decode_step(step: dict, pool: np.ndarray, state_idx=None, scale: float = 1.0
     state_dtype "bf16" models a pool stored in bf16: after the step each updated state is rounded to the
     nearest bf16 (ties to even), as storing it in 2 bytes per element does ("Kimi K3 changed the memory
     math for agentic AI forever", section "Linear Attention's Promise", sizes the state at 2 bytes)."""
+    step = alpha_per_channel(step)
     _check_token_arrays(step)
     if pool.dtype != np.float64 or not pool.flags["C_CONTIGUOUS"]:
         raise ValueError("pool must be a C-contiguous float64 array")

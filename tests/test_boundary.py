@@ -162,3 +162,25 @@ def test_prefill_ex_validates_snapshot_options(lib):
     assert call(binding.PrefillOptions(64, None, P)) == binding.KDA_ERR_INVALID_ARG
     assert call(binding.PrefillOptions(64, ctypes.c_void_p(0x10004), P)) == binding.KDA_ERR_INVALID_ARG
     assert call(binding.PrefillOptions(64, P, None)) == binding.KDA_ERR_INVALID_ARG
+
+
+def test_alpha_layout_validation(lib):
+    """An unknown alpha layout, or an alpha pointer that the layout's alignment rules out, is rejected on
+    the host (KDA_ALPHA_PER_HEAD needs 4 bytes, KDA_ALPHA_PER_CHANNEL 16)."""
+    def pre(mode, alpha):
+        opts = binding.PrefillOptions(0, None, None, mode)
+        return lib.kda_prefill_ex(P, P, P, P, alpha, P, 1, 64, 2, 16, 16, 0, 1.0, None, P, P, None, 0, None,
+                                  ctypes.byref(opts))
+    assert pre(3, P) == binding.KDA_ERR_INVALID_ARG
+    assert pre(binding.KDA_ALPHA_PER_HEAD, ctypes.c_void_p(0x10002)) == binding.KDA_ERR_INVALID_ARG
+    assert pre(binding.KDA_ALPHA_PER_CHANNEL, ctypes.c_void_p(0x10004)) == binding.KDA_ERR_INVALID_ARG
+    assert pre(binding.KDA_ALPHA_PER_HEAD, None) == binding.KDA_ERR_INVALID_ARG
+
+    def dec(mode, alpha, sdt=0):
+        opts = binding.DecodeOptions(mode, sdt)
+        return lib.kda_decode_step_ex(P, P, P, P, alpha, P, None, 4, P, 4, 2, 16, 16, 1, 1.0, None,
+                                      ctypes.byref(opts))
+    assert dec(7, P) == binding.KDA_ERR_INVALID_ARG
+    assert dec(binding.KDA_ALPHA_PER_HEAD, ctypes.c_void_p(0x10001)) == binding.KDA_ERR_INVALID_ARG
+    assert dec(binding.KDA_ALPHA_PER_CHANNEL, None) == binding.KDA_ERR_INVALID_ARG
+    assert dec(binding.KDA_ALPHA_PER_CHANNEL, P, 5) == binding.KDA_ERR_INVALID_ARG   # unknown state dtype

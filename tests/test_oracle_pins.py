@@ -343,3 +343,29 @@ def test_snapshots_are_prefix_states_and_the_last_is_state_out():
     pre["state_in"] = np.ascontiguousarray(inp["state_in"][0:1])
     _, s128 = O.prefill(pre)
     assert np.allclose(snaps[1], s128[0], rtol=1e-12, atol=1e-12)
+
+
+# ---- alpha layouts (Gated DeltaNet, DeltaNet) ----
+
+def test_gated_deltanet_one_token_closed_form():
+    """One token with one forget value per head: S_1 = alpha (I - beta k k^T) S_0 + beta k v^T.  With
+    k = e_0, beta = 1, alpha = 1/2: row 0 of S_1 is v, every other row is half of S_0's."""
+    d = 4
+    S0 = np.arange(1.0, 17.0).reshape(1, 1, d, d)
+    k = np.zeros((1, 1, d), np.float32); k[0, 0, 0] = 1.0
+    v = np.array([[[1.0, 2.0, 3.0, 4.0]]], np.float32)
+    step = dict(q=k.copy(), k=k, v=v, beta=np.ones((1, 1), np.float32), alpha=np.full((1, 1), 0.5, np.float32),
+                alpha_mode=1, dtype="f32", H=1, dk=d, dv=d)
+    pool = S0.copy()
+    o = O.decode_step(step, pool)
+    assert np.array_equal(pool[0, 0, 0], v[0, 0])
+    assert np.array_equal(pool[0, 0, 1:], 0.5 * S0[0, 0, 1:])
+    assert np.array_equal(o[0, 0], v[0, 0])           # q = k reads row 0 back
+
+
+def test_deltanet_layout_equals_unit_decay():
+    """alpha_mode 2 (no decay, alpha not read) equals per-channel alpha = 1 exactly."""
+    inp = I.prefill_inputs([70, 5], 2, 16, 16, "f32", 39, decay="one", state="randn")
+    o1, s1 = O.prefill(inp)
+    o2, s2 = O.prefill(dict(inp, alpha=None, alpha_mode=2))
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
