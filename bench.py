@@ -195,11 +195,12 @@ def decode_bytes_per_step(B: int, H: int, d: int, esize: int, state_esize: int =
     return B * H * (2 * d * d * state_esize + 4 * d * esize + 4 * d + 4)
 
 
-def gpu_prefill(inp, steps, warmup, dev, e2e_steps, snapshot_every=0):
+def gpu_prefill(inp, steps, warmup, dev, e2e_steps, snapshot_every=0, alpha_mode=0):
     import torch
     import kda_gated_delta_03_gb300 as kda
     bf = inp["dtype"] == "bf16"
-    names = ("q", "k", "v", "beta", "alpha", "cu_seqlens")
+    names = ("q", "k", "v", "beta", "alpha", "cu_seqlens") if alpha_mode != 2 else ("q", "k", "v", "beta",
+                                                                                     "cu_seqlens")
     host = {n: to_dev(inp[n], bf and n in ("q", "k", "v"), pin=True) for n in names}
     d = {n: host[n].to(dev) for n in names}
     s_in = None if inp["state_in"] is None else to_dev(inp["state_in"], dev=dev)
@@ -220,8 +221,8 @@ def gpu_prefill(inp, steps, warmup, dev, e2e_steps, snapshot_every=0):
                     snapshot_offsets=torch.tensor([0, cnt], dtype=torch.int32, device=dev))
 
     def call():
-        kda.kda_prefill(d["q"], d["k"], d["v"], d["beta"], d["alpha"], d["cu_seqlens"], s_in, state_out=st, o=o,
-                        workspace=ws, **snap)
+        kda.kda_prefill(d["q"], d["k"], d["v"], d["beta"], d.get("alpha"), d["cu_seqlens"], s_in, state_out=st, o=o,
+                        workspace=ws, alpha_mode=alpha_mode, **snap)
 
     for _ in range(warmup):
         call()
@@ -407,6 +408,17 @@ def run_ours(args, rank, world, local_rank):
                                      "ms_per_step": round(bms, 4), "state_hbm_gbs": roofb["achieved"],
                                      "roofline": roofb, "gpu_launches": rb["launches"]}
         line["gpu_launches"] += rb["launches"]
+        # the same prefill with one forget value per (token, head): Gated DeltaNet's layout of alpha
+        gd = dict(inp, alpha=np.ascontiguousarray(inp["alpha"][..., 0]))
+        rg = gpu_prefill(gd, args.steps, args.warmup, dev, 1, alpha_mode=1)
+        gms = max_over_ranks(rg["ms_per_step"], world)
+        algg = alg - tokens * r["H"] * (inp["dk"] - 1) * 4
+        line["prefill_gated_deltanet"] = {"workload": name + ", alpha one value per (token, head)",
+                                          "tokens_per_s": round(world * tokens * 1e3 / gms, 1),
+                                          "ms_per_step": round(gms, 4),
+                                          "roofline": roofline_obj(algg, rg["kernel_ms"], peaks, "prefill_2p_gdn",
+                                                                   PREFILL_2P_SRC, PREFILL_2P_LABEL, name + "_gdn"),
+                                          "gpu_launches": rg["launches"]}
     if rank == 0 and not args.no_cpu_baseline:
         threads = cpu_threads()
         secs = oracle_prefill_time(inp, threads)
@@ -455,7 +467,7 @@ def run_append(args, w, dev, peaks, line, world, local_rank):
                 snapshots={"every_tokens": every, "count": T1 // every,
                            "bytes": (T1 // every) * w["H"] * w["dk"] * w["dv"] * 4,
                            "tokens_per_s": round(world * T1 * 1e3 / ms3, 1), "ms_per_step": round(ms3, 4),
-                           "overhead": round(ms3 / ms1 - 1.0, 4)},
+                           "overhead": round(ms3 / ms1 - 1.0, 4), "gpu_launches": r3["launches"]},
                 gpu_launches=r1["launches"] + r2["launches"], clocks=clk.summary())
     return line
 

@@ -757,6 +757,8 @@ __global__ void __launch_bounds__(C_NT, 1)
         };
         write_state_operand(0);
         if (n_chunks > 0) fetch_b(0);
+        // the next snapshot point after the window start (never reached when there are no snapshots)
+        int32_t snap_next = p.snap_every > 0 ? (c_begin * C / p.snap_every + 1) * p.snap_every : -1;
         bool ok = true;
         for (int ci = 0; ci < n_chunks; ++ci) {
             const int b = ci & 1;
@@ -773,15 +775,7 @@ __global__ void __launch_bounds__(C_NT, 1)
                 S[4 * m + 2] = fmaf(gamC, S[4 * m + 2], bq[m].z - d[4 * m + 2]);
                 S[4 * m + 3] = fmaf(gamC, S[4 * m + 3], bq[m].w - d[4 * m + 3]);
             }
-            if (p.snap_every > 0) {                  // the state after this chunk, if a snapshot is due
-                const int64_t slot = snapshot_slot(p, 0, min(T, (c_begin + ci + 1) * C), T);
-                if (slot >= 0) {
-                    float* dst = p.snapshots + ((slot * H + h) * DK + srow) * (int64_t)p.dv + jc;
-#pragma unroll
-                    for (int x = 0; x < CPT; x += 4)
-                        *reinterpret_cast<float4*>(dst + x) = make_float4(S[x], S[x + 1], S[x + 2], S[x + 3]);
-                }
-            }
+            const int32_t t_done = min(T, (c_begin + ci + 1) * C);   // tokens of the sequence now in S
             if (ci + 1 < n_chunks) {
                 // the operand buffer of S_{c+1} was last read by the products of chunk c-1 (obar)
                 if (ci > 0 && !mbar_wait(obar + 8 * (b ^ 1), (uint32_t)((ci - 1) >> 1) & 1u)) {
@@ -789,6 +783,18 @@ __global__ void __launch_bounds__(C_NT, 1)
                 }
                 write_state_operand(b ^ 1);
                 fetch_b(ci + 1);
+            }
+            // a snapshot of the state after this chunk, if due (off the sequential path: after the operand
+            // of the next chunk is out; the check is a compare against the next snapshot point)
+            if (t_done == snap_next) {
+                const int64_t slot = snapshot_slot(p, 0, t_done, T);
+                if (slot >= 0) {
+                    float* dst = p.snapshots + ((slot * H + h) * DK + srow) * (int64_t)p.dv + jc;
+#pragma unroll
+                    for (int x = 0; x < CPT; x += 4)
+                        *reinterpret_cast<float4*>(dst + x) = make_float4(S[x], S[x + 1], S[x + 2], S[x + 3]);
+                }
+                snap_next += p.snap_every;
             }
         }
         if (ok && !*s_abort) {
