@@ -7,8 +7,11 @@ CUDA library and its binding) never imports or calls it.
 The recurrence lives in ``kda_oracle.c`` ("Kimi K3, explained", section "The
 math"); this module compiles it with gcc, marshals the seeded storage arrays
 into it and spreads independent (sequence, head) units, or decode rows, over
-host threads (ctypes releases the GIL during the call).  No arithmetic of the
-method happens here.
+host threads (ctypes releases the GIL during the call).  What happens here
+besides marshalling is plain composition and storage: the alpha layouts of
+Gated DeltaNet and DeltaNet are expanded to per-channel alpha, a bf16-stored
+decode state is rounded to bf16 after each step, and snapshots are prefills of
+successive segments.  The backward pass is ``backward.py``.
 """
 
 from __future__ import annotations

@@ -369,3 +369,35 @@ def test_deltanet_layout_equals_unit_decay():
     o1, s1 = O.prefill(inp)
     o2, s2 = O.prefill(dict(inp, alpha=None, alpha_mode=2))
     assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
+# ---- backward pass ----
+
+def test_backward_matches_finite_differences_of_the_forward_oracle():
+    """The reverse-mode gradients of loss = sum(o * do) + sum(state_out * dS) equal central differences
+    of the (independently pinned) forward oracle, element by element, for q, k, v, beta, alpha and the
+    initial state."""
+    from oracle.backward import prefill_backward
+    rng = np.random.default_rng(41)
+    inp = I.prefill_inputs([7, 5], 1, 8, 8, "f32", 42, decay="config", state="randn")
+    T, H, dv = inp["v"].shape
+    do = rng.standard_normal((T, H, dv))
+    dS = rng.standard_normal((2, H, 8, 8))
+    g = prefill_backward(inp, do, dS)
+
+    def loss(x):
+        o, st = O.prefill(x)
+        return float((o * do).sum() + (st * dS).sum())
+
+    eps = 2.0 ** -12
+    names = {"q": "dq", "k": "dk", "v": "dv", "beta": "dbeta", "alpha": "dalpha", "state_in": "d_state_in"}
+    for name, gname in names.items():
+        arr = inp[name]
+        for flat in rng.choice(arr.size, size=6, replace=False):
+            idx = np.unravel_index(flat, arr.shape)
+            hi, lo = dict(inp), dict(inp)
+            hi[name], lo[name] = arr.copy(), arr.copy()
+            hi[name][idx] += eps
+            lo[name][idx] -= eps
+            fd = (loss(hi) - loss(lo)) / (2 * eps)
+            assert abs(fd - g[gname][idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, g[gname][idx])
