@@ -270,6 +270,36 @@ def gpu_prefill(inp, steps, warmup, dev, e2e_steps, snapshot_every=0, alpha_mode
                 d2h=d2h, launches=steps * launches_per_call, T=T, H=H, N=N)
 
 
+def gpu_backward(inp, steps, warmup, dev):
+    """kda_prefill_backward on the workload (gradients of q, k, v, beta, alpha and state_in), inputs and
+    the output gradient resident on the device."""
+    import torch
+    import kda_gated_delta_03_gb300 as kda
+    bf = inp["dtype"] == "bf16"
+    d = {n: to_dev(inp[n], bf and n in ("q", "k", "v"), dev=dev) for n in ("q", "k", "v", "beta", "alpha",
+                                                                          "cu_seqlens")}
+    T, H, dv = inp["v"].shape
+    N = len(inp["cu_seqlens"]) - 1
+    go = torch.randn((T, H, dv), device=dev).to(d["q"].dtype)
+    need = kda.load().kda_prefill_backward_workspace_size(N, T, H, inp["dk"], dv, 1 if bf else 0)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        kda.kda_prefill_backward(d["q"], d["k"], d["v"], d["beta"], d["alpha"], d["cu_seqlens"], go, workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return dict(ms_per_step=e0.elapsed_time(e1) / steps, T=T, H=H, N=N)
+
+
 def gpu_decode(w, steps, warmup, dev, distinct=16, state_dtype="f32"):
     """Batched decode: `steps` fused steps over the resident pool; step s uses input set s mod `distinct`.
     state_dtype "bf16" runs the bf16-stored state (kda_decode_step_bf16_state)."""
@@ -408,6 +438,17 @@ def run_ours(args, rank, world, local_rank):
                                      "ms_per_step": round(bms, 4), "state_hbm_gbs": roofb["achieved"],
                                      "roofline": roofb, "gpu_launches": rb["launches"]}
         line["gpu_launches"] += rb["launches"]
+        # the backward pass of the same prefill (per-channel alpha)
+        rw = gpu_backward(inp, 5, 3, dev)
+        wms = max_over_ranks(rw["ms_per_step"], world)
+        dk_, dv_ = inp["dk"], inp["dv"]
+        # reads q, k, v, alpha, beta, grad_o; writes grad_q, grad_k, grad_v, grad_alpha, grad_beta
+        bwd_bytes = tokens * r["H"] * (2 * (2 * dk_ + dv_) * esize + 2 * (4 * dk_ + 4) + dv_ * esize)
+        line["prefill_backward"] = {"workload": name + ", gradients of q, k, v, beta, alpha (forward recompute "
+                                                       "with a snapshot every 64 tokens, then token by token back)",
+                                    "tokens_per_s": round(world * tokens * 1e3 / wms, 1), "ms_per_step": round(wms, 4),
+                                    "alg_bytes_per_step": int(bwd_bytes),
+                                    "hbm_gbs": round(bwd_bytes / (wms * 1e-3) / 1e9, 1)}
         # the same prefill with one forget value per (token, head): Gated DeltaNet's layout of alpha
         gd = dict(inp, alpha=np.ascontiguousarray(inp["alpha"][..., 0]))
         rg = gpu_prefill(gd, args.steps, args.warmup, dev, 1, alpha_mode=1)

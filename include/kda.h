@@ -186,6 +186,33 @@ KDA_API kda_status kda_prefill_ex(const void* q, const void* k, const void* v, c
                           const kda_prefill_options* options);
 
 /*
+ * Backward pass of kda_prefill (per-channel alpha): given the gradients grad_o
+ * of the outputs and grad_state_out of the final states (NULL = zero),
+ * computes the gradients of q, k, v, beta, alpha and state_in for the loss
+ * sum(o * grad_o) + sum(state_out * grad_state_out).  It is the reverse mode of
+ * the token recurrence ("Kimi K3, explained", section "The math"), walked back
+ * token by token per (sequence, head) from states that a forward recompute
+ * stores at every 64-token boundary.  Arguments are kda_prefill's, plus:
+ *   grad_o          [total_tokens, H, d_v] dtype dt
+ *   grad_state_out  [num_seqs, H, d_k, d_v] float32, or NULL
+ *   grad_q, grad_k  [total_tokens, H, d_k] dtype dt;  grad_v [total_tokens, H, d_v]
+ *   grad_beta       [total_tokens, H] float32;  grad_alpha [total_tokens, H, d_k]
+ *   grad_state_in   [num_seqs, H, d_k, d_v] float32, or NULL (not computed)
+ *   workspace       at least kda_prefill_backward_workspace_size(...) bytes
+ * The decay clamp of the forward (log2 alpha >= -15 per token) is not
+ * differentiated: gradients are those of the unclamped recurrence.
+ */
+KDA_API size_t kda_prefill_backward_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                           int32_t d_k, int32_t d_v, kda_dtype dt);
+KDA_API kda_status kda_prefill_backward(const void* q, const void* k, const void* v, const float* beta,
+                                const float* alpha, const int32_t* cu_seqlens, int32_t num_seqs,
+                                int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                                float scale, const float* state_in, const void* grad_o,
+                                const float* grad_state_out, void* grad_q, void* grad_k, void* grad_v,
+                                float* grad_beta, float* grad_alpha, float* grad_state_in, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
  * One fused decode step for B sequences, each with H resident states
  * ("Kimi K3, explained", section "How Kimi Delta Attention works, step by
  * step", and the question on constant-cost decode: one fixed-size state update

@@ -5,8 +5,10 @@ The operator runs in hand-written CUDA kernels behind the C ABI of libkda
 input generator (``inputs``) and the build step (``build``).
 """
 
-from .binding import (KdaError, kda_decode_step, kda_get_device_error, kda_prefill, kda_prefill_launch_count,
-                      kda_prefill_noalloc, kda_prefill_workspace_size, kda_status_string, load)
+from .binding import (KdaError, kda_decode_step, kda_get_device_error, kda_prefill, kda_prefill_backward,
+                      kda_prefill_launch_count, kda_prefill_noalloc, kda_prefill_workspace_size, kda_status_string,
+                      load)
 
-__all__ = ["KdaError", "kda_decode_step", "kda_get_device_error", "kda_prefill", "kda_prefill_launch_count",
-           "kda_prefill_noalloc", "kda_prefill_workspace_size", "kda_status_string", "load"]
+__all__ = ["KdaError", "kda_decode_step", "kda_get_device_error", "kda_prefill", "kda_prefill_backward",
+           "kda_prefill_launch_count", "kda_prefill_noalloc", "kda_prefill_workspace_size", "kda_status_string",
+           "load"]

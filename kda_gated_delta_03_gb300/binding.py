@@ -46,6 +46,10 @@ SIGNATURES = {
                                       _f32, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "kda_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                        ctypes.c_int, _f32, _vp]),
+    "kda_prefill_backward_workspace_size": (_sz, [_i32, _i64, _i32, _i32, _i32, ctypes.c_int]),
+    "kda_prefill_backward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
+                                            ctypes.c_int, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                            _vp, _sz, _vp]),
     "kda_decode_step_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                           ctypes.c_int, _f32, _vp, _vp]),
     "kda_decode_step_bf16_state": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
@@ -257,6 +261,41 @@ def kda_decode_step(q, k, v, beta, alpha, state, state_idx=None, *, scale: float
     if rc != KDA_OK:
         raise KdaError(name, rc)
     return o
+
+
+def kda_prefill_backward(q, k, v, beta, alpha, cu_seqlens, grad_o, state_in=None, grad_state_out=None, *,
+                         scale: float = 1.0, want_state_grad: bool = True, workspace=None, stream=None):
+    """Backward pass of kda_prefill (per-channel alpha).  Returns (grad_q, grad_k, grad_v, grad_beta,
+    grad_alpha, grad_state_in or None) for the loss sum(o * grad_o) + sum(state_out * grad_state_out)."""
+    L = load()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dev = q.device
+    N = cu_seqlens.shape[0] - 1
+    for name, t, dt_, shape in (("q", q, q.dtype, (T, H, dk)), ("k", k, q.dtype, (T, H, dk)),
+                                ("v", v, q.dtype, (T, H, dv)), ("beta", beta, torch.float32, (T, H)),
+                                ("alpha", alpha, torch.float32, (T, H, dk)),
+                                ("cu_seqlens", cu_seqlens, torch.int32, (N + 1,)),
+                                ("grad_o", grad_o, q.dtype, (T, H, dv))):
+        _check(name, t, dt_, shape, dev)
+    for name, t in (("state_in", state_in), ("grad_state_out", grad_state_out)):
+        if t is not None:
+            _check(name, t, torch.float32, (N, H, dk, dv), dev)
+    gq, gk, gv = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    gb = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ga = torch.empty((T, H, dk), dtype=torch.float32, device=dev)
+    gs = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev) if want_state_grad else None
+    need = int(L.kda_prefill_backward_workspace_size(N, T, H, dk, dv, _dt(q.dtype)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = L.kda_prefill_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(cu_seqlens), N, T, H, dk,
+                                dv, _dt(q.dtype), float(scale), _ptr(state_in), _ptr(grad_o), _ptr(grad_state_out),
+                                _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb), _ptr(ga), _ptr(gs), _ptr(workspace), wbytes,
+                                _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError("kda_prefill_backward", rc)
+    return gq, gk, gv, gb, ga, gs
 
 
 def kda_get_device_error(stream=None) -> int:

@@ -312,6 +312,100 @@ kda_status kda_prefill_noalloc(const void* q, const void* k, const void* v, cons
     return KDA_OK;
 }
 
+namespace {
+// Workspace of the backward pass: [snapshot offsets | snapshots | o and state_out of the recompute |
+// the recompute's own workspace | per-CTA chunk states]
+struct BwdLayout {
+    size_t off, snaps, o, st, fwd, scratch, total;
+};
+BwdLayout bwd_layout(int32_t N, int64_t T, int32_t H, int32_t d, kda_dtype dt) {
+    BwdLayout L{};
+    const size_t dd = (size_t)d * d * 4, esize = dt == KDA_DTYPE_BF16 ? 2 : 4;
+    const int64_t units = (int64_t)N * H;
+    const size_t ctas = (size_t)(units < kda::kBwdMaxCtas ? units : kda::kBwdMaxCtas);
+    size_t at = 0;
+    L.off = at; at = align_up(at + (size_t)(N + 1) * 4, 256);
+    L.snaps = at; at = align_up(at + (size_t)(T / kda::kChunk) * H * dd, 256);
+    L.o = at; at = align_up(at + (size_t)T * H * d * esize, 256);
+    L.st = at; at = align_up(at + (size_t)N * H * dd, 256);
+    L.fwd = at; at = align_up(at + kda_prefill_workspace_size(N, T, H, d, d, dt), 256);
+    L.scratch = at; at = align_up(at + ctas * (kda::kChunk - 1) * dd, 256);
+    L.total = at;
+    return L;
+}
+}  // namespace
+
+size_t kda_prefill_backward_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                                           int32_t d_v, kda_dtype dt) {
+    if (num_seqs <= 0 || total_tokens < 0 || H <= 0 || !supported_head(d_k, d_v)) return 0;
+    return bwd_layout(num_seqs, total_tokens, H, d_k, dt).total;
+}
+
+kda_status kda_prefill_backward(const void* q, const void* k, const void* v, const float* beta, const float* alpha,
+                                const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                int32_t d_k, int32_t d_v, kda_dtype dt, float scale, const float* state_in,
+                                const void* grad_o, const float* grad_state_out, void* grad_q, void* grad_k,
+                                void* grad_v, float* grad_beta, float* grad_alpha, float* grad_state_in, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    // ---- host-side validation ----
+    if (num_seqs < 0 || total_tokens < 0 || total_tokens > INT32_MAX || H <= 0 || d_k <= 0 || d_v <= 0 ||
+        !std::isfinite(scale))
+        return KDA_ERR_INVALID_ARG;
+    if (dt != KDA_DTYPE_F32 && dt != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
+    if (!supported_head(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !aligned(cu_seqlens, 4)) return KDA_ERR_INVALID_ARG;
+    if ((state_in && !aligned(state_in, 16)) || (grad_state_out && !aligned(grad_state_out, 16)) ||
+        (grad_state_in && !aligned(grad_state_in, 16)))
+        return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0) {
+        if (!q || !k || !v || !beta || !alpha || !grad_o || !grad_q || !grad_k || !grad_v || !grad_beta ||
+            !grad_alpha)
+            return KDA_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(alpha, 16) || !aligned(beta, 4) ||
+            !aligned(grad_o, 16) || !aligned(grad_q, 16) || !aligned(grad_k, 16) || !aligned(grad_v, 16) ||
+            !aligned(grad_beta, 4) || !aligned(grad_alpha, 16))
+            return KDA_ERR_INVALID_ARG;
+    }
+    const BwdLayout L = bwd_layout(num_seqs, total_tokens, H, d_k, dt);
+    if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
+
+    // ---- forward recompute with a snapshot at every chunk boundary, then the walk back ----
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned* err = nullptr;
+    if (error_word(&err) != KDA_OK) return KDA_ERR_CUDA;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
+    float* snaps = reinterpret_cast<float*>(ws + L.snaps);
+    if (kda::launch_bwd_offsets(cu_seqlens, num_seqs, off, s) != cudaSuccess) return KDA_ERR_CUDA;
+    kda_prefill_options opts{};
+    opts.snapshot_every = kda::kChunk;
+    opts.snapshots = snaps;
+    opts.snapshot_offsets = off;
+    const kda_status fs = kda_prefill_ex(q, k, v, beta, alpha, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, dt,
+                                         scale, state_in, reinterpret_cast<float*>(ws + L.st), ws + L.o, ws + L.fwd,
+                                         L.scratch - L.fwd, stream, &opts);
+    if (fs != KDA_OK) return fs;
+    if (total_tokens == 0 && !grad_state_in) return KDA_OK;
+    kda::BwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.alpha = alpha; p.cu_seqlens = cu_seqlens;
+    p.num_seqs = num_seqs; p.total_tokens = static_cast<int32_t>(total_tokens); p.H = H; p.dk = d_k; p.dv = d_v;
+    p.scale = scale; p.state_in = state_in; p.d_o = grad_o; p.d_state_out = grad_state_out;
+    p.d_q = grad_q; p.d_k = grad_k; p.d_v = grad_v; p.d_beta = grad_beta; p.d_alpha = grad_alpha;
+    p.d_state_in = grad_state_in;
+    p.snapshots = snaps; p.snap_offsets = off;
+    p.scratch = reinterpret_cast<float*>(ws + L.scratch);
+    p.err = err;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    const int64_t units = (int64_t)num_seqs * H;
+    int grid = (int)(units < kda::kBwdMaxCtas ? units : kda::kBwdMaxCtas);
+    if (grid > sms) grid = sms;
+    if (kda::launch_prefill_bwd(p, dt, grid, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
 kda_status kda_get_device_error(void* stream, uint32_t* bits) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned* err = nullptr;

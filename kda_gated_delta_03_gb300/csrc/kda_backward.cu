@@ -1,0 +1,258 @@
+// Backward pass of the KDA prefill (reverse mode of the recurrence), token by token per (sequence, head).
+//
+// Forward per head and token ("Kimi K3, explained", section "The math"; S is d_k x d_v, key channel
+// i = row, value channel j = column):
+//   S' = Diag(alpha_t) S_{t-1},  x = S'^T k_t,  S_t = S' + beta_t k_t (v_t - x)^T,  o_t = scale S_t^T q_t
+// Backward, from the last token back, with G the gradient of S_t (later tokens included), u = v_t - x:
+//   G += scale q_t do_t^T
+//   dq_t = scale S_t do_t;  dbeta_t = k_t^T G u;  du = beta_t G^T k_t;  dv_t = du;  dx = -du
+//   dk_t = beta_t G u + S' dx;  G' = G + k_t dx^T;  dalpha_t[i] = sum_j G'[i][j] S_{t-1}[i][j]
+//   G <- Diag(alpha_t) G'                                       (the gradient of S_{t-1})
+//
+// The states S_{t-1}, S_t come from a forward recompute: the library's own prefill writes the state at
+// every chunk boundary (snapshots every 64 tokens) into the workspace, and per chunk this kernel
+// replays the chunk's tokens from its start state into a per-CTA scratch (63 states), then walks them
+// back.  One CTA per (sequence, head); a thread holds 8 key rows x 4 value columns of S, of G and of
+// S_{t-1}; sums over key rows go through shared memory, sums over value columns through warp shuffles
+// (the LPR threads of a row group are consecutive lanes).
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+// snapshot offsets of the forward recompute: off[n] = sum over m < n of floor(len_m / 64)
+__global__ void kda_bwd_offsets_kernel(const int32_t* cu, int32_t N, int32_t* off) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        int32_t acc = 0;
+        off[0] = 0;
+        for (int n = 0; n < N; ++n) {
+            const int32_t len = cu[n + 1] - cu[n];
+            acc += (len > 0 ? len : 0) / kChunk;
+            off[n + 1] = acc;
+        }
+    }
+}
+
+template <int D, int NT>
+struct BwdCfg {
+    static constexpr int LPR = D / 4;          // float4 column groups per row (= lanes sharing a row group)
+    static constexpr int RPP = NT / LPR;       // row groups
+    static constexpr int PASSES = D / RPP;     // rows per thread
+    static_assert(NT % LPR == 0 && D % RPP == 0 && LPR <= 32 && 32 % LPR == 0, "bad backward tiling");
+};
+
+// Sum over the LPR consecutive lanes of a row group.
+template <int LPR>
+__device__ __forceinline__ float row_sum(float x) {
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+template <int D, int NT, typename TIn>
+__global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
+    using CF = BwdCfg<D, NT>;
+    constexpr int LPR = CF::LPR, RPP = CF::RPP, PASSES = CF::PASSES;
+    __shared__ float sq[D], sk[D], sa[D], sv[D], sdo[D], su[D], sdx[D];
+    __shared__ float red0[RPP][D], red1[RPP][D];
+    __shared__ float sdb[RPP];
+    __shared__ float s_beta;
+
+    const int tid = threadIdx.x;
+    const int cg = tid % LPR, rg = tid / LPR;
+    const int H = p.H;
+    const TIn* gq = static_cast<const TIn*>(p.q);
+    const TIn* gk = static_cast<const TIn*>(p.k);
+    const TIn* gv = static_cast<const TIn*>(p.v);
+    const TIn* gdo = static_cast<const TIn*>(p.d_o);
+    TIn* gdq = static_cast<TIn*>(p.d_q);
+    TIn* gdk = static_cast<TIn*>(p.d_k);
+    TIn* gdv = static_cast<TIn*>(p.d_v);
+    float* scratch = p.scratch + (int64_t)blockIdx.x * (kChunk - 1) * D * D;
+    auto row_of = [&](int m) { return rg + RPP * m; };
+    auto ld_state = [&](const float* base, float4* s) {
+#pragma unroll
+        for (int m = 0; m < PASSES; ++m) s[m] = *reinterpret_cast<const float4*>(base + (int64_t)row_of(m) * D + 4 * cg);
+    };
+    auto st_state = [&](float* base, const float4* s) {
+#pragma unroll
+        for (int m = 0; m < PASSES; ++m) *reinterpret_cast<float4*>(base + (int64_t)row_of(m) * D + 4 * cg) = s[m];
+    };
+
+    for (int unit = blockIdx.x; unit < p.num_seqs * H; unit += gridDim.x) {
+        const int n = unit / H, h = unit % H;
+        const int32_t tb = p.cu_seqlens[n], te = p.cu_seqlens[n + 1];
+        if (tb < 0 || te < tb || te > p.total_tokens) {
+            if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
+            continue;
+        }
+        const int64_t sidx = ((int64_t)n * H + h) * D * D;
+        float4 g[PASSES];                             // gradient of the current state
+        if (p.d_state_out) ld_state(p.d_state_out + sidx, g);
+        else
+#pragma unroll
+            for (int m = 0; m < PASSES; ++m) g[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int nch = (te - tb + kChunk - 1) / kChunk;
+        for (int c = nch - 1; c >= 0; --c) {
+            const int32_t t0 = tb + c * kChunk;
+            const int L = min(kChunk, te - t0);
+            // the chunk's start state: the initial state, or the snapshot after chunk c - 1
+            const float* start = c == 0 ? (p.state_in ? p.state_in + sidx : nullptr)
+                                        : p.snapshots + ((int64_t)(p.snap_offsets[n] + c - 1) * H + h) * D * D;
+            float4 s[PASSES];
+            if (start) ld_state(start, s);
+            else
+#pragma unroll
+                for (int m = 0; m < PASSES; ++m) s[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+            // ---- forward replay of the chunk; states after tokens 0 .. L-2 go to the scratch ----
+            for (int i = 0; i < L; ++i) {
+                const int64_t row = (int64_t)(t0 + i) * H + h;
+                __syncthreads();
+                for (int e = tid; e < D; e += NT) {
+                    sk[e] = load_as_float(gk, row * D + e);
+                    sa[e] = p.alpha[row * D + e];
+                    sv[e] = load_as_float(gv, row * D + e);
+                }
+                if (tid == 0) s_beta = p.beta[row];
+                __syncthreads();
+                float4 px = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int m = 0; m < PASSES; ++m) {
+                    const float w = sa[row_of(m)] * sk[row_of(m)];
+                    px.x = fmaf(w, s[m].x, px.x); px.y = fmaf(w, s[m].y, px.y);
+                    px.z = fmaf(w, s[m].z, px.z); px.w = fmaf(w, s[m].w, px.w);
+                }
+                reinterpret_cast<float4*>(red0[rg])[cg] = px;
+                __syncthreads();
+                for (int j = tid; j < D; j += NT) {
+                    float x = 0.f;
+#pragma unroll
+                    for (int r = 0; r < RPP; ++r) x += red0[r][j];
+                    su[j] = s_beta * (sv[j] - x);     // beta (v - x)
+                }
+                __syncthreads();
+                const float4 bu = reinterpret_cast<const float4*>(su)[cg];
+#pragma unroll
+                for (int m = 0; m < PASSES; ++m) {
+                    const int r = row_of(m);
+                    const float a = sa[r], kk = sk[r];
+                    s[m].x = fmaf(kk, bu.x, a * s[m].x); s[m].y = fmaf(kk, bu.y, a * s[m].y);
+                    s[m].z = fmaf(kk, bu.z, a * s[m].z); s[m].w = fmaf(kk, bu.w, a * s[m].w);
+                }
+                if (i < L - 1) st_state(scratch + (int64_t)i * D * D, s);
+            }
+            __syncthreads();                          // the scratch is written before it is read back
+
+            // ---- backward over the chunk; s holds S_t, prev S_{t-1} ----
+            for (int i = L - 1; i >= 0; --i) {
+                const int64_t row = (int64_t)(t0 + i) * H + h;
+                float4 prev[PASSES];
+                const float* pb = i > 0 ? scratch + (int64_t)(i - 1) * D * D : start;
+                if (pb) ld_state(pb, prev);
+                else
+#pragma unroll
+                    for (int m = 0; m < PASSES; ++m) prev[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                __syncthreads();
+                for (int e = tid; e < D; e += NT) {
+                    sq[e] = load_as_float(gq, row * D + e);
+                    sk[e] = load_as_float(gk, row * D + e);
+                    sa[e] = p.alpha[row * D + e];
+                    sv[e] = load_as_float(gv, row * D + e);
+                    sdo[e] = load_as_float(gdo, row * D + e);
+                }
+                if (tid == 0) s_beta = p.beta[row];
+                __syncthreads();
+                const float beta = s_beta;
+                const float4 dov = reinterpret_cast<const float4*>(sdo)[cg];
+                // G += scale q do^T; dq = scale S_t do; column partials of x = S'^T k and G^T k
+                float4 px = make_float4(0.f, 0.f, 0.f, 0.f), pg = px;
+#pragma unroll
+                for (int m = 0; m < PASSES; ++m) {
+                    const int r = row_of(m);
+                    const float sqr = p.scale * sq[r];
+                    g[m].x = fmaf(sqr, dov.x, g[m].x); g[m].y = fmaf(sqr, dov.y, g[m].y);
+                    g[m].z = fmaf(sqr, dov.z, g[m].z); g[m].w = fmaf(sqr, dov.w, g[m].w);
+                    const float dq = row_sum<LPR>(s[m].x * dov.x + s[m].y * dov.y + s[m].z * dov.z + s[m].w * dov.w);
+                    if (cg == 0) store_from_float(gdq, row * D + r, p.scale * dq);
+                    const float ak = sa[r] * sk[r], kk = sk[r];
+                    px.x = fmaf(ak, prev[m].x, px.x); px.y = fmaf(ak, prev[m].y, px.y);
+                    px.z = fmaf(ak, prev[m].z, px.z); px.w = fmaf(ak, prev[m].w, px.w);
+                    pg.x = fmaf(kk, g[m].x, pg.x); pg.y = fmaf(kk, g[m].y, pg.y);
+                    pg.z = fmaf(kk, g[m].z, pg.z); pg.w = fmaf(kk, g[m].w, pg.w);
+                }
+                reinterpret_cast<float4*>(red0[rg])[cg] = px;
+                reinterpret_cast<float4*>(red1[rg])[cg] = pg;
+                __syncthreads();
+                for (int j = tid; j < D; j += NT) {
+                    float x = 0.f, gk = 0.f;
+#pragma unroll
+                    for (int r = 0; r < RPP; ++r) { x += red0[r][j]; gk += red1[r][j]; }
+                    const float du = beta * gk;
+                    su[j] = sv[j] - x;                // u
+                    sdx[j] = -du;                     // dx
+                    store_from_float(gdv, row * D + j, du);
+                }
+                __syncthreads();
+                const float4 u4 = reinterpret_cast<const float4*>(su)[cg];
+                const float4 dx4 = reinterpret_cast<const float4*>(sdx)[cg];
+                float dbp = 0.f;
+#pragma unroll
+                for (int m = 0; m < PASSES; ++m) {
+                    const int r = row_of(m);
+                    const float a = sa[r], kk = sk[r];
+                    const float gu = row_sum<LPR>(g[m].x * u4.x + g[m].y * u4.y + g[m].z * u4.z + g[m].w * u4.w);
+                    const float sdxr = row_sum<LPR>(a * (prev[m].x * dx4.x + prev[m].y * dx4.y + prev[m].z * dx4.z +
+                                                        prev[m].w * dx4.w));
+                    // G' = G + k dx^T; dalpha = row sums of G' (.) S_{t-1}; G <- Diag(alpha) G'
+                    float4 gp;
+                    gp.x = fmaf(kk, dx4.x, g[m].x); gp.y = fmaf(kk, dx4.y, g[m].y);
+                    gp.z = fmaf(kk, dx4.z, g[m].z); gp.w = fmaf(kk, dx4.w, g[m].w);
+                    const float da = row_sum<LPR>(gp.x * prev[m].x + gp.y * prev[m].y + gp.z * prev[m].z +
+                                                  gp.w * prev[m].w);
+                    g[m] = make_float4(a * gp.x, a * gp.y, a * gp.z, a * gp.w);
+                    if (cg == 0) {
+                        store_from_float(gdk, row * D + r, beta * gu + sdxr);
+                        p.d_alpha[row * D + r] = da;
+                        dbp = fmaf(kk, gu, dbp);
+                    }
+                    s[m] = prev[m];
+                }
+                if (cg == 0) sdb[rg] = dbp;
+                __syncthreads();
+                if (tid == 0) {
+                    float db = 0.f;
+                    for (int r = 0; r < RPP; ++r) db += sdb[r];
+                    p.d_beta[row] = db;
+                }
+            }
+        }
+        if (p.d_state_in) st_state(p.d_state_in + sidx, g);
+        __syncthreads();
+    }
+}
+
+template <typename TIn>
+cudaError_t launch_bwd_t(const BwdParams& p, int grid, cudaStream_t s) {
+    switch (p.dk) {
+        case 128: kda_prefill_bwd_kernel<128, 512, TIn><<<grid, 512, 0, s>>>(p); break;
+        case 64: kda_prefill_bwd_kernel<64, 256, TIn><<<grid, 256, 0, s>>>(p); break;
+        case 16: kda_prefill_bwd_kernel<16, 32, TIn><<<grid, 32, 0, s>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_offsets(const int32_t* cu, int32_t N, int32_t* off, cudaStream_t s) {
+    kda_bwd_offsets_kernel<<<1, 32, 0, s>>>(cu, N, off);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_bwd(const BwdParams& p, kda_dtype dt, int grid, cudaStream_t s) {
+    return dt == KDA_DTYPE_BF16 ? launch_bwd_t<__nv_bfloat16>(p, grid, s) : launch_bwd_t<float>(p, grid, s);
+}
+
+}  // namespace kda

@@ -58,6 +58,36 @@ struct DecodeParams {
     unsigned* err;
 };
 
+// Everything the backward kernel needs (per-channel alpha), already validated on the host.
+struct BwdParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* beta;
+    const float* alpha;
+    const int32_t* cu_seqlens;
+    int32_t num_seqs;
+    int32_t total_tokens;
+    int32_t H;
+    int32_t dk;
+    int32_t dv;
+    float scale;
+    const float* state_in;       // may be nullptr
+    const void* d_o;
+    const float* d_state_out;    // may be nullptr
+    void* d_q;
+    void* d_k;
+    void* d_v;
+    float* d_beta;
+    float* d_alpha;
+    float* d_state_in;           // may be nullptr
+    const float* snapshots;      // forward state after every 64 tokens of each sequence
+    const int32_t* snap_offsets; // [num_seqs + 1]
+    float* scratch;              // per CTA: 63 states of the chunk being walked back
+    unsigned* err;
+};
+constexpr int kBwdMaxCtas = 256;
+
 // Launchers (return the launch error, if any).
 cudaError_t launch_decode(const DecodeParams& p, kda_dtype dt, cudaStream_t s);
 cudaError_t launch_prefill_cc(const PrefillParams& p, kda_dtype dt, cudaStream_t s);
@@ -76,6 +106,8 @@ WindowPlan prefill_2p_plan(int64_t chunks, int32_t H, size_t workspace_bytes, in
 size_t prefill_2p_min_workspace(int32_t H);                     // bytes for one chunk per window
 cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t workspace_bytes, cudaStream_t s);
 cudaError_t launch_order(const int32_t* cu_seqlens, int32_t num_seqs, int32_t* order, cudaStream_t s);
+cudaError_t launch_bwd_offsets(const int32_t* cu, int32_t N, int32_t* off, cudaStream_t s);
+cudaError_t launch_prefill_bwd(const BwdParams& p, kda_dtype dt, int grid, cudaStream_t s);
 
 // Number of CUDA-core prefill d_v slices for a head size.
 int prefill_cc_slices(int dv);

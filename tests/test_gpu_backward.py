@@ -1,0 +1,48 @@
+"""kda_prefill_backward against the float64 backward oracle (itself pinned to finite differences of the
+forward oracle), on every forward path the recompute takes: CUDA-core fp32, single-kernel tensor-core
+(several bf16 d=128 sequences) and two-phase (one bf16 d=128 sequence)."""
+
+import numpy as np
+import pytest
+import torch
+
+from kda_gated_delta_03_gb300 import inputs as I
+from oracle.backward import prefill_backward
+from kda_testutil import TOL, rel_frob, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run(seqlens, H, d, dtype, seed, decay="slow"):
+    import kda_gated_delta_03_gb300 as kda
+    inp = I.prefill_inputs(seqlens, H, d, d, dtype, seed, decay=decay, state="randn")
+    rng = np.random.default_rng(seed + 1)
+    T = inp["v"].shape[0]
+    N = len(seqlens)
+    do = rng.standard_normal((T, H, d)).astype(np.float32)
+    if dtype == "bf16":                               # grad_o in the storage dtype, as the oracle sees it
+        do_store = I.f32_to_bf16_bits(do)
+        do = I.bf16_bits_to_f32(do_store)
+    else:
+        do_store = do
+    dS = (0.1 * rng.standard_normal((N, H, d, d))).astype(np.float32)
+    bf = dtype == "bf16"
+    args = [to_dev(inp[n], bf and n in ("q", "k", "v")) for n in ("q", "k", "v", "beta", "alpha", "cu_seqlens")]
+    gq, gk, gv, gb, ga, gs = kda.kda_prefill_backward(*args, to_dev(do_store, bf), to_dev(inp["state_in"]),
+                                                      to_dev(dS))
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_error() == 0
+    got = dict(dq=gq, dk=gk, dv=gv, dbeta=gb, dalpha=ga, d_state_in=gs)
+    ref = prefill_backward(inp, do, dS)
+    return {n: (got[n].double().cpu().numpy(), ref[n]) for n in got}
+
+
+@pytest.mark.parametrize("case", [([70, 1, 0, 130], 2, 16, "f32"), ([200], 2, 64, "f32"),
+                                  ([100, 64, 129], 2, 128, "bf16"), ([300], 2, 128, "bf16")],
+                         ids=["cuda_core_d16", "cuda_core_d64", "tensor_core_varlen", "two_phase"])
+def test_backward_matches_oracle(case):
+    seqlens, H, d, dtype = case
+    res = run(seqlens, H, d, dtype, 61 + d)
+    tol = TOL[dtype]
+    for name, (got, ref) in res.items():
+        assert rel_frob(got, ref) <= tol, (name, rel_frob(got, ref))
