@@ -50,14 +50,34 @@ __device__ __forceinline__ float row_sum(float x) {
     return x;
 }
 
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// Per-token vectors of the chunk, double-buffered in shared memory and fetched one token ahead.
+template <int D, typename TIn>
+struct TokVec {
+    TIn q[D], k[D], v[D], g[D];   // g: the output gradient
+    float a[D];
+    float beta[4];
+};
+
 template <int D, int NT, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
     using CF = BwdCfg<D, NT>;
     constexpr int LPR = CF::LPR, RPP = CF::RPP, PASSES = CF::PASSES;
-    __shared__ float sq[D], sk[D], sa[D], sv[D], sdo[D], su[D], sdx[D];
+    constexpr int EV = 16 / sizeof(TIn);              // elements of TIn per 16-byte copy
+    extern __shared__ __align__(16) unsigned char dsm[];
+    float* prevbuf = reinterpret_cast<float*>(dsm);   // [2][D * D]: S_{t-1} of the next backward step
+    TokVec<D, TIn>* tv = reinterpret_cast<TokVec<D, TIn>*>(dsm + 2 * D * D * 4);
+    __shared__ float su[D], sdx[D];
     __shared__ float red0[RPP][D], red1[RPP][D];
     __shared__ float sdb[RPP];
-    __shared__ float s_beta;
 
     const int tid = threadIdx.x;
     const int cg = tid % LPR, rg = tid / LPR;
@@ -79,6 +99,36 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
 #pragma unroll
         for (int m = 0; m < PASSES; ++m) *reinterpret_cast<float4*>(base + (int64_t)row_of(m) * D + 4 * cg) = s[m];
     };
+    // asynchronous fetches: the vectors of token `row` into buffer b (q and g only when `full`), and a
+    // state (each thread its own elements) into prevbuf b
+    auto fetch_vec = [&](int b, int64_t row, bool full) {
+        TokVec<D, TIn>& t = tv[b];
+        for (int e = tid; e < D / EV; e += NT) {
+            cp16(t.k + e * EV, gk + row * D + e * EV);
+            cp16(t.v + e * EV, gv + row * D + e * EV);
+            if (full) {
+                cp16(t.q + e * EV, gq + row * D + e * EV);
+                cp16(t.g + e * EV, gdo + row * D + e * EV);
+            }
+        }
+        for (int e = tid; e < D / 4; e += NT) cp16(t.a + e * 4, p.alpha + row * D + e * 4);
+        if (tid == 0) t.beta[0] = p.beta[row];       // plain load; visible after the barrier that follows
+    };
+    auto fetch_state = [&](int b, const float* base) {
+        float* dst = prevbuf + b * D * D;
+#pragma unroll
+        for (int m = 0; m < PASSES; ++m) {
+            const int64_t off = (int64_t)row_of(m) * D + 4 * cg;
+            if (base) cp16(dst + off, base + off);
+            else *reinterpret_cast<float4*>(dst + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    auto own_state = [&](int b, float4* s) {          // this thread's elements of prevbuf b
+        const float* src = prevbuf + b * D * D;
+#pragma unroll
+        for (int m = 0; m < PASSES; ++m) s[m] = *reinterpret_cast<const float4*>(src + (int64_t)row_of(m) * D + 4 * cg);
+    };
+    auto f = [](TIn x) { return to_float(x); };
 
     for (int unit = blockIdx.x; unit < p.num_seqs * H; unit += gridDim.x) {
         const int n = unit / H, h = unit % H;
@@ -107,20 +157,21 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
                 for (int m = 0; m < PASSES; ++m) s[m] = make_float4(0.f, 0.f, 0.f, 0.f);
 
             // ---- forward replay of the chunk; states after tokens 0 .. L-2 go to the scratch ----
+            __syncthreads();                          // the vector buffers are free
+            fetch_vec(0, (int64_t)t0 * H + h, false);
+            cp_commit();
             for (int i = 0; i < L; ++i) {
-                const int64_t row = (int64_t)(t0 + i) * H + h;
-                __syncthreads();
-                for (int e = tid; e < D; e += NT) {
-                    sk[e] = load_as_float(gk, row * D + e);
-                    sa[e] = p.alpha[row * D + e];
-                    sv[e] = load_as_float(gv, row * D + e);
-                }
-                if (tid == 0) s_beta = p.beta[row];
-                __syncthreads();
+                const int b = i & 1;
+                cp_wait<0>();
+                __syncthreads();                      // buffer b landed; every thread is past step i - 1 (buffer b ^ 1)
+                if (i + 1 < L) fetch_vec(b ^ 1, (int64_t)(t0 + i + 1) * H + h, false);
+                cp_commit();
+                const TokVec<D, TIn>& t = tv[b];
                 float4 px = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int m = 0; m < PASSES; ++m) {
-                    const float w = sa[row_of(m)] * sk[row_of(m)];
+                    const int r = row_of(m);
+                    const float w = t.a[r] * f(t.k[r]);
                     px.x = fmaf(w, s[m].x, px.x); px.y = fmaf(w, s[m].y, px.y);
                     px.z = fmaf(w, s[m].z, px.z); px.w = fmaf(w, s[m].w, px.w);
                 }
@@ -130,53 +181,51 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
                     float x = 0.f;
 #pragma unroll
                     for (int r = 0; r < RPP; ++r) x += red0[r][j];
-                    su[j] = s_beta * (sv[j] - x);     // beta (v - x)
+                    su[j] = t.beta[0] * (f(t.v[j]) - x);   // beta (v - x)
                 }
                 __syncthreads();
                 const float4 bu = reinterpret_cast<const float4*>(su)[cg];
 #pragma unroll
                 for (int m = 0; m < PASSES; ++m) {
                     const int r = row_of(m);
-                    const float a = sa[r], kk = sk[r];
+                    const float a = t.a[r], kk = f(t.k[r]);
                     s[m].x = fmaf(kk, bu.x, a * s[m].x); s[m].y = fmaf(kk, bu.y, a * s[m].y);
                     s[m].z = fmaf(kk, bu.z, a * s[m].z); s[m].w = fmaf(kk, bu.w, a * s[m].w);
                 }
                 if (i < L - 1) st_state(scratch + (int64_t)i * D * D, s);
             }
-            __syncthreads();                          // the scratch is written before it is read back
+            __threadfence_block();                    // this thread's scratch stores before its own re-reads
+            __syncthreads();
 
-            // ---- backward over the chunk; s holds S_t, prev S_{t-1} ----
-            for (int i = L - 1; i >= 0; --i) {
+            // ---- backward over the chunk; s holds S_t; the step's S_{t-1} and vectors were fetched ahead ----
+            fetch_vec(0, (int64_t)(t0 + L - 1) * H + h, true);
+            fetch_state(0, L >= 2 ? scratch + (int64_t)(L - 2) * D * D : start);
+            cp_commit();
+            for (int i = L - 1, b = 0; i >= 0; --i, b ^= 1) {
                 const int64_t row = (int64_t)(t0 + i) * H + h;
-                float4 prev[PASSES];
-                const float* pb = i > 0 ? scratch + (int64_t)(i - 1) * D * D : start;
-                if (pb) ld_state(pb, prev);
-                else
-#pragma unroll
-                    for (int m = 0; m < PASSES; ++m) prev[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-                __syncthreads();
-                for (int e = tid; e < D; e += NT) {
-                    sq[e] = load_as_float(gq, row * D + e);
-                    sk[e] = load_as_float(gk, row * D + e);
-                    sa[e] = p.alpha[row * D + e];
-                    sv[e] = load_as_float(gv, row * D + e);
-                    sdo[e] = load_as_float(gdo, row * D + e);
+                if (i >= 1) {                         // the next step's vectors and S_{t-2}
+                    fetch_vec(b ^ 1, row - H, true);
+                    fetch_state(b ^ 1, i >= 2 ? scratch + (int64_t)(i - 2) * D * D : start);
                 }
-                if (tid == 0) s_beta = p.beta[row];
+                cp_commit();
+                cp_wait<1>();
                 __syncthreads();
-                const float beta = s_beta;
-                const float4 dov = reinterpret_cast<const float4*>(sdo)[cg];
+                const TokVec<D, TIn>& t = tv[b];
+                float4 prev[PASSES];
+                own_state(b, prev);
+                const float beta = t.beta[0];
+                const float4 dov = make_float4(f(t.g[4 * cg]), f(t.g[4 * cg + 1]), f(t.g[4 * cg + 2]), f(t.g[4 * cg + 3]));
                 // G += scale q do^T; dq = scale S_t do; column partials of x = S'^T k and G^T k
                 float4 px = make_float4(0.f, 0.f, 0.f, 0.f), pg = px;
 #pragma unroll
                 for (int m = 0; m < PASSES; ++m) {
                     const int r = row_of(m);
-                    const float sqr = p.scale * sq[r];
+                    const float sqr = p.scale * f(t.q[r]);
                     g[m].x = fmaf(sqr, dov.x, g[m].x); g[m].y = fmaf(sqr, dov.y, g[m].y);
                     g[m].z = fmaf(sqr, dov.z, g[m].z); g[m].w = fmaf(sqr, dov.w, g[m].w);
                     const float dq = row_sum<LPR>(s[m].x * dov.x + s[m].y * dov.y + s[m].z * dov.z + s[m].w * dov.w);
                     if (cg == 0) store_from_float(gdq, row * D + r, p.scale * dq);
-                    const float ak = sa[r] * sk[r], kk = sk[r];
+                    const float kk = f(t.k[r]), ak = t.a[r] * kk;
                     px.x = fmaf(ak, prev[m].x, px.x); px.y = fmaf(ak, prev[m].y, px.y);
                     px.z = fmaf(ak, prev[m].z, px.z); px.w = fmaf(ak, prev[m].w, px.w);
                     pg.x = fmaf(kk, g[m].x, pg.x); pg.y = fmaf(kk, g[m].y, pg.y);
@@ -190,7 +239,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
 #pragma unroll
                     for (int r = 0; r < RPP; ++r) { x += red0[r][j]; gk += red1[r][j]; }
                     const float du = beta * gk;
-                    su[j] = sv[j] - x;                // u
+                    su[j] = f(t.v[j]) - x;            // u
                     sdx[j] = -du;                     // dx
                     store_from_float(gdv, row * D + j, du);
                 }
@@ -201,7 +250,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
 #pragma unroll
                 for (int m = 0; m < PASSES; ++m) {
                     const int r = row_of(m);
-                    const float a = sa[r], kk = sk[r];
+                    const float a = t.a[r], kk = f(t.k[r]);
                     const float gu = row_sum<LPR>(g[m].x * u4.x + g[m].y * u4.y + g[m].z * u4.z + g[m].w * u4.w);
                     const float sdxr = row_sum<LPR>(a * (prev[m].x * dx4.x + prev[m].y * dx4.y + prev[m].z * dx4.z +
                                                         prev[m].w * dx4.w));
@@ -231,17 +280,30 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
         if (p.d_state_in) st_state(p.d_state_in + sidx, g);
         __syncthreads();
     }
+    cp_wait<0>();
+}
+
+template <int D, int NT, typename TIn>
+constexpr int bwd_smem() { return 2 * D * D * 4 + 2 * (int)sizeof(TokVec<D, TIn>); }
+
+template <int D, int NT, typename TIn>
+cudaError_t launch_bwd_d(const BwdParams& p, int grid, cudaStream_t s) {
+    constexpr int smem = bwd_smem<D, NT, TIn>();
+    cudaError_t e = cudaFuncSetAttribute(kda_prefill_bwd_kernel<D, NT, TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem);
+    if (e != cudaSuccess) return e;
+    kda_prefill_bwd_kernel<D, NT, TIn><<<grid, NT, smem, s>>>(p);
+    return cudaGetLastError();
 }
 
 template <typename TIn>
 cudaError_t launch_bwd_t(const BwdParams& p, int grid, cudaStream_t s) {
     switch (p.dk) {
-        case 128: kda_prefill_bwd_kernel<128, 512, TIn><<<grid, 512, 0, s>>>(p); break;
-        case 64: kda_prefill_bwd_kernel<64, 256, TIn><<<grid, 256, 0, s>>>(p); break;
-        case 16: kda_prefill_bwd_kernel<16, 32, TIn><<<grid, 32, 0, s>>>(p); break;
+        case 128: return launch_bwd_d<128, 512, TIn>(p, grid, s);
+        case 64: return launch_bwd_d<64, 256, TIn>(p, grid, s);
+        case 16: return launch_bwd_d<16, 32, TIn>(p, grid, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace

@@ -134,6 +134,9 @@ __device__ __forceinline__ float alpha_at(const float* alpha, int mode, int64_t 
     return mode == KDA_ALPHA_PER_CHANNEL ? alpha[row * dk + i] : mode == KDA_ALPHA_PER_HEAD ? alpha[row] : 1.f;
 }
 
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+
 __device__ __forceinline__ float load_as_float(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float load_as_float(const __nv_bfloat16* p, int64_t i) {
     return __bfloat162float(p[i]);
