@@ -190,9 +190,12 @@ KDA_API kda_status kda_prefill_ex(const void* q, const void* k, const void* v, c
  * of the outputs and grad_state_out of the final states (NULL = zero),
  * computes the gradients of q, k, v, beta, alpha and state_in for the loss
  * sum(o * grad_o) + sum(state_out * grad_state_out).  It is the reverse mode of
- * the token recurrence ("Kimi K3, explained", section "The math"), walked back
- * token by token per (sequence, head) from states that a forward recompute
- * stores at every 64-token boundary.  Arguments are kda_prefill's, plus:
+ * the token recurrence ("Kimi K3, explained", section "The math"), in three
+ * passes: a forward recompute that stores the state at every 64-token
+ * boundary; a reverse chain that carries only the state gradient and stores it
+ * at the same boundaries; and a chunk-parallel pass that, per (sequence, 64-token
+ * chunk, head), replays the chunk from its start state and walks it back token
+ * by token from its end-state gradient.  Arguments are kda_prefill's, plus:
  *   grad_o          [total_tokens, H, d_v] dtype dt
  *   grad_state_out  [num_seqs, H, d_k, d_v] float32, or NULL
  *   grad_q, grad_k  [total_tokens, H, d_k] dtype dt;  grad_v [total_tokens, H, d_v]

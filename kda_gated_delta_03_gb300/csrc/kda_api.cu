@@ -313,19 +313,22 @@ kda_status kda_prefill_noalloc(const void* q, const void* k, const void* v, cons
 }
 
 namespace {
-// Workspace of the backward pass: [snapshot offsets | snapshots | o and state_out of the recompute |
-// the recompute's own workspace | per-CTA chunk states]
+// Workspace of the backward pass: [snapshot and chunk offsets | snapshots | state gradients at the same
+// boundaries | o and state_out of the recompute | the recompute's own workspace | per-CTA chunk states]
 struct BwdLayout {
-    size_t off, snaps, o, st, fwd, scratch, total;
+    size_t off, snaps, gb, o, st, fwd, scratch, total;
 };
+// chunk units of the chunk pass, at most: every sequence adds at most one partial chunk
+int64_t bwd_max_units(int32_t N, int64_t T, int32_t H) { return (T / kda::kChunk + N) * H; }
 BwdLayout bwd_layout(int32_t N, int64_t T, int32_t H, int32_t d, kda_dtype dt) {
     BwdLayout L{};
     const size_t dd = (size_t)d * d * 4, esize = dt == KDA_DTYPE_BF16 ? 2 : 4;
-    const int64_t units = (int64_t)N * H;
+    const int64_t units = bwd_max_units(N, T, H);
     const size_t ctas = (size_t)(units < kda::kBwdMaxCtas ? units : kda::kBwdMaxCtas);
     size_t at = 0;
-    L.off = at; at = align_up(at + (size_t)(N + 1) * 4, 256);
+    L.off = at; at = align_up(at + (size_t)(N + 1) * 8, 256);
     L.snaps = at; at = align_up(at + (size_t)(T / kda::kChunk) * H * dd, 256);
+    L.gb = at; at = align_up(at + (size_t)(T / kda::kChunk) * H * dd, 256);
     L.o = at; at = align_up(at + (size_t)T * H * d * esize, 256);
     L.st = at; at = align_up(at + (size_t)N * H * dd, 256);
     L.fwd = at; at = align_up(at + kda_prefill_workspace_size(N, T, H, d, d, dt), 256);
@@ -376,8 +379,11 @@ kda_status kda_prefill_backward(const void* q, const void* k, const void* v, con
     if (error_word(&err) != KDA_OK) return KDA_ERR_CUDA;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
+    int32_t* choff = off + (num_seqs + 1);
     float* snaps = reinterpret_cast<float*>(ws + L.snaps);
-    if (kda::launch_bwd_offsets(cu_seqlens, num_seqs, off, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::launch_bwd_offsets(cu_seqlens, num_seqs, static_cast<int32_t>(total_tokens), off, choff, err, s) !=
+        cudaSuccess)
+        return KDA_ERR_CUDA;
     kda_prefill_options opts{};
     opts.snapshot_every = kda::kChunk;
     opts.snapshots = snaps;
@@ -393,15 +399,17 @@ kda_status kda_prefill_backward(const void* q, const void* k, const void* v, con
     p.scale = scale; p.state_in = state_in; p.d_o = grad_o; p.d_state_out = grad_state_out;
     p.d_q = grad_q; p.d_k = grad_k; p.d_v = grad_v; p.d_beta = grad_beta; p.d_alpha = grad_alpha;
     p.d_state_in = grad_state_in;
-    p.snapshots = snaps; p.snap_offsets = off;
+    p.snapshots = snaps; p.snap_offsets = off; p.chunk_offsets = choff;
+    p.dstate_b = reinterpret_cast<float*>(ws + L.gb);
     p.scratch = reinterpret_cast<float*>(ws + L.scratch);
     p.err = err;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return KDA_ERR_CUDA;
-    const int64_t units = (int64_t)num_seqs * H;
+    const int64_t units = bwd_max_units(num_seqs, total_tokens, H);
     int grid = (int)(units < kda::kBwdMaxCtas ? units : kda::kBwdMaxCtas);
     if (grid > sms) grid = sms;
+    if (grid < 1) grid = 1;
     if (kda::launch_prefill_bwd(p, dt, grid, s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }

@@ -1,4 +1,4 @@
-// Backward pass of the KDA prefill (reverse mode of the recurrence), token by token per (sequence, head).
+// Backward pass of the KDA prefill (reverse mode of the recurrence), chunk-parallel.
 //
 // Forward per head and token ("Kimi K3, explained", section "The math"; S is d_k x d_v, key channel
 // i = row, value channel j = column):
@@ -9,28 +9,45 @@
 //   dk_t = beta_t G u + S' dx;  G' = G + k_t dx^T;  dalpha_t[i] = sum_j G'[i][j] S_{t-1}[i][j]
 //   G <- Diag(alpha_t) G'                                       (the gradient of S_{t-1})
 //
-// The states S_{t-1}, S_t come from a forward recompute: the library's own prefill writes the state at
-// every chunk boundary (snapshots every 64 tokens) into the workspace, and per chunk this kernel
-// replays the chunk's tokens from its start state into a per-CTA scratch (63 states), then walks them
-// back.  One CTA per (sequence, head); a thread holds 8 key rows x 4 value columns of S, of G and of
-// S_{t-1}; sums over key rows go through shared memory, sums over value columns through warp shuffles
-// (the LPR threads of a row group are consecutive lanes).
+// Three passes after the snapshot offsets:
+//   1. forward recompute: the library's own prefill writes the state at every 64-token boundary;
+//   2. the state-gradient chain (kda_bwd_dstate_kernel): G alone, carried back token by token,
+//      G <- Diag(alpha_t) (I - beta_t k_t k_t^T) (G + scale q_t do_t^T), which needs no forward state
+//      and splits by value column; it writes G at every 64-token boundary and the gradient of the
+//      initial state;
+//   3. the chunk pass (kda_prefill_bwd_kernel): one unit per (sequence, chunk, head), independent of
+//      the others given the chunk's start state (a snapshot) and the gradient of its end state (from
+//      pass 2): it replays the chunk's tokens into a per-CTA scratch (63 states) and walks them back
+//      with the per-token rules above.  A thread holds 8 key rows x 4 value columns of S, of G and of
+//      S_{t-1}; sums over key rows go through shared memory, sums over value columns through warp
+//      shuffles (the LPR threads of a row group are consecutive lanes).
 
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
-// snapshot offsets of the forward recompute: off[n] = sum over m < n of floor(len_m / 64)
-__global__ void kda_bwd_offsets_kernel(const int32_t* cu, int32_t N, int32_t* off) {
+// Snapshot offsets of the forward recompute, off[n] = sum over m < n of floor(len_m / 64), and chunk
+// offsets, choff[n] = sum over m < n of ceil(len_m / 64) (the chunk units of pass 3).  The workspace
+// holds floor(T / 64) boundary slots, enough for any cu_seqlens with 0 <= cu[0] <= ... <= cu[N] <= T;
+// any other cu_seqlens sets the error bit and zeroes both arrays, so that nothing is written past the
+// slots (the recompute then writes no snapshot, and the chunk pass has no units).
+__global__ void kda_bwd_offsets_kernel(const int32_t* cu, int32_t N, int32_t T, int32_t* off, int32_t* choff,
+                                       unsigned* err) {
     if (blockIdx.x == 0 && threadIdx.x == 0) {
-        int32_t acc = 0;
+        bool ok = cu[0] >= 0 && cu[N] <= T;
+        for (int n = 0; n < N && ok; ++n) ok = cu[n + 1] >= cu[n];
+        int32_t acc = 0, cacc = 0;
         off[0] = 0;
+        choff[0] = 0;
         for (int n = 0; n < N; ++n) {
-            const int32_t len = cu[n + 1] - cu[n];
-            acc += (len > 0 ? len : 0) / kChunk;
+            const int32_t len = ok ? cu[n + 1] - cu[n] : 0;
+            acc += len / kChunk;
+            cacc += (len + kChunk - 1) / kChunk;
             off[n + 1] = acc;
+            choff[n + 1] = cacc;
         }
+        if (!ok) atomicOr(err, KDA_DEVERR_CU_SEQLENS);
     }
 }
 
@@ -55,9 +72,150 @@ __device__ __forceinline__ void cp16(void* dst, const void* src) {
                  "l"(src)
                  : "memory");
 }
+__device__ __forceinline__ void cp4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// ---- pass 2: the state-gradient chain ----
+// One CTA per (sequence, head, slice of SW value columns); lane j of every warp holds column j of the
+// slice, warp w key rows RPW w .. RPW w + RPW - 1.  The token vectors stream through a ring of NBUF
+// slots, NBUF - 1 tokens ahead.
+template <int D>
+struct DsCfg {
+    static constexpr int SW = D < 32 ? D : 32;      // value columns per CTA
+    static constexpr int RPW = D < 32 ? D : 32;     // key rows per warp
+    static constexpr int NW = D / RPW;              // warps
+    static constexpr int NT = 32 * NW;
+    static constexpr int SLICES = D / SW;
+    static constexpr int NBUF = 8;
+};
+
+template <int D, int SW, typename TIn>
+struct DsTok {
+    TIn q[D], k[D];
+    float a[D];
+    TIn g[SW];                                      // the slice of the output gradient
+    float beta[4];
+};
+
+// eight consecutive elements as float
+__device__ __forceinline__ void ld8(const float* p, float* o) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float* o) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[2 * i] = __uint_as_float(u[i] << 16);
+        o[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    }
+}
+
+template <int D, typename TIn>
+__global__ void __launch_bounds__(DsCfg<D>::NT) kda_bwd_dstate_kernel(BwdParams p) {
+    using CF = DsCfg<D>;
+    constexpr int SW = CF::SW, RPW = CF::RPW, NW = CF::NW, NT = CF::NT, NBUF = CF::NBUF;
+    constexpr int EV = 16 / sizeof(TIn);
+    __shared__ __align__(16) DsTok<D, SW, TIn> ring[NBUF];
+    __shared__ float red[NW][SW];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.H;
+    const int slice = blockIdx.x % CF::SLICES, nh = blockIdx.x / CF::SLICES;
+    const int h = nh % H, n = nh / H;
+    const int32_t tb = p.cu_seqlens[n], te = p.cu_seqlens[n + 1];
+    if (tb < 0 || te < tb || te > p.total_tokens) {
+        if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
+        return;
+    }
+    const TIn* gq = static_cast<const TIn*>(p.q);
+    const TIn* gk = static_cast<const TIn*>(p.k);
+    const TIn* gdo = static_cast<const TIn*>(p.d_o);
+    const bool col = lane < SW;
+    const int j = slice * SW + (col ? lane : 0);
+    const int r0 = warp * RPW;
+    const int64_t sidx = ((int64_t)n * H + h) * D * D;
+    float G[RPW];
+#pragma unroll
+    for (int x = 0; x < RPW; ++x)
+        G[x] = (p.d_state_out && col) ? p.d_state_out[sidx + (int64_t)(r0 + x) * D + j] : 0.f;
+
+    const int len = te - tb;
+    auto fetch = [&](int slot, int32_t t) {
+        const int64_t row = (int64_t)t * H + h;
+        DsTok<D, SW, TIn>& s = ring[slot];
+        for (int e = tid; e < D / EV; e += NT) {
+            cp16(s.q + e * EV, gq + row * D + e * EV);
+            cp16(s.k + e * EV, gk + row * D + e * EV);
+        }
+        for (int e = tid; e < D / 4; e += NT) cp16(s.a + e * 4, p.alpha + row * D + e * 4);
+        for (int e = tid; e < SW / EV; e += NT) cp16(s.g + e * EV, gdo + row * D + slice * SW + e * EV);
+        if (tid == 0) cp4(s.beta, p.beta + row);
+    };
+#pragma unroll 1
+    for (int i = 0; i < NBUF - 1; ++i) {
+        if (i < len) fetch(i, te - 1 - i);
+        cp_commit();
+    }
+#pragma unroll 1
+    for (int i = 0; i < len; ++i) {
+        const int32_t t = te - 1 - i;
+        cp_wait<NBUF - 2>();
+        __syncthreads();                            // token i landed; every thread is past token i - 1
+        if (i + NBUF - 1 < len) fetch((i + NBUF - 1) % NBUF, te - NBUF - i);
+        cp_commit();
+        const DsTok<D, SW, TIn>& s = ring[i % NBUF];
+        const float dov = col ? p.scale * to_float(s.g[lane]) : 0.f;
+        float part = 0.f;
+#pragma unroll
+        for (int x0 = 0; x0 < RPW; x0 += 8) {
+            float qv[8], kv[8];
+            ld8(s.q + r0 + x0, qv);
+            ld8(s.k + r0 + x0, kv);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                G[x0 + x] = fmaf(qv[x], dov, G[x0 + x]);
+                part = fmaf(G[x0 + x], kv[x], part);
+            }
+        }
+        float w = part;
+        if constexpr (NW > 1) {
+            if (col) red[warp][lane] = part;
+            __syncthreads();
+            w = 0.f;
+#pragma unroll
+            for (int x = 0; x < NW; ++x) w += red[x][col ? lane : 0];
+        }
+        const float bw = s.beta[0] * w;
+#pragma unroll
+        for (int x0 = 0; x0 < RPW; x0 += 8) {
+            float kv[8], av[8];
+            ld8(s.k + r0 + x0, kv);
+            ld8(s.a + r0 + x0, av);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) G[x0 + x] = av[x] * fmaf(-kv[x], bw, G[x0 + x]);
+        }
+        // after token tb + 64 c (c >= 1), G is the gradient of the state after chunk c - 1
+        const int32_t rel = t - tb;
+        if (rel > 0 && (rel % kChunk) == 0 && col) {
+            float* dst = p.dstate_b + ((int64_t)(p.snap_offsets[n] + rel / kChunk - 1) * H + h) * D * D + j;
+#pragma unroll
+            for (int x = 0; x < RPW; ++x) dst[(int64_t)(r0 + x) * D] = G[x];
+        }
+    }
+    if (p.d_state_in && col) {
+#pragma unroll
+        for (int x = 0; x < RPW; ++x) p.d_state_in[sidx + (int64_t)(r0 + x) * D + j] = G[x];
+    }
+    cp_wait<0>();
+}
 
 // Per-token vectors of the chunk, double-buffered in shared memory and fetched one token ahead.
 template <int D, typename TIn>
@@ -112,7 +270,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
             }
         }
         for (int e = tid; e < D / 4; e += NT) cp16(t.a + e * 4, p.alpha + row * D + e * 4);
-        if (tid == 0) t.beta[0] = p.beta[row];       // plain load; visible after the barrier that follows
+        if (tid == 0) cp4(t.beta, p.beta + row);
     };
     auto fetch_state = [&](int b, const float* base) {
         float* dst = prevbuf + b * D * D;
@@ -130,21 +288,34 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
     };
     auto f = [](TIn x) { return to_float(x); };
 
-    for (int unit = blockIdx.x; unit < p.num_seqs * H; unit += gridDim.x) {
-        const int n = unit / H, h = unit % H;
+    const int units = p.chunk_offsets[p.num_seqs] * H;
+    for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const int h = unit % H, ci = unit / H;
+        int n = 0;
+        {                                             // the sequence of chunk unit ci: choff[n] <= ci < choff[n + 1]
+            int hi = p.num_seqs;
+            while (hi - n > 1) {
+                const int mid = (n + hi) >> 1;
+                if (p.chunk_offsets[mid] <= ci) n = mid; else hi = mid;
+            }
+        }
+        const int c = ci - p.chunk_offsets[n];
         const int32_t tb = p.cu_seqlens[n], te = p.cu_seqlens[n + 1];
         if (tb < 0 || te < tb || te > p.total_tokens) {
             if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
             continue;
         }
         const int64_t sidx = ((int64_t)n * H + h) * D * D;
-        float4 g[PASSES];                             // gradient of the current state
-        if (p.d_state_out) ld_state(p.d_state_out + sidx, g);
+        const int nch = (te - tb + kChunk - 1) / kChunk;
+        // the gradient of the chunk's end state: grad_state_out for the last chunk, else from pass 2
+        float4 g[PASSES];
+        const float* gend = c == nch - 1 ? (p.d_state_out ? p.d_state_out + sidx : nullptr)
+                                         : p.dstate_b + ((int64_t)(p.snap_offsets[n] + c) * H + h) * D * D;
+        if (gend) ld_state(gend, g);
         else
 #pragma unroll
             for (int m = 0; m < PASSES; ++m) g[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int nch = (te - tb + kChunk - 1) / kChunk;
-        for (int c = nch - 1; c >= 0; --c) {
+        {
             const int32_t t0 = tb + c * kChunk;
             const int L = min(kChunk, te - t0);
             // the chunk's start state: the initial state, or the snapshot after chunk c - 1
@@ -277,7 +448,6 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
                 }
             }
         }
-        if (p.d_state_in) st_state(p.d_state_in + sidx, g);
         __syncthreads();
     }
     cp_wait<0>();
@@ -296,8 +466,24 @@ cudaError_t launch_bwd_d(const BwdParams& p, int grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <int D, typename TIn>
+cudaError_t launch_dstate_d(const BwdParams& p, cudaStream_t s) {
+    const int64_t grid = (int64_t)p.num_seqs * p.H * DsCfg<D>::SLICES;
+    if (grid <= 0) return cudaSuccess;
+    kda_bwd_dstate_kernel<D, TIn><<<(unsigned)grid, DsCfg<D>::NT, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <typename TIn>
 cudaError_t launch_bwd_t(const BwdParams& p, int grid, cudaStream_t s) {
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (p.dk) {
+        case 128: e = launch_dstate_d<128, TIn>(p, s); break;
+        case 64: e = launch_dstate_d<64, TIn>(p, s); break;
+        case 16: e = launch_dstate_d<16, TIn>(p, s); break;
+        default: break;
+    }
+    if (e != cudaSuccess) return e;
     switch (p.dk) {
         case 128: return launch_bwd_d<128, 512, TIn>(p, grid, s);
         case 64: return launch_bwd_d<64, 256, TIn>(p, grid, s);
@@ -308,8 +494,9 @@ cudaError_t launch_bwd_t(const BwdParams& p, int grid, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_bwd_offsets(const int32_t* cu, int32_t N, int32_t* off, cudaStream_t s) {
-    kda_bwd_offsets_kernel<<<1, 32, 0, s>>>(cu, N, off);
+cudaError_t launch_bwd_offsets(const int32_t* cu, int32_t N, int32_t T, int32_t* off, int32_t* choff, unsigned* err,
+                               cudaStream_t s) {
+    kda_bwd_offsets_kernel<<<1, 32, 0, s>>>(cu, N, T, off, choff, err);
     return cudaGetLastError();
 }
 

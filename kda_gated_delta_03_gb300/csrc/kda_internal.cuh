@@ -82,11 +82,13 @@ struct BwdParams {
     float* d_alpha;
     float* d_state_in;           // may be nullptr
     const float* snapshots;      // forward state after every 64 tokens of each sequence
-    const int32_t* snap_offsets; // [num_seqs + 1]
+    const int32_t* snap_offsets; // [num_seqs + 1]: first snapshot slot of each sequence
+    const int32_t* chunk_offsets;// [num_seqs + 1]: first chunk unit of each sequence
+    float* dstate_b;             // gradient of the state after every 64 tokens (snapshot slots)
     float* scratch;              // per CTA: 63 states of the chunk being walked back
     unsigned* err;
 };
-constexpr int kBwdMaxCtas = 256;
+constexpr int kBwdMaxCtas = 160;   // chunk-pass CTAs (one per SM)
 
 // Launchers (return the launch error, if any).
 cudaError_t launch_decode(const DecodeParams& p, kda_dtype dt, cudaStream_t s);
@@ -106,7 +108,8 @@ WindowPlan prefill_2p_plan(int64_t chunks, int32_t H, size_t workspace_bytes, in
 size_t prefill_2p_min_workspace(int32_t H);                     // bytes for one chunk per window
 cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t workspace_bytes, cudaStream_t s);
 cudaError_t launch_order(const int32_t* cu_seqlens, int32_t num_seqs, int32_t* order, cudaStream_t s);
-cudaError_t launch_bwd_offsets(const int32_t* cu, int32_t N, int32_t* off, cudaStream_t s);
+cudaError_t launch_bwd_offsets(const int32_t* cu, int32_t N, int32_t T, int32_t* off, int32_t* choff, unsigned* err,
+                               cudaStream_t s);
 cudaError_t launch_prefill_bwd(const BwdParams& p, kda_dtype dt, int grid, cudaStream_t s);
 
 // Number of CUDA-core prefill d_v slices for a head size.
