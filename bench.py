@@ -445,7 +445,8 @@ def run_ours(args, rank, world, local_rank):
         # reads q, k, v, alpha, beta, grad_o; writes grad_q, grad_k, grad_v, grad_alpha, grad_beta
         bwd_bytes = tokens * r["H"] * (2 * (2 * dk_ + dv_) * esize + 2 * (4 * dk_ + 4) + dv_ * esize)
         line["prefill_backward"] = {"workload": name + ", gradients of q, k, v, beta, alpha (forward recompute "
-                                                       "with a snapshot every 64 tokens, then token by token back)",
+                                                       "with a snapshot every 64 tokens, state-gradient chain, "
+                                                       "then one unit per (chunk, head))",
                                     "tokens_per_s": round(world * tokens * 1e3 / wms, 1), "ms_per_step": round(wms, 4),
                                     "alg_bytes_per_step": int(bwd_bytes),
                                     "hbm_gbs": round(bwd_bytes / (wms * 1e-3) / 1e9, 1)}

@@ -59,12 +59,48 @@ struct BwdCfg {
     static_assert(NT % LPR == 0 && D % RPP == 0 && LPR <= 32 && 32 % LPR == 0, "bad backward tiling");
 };
 
-// Sum over the LPR consecutive lanes of a row group.
-template <int LPR>
-__device__ __forceinline__ float row_sum(float x) {
+// Reduce-scatter over the consecutive lanes of a row group (xor offsets O, O/2, .., 1): each lane brings
+// V partial sums; while the count is even a level halves it (a lane keeps the half its offset bit
+// selects and adds its partner's copy of that half), after that a level adds all of them.  Afterwards
+// v[0 .. rs_count - 1] of the lane at position c are complete sums of the values rs_base(c) ..
+// rs_base(c) + rs_count - 1, replicated over the lanes that differ only in the bits rs_mask().
+template <int O, int V>
+__device__ __forceinline__ void rs_step(float* v, int c) {
+    if constexpr (O >= 1) {
+        if constexpr (V % 2 == 0) {
+            constexpr int HV = V / 2;
+            const bool up = (c & O) != 0;
 #pragma unroll
-    for (int off = LPR / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-    return x;
+            for (int i = 0; i < HV; ++i) {
+                const float send = up ? v[i] : v[HV + i];
+                const float keep = up ? v[HV + i] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+            }
+            rs_step<O / 2, HV>(v, c);
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], O);
+            rs_step<O / 2, V>(v, c);
+        }
+    }
+}
+template <int O, int V>
+__device__ __forceinline__ int rs_base(int c) {
+    if constexpr (O >= 1) {
+        if constexpr (V % 2 == 0) return ((c & O) ? V / 2 : 0) + rs_base<O / 2, V / 2>(c);
+        else return rs_base<O / 2, V>(c);
+    } else {
+        return 0;
+    }
+}
+template <int O, int V>
+__host__ __device__ constexpr int rs_mask() {
+    if constexpr (O >= 1) {
+        if constexpr (V % 2 == 0) return rs_mask<O / 2, V / 2>();
+        else return O | rs_mask<O / 2, V>();
+    } else {
+        return 0;
+    }
 }
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
@@ -173,7 +209,7 @@ __global__ void __launch_bounds__(DsCfg<D>::NT) kda_bwd_dstate_kernel(BwdParams 
         cp_commit();
         const DsTok<D, SW, TIn>& s = ring[i % NBUF];
         const float dov = col ? p.scale * to_float(s.g[lane]) : 0.f;
-        float part = 0.f;
+        float pp[4] = {0.f, 0.f, 0.f, 0.f};           // four independent partial sums
 #pragma unroll
         for (int x0 = 0; x0 < RPW; x0 += 8) {
             float qv[8], kv[8];
@@ -182,9 +218,10 @@ __global__ void __launch_bounds__(DsCfg<D>::NT) kda_bwd_dstate_kernel(BwdParams 
 #pragma unroll
             for (int x = 0; x < 8; ++x) {
                 G[x0 + x] = fmaf(qv[x], dov, G[x0 + x]);
-                part = fmaf(G[x0 + x], kv[x], part);
+                pp[x & 3] = fmaf(G[x0 + x], kv[x], pp[x & 3]);
             }
         }
+        const float part = (pp[0] + pp[1]) + (pp[2] + pp[3]);
         float w = part;
         if constexpr (NW > 1) {
             if (col) red[warp][lane] = part;
@@ -388,20 +425,23 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
                 const float4 dov = make_float4(f(t.g[4 * cg]), f(t.g[4 * cg + 1]), f(t.g[4 * cg + 2]), f(t.g[4 * cg + 3]));
                 // G += scale q do^T; dq = scale S_t do; column partials of x = S'^T k and G^T k
                 float4 px = make_float4(0.f, 0.f, 0.f, 0.f), pg = px;
+                float dqv[PASSES];
 #pragma unroll
                 for (int m = 0; m < PASSES; ++m) {
                     const int r = row_of(m);
                     const float sqr = p.scale * f(t.q[r]);
                     g[m].x = fmaf(sqr, dov.x, g[m].x); g[m].y = fmaf(sqr, dov.y, g[m].y);
                     g[m].z = fmaf(sqr, dov.z, g[m].z); g[m].w = fmaf(sqr, dov.w, g[m].w);
-                    const float dq = row_sum<LPR>(s[m].x * dov.x + s[m].y * dov.y + s[m].z * dov.z + s[m].w * dov.w);
-                    if (cg == 0) store_from_float(gdq, row * D + r, p.scale * dq);
+                    dqv[m] = s[m].x * dov.x + s[m].y * dov.y + s[m].z * dov.z + s[m].w * dov.w;
                     const float kk = f(t.k[r]), ak = t.a[r] * kk;
                     px.x = fmaf(ak, prev[m].x, px.x); px.y = fmaf(ak, prev[m].y, px.y);
                     px.z = fmaf(ak, prev[m].z, px.z); px.w = fmaf(ak, prev[m].w, px.w);
                     pg.x = fmaf(kk, g[m].x, pg.x); pg.y = fmaf(kk, g[m].y, pg.y);
                     pg.z = fmaf(kk, g[m].z, pg.z); pg.w = fmaf(kk, g[m].w, pg.w);
                 }
+                rs_step<LPR / 2, PASSES>(dqv, cg);
+                if ((cg & rs_mask<LPR / 2, PASSES>()) == 0)
+                    store_from_float(gdq, row * D + row_of(rs_base<LPR / 2, PASSES>(cg)), p.scale * dqv[0]);
                 reinterpret_cast<float4*>(red0[rg])[cg] = px;
                 reinterpret_cast<float4*>(red1[rg])[cg] = pg;
                 __syncthreads();
@@ -417,27 +457,32 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_bwd_kernel(BwdParams p) {
                 __syncthreads();
                 const float4 u4 = reinterpret_cast<const float4*>(su)[cg];
                 const float4 dx4 = reinterpret_cast<const float4*>(sdx)[cg];
-                float dbp = 0.f;
+                // per row: gu = (G u)_r, sdxr = (S' dx)_r, da = sum_j G'_rj S_{t-1,rj}, interleaved as
+                // tv[3 m + 0 .. 2] so that the reduce-scatter leaves all three of one row on one lane
+                float tv[3 * PASSES];
 #pragma unroll
                 for (int m = 0; m < PASSES; ++m) {
                     const int r = row_of(m);
                     const float a = t.a[r], kk = f(t.k[r]);
-                    const float gu = row_sum<LPR>(g[m].x * u4.x + g[m].y * u4.y + g[m].z * u4.z + g[m].w * u4.w);
-                    const float sdxr = row_sum<LPR>(a * (prev[m].x * dx4.x + prev[m].y * dx4.y + prev[m].z * dx4.z +
-                                                        prev[m].w * dx4.w));
+                    tv[3 * m] = g[m].x * u4.x + g[m].y * u4.y + g[m].z * u4.z + g[m].w * u4.w;
+                    tv[3 * m + 1] = a * (prev[m].x * dx4.x + prev[m].y * dx4.y + prev[m].z * dx4.z + prev[m].w * dx4.w);
                     // G' = G + k dx^T; dalpha = row sums of G' (.) S_{t-1}; G <- Diag(alpha) G'
                     float4 gp;
                     gp.x = fmaf(kk, dx4.x, g[m].x); gp.y = fmaf(kk, dx4.y, g[m].y);
                     gp.z = fmaf(kk, dx4.z, g[m].z); gp.w = fmaf(kk, dx4.w, g[m].w);
-                    const float da = row_sum<LPR>(gp.x * prev[m].x + gp.y * prev[m].y + gp.z * prev[m].z +
-                                                  gp.w * prev[m].w);
+                    tv[3 * m + 2] = gp.x * prev[m].x + gp.y * prev[m].y + gp.z * prev[m].z + gp.w * prev[m].w;
                     g[m] = make_float4(a * gp.x, a * gp.y, a * gp.z, a * gp.w);
-                    if (cg == 0) {
-                        store_from_float(gdk, row * D + r, beta * gu + sdxr);
-                        p.d_alpha[row * D + r] = da;
-                        dbp = fmaf(kk, gu, dbp);
-                    }
                     s[m] = prev[m];
+                }
+                rs_step<LPR / 2, 3 * PASSES>(tv, cg);
+                constexpr int TMASK = rs_mask<LPR / 2, 3 * PASSES>();
+                const int rr = row_of(rs_base<LPR / 2, 3 * PASSES>(cg) / 3);
+                float dbp = f(t.k[rr]) * tv[0];               // k_r (G u)_r, summed over this row group's rows
+#pragma unroll
+                for (int o = LPR / 2; o > TMASK; o >>= 1) dbp += __shfl_xor_sync(0xffffffffu, dbp, o);
+                if ((cg & TMASK) == 0) {
+                    store_from_float(gdk, row * D + rr, beta * tv[0] + tv[1]);
+                    p.d_alpha[row * D + rr] = tv[2];
                 }
                 if (cg == 0) sdb[rg] = dbp;
                 __syncthreads();
