@@ -438,6 +438,7 @@ def run_ours(args, rank, world, local_rank):
                                      "ms_per_step": round(bms, 4), "state_hbm_gbs": roofb["achieved"],
                                      "roofline": roofb, "gpu_launches": rb["launches"]}
         line["gpu_launches"] += rb["launches"]
+    if name == "prefill_8k" and not args.no_backward:
         # the backward pass of the same prefill (per-channel alpha)
         rw = gpu_backward(inp, 5, 3, dev)
         wms = max_over_ranks(rw["ms_per_step"], world)
@@ -450,6 +451,7 @@ def run_ours(args, rank, world, local_rank):
                                     "tokens_per_s": round(world * tokens * 1e3 / wms, 1), "ms_per_step": round(wms, 4),
                                     "alg_bytes_per_step": int(bwd_bytes),
                                     "hbm_gbs": round(bwd_bytes / (wms * 1e-3) / 1e9, 1)}
+    if name == "prefill_8k" and not args.no_gdn:
         # the same prefill with one forget value per (token, head): Gated DeltaNet's layout of alpha
         gd = dict(inp, alpha=np.ascontiguousarray(inp["alpha"][..., 0]))
         rg = gpu_prefill(gd, args.steps, args.warmup, dev, 1, alpha_mode=1)
@@ -568,7 +570,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="prefill_8k",
                     choices=["prefill_8k", "varlen_64", "decode_512x32", "decode_512x32_bf16_state", "append_1m"])
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode lines of the prefill_8k run")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward line of the prefill_8k run")
+    ap.add_argument("--no-gdn", action="store_true", help="skip the Gated DeltaNet line of the prefill_8k run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -119,7 +119,8 @@ __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0
 
 // ---- pass 2: the state-gradient chain ----
 // One CTA per (sequence, head, slice of SW value columns); lane j of every warp holds column j of the
-// slice, warp w key rows RPW w .. RPW w + RPW - 1.  The token vectors stream through a ring of NBUF
+// slice, warp w key rows RPW w .. RPW w + RPW - 1.  (Eight warps of 16 rows at d = 128 were slower: the
+// chain is bound by its per-token barrier and reduction latency, which more warps lengthen.)  The token vectors stream through a ring of NBUF
 // slots, NBUF - 1 tokens ahead.
 template <int D>
 struct DsCfg {
@@ -210,15 +211,16 @@ __global__ void __launch_bounds__(DsCfg<D>::NT) kda_bwd_dstate_kernel(BwdParams 
         const DsTok<D, SW, TIn>& s = ring[i % NBUF];
         const float dov = col ? p.scale * to_float(s.g[lane]) : 0.f;
         float pp[4] = {0.f, 0.f, 0.f, 0.f};           // four independent partial sums
+        float kv[RPW];                                // k of this warp's rows, kept for the update
 #pragma unroll
         for (int x0 = 0; x0 < RPW; x0 += 8) {
-            float qv[8], kv[8];
+            float qv[8];
             ld8(s.q + r0 + x0, qv);
-            ld8(s.k + r0 + x0, kv);
+            ld8(s.k + r0 + x0, kv + x0);
 #pragma unroll
             for (int x = 0; x < 8; ++x) {
                 G[x0 + x] = fmaf(qv[x], dov, G[x0 + x]);
-                pp[x & 3] = fmaf(G[x0 + x], kv[x], pp[x & 3]);
+                pp[x & 3] = fmaf(G[x0 + x], kv[x0 + x], pp[x & 3]);
             }
         }
         const float part = (pp[0] + pp[1]) + (pp[2] + pp[3]);
@@ -233,11 +235,10 @@ __global__ void __launch_bounds__(DsCfg<D>::NT) kda_bwd_dstate_kernel(BwdParams 
         const float bw = s.beta[0] * w;
 #pragma unroll
         for (int x0 = 0; x0 < RPW; x0 += 8) {
-            float kv[8], av[8];
-            ld8(s.k + r0 + x0, kv);
+            float av[8];
             ld8(s.a + r0 + x0, av);
 #pragma unroll
-            for (int x = 0; x < 8; ++x) G[x0 + x] = av[x] * fmaf(-kv[x], bw, G[x0 + x]);
+            for (int x = 0; x < 8; ++x) G[x0 + x] = av[x] * fmaf(-kv[x0 + x], bw, G[x0 + x]);
         }
         // after token tb + 64 c (c >= 1), G is the gradient of the state after chunk c - 1
         const int32_t rel = t - tb;
