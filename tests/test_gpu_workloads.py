@@ -91,3 +91,28 @@ def test_append_1m_sampled_heads():
     o_one, s_one = prefill_gpu(full)
     assert np.array_equal(np.concatenate([o1, o2]), o_one)          # chunk-aligned split: identical chunking
     assert np.array_equal(s2, s_one)
+
+
+def test_prefill_8k_backward_sampled_heads():
+    """The backward pass at the full prefill_8k size, in the configuration the benchmark times (no initial
+    state, no final-state gradient, 4,096 chunk units on every SM); the float64 backward oracle follows two
+    of the 32 heads, each of which depends on its own head's inputs only."""
+    import kda_gated_delta_03_gb300 as kda
+    from oracle.backward import prefill_backward
+    w = I.workload("prefill_8k")
+    inp = I.prefill_inputs(w["seqlens"], w["H"], w["dk"], w["dv"], w["dtype"], w["seed"], state=w["state"])
+    T, H, d = inp["v"].shape
+    do = I.f32_to_bf16_bits(np.random.default_rng(8).standard_normal((T, H, d)).astype(np.float32))
+    args = [to_dev(inp[n], n in ("q", "k", "v")) for n in ("q", "k", "v", "beta", "alpha", "cu_seqlens")]
+    gq, gk, gv, gb, ga, gs = kda.kda_prefill_backward(*args, to_dev(do, True))
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_error() == 0
+    heads = [0, 21]
+    sub = dict(inp, H=len(heads))
+    for n in ("q", "k", "v", "beta", "alpha"):
+        sub[n] = np.ascontiguousarray(inp[n][:, heads])
+    ref = prefill_backward(sub, I.bf16_bits_to_f32(np.ascontiguousarray(do[:, heads])))
+    got = dict(dq=gq, dk=gk, dv=gv, dbeta=gb, dalpha=ga, d_state_in=gs)
+    for name, t in got.items():
+        g = t.double().cpu().numpy()[:, heads]
+        assert rel_frob(g, ref[name]) <= TOL, (name, rel_frob(g, ref[name]))
