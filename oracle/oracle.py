@@ -11,7 +11,8 @@ host threads (ctypes releases the GIL during the call).  What happens here
 besides marshalling is plain composition and storage: the alpha layouts of
 Gated DeltaNet and DeltaNet are expanded to per-channel alpha, a bf16-stored
 decode state is rounded to bf16 after each step, and snapshots are prefills of
-successive segments.  The backward pass is ``backward.py``.
+successive segments.  The backward pass is ``backward.py`` (token by token) and
+``chunked_backward.py`` (its chunkwise matrix form, pinned against it).
 """
 
 from __future__ import annotations
