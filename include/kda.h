@@ -301,6 +301,41 @@ KDA_API kda_status kda_prefill_noalloc(const void* q, const void* k, const void*
                                        float* state_out, void* o, void* stream);
 
 /*
+ * kda_prefill with q, k, v, beta, alpha, cu_seqlens, state_in, state_out and o
+ * in HOST memory (same shapes and dtypes as kda_prefill; alpha per key
+ * channel).  The inputs cross to the device segment by segment on an internal
+ * copy stream while earlier segments compute on `stream`, and each segment's o
+ * (and its sequences' final states) cross back on a second internal stream as
+ * soon as they are ready, so the transfers and the compute overlap.  One
+ * sequence is cut at multiples of 64 tokens with its state carried between
+ * segments (the same chunks as one kda_prefill call, so the same results);
+ * several sequences are grouped at sequence boundaries.
+ *
+ *   cu_seqlens       host [num_seqs + 1]: cu[0] = 0, non-decreasing,
+ *                    cu[num_seqs] = total_tokens (checked here, on the host)
+ *   state_in         host [num_seqs, H, d_k, d_v] float32, or NULL (zeros)
+ *   state_out, o     host outputs, written when `stream` completes
+ *   device_buffer    device memory of at least
+ *                    kda_prefill_host_buffer_size(...) bytes, 256-byte aligned,
+ *                    caller-owned: device copies of inputs and outputs and
+ *                    the prefill's workspace.  Reuse it only on `stream`.
+ *
+ * Asynchronous on `stream`: every host buffer must stay valid and unchanged
+ * until `stream` completes.  Pinned (page-locked) host memory is needed for
+ * the copies to overlap; pageable memory works but serialises them.  Returns
+ * KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED / KDA_ERR_WORKSPACE before any
+ * copy or launch, KDA_ERR_CUDA if a CUDA call fails.  As for kda_prefill, the
+ * "Kimi K3, explained" section "The math" defines what is computed.
+ */
+KDA_API size_t kda_prefill_host_buffer_size(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                                            int32_t d_v, kda_dtype dt);
+KDA_API kda_status kda_prefill_host(const void* q, const void* k, const void* v, const float* beta,
+                                    const float* alpha, const int32_t* cu_seqlens, int32_t num_seqs,
+                                    int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                                    float scale, const float* state_in, float* state_out, void* o,
+                                    void* device_buffer, size_t device_buffer_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  *bits (may be NULL) receives the KDA_DEVERR_* bits that were set.
  * Returns KDA_OK if none were set, KDA_ERR_DEVICE if some were, KDA_ERR_CUDA if

@@ -6,9 +6,9 @@ input generator (``inputs``) and the build step (``build``).
 """
 
 from .binding import (KdaError, kda_decode_step, kda_get_device_error, kda_prefill, kda_prefill_backward,
-                      kda_prefill_launch_count, kda_prefill_noalloc, kda_prefill_workspace_size, kda_status_string,
-                      load)
+                      kda_prefill_host, kda_prefill_launch_count, kda_prefill_noalloc, kda_prefill_workspace_size,
+                      kda_status_string, load)
 
 __all__ = ["KdaError", "kda_decode_step", "kda_get_device_error", "kda_prefill", "kda_prefill_backward",
-           "kda_prefill_launch_count", "kda_prefill_noalloc", "kda_prefill_workspace_size", "kda_status_string",
+           "kda_prefill_host", "kda_prefill_launch_count", "kda_prefill_noalloc", "kda_prefill_workspace_size", "kda_status_string",
            "load"]

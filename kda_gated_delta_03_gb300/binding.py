@@ -56,6 +56,9 @@ SIGNATURES = {
                                                   _i32, ctypes.c_int, _f32, _vp]),
     "kda_prefill_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
                                            ctypes.c_int, _f32, _vp, _vp, _vp, _vp]),
+    "kda_prefill_host_buffer_size": (_sz, [_i32, _i64, _i32, _i32, _i32, ctypes.c_int]),
+    "kda_prefill_host": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, ctypes.c_int,
+                                        _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "kda_get_device_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -225,6 +228,44 @@ def kda_prefill_noalloc(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scal
                                _stream(stream))
     if rc != KDA_OK:
         raise KdaError("kda_prefill_noalloc", rc)
+    return o, state_out
+
+
+def kda_prefill_host(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float = 1.0, state_out=None,
+                     o=None, device_buffer=None, stream=None):
+    """kda_prefill with every tensor in host memory (CPU tensors; pin them for the copies to overlap with
+    the compute).  The library streams the inputs to the device and the outputs back, segment by segment,
+    through `device_buffer` (a uint8 CUDA tensor of kda_prefill_host_buffer_size bytes, allocated here when
+    None).  Asynchronous on `stream`: synchronise it before reading the returned (o, state_out)."""
+    L = load()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    cpu = torch.device("cpu")
+    N = cu_seqlens.shape[0] - 1
+    _check("q", q, q.dtype, (T, H, dk), cpu)
+    _check("k", k, q.dtype, (T, H, dk), cpu)
+    _check("v", v, q.dtype, (T, H, dv), cpu)
+    _check("beta", beta, torch.float32, (T, H), cpu)
+    _check("alpha", alpha, torch.float32, (T, H, dk), cpu)
+    _check("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), cpu)
+    if state_in is not None:
+        _check("state_in", state_in, torch.float32, (N, H, dk, dv), cpu)
+    pin = q.is_pinned()
+    if state_out is None:
+        state_out = torch.empty((N, H, dk, dv), dtype=torch.float32, pin_memory=pin)
+    _check("state_out", state_out, torch.float32, (N, H, dk, dv), cpu)
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, pin_memory=pin)
+    _check("o", o, q.dtype, (T, H, dv), cpu)
+    need = int(L.kda_prefill_host_buffer_size(N, T, H, dk, dv, _dt(q.dtype)))
+    if device_buffer is None:
+        device_buffer = torch.empty(max(need, 1), dtype=torch.uint8, device=torch.device("cuda",
+                                                                                           torch.cuda.current_device()))
+    rc = L.kda_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(cu_seqlens), N, T, H, dk, dv,
+                            _dt(q.dtype), float(scale), _ptr(state_in), _ptr(state_out), _ptr(o), _ptr(device_buffer),
+                            device_buffer.numel() * device_buffer.element_size(), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError("kda_prefill_host", rc)
     return o, state_out
 
 

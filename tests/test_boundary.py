@@ -184,3 +184,37 @@ def test_alpha_layout_validation(lib):
     assert dec(binding.KDA_ALPHA_PER_HEAD, ctypes.c_void_p(0x10001)) == binding.KDA_ERR_INVALID_ARG
     assert dec(binding.KDA_ALPHA_PER_CHANNEL, None) == binding.KDA_ERR_INVALID_ARG
     assert dec(binding.KDA_ALPHA_PER_CHANNEL, P, 5) == binding.KDA_ERR_INVALID_ARG   # unknown state dtype
+
+
+# ---- kda_prefill_host: cu_seqlens is host memory, so all of it is checked on the host ----
+def host_prefill(lib, cu, N, T, d=128, dt=1, state_out=P, buf=P, buf_bytes=1 << 40):
+    arr = (ctypes.c_int32 * len(cu))(*cu)
+    return lib.kda_prefill_host(P, P, P, P, P, arr, N, T, 2, d, d, dt, 1.0, None, state_out, P, buf, buf_bytes, None)
+
+
+def test_host_prefill_buffer_size(lib):
+    # bf16 d=128, one sequence of 8192 tokens, H=32: device copies of q, k, v, beta, alpha, o, two states,
+    # the cu_seqlens area and the workspace of one 1024-token segment
+    rows = 8192 * 32
+    a = lambda x: (x + 255) // 256 * 256
+    want = a(rows * 256) * 3 + a(rows * 4) + a(rows * 512) + a(rows * 256) + 2 * a(32 * 128 * 128 * 4) + a(36 * 4)
+    want += a(lib.kda_prefill_workspace_size(1, 1024, 32, 128, 128, 1))
+    assert lib.kda_prefill_host_buffer_size(1, 8192, 32, 128, 128, 1) == want
+    assert lib.kda_prefill_host_buffer_size(0, 10, 2, 16, 16, 0) == 0
+    assert lib.kda_prefill_host_buffer_size(1, 10, 2, 32, 32, 0) == 0
+    assert lib.kda_prefill_host_buffer_size(2, 0, 2, 16, 16, 0) > 0
+
+
+def test_host_prefill_rejects_bad_arguments(lib):
+    OK_, INV, UNS, WS = 0, 1, 2, 3
+    assert host_prefill(lib, [1, 10], 1, 10) == INV                  # cu[0] != 0
+    assert host_prefill(lib, [0, 10, 5, 20], 3, 20) == INV           # decreasing
+    assert host_prefill(lib, [0, 10, 20], 2, 21) == INV              # cu[N] != T
+    assert host_prefill(lib, [0, 10], 1, 10, d=32) == UNS
+    assert host_prefill(lib, [0, 10], 1, 10, state_out=None) == INV
+    assert host_prefill(lib, [0, 10], 1, 10, buf=None) == WS
+    assert host_prefill(lib, [0, 10], 1, 10, buf=ctypes.c_void_p(0x10010)) == WS     # not 256-byte aligned
+    assert host_prefill(lib, [0, 10], 1, 10, buf_bytes=1024) == WS
+    assert lib.kda_prefill_host(P, P, P, P, P, None, 1, 10, 2, 16, 16, 0, 1.0, None, P, P, P, 1 << 40, None) == INV
+    assert lib.kda_prefill_host(None, P, P, P, P, (ctypes.c_int32 * 2)(0, 10), 1, 10, 2, 16, 16, 0, 1.0, None, P,
+                                P, P, 1 << 40, None) == INV
