@@ -135,6 +135,13 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t tlane = (uint32_t)(quad * 32) << 16;
+    // TMEM columns: [M | B] of step 6 at 0..255 and [P W | P Utilde] at 256..511; the A/P and [W | Utilde]^T
+    // products of steps 2 and 4 use 256..383, so that a unit's M, B and P Utilde can stay in TMEM and drain
+    // to its record while the next unit runs its steps 1-5
+    constexpr uint32_t TM_W = 2 * DK;
+    const int mi = 32 * quad + lane;                         // M=128 accumulator row of this thread
+    const int mr = 16 * quad + lane;                         // M=64 accumulator row (lanes < 16)
+    unsigned char* rec_prev = nullptr;                       // record whose M, B, P Utilde are still in TMEM
     uint32_t phase = 0;
 
     auto wait_mma = [&]() -> bool {
@@ -167,6 +174,41 @@ __global__ void __launch_bounds__(NT, 1)
             tma_load_3d(saddr(sm + P_OFF_V), &maps.v, 0, hu, tu, lbar);
         }
     };
+    // piece 0-1: M (columns 0..127, TF32 rows 64.. of [Q'; M]); 2-3: B (128..255, fp32); 4: P Utilde
+    // (384..511, lanes of rows 0..63).  Warp-collective; every thread calls it.
+    auto drain = [&](int piece) {
+        if (!rec_prev) return;
+        tc_fence_after();
+        float v[32];
+        if (piece < 4) {
+            const int c0 = 64 * half + 32 * (piece & 1);
+            tmem_ld32(tmem + tlane + (piece >= 2 ? DK : 0) + c0, v);
+            if (piece < 2) {
+#pragma unroll
+                for (int x = 0; x < 32; x += 4)
+                    *reinterpret_cast<float4*>(rec_prev + REC_QM + op_off(C + mi, c0 + x, DK)) =
+                        make_float4(tf32r(v[x]), tf32r(v[x + 1]), tf32r(v[x + 2]), tf32r(v[x + 3]));
+            } else {
+#pragma unroll
+                for (int x = 0; x < 32; x += 4)
+                    *reinterpret_cast<float4*>(rec_prev + REC_B + (((c0 + x) >> 2) * DK + mi) * 16) =
+                        make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+            }
+        } else {
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+                const int c0 = 64 * half + 32 * cb;
+                tmem_ld32(tmem + tlane + 3 * DK + c0, v);
+                if (lane < 16) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 4)
+                        *reinterpret_cast<float4*>(rec_prev + REC_O + (((c0 + x) >> 2) * C + mr) * 16) =
+                            make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+                }
+            }
+        }
+        tc_fence_before();
+    };
     uint32_t lph = 0;
     bool load_pending = (int)blockIdx.x < n_units;
     float beta_next = 0.f, alpha_next = 1.f;          // this thread's token row of the next unit
@@ -196,7 +238,6 @@ __global__ void __launch_bounds__(NT, 1)
         }
         lph ^= 1u;
         load_pending = false;
-        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");   // staging is free
         tc_fence_before();
         __syncthreads();
         if (*s_abort) break;
@@ -233,6 +274,7 @@ __global__ void __launch_bounds__(NT, 1)
                 sgam[ch] = ex2f(la[31] + base);
             }
         }
+        drain(0);
         __syncthreads();
 
         // ---- 2. A and P: per 16-row block b, R_b [Lk_b; Lq_b]^T on tcgen05 (M=64, N=32, K=128) ----
@@ -299,7 +341,7 @@ __global__ void __launch_bounds__(NT, 1)
             for (int ks = 0; ks < DK / 8; ++ks) {
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
-                    umma_tf32_1(tmem + 32 * b, ad[b] + (uint64_t)(ks * 16), bdsc[b] + (uint64_t)(ks * 16), id,
+                    umma_tf32_1(tmem + TM_W + 32 * b, ad[b] + (uint64_t)(ks * 16), bdsc[b] + (uint64_t)(ks * 16), id,
                                 ks > 0 ? 1u : 0u);
             }
             umma_commit(mbar);
@@ -311,7 +353,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int bb = 0; bb < 2; ++bb) {
                 const int b = 2 * half + bb;
-                tmem_ld32(tmem + tlane + 32 * b, v);
+                tmem_ld32(tmem + tlane + TM_W + 32 * b, v);
                 if (lane < 16) {
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
@@ -322,6 +364,7 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
         }
+        drain(1);
         tc_fence_before();
         __syncthreads();
 
@@ -385,6 +428,7 @@ __global__ void __launch_bounds__(NT, 1)
                 __syncthreads();
             }
         }
+        drain(2);
         // T' = T Diag(beta) -> operand (M=64, K=64)
         for (int e = tid; e < C * 16; e += NT) {
             const int r = ((e >> 7) << 3) | (e & 7), m0 = 4 * ((e >> 3) & 15);
@@ -407,6 +451,7 @@ __global__ void __launch_bounds__(NT, 1)
                 make_float4(bf(vraw + (m0 + 0) * DK + i), bf(vraw + (m0 + 1) * DK + i), bf(vraw + (m0 + 2) * DK + i),
                             bf(vraw + (m0 + 3) * DK + i));
         }
+        drain(3);
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -419,13 +464,15 @@ __global__ void __launch_bounds__(NT, 1)
             const uint64_t bt = op_desc(saddr(X + PS_OPT), C);
 #pragma unroll
             for (int ks = 0; ks < C / 8; ++ks) {
-                umma_tf32_1(tmem, aw + (uint64_t)(ks * 16), bt + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
-                umma_tf32_1(tmem + C, au + (uint64_t)(ks * 16), bt + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
+                umma_tf32_1(tmem + TM_W, aw + (uint64_t)(ks * 16), bt + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
+                umma_tf32_1(tmem + TM_W + C, au + (uint64_t)(ks * 16), bt + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
             }
             umma_commit(mbar);
         }
         if (!wait_mma()) break;
 
+        drain(4);
+        rec_prev = nullptr;
         // ---- 5. fold operands: [W | Utilde]^T (N=256, K=64) and Khat^T (M=128, K=64) ----
         unsigned char* opWU = X + PS_WU;
         unsigned char* opKH = X + PS_KH;
@@ -434,7 +481,7 @@ __global__ void __launch_bounds__(NT, 1)
             float v[32];
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
-                tmem_ld32(tmem + tlane + C * half + 32 * cb, v);
+                tmem_ld32(tmem + tlane + TM_W + C * half + 32 * cb, v);
 #pragma unroll
                 for (int x = 0; x < 32; x += 4)
                     *reinterpret_cast<float4*>(opWU + op_off(n, 32 * cb + x, C)) =
@@ -473,9 +520,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         if (!wait_mma()) break;
 
-        // ---- 7. the record, from TMEM straight to global memory ----
-        const int i = 32 * quad + lane;                          // M=128 accumulator row
-        const int r = 16 * quad + lane;                          // M=64 accumulator row (lanes < 16)
+        // ---- 7. the record: Q' and Gamma_C now; M, B and P Utilde stay in TMEM and drain during the next unit ----
         float v[32];
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {                         // Q' = Gamma.Q - P W -> rows 0..63 of [Q'; M]
@@ -484,10 +529,10 @@ __global__ void __launch_bounds__(NT, 1)
             if (lane < 16) {
 #pragma unroll
                 for (int x = 0; x < 32; x += 4) {
-                    const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(r, c0 + x));
-                    const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(r, c0 + x));
+                    const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(mr, c0 + x));
+                    const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(mr, c0 + x));
                     const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
-                    *reinterpret_cast<float4*>(rec + REC_QM + op_off(r, c0 + x, DK)) =
+                    *reinterpret_cast<float4*>(rec + REC_QM + op_off(mr, c0 + x, DK)) =
                         make_float4(tf32r(ex2f(gg.x) * __low2float(q2[0]) - v[x]),
                                     tf32r(ex2f(gg.y) * __high2float(q2[0]) - v[x + 1]),
                                     tf32r(ex2f(gg.z) * __low2float(q2[1]) - v[x + 2]),
@@ -496,29 +541,10 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         if (tid < DK) reinterpret_cast<float*>(rec + REC_G)[tid] = sgam[tid];
-        // M and B are staged in the scratch (free once the fold products are done) in their record byte
-        // layout and written by two bulk copies, which drain while the next unit starts
-        unsigned char* stage = X;                                // [M rows of [Q'; M] (64 KiB) | B (64 KiB)]
-#pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {                         // M = Khat^T W -> rows 64.. of [Q'; M]
-            const int c0 = 64 * half + 32 * cb;
-            tmem_ld32(tmem + tlane + c0, v);
-#pragma unroll
-            for (int x = 0; x < 32; x += 4)
-                *reinterpret_cast<float4*>(stage + op_off(C + i, c0 + x, DK) - C * DK * 4) =
-                    make_float4(tf32r(v[x]), tf32r(v[x + 1]), tf32r(v[x + 2]), tf32r(v[x + 3]));
-        }
-#pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {                         // B = Khat^T Utilde
-            const int c0 = 64 * half + 32 * cb;
-            tmem_ld32(tmem + tlane + DK + c0, v);
-#pragma unroll
-            for (int x = 0; x < 32; x += 4)
-                *reinterpret_cast<float4*>(stage + DK * DK * 4 + (((c0 + x) >> 2) * DK + i) * 16) =
-                    make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
-        }
+        rec_prev = rec;
         fence_async_smem();
-        __syncthreads();                                         // staged; the raw tiles are free
+        tc_fence_before();
+        __syncthreads();                                         // the raw tiles are free
         const int un = u + (int)gridDim.x;
         if (un < n_units) {                                      // fetch the next unit's tiles and beta
             issue_loads(un);
@@ -530,26 +556,11 @@ __global__ void __launch_bounds__(NT, 1)
                 alpha_next = per_head && tn + tid < p.total_tokens ? p.alpha[row] : 1.f;
             }
         }
-        if (tid == 0) {
-            bulk_s2g(rec + REC_QM + C * DK * 4, saddr(stage), DK * DK * 4);
-            bulk_s2g(rec + REC_B, saddr(stage + DK * DK * 4), DK * DK * 4);
-            asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
-        }
-#pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {                         // P Utilde
-            const int c0 = 64 * half + 32 * cb;
-            tmem_ld32(tmem + tlane + 3 * DK + c0, v);
-            if (lane < 16) {
-#pragma unroll
-                for (int x = 0; x < 32; x += 4)
-                    *reinterpret_cast<float4*>(rec + REC_O + (((c0 + x) >> 2) * C + r) * 16) =
-                        make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
-            }
-        }
-        tc_fence_before();
     }
 
-    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+    // the last unit's M, B and P Utilde (not after an abort: the products may not have completed)
+    if (!*s_abort)
+        for (int piece = 0; piece < 5; ++piece) drain(piece);
     if (load_pending) mbar_wait(lbar, lph);              // bounded: never leave copies in flight
     tc_fence_before();
     __syncthreads();
