@@ -36,7 +36,8 @@ constexpr int REC_BYTES = 197120;
 constexpr int QM_BYTES = (C + DK) * DK * 4;
 constexpr int SNV = 32;            // value columns per chain CTA
 constexpr int SLICES = DK / SNV;
-constexpr size_t kBufBudget = size_t(256) << 20;      // record bytes per window buffer (two buffers at most)
+constexpr size_t kBufBudget = size_t(256) << 20;      // record bytes per buffer of the overlapped schedule
+constexpr size_t kOneWindowBudget = size_t(1) << 30;  // record bytes of the workspace, at most
 static_assert(QM_BYTES == REC_B && REC_B + DK * DK * 4 == REC_O && REC_O + C * DK * 4 == REC_G, "record layout");
 
 // ---- phase 1 shared memory ----
@@ -178,6 +179,7 @@ __global__ void __launch_bounds__(NT, 1)
     // (384..511, lanes of rows 0..63).  Warp-collective; every thread calls it.
     auto drain = [&](int piece) {
         if (!rec_prev) return;
+        __syncwarp();                                        // converged after an elected-lane MMA issue
         tc_fence_after();
         float v[32];
         if (piece < 4) {
@@ -274,7 +276,6 @@ __global__ void __launch_bounds__(NT, 1)
                 sgam[ch] = ex2f(la[31] + base);
             }
         }
-        drain(0);
         __syncthreads();
 
         // ---- 2. A and P: per 16-row block b, R_b [Lk_b; Lq_b]^T on tcgen05 (M=64, N=32, K=128) ----
@@ -346,6 +347,8 @@ __global__ void __launch_bounds__(NT, 1)
             }
             umma_commit(mbar);
         }
+        drain(0);                                       // while the products run
+        drain(1);
         if (!wait_mma()) break;
         {                                               // scatter: A (fp32) and P (TF32 operand)
             const int sr = 16 * quad + lane;
@@ -364,7 +367,6 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
         }
-        drain(1);
         tc_fence_before();
         __syncthreads();
 
@@ -428,7 +430,6 @@ __global__ void __launch_bounds__(NT, 1)
                 __syncthreads();
             }
         }
-        drain(2);
         // T' = T Diag(beta) -> operand (M=64, K=64)
         for (int e = tid; e < C * 16; e += NT) {
             const int r = ((e >> 7) << 3) | (e & 7), m0 = 4 * ((e >> 3) & 15);
@@ -451,7 +452,6 @@ __global__ void __launch_bounds__(NT, 1)
                 make_float4(bf(vraw + (m0 + 0) * DK + i), bf(vraw + (m0 + 1) * DK + i), bf(vraw + (m0 + 2) * DK + i),
                             bf(vraw + (m0 + 3) * DK + i));
         }
-        drain(3);
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -469,10 +469,10 @@ __global__ void __launch_bounds__(NT, 1)
             }
             umma_commit(mbar);
         }
+        drain(2);                                       // while the products run
+        drain(3);
         if (!wait_mma()) break;
 
-        drain(4);
-        rec_prev = nullptr;
         // ---- 5. fold operands: [W | Utilde]^T (N=256, K=64) and Khat^T (M=128, K=64) ----
         unsigned char* opWU = X + PS_WU;
         unsigned char* opKH = X + PS_KH;
@@ -498,6 +498,8 @@ __global__ void __launch_bounds__(NT, 1)
                 make_float4(tf32r(ex2f(gl - gg[0]) * kk4[0]), tf32r(ex2f(gl - gg[1]) * kk4[1]),
                             tf32r(ex2f(gl - gg[2]) * kk4[2]), tf32r(ex2f(gl - gg[3]) * kk4[3]));
         }
+        drain(4);                                       // the last piece, before step 6 writes its columns
+        rec_prev = nullptr;
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -866,7 +868,9 @@ bool prefill_2p_supported(int32_t num_seqs, int64_t total_tokens, int32_t H, int
 size_t prefill_2p_min_workspace(int32_t H) { return (size_t)H * REC_BYTES; }
 
 size_t prefill_2p_workspace(int64_t total_tokens, int32_t H) {
-    const int64_t chunks = (total_tokens + C - 1) / C, cap = 2 * buffer_chunks(H);
+    const int64_t chunks = (total_tokens + C - 1) / C;
+    int64_t cap = (int64_t)(kOneWindowBudget / ((size_t)H * REC_BYTES));
+    if (cap < 2 * buffer_chunks(H)) cap = 2 * buffer_chunks(H);
     return (size_t)(chunks < cap ? chunks : cap) * H * REC_BYTES;
 }
 
@@ -875,12 +879,12 @@ WindowPlan prefill_2p_plan(int64_t chunks, int32_t H, size_t workspace_bytes, in
     const int64_t one = buffer_chunks(H);
     const bool overlap_ok = 2 * H * SLICES <= sms;   // the chain leaves at least half the SMs to phase 1
     WindowPlan w;
-    if (chunks <= cap && chunks <= 2 * one) {
-        w.window = chunks; w.buffers = 1;             // one window
-    } else if (overlap_ok && cap >= 2) {
+    if (overlap_ok && chunks > one && cap >= 2) {
+        // few heads: phase 1 of the next window runs beside the chain of this one, on double buffers
         w.window = cap / 2 < one ? cap / 2 : one; w.buffers = 2;
     } else {
-        w.window = cap < 2 * one ? cap : 2 * one; w.buffers = 1;
+        // many heads: the chain occupies most SMs, so the windows run back to back, as few as fit
+        w.window = chunks < cap ? chunks : cap; w.buffers = 1;
     }
     if (w.window < 1) w.window = 1;
     return w;

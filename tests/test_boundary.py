@@ -53,9 +53,10 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # one bf16 d=128 sequence: 197,120 bytes of records per (chunk, head), windows of at most 512 MiB
-    assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 1) == 84 * 32 * 197120
-    assert lib.kda_prefill_workspace_size(1, 1_032_192, 8, 128, 128, 1) == 340 * 8 * 197120
+    # one bf16 d=128 sequence: 197,120 bytes of records per (chunk, head), at most 1 GiB of them
+    assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 1) == 128 * 32 * 197120
+    assert lib.kda_prefill_workspace_size(1, 1_032_192, 8, 128, 128, 1) == 680 * 8 * 197120
+    assert lib.kda_prefill_workspace_size(1, 1 << 20, 32, 128, 128, 1) == 170 * 32 * 197120
     assert lib.kda_prefill_workspace_size(1, 65, 4, 128, 128, 1) == 2 * 4 * 197120
     assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 0) == 0      # fp32: single-kernel path
     assert lib.kda_prefill_workspace_size(1, 8192, 32, 64, 64, 1) == 0
