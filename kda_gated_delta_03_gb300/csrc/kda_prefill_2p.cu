@@ -116,13 +116,17 @@ __global__ void __launch_bounds__(NT, 1)
     unsigned char* X = sm + P_OFF_S;
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + P_OFF_MISC + 12);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P_OFF_MISC + 8);
+    // lbar: the q and alpha tiles; vkbar: the v and k tiles, which are fetched earlier (v once step 3 has
+    // read this unit's v, k once step 5 has read its k)
     const uint32_t mbar = saddr(sm + P_OFF_MISC), lbar = saddr(sm + P_OFF_MISC + 16);
+    const uint32_t vkbar = saddr(sm + P_OFF_MISC + 24);
     auto Gat = [&](int r, int i) -> float& { return *reinterpret_cast<float*>(sm + OFF_G + g_off(r, i)); };
     auto kat = [&](int r, int i) { return bf(reinterpret_cast<const __nv_bfloat16*>(sm + OFF_K + kq_off(r, i))); };
 
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar) : "memory");
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(lbar) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(vkbar) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *s_abort = 0;
     }
@@ -156,15 +160,33 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_after();
         return true;
     };
-    // raw tiles of unit u by TMA (v with one 128-column box)
-    auto issue_loads = [&](int u) {
+    // raw tiles of unit u by TMA (v with one 128-column box), in three groups
+    auto unit_rows = [&](int u, int& hu, int32_t& tu) {
+        hu = u % H;
+        tu = (int32_t)(c_begin + u / H) * C;
+    };
+    auto issue_v = [&](int u) {                      // arms vkbar for v and k together
         if (tid == 32) {
-            const int hu = u % H;
-            const int32_t tu = (int32_t)(c_begin + u / H) * C;
+            int hu; int32_t tu;
+            unit_rows(u, hu, tu);
+            mbar_expect_tx(vkbar, 16384 + C * DK * 2);
+            tma_load_3d(saddr(sm + P_OFF_V), &maps.v, 0, hu, tu, vkbar);
+        }
+    };
+    auto issue_k = [&](int u) {
+        if (tid == 32) {
+            int hu; int32_t tu;
+            unit_rows(u, hu, tu);
+            tma_load_3d(saddr(sm + OFF_K), &maps.k, 0, hu, tu, vkbar);
+            tma_load_3d(saddr(sm + OFF_K + 8192), &maps.k, 64, hu, tu, vkbar);
+        }
+    };
+    auto issue_qa = [&](int u) {
+        if (tid == 32) {
+            int hu; int32_t tu;
+            unit_rows(u, hu, tu);
             const bool per_channel = p.alpha_mode == KDA_ALPHA_PER_CHANNEL;
-            mbar_expect_tx(lbar, 2 * 16384 + (per_channel ? 32768 : 0) + C * DK * 2);
-            tma_load_3d(saddr(sm + OFF_K), &maps.k, 0, hu, tu, lbar);
-            tma_load_3d(saddr(sm + OFF_K + 8192), &maps.k, 64, hu, tu, lbar);
+            mbar_expect_tx(lbar, 16384 + (per_channel ? 32768 : 0));
             tma_load_3d(saddr(sm + OFF_Q), &maps.q, 0, hu, tu, lbar);
             tma_load_3d(saddr(sm + OFF_Q + 8192), &maps.q, 64, hu, tu, lbar);
             if (per_channel) {
@@ -172,7 +194,6 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int b = 0; b < 4; ++b)
                     tma_load_3d(saddr(sm + OFF_G + b * 8192), &maps.a, 32 * b, hu, tu, lbar);
             }
-            tma_load_3d(saddr(sm + P_OFF_V), &maps.v, 0, hu, tu, lbar);
         }
     };
     // piece 0-1: M (columns 0..127, TF32 rows 64.. of [Q'; M]); 2-3: B (128..255, fp32); 4: P Utilde
@@ -211,12 +232,16 @@ __global__ void __launch_bounds__(NT, 1)
         }
         tc_fence_before();
     };
-    uint32_t lph = 0;
-    bool load_pending = (int)blockIdx.x < n_units;
+    uint32_t lph = 0, vkph = 0;
+    bool load_pending = (int)blockIdx.x < n_units;   // q and alpha of the next unit in flight
+    bool vk_pending = load_pending;                   // v (and k) of the next unit in flight
+    bool k_issued = load_pending;
     float beta_next = 0.f, alpha_next = 1.f;          // this thread's token row of the next unit
     const bool per_head = p.alpha_mode == KDA_ALPHA_PER_HEAD;
     if (load_pending) {
-        issue_loads(blockIdx.x);
+        issue_v(blockIdx.x);
+        issue_k(blockIdx.x);
+        issue_qa(blockIdx.x);
         const int32_t tn = (int32_t)(c_begin + (int)blockIdx.x / H) * C;
         if (tid < C && tn + tid < p.total_tokens) {
             const int64_t row = (int64_t)(tn + tid) * H + (int)blockIdx.x % H;
@@ -230,16 +255,18 @@ __global__ void __launch_bounds__(NT, 1)
         const int32_t t0 = (int32_t)(c_begin + cw) * C;
         const int L = min(C, p.total_tokens - t0);
         unsigned char* rec = records + (size_t)u * REC_BYTES;
+        const int un = u + (int)gridDim.x;                       // this CTA's next unit
         if (tid < C) {
             sbeta[tid] = beta_next;
             sasc[tid] = alpha_next;
         }
-        if (!mbar_wait(lbar, lph)) {
+        if (!mbar_wait(vkbar, vkph) || !mbar_wait(lbar, lph)) {
             atomicOr(p.err, KDA_DEVERR_TIMEOUT);
             *s_abort = 1;
         }
         lph ^= 1u;
-        load_pending = false;
+        vkph ^= 1u;
+        load_pending = vk_pending = false;
         tc_fence_before();
         __syncthreads();
         if (*s_abort) break;
@@ -455,6 +482,11 @@ __global__ void __launch_bounds__(NT, 1)
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        if (un < n_units) {                                      // this unit's v is read: fetch the next v
+            issue_v(un);
+            vk_pending = true;
+            k_issued = false;
+        }
 
         // ---- 4. [W | Utilde]^T = [Gamma.K | V]^T T'^T  (two M=128 halves, N=64, K=64) ----
         if (warp == 0 && elect_one()) {
@@ -503,6 +535,10 @@ __global__ void __launch_bounds__(NT, 1)
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        if (un < n_units) {                                      // this unit's k is read: fetch the next k
+            issue_k(un);
+            k_issued = true;
+        }
 
         // ---- 6. [M | B] = Khat^T [W | Utilde] (M=128) and [PW | P Utilde] = P [W | Utilde] (M=64); N=256, K=64 ----
         if (warp == 0) {
@@ -546,10 +582,9 @@ __global__ void __launch_bounds__(NT, 1)
         rec_prev = rec;
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();                                         // the raw tiles are free
-        const int un = u + (int)gridDim.x;
-        if (un < n_units) {                                      // fetch the next unit's tiles and beta
-            issue_loads(un);
+        __syncthreads();                                         // q and alpha (g) are read
+        if (un < n_units) {                                      // fetch the next unit's q, alpha and beta
+            issue_qa(un);
             load_pending = true;
             if (tid < C) {
                 const int32_t tn = (int32_t)(c_begin + un / H) * C;
@@ -563,7 +598,11 @@ __global__ void __launch_bounds__(NT, 1)
     // the last unit's M, B and P Utilde (not after an abort: the products may not have completed)
     if (!*s_abort)
         for (int piece = 0; piece < 5; ++piece) drain(piece);
-    if (load_pending) mbar_wait(lbar, lph);              // bounded: never leave copies in flight
+    // bounded: never leave copies in flight (after an abort between the v and k fetches the k tiles are
+    // fetched too, so that vkbar's phase can complete)
+    if (vk_pending && !k_issued) issue_k(blockIdx.x);
+    if (vk_pending) mbar_wait(vkbar, vkph);
+    if (load_pending) mbar_wait(lbar, lph);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
