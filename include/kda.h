@@ -83,6 +83,8 @@ typedef enum {
 #define KDA_DEVERR_STATE_IDX 0x2u   /* decode state_idx entry outside [0, num_slots)          */
 #define KDA_DEVERR_TIMEOUT 0x4u     /* a bounded wait inside a kernel gave up (work abandoned) */
 #define KDA_DEVERR_SNAPSHOTS 0x8u   /* snapshot_offsets disagree with the sequence lengths       */
+#define KDA_DEVERR_RANGE 0x10u      /* one-sequence bf16 d=128 prefill: a state or folded chunk
+                                       value beyond fp16's range (|x| > 65504); results invalid */
 
 /*
  * Bytes of device workspace kda_prefill needs for this problem (0 is a valid

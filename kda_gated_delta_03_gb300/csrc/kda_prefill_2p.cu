@@ -28,12 +28,15 @@ namespace kda {
 namespace {
 
 // ---- one (head, chunk) record in the workspace ----
-constexpr int REC_QM = 0;          // [Q'; M]: 192 x 128 TF32 K-major operand (96 KiB)
-constexpr int REC_B = 98304;       // B = Khat^T Utilde: fp32 [32 column quads][128 rows][4] (64 KiB)
-constexpr int REC_O = 163840;      // P Utilde: fp32 [32 column quads][64 rows][4] (32 KiB)
-constexpr int REC_G = 196608;      // Gamma_C: fp32 [128]
-constexpr int REC_BYTES = 197120;
-constexpr int QM_BYTES = (C + DK) * DK * 4;
+constexpr int REC_QM = 0;          // [Q'; M]: 192 x 128 fp16 K-major operand (48 KiB)
+constexpr int REC_B = 49152;       // B = Khat^T Utilde: fp32 [32 column quads][128 rows][4] (64 KiB)
+constexpr int REC_O = 114688;      // P Utilde: fp32 [32 column quads][64 rows][4] (32 KiB)
+constexpr int REC_G = 147456;      // Gamma_C: fp32 [128]
+constexpr int REC_BYTES = 147968;
+constexpr int QM_BYTES = (C + DK) * DK * 2;
+// Q', M and the chain's state operand are fp16: the same 10-bit significand as TF32, in half the bytes,
+// for values within fp16's range, which the kernels check (KDA_DEVERR_RANGE)
+constexpr float kF16Max = 65504.f;
 constexpr int SNV = 32;            // value columns per chain CTA
 constexpr int SLICES = DK / SNV;
 constexpr size_t kBufBudget = size_t(256) << 20;      // record bytes per buffer of the overlapped schedule
@@ -57,7 +60,7 @@ static_assert(PS_KH + DK * C * 4 <= PS_P, "phase-1 fold operands");
 static_assert(P_SMEM <= 232448, "phase-1 shared memory");
 
 // ---- phase 2 shared memory and threads ----
-constexpr int SOP_BYTES = SNV * DK * 4;            // S^T operand: TF32 32 x 128, 128-byte swizzle
+constexpr int SOP_BYTES = SNV * DK * 2;            // S^T operand: fp16 32 x 128, 128-byte swizzle
 constexpr int C_OFF_S = 2 * QM_BYTES;              // two record buffers, then two S^T operands
 constexpr int C_OFF_MISC = C_OFF_S + 2 * SOP_BYTES;
 constexpr int C_SMEM = C_OFF_MISC + 128;
@@ -80,6 +83,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __device__ __forceinline__ bool valid_single_sequence(const PrefillParams& p) {
@@ -198,6 +206,7 @@ __global__ void __launch_bounds__(NT, 1)
     };
     // piece 0-1: M (columns 0..127, TF32 rows 64.. of [Q'; M]); 2-3: B (128..255, fp32); 4: P Utilde
     // (384..511, lanes of rows 0..63).  Warp-collective; every thread calls it.
+    bool big = false;                                        // a value outside fp16's range was seen
     auto drain = [&](int piece) {
         if (!rec_prev) return;
         __syncwarp();                                        // converged after an elected-lane MMA issue
@@ -208,9 +217,11 @@ __global__ void __launch_bounds__(NT, 1)
             tmem_ld32(tmem + tlane + (piece >= 2 ? DK : 0) + c0, v);
             if (piece < 2) {
 #pragma unroll
-                for (int x = 0; x < 32; x += 4)
-                    *reinterpret_cast<float4*>(rec_prev + REC_QM + op_off(C + mi, c0 + x, DK)) =
-                        make_float4(tf32r(v[x]), tf32r(v[x + 1]), tf32r(v[x + 2]), tf32r(v[x + 3]));
+                for (int x = 0; x < 32; x += 4) {
+                    big |= fmaxf(fmaxf(fabsf(v[x]), fabsf(v[x + 1])), fmaxf(fabsf(v[x + 2]), fabsf(v[x + 3]))) > kF16Max;
+                    *reinterpret_cast<uint2*>(rec_prev + REC_QM + op_off_h(C + mi, c0 + x, DK)) =
+                        make_uint2(pack_half2(v[x], v[x + 1]), pack_half2(v[x + 2], v[x + 3]));
+                }
             } else {
 #pragma unroll
                 for (int x = 0; x < 32; x += 4)
@@ -570,11 +581,13 @@ __global__ void __launch_bounds__(NT, 1)
                     const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(mr, c0 + x));
                     const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(mr, c0 + x));
                     const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
-                    *reinterpret_cast<float4*>(rec + REC_QM + op_off(mr, c0 + x, DK)) =
-                        make_float4(tf32r(ex2f(gg.x) * __low2float(q2[0]) - v[x]),
-                                    tf32r(ex2f(gg.y) * __high2float(q2[0]) - v[x + 1]),
-                                    tf32r(ex2f(gg.z) * __low2float(q2[1]) - v[x + 2]),
-                                    tf32r(ex2f(gg.w) * __high2float(q2[1]) - v[x + 3]));
+                    const float a0 = ex2f(gg.x) * __low2float(q2[0]) - v[x];
+                    const float a1 = ex2f(gg.y) * __high2float(q2[0]) - v[x + 1];
+                    const float a2 = ex2f(gg.z) * __low2float(q2[1]) - v[x + 2];
+                    const float a3 = ex2f(gg.w) * __high2float(q2[1]) - v[x + 3];
+                    big |= fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))) > kF16Max;
+                    *reinterpret_cast<uint2*>(rec + REC_QM + op_off_h(mr, c0 + x, DK)) =
+                        make_uint2(pack_half2(a0, a1), pack_half2(a2, a3));
                 }
             }
         }
@@ -600,6 +613,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int piece = 0; piece < 5; ++piece) drain(piece);
     // bounded: never leave copies in flight (after an abort between the v and k fetches the k tiles are
     // fetched too, so that vkbar's phase can complete)
+    if (big) atomicOr(p.err, KDA_DEVERR_RANGE);
     if (vk_pending && !k_issued) issue_k(blockIdx.x);
     if (vk_pending) mbar_wait(vkbar, vkph);
     if (load_pending) mbar_wait(lbar, lph);
@@ -684,7 +698,7 @@ __global__ void __launch_bounds__(C_NT, 1)
     const uint32_t sop0 = saddr(sm + C_OFF_S);
     if (warp == 8) {
         // ---------------- products: M S_c (sequential path), then [Q'; M_top] S_c ----------------
-        const uint64_t a_s0 = op_desc(saddr(sm) + C * DK * 4, DK), a_o0 = op_desc(saddr(sm), DK);
+        const uint64_t a_s0 = op_desc_h(saddr(sm) + C * DK * 2, DK), a_o0 = op_desc_h(saddr(sm), DK);
         const uint64_t b_s0 = desc_sw128(sop0);
         int issued = 0;                               // chunks whose products were issued
         for (int ci = 0; ci < n_chunks; ++ci) {
@@ -700,16 +714,16 @@ __global__ void __launch_bounds__(C_NT, 1)
                 const uint64_t bs = b_s0 + (uint64_t)((b * SOP_BYTES) >> 4);
                 const uint64_t as = a_s0 + (uint64_t)((b * QM_BYTES) >> 4), ao = a_o0 + (uint64_t)((b * QM_BYTES) >> 4);
 #pragma unroll
-                for (int ks = 0; ks < DK / 8; ++ks)
-                    umma_tf32_1(tmem + TM_S, as + (uint64_t)(ks * 16),
-                                bs + (uint64_t)(((ks >> 2) * (SNV * 128) + (ks & 3) * 32) >> 4), idesc_tf32(128, SNV),
-                                ks > 0 ? 1u : 0u);
+                for (int ks = 0; ks < DK / 16; ++ks)           // 16 fp16 = 32 bytes of K per step
+                    umma_f16_1(tmem + TM_S, as + (uint64_t)(ks * 16),
+                               bs + (uint64_t)(((ks >> 2) * (SNV * 128) + (ks & 3) * 32) >> 4), idesc_f16(128, SNV),
+                               ks > 0 ? 1u : 0u);
                 umma_commit(dbar + 8 * b);
 #pragma unroll
-                for (int ks = 0; ks < DK / 8; ++ks)
-                    umma_tf32_1(tmem + TM_O + SNV * b, ao + (uint64_t)(ks * 16),
-                                bs + (uint64_t)(((ks >> 2) * (SNV * 128) + (ks & 3) * 32) >> 4), idesc_tf32(128, SNV),
-                                ks > 0 ? 1u : 0u);
+                for (int ks = 0; ks < DK / 16; ++ks)
+                    umma_f16_1(tmem + TM_O + SNV * b, ao + (uint64_t)(ks * 16),
+                               bs + (uint64_t)(((ks >> 2) * (SNV * 128) + (ks & 3) * 32) >> 4), idesc_f16(128, SNV),
+                               ks > 0 ? 1u : 0u);
                 umma_commit(obar + 8 * b);
             }
             __syncwarp();
@@ -788,11 +802,14 @@ __global__ void __launch_bounds__(C_NT, 1)
                                        : make_float4(0.f, 0.f, 0.f, 0.f);
             S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
         }
-        auto write_state_operand = [&](int b) {      // S^T: row = value column, K = srow
+        bool big = false;                             // a state value outside fp16's range was seen
+        auto write_state_operand = [&](int b) {      // S^T: row = value column, K = srow, fp16
             unsigned char* sop = sm + C_OFF_S + b * SOP_BYTES;
 #pragma unroll
-            for (int j = 0; j < CPT; ++j)
-                *reinterpret_cast<float*>(sop + sw128_off(CPT * half + j, srow, SNV)) = tf32r(S[j]);
+            for (int j = 0; j < CPT; ++j) {
+                big |= fabsf(S[j]) > kF16Max;
+                *reinterpret_cast<__half*>(sop + sw128_off_h(CPT * half + j, srow, SNV)) = __float2half_rn(S[j]);
+            }
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(sbar);
@@ -855,6 +872,7 @@ __global__ void __launch_bounds__(C_NT, 1)
                 *reinterpret_cast<float4*>(p.state_out + state_off + j) =
                     make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
+        if (big) atomicOr(p.err, KDA_DEVERR_RANGE);
     }
     tc_fence_before();
     __syncthreads();

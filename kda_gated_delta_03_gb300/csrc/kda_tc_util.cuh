@@ -64,6 +64,8 @@ __device__ __forceinline__ uint64_t desc_sbo(uint32_t addr, uint32_t sbo) {
            (1ull << 46);
 }
 __device__ __forceinline__ uint64_t op_desc(uint32_t addr, int K) { return desc_sbo(addr, (uint32_t)K * 32u); }
+// The same for a 16-bit operand (op_off_h layout: 8-row groups K*16 B apart).
+__device__ __forceinline__ uint64_t op_desc_h(uint32_t addr, int K) { return desc_sbo(addr, (uint32_t)K * 16u); }
 
 // K-major TF32 operand with 128-byte swizzle: atoms of 8 rows x 128 B (32 elements of K) on 1 KiB
 // boundaries, 16-byte chunk c of atom row r stored at chunk c ^ r; row-groups 1 KiB apart, K-atoms
@@ -72,7 +74,13 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int k, int N) {
     return (uint32_t)((k >> 5) * (N * 128) + (row >> 3) * 1024 + (row & 7) * 128 + ((((k & 31) >> 2) ^ (row & 7)) << 4) +
                       (k & 3) * 4);
 }
-// Descriptor of one 8-element K-step of such an operand: `addr` = base + K-atom offset + (k % 32) * 4.
+// The same layout for 16-bit elements: an atom row holds 64 elements of K.
+__device__ __forceinline__ uint32_t sw128_off_h(int row, int k, int N) {
+    return (uint32_t)((k >> 6) * (N * 128) + (row >> 3) * 1024 + (row & 7) * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) +
+                      (k & 7) * 2);
+}
+// Descriptor of one 32-byte K-step of such an operand (8 TF32 or 16 fp16 elements): `addr` = base +
+// K-atom offset + offset within the atom row.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) |
            (2ull << 61);
@@ -87,6 +95,10 @@ __device__ __forceinline__ bool elect_one() {
 
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {      // fp16 A and B, fp32 accumulator
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
@@ -106,6 +118,10 @@ __device__ __forceinline__ void umma_bf16_1(uint32_t d_tmem, uint64_t a, uint64_
         "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+// kind::f16 with fp16 operands: the same instruction, the types are the instruction descriptor's.
+__device__ __forceinline__ void umma_f16_1(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    umma_bf16_1(d_tmem, a, b, idesc, acc);
 }
 
 // D (+)= A B^T with A [M x K] and B [N x K] K-major TF32 operands in shared memory (8 elements per step).
