@@ -406,6 +406,13 @@ kda_status kda_prefill_backward(const void* q, const void* k, const void* v, con
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return KDA_ERR_CUDA;
+    // one bf16 d=128 sequence whose forward recompute ran as one window: every chunk's record (Q', M,
+    // Gamma_C) is still in the workspace, and the state-gradient chain walks chunks instead of tokens
+    if (kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt) && total_tokens > 0) {
+        const int64_t chunks = (total_tokens + kda::kChunk - 1) / kda::kChunk;
+        const kda::WindowPlan plan = kda::prefill_2p_plan(chunks, H, L.scratch - L.fwd, sms);
+        if (plan.window >= chunks) p.records = ws + L.fwd;
+    }
     const int64_t units = bwd_max_units(num_seqs, total_tokens, H);
     int grid = (int)(units < kda::kBwdMaxCtas ? units : kda::kBwdMaxCtas);
     if (grid > sms) grid = sms;

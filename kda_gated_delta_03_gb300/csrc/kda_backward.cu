@@ -521,9 +521,10 @@ cudaError_t launch_dstate_d(const BwdParams& p, cudaStream_t s) {
 }
 
 template <typename TIn>
-cudaError_t launch_bwd_t(const BwdParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_bwd_t(const BwdParams& p, kda_dtype dt, int grid, cudaStream_t s) {
     cudaError_t e = cudaErrorInvalidValue;
-    switch (p.dk) {
+    if (p.records) e = launch_bwd_dstate_records(p, dt, p.records, s);   // chunk by chunk from the records
+    else switch (p.dk) {
         case 128: e = launch_dstate_d<128, TIn>(p, s); break;
         case 64: e = launch_dstate_d<64, TIn>(p, s); break;
         case 16: e = launch_dstate_d<16, TIn>(p, s); break;
@@ -547,7 +548,7 @@ cudaError_t launch_bwd_offsets(const int32_t* cu, int32_t N, int32_t T, int32_t*
 }
 
 cudaError_t launch_prefill_bwd(const BwdParams& p, kda_dtype dt, int grid, cudaStream_t s) {
-    return dt == KDA_DTYPE_BF16 ? launch_bwd_t<__nv_bfloat16>(p, grid, s) : launch_bwd_t<float>(p, grid, s);
+    return dt == KDA_DTYPE_BF16 ? launch_bwd_t<__nv_bfloat16>(p, dt, grid, s) : launch_bwd_t<float>(p, dt, grid, s);
 }
 
 }  // namespace kda

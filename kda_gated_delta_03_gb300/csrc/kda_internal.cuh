@@ -87,6 +87,7 @@ struct BwdParams {
     const int32_t* chunk_offsets;// [num_seqs + 1]: first chunk unit of each sequence
     float* dstate_b;             // gradient of the state after every 64 tokens (snapshot slots)
     float* scratch;              // per CTA: 63 states of the chunk being walked back
+    const unsigned char* records;// the one-window forward recompute's per-chunk records, or nullptr
     unsigned* err;
 };
 constexpr int kBwdMaxCtas = 160;   // chunk-pass CTAs (one per SM)
@@ -112,6 +113,7 @@ cudaError_t launch_order(const int32_t* cu_seqlens, int32_t num_seqs, int32_t* o
 cudaError_t launch_bwd_offsets(const int32_t* cu, int32_t N, int32_t T, int32_t* off, int32_t* choff, unsigned* err,
                                cudaStream_t s);
 cudaError_t launch_prefill_bwd(const BwdParams& p, kda_dtype dt, int grid, cudaStream_t s);
+cudaError_t launch_bwd_dstate_records(const BwdParams& p, kda_dtype dt, const unsigned char* records, cudaStream_t s);
 
 // Number of CUDA-core prefill d_v slices for a head size.
 int prefill_cc_slices(int dv);

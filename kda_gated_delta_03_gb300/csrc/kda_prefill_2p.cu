@@ -882,6 +882,131 @@ __global__ void __launch_bounds__(C_NT, 1)
     }
 }
 
+// ============================================================================================
+// Backward pass, state-gradient chain from the records of a one-window forward recompute.  The chunk's
+// map from its start state to its end state is S -> Diag(Gamma_C) S + B - M S and its output O = Q' S +
+// P Utilde, so the gradient of its start state is
+//     dS_start = Diag(Gamma_C) dS_end - M^T dS_end + Q'^T dO          (dO = scale * grad_o of the chunk)
+// ("Kimi K3, explained", section "Training in chunks": the state alone passes between chunks, here in
+// reverse).  One CTA per (head, 32 value columns) walks the chunks from the last to the first; a thread
+// holds 4 key rows x 4 value columns of the new gradient.  The record of the next chunk to walk and its
+// grad_o rows are fetched with cp.async while the current one is used.
+// ============================================================================================
+constexpr int BR_NT = 256;
+constexpr int BR_OFF_DS = 2 * (QM_BYTES + 512);                 // two record buffers ([Q'; M] and Gamma_C)
+constexpr int BR_OFF_DO = BR_OFF_DS + 2 * DK * SNV * 4;          // two gradient buffers (128 x 32 fp32)
+constexpr int BR_SMEM = BR_OFF_DO + 2 * C * SNV * 4;             // two grad_o tiles (64 x 32 fp32)
+
+__device__ __forceinline__ void br_cp16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(saddr(dst)), "l"(src) : "memory");
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(BR_NT, 1) kda_bwd_dstate_records_kernel(BwdParams p, const unsigned char* records) {
+    extern __shared__ __align__(16) unsigned char sm[];
+    const int tid = threadIdx.x;
+    const int H = p.H, h = blockIdx.x / SLICES, j0 = (blockIdx.x % SLICES) * SNV;
+    const int32_t T = p.total_tokens;
+    if (p.num_seqs != 1 || p.cu_seqlens[0] != 0 || p.cu_seqlens[1] != T) {
+        if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
+        return;
+    }
+    const int nch = (T + C - 1) / C;
+    const int ag = tid >> 3, jg = tid & 7;                 // key rows 4 ag .. +3, value columns 4 jg .. +3
+    const TIn* gdo = static_cast<const TIn*>(p.d_o);
+    auto rec_buf = [&](int b) { return sm + b * (QM_BYTES + 512); };
+    float* dsb = reinterpret_cast<float*>(sm + BR_OFF_DS);   // [2][128][32]
+    float* dob = reinterpret_cast<float*>(sm + BR_OFF_DO);   // [2][64][32]
+    // the chunk's [Q'; M], Gamma_C and grad_o rows (scaled, zero past the sequence end) into buffer b
+    auto fetch = [&](int c, int b) {
+        const unsigned char* rec = records + ((size_t)c * H + h) * REC_BYTES;
+        unsigned char* dst = rec_buf(b);
+        for (int e = tid; e < QM_BYTES / 16; e += BR_NT) br_cp16(dst + e * 16, rec + REC_QM + e * 16);
+        if (tid < 32) br_cp16(dst + QM_BYTES + tid * 16, rec + REC_G + tid * 16);
+        const int32_t t0 = c * C;
+        for (int e = tid; e < C * SNV; e += BR_NT) {         // plain loads: the scale and the conversion
+            const int r = e / SNV, jj = e % SNV;
+            dob[b * C * SNV + e] = t0 + r < T ? p.scale * load_as_float(gdo, ((int64_t)(t0 + r) * H + h) * DK + j0 + jj)
+                                              : 0.f;
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
+    // gradient of the final state
+    for (int e = tid; e < DK * SNV; e += BR_NT) {
+        const int a = e / SNV, jj = e % SNV;
+        dsb[e] = p.d_state_out ? p.d_state_out[((int64_t)h * DK + a) * DK + j0 + jj] : 0.f;
+    }
+    if (nch > 0) fetch(nch - 1, 0);
+    int cur = 0;
+    float nw[4][4];
+    for (int c = nch - 1; c >= 0; --c) {
+        const int b = (nch - 1 - c) & 1;
+        if (c > 0) fetch(c - 1, b ^ 1);
+        else asm volatile("cp.async.commit_group;\n" ::: "memory");
+        asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+        __syncthreads();                                   // chunk c's record and grad_o, and dS, are in place
+        const unsigned char* qm = rec_buf(b);
+        const float* gam = reinterpret_cast<const float*>(qm + QM_BYTES);
+        const float* ds = dsb + cur * DK * SNV;
+        const float* dO = dob + b * C * SNV;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const float g = gam[4 * ag + x];
+            const float4 d4 = *reinterpret_cast<const float4*>(ds + (4 * ag + x) * SNV + 4 * jg);
+            nw[x][0] = g * d4.x; nw[x][1] = g * d4.y; nw[x][2] = g * d4.z; nw[x][3] = g * d4.w;
+        }
+        // - M^T dS: sum over i of M[i][a] dS[i][j]; M's row i is row 64 + i of the fp16 operand
+#pragma unroll 4
+        for (int i = 0; i < DK; ++i) {
+            const uint2 mw = *reinterpret_cast<const uint2*>(qm + op_off_h(C + i, 4 * ag, DK));
+            const float2 m01 = __half22float2(*reinterpret_cast<const __half2*>(&mw.x));
+            const float2 m23 = __half22float2(*reinterpret_cast<const __half2*>(&mw.y));
+            const float4 d4 = *reinterpret_cast<const float4*>(ds + i * SNV + 4 * jg);
+            const float m[4] = {m01.x, m01.y, m23.x, m23.y};
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                nw[x][0] = fmaf(-m[x], d4.x, nw[x][0]); nw[x][1] = fmaf(-m[x], d4.y, nw[x][1]);
+                nw[x][2] = fmaf(-m[x], d4.z, nw[x][2]); nw[x][3] = fmaf(-m[x], d4.w, nw[x][3]);
+            }
+        }
+        // + Q'^T dO: sum over the chunk's rows r of Q'[r][a] dO[r][j]
+#pragma unroll 4
+        for (int r = 0; r < C; ++r) {
+            const uint2 qw = *reinterpret_cast<const uint2*>(qm + op_off_h(r, 4 * ag, DK));
+            const float2 q01 = __half22float2(*reinterpret_cast<const __half2*>(&qw.x));
+            const float2 q23 = __half22float2(*reinterpret_cast<const __half2*>(&qw.y));
+            const float4 o4 = *reinterpret_cast<const float4*>(dO + r * SNV + 4 * jg);
+            const float qv[4] = {q01.x, q01.y, q23.x, q23.y};
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                nw[x][0] = fmaf(qv[x], o4.x, nw[x][0]); nw[x][1] = fmaf(qv[x], o4.y, nw[x][1]);
+                nw[x][2] = fmaf(qv[x], o4.z, nw[x][2]); nw[x][3] = fmaf(qv[x], o4.w, nw[x][3]);
+            }
+        }
+        float* nds = dsb + (cur ^ 1) * DK * SNV;
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+            *reinterpret_cast<float4*>(nds + (4 * ag + x) * SNV + 4 * jg) = make_float4(nw[x][0], nw[x][1], nw[x][2], nw[x][3]);
+        // the gradient of the state after chunk c - 1 (the snapshot slot of that boundary)
+        if (c > 0) {
+            float* dst = p.dstate_b + (((int64_t)(p.snap_offsets[0] + c - 1) * H + h) * DK) * DK + j0 + 4 * jg;
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+                *reinterpret_cast<float4*>(dst + (int64_t)(4 * ag + x) * DK) = make_float4(nw[x][0], nw[x][1], nw[x][2], nw[x][3]);
+        }
+        cur ^= 1;
+        __syncthreads();                                   // buffers b and the old dS are free
+    }
+    if (p.d_state_in) {
+        const float* ds = dsb + cur * DK * SNV;
+        for (int e = tid; e < DK * SNV; e += BR_NT) {
+            const int a = e / SNV, jj = e % SNV;
+            p.d_state_in[((int64_t)h * DK + a) * DK + j0 + jj] = ds[e];
+        }
+    }
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+}
+
 int64_t buffer_chunks(int32_t H) {                   // chunks of records one 256 MiB buffer holds
     const int64_t w = (int64_t)(kBufBudget / ((size_t)H * REC_BYTES));
     return w < 1 ? 1 : w;
@@ -1007,6 +1132,23 @@ cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t wo
         if (ss && (e = cudaEventRecord(ss->chain_done[buf], s)) != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_bwd_dstate_records(const BwdParams& p, kda_dtype dt, const unsigned char* records, cudaStream_t s) {
+    const unsigned grid = (unsigned)(p.H * SLICES);
+    cudaError_t e;
+    if (dt == KDA_DTYPE_BF16) {
+        e = cudaFuncSetAttribute(kda_bwd_dstate_records_kernel<__nv_bfloat16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, BR_SMEM);
+        if (e != cudaSuccess) return e;
+        kda_bwd_dstate_records_kernel<__nv_bfloat16><<<grid, BR_NT, BR_SMEM, s>>>(p, records);
+    } else {
+        e = cudaFuncSetAttribute(kda_bwd_dstate_records_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 BR_SMEM);
+        if (e != cudaSuccess) return e;
+        kda_bwd_dstate_records_kernel<float><<<grid, BR_NT, BR_SMEM, s>>>(p, records);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace kda
