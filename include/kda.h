@@ -194,9 +194,12 @@ KDA_API kda_status kda_prefill_ex(const void* q, const void* k, const void* v, c
  * the token recurrence ("Kimi K3, explained", section "The math"), in three
  * passes: a forward recompute that stores the state at every 64-token
  * boundary; a reverse chain that carries only the state gradient and stores it
- * at the same boundaries; and a chunk-parallel pass that, per (sequence, 64-token
- * chunk, head), replays the chunk from its start state and walks it back token
- * by token from its end-state gradient.  Arguments are kda_prefill's, plus:
+ * at the same boundaries (for one bf16 d=128 sequence whose recompute fits one
+ * window of records, chunk by chunk from those records: dS_start =
+ * Diag(Gamma_C) dS_end - M^T dS_end + Q'^T dO; otherwise token by token); and a
+ * chunk-parallel pass that, per (sequence, 64-token chunk, head), replays the
+ * chunk from its start state and walks it back token by token from its
+ * end-state gradient.  Arguments are kda_prefill's, plus:
  *   grad_o          [total_tokens, H, d_v] dtype dt
  *   grad_state_out  [num_seqs, H, d_k, d_v] float32, or NULL
  *   grad_q, grad_k  [total_tokens, H, d_k] dtype dt;  grad_v [total_tokens, H, d_v]
