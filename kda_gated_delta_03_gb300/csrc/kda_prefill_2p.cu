@@ -888,23 +888,40 @@ __global__ void __launch_bounds__(C_NT, 1)
 // P Utilde, so the gradient of its start state is
 //     dS_start = Diag(Gamma_C) dS_end - M^T dS_end + Q'^T dO          (dO = scale * grad_o of the chunk)
 // ("Kimi K3, explained", section "Training in chunks": the state alone passes between chunks, here in
-// reverse).  One CTA per (head, 32 value columns) walks the chunks from the last to the first; a thread
-// holds 4 key rows x 4 value columns of the new gradient.  The record of the next chunk to walk and its
-// grad_o rows are fetched with cp.async while the current one is used.
+// reverse).  One CTA per (head, 32 value columns) walks the chunks from the last to the first; warp w
+// owns rows 16 w .. 16 w + 15 of the gradient, in fp32 mma accumulators across chunks, and each chunk is
+// one product [-M^T | Q'^T] (16 x 192 per warp) x [dS; dO] (192 x 32) of warp-level m16n8k16 fp16 MMAs:
+// M and Q' come fp16 from the record, dS and dO are rounded to fp16 for the operand only (the same
+// 10-bit significand as the forward's TF32/fp16 operands).  The next chunk's record and grad_o rows are
+// fetched while the current one is used.
 // ============================================================================================
 constexpr int BR_NT = 256;
-constexpr int BR_OFF_DS = 2 * (QM_BYTES + 512);                 // two record buffers ([Q'; M] and Gamma_C)
-constexpr int BR_OFF_DO = BR_OFF_DS + 2 * DK * SNV * 4;          // two gradient buffers (128 x 32 fp32)
-constexpr int BR_SMEM = BR_OFF_DO + 2 * C * SNV * 4;             // two grad_o tiles (64 x 32 fp32)
+constexpr int BR_LD = SNV + 8;                                    // fp16 per operand row (80 B: no bank conflicts)
+constexpr int BR_OFF_DS = 2 * (QM_BYTES + 512);                   // two record buffers ([Q'; M] and Gamma_C)
+constexpr int BR_OFF_DO = BR_OFF_DS + 2 * DK * BR_LD * 2;         // two -dS operands (128 x 32 fp16)
+constexpr int BR_SMEM = BR_OFF_DO + 2 * C * BR_LD * 2;            // two dO operands (64 x 32 fp16)
 
 __device__ __forceinline__ void br_cp16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(saddr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 template <typename TIn>
 __global__ void __launch_bounds__(BR_NT, 1) kda_bwd_dstate_records_kernel(BwdParams p, const unsigned char* records) {
     extern __shared__ __align__(16) unsigned char sm[];
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gid = lane >> 2, tig = lane & 3;
     const int H = p.H, h = blockIdx.x / SLICES, j0 = (blockIdx.x % SLICES) * SNV;
     const int32_t T = p.total_tokens;
     if (p.num_seqs != 1 || p.cu_seqlens[0] != 0 || p.cu_seqlens[1] != T) {
@@ -912,98 +929,124 @@ __global__ void __launch_bounds__(BR_NT, 1) kda_bwd_dstate_records_kernel(BwdPar
         return;
     }
     const int nch = (T + C - 1) / C;
-    const int ag = tid >> 3, jg = tid & 7;                 // key rows 4 ag .. +3, value columns 4 jg .. +3
+    const int a0 = 16 * warp;                                     // this warp's gradient rows
     const TIn* gdo = static_cast<const TIn*>(p.d_o);
     auto rec_buf = [&](int b) { return sm + b * (QM_BYTES + 512); };
-    float* dsb = reinterpret_cast<float*>(sm + BR_OFF_DS);   // [2][128][32]
-    float* dob = reinterpret_cast<float*>(sm + BR_OFF_DO);   // [2][64][32]
-    // the chunk's [Q'; M], Gamma_C and grad_o rows (scaled, zero past the sequence end) into buffer b
+    __half* dsh = reinterpret_cast<__half*>(sm + BR_OFF_DS);      // [2][128][BR_LD]: -dS, fp16
+    __half* doh = reinterpret_cast<__half*>(sm + BR_OFF_DO);      // [2][64][BR_LD]: dO, fp16
+    bool big = false;
+    // the chunk's [Q'; M] and Gamma_C into buffer b (cp.async), and its grad_o rows into registers: they
+    // are stored (scaled, fp16, zero past the sequence end) only after the current chunk's products
+    constexpr int DOPT = C * SNV / 2 / BR_NT;                     // column pairs of grad_o per thread
+    float dov[DOPT][2];
     auto fetch = [&](int c, int b) {
         const unsigned char* rec = records + ((size_t)c * H + h) * REC_BYTES;
         unsigned char* dst = rec_buf(b);
         for (int e = tid; e < QM_BYTES / 16; e += BR_NT) br_cp16(dst + e * 16, rec + REC_QM + e * 16);
         if (tid < 32) br_cp16(dst + QM_BYTES + tid * 16, rec + REC_G + tid * 16);
-        const int32_t t0 = c * C;
-        for (int e = tid; e < C * SNV; e += BR_NT) {         // plain loads: the scale and the conversion
-            const int r = e / SNV, jj = e % SNV;
-            dob[b * C * SNV + e] = t0 + r < T ? p.scale * load_as_float(gdo, ((int64_t)(t0 + r) * H + h) * DK + j0 + jj)
-                                              : 0.f;
-        }
         asm volatile("cp.async.commit_group;\n" ::: "memory");
+        const int32_t t0 = c * C;
+#pragma unroll
+        for (int x = 0; x < DOPT; ++x) {
+            const int e = tid + x * BR_NT, r = e / (SNV / 2), jj = 2 * (e % (SNV / 2));
+            const int64_t at = ((int64_t)(t0 + r) * H + h) * DK + j0 + jj;
+            dov[x][0] = t0 + r < T ? load_as_float(gdo, at) : 0.f;
+            dov[x][1] = t0 + r < T ? load_as_float(gdo, at + 1) : 0.f;
+        }
     };
-    // gradient of the final state
-    for (int e = tid; e < DK * SNV; e += BR_NT) {
-        const int a = e / SNV, jj = e % SNV;
-        dsb[e] = p.d_state_out ? p.d_state_out[((int64_t)h * DK + a) * DK + j0 + jj] : 0.f;
+    auto store_do = [&](int b) {
+#pragma unroll
+        for (int x = 0; x < DOPT; ++x) {
+            const int e = tid + x * BR_NT, r = e / (SNV / 2), jj = 2 * (e % (SNV / 2));
+            const float x0 = p.scale * dov[x][0], x1 = p.scale * dov[x][1];
+            big |= fmaxf(fabsf(x0), fabsf(x1)) > kF16Max;
+            *reinterpret_cast<__half2*>(doh + (b * C + r) * BR_LD + jj) = __floats2half2_rn(x0, x1);
+        }
+    };
+    // accumulator fragment of n-tile nt: rows a0 + gid (+ 8), columns 8 nt + 2 tig (+ 1)
+    float acc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int a = a0 + gid + 8 * (e >> 1), jj = 8 * nt + 2 * tig + (e & 1);
+            acc[nt][e] = p.d_state_out ? p.d_state_out[((int64_t)h * DK + a) * DK + j0 + jj] : 0.f;
+        }
+    auto put_operand = [&](int b) {                               // -dS in fp16, for the next chunk's product
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int a = a0 + gid + 8 * hr, jj = 8 * nt + 2 * tig;
+                big |= fmaxf(fabsf(acc[nt][2 * hr]), fabsf(acc[nt][2 * hr + 1])) > kF16Max;
+                *reinterpret_cast<__half2*>(dsh + (b * DK + a) * BR_LD + jj) =
+                    __floats2half2_rn(-acc[nt][2 * hr], -acc[nt][2 * hr + 1]);
+            }
+    };
+    put_operand(0);
+    if (nch > 0) {
+        fetch(nch - 1, 0);
+        store_do(0);
     }
-    if (nch > 0) fetch(nch - 1, 0);
     int cur = 0;
-    float nw[4][4];
     for (int c = nch - 1; c >= 0; --c) {
         const int b = (nch - 1 - c) & 1;
         if (c > 0) fetch(c - 1, b ^ 1);
         else asm volatile("cp.async.commit_group;\n" ::: "memory");
         asm volatile("cp.async.wait_group 1;\n" ::: "memory");
-        __syncthreads();                                   // chunk c's record and grad_o, and dS, are in place
+        __syncthreads();                                   // chunk c's record and dO, and the -dS operand, are in place
         const unsigned char* qm = rec_buf(b);
         const float* gam = reinterpret_cast<const float*>(qm + QM_BYTES);
-        const float* ds = dsb + cur * DK * SNV;
-        const float* dO = dob + b * C * SNV;
+        const float g_lo = gam[a0 + gid], g_hi = gam[a0 + gid + 8];
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const float g = gam[4 * ag + x];
-            const float4 d4 = *reinterpret_cast<const float4*>(ds + (4 * ag + x) * SNV + 4 * jg);
-            nw[x][0] = g * d4.x; nw[x][1] = g * d4.y; nw[x][2] = g * d4.z; nw[x][3] = g * d4.w;
+        for (int nt = 0; nt < 4; ++nt) {
+            acc[nt][0] *= g_lo; acc[nt][1] *= g_lo; acc[nt][2] *= g_hi; acc[nt][3] *= g_hi;
         }
-        // - M^T dS: sum over i of M[i][a] dS[i][j]; M's row i is row 64 + i of the fp16 operand
-#pragma unroll 4
-        for (int i = 0; i < DK; ++i) {
-            const uint2 mw = *reinterpret_cast<const uint2*>(qm + op_off_h(C + i, 4 * ag, DK));
-            const float2 m01 = __half22float2(*reinterpret_cast<const __half2*>(&mw.x));
-            const float2 m23 = __half22float2(*reinterpret_cast<const __half2*>(&mw.y));
-            const float4 d4 = *reinterpret_cast<const float4*>(ds + i * SNV + 4 * jg);
-            const float m[4] = {m01.x, m01.y, m23.x, m23.y};
+        // A fragment (rows a0.., k0.. of -M^T or Q'^T): ldmatrix.trans of the stored M (rows k, 8 consecutive
+        // a per 16 bytes) or Q' (rows r); lanes 8m..8m+7 address the rows of tile m = (k0 + 8 (m >> 1),
+        // a0 + 8 (m & 1)), which come out in the fragment's register order.  B fragments (k0.., 8 nt..) of
+        // the row-major -dS / dO operands: tiles (k0, 8 nt), (k0 + 8, 8 nt) for two n-tiles per ldmatrix.
+        const __half* ds = dsh + cur * DK * BR_LD;
+        const __half* dO = doh + b * C * BR_LD;
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                nw[x][0] = fmaf(-m[x], d4.x, nw[x][0]); nw[x][1] = fmaf(-m[x], d4.y, nw[x][1]);
-                nw[x][2] = fmaf(-m[x], d4.z, nw[x][2]); nw[x][3] = fmaf(-m[x], d4.w, nw[x][3]);
-            }
+        for (int ks = 0; ks < (DK + C) / 16; ++ks) {
+            const bool mpart = ks < DK / 16;
+            const int k0 = mpart ? 16 * ks : 16 * (ks - DK / 16);
+            uint32_t af[4], b01[4], b23[4];
+            ldsm_x4_t(saddr(qm + op_off_h((mpart ? C : 0) + k0 + (lane & 7) + 8 * (lane >> 4),
+                                          a0 + 8 * ((lane >> 3) & 1), DK)), af);
+            const __half* brow = (mpart ? ds : dO) + (k0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * BR_LD + 8 * (lane >> 4);
+            ldsm_x4_t(saddr(brow), b01);                   // n-tiles 0 and 1
+            ldsm_x4_t(saddr(brow + 16), b23);              // n-tiles 2 and 3
+            mma_f16_16x8x16(acc[0], af, b01[0], b01[1]);
+            mma_f16_16x8x16(acc[1], af, b01[2], b01[3]);
+            mma_f16_16x8x16(acc[2], af, b23[0], b23[1]);
+            mma_f16_16x8x16(acc[3], af, b23[2], b23[3]);
         }
-        // + Q'^T dO: sum over the chunk's rows r of Q'[r][a] dO[r][j]
-#pragma unroll 4
-        for (int r = 0; r < C; ++r) {
-            const uint2 qw = *reinterpret_cast<const uint2*>(qm + op_off_h(r, 4 * ag, DK));
-            const float2 q01 = __half22float2(*reinterpret_cast<const __half2*>(&qw.x));
-            const float2 q23 = __half22float2(*reinterpret_cast<const __half2*>(&qw.y));
-            const float4 o4 = *reinterpret_cast<const float4*>(dO + r * SNV + 4 * jg);
-            const float qv[4] = {q01.x, q01.y, q23.x, q23.y};
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                nw[x][0] = fmaf(qv[x], o4.x, nw[x][0]); nw[x][1] = fmaf(qv[x], o4.y, nw[x][1]);
-                nw[x][2] = fmaf(qv[x], o4.z, nw[x][2]); nw[x][3] = fmaf(qv[x], o4.w, nw[x][3]);
-            }
-        }
-        float* nds = dsb + (cur ^ 1) * DK * SNV;
-#pragma unroll
-        for (int x = 0; x < 4; ++x)
-            *reinterpret_cast<float4*>(nds + (4 * ag + x) * SNV + 4 * jg) = make_float4(nw[x][0], nw[x][1], nw[x][2], nw[x][3]);
+        put_operand(cur ^ 1);
+        if (c > 0) store_do(b ^ 1);                        // chunk c - 1's grad_o, loaded during the products
         // the gradient of the state after chunk c - 1 (the snapshot slot of that boundary)
         if (c > 0) {
-            float* dst = p.dstate_b + (((int64_t)(p.snap_offsets[0] + c - 1) * H + h) * DK) * DK + j0 + 4 * jg;
+            float* dst = p.dstate_b + (((int64_t)(p.snap_offsets[0] + c - 1) * H + h) * DK) * DK + j0;
 #pragma unroll
-            for (int x = 0; x < 4; ++x)
-                *reinterpret_cast<float4*>(dst + (int64_t)(4 * ag + x) * DK) = make_float4(nw[x][0], nw[x][1], nw[x][2], nw[x][3]);
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr)
+                    *reinterpret_cast<float2*>(dst + (int64_t)(a0 + gid + 8 * hr) * DK + 8 * nt + 2 * tig) =
+                        make_float2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
         }
         cur ^= 1;
-        __syncthreads();                                   // buffers b and the old dS are free
+        __syncthreads();                                   // buffers b and the old operand are free
     }
     if (p.d_state_in) {
-        const float* ds = dsb + cur * DK * SNV;
-        for (int e = tid; e < DK * SNV; e += BR_NT) {
-            const int a = e / SNV, jj = e % SNV;
-            p.d_state_in[((int64_t)h * DK + a) * DK + j0 + jj] = ds[e];
-        }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr)
+                *reinterpret_cast<float2*>(p.d_state_in + ((int64_t)h * DK + a0 + gid + 8 * hr) * DK + j0 + 8 * nt + 2 * tig) =
+                    make_float2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
     }
+    if (big) atomicOr(p.err, KDA_DEVERR_RANGE);
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
 }
 
