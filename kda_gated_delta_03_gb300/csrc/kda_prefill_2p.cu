@@ -29,19 +29,22 @@ namespace {
 
 // ---- one (head, chunk) record in the workspace ----
 constexpr int REC_QM = 0;          // [Q'; M]: 192 x 128 fp16 K-major operand (48 KiB)
-constexpr int REC_B = 49152;       // B = Khat^T Utilde: fp32 [32 column quads][128 rows][4] (64 KiB)
-constexpr int REC_O = 114688;      // P Utilde: fp32 [32 column quads][64 rows][4] (32 KiB)
-constexpr int REC_G = 147456;      // Gamma_C: fp32 [128]
-constexpr int REC_BYTES = 147968;
+constexpr int REC_B = 49152;       // B = Khat^T Utilde: fp16 [32 column quads][128 rows][4] (32 KiB)
+constexpr int REC_O = 81920;       // P Utilde: fp16 [32 column quads][64 rows][4] (16 KiB)
+constexpr int REC_G = 98304;       // Gamma_C: fp32 [128]
+constexpr int REC_BYTES = 98816;
 constexpr int QM_BYTES = (C + DK) * DK * 2;
-// Q', M and the chain's state operand are fp16: the same 10-bit significand as TF32, in half the bytes,
-// for values within fp16's range, which the kernels check (KDA_DEVERR_RANGE)
+// Q', M, B, P Utilde and the chain's state operand are fp16: the same 10-bit significand as TF32, in half
+// the bytes, for values within fp16's range, which the kernels check (KDA_DEVERR_RANGE)
 constexpr float kF16Max = 65504.f;
 constexpr int SNV = 32;            // value columns per chain CTA
 constexpr int SLICES = DK / SNV;
-constexpr size_t kBufBudget = size_t(256) << 20;      // record bytes per buffer of the overlapped schedule
+constexpr size_t kBufBudget = size_t(128) << 20;      // record bytes per buffer of the overlapped schedule
+                                                      // (about 170 chunks at H = 8: short enough that the
+                                                      // first window's phase 1, which nothing overlaps, is
+                                                      // short; long enough to amortise the launches)
 constexpr size_t kOneWindowBudget = size_t(1) << 30;  // record bytes of the workspace, at most
-static_assert(QM_BYTES == REC_B && REC_B + DK * DK * 4 == REC_O && REC_O + C * DK * 4 == REC_G, "record layout");
+static_assert(QM_BYTES == REC_B && REC_B + DK * DK * 2 == REC_O && REC_O + C * DK * 2 == REC_G, "record layout");
 
 // ---- phase 1 shared memory ----
 constexpr int P_OFF_V = OFF_V;                     // v tile, dense 64 x 128 bf16
@@ -88,6 +91,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float4 half4_to_float4(uint2 w) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+    return make_float4(a.x, a.y, b.x, b.y);
 }
 
 __device__ __forceinline__ bool valid_single_sequence(const PrefillParams& p) {
@@ -224,9 +233,11 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             } else {
 #pragma unroll
-                for (int x = 0; x < 32; x += 4)
-                    *reinterpret_cast<float4*>(rec_prev + REC_B + (((c0 + x) >> 2) * DK + mi) * 16) =
-                        make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+                for (int x = 0; x < 32; x += 4) {
+                    big |= fmaxf(fmaxf(fabsf(v[x]), fabsf(v[x + 1])), fmaxf(fabsf(v[x + 2]), fabsf(v[x + 3]))) > kF16Max;
+                    *reinterpret_cast<uint2*>(rec_prev + REC_B + (((c0 + x) >> 2) * DK + mi) * 8) =
+                        make_uint2(pack_half2(v[x], v[x + 1]), pack_half2(v[x + 2], v[x + 3]));
+                }
             }
         } else {
 #pragma unroll
@@ -235,9 +246,11 @@ __global__ void __launch_bounds__(NT, 1)
                 tmem_ld32(tmem + tlane + 3 * DK + c0, v);
                 if (lane < 16) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 4)
-                        *reinterpret_cast<float4*>(rec_prev + REC_O + (((c0 + x) >> 2) * C + mr) * 16) =
-                            make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+                    for (int x = 0; x < 32; x += 4) {
+                        big |= fmaxf(fmaxf(fabsf(v[x]), fabsf(v[x + 1])), fmaxf(fabsf(v[x + 2]), fabsf(v[x + 3]))) > kF16Max;
+                        *reinterpret_cast<uint2*>(rec_prev + REC_O + (((c0 + x) >> 2) * C + mr) * 8) =
+                            make_uint2(pack_half2(v[x], v[x + 1]), pack_half2(v[x + 2], v[x + 3]));
+                    }
                 }
             }
         }
@@ -757,12 +770,12 @@ __global__ void __launch_bounds__(C_NT, 1)
         // ---------------- output warps: rows 0..63 of chunk c ----------------
         const int orow = 32 * (warp - 12) + lane;
         const uint32_t tlane = (uint32_t)(32 * (warp - 12)) << 16;
-        float4 oq[SNV / 4];
+        uint2 oq[SNV / 4];                             // raw fp16, converted where used
         auto fetch_o = [&](int ci) {                  // the chunk's P Utilde for this row and slice
             const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
 #pragma unroll
             for (int m = 0; m < SNV / 4; ++m)
-                oq[m] = __ldg(reinterpret_cast<const float4*>(rec + REC_O + (((j0 + 4 * m) >> 2) * C + orow) * 16));
+                oq[m] = __ldg(reinterpret_cast<const uint2*>(rec + REC_O + (((j0 + 4 * m) >> 2) * C + orow) * 8));
         };
         if (n_chunks > 0) fetch_o(0);
         for (int ci = 0; ci < n_chunks; ++ci) {
@@ -779,7 +792,7 @@ __global__ void __launch_bounds__(C_NT, 1)
                 __nv_bfloat16* dst = go + ((int64_t)(t0 + orow) * H + h) * p.dv + j0;
 #pragma unroll
                 for (int x = 0; x < SNV; x += 8) {
-                    const float4 o0 = oq[x / 4], o1 = oq[x / 4 + 1];
+                    const float4 o0 = half4_to_float4(oq[x / 4]), o1 = half4_to_float4(oq[x / 4 + 1]);
                     *reinterpret_cast<uint4*>(dst + x) =
                         make_uint4(pack_bf16x2(p.scale * (d[x] + o0.x), p.scale * (d[x + 1] + o0.y)),
                                    pack_bf16x2(p.scale * (d[x + 2] + o0.z), p.scale * (d[x + 3] + o0.w)),
@@ -815,13 +828,13 @@ __global__ void __launch_bounds__(C_NT, 1)
             mbar_arrive(sbar);
         };
         // the chunk's B and Gamma_C, fetched one chunk ahead (after the proxy fence, which would wait on them)
-        float4 bq[CPT / 4];
+        uint2 bq[CPT / 4];                             // raw fp16: converted where used, so the prefetch never waits
         float gamC = 0.f;
         auto fetch_b = [&](int ci) {
             const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
 #pragma unroll
             for (int m = 0; m < CPT / 4; ++m)
-                bq[m] = __ldg(reinterpret_cast<const float4*>(rec + REC_B + (((jc + 4 * m) >> 2) * DK + srow) * 16));
+                bq[m] = __ldg(reinterpret_cast<const uint2*>(rec + REC_B + (((jc + 4 * m) >> 2) * DK + srow) * 8));
             gamC = __ldg(reinterpret_cast<const float*>(rec + REC_G) + srow);
         };
         write_state_operand(0);
@@ -839,10 +852,11 @@ __global__ void __launch_bounds__(C_NT, 1)
             tmem_ld16(tmem + tlane + TM_S + CPT * half, d);
 #pragma unroll
             for (int m = 0; m < CPT / 4; ++m) {
-                S[4 * m + 0] = fmaf(gamC, S[4 * m + 0], bq[m].x - d[4 * m + 0]);
-                S[4 * m + 1] = fmaf(gamC, S[4 * m + 1], bq[m].y - d[4 * m + 1]);
-                S[4 * m + 2] = fmaf(gamC, S[4 * m + 2], bq[m].z - d[4 * m + 2]);
-                S[4 * m + 3] = fmaf(gamC, S[4 * m + 3], bq[m].w - d[4 * m + 3]);
+                const float4 b4 = half4_to_float4(bq[m]);
+                S[4 * m + 0] = fmaf(gamC, S[4 * m + 0], b4.x - d[4 * m + 0]);
+                S[4 * m + 1] = fmaf(gamC, S[4 * m + 1], b4.y - d[4 * m + 1]);
+                S[4 * m + 2] = fmaf(gamC, S[4 * m + 2], b4.z - d[4 * m + 2]);
+                S[4 * m + 3] = fmaf(gamC, S[4 * m + 3], b4.w - d[4 * m + 3]);
             }
             const int32_t t_done = min(T, (c_begin + ci + 1) * C);   // tokens of the sequence now in S
             if (ci + 1 < n_chunks) {
@@ -1050,7 +1064,7 @@ __global__ void __launch_bounds__(BR_NT, 1) kda_bwd_dstate_records_kernel(BwdPar
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
 }
 
-int64_t buffer_chunks(int32_t H) {                   // chunks of records one 256 MiB buffer holds
+int64_t buffer_chunks(int32_t H) {                   // chunks of records one overlap buffer holds
     const int64_t w = (int64_t)(kBufBudget / ((size_t)H * REC_BYTES));
     return w < 1 ? 1 : w;
 }
