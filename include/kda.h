@@ -158,6 +158,12 @@ KDA_API kda_status kda_prefill(const void* q, const void* k, const void* v, cons
  * snapshots[snapshot_offsets[n] + m] for m = 0 .. floor(len_n /
  * snapshot_every) - 1 (a snapshot at len_n equals that sequence's
  * state_out).
+ *
+ * single_kernel (nonzero): one bf16 sequence with d_k = d_v = 128 runs the
+ * single-kernel tensor-core path (TF32 / bf16 operands) instead of the
+ * two-phase path, whose per-chunk records and state operand are fp16; use it
+ * when that path reports KDA_DEVERR_RANGE (a state or folded chunk value beyond
+ * 65,504).  Results agree to the same tolerance; the two-phase path is faster.
  *   snapshot_every    tokens between snapshots: 0, or a positive multiple of 64
  *   snapshots         [snapshot_offsets[num_seqs], H, d_k, d_v] float32 device
  *                     buffer, 16-byte aligned
@@ -172,6 +178,7 @@ typedef struct kda_prefill_options {
     float* snapshots;
     const int32_t* snapshot_offsets;
     int32_t alpha_mode;             /* kda_alpha_mode; 0 = KDA_ALPHA_PER_CHANNEL */
+    int32_t single_kernel;          /* nonzero: see below */
 } kda_prefill_options;
 
 /*

@@ -24,7 +24,8 @@ KDA_DEVERR_CU_SEQLENS, KDA_DEVERR_STATE_IDX = 0x1, 0x2
 class PrefillOptions(ctypes.Structure):
     """kda_prefill_options (include/kda.h)."""
     _fields_ = [("snapshot_every", ctypes.c_int32), ("snapshots", ctypes.c_void_p),
-                ("snapshot_offsets", ctypes.c_void_p), ("alpha_mode", ctypes.c_int32)]
+                ("snapshot_offsets", ctypes.c_void_p), ("alpha_mode", ctypes.c_int32),
+                ("single_kernel", ctypes.c_int32)]
 
 
 class DecodeOptions(ctypes.Structure):
@@ -144,7 +145,7 @@ def _alpha_shape(mode, lead, dk):
 
 def kda_prefill(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float = 1.0, state_out=None,
                 o=None, workspace=None, stream=None, snapshot_every: int = 0, snapshots=None, snapshot_offsets=None,
-                alpha_mode: int = KDA_ALPHA_PER_CHANNEL):
+                alpha_mode: int = KDA_ALPHA_PER_CHANNEL, single_kernel: bool = False):
     """Chunkwise prefill over packed sequences; returns (o, state_out).
 
     q, k [T, H, d_k], v [T, H, d_v] (bf16 or f32); beta [T, H] f32; alpha [T, H, d_k] f32;
@@ -152,7 +153,9 @@ def kda_prefill(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float
     With snapshot_every > 0 (a multiple of 64): snapshots [S, H, d_k, d_v] f32 and snapshot_offsets
     [N + 1] int32 (device) receive the state of sequence n after each multiple of snapshot_every tokens
     (kda_prefill_ex).  alpha_mode: KDA_ALPHA_PER_CHANNEL (alpha [T, H, d_k]), KDA_ALPHA_PER_HEAD (Gated
-    DeltaNet, alpha [T, H]) or KDA_ALPHA_NONE (DeltaNet, alpha may be None).
+    DeltaNet, alpha [T, H]) or KDA_ALPHA_NONE (DeltaNet, alpha may be None).  single_kernel: run one bf16
+    d=128 sequence on the single-kernel path instead of the two-phase path (whose fp16 operands end at
+    65,504; KDA_DEVERR_RANGE reports values beyond).
     """
     L = load()
     T, H, dk = q.shape
@@ -180,12 +183,13 @@ def kda_prefill(q, k, v, beta, alpha, cu_seqlens, state_in=None, *, scale: float
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(cu_seqlens), N, T, H, dk, dv, _dt(q.dtype),
             float(scale), _ptr(state_in), _ptr(state_out), _ptr(o), _ptr(workspace), wbytes, _stream(stream))
-    if snapshot_every or alpha_mode != KDA_ALPHA_PER_CHANNEL:
+    if snapshot_every or alpha_mode != KDA_ALPHA_PER_CHANNEL or single_kernel:
         if snapshot_every:
             S = snapshots.shape[0]
             _check("snapshots", snapshots, torch.float32, (S, H, dk, dv), dev)
             _check("snapshot_offsets", snapshot_offsets, torch.int32, (N + 1,), dev)
-        opts = PrefillOptions(int(snapshot_every), _ptr(snapshots), _ptr(snapshot_offsets), int(alpha_mode))
+        opts = PrefillOptions(int(snapshot_every), _ptr(snapshots), _ptr(snapshot_offsets), int(alpha_mode),
+                              int(bool(single_kernel)))
         rc = L.kda_prefill_ex(*args, ctypes.byref(opts))
         name = "kda_prefill_ex"
     else:

@@ -149,7 +149,8 @@ kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const flo
         if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(beta, 4))
             return KDA_ERR_INVALID_ARG;
     }
-    const bool two_phase = kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt);
+    const bool two_phase = kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt) &&
+                           !(options && options->single_kernel);
     // the two-phase path takes any workspace down to one chunk's records and uses more windows
     const size_t need = two_phase ? kda::prefill_2p_min_workspace(H)
                                   : kda_prefill_workspace_size(num_seqs, total_tokens, H, d_k, d_v, dt);

@@ -206,3 +206,30 @@ def test_bad_cu_seqlens_is_reported_not_faulted():
     prefill_gpu(inp)
     assert kda.kda_get_device_error() & 0x1
     assert kda.kda_get_device_error() == 0
+
+
+def test_single_kernel_option_and_the_fp16_range():
+    """The two-phase path keeps its per-chunk records and state operand in fp16 and reports values beyond
+    fp16's range (KDA_DEVERR_RANGE); kda_prefill_options.single_kernel computes the same sequence on the
+    single-kernel path (TF32 / bf16 operands), which matches the oracle at any scale."""
+    import kda_gated_delta_03_gb300 as kda
+
+    def run(inp, single):
+        args = [to_dev(inp[n], n in ("q", "k", "v")) for n in ("q", "k", "v", "beta", "alpha", "cu_seqlens")]
+        o, st = kda.kda_prefill(*args, to_dev(inp["state_in"]), single_kernel=single)
+        torch.cuda.synchronize()
+        return o.double().cpu().numpy(), st.double().cpu().numpy()
+
+    inp = I.prefill_inputs([300], 2, 128, 128, "bf16", 95, decay="slow", state="randn")
+    o_ref, s_ref = O.prefill(inp)
+    o1, s1 = run(inp, True)
+    assert kda.kda_get_device_error() == 0
+    assert rel_frob(o1, o_ref) <= 3e-3 and rel_frob(s1, s_ref) <= 3e-3
+    big = dict(inp, v=I.f32_to_bf16_bits(I.bf16_bits_to_f32(inp["v"]) * 1e6))
+    big["state_in"] = inp["state_in"] * 1e6
+    run(big, False)
+    assert kda.kda_get_device_error() & 0x10                    # KDA_DEVERR_RANGE
+    o2, s2 = run(big, True)
+    assert kda.kda_get_device_error() == 0
+    ob_ref, sb_ref = O.prefill(big)
+    assert rel_frob(o2, ob_ref) <= 3e-3 and rel_frob(s2, sb_ref) <= 3e-3
