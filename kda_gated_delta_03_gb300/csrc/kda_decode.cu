@@ -115,6 +115,97 @@ __global__ void __launch_bounds__(NT, (D == 128 ? 2 : 4)) kda_decode_kernel(Deco
     }
 }
 
+// float32 state at d = 128, split by value columns: the step is independent per value column j (only
+// q . k is shared, and each CTA recomputes it), so two CTAs of 256 threads each take 64 columns of one
+// state; four CTAs per SM keep more loads and stores in flight than two whole-state CTAs.
+template <int D, int CW, int NT, typename TIn>
+__global__ void __launch_bounds__(NT, 4) kda_decode_cols_kernel(DecodeParams p) {
+    constexpr int LPR = CW / 4;         // float4 column groups per row of the slice
+    constexpr int RPP = NT / LPR;       // rows per pass
+    constexpr int PASSES = D / RPP;
+    constexpr int SPLIT = D / CW;
+    static_assert(NT % LPR == 0 && D % RPP == 0 && D % CW == 0, "bad decode tiling");
+
+    __shared__ float sq[D], sk[D], sa[D], sdelta[CW];
+    __shared__ float sx[RPP][CW], sy[RPP][CW];
+    __shared__ float s_qk;
+
+    const int tid = threadIdx.x;
+    const int bh = blockIdx.x / SPLIT, c0 = (blockIdx.x % SPLIT) * CW;
+    const int b = bh / p.H;
+    const int h = bh - b * p.H;
+    const int slot = p.state_idx ? p.state_idx[b] : b;
+    if (slot < 0 || slot >= p.num_slots) {
+        if (tid == 0) atomicOr(p.err, KDA_DEVERR_STATE_IDX);
+        return;
+    }
+    float* S = static_cast<float*>(p.state) + ((int64_t)slot * p.H + h) * (int64_t)(D * D) + c0;
+    const int cg = tid % LPR;
+    const int rg = tid / LPR;
+
+    float4 s[PASSES];
+#pragma unroll
+    for (int m = 0; m < PASSES; ++m)
+        s[m] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rg + RPP * m) * D) + cg);
+
+    const int64_t row = (int64_t)b * p.H + h;
+    const TIn* q = static_cast<const TIn*>(p.q);
+    const TIn* k = static_cast<const TIn*>(p.k);
+    for (int i = tid; i < D; i += NT) {
+        sq[i] = load_as_float(q, row * D + i);
+        sk[i] = load_as_float(k, row * D + i);
+        sa[i] = alpha_at(p.alpha, p.alpha_mode, row, D, i);
+    }
+    __syncthreads();
+
+    float4 px = make_float4(0.f, 0.f, 0.f, 0.f), py = px;
+#pragma unroll
+    for (int m = 0; m < PASSES; ++m) {
+        const int r = rg + RPP * m;
+        const float ak = sa[r] * sk[r], aq = sa[r] * sq[r];
+        px.x = fmaf(ak, s[m].x, px.x); px.y = fmaf(ak, s[m].y, px.y);
+        px.z = fmaf(ak, s[m].z, px.z); px.w = fmaf(ak, s[m].w, px.w);
+        py.x = fmaf(aq, s[m].x, py.x); py.y = fmaf(aq, s[m].y, py.y);
+        py.z = fmaf(aq, s[m].z, py.z); py.w = fmaf(aq, s[m].w, py.w);
+    }
+    reinterpret_cast<float4*>(sx[rg])[cg] = px;
+    reinterpret_cast<float4*>(sy[rg])[cg] = py;
+    if (tid < 32) {
+        float acc = 0.f;
+        for (int i = tid; i < D; i += 32) acc = fmaf(sq[i], sk[i], acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (tid == 0) s_qk = acc;
+    }
+    __syncthreads();
+
+    const float beta = p.beta[row];
+    const TIn* v = static_cast<const TIn*>(p.v);
+    TIn* o = static_cast<TIn*>(p.o);
+    for (int j = tid; j < CW; j += NT) {
+        float x = 0.f, y = 0.f;
+#pragma unroll
+        for (int g = 0; g < RPP; ++g) { x += sx[g][j]; y += sy[g][j]; }
+        const float delta = beta * (load_as_float(v, row * D + c0 + j) - x);
+        sdelta[j] = delta;
+        store_from_float(o, row * D + c0 + j, p.scale * fmaf(s_qk, delta, y));
+    }
+    __syncthreads();
+
+    const float4 d4 = reinterpret_cast<const float4*>(sdelta)[cg];
+#pragma unroll
+    for (int m = 0; m < PASSES; ++m) {
+        const int r = rg + RPP * m;
+        const float a = sa[r], kk = sk[r];
+        float4 n;
+        n.x = fmaf(kk, d4.x, a * s[m].x);
+        n.y = fmaf(kk, d4.y, a * s[m].y);
+        n.z = fmaf(kk, d4.z, a * s[m].z);
+        n.w = fmaf(kk, d4.w, a * s[m].w);
+        __stcs(reinterpret_cast<float4*>(S + (int64_t)r * D) + cg, n);
+    }
+}
+
 // bf16 state at d = 16 and 64: the same step through a storage adapter.
 // State storage: float, or bf16 (read as bf16, updated in fp32, rounded to nearest-even on the way back).
 // One 16-byte access holds VEC state elements of a row.
@@ -357,7 +448,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
     switch (p.d) {
         case 128:
             if (p.state_bf16) kda_decode_bf16s_kernel<128, 128, TIn><<<grid, 128, 0, s>>>(p);
-            else kda_decode_kernel<128, 256, TIn><<<grid, 256, 0, s>>>(p);
+            else kda_decode_cols_kernel<128, 64, 256, TIn><<<2 * grid, 256, 0, s>>>(p);
             break;
         case 64:
             if (p.state_bf16) kda_decode_gen_kernel<64, 64, TIn, TS><<<grid, 64, 0, s>>>(p);
