@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(NT, 1)
                     for (int c = 0; c < 16; ++c) {
                         const int r = 16 * b + c;
                         Ab[r * AT_LD + sr] = sr < r ? sbeta[r] * v[c] : 0.f;
-                        *reinterpret_cast<float*>(opP + op_off(r, sr, C)) = sr <= r ? v[16 + c] : 0.f;
+                        *reinterpret_cast<__half*>(opP + op_off_h(r, sr, C)) = __float2half_rn(sr <= r ? v[16 + c] : 0.f);
                     }
                 }
             }
@@ -481,7 +481,8 @@ __global__ void __launch_bounds__(NT, 1)
                 __syncthreads();
             }
         }
-        // T' = T Diag(beta) -> operand (M=64, K=64)
+        // T' = T Diag(beta) -> fp16 operand (M=64, K=64); the operands of steps 4 and 6 are fp16 (the same
+        // 10-bit significand as TF32; their values are O(1) for unit-norm keys, and v and T' are checked)
         for (int e = tid; e < C * 16; e += NT) {
             const int r = ((e >> 7) << 3) | (e & 7), m0 = 4 * ((e >> 3) & 15);
             float4 v;
@@ -489,19 +490,23 @@ __global__ void __launch_bounds__(NT, 1)
             v.y = m0 + 1 <= r ? Tb[r * AT_LD + m0 + 1] * sbeta[m0 + 1] : 0.f;
             v.z = m0 + 2 <= r ? Tb[r * AT_LD + m0 + 2] * sbeta[m0 + 2] : 0.f;
             v.w = m0 + 3 <= r ? Tb[r * AT_LD + m0 + 3] * sbeta[m0 + 3] : 0.f;
-            *reinterpret_cast<float4*>(X + PS_OPT + op_off(r, m0, C)) = v;
+            big |= fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) > kF16Max;
+            *reinterpret_cast<uint2*>(X + PS_OPT + op_off_h(r, m0, C)) =
+                make_uint2(pack_half2(v.x, v.y), pack_half2(v.z, v.w));
         }
-        // [Gamma.K | V]^T -> operand (N=256 rows, K=64 time)
+        // [Gamma.K | V]^T -> fp16 operand (N=256 rows, K=64 time)
         for (int e = tid; e < DK * 16; e += NT) {
             const int i = e & (DK - 1), m0 = 4 * (e >> 7);
             float gg[4], kk4[4];
 #pragma unroll
             for (int x = 0; x < 4; ++x) { gg[x] = Gat(m0 + x, i); kk4[x] = kat(m0 + x, i); }
-            *reinterpret_cast<float4*>(X + PS_KV + op_off(i, m0, C)) =
-                make_float4(ex2f(gg[0]) * kk4[0], ex2f(gg[1]) * kk4[1], ex2f(gg[2]) * kk4[2], ex2f(gg[3]) * kk4[3]);
-            *reinterpret_cast<float4*>(X + PS_KV + op_off(DK + i, m0, C)) =
-                make_float4(bf(vraw + (m0 + 0) * DK + i), bf(vraw + (m0 + 1) * DK + i), bf(vraw + (m0 + 2) * DK + i),
-                            bf(vraw + (m0 + 3) * DK + i));
+            *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(i, m0, C)) =
+                make_uint2(pack_half2(ex2f(gg[0]) * kk4[0], ex2f(gg[1]) * kk4[1]),
+                           pack_half2(ex2f(gg[2]) * kk4[2], ex2f(gg[3]) * kk4[3]));
+            const float v0 = bf(vraw + (m0 + 0) * DK + i), v1 = bf(vraw + (m0 + 1) * DK + i);
+            const float v2 = bf(vraw + (m0 + 2) * DK + i), v3 = bf(vraw + (m0 + 3) * DK + i);
+            big |= fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))) > kF16Max;
+            *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(DK + i, m0, C)) = make_uint2(pack_half2(v0, v1), pack_half2(v2, v3));
         }
         fence_async_smem();
         tc_fence_before();
@@ -515,13 +520,13 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- 4. [W | Utilde]^T = [Gamma.K | V]^T T'^T  (two M=128 halves, N=64, K=64) ----
         if (warp == 0 && elect_one()) {
             tc_fence_after();
-            constexpr uint32_t id = idesc_tf32(128, C);
-            const uint64_t aw = op_desc(saddr(X + PS_KV), C), au = op_desc(saddr(X + PS_KV + DK * C * 4), C);
-            const uint64_t bt = op_desc(saddr(X + PS_OPT), C);
+            constexpr uint32_t id = idesc_f16(128, C);
+            const uint64_t aw = op_desc_h(saddr(X + PS_KV), C), au = op_desc_h(saddr(X + PS_KV + DK * C * 2), C);
+            const uint64_t bt = op_desc_h(saddr(X + PS_OPT), C);
 #pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks) {
-                umma_tf32_1(tmem + TM_W, aw + (uint64_t)(ks * 16), bt + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
-                umma_tf32_1(tmem + TM_W + C, au + (uint64_t)(ks * 16), bt + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < C / 16; ++ks) {
+                umma_f16_1(tmem + TM_W, aw + (uint64_t)(ks * 16), bt + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
+                umma_f16_1(tmem + TM_W + C, au + (uint64_t)(ks * 16), bt + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
             }
             umma_commit(mbar);
         }
@@ -539,9 +544,11 @@ __global__ void __launch_bounds__(NT, 1)
             for (int cb = 0; cb < 2; ++cb) {
                 tmem_ld32(tmem + tlane + TM_W + C * half + 32 * cb, v);
 #pragma unroll
-                for (int x = 0; x < 32; x += 4)
-                    *reinterpret_cast<float4*>(opWU + op_off(n, 32 * cb + x, C)) =
-                        make_float4(tf32r(v[x]), tf32r(v[x + 1]), tf32r(v[x + 2]), tf32r(v[x + 3]));
+                for (int x = 0; x < 32; x += 4) {
+                    big |= fmaxf(fmaxf(fabsf(v[x]), fabsf(v[x + 1])), fmaxf(fabsf(v[x + 2]), fabsf(v[x + 3]))) > kF16Max;
+                    *reinterpret_cast<uint2*>(opWU + op_off_h(n, 32 * cb + x, C)) =
+                        make_uint2(pack_half2(v[x], v[x + 1]), pack_half2(v[x + 2], v[x + 3]));
+                }
             }
         }
         for (int e = tid; e < DK * 16; e += NT) {
@@ -550,9 +557,9 @@ __global__ void __launch_bounds__(NT, 1)
             float gg[4], kk4[4];
 #pragma unroll
             for (int x = 0; x < 4; ++x) { gg[x] = Gat(s0 + x, i); kk4[x] = kat(s0 + x, i); }
-            *reinterpret_cast<float4*>(opKH + op_off(i, s0, C)) =
-                make_float4(tf32r(ex2f(gl - gg[0]) * kk4[0]), tf32r(ex2f(gl - gg[1]) * kk4[1]),
-                            tf32r(ex2f(gl - gg[2]) * kk4[2]), tf32r(ex2f(gl - gg[3]) * kk4[3]));
+            *reinterpret_cast<uint2*>(opKH + op_off_h(i, s0, C)) =
+                make_uint2(pack_half2(ex2f(gl - gg[0]) * kk4[0], ex2f(gl - gg[1]) * kk4[1]),
+                           pack_half2(ex2f(gl - gg[2]) * kk4[2], ex2f(gl - gg[3]) * kk4[3]));
         }
         drain(4);                                       // the last piece, before step 6 writes its columns
         rec_prev = nullptr;
@@ -568,13 +575,13 @@ __global__ void __launch_bounds__(NT, 1)
         if (warp == 0) {
             if (elect_one()) {
                 tc_fence_after();
-                const uint64_t ak = op_desc(saddr(opKH), C), ap = op_desc(saddr(opP), C);
-                const uint64_t bw = op_desc(saddr(opWU), C);
+                const uint64_t ak = op_desc_h(saddr(opKH), C), ap = op_desc_h(saddr(opP), C);
+                const uint64_t bw = op_desc_h(saddr(opWU), C);
 #pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks) {
+                for (int ks = 0; ks < C / 16; ++ks) {
                     const uint64_t bd = bw + (uint64_t)(ks * 16);
-                    umma_tf32_1(tmem, ak + (uint64_t)(ks * 16), bd, idesc_tf32(128, 2 * DK), ks > 0 ? 1u : 0u);
-                    umma_tf32_1(tmem + 2 * DK, ap + (uint64_t)(ks * 16), bd, idesc_tf32(64, 2 * DK), ks > 0 ? 1u : 0u);
+                    umma_f16_1(tmem, ak + (uint64_t)(ks * 16), bd, idesc_f16(128, 2 * DK), ks > 0 ? 1u : 0u);
+                    umma_f16_1(tmem + 2 * DK, ap + (uint64_t)(ks * 16), bd, idesc_f16(64, 2 * DK), ks > 0 ? 1u : 0u);
                 }
                 umma_commit(mbar);
             }
