@@ -42,7 +42,8 @@ PREFILL_TC_SRC = [CSRC + "kda_prefill_tc.cu", CSRC + "kda_tc_util.cuh"]
 DECODE_KERNEL_SRC = [CSRC + "kda_decode.cu"]
 PREFILL_2P_LABEL = "kda_prefill_prep_kernel + kda_prefill_chain_kernel (one call, all windows)"
 PREFILL_TC_LABEL = "kda_order_kernel + kda_prefill_tc_kernel (one call)"
-DECODE_LABEL = "kda_decode_kernel"
+DECODE_LABEL = "kda_decode_cols_kernel (fp32 state, two CTAs per state)"
+DECODE_BF16S_LABEL = "kda_decode_bf16s_kernel (bf16-stored state)"
 
 
 def prefill_path(N, dtype, dk):
@@ -405,8 +406,9 @@ def run_ours(args, rank, world, local_rank):
                     config={"workload": name, "B": w["B"], "H": w["H"], "d": w["dk"], "qkv": w["dtype"],
                             "state": "bf16" if sdt == "bf16" else "f32",
                             "l2": f"state pool ({'0.5' if sdt == 'bf16' else '1'} GiB) larger than L2"},
-                    roofline=roofline_obj(r["bytes_per_step"], r["kernel_ms"], peaks, "decode", DECODE_KERNEL_SRC,
-                                          DECODE_LABEL, name),
+                    roofline=roofline_obj(r["bytes_per_step"], r["kernel_ms"], peaks,
+                                          "decode_bf16" if sdt == "bf16" else "decode", DECODE_KERNEL_SRC,
+                                          DECODE_BF16S_LABEL if sdt == "bf16" else DECODE_LABEL, name),
                     gpu_launches=r["launches"], clocks=clk.summary())
         return line
 
@@ -441,7 +443,7 @@ def run_ours(args, rank, world, local_rank):
         rb = gpu_decode(wd, wd["steps"], 3, dev, state_dtype="bf16")
         bms = max_over_ranks(rb["ms_per_step"], world)
         roofb = roofline_obj(rb["bytes_per_step"], rb["kernel_ms"], peaks, "decode_bf16", DECODE_KERNEL_SRC,
-                             DECODE_LABEL + " (bf16 state)", "decode_512x32_bf16_state")
+                             DECODE_BF16S_LABEL, "decode_512x32_bf16_state")
         line["decode_bf16_state"] = {"workload": "decode_512x32, state stored in bf16", "steps": wd["steps"],
                                      "steps_per_s": round(world * 1e3 / bms, 2),
                                      "tokens_per_s": round(world * wd["B"] * 1e3 / bms, 1),
