@@ -40,10 +40,11 @@ CSRC = "kda_gated_delta_03_gb300/csrc/"
 PREFILL_2P_SRC = [CSRC + "kda_prefill_2p.cu", CSRC + "kda_tc_util.cuh"]
 PREFILL_TC_SRC = [CSRC + "kda_prefill_tc.cu", CSRC + "kda_tc_util.cuh"]
 DECODE_KERNEL_SRC = [CSRC + "kda_decode.cu"]
+DECODE_BF16S_SRC = [CSRC + "kda_decode.cu", CSRC + "kda_decode_bf16s.cu"]
 PREFILL_2P_LABEL = "kda_prefill_prep_kernel + kda_prefill_chain_kernel (one call, all windows)"
 PREFILL_TC_LABEL = "kda_order_kernel + kda_prefill_tc_kernel (one call)"
 DECODE_LABEL = "kda_decode_cols_kernel (fp32 state, two CTAs per state)"
-DECODE_BF16S_LABEL = "kda_decode_bf16s_kernel (bf16-stored state)"
+DECODE_BF16S_LABEL = "kda_decode_bf16s_stream_kernel (bf16-stored state, streamed through shared memory)"
 
 
 def prefill_path(N, dtype, dk):
@@ -407,7 +408,8 @@ def run_ours(args, rank, world, local_rank):
                             "state": "bf16" if sdt == "bf16" else "f32",
                             "l2": f"state pool ({'0.5' if sdt == 'bf16' else '1'} GiB) larger than L2"},
                     roofline=roofline_obj(r["bytes_per_step"], r["kernel_ms"], peaks,
-                                          "decode_bf16" if sdt == "bf16" else "decode", DECODE_KERNEL_SRC,
+                                          "decode_bf16" if sdt == "bf16" else "decode",
+                                          DECODE_BF16S_SRC if sdt == "bf16" else DECODE_KERNEL_SRC,
                                           DECODE_BF16S_LABEL if sdt == "bf16" else DECODE_LABEL, name),
                     gpu_launches=r["launches"], clocks=clk.summary())
         return line
@@ -442,7 +444,7 @@ def run_ours(args, rank, world, local_rank):
         line["gpu_launches"] += rd["launches"]
         rb = gpu_decode(wd, wd["steps"], 3, dev, state_dtype="bf16")
         bms = max_over_ranks(rb["ms_per_step"], world)
-        roofb = roofline_obj(rb["bytes_per_step"], rb["kernel_ms"], peaks, "decode_bf16", DECODE_KERNEL_SRC,
+        roofb = roofline_obj(rb["bytes_per_step"], rb["kernel_ms"], peaks, "decode_bf16", DECODE_BF16S_SRC,
                              DECODE_BF16S_LABEL, "decode_512x32_bf16_state")
         line["decode_bf16_state"] = {"workload": "decode_512x32, state stored in bf16", "steps": wd["steps"],
                                      "steps_per_s": round(world * 1e3 / bms, 2),

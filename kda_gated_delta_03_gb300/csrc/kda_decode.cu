@@ -11,7 +11,7 @@
 //   o_j = scale (y_j + (q . k) delta_j)    (= scale * S_new^T q)
 //
 // The state is read from HBM once and written once, as float32 or (kda_decode_step_bf16_state) as
-// bf16.  Each CTA owns one (sequence, head) state: a warp reads whole rows with 128-bit
+// bf16 (at d = 128 by the streaming kernel of kda_decode_bf16s.cu).  Each CTA owns one (sequence, head) state: a warp reads whole rows with 128-bit
 // streaming loads, so every thread holds D*D/NT values in registers across the
 // two reductions over the key channels (partial sums in registers, then across
 // row groups through shared memory), and writes the updated rows back with
@@ -335,120 +335,13 @@ __global__ void __launch_bounds__(NT, (D == 128 ? 2 : 4)) kda_decode_gen_kernel(
     }
 }
 
-// bf16-stored state: the same step with the state kept packed (two bf16 per 32-bit register) between
-// the reductions and the write-back, so that one thread can hold twice the elements and a CTA of 128
-// threads covers a 128 x 128 state (three CTAs per SM keep enough loads in flight).
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-template <int D, int NT, typename TIn>
-__global__ void __launch_bounds__(NT, 3) kda_decode_bf16s_kernel(DecodeParams p) {
-    constexpr int LPR = D / 8;          // 16-byte (8-element) column groups per row
-    constexpr int RPP = NT / LPR;       // rows per pass
-    constexpr int PASSES = D / RPP;
-    static_assert(NT % LPR == 0 && D % RPP == 0, "bad decode tiling");
-
-    __shared__ float sq[D], sk[D], sa[D], sdelta[D];
-    __shared__ float sx[RPP][D], sy[RPP][D];
-    __shared__ float s_qk;
-
-    const int tid = threadIdx.x;
-    const int bh = blockIdx.x;
-    const int b = bh / p.H;
-    const int h = bh - b * p.H;
-    const int slot = p.state_idx ? p.state_idx[b] : b;
-    if (slot < 0 || slot >= p.num_slots) {
-        if (tid == 0) atomicOr(p.err, KDA_DEVERR_STATE_IDX);
-        return;
-    }
-    __nv_bfloat16* S = static_cast<__nv_bfloat16*>(p.state) + ((int64_t)slot * p.H + h) * (int64_t)(D * D);
-    const int cg = tid % LPR;
-    const int rg = tid / LPR;
-
-    uint4 s[PASSES];
-#pragma unroll
-    for (int m = 0; m < PASSES; ++m)
-        s[m] = __ldcs(reinterpret_cast<const uint4*>(S + (int64_t)(rg + RPP * m) * D) + cg);
-
-    const int64_t row = (int64_t)b * p.H + h;
-    const TIn* q = static_cast<const TIn*>(p.q);
-    const TIn* k = static_cast<const TIn*>(p.k);
-    for (int i = tid; i < D; i += NT) {
-        sq[i] = load_as_float(q, row * D + i);
-        sk[i] = load_as_float(k, row * D + i);
-        sa[i] = alpha_at(p.alpha, p.alpha_mode, row, D, i);
-    }
-    __syncthreads();
-
-    float px[8], py[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) px[c] = py[c] = 0.f;
-#pragma unroll
-    for (int m = 0; m < PASSES; ++m) {
-        const int r = rg + RPP * m;
-        const float ak = sa[r] * sk[r], aq = sa[r] * sq[r];
-        const uint32_t w[4] = {s[m].x, s[m].y, s[m].z, s[m].w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const float lo = bf_lo(w[c]), hi = bf_hi(w[c]);
-            px[2 * c] = fmaf(ak, lo, px[2 * c]);
-            px[2 * c + 1] = fmaf(ak, hi, px[2 * c + 1]);
-            py[2 * c] = fmaf(aq, lo, py[2 * c]);
-            py[2 * c + 1] = fmaf(aq, hi, py[2 * c + 1]);
-        }
-    }
-    reinterpret_cast<float4*>(sx[rg] + cg * 8)[0] = make_float4(px[0], px[1], px[2], px[3]);
-    reinterpret_cast<float4*>(sx[rg] + cg * 8)[1] = make_float4(px[4], px[5], px[6], px[7]);
-    reinterpret_cast<float4*>(sy[rg] + cg * 8)[0] = make_float4(py[0], py[1], py[2], py[3]);
-    reinterpret_cast<float4*>(sy[rg] + cg * 8)[1] = make_float4(py[4], py[5], py[6], py[7]);
-    if (tid < 32) {
-        float acc = 0.f;
-        for (int i = tid; i < D; i += 32) acc = fmaf(sq[i], sk[i], acc);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (tid == 0) s_qk = acc;
-    }
-    __syncthreads();
-
-    const float beta = p.beta[row];
-    const TIn* v = static_cast<const TIn*>(p.v);
-    TIn* o = static_cast<TIn*>(p.o);
-    for (int j = tid; j < D; j += NT) {
-        float x = 0.f, y = 0.f;
-#pragma unroll
-        for (int g = 0; g < RPP; ++g) { x += sx[g][j]; y += sy[g][j]; }
-        const float delta = beta * (load_as_float(v, row * D + j) - x);
-        sdelta[j] = delta;
-        store_from_float(o, row * D + j, p.scale * fmaf(s_qk, delta, y));
-    }
-    __syncthreads();
-
-    float dl[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) dl[c] = sdelta[cg * 8 + c];
-#pragma unroll
-    for (int m = 0; m < PASSES; ++m) {
-        const int r = rg + RPP * m;
-        const float a = sa[r], kk = sk[r];
-        const uint32_t w[4] = {s[m].x, s[m].y, s[m].z, s[m].w};
-        uint32_t n[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const __nv_bfloat162 t = __floats2bfloat162_rn(fmaf(kk, dl[2 * c], a * bf_lo(w[c])),
-                                                           fmaf(kk, dl[2 * c + 1], a * bf_hi(w[c])));
-            n[c] = *reinterpret_cast<const uint32_t*>(&t);
-        }
-        __stcs(reinterpret_cast<uint4*>(S + (int64_t)r * D) + cg, make_uint4(n[0], n[1], n[2], n[3]));
-    }
-}
-
 template <typename TIn, typename TS>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
     const unsigned grid = (unsigned)((int64_t)p.B * p.H);
     switch (p.d) {
         case 128:
-            if (p.state_bf16) kda_decode_bf16s_kernel<128, 128, TIn><<<grid, 128, 0, s>>>(p);
-            else kda_decode_cols_kernel<128, 64, 256, TIn><<<2 * grid, 256, 0, s>>>(p);
+            if (p.state_bf16) return cudaErrorInvalidValue;   // streamed by launch_decode_bf16s_stream
+            kda_decode_cols_kernel<128, 64, 256, TIn><<<2 * grid, 256, 0, s>>>(p);
             break;
         case 64:
             if (p.state_bf16) kda_decode_gen_kernel<64, 64, TIn, TS><<<grid, 64, 0, s>>>(p);
@@ -466,6 +359,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, kda_dtype dt, cudaStream_t s) {
+    if (p.state_bf16 && p.d == 128) return launch_decode_bf16s_stream(p, dt, s);
     if (p.state_bf16)
         return dt == KDA_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16, __nv_bfloat16>(p, s)
                                     : launch_decode_t<float, __nv_bfloat16>(p, s);

@@ -94,6 +94,8 @@ constexpr int kBwdMaxCtas = 160;   // chunk-pass CTAs (one per SM)
 
 // Launchers (return the launch error, if any).
 cudaError_t launch_decode(const DecodeParams& p, kda_dtype dt, cudaStream_t s);
+// The bf16-stored state at d = 128 (kda_decode_bf16s.cu): a persistent kernel streaming the states.
+cudaError_t launch_decode_bf16s_stream(const DecodeParams& p, kda_dtype dt, cudaStream_t s);
 cudaError_t launch_prefill_cc(const PrefillParams& p, kda_dtype dt, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s);
 bool prefill_tc_supported(const PrefillParams& p, kda_dtype dt);

@@ -98,3 +98,45 @@ def test_decode_bf16_state_idx_and_untouched_slots():
     assert rel_frob(pool, pool_ref) <= 3e-3
     untouched = [2, 4, 5, 7]
     assert np.array_equal(pool[untouched], pool_ref[untouched])
+
+
+def test_decode_bf16_state_many_states_per_cta():
+    """Thousands of states, so that every CTA of the d = 128 bf16-state kernel streams several of them
+    through its ring of shared-memory stages (and wraps around it), with a state_idx permutation."""
+    B, H, d, P = 300, 8, 128, 310
+    rng = np.random.default_rng(52)
+    idx = rng.permutation(P)[:B].astype(np.int32)
+    o, o_ref, pool, pool_ref = run_steps(B, H, d, "bf16", 3, 52, P=P, idx=idx, decay="slow", state_dtype="bf16")
+    assert rel_frob(o, o_ref) <= 3e-3
+    assert rel_frob(pool, pool_ref) <= 3e-3
+    untouched = np.setdiff1d(np.arange(P), idx)
+    assert np.array_equal(pool[untouched], pool_ref[untouched])
+
+
+def test_decode_bf16_state_bad_slots_are_skipped():
+    """Out-of-range slots among many valid ones: the error word says so, those rows touch nothing, and
+    every other row is still stepped correctly."""
+    import kda_gated_delta_03_gb300 as kda
+    B, H, d, P = 700, 1, 128, 800
+    rng = np.random.default_rng(53)
+    idx = rng.permutation(P)[:B].astype(np.int32)
+    bad = [5, 300, 699]
+    idx[bad] = [-1, P, P + 7]
+    good = np.setdiff1d(np.arange(B), bad)
+    pool = I.bf16_bits_to_f32(I.f32_to_bf16_bits(I.random_state(P, H, d, d, 54)))
+    pool_d = to_dev(I.f32_to_bf16_bits(pool), True)
+    st = I.decode_step_inputs(B, H, d, d, "bf16", 55, 0, decay="slow")
+    o = kda.kda_decode_step(*(to_dev(st[n], n in ("q", "k", "v")) for n in ("q", "k", "v", "beta", "alpha")),
+                            pool_d, to_dev(idx))
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_error() & 0x2
+    sub = dict(st)
+    for n in ("q", "k", "v", "beta", "alpha"):
+        sub[n] = np.ascontiguousarray(st[n][good])
+    ref = pool.astype(np.float64)
+    o_ref = O.decode_step(sub, ref, idx[good], state_dtype="bf16")
+    got = pool_d.double().cpu().numpy()
+    assert rel_frob(o.double().cpu().numpy()[good], o_ref) <= 3e-3
+    assert rel_frob(got[idx[good]], ref[idx[good]]) <= 3e-3
+    untouched = np.setdiff1d(np.arange(P), idx[good])
+    assert np.array_equal(got[untouched], ref[untouched])
