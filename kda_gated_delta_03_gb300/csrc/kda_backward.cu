@@ -532,7 +532,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, kda_dtype dt, int grid, cudaStream_
     }
     if (e != cudaSuccess) return e;
     switch (p.dk) {
-        case 128: return launch_bwd_d<128, 512, TIn>(p, grid, s);
+        case 128: return launch_bwd_chunk_mat(p, dt, grid, s);
         case 64: return launch_bwd_d<64, 256, TIn>(p, grid, s);
         case 16: return launch_bwd_d<16, 32, TIn>(p, grid, s);
         default: return cudaErrorInvalidValue;

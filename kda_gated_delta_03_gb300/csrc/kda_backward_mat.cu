@@ -1,0 +1,718 @@
+// Backward pass 3 at d = 128 in matrix form: one unit per (sequence, chunk, head), every gradient of the
+// chunk from a fixed sequence of products, with no per-token state.
+//
+// "Kimi K3, explained" (section "Training in chunks") writes a chunk of L tokens as products of small
+// matrices once its start state S_0 is known: with g_r the running sum of ln alpha over the chunk,
+// Gamma = exp(g), E_rsi = exp(g_ri - g_si) (s <= r),
+//
+//   Bt_rs = sum_i k_ri k_si E_rsi (s < r),  P_rs = sum_i q_ri k_si E_rsi (s <= r),  T = (I + Diag(beta) Bt)^-1
+//   W = T Diag(beta) (Gamma . K),  U = T Diag(beta) V - W S_0,  Khat = (Gamma_L / Gamma) . K
+//   O = (Gamma . Q) S_0 + P U,  S_1 = Diag(Gamma_L) S_0 + Khat^T U.
+//
+// Reverse mode through those products, given dO = scale * grad_o and the gradient dS_1 of the end state
+// (pass 2), is again a sequence of products:
+//
+//   dU = P^T dO + Khat dS_1,  dP = (dO U^T) on s <= r,  dQs = dO S_0^T,  dKhat = U dS_1^T,  dW = -dU S_0^T
+//   dT = dW (beta . Gamma . K)^T + dU (beta . V)^T,  dA = -(T^T dT T^T) on s < r,  dBt = Diag(beta) dA
+//   dq = sum_s dP_rs k_s E_rs + Gamma . dQs,  dv = beta . (T^T dU)
+//   dk = sum_r dP_rs q_r E_rs + sum_s dBt_rs k_s E_rs + sum_r dBt_rs k_r E_rs + beta Gamma . (T^T dW)
+//        + (Gamma_L / Gamma) . dKhat
+//   dbeta_r = sum_s dA_rs Bt_rs + sum_i (Gamma k)_ri (T^T dW)_ri + sum_i v_ri (T^T dU)_ri
+//   dg = q . (first dq term) - k . (first dk term) + k . (second) - k . (third) + q Gamma . dQs
+//        + beta Gamma k . (T^T dW) - k (Gamma_L / Gamma) . dKhat,
+//        and on the chunk's last row also sum_s (dKhat . Khat)_s + Gamma_L . rowsum(dS_1 . S_0)
+//   d ln alpha_s = sum_{r >= s} dg_r,  dalpha = d ln alpha / alpha.
+//
+// The decayed sums over E are taken per block of 16 rows with a reference row inside the block (the
+// forward's own device): E_rsi = 2^(G_ri - G_ref) 2^(G_ref - G_si) with G = running sum of log2 alpha
+// (clamped at -15 per token, as in the forward), so that no factor exceeds 2^120 and every product is a
+// plain dot product of scaled operands.  Everything is fp32 on the CUDA cores: 64-row products staged 16
+// k at a time through shared memory; the chunk's 64 x 128 matrices live in a per-CTA scratch (L2), its
+// 64 x 64 matrices, k and G in shared memory.  Rows past the end of a partial chunk read as zero with beta = 0 and
+// alpha = 1, which leaves the valid rows' results unchanged.
+
+#include <type_traits>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int MC = 64;                 // chunk rows
+constexpr int MD = 128;                // head dimension (key = value)
+constexpr int MNT = 256;
+constexpr int LD64 = 68;               // floats per row of a shared 64 x 64 matrix
+constexpr int LDY = 132;               // floats per row of a shared scaled operand (float4 reads, no conflicts)
+constexpr int MAT = MC * MD;           // floats per scratch matrix
+
+// shared memory (floats)
+constexpr int F_P = 0;                             // P
+constexpr int F_T = F_P + MC * LD64;               // T
+constexpr int F_DP = F_T + MC * LD64;              // dP
+constexpr int F_DA = F_DP + MC * LD64;             // dA, then dBt
+constexpr int F_BT = F_DA + MC * LD64;             // Bt
+constexpr int F_Y = F_BT + MC * LD64;              // scaled operands [64][LDY]; dT and X [64][LD64] each
+constexpr int F_STG = F_Y + 2 * MC * LD64;         // product staging: A [16][LD64], B [16][LDY]; also 2 x [16][LDY]
+constexpr int F_VEC = F_STG + 2 * 16 * LDY;        // beta [64], G_C [128], row sums [128], column sums [2][128], misc
+constexpr int F_K = F_VEC + 64 + 128 + 128 + 256 + 64;   // k [64][128]
+constexpr int F_G = F_K + MC * MD;                 // G [64][128]
+constexpr int MAT_SMEM_FLOATS = F_G + MC * MD;
+static_assert(2 * MC * LD64 >= MC * LDY, "scaled operand area");
+
+// scratch matrices (each [64][128] fp32, row-major) per CTA; a later matrix takes the slot of one whose
+// last reader has run (dO -> T^T dW, beta Gamma K -> dq_p, beta V -> dk_r, W -> dQs, U -> dk_p,
+// Khat -> dKhat, dU -> dk_s, dW -> T^T dU), so that the scratch of all CTAs stays within L2
+enum : int { XQ = 0, XV, XDO, XKTB, XVB, XW, XU, XKH, XDU, XDW, X_COUNT,
+             XTDW = XDO, XRQ = XKTB, XRK = XVB, XDQS = XW, XCP = XU, XDKH = XKH, XCK = XDU, XTDU = XDW };
+
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+// 16 bytes of a token row as floats
+__device__ __forceinline__ void ld16f(const float* p, float* o) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+}
+__device__ __forceinline__ void ld16f(const __nv_bfloat16* p, float* o) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        o[2 * c] = __uint_as_float(w[c] << 16);
+        o[2 * c + 1] = __uint_as_float(w[c] & 0xFFFF0000u);
+    }
+}
+__device__ __forceinline__ void st4(float* p, const float* v, float s = 1.f) {
+    *reinterpret_cast<float4*>(p) = make_float4(s * v[0], s * v[1], s * v[2], s * v[3]);
+}
+
+__device__ __forceinline__ uint32_t tf32_bits(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};\n"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Output element acc[i][j] of a 64 x NN product sits at (mrow(i), mcol(j)).  CUDA-core path (TC false):
+// thread (tr, tc) = (tid / 16, tid % 16) owns rows 4 tr + i and columns 4 tc + (j & 3) + 64 (j >> 2) (NN =
+// 128) or 4 tc + j (NN = 64).  Tensor-core path: warp w owns rows 32 (w & 1) .. + 31 and columns NN/4 (w >> 1)
+// .. + NN/4 - 1 as 2 x (NN / 32) m16n8 tiles; lane (g, t) = (lane / 4, lane % 4) holds rows g, g + 8 and
+// columns 2 t, 2 t + 1 of each tile (i = 2 m-tile + row half, j = 2 n-tile + column).
+template <bool TC>
+__device__ __forceinline__ int mrow(int i) {
+    const int tid = threadIdx.x;
+    if constexpr (TC) return 32 * ((tid >> 5) & 1) + 16 * (i >> 1) + ((tid & 31) >> 2) + 8 * (i & 1);
+    else return 4 * (tid >> 4) + i;
+}
+template <int NN, bool TC>
+__device__ __forceinline__ int mcol(int j) {
+    const int tid = threadIdx.x;
+    if constexpr (TC) return (NN / 4) * (tid >> 6) + 8 * (j >> 1) + 2 * (tid & 3) + (j & 1);
+    else return NN == 128 ? 4 * (tid & 15) + (j & 3) + 64 * (j >> 2) : 4 * (tid & 15) + j;
+}
+
+// acc[i][j] += sum_{k < KK} A(mrow(i), k) B(k, mcol(j)) for this thread's part of a 64 x NN product, with
+// A(m, k) = A[m am + k ak] and B(k, n) = B[k bk + n bn] (global or shared).  16 k at a time are staged
+// through shared memory (as TF32 on the tensor-core path), the next 16 fetched into registers while the
+// current ones are used.  CUDA-core path: fp32 FFMA; tensor-core path: mma.sync m16n8k8 TF32, fp32
+// accumulate.
+constexpr int LDA = 72;                               // staged A row (k-major): conflict-free fragment loads
+static_assert(16 * LDA + 16 * (128 + 8) <= 2 * 16 * LDY, "staging area");
+template <int NN, int KK, bool TC>
+__device__ __forceinline__ void mm(const float* A, int am, int ak, const float* B, int bk, int bn, float* stage,
+                                   float (&acc)[4][NN / 16]) {
+    constexpr int NJ = NN / 16;
+    constexpr int LB = NN + 8;
+    float* sa = stage;                                 // [16][LDA]: sa[k][m]
+    float* sb = stage + 16 * LDA;                      // [16][LB]:  sb[k][n]
+    const int tid = threadIdx.x, tr = tid >> 4, tc = tid & 15;
+    float ra[4], rb[NJ];
+    auto fetch = [&](int k0) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int idx = tid + MNT * e;
+            const int m = ak == 1 ? idx >> 4 : idx & 63, k = ak == 1 ? idx & 15 : idx >> 6;
+            ra[e] = ldf(A + m * am + (k0 + k) * ak);
+        }
+#pragma unroll
+        for (int e = 0; e < NJ; ++e) {
+            const int idx = tid + MNT * e;
+            const int n = bn == 1 ? idx % NN : idx >> 4, k = bn == 1 ? idx / NN : idx & 15;
+            rb[e] = ldf(B + (k0 + k) * bk + n * bn);
+        }
+    };
+    auto cv = [](float x) { return TC ? __uint_as_float(tf32_bits(x)) : x; };
+    auto put = [&]() {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int idx = tid + MNT * e;
+            const int m = ak == 1 ? idx >> 4 : idx & 63, k = ak == 1 ? idx & 15 : idx >> 6;
+            sa[k * LDA + m] = cv(ra[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < NJ; ++e) {
+            const int idx = tid + MNT * e;
+            const int n = bn == 1 ? idx % NN : idx >> 4, k = bn == 1 ? idx / NN : idx & 15;
+            sb[k * LB + n] = cv(rb[e]);
+        }
+    };
+    fetch(0);
+#pragma unroll 1
+    for (int k0 = 0; k0 < KK; k0 += 16) {
+        __syncthreads();                               // the previous chunk's readers are done
+        put();
+        __syncthreads();
+        if (k0 + 16 < KK) fetch(k0 + 16);
+        if constexpr (TC) {
+            const uint32_t* ua = reinterpret_cast<const uint32_t*>(sa);
+            const uint32_t* ub = reinterpret_cast<const uint32_t*>(sb);
+            const int lane = tid & 31, w = tid >> 5, g = lane >> 2, t = lane & 3;
+            const int m0 = 32 * (w & 1), n0 = (NN / 4) * (w >> 1);
+#pragma unroll
+            for (int kk = 0; kk < 16; kk += 8) {
+                uint32_t a[2][4];
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int m = m0 + 16 * mt + g;
+                    a[mt][0] = ua[(kk + t) * LDA + m];
+                    a[mt][1] = ua[(kk + t) * LDA + m + 8];
+                    a[mt][2] = ua[(kk + t + 4) * LDA + m];
+                    a[mt][3] = ua[(kk + t + 4) * LDA + m + 8];
+                }
+#pragma unroll
+                for (int nt = 0; nt < NN / 32; ++nt) {
+                    const int n = n0 + 8 * nt + g;
+                    const uint32_t b0 = ub[(kk + t) * LB + n], b1 = ub[(kk + t + 4) * LB + n];
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) {
+                        float d[4] = {acc[2 * mt][2 * nt], acc[2 * mt][2 * nt + 1], acc[2 * mt + 1][2 * nt],
+                                      acc[2 * mt + 1][2 * nt + 1]};
+                        mma_tf32(d, a[mt], b0, b1);
+                        acc[2 * mt][2 * nt] = d[0];
+                        acc[2 * mt][2 * nt + 1] = d[1];
+                        acc[2 * mt + 1][2 * nt] = d[2];
+                        acc[2 * mt + 1][2 * nt + 1] = d[3];
+                    }
+                }
+            }
+        } else {
+#pragma unroll 4
+            for (int k = 0; k < 16; ++k) {
+                const float4 a = *reinterpret_cast<const float4*>(sa + k * LDA + 4 * tr);
+                float b[NJ];
+                const float4 b0 = *reinterpret_cast<const float4*>(sb + k * LB + 4 * tc);
+                b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+                if constexpr (NJ == 8) {
+                    const float4 b1 = *reinterpret_cast<const float4*>(sb + k * LB + 64 + 4 * tc);
+                    b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+                }
+                const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < NJ; ++j) acc[i][j] = fmaf(av[i], b[j], acc[i][j]);
+            }
+        }
+    }
+    __syncthreads();                                   // the staging area is free again
+}
+
+// the 128-column layout of the elementwise and decayed passes: thread tid % 16 owns columns
+// 4 (tid % 16) + (j & 3) + 64 (j >> 2)
+__device__ __forceinline__ int col8(int j) {
+    const int tc = threadIdx.x & 15;
+    return 4 * tc + (j & 3) + 64 * (j >> 2);
+}
+template <int NN>
+__device__ __forceinline__ void zero(float (&acc)[4][NN / 16]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < NN / 16; ++j) acc[i][j] = 0.f;
+}
+// store a 64 x 128 product (times s) into a scratch matrix
+template <bool TC>
+__device__ __forceinline__ void put128(float* X, const float (&acc)[4][8], float s = 1.f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) X[mrow<TC>(i) * MD + mcol<128, TC>(j)] = s * acc[i][j];
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) {
+    extern __shared__ __align__(16) float fsm[];
+    float* sP = fsm + F_P;
+    float* sT = fsm + F_T;
+    float* sDP = fsm + F_DP;
+    float* sDA = fsm + F_DA;
+    float* sBT = fsm + F_BT;
+    float* sY = fsm + F_Y;
+    float* stg = fsm + F_STG;
+    float* sbeta = fsm + F_VEC;
+    float* sgc = sbeta + 64;                           // G of the chunk's last row, per key channel
+    float* srow = sgc + 128;                           // sum_j dS_1[i][j] S_0[i][j], per key channel i
+    float* scol = srow + 128;                          // [2][128] column partial sums
+    float* sdb = scol + 256;                           // [64] sum_s dA_rs Bt_rs
+    float* sK = fsm + F_K;
+    float* sG = fsm + F_G;
+    const float* G = sG;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, tr = tid >> 4, tc = tid & 15;
+    // bf16 inputs: the plain products on TF32 tensor cores; fp32 inputs: on the CUDA cores in fp32
+    constexpr bool TC = std::is_same<TIn, __nv_bfloat16>::value;
+    const int H = p.H;
+    const TIn* gq = static_cast<const TIn*>(p.q);
+    const TIn* gk = static_cast<const TIn*>(p.k);
+    const TIn* gv = static_cast<const TIn*>(p.v);
+    const TIn* gdo = static_cast<const TIn*>(p.d_o);
+    TIn* gdq = static_cast<TIn*>(p.d_q);
+    TIn* gdk = static_cast<TIn*>(p.d_k);
+    TIn* gdv = static_cast<TIn*>(p.d_v);
+    float* X = p.scratch + (int64_t)blockIdx.x * (kChunk - 1) * MD * MD;
+    auto M = [&](int x) { return X + x * MAT; };
+
+    const int units = p.chunk_offsets[p.num_seqs] * H;
+    for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const int h = unit % H, ci = unit / H;
+        int n = 0;
+        {                                             // the sequence of chunk unit ci: choff[n] <= ci < choff[n + 1]
+            int hi = p.num_seqs;
+            while (hi - n > 1) {
+                const int mid = (n + hi) >> 1;
+                if (p.chunk_offsets[mid] <= ci) n = mid; else hi = mid;
+            }
+        }
+        const int c = ci - p.chunk_offsets[n];
+        const int32_t tb = p.cu_seqlens[n], te = p.cu_seqlens[n + 1];
+        if (tb < 0 || te < tb || te > p.total_tokens) {
+            if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
+            continue;
+        }
+        const int64_t sidx = ((int64_t)n * H + h) * MD * MD;
+        const int nch = (te - tb + kChunk - 1) / kChunk;
+        const int32_t t0 = tb + c * kChunk;
+        const int L = min(kChunk, te - t0);
+        // S_0: the initial state or the snapshot after chunk c - 1; dS_1: grad_state_out or from pass 2
+        const float* S0 = c == 0 ? (p.state_in ? p.state_in + sidx : nullptr)
+                                 : p.snapshots + ((int64_t)(p.snap_offsets[n] + c - 1) * H + h) * MD * MD;
+        const float* dS1 = c == nch - 1 ? (p.d_state_out ? p.d_state_out + sidx : nullptr)
+                                        : p.dstate_b + ((int64_t)(p.snap_offsets[n] + c) * H + h) * MD * MD;
+
+        // ---- inputs: k (shared), q, v, dO = scale grad_o (scratch), log2 alpha (shared), beta ----
+        {
+            constexpr int EV = 16 / (int)sizeof(TIn);
+#pragma unroll
+            for (int jj = 0; jj < MAT / EV / MNT; ++jj) {
+                const int e0 = (tid + MNT * jj) * EV, r = e0 >> 7;
+                const int64_t g0 = ((int64_t)(t0 + r) * H + h) * MD + (e0 & 127);
+                float kv[EV], qv[EV], vv[EV], dv[EV], av[EV];
+                if (r < L) {
+                    ld16f(gk + g0, kv);
+                    ld16f(gq + g0, qv);
+                    ld16f(gv + g0, vv);
+                    ld16f(gdo + g0, dv);
+#pragma unroll
+                    for (int x = 0; x < EV; x += 4) ld16f(p.alpha + g0 + x, av + x);
+#pragma unroll
+                    for (int x = 0; x < EV; ++x) av[x] = fmaxf(__log2f(av[x]), kLog2AlphaMin);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < EV; ++x) kv[x] = qv[x] = vv[x] = dv[x] = av[x] = 0.f;
+                }
+#pragma unroll
+                for (int x = 0; x < EV; x += 4) {
+                    st4(sK + e0 + x, kv + x);
+                    st4(M(XQ) + e0 + x, qv + x);
+                    st4(M(XV) + e0 + x, vv + x);
+                    st4(M(XDO) + e0 + x, dv + x, p.scale);
+                    st4(sG + e0 + x, av + x);
+                }
+            }
+        }
+        if (tid < MC) sbeta[tid] = tid < L ? p.beta[(int64_t)(t0 + tid) * H + h] : 0.f;
+        {                                              // sum_j dS_1[i][j] S_0[i][j]: two threads per key row
+            const int i = tid >> 1, j0 = (tid & 1) * 64;
+            float sr = 0.f;
+            if (S0 && dS1) {
+#pragma unroll
+                for (int j = 0; j < 64; j += 4) {
+                    const float4 a4 = __ldg(reinterpret_cast<const float4*>(dS1 + i * MD + j0 + j));
+                    const float4 b4 = __ldg(reinterpret_cast<const float4*>(S0 + i * MD + j0 + j));
+                    sr = fmaf(a4.x, b4.x, fmaf(a4.y, b4.y, fmaf(a4.z, b4.z, fmaf(a4.w, b4.w, sr))));
+                }
+            }
+            sr += __shfl_xor_sync(0xffffffffu, sr, 1);
+            if ((tid & 1) == 0) srow[i] = sr;
+        }
+        __syncthreads();
+        {                                              // G = running sum over rows, two threads per key channel
+            const int i = tid & 127, half = tid >> 7;
+            float run = 0.f, v[32];
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) {
+                run += sG[(32 * half + rr) * MD + i];
+                v[rr] = run;
+            }
+            if (half == 0) scol[i] = run;
+            __syncthreads();
+            const float off = half ? scol[i] : 0.f;
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) sG[(32 * half + rr) * MD + i] = v[rr] + off;
+            if (half) sgc[i] = v[31] + off;
+        }
+        __syncthreads();
+
+        // ---- Bt and P, one block of 16 rows at a time (reference row 16 b + 7) ----
+        for (int b = 0; b < 4; ++b) {
+            const int ref = 16 * b + 7, ns = 16 * (b + 1);
+            float* sKB = stg;                          // [16][LDY]: k_r 2^(G_r - G_ref) for the block's rows
+            float* sQB = stg + 16 * LDY;               // [16][LDY]: q_r 2^(G_r - G_ref)
+            for (int e = tid; e < ns * MD; e += MNT) {
+                const int s = e >> 7, i = e & 127;
+                sY[s * LDY + i] = sK[e] * exp2f(G[ref * MD + i] - G[e]);
+            }
+#pragma unroll
+            for (int e = tid; e < 16 * MD; e += MNT) {
+                const int r = e >> 7, i = e & 127, x = (16 * b + r) * MD + i;
+                const float f = exp2f(G[x] - G[ref * MD + i]);
+                sKB[r * LDY + i] = sK[x] * f;
+                sQB[r * LDY + i] = M(XQ)[x] * f;
+            }
+            __syncthreads();
+            const int o = tr, r = 16 * b + o;
+            float dk4[4] = {0.f, 0.f, 0.f, 0.f}, dq4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int i = 0; i < MD; i += 4) {
+                const float4 kb = *reinterpret_cast<const float4*>(sKB + o * LDY + i);
+                const float4 qb = *reinterpret_cast<const float4*>(sQB + o * LDY + i);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int s = tc + 16 * j;
+                    if (s < ns) {
+                        const float4 y = *reinterpret_cast<const float4*>(sY + s * LDY + i);
+                        dk4[j] = fmaf(kb.x, y.x, fmaf(kb.y, y.y, fmaf(kb.z, y.z, fmaf(kb.w, y.w, dk4[j]))));
+                        dq4[j] = fmaf(qb.x, y.x, fmaf(qb.y, y.y, fmaf(qb.z, y.z, fmaf(qb.w, y.w, dq4[j]))));
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int s = tc + 16 * j;
+                sBT[r * LD64 + s] = s < r ? dk4[j] : 0.f;
+                sP[r * LD64 + s] = s <= r ? dq4[j] : 0.f;
+            }
+            __syncthreads();
+        }
+
+        // ---- T = (I + A)^-1, A = Diag(beta) Bt, by 16 x 16 blocks: each diagonal block by forward substitution
+        //      (a thread per column), then T_bc = -T_bb sum_{m = c}^{b - 1} A_bm T_mc in order of b - c ----
+        for (int e = tid; e < MC * MC; e += MNT) sT[(e >> 6) * LD64 + (e & 63)] = 0.f;
+        __syncthreads();
+        if (tid < MC) {
+            const int b = tid >> 4, c = tid & 15;
+            float t[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) t[r] = r == c ? 1.f : 0.f;
+#pragma unroll
+            for (int r = 1; r < 16; ++r) {
+                float z = 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) z = fmaf(sBT[(16 * b + r) * LD64 + 16 * b + m], t[m], z);
+                if (r > c) t[r] = -sbeta[16 * b + r] * z;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sT[(16 * b + r) * LD64 + 16 * b + c] = t[r];
+        }
+        __syncthreads();
+        {
+            float* sZ = sY;                            // [64][LD64]
+            for (int d = 1; d < 4; ++d) {
+                for (int e = tid; e < (4 - d) * 256; e += MNT) {
+                    const int c = e >> 8, b = c + d, r = 16 * b + ((e >> 4) & 15), col = 16 * c + (e & 15);
+                    float z = 0.f;
+                    for (int m = 16 * c; m < 16 * b; ++m) z = fmaf(sBT[r * LD64 + m], sT[m * LD64 + col], z);
+                    sZ[r * LD64 + col] = sbeta[r] * z;
+                }
+                __syncthreads();
+                for (int e = tid; e < (4 - d) * 256; e += MNT) {
+                    const int c = e >> 8, b = c + d, r = 16 * b + ((e >> 4) & 15), col = 16 * c + (e & 15);
+                    float t = 0.f;
+                    for (int m = 16 * b; m <= r; ++m) t = fmaf(sT[r * LD64 + m], sZ[m * LD64 + col], t);
+                    sT[r * LD64 + col] = -t;
+                }
+                __syncthreads();
+            }
+        }
+        // beta Gamma K, beta V and Khat = 2^(G_C - G) K
+#pragma unroll 4
+        for (int e = tid; e < MAT; e += MNT) {
+            const int r = e >> 7, i = e & 127;
+            const float kk = sK[e], g = G[e];
+            M(XKTB)[e] = sbeta[r] * kk * exp2f(g);
+            M(XVB)[e] = sbeta[r] * M(XV)[e];
+            M(XKH)[e] = kk * exp2f(sgc[i] - g);
+        }
+        __syncthreads();
+
+        float acc[4][8];
+        // W = T (beta Gamma K);  Utilde = T (beta V);  U = Utilde - W S_0
+        zero<128>(acc);
+        mm<128, 64, TC>(sT, LD64, 1, M(XKTB), MD, 1, stg, acc);
+        put128<TC>(M(XW), acc);
+        zero<128>(acc);
+        mm<128, 64, TC>(sT, LD64, 1, M(XVB), MD, 1, stg, acc);
+        __syncthreads();                               // W is written
+        if (S0) {
+            float ws[4][8];
+            zero<128>(ws);
+            mm<128, 128, TC>(M(XW), MD, 1, S0, MD, 1, stg, ws);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] -= ws[i][j];
+        }
+        put128<TC>(M(XU), acc);
+        __syncthreads();
+        // dU = P^T dO + Khat dS_1
+        zero<128>(acc);
+        mm<128, 64, TC>(sP, 1, LD64, M(XDO), MD, 1, stg, acc);
+        if (dS1) mm<128, 128, TC>(M(XKH), MD, 1, dS1, MD, 1, stg, acc);
+        put128<TC>(M(XDU), acc);
+        // dP = dO U^T on s <= r
+        {
+            float a64[4][4];
+            zero<64>(a64);
+            mm<64, 128, TC>(M(XDO), MD, 1, M(XU), 1, MD, stg, a64);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = mrow<TC>(i), s = mcol<64, TC>(j);
+                    sDP[r * LD64 + s] = s <= r ? a64[i][j] : 0.f;
+                }
+        }
+        __syncthreads();
+        // dQs = dO S_0^T;  dKhat = U dS_1^T;  dW = -dU S_0^T
+        zero<128>(acc);
+        if (S0) mm<128, 128, TC>(M(XDO), MD, 1, S0, 1, MD, stg, acc);
+        put128<TC>(M(XDQS), acc);
+        zero<128>(acc);
+        if (dS1) mm<128, 128, TC>(M(XU), MD, 1, dS1, 1, MD, stg, acc);
+        put128<TC>(M(XDKH), acc);
+        zero<128>(acc);
+        if (S0) mm<128, 128, TC>(M(XDU), MD, 1, S0, 1, MD, stg, acc);
+        put128<TC>(M(XDW), acc, -1.f);
+        __syncthreads();
+        // dT = dW (beta Gamma K)^T + dU (beta V)^T, kept on a > b (the only part T^T dT T^T reads below
+        // the diagonal); X = dT T^T; dA = -(T^T X) on s < r
+        float* sDT = sY;
+        float* sX = sY + MC * LD64;
+        {
+            float a64[4][4];
+            zero<64>(a64);
+            mm<64, 128, TC>(M(XDW), MD, 1, M(XKTB), 1, MD, stg, a64);
+            mm<64, 128, TC>(M(XDU), MD, 1, M(XVB), 1, MD, stg, a64);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = mrow<TC>(i), s = mcol<64, TC>(j);
+                    sDT[r * LD64 + s] = s < r ? a64[i][j] : 0.f;
+                }
+            __syncthreads();
+            zero<64>(a64);
+            mm<64, 64, TC>(sDT, LD64, 1, sT, 1, LD64, stg, a64);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) sX[mrow<TC>(i) * LD64 + mcol<64, TC>(j)] = a64[i][j];
+            __syncthreads();
+            zero<64>(a64);
+            mm<64, 64, TC>(sT, 1, LD64, sX, LD64, 1, stg, a64);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = mrow<TC>(i), s = mcol<64, TC>(j);
+                    sDA[r * LD64 + s] = s < r ? -a64[i][j] : 0.f;
+                }
+        }
+        // T^T dW, T^T dU
+        zero<128>(acc);
+        mm<128, 64, TC>(sT, 1, LD64, M(XDW), MD, 1, stg, acc);
+        put128<TC>(M(XTDW), acc);
+        zero<128>(acc);
+        mm<128, 64, TC>(sT, 1, LD64, M(XDU), MD, 1, stg, acc);
+        put128<TC>(M(XTDU), acc);
+        __syncthreads();
+        // sum_s dA_rs Bt_rs per row, then dA -> dBt = Diag(beta) dA
+        for (int r = warp; r < MC; r += 8) {
+            float s = sDA[r * LD64 + lane] * sBT[r * LD64 + lane] + sDA[r * LD64 + 32 + lane] * sBT[r * LD64 + 32 + lane];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) sdb[r] = s;
+        }
+        __syncthreads();
+        for (int e = tid; e < MC * MC; e += MNT) sDA[(e >> 6) * LD64 + (e & 63)] *= sbeta[e >> 6];
+        __syncthreads();
+
+        // ---- row-side decayed sums for block b: sum_{s} X_rs k_s E_rs = 2^(G_r - G_ref) sum_s X_rs Y_s ----
+        for (int b = 0; b < 4; ++b) {
+            const int ref = 16 * b + 7, ns = 16 * (b + 1);
+            for (int e = tid; e < ns * MD; e += MNT) {
+                const int s = e >> 7, i = e & 127;
+                sY[s * LDY + i] = sK[e] * exp2f(G[ref * MD + i] - G[e]);
+            }
+            __syncthreads();
+            const int r = 16 * b + tr;
+            float aq[8], ak[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) aq[j] = ak[j] = 0.f;
+            for (int s = 0; s < ns; ++s) {
+                const float xp = sDP[r * LD64 + s], xa = sDA[r * LD64 + s];
+                const float4 y0 = *reinterpret_cast<const float4*>(sY + s * LDY + 4 * tc);
+                const float4 y1 = *reinterpret_cast<const float4*>(sY + s * LDY + 64 + 4 * tc);
+                const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    aq[j] = fmaf(xp, yv[j], aq[j]);
+                    ak[j] = fmaf(xa, yv[j], ak[j]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = col8(j);
+                const float f = exp2f(G[r * MD + i] - G[ref * MD + i]);
+                M(XRQ)[r * MD + i] = f * aq[j];
+                M(XRK)[r * MD + i] = f * ak[j];
+            }
+            __syncthreads();
+        }
+        // ---- column-side decayed sums for block b of s: sum_{r >= s} X_rs y_r E_rs
+        //      = 2^(G_ref - G_s) sum_r X_rs (y_r 2^(G_r - G_ref)), y = q with X = dP, y = k with X = dBt ----
+        for (int b = 0; b < 4; ++b) {
+            const int ref = 16 * b + 7, r0 = 16 * b;
+            for (int pass = 0; pass < 2; ++pass) {
+                const float* src = pass == 0 ? M(XQ) : sK;
+                const float* xs = pass == 0 ? sDP : sDA;
+#pragma unroll 4
+                for (int e = r0 * MD + tid; e < MAT; e += MNT) {
+                    const int r = e >> 7, i = e & 127;
+                    sY[(r - r0) * LDY + i] = src[e] * exp2f(G[e] - G[ref * MD + i]);
+                }
+                __syncthreads();
+                const int s = r0 + tr;
+                float a8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) a8[j] = 0.f;
+                for (int r = r0; r < MC; ++r) {
+                    const float x = xs[r * LD64 + s];
+                    const float4 y0 = *reinterpret_cast<const float4*>(sY + (r - r0) * LDY + 4 * tc);
+                    const float4 y1 = *reinterpret_cast<const float4*>(sY + (r - r0) * LDY + 64 + 4 * tc);
+                    const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) a8[j] = fmaf(x, yv[j], a8[j]);
+                }
+                float* out = M(pass == 0 ? XCP : XCK);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int i = col8(j);
+                    out[s * MD + i] = exp2f(G[ref * MD + i] - G[s * MD + i]) * a8[j];
+                }
+                __syncthreads();
+            }
+        }
+
+        // ---- column sums of dKhat . Khat (the last row's term), and dbeta with a warp per row ----
+        {
+            const int i = tid & 127, half = tid >> 7;
+            float colp = 0.f;
+#pragma unroll 8
+            for (int rr = 0; rr < 32; ++rr) {
+                const int x = (32 * half + rr) * MD + i;
+                colp = fmaf(M(XDKH)[x], sK[x] * exp2f(sgc[i] - G[x]), colp);
+            }
+            scol[half * 128 + i] = colp;
+        }
+        for (int r = warp; r < L; r += 8) {
+            float sb = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int x = r * MD + 32 * u + lane;
+                sb = fmaf(sK[x] * exp2f(G[x]), M(XTDW)[x], sb);
+                sb = fmaf(M(XV)[x], M(XTDU)[x], sb);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sb += __shfl_xor_sync(0xffffffffu, sb, o);
+            if (lane == 0) p.d_beta[(int64_t)(t0 + r) * H + h] = sb + sdb[r];
+        }
+        __syncthreads();
+        // ---- dq, dk, dv; dg into the dq_p scratch (dq_p is used only here) ----
+#pragma unroll 4
+        for (int x = tid; x < MAT; x += MNT) {
+            const int r = x >> 7, i = x & 127;
+            const float gam = exp2f(G[x]), kh = exp2f(sgc[i] - G[x]);
+            const float qv = M(XQ)[x], kv = sK[x], be = sbeta[r];
+            const float rq = M(XRQ)[x], rk = M(XRK)[x], cp = M(XCP)[x], ck = M(XCK)[x];
+            const float dqs = M(XDQS)[x], tdw = M(XTDW)[x], dkh = M(XDKH)[x], tdu = M(XTDU)[x];
+            float d = qv * rq - kv * cp + kv * rk - kv * ck + dqs * qv * gam + be * tdw * kv * gam - dkh * kv * kh;
+            if (r == L - 1) d += scol[i] + scol[128 + i] + exp2f(sgc[i]) * srow[i];
+            M(XRQ)[x] = r < L ? d : 0.f;
+            if (r < L) {
+                const int64_t o = ((int64_t)(t0 + r) * H + h) * MD + i;
+                store_from_float(gdq, o, rq + dqs * gam);
+                store_from_float(gdk, o, cp + rk + ck + be * tdw * gam + dkh * kh);
+                store_from_float(gdv, o, be * tdu);
+            }
+        }
+        __syncthreads();
+        // ---- d ln alpha = running sum of dg from the last row up; dalpha = d ln alpha / alpha ----
+        {
+            const int i = tid & 127, half = tid >> 7;
+            float dg[32], tot = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) {
+                dg[rr] = M(XRQ)[(32 * half + rr) * MD + i];
+                tot += dg[rr];
+            }
+            if (half == 1) scol[i] = tot;
+            __syncthreads();
+            float run = half == 0 ? scol[i] : 0.f;
+#pragma unroll
+            for (int rr = 31; rr >= 0; --rr) {
+                const int r = 32 * half + rr;
+                run += dg[rr];
+                if (r < L) {
+                    const int64_t o = ((int64_t)(t0 + r) * H + h) * MD + i;
+                    p.d_alpha[o] = run / __ldg(p.alpha + o);
+                }
+            }
+        }
+        __syncthreads();                               // the scratch and shared matrices are free
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_chunk_mat(const BwdParams& p, kda_dtype dt, int grid, cudaStream_t s) {
+    constexpr int smem = MAT_SMEM_FLOATS * 4;
+    cudaError_t e;
+    if (dt == KDA_DTYPE_BF16) {
+        if ((e = cudaFuncSetAttribute(kda_bwd_chunk_mat_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      smem)) != cudaSuccess)
+            return e;
+        kda_bwd_chunk_mat_kernel<__nv_bfloat16><<<grid, MNT, smem, s>>>(p);
+    } else {
+        if ((e = cudaFuncSetAttribute(kda_bwd_chunk_mat_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      smem)) != cudaSuccess)
+            return e;
+        kda_bwd_chunk_mat_kernel<float><<<grid, MNT, smem, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

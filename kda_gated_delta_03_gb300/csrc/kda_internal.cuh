@@ -91,6 +91,8 @@ struct BwdParams {
     unsigned* err;
 };
 constexpr int kBwdMaxCtas = 160;   // chunk-pass CTAs (one per SM)
+// Pass 3 at d = 128 in matrix form (kda_backward_mat.cu), one CTA per SM.
+cudaError_t launch_bwd_chunk_mat(const BwdParams& p, kda_dtype dt, int grid, cudaStream_t s);
 
 // Launchers (return the launch error, if any).
 cudaError_t launch_decode(const DecodeParams& p, kda_dtype dt, cudaStream_t s);
