@@ -96,6 +96,20 @@ __device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, uint32_t b
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// One m16n8 tile over `ksteps` steps of k = 8: d += A B with A(m, k) = fa(m, k), B(k, n) = fb(k, n) given as
+// TF32 bits (m < 16, n < 8 relative to the tile).
+template <class FA, class FB>
+__device__ __forceinline__ void tile_mma(float (&d)[4], int ksteps, FA fa, FB fb) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll 2
+    for (int ks = 0; ks < ksteps; ++ks) {
+        const int k0 = 8 * ks;
+        const uint32_t a[4] = {fa(g, k0 + t), fa(g + 8, k0 + t), fa(g, k0 + t + 4), fa(g + 8, k0 + t + 4)};
+        mma_tf32(d, a, fb(k0 + t, g), fb(k0 + t + 4, g));
+    }
+}
+__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(tf32_bits(x)); }
+
 // Output element acc[i][j] of a 64 x NN product sits at (mrow(i), mcol(j)).  CUDA-core path (TC false):
 // thread (tr, tc) = (tid / 16, tid % 16) owns rows 4 tr + i and columns 4 tc + (j & 3) + 64 (j >> 2) (NN =
 // 128) or 4 tc + j (NN = 64).  Tensor-core path: warp w owns rows 32 (w & 1) .. + 31 and columns NN/4 (w >> 1)
@@ -264,6 +278,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, tr = tid >> 4, tc = tid & 15;
     // bf16 inputs: the plain products on TF32 tensor cores; fp32 inputs: on the CUDA cores in fp32
     constexpr bool TC = std::is_same<TIn, __nv_bfloat16>::value;
+    auto cv = [](float x) { return TC ? tf32r(x) : x; };      // operands of the tensor-core products
     const int H = p.H;
     const TIn* gq = static_cast<const TIn*>(p.q);
     const TIn* gk = static_cast<const TIn*>(p.k);
@@ -373,16 +388,45 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             float* sQB = stg + 16 * LDY;               // [16][LDY]: q_r 2^(G_r - G_ref)
             for (int e = tid; e < ns * MD; e += MNT) {
                 const int s = e >> 7, i = e & 127;
-                sY[s * LDY + i] = sK[e] * exp2f(G[ref * MD + i] - G[e]);
+                sY[s * LDY + i] = cv(sK[e] * exp2f(G[ref * MD + i] - G[e]));
             }
+            {
+                float qv[16 * MD / MNT];
 #pragma unroll
-            for (int e = tid; e < 16 * MD; e += MNT) {
-                const int r = e >> 7, i = e & 127, x = (16 * b + r) * MD + i;
-                const float f = exp2f(G[x] - G[ref * MD + i]);
-                sKB[r * LDY + i] = sK[x] * f;
-                sQB[r * LDY + i] = M(XQ)[x] * f;
+                for (int u = 0; u < 16 * MD / MNT; ++u) qv[u] = M(XQ)[16 * b * MD + tid + MNT * u];
+#pragma unroll
+                for (int u = 0; u < 16 * MD / MNT; ++u) {
+                    const int e = tid + MNT * u, r = e >> 7, i = e & 127, x = 16 * b * MD + e;
+                    const float f = exp2f(G[x] - G[ref * MD + i]);
+                    sKB[r * LDY + i] = cv(sK[x] * f);
+                    sQB[r * LDY + i] = cv(qv[u] * f);
+                }
             }
             __syncthreads();
+            if constexpr (TC) {
+                // [KB; QB] (32 x 128) times Y^T (128 x ns): m-tile 0 gives Bt, m-tile 1 gives P
+                const int ntn = ns / 8, g = lane >> 2, t = lane & 3;
+                for (int tau = warp; tau < 2 * ntn; tau += 8) {
+                    const int mt = tau / ntn, nt = tau - mt * ntn;
+                    const float* Ab = stg + mt * 16 * LDY;
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    tile_mma(d, MD / 8, [&](int m, int k) { return __float_as_uint(Ab[m * LDY + k]); },
+                             [&](int k, int n) { return __float_as_uint(sY[(8 * nt + n) * LDY + k]); });
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int r = 16 * b + g + 8 * (q >> 1), sc = 8 * nt + 2 * t + (q & 1);
+                        if (mt == 0) sBT[r * LD64 + sc] = sc < r ? d[q] : 0.f;
+                        else sP[r * LD64 + sc] = sc <= r ? d[q] : 0.f;
+                    }
+                }
+                for (int e = tid; e < 16 * (MC - ns); e += MNT) {     // the block's rows right of column ns
+                    const int r = 16 * b + e / (MC - ns), sc = ns + e % (MC - ns);
+                    sBT[r * LD64 + sc] = 0.f;
+                    sP[r * LD64 + sc] = 0.f;
+                }
+                __syncthreads();
+                continue;
+            }
             const int o = tr, r = 16 * b + o;
             float dk4[4] = {0.f, 0.f, 0.f, 0.f}, dq4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
@@ -448,13 +492,19 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             }
         }
         // beta Gamma K, beta V and Khat = 2^(G_C - G) K
-#pragma unroll 4
-        for (int e = tid; e < MAT; e += MNT) {
-            const int r = e >> 7, i = e & 127;
-            const float kk = sK[e], g = G[e];
-            M(XKTB)[e] = sbeta[r] * kk * exp2f(g);
-            M(XVB)[e] = sbeta[r] * M(XV)[e];
-            M(XKH)[e] = kk * exp2f(sgc[i] - g);
+#pragma unroll 1
+        for (int e0 = tid; e0 < MAT; e0 += 8 * MNT) {
+            float vv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) vv[u] = M(XV)[e0 + MNT * u];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = e0 + MNT * u, r = e >> 7, i = e & 127;
+                const float kk = sK[e], g = G[e];
+                M(XKTB)[e] = sbeta[r] * kk * exp2f(g);
+                M(XVB)[e] = sbeta[r] * vv[u];
+                M(XKH)[e] = kk * exp2f(sgc[i] - g);
+            }
         }
         __syncthreads();
 
@@ -565,9 +615,28 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             const int ref = 16 * b + 7, ns = 16 * (b + 1);
             for (int e = tid; e < ns * MD; e += MNT) {
                 const int s = e >> 7, i = e & 127;
-                sY[s * LDY + i] = sK[e] * exp2f(G[ref * MD + i] - G[e]);
+                sY[s * LDY + i] = cv(sK[e] * exp2f(G[ref * MD + i] - G[e]));
             }
             __syncthreads();
+            if constexpr (TC) {
+                // [dP; dBt] rows of the block (32 x ns) times Y (ns x 128): m-tile 0 gives dq_p, 1 gives dk_r
+                const int g = lane >> 2, t = lane & 3;
+                for (int tau = warp; tau < 32; tau += 8) {
+                    const int mt = tau >> 4, nt = tau & 15;
+                    const float* Xm = mt == 0 ? sDP : sDA;
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    tile_mma(d, ns / 8, [&](int m, int k) { return tf32_bits(Xm[(16 * b + m) * LD64 + k]); },
+                             [&](int k, int n) { return __float_as_uint(sY[k * LDY + 8 * nt + n]); });
+                    float* out = M(mt == 0 ? XRQ : XRK);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int r = 16 * b + g + 8 * (q >> 1), i = 8 * nt + 2 * t + (q & 1);
+                        out[r * MD + i] = exp2f(G[r * MD + i] - G[ref * MD + i]) * d[q];
+                    }
+                }
+                __syncthreads();
+                continue;
+            }
             const int r = 16 * b + tr;
             float aq[8], ak[8];
 #pragma unroll
@@ -599,12 +668,35 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             for (int pass = 0; pass < 2; ++pass) {
                 const float* src = pass == 0 ? M(XQ) : sK;
                 const float* xs = pass == 0 ? sDP : sDA;
-#pragma unroll 4
-                for (int e = r0 * MD + tid; e < MAT; e += MNT) {
-                    const int r = e >> 7, i = e & 127;
-                    sY[(r - r0) * LDY + i] = src[e] * exp2f(G[e] - G[ref * MD + i]);
+#pragma unroll 1
+                for (int e0 = r0 * MD + tid; e0 < MAT; e0 += 8 * MNT) {      // (64 - r0) x 128 = 2048 multiples
+                    float yv[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) yv[u] = src[e0 + MNT * u];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int e = e0 + MNT * u, r = e >> 7, i = e & 127;
+                        sY[(r - r0) * LDY + i] = cv(yv[u] * exp2f(G[e] - G[ref * MD + i]));
+                    }
                 }
                 __syncthreads();
+                if constexpr (TC) {
+                    // X^T (16 x (64 - r0), the block's columns s) times Y ((64 - r0) x 128)
+                    const int g = lane >> 2, t = lane & 3;
+                    float* out = M(pass == 0 ? XCP : XCK);
+                    for (int nt = warp; nt < 16; nt += 8) {
+                        float d[4] = {0.f, 0.f, 0.f, 0.f};
+                        tile_mma(d, (MC - r0) / 8, [&](int m, int k) { return tf32_bits(xs[(r0 + k) * LD64 + r0 + m]); },
+                                 [&](int k, int n) { return __float_as_uint(sY[k * LDY + 8 * nt + n]); });
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int sr = r0 + g + 8 * (q >> 1), i = 8 * nt + 2 * t + (q & 1);
+                            out[sr * MD + i] = exp2f(G[ref * MD + i] - G[sr * MD + i]) * d[q];
+                        }
+                    }
+                    __syncthreads();
+                    continue;
+                }
                 const int s = r0 + tr;
                 float a8[8];
 #pragma unroll
@@ -651,32 +743,44 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             if (lane == 0) p.d_beta[(int64_t)(t0 + r) * H + h] = sb + sdb[r];
         }
         __syncthreads();
-        // ---- dq, dk, dv; dg into the dq_p scratch (dq_p is used only here) ----
-#pragma unroll 4
-        for (int x = tid; x < MAT; x += MNT) {
-            const int r = x >> 7, i = x & 127;
-            const float gam = exp2f(G[x]), kh = exp2f(sgc[i] - G[x]);
-            const float qv = M(XQ)[x], kv = sK[x], be = sbeta[r];
-            const float rq = M(XRQ)[x], rk = M(XRK)[x], cp = M(XCP)[x], ck = M(XCK)[x];
-            const float dqs = M(XDQS)[x], tdw = M(XTDW)[x], dkh = M(XDKH)[x], tdu = M(XTDU)[x];
-            float d = qv * rq - kv * cp + kv * rk - kv * ck + dqs * qv * gam + be * tdw * kv * gam - dkh * kv * kh;
-            if (r == L - 1) d += scol[i] + scol[128 + i] + exp2f(sgc[i]) * srow[i];
-            M(XRQ)[x] = r < L ? d : 0.f;
-            if (r < L) {
-                const int64_t o = ((int64_t)(t0 + r) * H + h) * MD + i;
-                store_from_float(gdq, o, rq + dqs * gam);
-                store_from_float(gdk, o, cp + rk + ck + be * tdw * gam + dkh * kh);
-                store_from_float(gdv, o, be * tdu);
+        // ---- dq, dk, dv; dg into the dq_p scratch (dq_p is used only here); 8 elements at a time, their
+        //      loads issued before any store ----
+#pragma unroll 1
+        for (int x0 = tid; x0 < MAT; x0 += 8 * MNT) {
+            float rq[8], rk[8], cp[8], ck[8], dqs[8], tdw[8], dkh[8], tdu[8], qv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int x = x0 + MNT * u;
+                rq[u] = M(XRQ)[x]; rk[u] = M(XRK)[x]; cp[u] = M(XCP)[x]; ck[u] = M(XCK)[x];
+                dqs[u] = M(XDQS)[x]; tdw[u] = M(XTDW)[x]; dkh[u] = M(XDKH)[x]; tdu[u] = M(XTDU)[x]; qv[u] = M(XQ)[x];
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int x = x0 + MNT * u, r = x >> 7, i = x & 127;
+                const float gam = exp2f(G[x]), kh = exp2f(sgc[i] - G[x]);
+                const float kv = sK[x], be = sbeta[r];
+                float d = qv[u] * rq[u] - kv * cp[u] + kv * rk[u] - kv * ck[u] + dqs[u] * qv[u] * gam +
+                          be * tdw[u] * kv * gam - dkh[u] * kv * kh;
+                if (r == L - 1) d += scol[i] + scol[128 + i] + exp2f(sgc[i]) * srow[i];
+                M(XRQ)[x] = r < L ? d : 0.f;
+                if (r < L) {
+                    const int64_t o = ((int64_t)(t0 + r) * H + h) * MD + i;
+                    store_from_float(gdq, o, rq[u] + dqs[u] * gam);
+                    store_from_float(gdk, o, cp[u] + rk[u] + ck[u] + be * tdw[u] * gam + dkh[u] * kh);
+                    store_from_float(gdv, o, be * tdu[u]);
+                }
             }
         }
         __syncthreads();
         // ---- d ln alpha = running sum of dg from the last row up; dalpha = d ln alpha / alpha ----
         {
             const int i = tid & 127, half = tid >> 7;
-            float dg[32], tot = 0.f;
+            float dg[32], al[32], tot = 0.f;
 #pragma unroll
             for (int rr = 0; rr < 32; ++rr) {
-                dg[rr] = M(XRQ)[(32 * half + rr) * MD + i];
+                const int r = 32 * half + rr;
+                dg[rr] = M(XRQ)[r * MD + i];
+                al[rr] = r < L ? __ldg(p.alpha + ((int64_t)(t0 + r) * H + h) * MD + i) : 1.f;
                 tot += dg[rr];
             }
             if (half == 1) scol[i] = tot;
@@ -686,10 +790,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             for (int rr = 31; rr >= 0; --rr) {
                 const int r = 32 * half + rr;
                 run += dg[rr];
-                if (r < L) {
-                    const int64_t o = ((int64_t)(t0 + r) * H + h) * MD + i;
-                    p.d_alpha[o] = run / __ldg(p.alpha + o);
-                }
+                if (r < L) p.d_alpha[((int64_t)(t0 + r) * H + h) * MD + i] = run / al[rr];
             }
         }
         __syncthreads();                               // the scratch and shared matrices are free
