@@ -204,9 +204,12 @@ KDA_API kda_status kda_prefill_ex(const void* q, const void* k, const void* v, c
  * at the same boundaries (for one bf16 d=128 sequence whose recompute fits one
  * window of records, chunk by chunk from those records: dS_start =
  * Diag(Gamma_C) dS_end - M^T dS_end + Q'^T dO; otherwise token by token); and a
- * chunk-parallel pass that, per (sequence, 64-token chunk, head), replays the
- * chunk from its start state and walks it back token by token from its
- * end-state gradient.  Arguments are kda_prefill's, plus:
+ * chunk-parallel pass that, per (sequence, 64-token chunk, head), takes every
+ * gradient of the chunk from its start state and its end-state gradient: at
+ * d = 128 in matrix form, the chunk's products of "Training in chunks" run in
+ * reverse (on TF32 tensor cores for bf16 inputs, in fp32 for fp32 inputs), at
+ * d = 16 and 64 by replaying the chunk and walking it back token by token.
+ * Arguments are kda_prefill's, plus:
  *   grad_o          [total_tokens, H, d_v] dtype dt
  *   grad_state_out  [num_seqs, H, d_k, d_v] float32, or NULL
  *   grad_q, grad_k  [total_tokens, H, d_k] dtype dt;  grad_v [total_tokens, H, d_v]
@@ -214,7 +217,9 @@ KDA_API kda_status kda_prefill_ex(const void* q, const void* k, const void* v, c
  *   grad_state_in   [num_seqs, H, d_k, d_v] float32, or NULL (not computed)
  *   workspace       at least kda_prefill_backward_workspace_size(...) bytes
  * The decay clamp of the forward (log2 alpha >= -15 per token) is not
- * differentiated: gradients are those of the unclamped recurrence.
+ * differentiated: the d = 16 and 64 walk uses alpha as given, the d = 128
+ * chunk form the clamped decays inside a chunk (as the forward does), and
+ * both give the gradient of alpha itself.
  */
 KDA_API size_t kda_prefill_backward_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H,
                                            int32_t d_k, int32_t d_v, kda_dtype dt);

@@ -333,7 +333,8 @@ BwdLayout bwd_layout(int32_t N, int64_t T, int32_t H, int32_t d, kda_dtype dt) {
     L.o = at; at = align_up(at + (size_t)T * H * d * esize, 256);
     L.st = at; at = align_up(at + (size_t)N * H * dd, 256);
     L.fwd = at; at = align_up(at + kda_prefill_workspace_size(N, T, H, d, d, dt), 256);
-    L.scratch = at; at = align_up(at + ctas * (kda::kChunk - 1) * dd, 256);
+    // per-CTA scratch of the chunk pass: the matrix form's matrices at d = 128, the token walk's states else
+    L.scratch = at; at = align_up(at + ctas * (d == 128 ? kda::kBwdMatScratchBytes : (kda::kChunk - 1) * dd), 256);
     L.total = at;
     return L;
 }

@@ -64,6 +64,7 @@ static_assert(2 * MC * LD64 >= MC * LDY, "scaled operand area");
 // Khat -> dKhat, dU -> dk_s, dW -> T^T dU), so that the scratch of all CTAs stays within L2
 enum : int { XQ = 0, XV, XDO, XKTB, XVB, XW, XU, XKH, XDU, XDW, X_COUNT,
              XTDW = XDO, XRQ = XKTB, XRK = XVB, XDQS = XW, XCP = XU, XDKH = XKH, XCK = XDU, XTDU = XDW };
+static_assert((size_t)X_COUNT * MAT * 4 <= kBwdMatScratchBytes, "per-CTA scratch");
 
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
 // 16 bytes of a token row as floats
@@ -109,6 +110,32 @@ __device__ __forceinline__ void tile_mma(float (&d)[4], int ksteps, FA fa, FB fb
     }
 }
 __device__ __forceinline__ float tf32r(float x) { return __uint_as_float(tf32_bits(x)); }
+// The same with fp32 operands split as x = hi + lo (both TF32) and d += A_hi B_hi + A_hi B_lo + A_lo B_hi:
+// about fp32 accuracy.  The decayed sums that feed the decay gradient need it: its terms cancel, and
+// single TF32 operands there leave a relative error of about 3e-2 in dalpha (a float64 emulation of
+// this arithmetic on the prefill workload), against 3e-4 split.
+template <class FA, class FB>
+__device__ __forceinline__ void tile_mma3(float (&d)[4], int ksteps, FA fa, FB fb) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    auto split = [](float x, uint32_t& hi, uint32_t& lo) {
+        hi = tf32_bits(x);
+        lo = tf32_bits(x - __uint_as_float(hi));
+    };
+#pragma unroll 2
+    for (int ks = 0; ks < ksteps; ++ks) {
+        const int k0 = 8 * ks;
+        uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
+        split(fa(g, k0 + t), ah[0], al[0]);
+        split(fa(g + 8, k0 + t), ah[1], al[1]);
+        split(fa(g, k0 + t + 4), ah[2], al[2]);
+        split(fa(g + 8, k0 + t + 4), ah[3], al[3]);
+        split(fb(k0 + t, g), bh0, bl0);
+        split(fb(k0 + t + 4, g), bh1, bl1);
+        mma_tf32(d, al, bh0, bh1);
+        mma_tf32(d, ah, bl0, bl1);
+        mma_tf32(d, ah, bh0, bh1);
+    }
+}
 
 // Output element acc[i][j] of a 64 x NN product sits at (mrow(i), mcol(j)).  CUDA-core path (TC false):
 // thread (tr, tc) = (tid / 16, tid % 16) owns rows 4 tr + i and columns 4 tc + (j & 3) + 64 (j >> 2) (NN =
@@ -287,7 +314,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
     TIn* gdq = static_cast<TIn*>(p.d_q);
     TIn* gdk = static_cast<TIn*>(p.d_k);
     TIn* gdv = static_cast<TIn*>(p.d_v);
-    float* X = p.scratch + (int64_t)blockIdx.x * (kChunk - 1) * MD * MD;
+    float* X = p.scratch + (int64_t)blockIdx.x * (int64_t)(kBwdMatScratchBytes / 4);
     auto M = [&](int x) { return X + x * MAT; };
 
     const int units = p.chunk_offsets[p.num_seqs] * H;
@@ -615,18 +642,19 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             const int ref = 16 * b + 7, ns = 16 * (b + 1);
             for (int e = tid; e < ns * MD; e += MNT) {
                 const int s = e >> 7, i = e & 127;
-                sY[s * LDY + i] = cv(sK[e] * exp2f(G[ref * MD + i] - G[e]));
+                sY[s * LDY + i] = sK[e] * exp2f(G[ref * MD + i] - G[e]);
             }
             __syncthreads();
             if constexpr (TC) {
-                // [dP; dBt] rows of the block (32 x ns) times Y (ns x 128): m-tile 0 gives dq_p, 1 gives dk_r
+                // [dP; dBt] rows of the block (32 x ns) times Y (ns x 128), split TF32: m-tile 0 gives dq_p,
+                // m-tile 1 dk_r
                 const int g = lane >> 2, t = lane & 3;
                 for (int tau = warp; tau < 32; tau += 8) {
                     const int mt = tau >> 4, nt = tau & 15;
                     const float* Xm = mt == 0 ? sDP : sDA;
                     float d[4] = {0.f, 0.f, 0.f, 0.f};
-                    tile_mma(d, ns / 8, [&](int m, int k) { return tf32_bits(Xm[(16 * b + m) * LD64 + k]); },
-                             [&](int k, int n) { return __float_as_uint(sY[k * LDY + 8 * nt + n]); });
+                    tile_mma3(d, ns / 8, [&](int m, int k) { return Xm[(16 * b + m) * LD64 + k]; },
+                              [&](int k, int n) { return sY[k * LDY + 8 * nt + n]; });
                     float* out = M(mt == 0 ? XRQ : XRK);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -676,18 +704,18 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         const int e = e0 + MNT * u, r = e >> 7, i = e & 127;
-                        sY[(r - r0) * LDY + i] = cv(yv[u] * exp2f(G[e] - G[ref * MD + i]));
+                        sY[(r - r0) * LDY + i] = yv[u] * exp2f(G[e] - G[ref * MD + i]);
                     }
                 }
                 __syncthreads();
                 if constexpr (TC) {
-                    // X^T (16 x (64 - r0), the block's columns s) times Y ((64 - r0) x 128)
+                    // X^T (16 x (64 - r0), the block's columns s) times Y ((64 - r0) x 128), split TF32
                     const int g = lane >> 2, t = lane & 3;
                     float* out = M(pass == 0 ? XCP : XCK);
                     for (int nt = warp; nt < 16; nt += 8) {
                         float d[4] = {0.f, 0.f, 0.f, 0.f};
-                        tile_mma(d, (MC - r0) / 8, [&](int m, int k) { return tf32_bits(xs[(r0 + k) * LD64 + r0 + m]); },
-                                 [&](int k, int n) { return __float_as_uint(sY[k * LDY + 8 * nt + n]); });
+                        tile_mma3(d, (MC - r0) / 8, [&](int m, int k) { return xs[(r0 + k) * LD64 + r0 + m]; },
+                                  [&](int k, int n) { return sY[k * LDY + 8 * nt + n]; });
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const int sr = r0 + g + 8 * (q >> 1), i = 8 * nt + 2 * t + (q & 1);

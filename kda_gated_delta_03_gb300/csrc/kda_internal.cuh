@@ -91,7 +91,9 @@ struct BwdParams {
     unsigned* err;
 };
 constexpr int kBwdMaxCtas = 160;   // chunk-pass CTAs (one per SM)
-// Pass 3 at d = 128 in matrix form (kda_backward_mat.cu), one CTA per SM.
+// Pass 3 at d = 128 in matrix form (kda_backward_mat.cu), one CTA per SM, each with this much scratch
+// (ten 64 x 128 fp32 matrices; the token walk at d = 16, 64 takes 63 states per CTA instead).
+constexpr size_t kBwdMatScratchBytes = (size_t)10 * 64 * 128 * 4;
 cudaError_t launch_bwd_chunk_mat(const BwdParams& p, kda_dtype dt, int grid, cudaStream_t s);
 
 // Launchers (return the launch error, if any).

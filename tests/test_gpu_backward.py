@@ -76,3 +76,12 @@ def test_backward_bad_cu_seqlens_is_reported_not_faulted():
     torch.cuda.synchronize()
     assert kda.kda_get_device_error() & 0x1
     assert kda.kda_get_device_error() == 0
+
+
+def test_backward_workload_decay_from_a_zero_state():
+    """The workload's decay (strong: about a factor 10 per token) from a zero initial state, over several
+    chunks at d = 128: the decay gradient of the first rows is a sum whose terms cancel almost exactly
+    (alpha of the first token multiplies a zero state), which is where a low-precision chunk form shows."""
+    res = run([1024], 2, 128, "bf16", 84, decay="config", with_states=False)
+    for name, (got, ref) in res.items():
+        assert rel_frob(got, ref) <= TOL["bf16"], (name, rel_frob(got, ref))
