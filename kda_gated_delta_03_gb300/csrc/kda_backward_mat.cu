@@ -162,6 +162,7 @@ __device__ __forceinline__ int mcol(int j) {
 // accumulate.
 constexpr int LDA = 72;                               // staged A row (k-major): conflict-free fragment loads
 static_assert(16 * LDA + 16 * (128 + 8) <= 2 * 16 * LDY, "staging area");
+static_assert(3 * (64 * 20 + 128 * 20) <= 2 * MC * LD64 + 2 * 16 * LDY, "product ring (scaled-operand and staging areas)");
 template <int NN, int KK, bool TC>
 __device__ __forceinline__ void mm(const float* A, int am, int ak, const float* B, int bk, int bn, float* stage,
                                    float (&acc)[4][NN / 16]) {
@@ -259,6 +260,114 @@ __device__ __forceinline__ void mm(const float* A, int am, int ak, const float* 
         }
     }
     __syncthreads();                                   // the staging area is free again
+}
+
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// The tensor-core product: acc[i][j] += sum_{k < KK} A(mrow(i), k) B(k, mcol(j)) on mma.sync m16n8k8 TF32
+// (fp32 accumulate), with A(m, k) = AT ? A[k lda + m] : A[m lda + k] and B(k, n) = BT ? B[n ldb + k] :
+// B[k ldb + n].  An operand in shared memory (AS, BS) is read in place; one in global memory streams
+// through a ring of three 16-k stages by 16-byte cp.async, two stages ahead of the one in use, each
+// stored so that the fragment loads are free of bank conflicts (k-contiguous rows of 20 floats, or
+// k-major rows of 72 / NN + 8).  Operands are rounded to TF32 (nearest) as their fragments are loaded.
+constexpr int RING_STAGE = 64 * 20 + 128 * 20;     // floats per stage: A 64 x 20, B up to 128 x 20
+template <int NN, int KK, bool AS, bool AT, bool BS, bool BT>
+__device__ __forceinline__ void mm_tc(const float* A, int lda, const float* B, int ldb, float* ring,
+                                      float (&acc)[4][NN / 16]) {
+    constexpr int NST = KK / 16;
+    constexpr int LAR = 20, LAT = 72, LBR = NN + 8, LBT = 20;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, g = lane >> 2, t = lane & 3;
+    const int m0 = 32 * (w & 1), n0 = (NN / 4) * (w >> 1);
+    auto issue = [&](int st) {
+        float* sa = ring + (st % 3) * RING_STAGE;
+        float* sb = sa + 64 * 20;
+        const int k0 = 16 * st;
+        if constexpr (!AS) {
+            if constexpr (!AT) {
+                const int m = tid >> 2, kq = (tid & 3) * 4;
+                cp_async16(sa + m * LAR + kq, A + m * lda + k0 + kq);
+            } else {
+                const int k = tid >> 4, mq = (tid & 15) * 4;
+                cp_async16(sa + k * LAT + mq, A + (k0 + k) * lda + mq);
+            }
+        }
+        if constexpr (!BS) {
+#pragma unroll
+            for (int e = 0; e < NN / 64; ++e) {
+                const int idx = tid + MNT * e;
+                if constexpr (!BT) {
+                    const int k = idx / (NN / 4), nq = (idx % (NN / 4)) * 4;
+                    cp_async16(sb + k * LBR + nq, B + (k0 + k) * ldb + nq);
+                } else {
+                    const int n = idx >> 2, kq = (idx & 3) * 4;
+                    cp_async16(sb + n * LBT + kq, B + n * ldb + k0 + kq);
+                }
+            }
+        }
+        cp_async_commit_group();
+    };
+    issue(0);
+    if (NST > 1) issue(1);
+#pragma unroll 1
+    for (int st = 0; st < NST; ++st) {
+        if (st + 1 < NST) cp_async_wait_group<1>();
+        else cp_async_wait_group<0>();
+        __syncthreads();                               // stage st landed for every thread; stage st - 1 is read
+        if (st + 2 < NST) issue(st + 2);               // into the slot of stage st - 1
+        const float* sa = ring + (st % 3) * RING_STAGE;
+        const float* sb = sa + 64 * 20;
+        const int k0 = 16 * st;
+        auto fa = [&](int m, int kl) -> float {        // kl: k within the stage
+            if constexpr (AS) return AT ? A[(k0 + kl) * lda + m] : A[m * lda + k0 + kl];
+            else return AT ? sa[kl * LAT + m] : sa[m * LAR + kl];
+        };
+        auto fb = [&](int kl, int n) -> float {
+            if constexpr (BS) return BT ? B[n * ldb + k0 + kl] : B[(k0 + kl) * ldb + n];
+            else return BT ? sb[n * LBT + kl] : sb[kl * LBR + n];
+        };
+#pragma unroll
+        for (int kk = 0; kk < 16; kk += 8) {
+            uint32_t a[2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const int m = m0 + 16 * mt + g;
+                a[mt][0] = tf32_bits(fa(m, kk + t));
+                a[mt][1] = tf32_bits(fa(m + 8, kk + t));
+                a[mt][2] = tf32_bits(fa(m, kk + t + 4));
+                a[mt][3] = tf32_bits(fa(m + 8, kk + t + 4));
+            }
+#pragma unroll
+            for (int nt = 0; nt < NN / 32; ++nt) {
+                const int n = n0 + 8 * nt + g;
+                const uint32_t b0 = tf32_bits(fb(kk + t, n)), b1 = tf32_bits(fb(kk + t + 4, n));
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    float d[4] = {acc[2 * mt][2 * nt], acc[2 * mt][2 * nt + 1], acc[2 * mt + 1][2 * nt],
+                                  acc[2 * mt + 1][2 * nt + 1]};
+                    mma_tf32(d, a[mt], b0, b1);
+                    acc[2 * mt][2 * nt] = d[0];
+                    acc[2 * mt][2 * nt + 1] = d[1];
+                    acc[2 * mt + 1][2 * nt] = d[2];
+                    acc[2 * mt + 1][2 * nt + 1] = d[3];
+                }
+            }
+        }
+    }
+    __syncthreads();                                   // the ring is free again
+}
+
+// One product of the chunk: on the tensor cores (TC) or in fp32 on the CUDA cores.
+template <bool TC, int NN, int KK, bool AS, bool AT, bool BS, bool BT>
+__device__ __forceinline__ void prod(const float* A, int lda, const float* B, int ldb, float* ring, float* stage,
+                                     float (&acc)[4][NN / 16]) {
+    if constexpr (TC) mm_tc<NN, KK, AS, AT, BS, BT>(A, lda, B, ldb, ring, acc);
+    else mm<NN, KK, false>(A, AT ? 1 : lda, AT ? lda : 1, B, BT ? 1 : ldb, BT ? ldb : 1, stage, acc);
 }
 
 // the 128-column layout of the elementwise and decayed passes: thread tid % 16 owns columns
@@ -538,15 +647,15 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         float acc[4][8];
         // W = T (beta Gamma K);  Utilde = T (beta V);  U = Utilde - W S_0
         zero<128>(acc);
-        mm<128, 64, TC>(sT, LD64, 1, M(XKTB), MD, 1, stg, acc);
+        prod<TC, 128, 64, true, false, false, false>(sT, LD64, M(XKTB), MD, sY, stg, acc);
         put128<TC>(M(XW), acc);
         zero<128>(acc);
-        mm<128, 64, TC>(sT, LD64, 1, M(XVB), MD, 1, stg, acc);
+        prod<TC, 128, 64, true, false, false, false>(sT, LD64, M(XVB), MD, sY, stg, acc);
         __syncthreads();                               // W is written
         if (S0) {
             float ws[4][8];
             zero<128>(ws);
-            mm<128, 128, TC>(M(XW), MD, 1, S0, MD, 1, stg, ws);
+            prod<TC, 128, 128, false, false, false, false>(M(XW), MD, S0, MD, sY, stg, ws);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -556,14 +665,14 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         __syncthreads();
         // dU = P^T dO + Khat dS_1
         zero<128>(acc);
-        mm<128, 64, TC>(sP, 1, LD64, M(XDO), MD, 1, stg, acc);
-        if (dS1) mm<128, 128, TC>(M(XKH), MD, 1, dS1, MD, 1, stg, acc);
+        prod<TC, 128, 64, true, true, false, false>(sP, LD64, M(XDO), MD, sY, stg, acc);
+        if (dS1) prod<TC, 128, 128, false, false, false, false>(M(XKH), MD, dS1, MD, sY, stg, acc);
         put128<TC>(M(XDU), acc);
         // dP = dO U^T on s <= r
         {
             float a64[4][4];
             zero<64>(a64);
-            mm<64, 128, TC>(M(XDO), MD, 1, M(XU), 1, MD, stg, a64);
+            prod<TC, 64, 128, false, false, false, true>(M(XDO), MD, M(XU), MD, sY, stg, a64);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -575,24 +684,24 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         __syncthreads();
         // dQs = dO S_0^T;  dKhat = U dS_1^T;  dW = -dU S_0^T
         zero<128>(acc);
-        if (S0) mm<128, 128, TC>(M(XDO), MD, 1, S0, 1, MD, stg, acc);
+        if (S0) prod<TC, 128, 128, false, false, false, true>(M(XDO), MD, S0, MD, sY, stg, acc);
         put128<TC>(M(XDQS), acc);
         zero<128>(acc);
-        if (dS1) mm<128, 128, TC>(M(XU), MD, 1, dS1, 1, MD, stg, acc);
+        if (dS1) prod<TC, 128, 128, false, false, false, true>(M(XU), MD, dS1, MD, sY, stg, acc);
         put128<TC>(M(XDKH), acc);
         zero<128>(acc);
-        if (S0) mm<128, 128, TC>(M(XDU), MD, 1, S0, 1, MD, stg, acc);
+        if (S0) prod<TC, 128, 128, false, false, false, true>(M(XDU), MD, S0, MD, sY, stg, acc);
         put128<TC>(M(XDW), acc, -1.f);
         __syncthreads();
         // dT = dW (beta Gamma K)^T + dU (beta V)^T, kept on a > b (the only part T^T dT T^T reads below
         // the diagonal); X = dT T^T; dA = -(T^T X) on s < r
-        float* sDT = sY;
-        float* sX = sY + MC * LD64;
+        float* sDT = sP;                               // P is not read after dU
+        float* sX = sDA;                               // dA is written once X has been read
         {
             float a64[4][4];
             zero<64>(a64);
-            mm<64, 128, TC>(M(XDW), MD, 1, M(XKTB), 1, MD, stg, a64);
-            mm<64, 128, TC>(M(XDU), MD, 1, M(XVB), 1, MD, stg, a64);
+            prod<TC, 64, 128, false, false, false, true>(M(XDW), MD, M(XKTB), MD, sY, stg, a64);
+            prod<TC, 64, 128, false, false, false, true>(M(XDU), MD, M(XVB), MD, sY, stg, a64);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -602,14 +711,14 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
                 }
             __syncthreads();
             zero<64>(a64);
-            mm<64, 64, TC>(sDT, LD64, 1, sT, 1, LD64, stg, a64);
+            prod<TC, 64, 64, true, false, true, true>(sDT, LD64, sT, LD64, sY, stg, a64);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) sX[mrow<TC>(i) * LD64 + mcol<64, TC>(j)] = a64[i][j];
             __syncthreads();
             zero<64>(a64);
-            mm<64, 64, TC>(sT, 1, LD64, sX, LD64, 1, stg, a64);
+            prod<TC, 64, 64, true, true, true, false>(sT, LD64, sX, LD64, sY, stg, a64);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -620,10 +729,10 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         }
         // T^T dW, T^T dU
         zero<128>(acc);
-        mm<128, 64, TC>(sT, 1, LD64, M(XDW), MD, 1, stg, acc);
+        prod<TC, 128, 64, true, true, false, false>(sT, LD64, M(XDW), MD, sY, stg, acc);
         put128<TC>(M(XTDW), acc);
         zero<128>(acc);
-        mm<128, 64, TC>(sT, 1, LD64, M(XDU), MD, 1, stg, acc);
+        prod<TC, 128, 64, true, true, false, false>(sT, LD64, M(XDU), MD, sY, stg, acc);
         put128<TC>(M(XTDU), acc);
         __syncthreads();
         // sum_s dA_rs Bt_rs per row, then dA -> dBt = Diag(beta) dA
