@@ -53,8 +53,8 @@ constexpr int F_DA = F_DP + MC * LD64;             // dA, then dBt
 constexpr int F_BT = F_DA + MC * LD64;             // Bt
 constexpr int F_Y = F_BT + MC * LD64;              // scaled operands [64][LDY]; dT and X [64][LD64] each
 constexpr int F_STG = F_Y + 2 * MC * LD64;         // product staging: A [16][LD64], B [16][LDY]; also 2 x [16][LDY]
-constexpr int F_VEC = F_STG + 2 * 16 * LDY;        // beta [64], G_C [128], row sums [128], column sums [2][128], misc
-constexpr int F_K = F_VEC + 64 + 128 + 128 + 256 + 64;   // k [64][128]
+constexpr int F_VEC = F_STG + 2 * 16 * LDY;        // beta [64], G_C [128], row sums [128], column sums [2][128], 2 x [64]
+constexpr int F_K = F_VEC + 64 + 128 + 128 + 256 + 64 + 64;   // k [64][128]
 constexpr int F_G = F_K + MC * MD;                 // G [64][128]
 constexpr int MAT_SMEM_FLOATS = F_G + MC * MD;
 static_assert(2 * MC * LD64 >= MC * LDY, "scaled operand area");
@@ -155,15 +155,14 @@ __device__ __forceinline__ int mcol(int j) {
     else return NN == 128 ? 4 * (tid & 15) + (j & 3) + 64 * (j >> 2) : 4 * (tid & 15) + j;
 }
 
-// acc[i][j] += sum_{k < KK} A(mrow(i), k) B(k, mcol(j)) for this thread's part of a 64 x NN product, with
-// A(m, k) = A[m am + k ak] and B(k, n) = B[k bk + n bn] (global or shared).  16 k at a time are staged
-// through shared memory (as TF32 on the tensor-core path), the next 16 fetched into registers while the
-// current ones are used.  CUDA-core path: fp32 FFMA; tensor-core path: mma.sync m16n8k8 TF32, fp32
-// accumulate.
+// The CUDA-core product (fp32 inputs): acc[i][j] += sum_{k < KK} A(mrow(i), k) B(k, mcol(j)) for this
+// thread's part of a 64 x NN product in fp32 FFMA, with A(m, k) = A[m am + k ak] and B(k, n) = B[k bk +
+// n bn] (global or shared).  16 k at a time are staged through shared memory, the next 16 fetched into
+// registers while the current ones are used.
 constexpr int LDA = 72;                               // staged A row (k-major): conflict-free fragment loads
 static_assert(16 * LDA + 16 * (128 + 8) <= 2 * 16 * LDY, "staging area");
 static_assert(3 * (64 * 20 + 128 * 20) <= 2 * MC * LD64 + 2 * 16 * LDY, "product ring (scaled-operand and staging areas)");
-template <int NN, int KK, bool TC>
+template <int NN, int KK>
 __device__ __forceinline__ void mm(const float* A, int am, int ak, const float* B, int bk, int bn, float* stage,
                                    float (&acc)[4][NN / 16]) {
     constexpr int NJ = NN / 16;
@@ -186,19 +185,18 @@ __device__ __forceinline__ void mm(const float* A, int am, int ak, const float* 
             rb[e] = ldf(B + (k0 + k) * bk + n * bn);
         }
     };
-    auto cv = [](float x) { return TC ? __uint_as_float(tf32_bits(x)) : x; };
     auto put = [&]() {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int idx = tid + MNT * e;
             const int m = ak == 1 ? idx >> 4 : idx & 63, k = ak == 1 ? idx & 15 : idx >> 6;
-            sa[k * LDA + m] = cv(ra[e]);
+            sa[k * LDA + m] = ra[e];
         }
 #pragma unroll
         for (int e = 0; e < NJ; ++e) {
             const int idx = tid + MNT * e;
             const int n = bn == 1 ? idx % NN : idx >> 4, k = bn == 1 ? idx / NN : idx & 15;
-            sb[k * LB + n] = cv(rb[e]);
+            sb[k * LB + n] = rb[e];
         }
     };
     fetch(0);
@@ -208,39 +206,7 @@ __device__ __forceinline__ void mm(const float* A, int am, int ak, const float* 
         put();
         __syncthreads();
         if (k0 + 16 < KK) fetch(k0 + 16);
-        if constexpr (TC) {
-            const uint32_t* ua = reinterpret_cast<const uint32_t*>(sa);
-            const uint32_t* ub = reinterpret_cast<const uint32_t*>(sb);
-            const int lane = tid & 31, w = tid >> 5, g = lane >> 2, t = lane & 3;
-            const int m0 = 32 * (w & 1), n0 = (NN / 4) * (w >> 1);
-#pragma unroll
-            for (int kk = 0; kk < 16; kk += 8) {
-                uint32_t a[2][4];
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    const int m = m0 + 16 * mt + g;
-                    a[mt][0] = ua[(kk + t) * LDA + m];
-                    a[mt][1] = ua[(kk + t) * LDA + m + 8];
-                    a[mt][2] = ua[(kk + t + 4) * LDA + m];
-                    a[mt][3] = ua[(kk + t + 4) * LDA + m + 8];
-                }
-#pragma unroll
-                for (int nt = 0; nt < NN / 32; ++nt) {
-                    const int n = n0 + 8 * nt + g;
-                    const uint32_t b0 = ub[(kk + t) * LB + n], b1 = ub[(kk + t + 4) * LB + n];
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        float d[4] = {acc[2 * mt][2 * nt], acc[2 * mt][2 * nt + 1], acc[2 * mt + 1][2 * nt],
-                                      acc[2 * mt + 1][2 * nt + 1]};
-                        mma_tf32(d, a[mt], b0, b1);
-                        acc[2 * mt][2 * nt] = d[0];
-                        acc[2 * mt][2 * nt + 1] = d[1];
-                        acc[2 * mt + 1][2 * nt] = d[2];
-                        acc[2 * mt + 1][2 * nt + 1] = d[3];
-                    }
-                }
-            }
-        } else {
+        {
 #pragma unroll 4
             for (int k = 0; k < 16; ++k) {
                 const float4 a = *reinterpret_cast<const float4*>(sa + k * LDA + 4 * tr);
@@ -367,7 +333,7 @@ template <bool TC, int NN, int KK, bool AS, bool AT, bool BS, bool BT>
 __device__ __forceinline__ void prod(const float* A, int lda, const float* B, int ldb, float* ring, float* stage,
                                      float (&acc)[4][NN / 16]) {
     if constexpr (TC) mm_tc<NN, KK, AS, AT, BS, BT>(A, lda, B, ldb, ring, acc);
-    else mm<NN, KK, false>(A, AT ? 1 : lda, AT ? lda : 1, B, BT ? 1 : ldb, BT ? ldb : 1, stage, acc);
+    else mm<NN, KK>(A, AT ? 1 : lda, AT ? lda : 1, B, BT ? 1 : ldb, BT ? ldb : 1, stage, acc);
 }
 
 // the 128-column layout of the elementwise and decayed passes: thread tid % 16 owns columns
@@ -407,6 +373,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
     float* srow = sgc + 128;                           // sum_j dS_1[i][j] S_0[i][j], per key channel i
     float* scol = srow + 128;                          // [2][128] column partial sums
     float* sdb = scol + 256;                           // [64] sum_s dA_rs Bt_rs
+    float* sdb2 = sdb + 64;                            // [64] the rest of dbeta, by row
     float* sK = fsm + F_K;
     float* sG = fsm + F_G;
     const float* G = sG;
@@ -856,49 +823,35 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             }
         }
 
-        // ---- column sums of dKhat . Khat (the last row's term), and dbeta with a warp per row ----
-        {
-            const int i = tid & 127, half = tid >> 7;
-            float colp = 0.f;
-#pragma unroll 8
-            for (int rr = 0; rr < 32; ++rr) {
-                const int x = (32 * half + rr) * MD + i;
-                colp = fmaf(M(XDKH)[x], sK[x] * exp2f(sgc[i] - G[x]), colp);
-            }
-            scol[half * 128 + i] = colp;
-        }
-        for (int r = warp; r < L; r += 8) {
-            float sb = 0.f;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int x = r * MD + 32 * u + lane;
-                sb = fmaf(sK[x] * exp2f(G[x]), M(XTDW)[x], sb);
-                sb = fmaf(M(XV)[x], M(XTDU)[x], sb);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sb += __shfl_xor_sync(0xffffffffu, sb, o);
-            if (lane == 0) p.d_beta[(int64_t)(t0 + r) * H + h] = sb + sdb[r];
-        }
+        // ---- dq, dk, dv; dg into the dq_p scratch (dq_p is used only here); the rest of dbeta (row sums of
+        //      Gamma k . T^T dW + v . T^T dU) and the column sums of dKhat . Khat on the way.  Element x =
+        //      tid + 256 u keeps the key channel i = tid % 128; 8 elements at a time, their loads issued
+        //      before any store ----
+        if (tid < MC) sdb2[tid] = 0.f;
         __syncthreads();
-        // ---- dq, dk, dv; dg into the dq_p scratch (dq_p is used only here); 8 elements at a time, their
-        //      loads issued before any store ----
+        float colp = 0.f;
 #pragma unroll 1
         for (int x0 = tid; x0 < MAT; x0 += 8 * MNT) {
-            float rq[8], rk[8], cp[8], ck[8], dqs[8], tdw[8], dkh[8], tdu[8], qv[8];
+            float rq[8], rk[8], cp[8], ck[8], dqs[8], tdw[8], dkh[8], tdu[8], qv[8], vv[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int x = x0 + MNT * u;
                 rq[u] = M(XRQ)[x]; rk[u] = M(XRK)[x]; cp[u] = M(XCP)[x]; ck[u] = M(XCK)[x];
-                dqs[u] = M(XDQS)[x]; tdw[u] = M(XTDW)[x]; dkh[u] = M(XDKH)[x]; tdu[u] = M(XTDU)[x]; qv[u] = M(XQ)[x];
+                dqs[u] = M(XDQS)[x]; tdw[u] = M(XTDW)[x]; dkh[u] = M(XDKH)[x]; tdu[u] = M(XTDU)[x];
+                qv[u] = M(XQ)[x]; vv[u] = M(XV)[x];
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int x = x0 + MNT * u, r = x >> 7, i = x & 127;
                 const float gam = exp2f(G[x]), kh = exp2f(sgc[i] - G[x]);
                 const float kv = sK[x], be = sbeta[r];
-                float d = qv[u] * rq[u] - kv * cp[u] + kv * rk[u] - kv * ck[u] + dqs[u] * qv[u] * gam +
-                          be * tdw[u] * kv * gam - dkh[u] * kv * kh;
-                if (r == L - 1) d += scol[i] + scol[128 + i] + exp2f(sgc[i]) * srow[i];
+                const float d = qv[u] * rq[u] - kv * cp[u] + kv * rk[u] - kv * ck[u] + dqs[u] * qv[u] * gam +
+                                be * tdw[u] * kv * gam - dkh[u] * kv * kh;
+                colp = fmaf(dkh[u], kv * kh, colp);
+                float db = fmaf(kv * gam, tdw[u], vv[u] * tdu[u]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) db += __shfl_xor_sync(0xffffffffu, db, o);
+                if (lane == 0) atomicAdd(&sdb2[r], db);
                 M(XRQ)[x] = r < L ? d : 0.f;
                 if (r < L) {
                     const int64_t o = ((int64_t)(t0 + r) * H + h) * MD + i;
@@ -908,18 +861,23 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
                 }
             }
         }
+        scol[(tid >> 7) * 128 + (tid & 127)] = colp;
         __syncthreads();
+        if (tid < L) p.d_beta[(int64_t)(t0 + tid) * H + h] = sdb[tid] + sdb2[tid];
         // ---- d ln alpha = running sum of dg from the last row up; dalpha = d ln alpha / alpha ----
         {
             const int i = tid & 127, half = tid >> 7;
+            // the last row's own term: sum_s dKhat . Khat + Gamma_L . rowsum(dS_1 . S_0)
+            const float extra = scol[i] + scol[128 + i] + exp2f(sgc[i]) * srow[i];
             float dg[32], al[32], tot = 0.f;
 #pragma unroll
             for (int rr = 0; rr < 32; ++rr) {
                 const int r = 32 * half + rr;
-                dg[rr] = M(XRQ)[r * MD + i];
+                dg[rr] = M(XRQ)[r * MD + i] + (r == L - 1 ? extra : 0.f);
                 al[rr] = r < L ? __ldg(p.alpha + ((int64_t)(t0 + r) * H + h) * MD + i) : 1.f;
                 tot += dg[rr];
             }
+            __syncthreads();                           // every thread has read the column sums
             if (half == 1) scol[i] = tot;
             __syncthreads();
             float run = half == 0 ? scol[i] : 0.f;
