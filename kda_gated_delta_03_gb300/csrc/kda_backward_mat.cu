@@ -110,32 +110,52 @@ __device__ __forceinline__ void tile_mma(float (&d)[4], int ksteps, FA fa, FB fb
     }
 }
 __device__ __forceinline__ float tf32r(float x) { return __uint_as_float(tf32_bits(x)); }
-// The same with fp32 operands split as x = hi + lo (both TF32) and d += A_hi B_hi + A_hi B_lo + A_lo B_hi:
-// about fp32 accuracy.  The decayed sums that feed the decay gradient need it: its terms cancel, and
+// MA x NB m16n8 tiles (A fragments shared along a row of tiles, B along a column) with fp32 operands
+// split as x = hi + lo (both TF32) and d += A_hi B_hi + A_hi B_lo + A_lo B_hi: about fp32 accuracy.
+// The decayed sums that feed the decay gradient need it: its terms cancel, and
 // single TF32 operands there leave a relative error of about 3e-2 in dalpha (a float64 emulation of
 // this arithmetic on the prefill workload), against 3e-4 split.
-template <class FA, class FB>
-__device__ __forceinline__ void tile_mma3(float (&d)[4], int ksteps, FA fa, FB fb) {
+// The tiles' MMAs interleave, so that no warp waits on one accumulator's chain.
+template <int MA, int NB, class FA, class FB>
+__device__ __forceinline__ void tiles_mma3(float (&d)[MA][NB][4], int ksteps, FA fa, FB fb) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     auto split = [](float x, uint32_t& hi, uint32_t& lo) {
         hi = tf32_bits(x);
         lo = tf32_bits(x - __uint_as_float(hi));
     };
-#pragma unroll 2
+#pragma unroll 1
     for (int ks = 0; ks < ksteps; ++ks) {
         const int k0 = 8 * ks;
-        uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
-        split(fa(g, k0 + t), ah[0], al[0]);
-        split(fa(g + 8, k0 + t), ah[1], al[1]);
-        split(fa(g, k0 + t + 4), ah[2], al[2]);
-        split(fa(g + 8, k0 + t + 4), ah[3], al[3]);
-        split(fb(k0 + t, g), bh0, bl0);
-        split(fb(k0 + t + 4, g), bh1, bl1);
-        mma_tf32(d, al, bh0, bh1);
-        mma_tf32(d, ah, bl0, bl1);
-        mma_tf32(d, ah, bh0, bh1);
+        uint32_t ah[MA][4], al[MA][4], bh[NB][2], bl[NB][2];
+#pragma unroll
+        for (int ma = 0; ma < MA; ++ma) {
+            split(fa(ma, g, k0 + t), ah[ma][0], al[ma][0]);
+            split(fa(ma, g + 8, k0 + t), ah[ma][1], al[ma][1]);
+            split(fa(ma, g, k0 + t + 4), ah[ma][2], al[ma][2]);
+            split(fa(ma, g + 8, k0 + t + 4), ah[ma][3], al[ma][3]);
+        }
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            split(fb(nb, k0 + t, g), bh[nb][0], bl[nb][0]);
+            split(fb(nb, k0 + t + 4, g), bh[nb][1], bl[nb][1]);
+        }
+#pragma unroll
+        for (int ma = 0; ma < MA; ++ma)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_tf32(d[ma][nb], al[ma], bh[nb][0], bh[nb][1]);
+#pragma unroll
+        for (int ma = 0; ma < MA; ++ma)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_tf32(d[ma][nb], ah[ma], bl[nb][0], bl[nb][1]);
+#pragma unroll
+        for (int ma = 0; ma < MA; ++ma)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_tf32(d[ma][nb], ah[ma], bh[nb][0], bh[nb][1]);
     }
 }
+// outputs written once: streaming stores, so that they do not push the scratch out of L2
+__device__ __forceinline__ void st_out(float* p, int64_t i, float x) { __stcs(p + i, x); }
+__device__ __forceinline__ void st_out(__nv_bfloat16* p, int64_t i, float x) { __stcs(p + i, __float2bfloat16_rn(x)); }
 
 // Output element acc[i][j] of a 64 x NN product sits at (mrow(i), mcol(j)).  CUDA-core path (TC false):
 // thread (tr, tc) = (tid / 16, tid % 16) owns rows 4 tr + i and columns 4 tc + (j & 3) + 64 (j >> 2) (NN =
@@ -724,19 +744,22 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             if constexpr (TC) {
                 // [dP; dBt] rows of the block (32 x ns) times Y (ns x 128), split TF32: m-tile 0 gives dq_p,
                 // m-tile 1 dk_r
+                // (warp w: column tiles w and w + 8 of both)
                 const int g = lane >> 2, t = lane & 3;
-                for (int tau = warp; tau < 32; tau += 8) {
-                    const int mt = tau >> 4, nt = tau & 15;
-                    const float* Xm = mt == 0 ? sDP : sDA;
-                    float d[4] = {0.f, 0.f, 0.f, 0.f};
-                    tile_mma3(d, ns / 8, [&](int m, int k) { return Xm[(16 * b + m) * LD64 + k]; },
-                              [&](int k, int n) { return sY[k * LDY + 8 * nt + n]; });
-                    float* out = M(mt == 0 ? XRQ : XRK);
+                float d[2][2][4] = {};
+                tiles_mma3<2, 2>(d, ns / 8,
+                                 [&](int ma, int m, int k) { return (ma == 0 ? sDP : sDA)[(16 * b + m) * LD64 + k]; },
+                                 [&](int nb, int k, int n) { return sY[k * LDY + 8 * (warp + 8 * nb) + n]; });
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int r = 16 * b + g + 8 * (q >> 1), i = 8 * nt + 2 * t + (q & 1);
-                        out[r * MD + i] = exp2f(G[r * MD + i] - G[ref * MD + i]) * d[q];
-                    }
+                for (int ma = 0; ma < 2; ++ma) {
+                    float* out = M(ma == 0 ? XRQ : XRK);
+#pragma unroll
+                    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int r = 16 * b + g + 8 * (q >> 1), i = 8 * (warp + 8 * nb) + 2 * t + (q & 1);
+                            out[r * MD + i] = exp2f(G[r * MD + i] - G[ref * MD + i]) * d[ma][nb][q];
+                        }
                 }
                 __syncthreads();
                 continue;
@@ -788,16 +811,16 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
                     // X^T (16 x (64 - r0), the block's columns s) times Y ((64 - r0) x 128), split TF32
                     const int g = lane >> 2, t = lane & 3;
                     float* out = M(pass == 0 ? XCP : XCK);
-                    for (int nt = warp; nt < 16; nt += 8) {
-                        float d[4] = {0.f, 0.f, 0.f, 0.f};
-                        tile_mma3(d, (MC - r0) / 8, [&](int m, int k) { return xs[(r0 + k) * LD64 + r0 + m]; },
-                                  [&](int k, int n) { return sY[k * LDY + 8 * nt + n]; });
+                    float d[1][2][4] = {};
+                    tiles_mma3<1, 2>(d, (MC - r0) / 8, [&](int, int m, int k) { return xs[(r0 + k) * LD64 + r0 + m]; },
+                                     [&](int nb, int k, int n) { return sY[k * LDY + 8 * (warp + 8 * nb) + n]; });
+#pragma unroll
+                    for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const int sr = r0 + g + 8 * (q >> 1), i = 8 * nt + 2 * t + (q & 1);
-                            out[sr * MD + i] = exp2f(G[ref * MD + i] - G[sr * MD + i]) * d[q];
+                            const int sr = r0 + g + 8 * (q >> 1), i = 8 * (warp + 8 * nb) + 2 * t + (q & 1);
+                            out[sr * MD + i] = exp2f(G[ref * MD + i] - G[sr * MD + i]) * d[0][nb][q];
                         }
-                    }
                     __syncthreads();
                     continue;
                 }
@@ -855,9 +878,9 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
                 M(XRQ)[x] = r < L ? d : 0.f;
                 if (r < L) {
                     const int64_t o = ((int64_t)(t0 + r) * H + h) * MD + i;
-                    store_from_float(gdq, o, rq[u] + dqs[u] * gam);
-                    store_from_float(gdk, o, cp[u] + rk[u] + ck[u] + be * tdw[u] * gam + dkh[u] * kh);
-                    store_from_float(gdv, o, be * tdu[u]);
+                    st_out(gdq, o, rq[u] + dqs[u] * gam);
+                    st_out(gdk, o, cp[u] + rk[u] + ck[u] + be * tdw[u] * gam + dkh[u] * kh);
+                    st_out(gdv, o, be * tdu[u]);
                 }
             }
         }
@@ -885,7 +908,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             for (int rr = 31; rr >= 0; --rr) {
                 const int r = 32 * half + rr;
                 run += dg[rr];
-                if (r < L) p.d_alpha[((int64_t)(t0 + r) * H + h) * MD + i] = run / al[rr];
+                if (r < L) st_out(p.d_alpha, ((int64_t)(t0 + r) * H + h) * MD + i, run / al[rr]);
             }
         }
         __syncthreads();                               // the scratch and shared matrices are free
