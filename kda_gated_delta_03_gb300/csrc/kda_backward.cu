@@ -14,12 +14,14 @@
 //   2. the state-gradient chain (kda_bwd_dstate_kernel): G alone, carried back token by token,
 //      G <- Diag(alpha_t) (I - beta_t k_t k_t^T) (G + scale q_t do_t^T), which needs no forward state
 //      and splits by value column; it writes G at every 64-token boundary and the gradient of the
-//      initial state;
-//   3. the chunk pass (kda_prefill_bwd_kernel): one unit per (sequence, chunk, head), independent of
-//      the others given the chunk's start state (a snapshot) and the gradient of its end state (from
-//      pass 2): it replays the chunk's tokens into a per-CTA scratch (63 states) and walks them back
-//      with the per-token rules above.  A thread holds 8 key rows x 4 value columns of S, of G and of
-//      S_{t-1}; sums over key rows go through shared memory, sums over value columns through warp
+//      initial state (for one bf16 d = 128 sequence whose recompute ran as one window, the chain goes
+//      chunk by chunk from the recompute's records instead: kda_bwd_dstate_records_kernel);
+//   3. the chunk pass: one unit per (sequence, chunk, head), independent of the others given the
+//      chunk's start state (a snapshot) and the gradient of its end state (from pass 2).  At d = 128 it
+//      runs in matrix form (kda_bwd_chunk_mat_kernel, kda_backward_mat.cu); at d = 16 and 64
+//      kda_prefill_bwd_kernel replays the chunk's tokens into a per-CTA scratch (63 states) and walks
+//      them back with the per-token rules above.  A thread holds 8 key rows x 4 value columns of S, of G
+//      and of S_{t-1}; sums over key rows go through shared memory, sums over value columns through warp
 //      shuffles (the LPR threads of a row group are consecutive lanes).
 
 #include "kda_internal.cuh"

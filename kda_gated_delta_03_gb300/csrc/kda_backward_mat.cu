@@ -26,10 +26,12 @@
 // The decayed sums over E are taken per block of 16 rows with a reference row inside the block (the
 // forward's own device): E_rsi = 2^(G_ri - G_ref) 2^(G_ref - G_si) with G = running sum of log2 alpha
 // (clamped at -15 per token, as in the forward), so that no factor exceeds 2^120 and every product is a
-// plain dot product of scaled operands.  Everything is fp32 on the CUDA cores: 64-row products staged 16
-// k at a time through shared memory; the chunk's 64 x 128 matrices live in a per-CTA scratch (L2), its
-// 64 x 64 matrices, k and G in shared memory.  Rows past the end of a partial chunk read as zero with beta = 0 and
-// alpha = 1, which leaves the valid rows' results unchanged.
+// plain dot product of scaled operands.  For bf16 inputs the products run on mma.sync m16n8k8 TF32 (fp32
+// accumulate): the plain ones and Bt, P with single TF32 operands, the decayed sums that feed the decay
+// gradient with split (hi + lo) TF32; for fp32 inputs every product is fp32 FFMA.  The chunk's 64 x 128
+// matrices live in a per-CTA scratch (L2), its 64 x 64 matrices, k and G in shared memory.  Rows past
+// the end of a partial chunk read as zero with beta = 0 and alpha = 1, which leaves the valid rows'
+// results unchanged.
 
 #include <type_traits>
 
