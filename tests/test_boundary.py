@@ -64,6 +64,28 @@ def test_workspace_size(lib):
     assert lib.kda_prefill_workspace_size(65, 300000, 32, 128, 128, 1) == 512
 
 
+def test_backward_workspace_size(lib):
+    """The backward workspace: offsets, the recompute's snapshots and the state gradients at every 64-token
+    boundary, the recompute's o and state_out, its own prefill workspace, and the chunk pass's per-CTA
+    scratch (one CTA per SM, at most 160): ten 64 x 128 fp32 matrices for the matrix form at d = 128,
+    63 states for the token walk at d = 16 and 64."""
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    def expected(N, T, H, d, dt):
+        dd, es = d * d * 4, 2 if dt == 1 else 4
+        ctas = min((T // 64 + N) * H, 160)
+        parts = [(N + 1) * 8, (T // 64) * H * dd, (T // 64) * H * dd, T * H * d * es, N * H * dd,
+                 lib.kda_prefill_workspace_size(N, T, H, d, d, dt),
+                 ctas * (10 * 64 * 128 * 4 if d == 128 else 63 * dd)]
+        return sum(up(x) for x in parts)
+
+    for args in ((1, 8192, 32, 128, 1), (3, 700, 2, 128, 1), (2, 1000, 4, 64, 0), (4, 300, 2, 16, 0)):
+        N, T, H, d, dt = args
+        assert lib.kda_prefill_backward_workspace_size(N, T, H, d, d, dt) == expected(*args), args
+    assert lib.kda_prefill_backward_workspace_size(1, 8192, 32, 32, 32, 1) == 0        # unsupported head size
+
+
 def test_launch_count_host_paths(lib):
     """Launch counts that need no device: rejected arguments, the single-kernel paths."""
     assert lib.kda_prefill_launch_count(0, 0, 2, 16, 16, 0, 0) == 0
