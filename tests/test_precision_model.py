@@ -1,13 +1,18 @@
-"""A float64 model of the backward chunk pass's operand precision, against the float64 chunk oracle.
+"""Float64 models of the operand precision of two CUDA paths, against the float64 oracles.
 
-The d = 128 backward chunk pass (bf16 inputs) runs its plain products with TF32 operands (10-bit
-significand, rounded to nearest) and its decayed sums by 16-row blocks with a reference row inside each
-block.  This model repeats that arithmetic in numpy on one head of the prefill workload (its decay,
-a zero initial state) and checks the two facts the kernel's design rests on: TF32 operands everywhere
-but in the decayed sums that feed the decay gradient keep every gradient well inside the bf16
-tolerance, while single TF32 operands in those sums do not (the terms of dg cancel almost exactly for
-the first rows of a sequence that starts from zero), which is why they run in split (hi + lo) TF32.
-Nothing here touches the CUDA path."""
+Backward chunk pass at d = 128 (bf16 inputs): plain products on TF32 operands (10-bit significand,
+rounded to nearest), decayed sums by 16-row blocks with a reference row inside each block.  On one head
+of the prefill workload (its decay, a zero initial state): TF32 operands everywhere but in the decayed
+sums that feed the decay gradient keep every gradient well inside the bf16 tolerance, while single TF32
+operands in those sums do not (the terms of dg cancel almost exactly for the first rows of a sequence
+that starts from zero), which is why they run in split (hi + lo) TF32.
+
+Two-phase forward (one bf16 d = 128 sequence): fp16 records and operands with TF32 A/P factors stay
+inside the tolerance for every decay, and fp16 (not bf16) M and Q' are what keep the state error low
+when nothing decays.
+
+Nothing here touches the CUDA path: these are models of its arithmetic, written from the same chunk
+equations as the oracles."""
 
 import numpy as np
 import pytest
@@ -145,3 +150,84 @@ def test_single_tf32_decayed_sums_would_break_the_decay_gradient(chunks):
     e = errors(chunks, "tf32", "tf32", "tf32")
     assert e["dalpha"] > 3e-3, e
     assert max(v for n, v in e.items() if n != "dalpha") < 1e-3, e
+
+
+# ---- the two-phase forward (one bf16 d = 128 sequence) ----
+
+def f16(x):
+    """Round to fp16, nearest-even."""
+    return np.asarray(x, np.float64).astype(np.float32).astype(np.float16).astype(np.float64)
+
+
+def f32(x):
+    return np.asarray(x, np.float64).astype(np.float32).astype(np.float64)
+
+
+def bf16(x):
+    return I.bf16_bits_to_f32(I.f32_to_bf16_bits(np.asarray(x, np.float32))).astype(np.float64)
+
+
+def two_phase_model(q, k, v, beta, alpha, s0, mq):
+    """One head through the two-phase arithmetic: phase 1 per chunk (A and P on TF32 operands by 16-row
+    blocks; T' = (I + A)^-1 Diag(beta), Gamma K, V, W, Utilde, Khat and P as fp16 operands; the record
+    Q' = Gamma Q - P W, M = Khat^T W, B = Khat^T Utilde and P Utilde stored as fp16, M and Q' through `mq`),
+    then the chain: o = Q' S + P Utilde and S <- Diag(Gamma_C) S + B - M S with S fp32 and its operand
+    fp16 ("Kimi K3, explained", section "Training in chunks", with the chunk made affine in S)."""
+    T = k.shape[0]
+    S, o = s0.copy(), np.empty((T, v.shape[1]))
+    for c0 in range(0, T, C):
+        L = min(C, T - c0)
+        Q, K, V, b = q[c0:c0 + L], k[c0:c0 + L], v[c0:c0 + L], beta[c0:c0 + L]
+        g = np.cumsum(np.maximum(np.log2(alpha[c0:c0 + L]), -15.0), axis=0)
+        gam = 2.0 ** g
+        A, P = np.zeros((L, L)), np.zeros((L, L))
+        for blk in range(0, L, 16):
+            ref, rows, cols = g[min(blk + 7, L - 1)], slice(blk, min(blk + 16, L)), slice(0, min(blk + 16, L))
+            R = tf32(K[cols] * 2.0 ** (ref - g[cols]))
+            A[rows, cols] = b[rows, None] * (tf32(K[rows] * 2.0 ** (g[rows] - ref)) @ R.T)
+            P[rows, cols] = tf32(Q[rows] * 2.0 ** (g[rows] - ref)) @ R.T
+        A, P = np.tril(A, -1), f16(np.tril(P))
+        Tp = f16(np.linalg.inv(np.eye(L) + A) * b[None, :])
+        W, Ut = f16(Tp @ f16(gam * K)), f16(Tp @ f16(V))
+        Kh = f16(2.0 ** (g[-1][None, :] - g) * K)
+        M, B = mq(f32(Kh.T @ W)), f16(Kh.T @ Ut)
+        Qp, Oi = mq(f32(gam * Q - P @ W)), f16(P @ Ut)
+        o[c0:c0 + L] = Qp @ f16(S) + Oi
+        S = f32(2.0 ** g[-1][:, None] * S + B - M @ f16(S))
+    return o, S
+
+
+def two_phase_errors(decay, mq):
+    """Relative Frobenius errors of o (rounded to bf16) and of the final state against the float64 token
+    oracle, over two heads of a 1,024-token sequence with a random initial state."""
+    from oracle import oracle as O
+    inp = I.prefill_inputs([1024], 2, 128, 128, "bf16", 3, decay=decay, state="randn")
+    o_ref, s_ref = O.prefill(inp)
+    f = lambda x: I.bf16_bits_to_f32(x).astype(np.float64)
+    os_, ss_ = [], []
+    for h in range(2):
+        o, s = two_phase_model(f(inp["q"][:, h]), f(inp["k"][:, h]), f(inp["v"][:, h]),
+                               inp["beta"][:, h].astype(np.float64), inp["alpha"][:, h].astype(np.float64),
+                               inp["state_in"][0, h].astype(np.float64), mq)
+        os_.append(o)
+        ss_.append(s)
+    eo = np.linalg.norm(bf16(np.stack(os_, 1)) - o_ref) / np.linalg.norm(o_ref)
+    es = np.linalg.norm(np.stack(ss_) - s_ref[0]) / np.linalg.norm(s_ref[0])
+    return eo, es
+
+
+@pytest.mark.parametrize("decay", ["one", "slow", "config"])
+def test_two_phase_forward_precision_model_within_tolerance(decay):
+    """fp16 records and operands, TF32 A/P factors: o and the final state against the float64 token oracle,
+    inside the bf16 tolerance (3e-3) with margin, for no decay, slow decay and the workload's decay (about
+    1.7e-3 on o, most of it the bf16 rounding of o itself)."""
+    eo, es = two_phase_errors(decay, f16)
+    assert eo < 2.5e-3 and es < 1.0e-3, (eo, es)
+
+
+def test_fp16_records_beat_bf16_records_without_decay():
+    """M and Q' in bf16 (8-bit significand) instead of fp16 more than double the state error when nothing
+    decays (the chain then compounds every chunk's rounding); the reason the records are fp16."""
+    eo16, es16 = two_phase_errors("one", f16)
+    eob, esb = two_phase_errors("one", bf16)
+    assert esb > 2 * es16 and eob > eo16, (es16, esb, eo16, eob)
