@@ -45,9 +45,10 @@ def run(seqlens, H, d, dtype, seed, decay="slow", with_states=True):
 @pytest.mark.parametrize("case", [([70, 1, 0, 130], 2, 16, "f32"), ([200], 2, 64, "f32"),
                                   ([100, 64, 129], 2, 128, "bf16"), ([300], 2, 128, "bf16"),
                                   ([700, 1100], 3, 128, "bf16"), ([2000], 1, 128, "bf16"),
-                                  ([64, 128, 191], 2, 64, "bf16")],
+                                  ([64, 128, 191], 2, 64, "bf16"), ([130, 64], 2, 128, "f32")],
                          ids=["cuda_core_d16", "cuda_core_d64", "tensor_core_varlen", "two_phase",
-                              "tensor_core_many_chunks", "two_phase_many_chunks", "cuda_core_bf16_boundaries"])
+                              "tensor_core_many_chunks", "two_phase_many_chunks", "cuda_core_bf16_boundaries",
+                              "matrix_form_fp32"])
 def test_backward_matches_oracle(case):
     seqlens, H, d, dtype = case
     res = run(seqlens, H, d, dtype, 61 + d)
