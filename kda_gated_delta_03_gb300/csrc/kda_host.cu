@@ -9,6 +9,7 @@
 // the copies take longer than the compute and the pipeline hides all but the last segment's compute.
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -153,6 +154,7 @@ kda_status kda_prefill_host(const void* q, const void* k, const void* v, const f
     if (num_seqs <= 0 || total_tokens < 0 || total_tokens > INT32_MAX || H <= 0 || d_k <= 0 || d_v <= 0)
         return KDA_ERR_INVALID_ARG;
     if (dt != KDA_DTYPE_F32 && dt != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
     if (!supported(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
     if (!cu_seqlens || !state_out) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !beta || !alpha || !o)) return KDA_ERR_INVALID_ARG;
@@ -191,11 +193,18 @@ kda_status kda_prefill_host(const void* q, const void* k, const void* v, const f
     if (!ok(cudaEventRecord(hp->fork, s)) || !ok(cudaStreamWaitEvent(hp->h2d, hp->fork, 0)) ||
         !ok(cudaStreamWaitEvent(hp->d2h, hp->fork, 0)))
         return KDA_ERR_CUDA;
+    // once the copy streams are forked, every return joins them back into the caller's stream, so that no
+    // copy that reads or writes the caller's host buffers outlives the call unordered (also on an error)
+    auto join = [&](kda_status st_) -> kda_status {
+        bool joined = ok(cudaEventRecord(hp->fork, hp->h2d)) && ok(cudaStreamWaitEvent(hp->d2h, hp->fork, 0)) &&
+                      ok(cudaEventRecord(hp->out_done, hp->d2h)) && ok(cudaStreamWaitEvent(s, hp->out_done, 0));
+        return st_ != KDA_OK ? st_ : (joined ? KDA_OK : KDA_ERR_CUDA);
+    };
     int32_t* cu_dev = reinterpret_cast<int32_t*>(db + L.cu);
     if (!ok(cudaMemcpyAsync(cu_dev, cu_seqlens, (size_t)(num_seqs + 1) * 4, cudaMemcpyHostToDevice, hp->h2d)))
-        return KDA_ERR_CUDA;
+        return join(KDA_ERR_CUDA);
     kda_segment_cu_kernel<<<1, 128, 0, hp->h2d>>>(cu_dev, sc, cu_dev);
-    if (!ok(cudaGetLastError())) return KDA_ERR_CUDA;
+    if (!ok(cudaGetLastError())) return join(KDA_ERR_CUDA);
     // inputs, segment by segment
     for (int i = 0; i < S; ++i) {
         const size_t r0 = (size_t)seg[i].t0 * H, nr = (size_t)(seg[i].t1 - seg[i].t0) * H;
@@ -207,15 +216,15 @@ kda_status kda_prefill_host(const void* q, const void* k, const void* v, const f
             for (int a = 0; a < 5; ++a)
                 if (!ok(cudaMemcpyAsync(db + off[a] + r0 * width[a], src[a] + r0 * width[a], nr * width[a],
                                         cudaMemcpyHostToDevice, hp->h2d)))
-                    return KDA_ERR_CUDA;
+                    return join(KDA_ERR_CUDA);
         }
         if (state_in && (!cut || i == 0)) {
             const size_t b0 = (size_t)seg[i].n0 * st, nb = (size_t)(seg[i].n1 - seg[i].n0) * st;
             if (!ok(cudaMemcpyAsync(db + L.s_in + b0, reinterpret_cast<const char*>(state_in) + b0, nb,
                                     cudaMemcpyHostToDevice, hp->h2d)))
-                return KDA_ERR_CUDA;
+                return join(KDA_ERR_CUDA);
         }
-        if (!ok(cudaEventRecord(hp->in_done[i], hp->h2d))) return KDA_ERR_CUDA;
+        if (!ok(cudaEventRecord(hp->in_done[i], hp->h2d))) return join(KDA_ERR_CUDA);
     }
     // compute on the caller's stream, outputs back on the second copy stream
     for (int i = 0; i < S; ++i) {
@@ -226,27 +235,25 @@ kda_status kda_prefill_host(const void* q, const void* k, const void* v, const f
                               : reinterpret_cast<const float*>(db + L.s_out);
         else if (state_in) sin = reinterpret_cast<const float*>(db + L.s_in + (size_t)seg[i].n0 * st);
         float* sout = reinterpret_cast<float*>(db + L.s_out + (size_t)seg[i].n0 * st);
-        if (!ok(cudaStreamWaitEvent(s, hp->in_done[i], 0))) return KDA_ERR_CUDA;
+        if (!ok(cudaStreamWaitEvent(s, hp->in_done[i], 0))) return join(KDA_ERR_CUDA);
         const kda_status ks = kda_prefill_ex(db + L.q + r0 * d_k * es, db + L.k + r0 * d_k * es,
                                              db + L.v + r0 * d_v * es, reinterpret_cast<const float*>(db + L.beta) + r0,
                                              reinterpret_cast<const float*>(db + L.alpha) + r0 * d_k, cu_dev + sc.at[i],
                                              segN, seg[i].t1 - seg[i].t0, H, d_k, d_v, dt, scale, sin, sout,
                                              db + L.o + r0 * d_v * es, db + L.ws, L.ws_bytes, s, nullptr);
-        if (ks != KDA_OK) return ks;
+        if (ks != KDA_OK) return join(ks);
         if (!ok(cudaEventRecord(hp->seg_done[i], s)) || !ok(cudaStreamWaitEvent(hp->d2h, hp->seg_done[i], 0)))
-            return KDA_ERR_CUDA;
+            return join(KDA_ERR_CUDA);
         if (nr > 0 && !ok(cudaMemcpyAsync(static_cast<char*>(o) + r0 * d_v * es, db + L.o + r0 * d_v * es,
                                           nr * d_v * es, cudaMemcpyDeviceToHost, hp->d2h)))
-            return KDA_ERR_CUDA;
+            return join(KDA_ERR_CUDA);
         if (!cut || i == S - 1) {
             const size_t b0 = (size_t)seg[i].n0 * st, nb = (size_t)(seg[i].n1 - seg[i].n0) * st;
             if (!ok(cudaMemcpyAsync(reinterpret_cast<char*>(state_out) + b0, db + L.s_out + b0, nb,
                                     cudaMemcpyDeviceToHost, hp->d2h)))
-                return KDA_ERR_CUDA;
+                return join(KDA_ERR_CUDA);
         }
     }
     // the caller's stream completes only after the last copy back
-    if (!ok(cudaEventRecord(hp->out_done, hp->d2h)) || !ok(cudaStreamWaitEvent(s, hp->out_done, 0)))
-        return KDA_ERR_CUDA;
-    return KDA_OK;
+    return join(KDA_OK);
 }

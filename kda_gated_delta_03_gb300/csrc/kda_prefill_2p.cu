@@ -13,7 +13,7 @@
 // operand.  Phase 2 walks the chunks in order, one CTA per (head, 32 value columns), bulk-loading each
 // record one chunk ahead; per chunk it issues a single batch of tensor-core products,
 //
-//   [Q'; M_top] S  and  M S              tcgen05 kind::tf32, M=128, N=32, K=128
+//   M S  and  [Q'; M_top] S              tcgen05 kind::f16 (fp16 record and state operands), M=128, N=32, K=128
 //
 // followed by the fp32 update S <- Gamma_C . S + B - M S and o = scale (Q' S + P Utilde).  Folding W
 // into M and Q' doubles phase 1's work on W but leaves one round trip through the tensor core on the
@@ -67,7 +67,8 @@ constexpr int SOP_BYTES = SNV * DK * 2;            // S^T operand: fp16 32 x 128
 constexpr int C_OFF_S = 2 * QM_BYTES;              // two record buffers, then two S^T operands
 constexpr int C_OFF_MISC = C_OFF_S + 2 * SOP_BYTES;
 constexpr int C_SMEM = C_OFF_MISC + 128;
-constexpr int C_NT = NT + 6 * 32;                  // 8 state warps, 2 MMA-issue warps, 2 idle, 2 output warps
+constexpr int C_NT = NT + 6 * 32;                  // 8 state warps, the MMA-issue warp, the record-loader warp,
+                                                   // 2 idle warps, 2 output warps (on TMEM lanes 0..63)
 static_assert(C_OFF_S % 1024 == 0 && C_SMEM <= 232448, "phase-2 shared memory");
 
 struct PrepMaps {

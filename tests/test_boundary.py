@@ -210,9 +210,10 @@ def test_alpha_layout_validation(lib):
 
 
 # ---- kda_prefill_host: cu_seqlens is host memory, so all of it is checked on the host ----
-def host_prefill(lib, cu, N, T, d=128, dt=1, state_out=P, buf=P, buf_bytes=1 << 40):
+def host_prefill(lib, cu, N, T, d=128, dt=1, state_out=P, buf=P, buf_bytes=1 << 40, scale=1.0):
     arr = (ctypes.c_int32 * len(cu))(*cu)
-    return lib.kda_prefill_host(P, P, P, P, P, arr, N, T, 2, d, d, dt, 1.0, None, state_out, P, buf, buf_bytes, None)
+    return lib.kda_prefill_host(P, P, P, P, P, arr, N, T, 2, d, d, dt, scale, None, state_out, P, buf, buf_bytes,
+                                None)
 
 
 def test_host_prefill_buffer_size(lib):
@@ -238,6 +239,10 @@ def test_host_prefill_rejects_bad_arguments(lib):
     assert host_prefill(lib, [0, 10], 1, 10, buf=None) == WS
     assert host_prefill(lib, [0, 10], 1, 10, buf=ctypes.c_void_p(0x10010)) == WS     # not 256-byte aligned
     assert host_prefill(lib, [0, 10], 1, 10, buf_bytes=1024) == WS
+    # a non-finite scale is refused before any copy is queued (without a GPU, any CUDA call would give
+    # KDA_ERR_CUDA instead)
+    assert host_prefill(lib, [0, 10], 1, 10, scale=float("nan")) == INV
+    assert host_prefill(lib, [0, 10], 1, 10, scale=float("inf")) == INV
     assert lib.kda_prefill_host(P, P, P, P, P, None, 1, 10, 2, 16, 16, 0, 1.0, None, P, P, P, 1 << 40, None) == INV
     assert lib.kda_prefill_host(None, P, P, P, P, (ctypes.c_int32 * 2)(0, 10), 1, 10, 2, 16, 16, 0, 1.0, None, P,
                                 P, P, 1 << 40, None) == INV

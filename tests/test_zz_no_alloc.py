@@ -21,6 +21,7 @@ import torch
 from kda_gated_delta_03_gb300 import binding, build
 from kda_gated_delta_03_gb300 import inputs as I
 from kda_testutil import TOL, rel_frob, to_dev
+from oracle import oracle as O
 
 HAVE_NVCC = shutil.which("nvcc") is not None or os.path.exists("/usr/local/cuda/bin/nvcc")
 
@@ -34,6 +35,10 @@ def _device_inputs(inp):
 
 @pytest.mark.gpu
 def test_noalloc_matches_prefill_on_two_calls_in_a_row():
+    """Several sequences: the no-alloc call runs the same kernels as kda_prefill; only the home of the
+    longest-first sequence order differs.  So its results must be bit-identical, on two calls in a row with
+    different sequence counts (an order left stale by the first call would skip or repeat sequences), and
+    within tolerance of the float64 oracle."""
     build.build()
     binding.load()
     cases = [
@@ -56,9 +61,41 @@ def test_noalloc_matches_prefill_on_two_calls_in_a_row():
         o_ref, st_ref = binding.kda_prefill(d["q"], d["k"], d["v"], d["beta"], d["alpha"], d["cu_seqlens"],
                                             d["state_in"])
         torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16) if o.dtype == torch.bfloat16 else o,
+                           o_ref.view(torch.int16) if o_ref.dtype == torch.bfloat16 else o_ref)
+        assert torch.equal(st, st_ref)
+        o64, st64 = O.prefill(inp)
         tol = TOL[inp["dtype"]]
-        assert rel_frob(o.double().cpu().numpy(), o_ref.double().cpu().numpy()) <= tol
-        assert rel_frob(st.double().cpu().numpy(), st_ref.double().cpu().numpy()) <= tol
+        assert rel_frob(o.double().cpu().numpy(), o64) <= tol
+        assert rel_frob(st.double().cpu().numpy(), st64) <= tol
+    assert binding.kda_get_device_error() == 0
+
+
+@pytest.mark.gpu
+def test_noalloc_one_sequence_runs_the_single_kernel_path():
+    """One bf16 d=128 sequence: without a workspace for per-chunk records, the no-alloc call takes the
+    single-kernel chunkwise path.  It must equal kda_prefill_ex with single_kernel set, bit for bit, on two
+    calls in a row, and the float64 oracle within the bf16 tolerance."""
+    build.build()
+    binding.load()
+    inp = I.prefill_inputs([709], 3, 128, 128, "bf16", 73, decay="config", state="randn")
+    d = _device_inputs(inp)
+    T, H, dv = inp["v"].shape
+    o = torch.empty((T, H, dv), dtype=torch.bfloat16, device="cuda:0")
+    st = torch.empty((1, H, 128, dv), dtype=torch.float32, device="cuda:0")
+    o_ref, st_ref = binding.kda_prefill(d["q"], d["k"], d["v"], d["beta"], d["alpha"], d["cu_seqlens"],
+                                        d["state_in"], single_kernel=True)
+    for _ in range(2):
+        o.zero_()
+        st.zero_()
+        binding.kda_prefill_noalloc(d["q"], d["k"], d["v"], d["beta"], d["alpha"], d["cu_seqlens"], d["state_in"],
+                                    o=o, state_out=st)
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+        assert torch.equal(st, st_ref)
+    o64, st64 = O.prefill(inp)
+    assert rel_frob(o.double().cpu().numpy(), o64) <= TOL["bf16"]
+    assert rel_frob(st.double().cpu().numpy(), st64) <= TOL["bf16"]
     assert binding.kda_get_device_error() == 0
 
 
