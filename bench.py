@@ -4,9 +4,11 @@
 
 Default workload: the single-sequence prefill (B=1, H=32, T=8192, d_k=d_v=128, bf16 q/k/v, fp32
 gates and state).  One step is one kda_prefill call over that batch; `value` is prefill tokens/s
-with the inputs resident in HBM.  The same JSON line carries the batched decode workload
-(512 sequences x 32 heads of 128x128 fp32 state, 256 steps) as the `decode` object: steps/s and
-achieved state-HBM GB/s against the measured copy bandwidth.
+with the inputs resident in HBM.  The same JSON line carries the other workloads as objects, each with
+its roofline and the float64 oracle timed on a bounded sample beside it: `decode` (512 sequences x 32
+heads of 128x128 fp32 state, 256 steps: steps/s and achieved state-HBM GB/s against the measured copy
+bandwidth), `decode_bf16_state`, `varlen_64` (64 packed sequences), `append_1m` (both phases),
+`prefill_backward` and `prefill_gated_deltanet`.
 
 Other workloads (`--workload`): varlen_64 (64 packed sequences, ~291K tokens), append_1m (a
 1,032,192-token prefill followed by a 16,384-token append, H=8), decode_512x32.
@@ -53,6 +55,10 @@ def prefill_path(N, dtype, dk):
         return "prefill_2p", PREFILL_2P_SRC, PREFILL_2P_LABEL
     return "prefill_tc", PREFILL_TC_SRC, PREFILL_TC_LABEL
 METRIC = "KDA prefill tokens/s (H=32,d=128); decode steps/s and state HBM GB/s vs peak"
+# what the bf16 prefill computes in: bf16 q/k/v in HBM, tensor-core products on fp16 and TF32 operands with
+# fp32 accumulation, the state and every carried sum in fp32
+PREFILL_DTYPE = "bf16 in; fp16/tf32 tensor-core operands; fp32 accumulate and state"
+DECODE_DTYPE = "bf16 q/k/v; fp32 arithmetic and state"
 
 
 # ----------------------------------------------------------------------------
@@ -365,6 +371,49 @@ def cpu_threads():
     return max(1, os.cpu_count() or 1)
 
 
+def sub_sequences(inp, seqs):
+    """The inputs of a subset of the packed sequences (same values), for a bounded oracle sample."""
+    cu = inp["cu_seqlens"]
+    sub = dict(inp)
+    for key in ("q", "k", "v", "beta", "alpha"):
+        sub[key] = np.ascontiguousarray(np.concatenate([inp[key][cu[n]:cu[n + 1]] for n in seqs]))
+    sub["cu_seqlens"] = I.cu_seqlens_of([int(cu[n + 1] - cu[n]) for n in seqs])
+    if inp["state_in"] is not None:
+        sub["state_in"] = np.ascontiguousarray(inp["state_in"][list(seqs)])
+    return sub
+
+
+def oracle_varlen_baseline(inp, threads, min_tokens=16_000):
+    """The oracle on the first sequences of the packed batch whose lengths add up to at least min_tokens
+    (all heads), in tokens/s."""
+    cu = inp["cu_seqlens"]
+    seqs, tok = [], 0
+    for n in range(len(cu) - 1):
+        seqs.append(n)
+        tok += int(cu[n + 1] - cu[n])
+        if tok >= min_tokens:
+            break
+    secs = oracle_prefill_time(sub_sequences(inp, seqs), threads)
+    H = inp["v"].shape[1]
+    return {"value": round(tok / secs, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"the first {len(seqs)} of the {len(cu) - 1} sequences ({tok} tokens x {H} heads, "
+                      f"{tok / int(cu[-1]):.3f} of the workload), float64, {threads} threads"}
+
+
+def oracle_decode_baseline(w, threads, rows=64, steps=2):
+    """The oracle's decode step on `rows` of the batch's sequences (all heads), scaled to the full batch."""
+    from oracle import oracle as O
+    pool = I.random_state(rows, w["H"], w["dk"], w["dv"], (w["seed"], 0)).astype(np.float64)
+    sts = [I.decode_step_inputs(rows, w["H"], w["dk"], w["dv"], w["dtype"], w["seed"], s_) for s_ in range(steps)]
+    t0 = time.perf_counter()
+    for st in sts:
+        O.decode_step(st, pool, threads=threads)
+    per_step = (time.perf_counter() - t0) / steps * w["B"] / rows
+    return {"value": round(1.0 / per_step, 3), "unit": "steps/s", "cores": threads, "kind": "oracle",
+            "sample": f"{steps} steps of {rows} of the {w['B']} sequences x {w['H']} heads, scaled to the "
+                      f"full batch, float64, {threads} threads"}
+
+
 # ----------------------------------------------------------------------------
 # main
 # ----------------------------------------------------------------------------
@@ -382,6 +431,56 @@ def roofline_obj(alg_bytes, kernel_ms, peaks, kind, src, label, workload):
             "peak_source": peaks["source"]}
 
 
+def decode_object(wd, dev, peaks, world, state_dtype="f32"):
+    """The decode_512x32 workload (all 256 steps) as a sub-object of the default line."""
+    rd = gpu_decode(wd, wd["steps"], 3, dev, state_dtype=state_dtype)
+    dms = max_over_ranks(rd["ms_per_step"], world)
+    bf = state_dtype == "bf16"
+    roof = roofline_obj(rd["bytes_per_step"], rd["kernel_ms"], peaks, "decode_bf16" if bf else "decode",
+                        DECODE_BF16S_SRC if bf else DECODE_KERNEL_SRC, DECODE_BF16S_LABEL if bf else DECODE_LABEL,
+                        "decode_512x32_bf16_state" if bf else "decode_512x32")
+    return {"workload": "decode_512x32" + (", state stored in bf16" if bf else ""), "steps": wd["steps"],
+            "steps_per_s": round(world * 1e3 / dms, 2), "tokens_per_s": round(world * wd["B"] * 1e3 / dms, 1),
+            "ms_per_step": round(dms, 4), "state_hbm_gbs": roof["achieved"], "roofline": roof,
+            "dtype": DECODE_DTYPE if not bf else "bf16 q/k/v and state; fp32 arithmetic",
+            "gpu_launches": rd["launches"]}
+
+
+def varlen_object(dev, peaks, world, steps, warmup, with_oracle):
+    """The varlen_64 workload (64 packed sequences, about 291K tokens, random initial states)."""
+    w, inp = prefill_workload_inputs("varlen_64")
+    r = gpu_prefill(inp, steps, warmup, dev, 2)
+    ms = max_over_ranks(r["ms_per_step"], world)
+    e2e_ms = max_over_ranks(r["e2e_ms"], world)
+    alg = prefill_bytes(r["T"], r["H"], inp["dk"], inp["dv"], 2, r["N"], r["N"])
+    obj = {"workload": "varlen_64", "seqs": r["N"], "tokens": r["T"], "H": r["H"], "steps": steps,
+           "tokens_per_s": round(world * r["T"] * 1e3 / ms, 1), "ms_per_step": round(ms, 4),
+           "roofline": roofline_obj(alg, r["kernel_ms"], peaks, *prefill_path(r["N"], "bf16", inp["dk"]), "varlen_64"),
+           "e2e": {"value": round(world * r["T"] * 1e3 / e2e_ms, 1), "unit": "tokens/s",
+                   "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+           "gpu_launches": r["launches"]}
+    if with_oracle:
+        obj["cpu_baseline"] = oracle_varlen_baseline(inp, cpu_threads())
+    return obj
+
+
+def append_object(dev, peaks, world, steps, warmup, with_oracle):
+    """The append_1m workload: both phases (prefill and append), without the snapshot variant."""
+    w = I.workload("append_1m")
+    a = append_measure(w, steps, warmup, dev, peaks, world, snapshots=False)
+    obj = {"workload": "append_1m", "H": w["H"], "steps": steps,
+           "prefill": {"tokens": a["T1"], "tokens_per_s": round(world * a["T1"] * 1e3 / a["ms1"], 1),
+                       "ms_per_step": round(a["ms1"], 4), "roofline": a["roof1"],
+                       "e2e": {"value": round(world * a["T1"] * 1e3 / a["r1"]["e2e_ms"], 1), "unit": "tokens/s",
+                               "h2d_bytes_per_step": a["r1"]["h2d"], "d2h_bytes_per_step": a["r1"]["d2h"]}},
+           "append": {"tokens": a["T2"], "tokens_per_s": round(world * a["T2"] * 1e3 / a["ms2"], 1),
+                      "ms_per_step": round(a["ms2"], 4), "roofline": a["roof2"]},
+           "gpu_launches": a["r1"]["launches"] + a["r2"]["launches"]}
+    if with_oracle:
+        obj["cpu_baseline"] = oracle_append_baseline(a["prefix"], cpu_threads())
+    return obj
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import kda_gated_delta_03_gb300 as kda
@@ -392,6 +491,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     peaks = load_peaks()
     name = args.workload
+    oracle_here = rank == 0 and not args.no_cpu_baseline
     line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic"}
     if name in ("decode_512x32", "decode_512x32_bf16_state"):
@@ -403,7 +503,8 @@ def run_ours(args, rank, world, local_rank):
         ms = max_over_ranks(r["ms_per_step"], world)
         steps_s = world * 1e3 / ms
         line.update(metric="KDA decode steps/s (512 seqs x 32 heads, d=128)", value=round(steps_s, 2),
-                    unit="steps/s", ms_per_step=round(ms, 4), dtype="f32",
+                    unit="steps/s", ms_per_step=round(ms, 4),
+                    dtype=DECODE_DTYPE if sdt == "f32" else "bf16 q/k/v and state; fp32 arithmetic",
                     config={"workload": name, "B": w["B"], "H": w["H"], "d": w["dk"], "qkv": w["dtype"],
                             "state": "bf16" if sdt == "bf16" else "f32",
                             "l2": f"state pool ({'0.5' if sdt == 'bf16' else '1'} GiB) larger than L2"},
@@ -412,6 +513,8 @@ def run_ours(args, rank, world, local_rank):
                                           DECODE_BF16S_SRC if sdt == "bf16" else DECODE_KERNEL_SRC,
                                           DECODE_BF16S_LABEL if sdt == "bf16" else DECODE_LABEL, name),
                     gpu_launches=r["launches"], clocks=clk.summary())
+        if oracle_here:
+            line["cpu_baseline"] = oracle_decode_baseline(w, cpu_threads())
         return line
 
     if name == "append_1m":
@@ -425,33 +528,28 @@ def run_ours(args, rank, world, local_rank):
     tokens = r["T"]
     esize = 2 if inp["dtype"] == "bf16" else 4
     alg = prefill_bytes(tokens, r["H"], inp["dk"], inp["dv"], esize, 0 if inp["state_in"] is None else r["N"], r["N"])
-    line.update(value=round(world * tokens * 1e3 / ms, 1), unit="tokens/s", ms_per_step=round(ms, 4), dtype="f32",
+    line.update(value=round(world * tokens * 1e3 / ms, 1), unit="tokens/s", ms_per_step=round(ms, 4),
+                dtype=PREFILL_DTYPE if inp["dtype"] == "bf16" else "f32",
                 config={"workload": name, "seqs": r["N"], "tokens": tokens, "H": r["H"], "d": inp["dk"],
                         "qkv": inp["dtype"], "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{world}"},
                 roofline=roofline_obj(alg, r["kernel_ms"], peaks, *prefill_path(r["N"], inp["dtype"], inp["dk"]), name),
                 e2e={"value": round(world * tokens * 1e3 / e2e_ms, 1), "unit": "tokens/s",
                      "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
                 gpu_launches=r["launches"], clocks=clk.summary())
+    if name == "prefill_8k" and args.steady_steps > 0:
+        # the same call back to back over a longer region (inputs larger than L2), to show the number is steady
+        rs = gpu_prefill(inp, args.steady_steps, 3, dev, 1)
+        line["steady"] = {"steps": args.steady_steps, "ms_per_step": round(rs["ms_per_step"], 4),
+                          "timed_region_s": round(rs["total_ms"] / 1e3, 3),
+                          "tokens_per_s": round(tokens * 1e3 / rs["ms_per_step"], 1)}
     if name == "prefill_8k" and not args.no_decode:
         wd = I.workload("decode_512x32")
-        rd = gpu_decode(wd, wd["steps"], 3, dev)
-        dms = max_over_ranks(rd["ms_per_step"], world)
-        roof = roofline_obj(rd["bytes_per_step"], rd["kernel_ms"], peaks, "decode", DECODE_KERNEL_SRC, DECODE_LABEL,
-                            "decode_512x32")
-        line["decode"] = {"workload": "decode_512x32", "steps": wd["steps"], "steps_per_s": round(world * 1e3 / dms, 2),
-                          "tokens_per_s": round(world * wd["B"] * 1e3 / dms, 1), "ms_per_step": round(dms, 4),
-                          "state_hbm_gbs": roof["achieved"], "roofline": roof, "gpu_launches": rd["launches"]}
-        line["gpu_launches"] += rd["launches"]
-        rb = gpu_decode(wd, wd["steps"], 3, dev, state_dtype="bf16")
-        bms = max_over_ranks(rb["ms_per_step"], world)
-        roofb = roofline_obj(rb["bytes_per_step"], rb["kernel_ms"], peaks, "decode_bf16", DECODE_BF16S_SRC,
-                             DECODE_BF16S_LABEL, "decode_512x32_bf16_state")
-        line["decode_bf16_state"] = {"workload": "decode_512x32, state stored in bf16", "steps": wd["steps"],
-                                     "steps_per_s": round(world * 1e3 / bms, 2),
-                                     "tokens_per_s": round(world * wd["B"] * 1e3 / bms, 1),
-                                     "ms_per_step": round(bms, 4), "state_hbm_gbs": roofb["achieved"],
-                                     "roofline": roofb, "gpu_launches": rb["launches"]}
-        line["gpu_launches"] += rb["launches"]
+        line["decode"] = decode_object(wd, dev, peaks, world)
+        if oracle_here:
+            line["decode"]["cpu_baseline"] = oracle_decode_baseline(wd, cpu_threads())
+        line["gpu_launches"] += line["decode"]["gpu_launches"]
+        line["decode_bf16_state"] = decode_object(wd, dev, peaks, world, state_dtype="bf16")
+        line["gpu_launches"] += line["decode_bf16_state"]["gpu_launches"]
     if name == "prefill_8k" and not args.no_backward:
         # the backward pass of the same prefill (per-channel alpha)
         rw = gpu_backward(inp, 5, 3, dev)
@@ -477,17 +575,30 @@ def run_ours(args, rank, world, local_rank):
                                           "roofline": roofline_obj(algg, rg["kernel_ms"], peaks, "prefill_2p_gdn",
                                                                    PREFILL_2P_SRC, PREFILL_2P_LABEL, name + "_gdn"),
                                           "gpu_launches": rg["launches"]}
-    if rank == 0 and not args.no_cpu_baseline:
+    if oracle_here:
         threads = cpu_threads()
-        secs = oracle_prefill_time(inp, threads)
-        line["cpu_baseline"] = {"value": round(tokens / secs, 1), "unit": "tokens/s", "cores": threads,
-                                "kind": "oracle", "sample": f"the whole {name} workload once ({tokens} tokens x "
-                                                            f"{r['H']} heads), float64, {threads} threads"}
+        if name == "varlen_64":
+            line["cpu_baseline"] = oracle_varlen_baseline(inp, threads)
+        else:
+            secs = oracle_prefill_time(inp, threads)
+            line["cpu_baseline"] = {"value": round(tokens / secs, 1), "unit": "tokens/s", "cores": threads,
+                                    "kind": "oracle", "sample": f"the whole {name} workload once ({tokens} tokens x "
+                                                                f"{r['H']} heads), float64, {threads} threads"}
+    if name == "prefill_8k" and not args.no_varlen:
+        del inp
+        line["varlen_64"] = varlen_object(dev, peaks, world, args.sub_steps, 3, oracle_here)
+        line["gpu_launches"] += line["varlen_64"]["gpu_launches"]
+        torch.cuda.empty_cache()
+    if name == "prefill_8k" and not args.no_append:
+        line["append_1m"] = append_object(dev, peaks, world, args.sub_steps, 3, oracle_here)
+        line["gpu_launches"] += line["append_1m"]["gpu_launches"]
+        torch.cuda.empty_cache()
     return line
 
 
-def run_append(args, w, dev, peaks, line, world, local_rank):
-    import torch
+def append_measure(w, steps, warmup, dev, peaks, world, snapshots=True, e2e_steps=1):
+    """append_1m: the 1,032,192-token prefill from a zero state, then the 16,384-token append from the
+    carried state (timed from a state of the same shape), and optionally the prefill writing snapshots."""
     T1, T2 = w["seqlens"][0], w["append"]
     full = I.prefill_inputs([T1 + T2], w["H"], w["dk"], w["dv"], w["dtype"], w["seed"])
 
@@ -499,34 +610,63 @@ def run_append(args, w, dev, peaks, line, world, local_rank):
         return d
 
     p1 = part(0, T1)
-    barrier(world)
-    with ClockSampler(local_rank) as clk:
-        r1 = gpu_prefill(p1, args.steps, args.warmup, dev, 1)
+    r1 = gpu_prefill(p1, steps, warmup, dev, e2e_steps)
     p2 = part(T1, T1 + T2)
     p2["state_in"] = np.zeros((1, w["H"], w["dk"], w["dv"]), np.float32)
-    r2 = gpu_prefill(p2, args.steps, args.warmup, dev, 1)
-    every = 312 * 64                                  # restartable checkpoints about every 20,000 tokens
-    r3 = gpu_prefill(p1, args.steps, args.warmup, dev, 1, snapshot_every=every)
-    ms3 = max_over_ranks(r3["ms_per_step"], world)
+    r2 = gpu_prefill(p2, steps, warmup, dev, 1)
     ms1 = max_over_ranks(r1["ms_per_step"], world)
     ms2 = max_over_ranks(r2["ms_per_step"], world)
     alg1 = prefill_bytes(T1, w["H"], w["dk"], w["dv"], 2, 0, 1)
+    alg2 = prefill_bytes(T2, w["H"], w["dk"], w["dv"], 2, 1, 1)
+    out = {"T1": T1, "T2": T2, "r1": r1, "r2": r2, "ms1": ms1, "ms2": ms2,
+           "roof1": roofline_obj(alg1, r1["kernel_ms"], peaks, *prefill_path(1, "bf16", w["dk"]), "append_1m"),
+           "roof2": roofline_obj(alg2, r2["kernel_ms"], peaks, *prefill_path(1, "bf16", w["dk"]), "append_1m/append"),
+           "prefix": p1}
+    if snapshots:
+        every = 312 * 64                              # restartable checkpoints about every 20,000 tokens
+        r3 = gpu_prefill(p1, steps, warmup, dev, 1, snapshot_every=every)
+        ms3 = max_over_ranks(r3["ms_per_step"], world)
+        out["snapshots"] = {"every_tokens": every, "count": T1 // every,
+                            "bytes": (T1 // every) * w["H"] * w["dk"] * w["dv"] * 4,
+                            "tokens_per_s": round(world * T1 * 1e3 / ms3, 1), "ms_per_step": round(ms3, 4),
+                            "overhead": round(ms3 / ms1 - 1.0, 4), "gpu_launches": r3["launches"]}
+    return out
+
+
+def oracle_append_baseline(prefix, threads, tokens=16_384):
+    """The oracle on the first `tokens` tokens of the long sequence (all heads): the append phase's size.
+    The oracle's cost per token does not depend on the state it starts from."""
+    d = dict(prefix)
+    for k in ("q", "k", "v", "beta", "alpha"):
+        d[k] = prefix[k][:tokens]
+    d["cu_seqlens"] = I.cu_seqlens_of([tokens])
+    secs = oracle_prefill_time(d, threads)
+    H = prefix["v"].shape[1]
+    used = min(threads, H)
+    return {"value": round(tokens / secs, 1), "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"the first {tokens} tokens x {H} heads of the sequence (the append phase's size), "
+                      f"float64, {used} threads (one per head)"}
+
+
+def run_append(args, w, dev, peaks, line, world, local_rank):
+    barrier(world)
+    with ClockSampler(local_rank) as clk:
+        a = append_measure(w, args.steps, args.warmup, dev, peaks, world)
+    r1, r2 = a["r1"], a["r2"]
+    T1, T2 = a["T1"], a["T2"]
     line.update(metric="KDA append-prefill tokens/s (H=8, d=128): 1,032,192-token prefill",
-                value=round(world * T1 * 1e3 / ms1, 1), unit="tokens/s", ms_per_step=round(ms1, 4), dtype="f32",
+                value=round(world * T1 * 1e3 / a["ms1"], 1), unit="tokens/s", ms_per_step=round(a["ms1"], 4),
+                dtype=PREFILL_DTYPE,
                 config={"workload": "append_1m", "prefill_tokens": T1, "append_tokens": T2, "H": w["H"],
                         "d": w["dk"], "l2": "inputs larger than L2 (no flush)"},
-                roofline=roofline_obj(alg1, r1["kernel_ms"], peaks, *prefill_path(1, "bf16", w["dk"]), "append_1m"),
+                roofline=a["roof1"],
                 e2e={"value": round(world * T1 * 1e3 / r1["e2e_ms"], 1), "unit": "tokens/s",
                      "h2d_bytes_per_step": r1["h2d"], "d2h_bytes_per_step": r1["d2h"]},
-                append={"tokens_per_s": round(world * T2 * 1e3 / ms2, 1), "ms_per_step": round(ms2, 4),
-                        "roofline": roofline_obj(prefill_bytes(T2, w["H"], w["dk"], w["dv"], 2, 1, 1),
-                                                 r2["kernel_ms"], peaks, *prefill_path(1, "bf16", w["dk"]),
-                                                 "append_1m/append")},
-                snapshots={"every_tokens": every, "count": T1 // every,
-                           "bytes": (T1 // every) * w["H"] * w["dk"] * w["dv"] * 4,
-                           "tokens_per_s": round(world * T1 * 1e3 / ms3, 1), "ms_per_step": round(ms3, 4),
-                           "overhead": round(ms3 / ms1 - 1.0, 4), "gpu_launches": r3["launches"]},
-                gpu_launches=r1["launches"] + r2["launches"], clocks=clk.summary())
+                append={"tokens_per_s": round(world * T2 * 1e3 / a["ms2"], 1), "ms_per_step": round(a["ms2"], 4),
+                        "roofline": a["roof2"]},
+                snapshots=a["snapshots"], gpu_launches=r1["launches"] + r2["launches"], clocks=clk.summary())
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_append_baseline(a["prefix"], cpu_threads())
     return line
 
 
@@ -536,34 +676,49 @@ def run_reference(args, rank, world):
         return None
     name = args.workload
     threads = cpu_threads()
-    if name == "decode_512x32":
-        from oracle import oracle as O
-        w = I.workload(name)
-        rows = 16          # bounded sample: 16 of the 512 sequences (all 32 heads) per step
-        pool = I.random_state(rows, w["H"], w["dk"], w["dv"], (w["seed"], 0)).astype(np.float64)
-        st = I.decode_step_inputs(rows, w["H"], w["dk"], w["dv"], w["dtype"], w["seed"], 0)
+    if name.startswith("decode_512x32"):
+        w = I.workload("decode_512x32")
         times = []
         for i in range(args.warmup + args.steps):
             t0 = time.perf_counter()
-            O.decode_step(st, pool, threads=threads)
+            b = oracle_decode_baseline(w, threads, rows=16, steps=1)
             if i >= args.warmup:
                 times.append(time.perf_counter() - t0)
-        per_step = statistics.mean(times) * w["B"] / rows
-        value = 1.0 / per_step
-        unit, metric = "steps/s", "KDA decode steps/s (512 seqs x 32 heads, d=128)"
-        sample = f"{rows} of {w['B']} sequences x {w['H']} heads per step, scaled to the full batch"
-        ms = per_step * 1e3
+        value, unit = b["value"], "steps/s"
+        metric, sample = "KDA decode steps/s (512 seqs x 32 heads, d=128)", b["sample"]
+        ms = 1e3 / value
     else:
-        w, inp = prefill_workload_inputs("prefill_8k" if name == "append_1m" else name)
-        tokens = int(inp["cu_seqlens"][-1])
+        if name == "append_1m":
+            w = I.workload(name)
+            sample_inp = I.prefill_inputs([16_384], w["H"], w["dk"], w["dv"], w["dtype"], w["seed"])
+            sample = f"the first 16384 tokens x {w['H']} heads of the sequence (the append phase's size)"
+            metric = "KDA append-prefill tokens/s (H=8, d=128): 1,032,192-token prefill"
+        elif name == "varlen_64":
+            w, inp = prefill_workload_inputs(name)
+            cu = inp["cu_seqlens"]
+            seqs, tok = [], 0
+            for n in range(len(cu) - 1):
+                seqs.append(n)
+                tok += int(cu[n + 1] - cu[n])
+                if tok >= 16_000:
+                    break
+            sample_inp = sub_sequences(inp, seqs)
+            del inp
+            sample = f"the first {len(seqs)} of the 64 sequences ({tok} tokens x {w['H']} heads)"
+            metric = METRIC
+        else:
+            w, sample_inp = prefill_workload_inputs(name)
+            sample = f"the whole {name} workload ({int(sample_inp['cu_seqlens'][-1])} tokens x {w['H']} heads)"
+            metric = METRIC
+        tokens = int(sample_inp["cu_seqlens"][-1])
         times = []
         for i in range(args.warmup + args.steps):
-            s = oracle_prefill_time(inp, threads)
+            s_ = oracle_prefill_time(sample_inp, threads)
             if i >= args.warmup:
-                times.append(s)
+                times.append(s_)
         secs = statistics.mean(times)
-        value, unit, metric = tokens / secs, "tokens/s", METRIC
-        sample = f"the whole {w['kind']} workload ({tokens} tokens x {w['H']} heads) per step"
+        value, unit = tokens / secs, "tokens/s"
+        sample += " per step, float64"
         ms = secs * 1e3
     return {"impl": "reference", "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
@@ -588,6 +743,12 @@ def main(argv=None):
     ap.add_argument("--no-backward", action="store_true", help="skip the backward line of the prefill_8k run")
     ap.add_argument("--no-gdn", action="store_true", help="skip the Gated DeltaNet line of the prefill_8k run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-varlen", action="store_true", help="skip the varlen_64 object of the prefill_8k run")
+    ap.add_argument("--no-append", action="store_true", help="skip the append_1m object of the prefill_8k run")
+    ap.add_argument("--sub-steps", type=int, default=5,
+                    help="timed calls of the varlen_64 and append_1m objects of the prefill_8k run")
+    ap.add_argument("--steady-steps", type=int, default=1000,
+                    help="calls of the steadiness run of prefill_8k (0 = none)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

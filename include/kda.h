@@ -83,17 +83,19 @@ typedef enum {
 #define KDA_DEVERR_STATE_IDX 0x2u   /* decode state_idx entry outside [0, num_slots)          */
 #define KDA_DEVERR_TIMEOUT 0x4u     /* a bounded wait inside a kernel gave up (work abandoned) */
 #define KDA_DEVERR_SNAPSHOTS 0x8u   /* snapshot_offsets disagree with the sequence lengths       */
-#define KDA_DEVERR_RANGE 0x10u      /* one-sequence bf16 d=128 prefill: a state or folded chunk
-                                       value beyond fp16's range (|x| > 65504); results invalid */
+#define KDA_DEVERR_RANGE 0x10u      /* one-sequence bf16 d=128 prefill: a key-side chunk product
+                                       (Q', M, T' below) beyond fp16's range (|x| > 65504), which
+                                       needs keys far from unit norm; results invalid */
 
 /*
  * Bytes of device workspace kda_prefill needs for this problem (0 is a valid
  * answer).  Pure host function; never fails (returns 0 for invalid sizes).
  *  - Several sequences: the longest-first schedule, 4 bytes per sequence.
  *  - One bf16 sequence with d_k = d_v = 128: the per-chunk records of the
- *    two-phase path (98,816 bytes per chunk and head, up to 1 GiB of them).  kda_prefill also accepts less, down to the size
- *    returned for total_tokens = 64 (one chunk per window); it then walks the
- *    sequence in more windows, with identical results.
+ *    two-phase path (98,832 bytes per chunk and head, up to 1 GiB of them).
+ *    kda_prefill also accepts less, down to the size returned for
+ *    total_tokens = 64 (one chunk per window); it then walks the sequence in
+ *    more windows, with identical results.
  */
 KDA_API size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                                   int32_t d_v, kda_dtype dt);
@@ -161,9 +163,12 @@ KDA_API kda_status kda_prefill(const void* q, const void* k, const void* v, cons
  *
  * single_kernel (nonzero): one bf16 sequence with d_k = d_v = 128 runs the
  * single-kernel tensor-core path (TF32 / bf16 operands) instead of the
- * two-phase path, whose per-chunk records and state operand are fp16; use it
- * when that path reports KDA_DEVERR_RANGE (a state or folded chunk value beyond
- * 65,504).  Results agree to the same tolerance; the two-phase path is faster.
+ * two-phase path, whose per-chunk records and state operand are fp16.  The
+ * two-phase path keeps values and states of any magnitude inside fp16's range
+ * with exact power-of-two scales (per chunk for v, per chunk and slice for the
+ * state); only key-side products far outside O(1), which need keys far from
+ * unit norm, set KDA_DEVERR_RANGE, and this option is then the way out.  Results
+ * agree to the same tolerance; the two-phase path is faster.
  *   snapshot_every    tokens between snapshots: 0, or a positive multiple of 64
  *   snapshots         [snapshot_offsets[num_seqs], H, d_k, d_v] float32 device
  *                     buffer, 16-byte aligned

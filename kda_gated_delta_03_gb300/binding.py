@@ -75,7 +75,8 @@ _LIB = None
 
 
 def lib_path() -> str:
-    return _build.LIB
+    """The in-tree libkda, or the library named by the KDA_LIBRARY environment variable."""
+    return os.environ.get("KDA_LIBRARY") or _build.LIB
 
 
 def load():

@@ -67,7 +67,17 @@ kda_status noalloc_scratch(int32_t** out) {
     return KDA_OK;
 }
 
+#ifdef KDA_TEST_HOOKS
+int32_t g_test_stall = 0;   // test builds only: set by kda_test_stall_prefill
+#endif
+
 }  // namespace
+
+#ifdef KDA_TEST_HOOKS
+// Test builds only (-DKDA_TEST_HOOKS; not in kda.h): while `on` is nonzero, the tcgen05 prefill kernels of
+// later kda_prefill calls give up a bounded wait on purpose, so that a test can check the give-up path.
+extern "C" KDA_API void kda_test_stall_prefill(int32_t on) { g_test_stall = on; }
+#endif
 
 extern "C" {
 
@@ -173,6 +183,9 @@ kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const flo
     p.state_in = state_in; p.state_out = state_out; p.o = o;
     p.err = err;
     p.alpha_mode = alpha_mode;
+#ifdef KDA_TEST_HOOKS
+    p.test_stall = g_test_stall;
+#endif
     p.snap_every = snap_every;
     p.snapshots = snap_every > 0 ? options->snapshots : nullptr;
     p.snap_offsets = snap_every > 0 ? options->snapshot_offsets : nullptr;

@@ -38,6 +38,9 @@ struct PrefillParams {
     int32_t snap_every;          // tokens (a multiple of kChunk), 0 = none
     float* snapshots;            // [snap_offsets[num_seqs], H, dk, dv]
     const int32_t* snap_offsets; // device [num_seqs + 1]
+#ifdef KDA_TEST_HOOKS
+    int32_t test_stall;          // test builds only: make the tcgen05 prefill kernels' bounded waits give up
+#endif
 };
 
 struct DecodeParams {

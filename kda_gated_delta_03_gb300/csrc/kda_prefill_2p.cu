@@ -32,11 +32,39 @@ constexpr int REC_QM = 0;          // [Q'; M]: 192 x 128 fp16 K-major operand (4
 constexpr int REC_B = 49152;       // B = Khat^T Utilde: fp16 [32 column quads][128 rows][4] (32 KiB)
 constexpr int REC_O = 81920;       // P Utilde: fp16 [32 column quads][64 rows][4] (16 KiB)
 constexpr int REC_G = 98304;       // Gamma_C: fp32 [128]
-constexpr int REC_BYTES = 98816;
+constexpr int REC_E = 98816;       // e_c: int32, B and P Utilde are stored divided by 2^e_c (then 12 bytes of pad)
+constexpr int REC_BYTES = 98832;
 constexpr int QM_BYTES = (C + DK) * DK * 2;
 // Q', M, B, P Utilde and the chain's state operand are fp16: the same 10-bit significand as TF32, in half
 // the bytes, for values within fp16's range, which the kernels check (KDA_DEVERR_RANGE)
 constexpr float kF16Max = 65504.f;
+// Magnitudes are kept inside that range by powers of two.  A chunk whose largest |v| is at least 2^6 stores
+// its value-side products (Utilde, B, P Utilde) divided by 2^e_c, e_c = the exponent of that largest |v|.
+// The chain carries its state divided by 2^E: E is chosen before each chunk's state operand is written,
+// as the larger of the chunk's e_c and the exponent of the largest |state| at the previous chunk (all
+// state warps' maxima, exchanged in shared memory off the sequential path), so that neither large values
+// nor large states leave fp16's range, and a state that shrinks again returns to a small E.  Key-side
+// products (Q', M, T') stay O(1) for unit-norm keys and are still checked.  Powers of two are exact: with
+// every |v| and |state| below 2^6 nothing is scaled.
+constexpr uint32_t kScaleFromBf16 = 0x4280u;   // bf16 bits of 2^6
+constexpr int kScaleFromExp = 6;
+
+// 2^n as a float for n in [-126, 127] (exact)
+__device__ __forceinline__ float exp2i(int n) { return __int_as_float((n + 127) << 23); }
+// the scale exponent of a magnitude given as bf16 bits (0 below 2^8, at most 126)
+__device__ __forceinline__ int scale_exp_bf16(uint32_t mag_bits) {
+    return mag_bits >= kScaleFromBf16 ? min((int)((mag_bits >> 7) & 0xFFu) - 127, 126) : 0;
+}
+// the same for a magnitude given as fp32 bits
+__device__ __forceinline__ int scale_exp_f32(uint32_t mag_bits) {
+    return mag_bits >= (kScaleFromBf16 << 16) ? min((int)((mag_bits >> 23) & 0xFFu) - 127, 126) : 0;
+}
+// the same for a magnitude given as fp32 bits of the value divided by 2^E
+__device__ __forceinline__ int scale_exp_f32_at(uint32_t mag_bits, int E) {
+    if (mag_bits < 0x00800000u) return 0;          // zero or denormal: far below 2^6 for any E <= 126
+    const int e = (int)((mag_bits >> 23) & 0xFFu) - 127 + E;
+    return e >= kScaleFromExp ? min(e, 126) : 0;
+}
 constexpr int SNV = 32;            // value columns per chain CTA
 constexpr int SLICES = DK / SNV;
 constexpr size_t kBufBudget = size_t(128) << 20;      // record bytes per buffer of the overlapped schedule
@@ -51,22 +79,31 @@ constexpr int P_OFF_V = OFF_V;                     // v tile, dense 64 x 128 bf1
 constexpr int P_OFF_BETA = OFF_V + C * DK * 2;     // 81920
 constexpr int P_OFF_MISC = P_OFF_BETA + 256;
 constexpr int P_OFF_ASC = P_OFF_MISC + 64 + DK * 4;         // per-head alpha of the unit's rows (256 B)
-constexpr int P_OFF_S = align1k(P_OFF_ASC + 256);           // scratch, 144 KiB
+constexpr int P_OFF_VMX = P_OFF_ASC + 256;                  // per-warp largest |v| of the unit (8 x u32)
+constexpr int P_OFF_S = align1k(P_OFF_VMX + 32);            // scratch, 144 KiB
 // scratch sub-regions (offsets from P_OFF_S)
 constexpr int PS_A = 0, PS_T = C * AT_LD * 4, PS_SCR = 2 * C * AT_LD * 4;   // solve tiles
 constexpr int PS_OPT = 38912, PS_KV = PS_OPT + 16384;                     // T' and [Gamma.K | V]^T (N = 256)
 constexpr int PS_P = 122880;                                               // P operand
-constexpr int PS_WU = 0, PS_KH = 65536;                                    // fold operands, after [W | Utilde]
+constexpr int PS_WU = 0, PS_KH = 131072;            // fold operands: [W | Utilde]^T after step 4, Khat^T (built
+                                                     // during step 4, after the P operand)
+constexpr int ONE_L_OFF = C * DK * 4;                                     // one-reference A/P: R, then L
+constexpr float kOneRefMax = 125.f;                                        // log2 of the largest factor
 constexpr int P_SMEM = P_OFF_S + G1_BYTES;
 static_assert(PS_KV + (DK + DK) * 256 <= PS_P && PS_P + 16384 <= G1_BYTES, "phase-1 scratch");
-static_assert(PS_KH + DK * C * 4 <= PS_P, "phase-1 fold operands");
+static_assert(PS_WU + 2 * DK * C * 2 <= PS_OPT && PS_P + C * C * 2 <= PS_KH && PS_KH + DK * C * 2 <= G1_BYTES,
+              "phase-1 fold operands");
 static_assert(P_SMEM <= 232448, "phase-1 shared memory");
 
 // ---- phase 2 shared memory and threads ----
 constexpr int SOP_BYTES = SNV * DK * 2;            // S^T operand: fp16 32 x 128, 128-byte swizzle
 constexpr int C_OFF_S = 2 * QM_BYTES;              // two record buffers, then two S^T operands
 constexpr int C_OFF_MISC = C_OFF_S + 2 * SOP_BYTES;
-constexpr int C_SMEM = C_OFF_MISC + 128;
+// misc: 0 lbar[2], 16 dbar[2], 32 obar[2], 48 sbar, 64 ofree[2], 96 TMEM address, 100 abort flag,
+// 104 test barrier, 128 per-warp largest |state_in| (8 x u32), 160 ebar[4], 192 E of chunk c (ring of 4),
+// 208 per-warp largest |S_c| / 2^E at the operand of chunk c (2 x 8 x u32)
+constexpr int CM_SMX0 = 128, CM_EBAR = 160, CM_ERING = 192, CM_SLOT = 208;
+constexpr int C_SMEM = C_OFF_MISC + 272;
 constexpr int C_NT = NT + 6 * 32;                  // 8 state warps, the MMA-issue warp, the record-loader warp,
                                                    // 2 idle warps, 2 output warps (on TMEM lanes 0..63)
 static_assert(C_OFF_S % 1024 == 0 && C_SMEM <= 232448, "phase-2 shared memory");
@@ -75,10 +112,6 @@ struct PrepMaps {
     CUtensorMap k, q, a, v;   // v with a 128-column box
 };
 
-__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
-}
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(mbar)
@@ -274,9 +307,23 @@ __global__ void __launch_bounds__(NT, 1)
             if (per_head) alpha_next = p.alpha[row];
         }
     }
+#ifdef KDA_TEST_HOOKS
+    if (p.test_stall) {                              // the first copies are in flight: give up a wait now
+        if (tid == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(sm + P_OFF_MISC + 32)) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+        if (!test_stall_wait(saddr(sm + P_OFF_MISC + 32))) {
+            atomicOr(p.err, KDA_DEVERR_TIMEOUT);
+            *s_abort = 1;
+        }
+        __syncthreads();
+    }
+#endif
 
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const int h = u % H, cw = u / H;
+        const int cw = u / H;
         const int32_t t0 = (int32_t)(c_begin + cw) * C;
         const int L = min(C, p.total_tokens - t0);
         unsigned char* rec = records + (size_t)u * REC_BYTES;
@@ -306,7 +353,20 @@ __global__ void __launch_bounds__(NT, 1)
             __syncthreads();
         }
 
-        // ---- 1. g = running sum of clamped log2 alpha per key channel ----
+        // ---- 1. g = running sum of clamped log2 alpha per key channel; the largest |v| of the chunk ----
+        {
+            const uint4* vv = reinterpret_cast<const uint4*>(sm + P_OFF_V) + tid;   // 16 B per thread per step
+            uint32_t vm = 0u;                           // largest bf16 magnitude bits of this thread's 32 values
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const uint4 w = vv[x * NT];
+                const uint32_t a = w.x & 0x7FFF7FFFu, b = w.y & 0x7FFF7FFFu, c = w.z & 0x7FFF7FFFu, d = w.w & 0x7FFF7FFFu;
+                vm = max(vm, max(max(a >> 16, a & 0xFFFFu), max(b >> 16, b & 0xFFFFu)));
+                vm = max(vm, max(max(c >> 16, c & 0xFFFFu), max(d >> 16, d & 0xFFFFu)));
+            }
+            vm = __reduce_max_sync(0xffffffffu, vm);
+            if (lane == 0) reinterpret_cast<uint32_t*>(sm + P_OFF_VMX)[warp] = vm;
+        }
         {
             float la[32];
 #pragma unroll
@@ -329,13 +389,64 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         __syncthreads();
+        int ec;                                         // this chunk's value scale exponent
+        {
+            const uint4 m0 = *reinterpret_cast<const uint4*>(sm + P_OFF_VMX);
+            const uint4 m1 = *reinterpret_cast<const uint4*>(sm + P_OFF_VMX + 16);
+            ec = scale_exp_bf16(max(max(max(m0.x, m0.y), max(m0.z, m0.w)), max(max(m1.x, m1.y), max(m1.z, m1.w))));
+        }
+        const float vscale = exp2i(-ec);
+        // One decay reference for the whole chunk (row 31) keeps every factor of step 2 inside float range when
+        // each channel decays by at most 2^kOneRefMax over rows 0..31 and over rows 31..63; then A and P are one
+        // product (16 tcgen05 instructions instead of 64).  Otherwise (strong decay) each 16-row block takes its
+        // own reference.
+        const bool one_ref = !__syncthreads_or(
+            (rh == 0 ? Gat(0, ch) - Gat(31, ch) : Gat(31, ch) - Gat(C - 1, ch)) > kOneRefMax);
 
-        // ---- 2. A and P: per 16-row block b, R_b [Lk_b; Lq_b]^T on tcgen05 (M=64, N=32, K=128) ----
+        // ---- 2. A and P on tcgen05 ----
         float* Ab = reinterpret_cast<float*>(X + PS_A);
         float* Tb = reinterpret_cast<float*>(X + PS_T);
         float* scr = reinterpret_cast<float*>(X + PS_SCR);
         unsigned char* opP = X + PS_P;
-        {
+        if (one_ref) {
+            // R = (2^(g_31 - g) . K) (M=64 rows s) and L = [2^(g - g_31) . K; 2^(g - g_31) . Q] (N=128 rows r), TF32,
+            // K=128 channels: D[s][r] = A-part (r < 64) and P-part (r >= 64) of the whole chunk
+            const int cq = 4 * warp + (lane >> 3), j = lane & 7, i0 = 4 * cq;
+            const float4 ref = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(31, i0));
+#pragma unroll
+            for (int gi = 0; gi < 8; ++gi) {
+                const int fr = 8 * gi + j;
+                const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(fr, i0));
+                const uint2 kk = *reinterpret_cast<const uint2*>(sm + OFF_K + kq_off(fr, i0));
+                const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(fr, i0));
+                const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kk);
+                const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
+                const float kx = __low2float(k2[0]), ky = __high2float(k2[0]), kz = __low2float(k2[1]),
+                            kw = __high2float(k2[1]);
+                const float fx = ex2f(gg.x - ref.x), fy = ex2f(gg.y - ref.y), fz = ex2f(gg.z - ref.z),
+                            fw = ex2f(gg.w - ref.w);
+                *reinterpret_cast<float4*>(X + op_off(fr, i0, DK)) =
+                    make_float4(tf32r(kx * ex2f(ref.x - gg.x)), tf32r(ky * ex2f(ref.y - gg.y)),
+                                tf32r(kz * ex2f(ref.z - gg.z)), tf32r(kw * ex2f(ref.w - gg.w)));
+                *reinterpret_cast<float4*>(X + ONE_L_OFF + op_off(fr, i0, DK)) =
+                    make_float4(tf32r(kx * fx), tf32r(ky * fy), tf32r(kz * fz), tf32r(kw * fw));
+                *reinterpret_cast<float4*>(X + ONE_L_OFF + op_off(C + fr, i0, DK)) =
+                    make_float4(tf32r(__low2float(q2[0]) * fx), tf32r(__high2float(q2[0]) * fy),
+                                tf32r(__low2float(q2[1]) * fz), tf32r(__high2float(q2[1]) * fw));
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (warp == 0 && elect_one()) {
+                tc_fence_after();
+                constexpr uint32_t id = idesc_tf32(64, 2 * C);
+                const uint64_t ad = op_desc(saddr(X), DK), bd = op_desc(saddr(X + ONE_L_OFF), DK);
+#pragma unroll
+                for (int ks = 0; ks < DK / 8; ++ks)
+                    umma_tf32_1(tmem + TM_W, ad + (uint64_t)(ks * 16), bd + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
+                umma_commit(mbar);
+            }
+        } else {
             const int cq = 4 * warp + (lane >> 3), j = lane & 7, i0 = 4 * cq;
             float4 rv[8];
             float4 refp = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -377,27 +488,27 @@ __global__ void __launch_bounds__(NT, 1)
                     *reinterpret_cast<float4*>(rb + op_off(8 * gi + j, i0, DK)) =
                         make_float4(tf32r(rv[gi].x), tf32r(rv[gi].y), tf32r(rv[gi].z), tf32r(rv[gi].w));
             }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0 && elect_one()) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc_tf32(64, 32);
-            uint64_t ad[4], bdsc[4];
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (warp == 0 && elect_one()) {             // per 16-row block b: R_b [Lk_b; Lq_b]^T, M=64, N=32
+                tc_fence_after();
+                constexpr uint32_t id = idesc_tf32(64, 32);
+                uint64_t ad[4], bdsc[4];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                ad[b] = op_desc(saddr(X + g1_r_off(b)), DK);
-                bdsc[b] = op_desc(saddr(X + G1_L_OFF + b * 16384), DK);
+                for (int b = 0; b < 4; ++b) {
+                    ad[b] = op_desc(saddr(X + g1_r_off(b)), DK);
+                    bdsc[b] = op_desc(saddr(X + G1_L_OFF + b * 16384), DK);
+                }
+#pragma unroll
+                for (int ks = 0; ks < DK / 8; ++ks) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        umma_tf32_1(tmem + TM_W + 32 * b, ad[b] + (uint64_t)(ks * 16), bdsc[b] + (uint64_t)(ks * 16),
+                                    id, ks > 0 ? 1u : 0u);
+                }
+                umma_commit(mbar);
             }
-#pragma unroll
-            for (int ks = 0; ks < DK / 8; ++ks) {
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-                    umma_tf32_1(tmem + TM_W + 32 * b, ad[b] + (uint64_t)(ks * 16), bdsc[b] + (uint64_t)(ks * 16), id,
-                                ks > 0 ? 1u : 0u);
-            }
-            umma_commit(mbar);
         }
         drain(0);                                       // while the products run
         drain(1);
@@ -408,7 +519,12 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int bb = 0; bb < 2; ++bb) {
                 const int b = 2 * half + bb;
-                tmem_ld32(tmem + tlane + TM_W + 32 * b, v);
+                if (one_ref) {                          // A-part columns r, P-part columns 64 + r
+                    tmem_ld16(tmem + tlane + TM_W + 16 * b, v);
+                    tmem_ld16(tmem + tlane + TM_W + C + 16 * b, v + 16);
+                } else {
+                    tmem_ld32(tmem + tlane + TM_W + 32 * b, v);
+                }
                 if (lane < 16) {
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
@@ -422,8 +538,24 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_before();
         __syncthreads();
 
-        // ---- 3. T = (I + A)^-1 by 16x16 blocks ----
-        if (tid < 64) {
+        // ---- 3. T = (I + A)^-1 by 16x16 blocks; while warps 0-1 invert the diagonal blocks, warps 2-7 build
+        //         the [Gamma.K | V]^T operand of step 4 (fp16, N=256 rows, K=64 time), which needs no T ----
+        if (tid >= 64) {
+            for (int e = tid - 64; e < DK * 16; e += NT - 64) {
+                const int i = e & (DK - 1), m0 = 4 * (e >> 7);
+                float gg[4], kk4[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) { gg[x] = Gat(m0 + x, i); kk4[x] = kat(m0 + x, i); }
+                *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(i, m0, C)) =
+                    make_uint2(pack_half2(ex2f(gg[0]) * kk4[0], ex2f(gg[1]) * kk4[1]),
+                               pack_half2(ex2f(gg[2]) * kk4[2], ex2f(gg[3]) * kk4[3]));
+                const float v0 = vscale * bf(vraw + (m0 + 0) * DK + i), v1 = vscale * bf(vraw + (m0 + 1) * DK + i);
+                const float v2 = vscale * bf(vraw + (m0 + 2) * DK + i), v3 = vscale * bf(vraw + (m0 + 3) * DK + i);
+                big |= fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))) > kF16Max;
+                *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(DK + i, m0, C)) =
+                    make_uint2(pack_half2(v0, v1), pack_half2(v2, v3));
+            }
+        } else {
             const int b = tid >> 4, c = tid & 15;
             float tc[16];
 #pragma unroll
@@ -495,20 +627,6 @@ __global__ void __launch_bounds__(NT, 1)
             *reinterpret_cast<uint2*>(X + PS_OPT + op_off_h(r, m0, C)) =
                 make_uint2(pack_half2(v.x, v.y), pack_half2(v.z, v.w));
         }
-        // [Gamma.K | V]^T -> fp16 operand (N=256 rows, K=64 time)
-        for (int e = tid; e < DK * 16; e += NT) {
-            const int i = e & (DK - 1), m0 = 4 * (e >> 7);
-            float gg[4], kk4[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) { gg[x] = Gat(m0 + x, i); kk4[x] = kat(m0 + x, i); }
-            *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(i, m0, C)) =
-                make_uint2(pack_half2(ex2f(gg[0]) * kk4[0], ex2f(gg[1]) * kk4[1]),
-                           pack_half2(ex2f(gg[2]) * kk4[2], ex2f(gg[3]) * kk4[3]));
-            const float v0 = bf(vraw + (m0 + 0) * DK + i), v1 = bf(vraw + (m0 + 1) * DK + i);
-            const float v2 = bf(vraw + (m0 + 2) * DK + i), v3 = bf(vraw + (m0 + 3) * DK + i);
-            big |= fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))) > kF16Max;
-            *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(DK + i, m0, C)) = make_uint2(pack_half2(v0, v1), pack_half2(v2, v3));
-        }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -533,11 +651,21 @@ __global__ void __launch_bounds__(NT, 1)
         }
         drain(2);                                       // while the products run
         drain(3);
-        if (!wait_mma()) break;
-
-        // ---- 5. fold operands: [W | Utilde]^T (N=256, K=64) and Khat^T (M=128, K=64) ----
         unsigned char* opWU = X + PS_WU;
         unsigned char* opKH = X + PS_KH;
+        for (int e = tid; e < DK * 16; e += NT) {       // Khat^T = ((Gamma_C / Gamma) . K)^T, fp16 (M=128, K=64)
+            const int i = e & (DK - 1), s0 = 4 * (e >> 7);
+            const float gl = Gat(C - 1, i);
+            float gg[4], kk4[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) { gg[x] = Gat(s0 + x, i); kk4[x] = kat(s0 + x, i); }
+            *reinterpret_cast<uint2*>(opKH + op_off_h(i, s0, C)) =
+                make_uint2(pack_half2(ex2f(gl - gg[0]) * kk4[0], ex2f(gl - gg[1]) * kk4[1]),
+                           pack_half2(ex2f(gl - gg[2]) * kk4[2], ex2f(gl - gg[3]) * kk4[3]));
+        }
+        if (!wait_mma()) break;
+
+        // ---- 5. fold operand [W | Utilde]^T (N=256, K=64) ----
         {
             const int n = DK * half + 32 * quad + lane;          // row of [W | Utilde]^T held by this lane
             float v[32];
@@ -551,16 +679,6 @@ __global__ void __launch_bounds__(NT, 1)
                         make_uint2(pack_half2(v[x], v[x + 1]), pack_half2(v[x + 2], v[x + 3]));
                 }
             }
-        }
-        for (int e = tid; e < DK * 16; e += NT) {
-            const int i = e & (DK - 1), s0 = 4 * (e >> 7);
-            const float gl = Gat(C - 1, i);
-            float gg[4], kk4[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) { gg[x] = Gat(s0 + x, i); kk4[x] = kat(s0 + x, i); }
-            *reinterpret_cast<uint2*>(opKH + op_off_h(i, s0, C)) =
-                make_uint2(pack_half2(ex2f(gl - gg[0]) * kk4[0], ex2f(gl - gg[1]) * kk4[1]),
-                           pack_half2(ex2f(gl - gg[2]) * kk4[2], ex2f(gl - gg[3]) * kk4[3]));
         }
         drain(4);                                       // the last piece, before step 6 writes its columns
         rec_prev = nullptr;
@@ -613,6 +731,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         if (tid < DK) reinterpret_cast<float*>(rec + REC_G)[tid] = sgam[tid];
+        if (tid == 0) *reinterpret_cast<int*>(rec + REC_E) = ec;
         rec_prev = rec;
         fence_async_smem();
         tc_fence_before();
@@ -688,6 +807,10 @@ __global__ void __launch_bounds__(C_NT, 1)
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + 96);
     const uint32_t lbar = saddr(misc), dbar = saddr(misc + 16), obar = saddr(misc + 32), sbar = saddr(misc + 48);
     const uint32_t ofree = saddr(misc + 64);
+    // ebar[c & 3]: E of chunk c's state operand is in E_ring[c & 3] (one arrival, by state warp 0)
+    const uint32_t ebar = saddr(misc + CM_EBAR);
+    volatile int* e_ring = reinterpret_cast<volatile int*>(misc + CM_ERING);
+    volatile uint32_t* smax = reinterpret_cast<volatile uint32_t*>(misc + CM_SLOT);
     constexpr uint32_t TM_S = 0, TM_O = 32;           // M S accumulator; two [Q'; M_top] S accumulators
 
     if (tid == 0) {
@@ -699,6 +822,8 @@ __global__ void __launch_bounds__(C_NT, 1)
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sbar), "r"(NT) : "memory");
         for (int b = 0; b < 2; ++b)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(ofree + 8 * b), "r"(64) : "memory");
+        for (int b = 0; b < 4; ++b)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(ebar + 8 * b) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *s_abort = 0;
     }
@@ -707,14 +832,52 @@ __global__ void __launch_bounds__(C_NT, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // the state scale exponent E_0 of this slice's state_in (the state warps' rows, read once here)
+    uint32_t* s_smx = reinterpret_cast<uint32_t*>(misc + CM_SMX0);
+    if (warp < 8) {
+        uint32_t m = 0u;
+        if (state_in) {
+            const float* src = state_in + (((int64_t)h) * DK + 32 * quad + lane) * (int64_t)p.dv + j0 + (SNV / 2) * half;
+#pragma unroll
+            for (int j = 0; j < SNV / 2; j += 4) {
+                const float4 v4 = *reinterpret_cast<const float4*>(src + j);
+                m = max(m, max(max(__float_as_uint(fabsf(v4.x)), __float_as_uint(fabsf(v4.y))),
+                               max(__float_as_uint(fabsf(v4.z)), __float_as_uint(fabsf(v4.w)))));
+            }
+        }
+        m = __reduce_max_sync(0xffffffffu, m);
+        if (lane == 0) s_smx[warp] = m;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    int E0;                                           // every thread: the state is carried divided by 2^E
+    {
+        uint32_t m = 0u;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) m = max(m, s_smx[w]);
+        E0 = scale_exp_f32(m);
+    }
+    if (tid == 0) {                                   // chunk 0's state operand is at scale E_0
+        e_ring[0] = E0;
+        mbar_arrive(ebar);
+    }
     auto fail = [&]() {
         atomicOr(p.err, KDA_DEVERR_TIMEOUT);
         *s_abort = 1;
     };
+#ifdef KDA_TEST_HOOKS
+    if (p.test_stall) {                              // give up a wait before the roles start
+        if (tid == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(misc + 104)) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+        if (!test_stall_wait(saddr(misc + 104))) fail();
+        __syncthreads();
+    }
+#endif
 
     const uint32_t sop0 = saddr(sm + C_OFF_S);
     if (warp == 8) {
@@ -779,17 +942,21 @@ __global__ void __launch_bounds__(C_NT, 1)
         const int orow = 32 * (warp - 12) + lane;
         const uint32_t tlane = (uint32_t)(32 * (warp - 12)) << 16;
         uint2 oq[SNV / 4];                             // raw fp16, converted where used
+        int eo = 0;                                    // the chunk's value scale exponent
         auto fetch_o = [&](int ci) {                  // the chunk's P Utilde for this row and slice
             const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
 #pragma unroll
             for (int m = 0; m < SNV / 4; ++m)
                 oq[m] = __ldg(reinterpret_cast<const uint2*>(rec + REC_O + (((j0 + 4 * m) >> 2) * C + orow) * 8));
+            eo = __ldg(reinterpret_cast<const int*>(rec + REC_E));
         };
         if (n_chunks > 0) fetch_o(0);
         for (int ci = 0; ci < n_chunks; ++ci) {
             const int b = ci & 1;
             if (*s_abort) break;
             if (!mbar_wait(obar + 8 * b, (uint32_t)(ci >> 1) & 1u)) { fail(); break; }
+            if (!mbar_wait(ebar + 8 * (ci & 3), (uint32_t)(ci >> 2) & 1u)) { fail(); break; }
+            const int E = e_ring[ci & 3];               // the scale of the chunk's state operand
             tc_fence_after();
             float d[SNV];
             tmem_ld32(tmem + tlane + TM_O + SNV * b, d);
@@ -798,14 +965,15 @@ __global__ void __launch_bounds__(C_NT, 1)
             const int32_t t0 = (c_begin + ci) * C;
             if (orow < min(C, T - t0)) {
                 __nv_bfloat16* dst = go + ((int64_t)(t0 + orow) * H + h) * p.dv + j0;
+                const float fd = exp2i(E), fo = exp2i(eo);      // 1 unless values or the state are large
 #pragma unroll
                 for (int x = 0; x < SNV; x += 8) {
                     const float4 o0 = half4_to_float4(oq[x / 4]), o1 = half4_to_float4(oq[x / 4 + 1]);
-                    *reinterpret_cast<uint4*>(dst + x) =
-                        make_uint4(pack_bf16x2(p.scale * (d[x] + o0.x), p.scale * (d[x + 1] + o0.y)),
-                                   pack_bf16x2(p.scale * (d[x + 2] + o0.z), p.scale * (d[x + 3] + o0.w)),
-                                   pack_bf16x2(p.scale * (d[x + 4] + o1.x), p.scale * (d[x + 5] + o1.y)),
-                                   pack_bf16x2(p.scale * (d[x + 6] + o1.z), p.scale * (d[x + 7] + o1.w)));
+                    *reinterpret_cast<uint4*>(dst + x) = make_uint4(
+                        pack_bf16x2(p.scale * (fd * d[x] + fo * o0.x), p.scale * (fd * d[x + 1] + fo * o0.y)),
+                        pack_bf16x2(p.scale * (fd * d[x + 2] + fo * o0.z), p.scale * (fd * d[x + 3] + fo * o0.w)),
+                        pack_bf16x2(p.scale * (fd * d[x + 4] + fo * o1.x), p.scale * (fd * d[x + 5] + fo * o1.y)),
+                        pack_bf16x2(p.scale * (fd * d[x + 6] + fo * o1.z), p.scale * (fd * d[x + 7] + fo * o1.w)));
                 }
             }
             if (ci + 1 < n_chunks) fetch_o(ci + 1);
@@ -816,37 +984,59 @@ __global__ void __launch_bounds__(C_NT, 1)
         const int srow = 32 * quad + lane;            // state row (key channel)
         const int jc = j0 + CPT * half;               // first value column of this thread
         const int64_t state_off = (((int64_t)h) * DK + srow) * (int64_t)p.dv + jc;
-        float S[CPT];
+        float S[CPT];                                 // the state divided by 2^E
+        int E = E0;
+        {
+            const float f = exp2i(-E0);
 #pragma unroll
-        for (int j = 0; j < CPT; j += 4) {
-            const float4 v4 = state_in ? *reinterpret_cast<const float4*>(state_in + state_off + j)
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-            S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
+            for (int j = 0; j < CPT; j += 4) {
+                const float4 v4 = state_in ? *reinterpret_cast<const float4*>(state_in + state_off + j)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                S[j] = f * v4.x; S[j + 1] = f * v4.y; S[j + 2] = f * v4.z; S[j + 3] = f * v4.w;
+            }
         }
         bool big = false;                             // a state value outside fp16's range was seen
-        auto write_state_operand = [&](int b) {      // S^T: row = value column, K = srow, fp16
-            unsigned char* sop = sm + C_OFF_S + b * SOP_BYTES;
+        // S^T of chunk c: row = value column, K = srow, fp16; and this warp's largest |S| (m, this thread's,
+        // computed where S is) for the choice of the next scale
+        auto write_state_operand = [&](int c, float m) {
+            unsigned char* sop = sm + C_OFF_S + (c & 1) * SOP_BYTES;
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) {
-                big |= fabsf(S[j]) > kF16Max;
+            for (int j = 0; j < CPT; ++j)
                 *reinterpret_cast<__half*>(sop + sw128_off_h(CPT * half + j, srow, SNV)) = __float2half_rn(S[j]);
-            }
+            big |= m > kF16Max;
+            const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+            if (lane == 0) smax[(c & 1) * 8 + warp] = mw;
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(sbar);
         };
-        // the chunk's B and Gamma_C, fetched one chunk ahead (after the proxy fence, which would wait on them)
-        uint2 bq[CPT / 4];                             // raw fp16: converted where used, so the prefetch never waits
-        float gamC = 0.f;
-        auto fetch_b = [&](int ci) {
+        auto absmax = [&]() {                         // a tree, not a chain of dependent maxima
+            float m[CPT / 2];
+#pragma unroll
+            for (int j = 0; j < CPT / 2; ++j) m[j] = fmaxf(fabsf(S[2 * j]), fabsf(S[2 * j + 1]));
+#pragma unroll
+            for (int w = CPT / 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+            return m[0];
+        };
+        // the chunk's B, Gamma_C and value scale, fetched two chunks ahead (records stream from HBM at a few
+        // TB/s while the chain runs, so one chunk of lead does not always cover the load latency); issued
+        // after the proxy fence, which would wait on them
+        uint2 bq[CPT / 4], bq2[CPT / 4];               // raw fp16: converted where used
+        float gamC = 0.f, gamC2 = 0.f;
+        int eb = 0, eb2 = 0;                           // the chunk's value scale exponent
+        auto fetch_b = [&](int ci, uint2 (&q)[CPT / 4], float& g, int& e) {
             const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
 #pragma unroll
             for (int m = 0; m < CPT / 4; ++m)
-                bq[m] = __ldg(reinterpret_cast<const uint2*>(rec + REC_B + (((jc + 4 * m) >> 2) * DK + srow) * 8));
-            gamC = __ldg(reinterpret_cast<const float*>(rec + REC_G) + srow);
+                q[m] = __ldg(reinterpret_cast<const uint2*>(rec + REC_B + (((jc + 4 * m) >> 2) * DK + srow) * 8));
+            g = __ldg(reinterpret_cast<const float*>(rec + REC_G) + srow);
+            e = __ldg(reinterpret_cast<const int*>(rec + REC_E));
         };
-        write_state_operand(0);
-        if (n_chunks > 0) fetch_b(0);
+        write_state_operand(0, absmax());
+        if (n_chunks > 0) fetch_b(0, bq, gamC, eb);
+        if (n_chunks > 1) fetch_b(1, bq2, gamC2, eb2);
         // the next snapshot point after the window start (never reached when there are no snapshots)
         int32_t snap_next = p.snap_every > 0 ? (c_begin * C / p.snap_every + 1) * p.snap_every : -1;
         bool ok = true;
@@ -854,17 +1044,44 @@ __global__ void __launch_bounds__(C_NT, 1)
             const int b = ci & 1;
             const uint32_t par = (uint32_t)(ci >> 1) & 1u;
             if (*s_abort) { ok = false; break; }
+            // every state warp's largest |S_c| (written before its arrival on sbar for chunk c; that phase is
+            // complete, so this wait returns at once and orders the reads after those writes)
+            if (!mbar_wait(sbar, (uint32_t)ci & 1u)) { fail(); ok = false; break; }
+            uint32_t ms = 0u;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) ms = max(ms, smax[b * 8 + w]);
+            const int e_state = scale_exp_f32_at(ms, E);
             if (!mbar_wait(dbar + 8 * b, par)) { fail(); ok = false; break; }
             tc_fence_after();
             float d[CPT];
             tmem_ld16(tmem + tlane + TM_S + CPT * half, d);
+            if (eb == E) {                             // the record's B is at the state's scale (always when nothing is scaled)
 #pragma unroll
-            for (int m = 0; m < CPT / 4; ++m) {
-                const float4 b4 = half4_to_float4(bq[m]);
-                S[4 * m + 0] = fmaf(gamC, S[4 * m + 0], b4.x - d[4 * m + 0]);
-                S[4 * m + 1] = fmaf(gamC, S[4 * m + 1], b4.y - d[4 * m + 1]);
-                S[4 * m + 2] = fmaf(gamC, S[4 * m + 2], b4.z - d[4 * m + 2]);
-                S[4 * m + 3] = fmaf(gamC, S[4 * m + 3], b4.w - d[4 * m + 3]);
+                for (int m = 0; m < CPT / 4; ++m) {
+                    const float4 b4 = half4_to_float4(bq[m]);
+                    S[4 * m + 0] = fmaf(gamC, S[4 * m + 0], b4.x - d[4 * m + 0]);
+                    S[4 * m + 1] = fmaf(gamC, S[4 * m + 1], b4.y - d[4 * m + 1]);
+                    S[4 * m + 2] = fmaf(gamC, S[4 * m + 2], b4.z - d[4 * m + 2]);
+                    S[4 * m + 3] = fmaf(gamC, S[4 * m + 3], b4.w - d[4 * m + 3]);
+                }
+            } else {                                   // B is stored divided by 2^eb; S carried divided by 2^E
+                const float sb = exp2i(eb - E);
+#pragma unroll
+                for (int m = 0; m < CPT / 4; ++m) {
+                    const float4 b4 = half4_to_float4(bq[m]);
+                    S[4 * m + 0] = fmaf(gamC, S[4 * m + 0], fmaf(sb, b4.x, -d[4 * m + 0]));
+                    S[4 * m + 1] = fmaf(gamC, S[4 * m + 1], fmaf(sb, b4.y, -d[4 * m + 1]));
+                    S[4 * m + 2] = fmaf(gamC, S[4 * m + 2], fmaf(sb, b4.z, -d[4 * m + 2]));
+                    S[4 * m + 3] = fmaf(gamC, S[4 * m + 3], fmaf(sb, b4.w, -d[4 * m + 3]));
+                }
+            }
+            // the scale of S_{c+1}: that of the chunk's values or of the state before it, whichever is larger
+            const int E_next = max(eb, e_state);
+            if (E_next != E) {
+                const float r = exp2i(E - E_next);
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) S[j] *= r;
+                E = E_next;
             }
             const int32_t t_done = min(T, (c_begin + ci + 1) * C);   // tokens of the sequence now in S
             if (ci + 1 < n_chunks) {
@@ -872,8 +1089,16 @@ __global__ void __launch_bounds__(C_NT, 1)
                 if (ci > 0 && !mbar_wait(obar + 8 * (b ^ 1), (uint32_t)((ci - 1) >> 1) & 1u)) {
                     fail(); ok = false; break;
                 }
-                write_state_operand(b ^ 1);
-                fetch_b(ci + 1);
+                write_state_operand(ci + 1, absmax());
+                if (tid == 0) {                        // the output warps' copy of E for chunk c+1
+                    e_ring[(ci + 1) & 3] = E;
+                    mbar_arrive(ebar + 8 * ((ci + 1) & 3));
+                }
+#pragma unroll
+                for (int m = 0; m < CPT / 4; ++m) bq[m] = bq2[m];
+                gamC = gamC2;
+                eb = eb2;
+                if (ci + 2 < n_chunks) fetch_b(ci + 2, bq2, gamC2, eb2);
             }
             // a snapshot of the state after this chunk, if due (off the sequential path: after the operand
             // of the next chunk is out; the check is a compare against the next snapshot point)
@@ -881,18 +1106,20 @@ __global__ void __launch_bounds__(C_NT, 1)
                 const int64_t slot = snapshot_slot(p, 0, t_done, T);
                 if (slot >= 0) {
                     float* dst = p.snapshots + ((slot * H + h) * DK + srow) * (int64_t)p.dv + jc;
+                    const float f = exp2i(E);
 #pragma unroll
                     for (int x = 0; x < CPT; x += 4)
-                        *reinterpret_cast<float4*>(dst + x) = make_float4(S[x], S[x + 1], S[x + 2], S[x + 3]);
+                        *reinterpret_cast<float4*>(dst + x) = make_float4(f * S[x], f * S[x + 1], f * S[x + 2], f * S[x + 3]);
                 }
                 snap_next += p.snap_every;
             }
         }
         if (ok && !*s_abort) {
+            const float f = exp2i(E);
 #pragma unroll
             for (int j = 0; j < CPT; j += 4)
                 *reinterpret_cast<float4*>(p.state_out + state_off + j) =
-                    make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                    make_float4(f * S[j], f * S[j + 1], f * S[j + 2], f * S[j + 3]);
         }
         if (big) atomicOr(p.err, KDA_DEVERR_RANGE);
     }
@@ -941,7 +1168,7 @@ __device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], const uint32_t (&
 
 template <typename TIn>
 __global__ void __launch_bounds__(BR_NT, 1) kda_bwd_dstate_records_kernel(BwdParams p, const unsigned char* records) {
-    extern __shared__ __align__(16) unsigned char sm[];
+    extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const int H = p.H, h = blockIdx.x / SLICES, j0 = (blockIdx.x % SLICES) * SNV;

@@ -199,6 +199,20 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(PrefillParams p, 
         issue_chunk_loads<NV>(sm, maps, g, t_begin, min(C, t_end - t_begin), tid, lbar);
         loads_pending = true;
     }
+#ifdef KDA_TEST_HOOKS
+    if (p.test_stall) {                              // the first copies are in flight: give up a wait now
+        if (tid == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(sm + OFF_MISC + 24)) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+        if (!test_stall_wait(saddr(sm + OFF_MISC + 24))) {
+            atomicOr(p.err, KDA_DEVERR_TIMEOUT);
+            *s_abort = 1;
+        }
+        __syncthreads();
+    }
+#endif
 
     auto write_state_operand = [&]() {           // S^T as a bf16 operand; even lanes store key pairs
 #pragma unroll

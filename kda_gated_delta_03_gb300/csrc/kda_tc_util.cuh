@@ -149,7 +149,7 @@ __device__ __forceinline__ void umma_commit(uint32_t mbar) {
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long long limit = kWaitLimit) {
     const long long t0 = clock64();
     while (true) {
         uint32_t done;
@@ -159,9 +159,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
             : "r"(mbar), "r"(parity)
             : "memory");
         if (done) return true;
-        if (clock64() - t0 > kWaitLimit) return false;
+        if (clock64() - t0 > limit) return false;
     }
 }
+
+#ifdef KDA_TEST_HOOKS
+// Test builds only (-DKDA_TEST_HOOKS): when PrefillParams::test_stall is set, a kernel waits on a barrier
+// that nothing completes, with its first copies already in flight, so that the bounded wait gives up
+// (after about 1 ms) and the kernel's abandon path runs: KDA_DEVERR_TIMEOUT, its copies drained, TMEM
+// freed.  `never` is an mbarrier initialised with one pending arrival that no thread ever makes.
+constexpr long long kTestStallLimit = 2000000LL;
+__device__ __forceinline__ bool test_stall_wait(uint32_t never) { return mbar_wait(never, 0u, kTestStallLimit); }
+#endif
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
