@@ -92,7 +92,7 @@ typedef enum {
  * answer).  Pure host function; never fails (returns 0 for invalid sizes).
  *  - Several sequences: the longest-first schedule, 4 bytes per sequence.
  *  - One bf16 sequence with d_k = d_v = 128: the per-chunk records of the
- *    two-phase path (98,832 bytes per chunk and head, up to 1 GiB of them).
+ *    two-phase path (99,072 bytes per chunk and head, up to 1 GiB of them).
  *    kda_prefill also accepts less, down to the size returned for
  *    total_tokens = 64 (one chunk per window); it then walks the sequence in
  *    more windows, with identical results.

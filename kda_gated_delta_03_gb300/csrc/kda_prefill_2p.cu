@@ -32,8 +32,8 @@ constexpr int REC_QM = 0;          // [Q'; M]: 192 x 128 fp16 K-major operand (4
 constexpr int REC_B = 49152;       // B = Khat^T Utilde: fp16 [32 column quads][128 rows][4] (32 KiB)
 constexpr int REC_O = 81920;       // P Utilde: fp16 [32 column quads][64 rows][4] (16 KiB)
 constexpr int REC_G = 98304;       // Gamma_C: fp32 [128]
-constexpr int REC_E = 98816;       // e_c: int32, B and P Utilde are stored divided by 2^e_c (then 12 bytes of pad)
-constexpr int REC_BYTES = 98832;
+constexpr int REC_E = 98816;       // e_c: int32, B and P Utilde are stored divided by 2^e_c
+constexpr int REC_BYTES = 99072;   // padded to 256 bytes, so that every record's stores and loads stay sector-aligned
 constexpr int QM_BYTES = (C + DK) * DK * 2;
 // Q', M, B, P Utilde and the chain's state operand are fp16: the same 10-bit significand as TF32, in half
 // the bytes, for values within fp16's range, which the kernels check (KDA_DEVERR_RANGE)
@@ -85,14 +85,12 @@ constexpr int P_OFF_S = align1k(P_OFF_VMX + 32);            // scratch, 144 KiB
 constexpr int PS_A = 0, PS_T = C * AT_LD * 4, PS_SCR = 2 * C * AT_LD * 4;   // solve tiles
 constexpr int PS_OPT = 38912, PS_KV = PS_OPT + 16384;                     // T' and [Gamma.K | V]^T (N = 256)
 constexpr int PS_P = 122880;                                               // P operand
-constexpr int PS_WU = 0, PS_KH = 131072;            // fold operands: [W | Utilde]^T after step 4, Khat^T (built
-                                                     // during step 4, after the P operand)
+constexpr int PS_WU = 0, PS_KH = 65536;                                    // fold operands, after [W | Utilde]
 constexpr int ONE_L_OFF = C * DK * 4;                                     // one-reference A/P: R, then L
 constexpr float kOneRefMax = 125.f;                                        // log2 of the largest factor
 constexpr int P_SMEM = P_OFF_S + G1_BYTES;
 static_assert(PS_KV + (DK + DK) * 256 <= PS_P && PS_P + 16384 <= G1_BYTES, "phase-1 scratch");
-static_assert(PS_WU + 2 * DK * C * 2 <= PS_OPT && PS_P + C * C * 2 <= PS_KH && PS_KH + DK * C * 2 <= G1_BYTES,
-              "phase-1 fold operands");
+static_assert(PS_KH + DK * C * 4 <= PS_P, "phase-1 fold operands");
 static_assert(P_SMEM <= 232448, "phase-1 shared memory");
 
 // ---- phase 2 shared memory and threads ----
@@ -294,17 +292,20 @@ __global__ void __launch_bounds__(NT, 1)
     bool load_pending = (int)blockIdx.x < n_units;   // q and alpha of the next unit in flight
     bool vk_pending = load_pending;                   // v (and k) of the next unit in flight
     bool k_issued = load_pending;
-    float beta_next = 0.f, alpha_next = 1.f;          // this thread's token row of the next unit
+    // beta (and a per-head alpha) of this thread's token row: a unit's values go to shared memory at the end
+    // of the previous unit, from registers loaded at that unit's start, so no load latency is waited on
+    float beta_next = 0.f, alpha_next = 1.f;
     const bool per_head = p.alpha_mode == KDA_ALPHA_PER_HEAD;
     if (load_pending) {
         issue_v(blockIdx.x);
         issue_k(blockIdx.x);
         issue_qa(blockIdx.x);
         const int32_t tn = (int32_t)(c_begin + (int)blockIdx.x / H) * C;
-        if (tid < C && tn + tid < p.total_tokens) {
+        if (tid < C) {
             const int64_t row = (int64_t)(tn + tid) * H + (int)blockIdx.x % H;
-            beta_next = p.beta[row];
-            if (per_head) alpha_next = p.alpha[row];
+            const bool in = tn + tid < p.total_tokens;
+            sbeta[tid] = in ? p.beta[row] : 0.f;
+            sasc[tid] = per_head && in ? p.alpha[row] : 1.f;
         }
     }
 #ifdef KDA_TEST_HOOKS
@@ -328,10 +329,6 @@ __global__ void __launch_bounds__(NT, 1)
         const int L = min(C, p.total_tokens - t0);
         unsigned char* rec = records + (size_t)u * REC_BYTES;
         const int un = u + (int)gridDim.x;                       // this CTA's next unit
-        if (tid < C) {
-            sbeta[tid] = beta_next;
-            sasc[tid] = alpha_next;
-        }
         if (!mbar_wait(vkbar, vkph) || !mbar_wait(lbar, lph)) {
             atomicOr(p.err, KDA_DEVERR_TIMEOUT);
             *s_abort = 1;
@@ -342,6 +339,12 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_before();
         __syncthreads();
         if (*s_abort) break;
+        if (tid < C && un < n_units) {                  // the next unit's beta (and alpha), used at this unit's end
+            const int32_t tn = (int32_t)(c_begin + un / H) * C;
+            const int64_t row = (int64_t)(tn + tid) * H + un % H;
+            beta_next = tn + tid < p.total_tokens ? p.beta[row] : 0.f;
+            alpha_next = per_head && tn + tid < p.total_tokens ? p.alpha[row] : 1.f;
+        }
         if (L < C) {                                    // rows past the sequence end read as zero
             for (int e = tid; e < (C - L) * 16; e += NT) {
                 const int r = L + (e >> 4), c = e & 15;
@@ -358,13 +361,12 @@ __global__ void __launch_bounds__(NT, 1)
             const uint4* vv = reinterpret_cast<const uint4*>(sm + P_OFF_V) + tid;   // 16 B per thread per step
             uint32_t vm = 0u;                           // largest bf16 magnitude bits of this thread's 32 values
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
+            for (int x = 0; x < 4; ++x) {               // two bf16 magnitudes per 32-bit word, maxima per half
                 const uint4 w = vv[x * NT];
-                const uint32_t a = w.x & 0x7FFF7FFFu, b = w.y & 0x7FFF7FFFu, c = w.z & 0x7FFF7FFFu, d = w.w & 0x7FFF7FFFu;
-                vm = max(vm, max(max(a >> 16, a & 0xFFFFu), max(b >> 16, b & 0xFFFFu)));
-                vm = max(vm, max(max(c >> 16, c & 0xFFFFu), max(d >> 16, d & 0xFFFFu)));
+                vm = __vmaxu2(vm, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                                           __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
             }
-            vm = __reduce_max_sync(0xffffffffu, vm);
+            vm = __reduce_max_sync(0xffffffffu, max(vm >> 16, vm & 0xFFFFu));
             if (lane == 0) reinterpret_cast<uint32_t*>(sm + P_OFF_VMX)[warp] = vm;
         }
         {
@@ -409,8 +411,8 @@ __global__ void __launch_bounds__(NT, 1)
         float* scr = reinterpret_cast<float*>(X + PS_SCR);
         unsigned char* opP = X + PS_P;
         if (one_ref) {
-            // R = (2^(g_31 - g) . K) (M=64 rows s) and L = [2^(g - g_31) . K; 2^(g - g_31) . Q] (N=128 rows r), TF32,
-            // K=128 channels: D[s][r] = A-part (r < 64) and P-part (r >= 64) of the whole chunk
+            // L = [2^(g - g_31) . K; 2^(g - g_31) . Q] (M=128 rows r') and R = 2^(g_31 - g) . K (N=64 rows s), TF32,
+            // K=128 channels: D[r'][s] = the A-part (rows r' < 64) and the P-part (rows r' >= 64) of the chunk
             const int cq = 4 * warp + (lane >> 3), j = lane & 7, i0 = 4 * cq;
             const float4 ref = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(31, i0));
 #pragma unroll
@@ -439,8 +441,8 @@ __global__ void __launch_bounds__(NT, 1)
             __syncthreads();
             if (warp == 0 && elect_one()) {
                 tc_fence_after();
-                constexpr uint32_t id = idesc_tf32(64, 2 * C);
-                const uint64_t ad = op_desc(saddr(X), DK), bd = op_desc(saddr(X + ONE_L_OFF), DK);
+                constexpr uint32_t id = idesc_tf32(128, C);
+                const uint64_t ad = op_desc(saddr(X + ONE_L_OFF), DK), bd = op_desc(saddr(X), DK);
 #pragma unroll
                 for (int ks = 0; ks < DK / 8; ++ks)
                     umma_tf32_1(tmem + TM_W, ad + (uint64_t)(ks * 16), bd + (uint64_t)(ks * 16), id, ks > 0 ? 1u : 0u);
@@ -513,18 +515,35 @@ __global__ void __launch_bounds__(NT, 1)
         drain(0);                                       // while the products run
         drain(1);
         if (!wait_mma()) break;
-        {                                               // scatter: A (fp32) and P (TF32 operand)
+        if (one_ref) {                                  // scatter: row r' of D, columns s = 32 half .. + 31
+            float v[32];
+            tmem_ld32(tmem + tlane + TM_W + 32 * half, v);
+            const int s0 = 32 * half;
+            if (quad < 2) {                             // A (fp32, strictly lower, beta-scaled), row r
+                const int r = 32 * quad + lane;
+                const float br = sbeta[r];
+#pragma unroll
+                for (int x = 0; x < 32; x += 4)
+                    *reinterpret_cast<float4*>(Ab + r * AT_LD + s0 + x) =
+                        make_float4(s0 + x < r ? br * v[x] : 0.f, s0 + x + 1 < r ? br * v[x + 1] : 0.f,
+                                    s0 + x + 2 < r ? br * v[x + 2] : 0.f, s0 + x + 3 < r ? br * v[x + 3] : 0.f);
+            } else {                                    // P (fp16 operand, lower with the diagonal), row r
+                const int r = 32 * quad + lane - C;
+#pragma unroll
+                for (int x = 0; x < 32; x += 8)
+                    *reinterpret_cast<uint4*>(opP + op_off_h(r, s0 + x, C)) = make_uint4(
+                        pack_half2(s0 + x <= r ? v[x] : 0.f, s0 + x + 1 <= r ? v[x + 1] : 0.f),
+                        pack_half2(s0 + x + 2 <= r ? v[x + 2] : 0.f, s0 + x + 3 <= r ? v[x + 3] : 0.f),
+                        pack_half2(s0 + x + 4 <= r ? v[x + 4] : 0.f, s0 + x + 5 <= r ? v[x + 5] : 0.f),
+                        pack_half2(s0 + x + 6 <= r ? v[x + 6] : 0.f, s0 + x + 7 <= r ? v[x + 7] : 0.f));
+            }
+        } else {                                        // scatter: A (fp32) and P (fp16 operand)
             const int sr = 16 * quad + lane;
             float v[32];
 #pragma unroll
             for (int bb = 0; bb < 2; ++bb) {
                 const int b = 2 * half + bb;
-                if (one_ref) {                          // A-part columns r, P-part columns 64 + r
-                    tmem_ld16(tmem + tlane + TM_W + 16 * b, v);
-                    tmem_ld16(tmem + tlane + TM_W + C + 16 * b, v + 16);
-                } else {
-                    tmem_ld32(tmem + tlane + TM_W + 32 * b, v);
-                }
+                tmem_ld32(tmem + tlane + TM_W + 32 * b, v);
                 if (lane < 16) {
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
@@ -538,24 +557,8 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_before();
         __syncthreads();
 
-        // ---- 3. T = (I + A)^-1 by 16x16 blocks; while warps 0-1 invert the diagonal blocks, warps 2-7 build
-        //         the [Gamma.K | V]^T operand of step 4 (fp16, N=256 rows, K=64 time), which needs no T ----
-        if (tid >= 64) {
-            for (int e = tid - 64; e < DK * 16; e += NT - 64) {
-                const int i = e & (DK - 1), m0 = 4 * (e >> 7);
-                float gg[4], kk4[4];
-#pragma unroll
-                for (int x = 0; x < 4; ++x) { gg[x] = Gat(m0 + x, i); kk4[x] = kat(m0 + x, i); }
-                *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(i, m0, C)) =
-                    make_uint2(pack_half2(ex2f(gg[0]) * kk4[0], ex2f(gg[1]) * kk4[1]),
-                               pack_half2(ex2f(gg[2]) * kk4[2], ex2f(gg[3]) * kk4[3]));
-                const float v0 = vscale * bf(vraw + (m0 + 0) * DK + i), v1 = vscale * bf(vraw + (m0 + 1) * DK + i);
-                const float v2 = vscale * bf(vraw + (m0 + 2) * DK + i), v3 = vscale * bf(vraw + (m0 + 3) * DK + i);
-                big |= fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))) > kF16Max;
-                *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(DK + i, m0, C)) =
-                    make_uint2(pack_half2(v0, v1), pack_half2(v2, v3));
-            }
-        } else {
+        // ---- 3. T = (I + A)^-1 by 16x16 blocks ----
+        if (tid < 64) {
             const int b = tid >> 4, c = tid & 15;
             float tc[16];
 #pragma unroll
@@ -627,6 +630,20 @@ __global__ void __launch_bounds__(NT, 1)
             *reinterpret_cast<uint2*>(X + PS_OPT + op_off_h(r, m0, C)) =
                 make_uint2(pack_half2(v.x, v.y), pack_half2(v.z, v.w));
         }
+        // [Gamma.K | V]^T -> fp16 operand (N=256 rows, K=64 time), v scaled by 2^-e_c
+        for (int e = tid; e < DK * 16; e += NT) {
+            const int i = e & (DK - 1), m0 = 4 * (e >> 7);
+            float gg[4], kk4[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) { gg[x] = Gat(m0 + x, i); kk4[x] = kat(m0 + x, i); }
+            *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(i, m0, C)) =
+                make_uint2(pack_half2(ex2f(gg[0]) * kk4[0], ex2f(gg[1]) * kk4[1]),
+                           pack_half2(ex2f(gg[2]) * kk4[2], ex2f(gg[3]) * kk4[3]));
+            const float v0 = vscale * bf(vraw + (m0 + 0) * DK + i), v1 = vscale * bf(vraw + (m0 + 1) * DK + i);
+            const float v2 = vscale * bf(vraw + (m0 + 2) * DK + i), v3 = vscale * bf(vraw + (m0 + 3) * DK + i);
+            big |= fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))) > kF16Max;
+            *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(DK + i, m0, C)) = make_uint2(pack_half2(v0, v1), pack_half2(v2, v3));
+        }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -651,21 +668,11 @@ __global__ void __launch_bounds__(NT, 1)
         }
         drain(2);                                       // while the products run
         drain(3);
-        unsigned char* opWU = X + PS_WU;
-        unsigned char* opKH = X + PS_KH;
-        for (int e = tid; e < DK * 16; e += NT) {       // Khat^T = ((Gamma_C / Gamma) . K)^T, fp16 (M=128, K=64)
-            const int i = e & (DK - 1), s0 = 4 * (e >> 7);
-            const float gl = Gat(C - 1, i);
-            float gg[4], kk4[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) { gg[x] = Gat(s0 + x, i); kk4[x] = kat(s0 + x, i); }
-            *reinterpret_cast<uint2*>(opKH + op_off_h(i, s0, C)) =
-                make_uint2(pack_half2(ex2f(gl - gg[0]) * kk4[0], ex2f(gl - gg[1]) * kk4[1]),
-                           pack_half2(ex2f(gl - gg[2]) * kk4[2], ex2f(gl - gg[3]) * kk4[3]));
-        }
         if (!wait_mma()) break;
 
-        // ---- 5. fold operand [W | Utilde]^T (N=256, K=64) ----
+        // ---- 5. fold operands: [W | Utilde]^T (N=256, K=64) and Khat^T (M=128, K=64) ----
+        unsigned char* opWU = X + PS_WU;
+        unsigned char* opKH = X + PS_KH;
         {
             const int n = DK * half + 32 * quad + lane;          // row of [W | Utilde]^T held by this lane
             float v[32];
@@ -679,6 +686,16 @@ __global__ void __launch_bounds__(NT, 1)
                         make_uint2(pack_half2(v[x], v[x + 1]), pack_half2(v[x + 2], v[x + 3]));
                 }
             }
+        }
+        for (int e = tid; e < DK * 16; e += NT) {
+            const int i = e & (DK - 1), s0 = 4 * (e >> 7);
+            const float gl = Gat(C - 1, i);
+            float gg[4], kk4[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) { gg[x] = Gat(s0 + x, i); kk4[x] = kat(s0 + x, i); }
+            *reinterpret_cast<uint2*>(opKH + op_off_h(i, s0, C)) =
+                make_uint2(pack_half2(ex2f(gl - gg[0]) * kk4[0], ex2f(gl - gg[1]) * kk4[1]),
+                           pack_half2(ex2f(gl - gg[2]) * kk4[2], ex2f(gl - gg[3]) * kk4[3]));
         }
         drain(4);                                       // the last piece, before step 6 writes its columns
         rec_prev = nullptr;
@@ -736,14 +753,12 @@ __global__ void __launch_bounds__(NT, 1)
         fence_async_smem();
         tc_fence_before();
         __syncthreads();                                         // q and alpha (g) are read
-        if (un < n_units) {                                      // fetch the next unit's q, alpha and beta
+        if (un < n_units) {                                      // fetch the next unit's q and alpha tiles
             issue_qa(un);
             load_pending = true;
-            if (tid < C) {
-                const int32_t tn = (int32_t)(c_begin + un / H) * C;
-                const int64_t row = (int64_t)(tn + tid) * H + un % H;
-                beta_next = tn + tid < p.total_tokens ? p.beta[row] : 0.f;
-                alpha_next = per_head && tn + tid < p.total_tokens ? p.alpha[row] : 1.f;
+            if (tid < C) {                                       // beta was read in steps 2-3, alpha in step 1
+                sbeta[tid] = beta_next;
+                sasc[tid] = alpha_next;
             }
         }
     }
@@ -810,7 +825,7 @@ __global__ void __launch_bounds__(C_NT, 1)
     // ebar[c & 3]: E of chunk c's state operand is in E_ring[c & 3] (one arrival, by state warp 0)
     const uint32_t ebar = saddr(misc + CM_EBAR);
     volatile int* e_ring = reinterpret_cast<volatile int*>(misc + CM_ERING);
-    volatile uint32_t* smax = reinterpret_cast<volatile uint32_t*>(misc + CM_SLOT);
+    uint32_t* smax = reinterpret_cast<uint32_t*>(misc + CM_SLOT);   // read only after an mbarrier acquire
     constexpr uint32_t TM_S = 0, TM_O = 32;           // M S accumulator; two [Q'; M_top] S accumulators
 
     if (tid == 0) {
@@ -1020,23 +1035,21 @@ __global__ void __launch_bounds__(C_NT, 1)
                 for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
             return m[0];
         };
-        // the chunk's B, Gamma_C and value scale, fetched two chunks ahead (records stream from HBM at a few
-        // TB/s while the chain runs, so one chunk of lead does not always cover the load latency); issued
-        // after the proxy fence, which would wait on them
-        uint2 bq[CPT / 4], bq2[CPT / 4];               // raw fp16: converted where used
-        float gamC = 0.f, gamC2 = 0.f;
-        int eb = 0, eb2 = 0;                           // the chunk's value scale exponent
-        auto fetch_b = [&](int ci, uint2 (&q)[CPT / 4], float& g, int& e) {
+        // the chunk's B, Gamma_C and value scale, fetched one chunk ahead, after the proxy fence (which would
+        // wait on them)
+        uint2 bq[CPT / 4];                             // raw fp16: converted where used
+        float gamC = 0.f;
+        int eb = 0;                                    // the chunk's value scale exponent
+        auto fetch_b = [&](int ci) {
             const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
 #pragma unroll
             for (int m = 0; m < CPT / 4; ++m)
-                q[m] = __ldg(reinterpret_cast<const uint2*>(rec + REC_B + (((jc + 4 * m) >> 2) * DK + srow) * 8));
-            g = __ldg(reinterpret_cast<const float*>(rec + REC_G) + srow);
-            e = __ldg(reinterpret_cast<const int*>(rec + REC_E));
+                bq[m] = __ldg(reinterpret_cast<const uint2*>(rec + REC_B + (((jc + 4 * m) >> 2) * DK + srow) * 8));
+            gamC = __ldg(reinterpret_cast<const float*>(rec + REC_G) + srow);
+            eb = __ldg(reinterpret_cast<const int*>(rec + REC_E));
         };
         write_state_operand(0, absmax());
-        if (n_chunks > 0) fetch_b(0, bq, gamC, eb);
-        if (n_chunks > 1) fetch_b(1, bq2, gamC2, eb2);
+        if (n_chunks > 0) fetch_b(0);
         // the next snapshot point after the window start (never reached when there are no snapshots)
         int32_t snap_next = p.snap_every > 0 ? (c_begin * C / p.snap_every + 1) * p.snap_every : -1;
         bool ok = true;
@@ -1047,9 +1060,9 @@ __global__ void __launch_bounds__(C_NT, 1)
             // every state warp's largest |S_c| (written before its arrival on sbar for chunk c; that phase is
             // complete, so this wait returns at once and orders the reads after those writes)
             if (!mbar_wait(sbar, (uint32_t)ci & 1u)) { fail(); ok = false; break; }
-            uint32_t ms = 0u;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) ms = max(ms, smax[b * 8 + w]);
+            const uint4 m0 = reinterpret_cast<const uint4*>(const_cast<const uint32_t*>(smax))[2 * b];
+            const uint4 m1 = reinterpret_cast<const uint4*>(const_cast<const uint32_t*>(smax))[2 * b + 1];
+            const uint32_t ms = max(max(max(m0.x, m0.y), max(m0.z, m0.w)), max(max(m1.x, m1.y), max(m1.z, m1.w)));
             const int e_state = scale_exp_f32_at(ms, E);
             if (!mbar_wait(dbar + 8 * b, par)) { fail(); ok = false; break; }
             tc_fence_after();
@@ -1085,20 +1098,15 @@ __global__ void __launch_bounds__(C_NT, 1)
             }
             const int32_t t_done = min(T, (c_begin + ci + 1) * C);   // tokens of the sequence now in S
             if (ci + 1 < n_chunks) {
-                // the operand buffer of S_{c+1} was last read by the products of chunk c-1 (obar)
-                if (ci > 0 && !mbar_wait(obar + 8 * (b ^ 1), (uint32_t)((ci - 1) >> 1) & 1u)) {
-                    fail(); ok = false; break;
-                }
+                // the operand buffer of S_{c+1} was last read by the products of chunk c-1; they were issued
+                // before chunk c's state products, whose commit (dbar, waited above) tracks every earlier
+                // tensor-core operation of the issuing thread, so they are complete
                 write_state_operand(ci + 1, absmax());
                 if (tid == 0) {                        // the output warps' copy of E for chunk c+1
                     e_ring[(ci + 1) & 3] = E;
                     mbar_arrive(ebar + 8 * ((ci + 1) & 3));
                 }
-#pragma unroll
-                for (int m = 0; m < CPT / 4; ++m) bq[m] = bq2[m];
-                gamC = gamC2;
-                eb = eb2;
-                if (ci + 2 < n_chunks) fetch_b(ci + 2, bq2, gamC2, eb2);
+                fetch_b(ci + 1);
             }
             // a snapshot of the state after this chunk, if due (off the sequential path: after the operand
             // of the next chunk is out; the check is a compare against the next snapshot point)

@@ -53,11 +53,11 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # one bf16 d=128 sequence: 98,832 bytes of records per (chunk, head), at most 1 GiB of them
-    assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 1) == 128 * 32 * 98832
-    assert lib.kda_prefill_workspace_size(1, 1_032_192, 8, 128, 128, 1) == 1358 * 8 * 98832
-    assert lib.kda_prefill_workspace_size(1, 1 << 20, 32, 128, 128, 1) == 339 * 32 * 98832
-    assert lib.kda_prefill_workspace_size(1, 65, 4, 128, 128, 1) == (2 * 4 * 98832 + 255) // 256 * 256
+    # one bf16 d=128 sequence: 99,072 bytes of records per (chunk, head), at most 1 GiB of them
+    assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 1) == 128 * 32 * 99072
+    assert lib.kda_prefill_workspace_size(1, 1_032_192, 8, 128, 128, 1) == 1354 * 8 * 99072
+    assert lib.kda_prefill_workspace_size(1, 1 << 20, 32, 128, 128, 1) == 338 * 32 * 99072
+    assert lib.kda_prefill_workspace_size(1, 65, 4, 128, 128, 1) == (2 * 4 * 99072 + 255) // 256 * 256
     assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 0) == 0      # fp32: single-kernel path
     assert lib.kda_prefill_workspace_size(1, 8192, 32, 64, 64, 1) == 0
     assert lib.kda_prefill_workspace_size(64, 300000, 32, 128, 128, 1) == 256
@@ -137,10 +137,10 @@ def decode(lib, fn="kda_decode_step", **over):
     (dict(N=4), binding.KDA_ERR_WORKSPACE),
     (dict(N=4, ws=P, wsb=255), binding.KDA_ERR_WORKSPACE),
     (dict(N=4, ws=ctypes.c_void_p(0x10010), wsb=4096), binding.KDA_ERR_WORKSPACE),
-    # one bf16 d=128 sequence needs at least one chunk's records (H x 98,832 bytes)
+    # one bf16 d=128 sequence needs at least one chunk's records (H x 99,072 bytes)
     (dict(dk=128, dv=128, dt=1), binding.KDA_ERR_WORKSPACE),
-    (dict(dk=128, dv=128, dt=1, ws=P, wsb=2 * 98832 - 1), binding.KDA_ERR_WORKSPACE),
-    (dict(dk=128, dv=128, dt=1, ws=ctypes.c_void_p(0x10010), wsb=2 * 98832), binding.KDA_ERR_WORKSPACE),
+    (dict(dk=128, dv=128, dt=1, ws=P, wsb=2 * 99072 - 1), binding.KDA_ERR_WORKSPACE),
+    (dict(dk=128, dv=128, dt=1, ws=ctypes.c_void_p(0x10010), wsb=2 * 99072), binding.KDA_ERR_WORKSPACE),
     (dict(N=0, T=5), binding.KDA_ERR_INVALID_ARG),
     (dict(N=0, T=0), binding.KDA_OK),
 ])

@@ -128,7 +128,7 @@ def test_two_phase_windows_give_identical_results():
     inp = I.prefill_inputs([1000], 2, 128, 128, "bf16", 15, decay="slow", state="randn")
     args = [to_dev(inp[n], n in ("q", "k", "v")) for n in ("q", "k", "v", "beta", "alpha", "cu_seqlens")]
     s0 = to_dev(inp["state_in"])
-    rec = 2 * 98832                                           # one chunk of records for H = 2
+    rec = 2 * 99072                                           # one chunk of records for H = 2
     assert kda.kda_prefill_workspace_size(1, 1000, 2, 128, 128, torch.bfloat16) == 16 * rec
     runs = []
     for chunks in (16, 5, 1):

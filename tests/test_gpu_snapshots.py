@@ -22,7 +22,7 @@ def run(inp, every, workspace_chunks=None):
     snaps = torch.full((max(len(ref), 1), inp["H"], inp["dk"], inp["dv"]), float("nan"), device="cuda:0")
     ws = None
     if workspace_chunks:
-        ws = torch.empty(workspace_chunks * inp["H"] * 98832, dtype=torch.uint8, device="cuda:0")
+        ws = torch.empty(workspace_chunks * inp["H"] * 99072, dtype=torch.uint8, device="cuda:0")
     o, st = kda.kda_prefill(*args, s0, workspace=ws, snapshot_every=every, snapshots=snaps,
                             snapshot_offsets=to_dev(offs))
     torch.cuda.synchronize()
