@@ -357,6 +357,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
 
         // ---- 1. g = running sum of clamped log2 alpha per key channel; the largest |v| of the chunk ----
+        bool one_ref;
         {
             const uint4* vv = reinterpret_cast<const uint4*>(sm + P_OFF_V) + tid;   // 16 B per thread per step
             uint32_t vm = 0u;                           // largest bf16 magnitude bits of this thread's 32 values
@@ -383,14 +384,18 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int x = 0; x < 32; ++x) Gat(32 * rh + x, ch) = la[x];
             __syncthreads();
+            // one decay reference for the whole chunk (row 31) keeps every factor of step 2 inside float range
+            // when each channel decays by at most 2^kOneRefMax over rows 0..31 and over rows 31..63
+            float span = la[0] - la[31];                // g_0 - g_31 (rows 0..31 of this channel)
             if (rh == 1) {
                 const float base = Gat(31, ch);
 #pragma unroll
                 for (int x = 0; x < 32; ++x) Gat(32 + x, ch) = la[x] + base;
                 sgam[ch] = ex2f(la[31] + base);
+                span = -la[31];                         // g_31 - g_63
             }
+            one_ref = !__syncthreads_or(span > kOneRefMax);
         }
-        __syncthreads();
         int ec;                                         // this chunk's value scale exponent
         {
             const uint4 m0 = *reinterpret_cast<const uint4*>(sm + P_OFF_VMX);
@@ -398,14 +403,9 @@ __global__ void __launch_bounds__(NT, 1)
             ec = scale_exp_bf16(max(max(max(m0.x, m0.y), max(m0.z, m0.w)), max(max(m1.x, m1.y), max(m1.z, m1.w))));
         }
         const float vscale = exp2i(-ec);
-        // One decay reference for the whole chunk (row 31) keeps every factor of step 2 inside float range when
-        // each channel decays by at most 2^kOneRefMax over rows 0..31 and over rows 31..63; then A and P are one
-        // product (16 tcgen05 instructions instead of 64).  Otherwise (strong decay) each 16-row block takes its
-        // own reference.
-        const bool one_ref = !__syncthreads_or(
-            (rh == 0 ? Gat(0, ch) - Gat(31, ch) : Gat(31, ch) - Gat(C - 1, ch)) > kOneRefMax);
 
-        // ---- 2. A and P on tcgen05 ----
+        // ---- 2. A and P on tcgen05: with one reference (the decay allows it) one product of 16 instructions,
+        //         otherwise one per 16-row block with its own reference ----
         float* Ab = reinterpret_cast<float*>(X + PS_A);
         float* Tb = reinterpret_cast<float*>(X + PS_T);
         float* scr = reinterpret_cast<float*>(X + PS_SCR);
@@ -699,12 +699,40 @@ __global__ void __launch_bounds__(NT, 1)
         }
         drain(4);                                       // the last piece, before step 6 writes its columns
         rec_prev = nullptr;
+        {
+            // -Gamma.Q into the PW half of step 6's M=64 accumulator (row r at lane r % 16 of quadrant r / 16,
+            // columns 2 DK + c) and zeros into its P Utilde half, so that step 6 accumulates PW - Gamma.Q = -Q'
+            // and q and alpha are free from here on; each warp writes the columns of its own quadrant that it
+            // has just read the [W | Utilde]^T accumulator from
+            const int gr = mr & (C - 1);                // lanes 16..31 repeat rows into lanes the MMA does not use
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                const int c0 = 64 * half + 16 * cb;
+                float v[16];
+#pragma unroll
+                for (int x = 0; x < 16; x += 4) {
+                    const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(gr, c0 + x));
+                    const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(gr, c0 + x));
+                    const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
+                    v[x] = -ex2f(gg.x) * __low2float(q2[0]);
+                    v[x + 1] = -ex2f(gg.y) * __high2float(q2[0]);
+                    v[x + 2] = -ex2f(gg.z) * __low2float(q2[1]);
+                    v[x + 3] = -ex2f(gg.w) * __high2float(q2[1]);
+                }
+                tmem_st16(tmem + tlane + 2 * DK + c0, v);
+                const float zero[16] = {};
+                tmem_st16(tmem + tlane + 3 * DK + c0, zero);
+            }
+            tmem_wait_st();
+        }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (un < n_units) {                                      // this unit's k is read: fetch the next k
+        if (un < n_units) {                  // this unit's k, q and alpha are read: fetch the next unit's tiles
             issue_k(un);
             k_issued = true;
+            issue_qa(un);
+            load_pending = true;
         }
 
         // ---- 6. [M | B] = Khat^T [W | Utilde] (M=128) and [PW | P Utilde] = P [W | Utilde] (M=64); N=256, K=64 ----
@@ -717,7 +745,7 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int ks = 0; ks < C / 16; ++ks) {
                     const uint64_t bd = bw + (uint64_t)(ks * 16);
                     umma_f16_1(tmem, ak + (uint64_t)(ks * 16), bd, idesc_f16(128, 2 * DK), ks > 0 ? 1u : 0u);
-                    umma_f16_1(tmem + 2 * DK, ap + (uint64_t)(ks * 16), bd, idesc_f16(64, 2 * DK), ks > 0 ? 1u : 0u);
+                    umma_f16_1(tmem + 2 * DK, ap + (uint64_t)(ks * 16), bd, idesc_f16(64, 2 * DK), 1u);
                 }
                 umma_commit(mbar);
             }
@@ -729,18 +757,13 @@ __global__ void __launch_bounds__(NT, 1)
         float v[32];
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {                         // Q' = Gamma.Q - P W -> rows 0..63 of [Q'; M]
+            // (the accumulator holds P W - Gamma.Q)
             const int c0 = 64 * half + 32 * cb;
             tmem_ld32(tmem + tlane + 2 * DK + c0, v);
             if (lane < 16) {
 #pragma unroll
                 for (int x = 0; x < 32; x += 4) {
-                    const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(mr, c0 + x));
-                    const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(mr, c0 + x));
-                    const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
-                    const float a0 = ex2f(gg.x) * __low2float(q2[0]) - v[x];
-                    const float a1 = ex2f(gg.y) * __high2float(q2[0]) - v[x + 1];
-                    const float a2 = ex2f(gg.z) * __low2float(q2[1]) - v[x + 2];
-                    const float a3 = ex2f(gg.w) * __high2float(q2[1]) - v[x + 3];
+                    const float a0 = -v[x], a1 = -v[x + 1], a2 = -v[x + 2], a3 = -v[x + 3];
                     big |= fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))) > kF16Max;
                     *reinterpret_cast<uint2*>(rec + REC_QM + op_off_h(mr, c0 + x, DK)) =
                         make_uint2(pack_half2(a0, a1), pack_half2(a2, a3));
@@ -752,14 +775,10 @@ __global__ void __launch_bounds__(NT, 1)
         rec_prev = rec;
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();                                         // q and alpha (g) are read
-        if (un < n_units) {                                      // fetch the next unit's q and alpha tiles
-            issue_qa(un);
-            load_pending = true;
-            if (tid < C) {                                       // beta was read in steps 2-3, alpha in step 1
-                sbeta[tid] = beta_next;
-                sasc[tid] = alpha_next;
-            }
+        __syncthreads();
+        if (un < n_units && tid < C) {                           // beta was read in steps 2-3, alpha in step 1
+            sbeta[tid] = beta_next;
+            sasc[tid] = alpha_next;
         }
     }
 
