@@ -49,10 +49,16 @@ DECODE_LABEL = "kda_decode_cols_kernel (fp32 state, two CTAs per state)"
 DECODE_BF16S_LABEL = "kda_decode_bf16s_stream_kernel (bf16-stored state, streamed through shared memory)"
 
 
+PREFILL_2P_MULTI_LABEL = ("kda_chunk_offsets_kernel + kda_order_kernel + kda_prefill_prep_kernel + "
+                          "kda_prefill_chain_kernel (one call, all windows)")
+
+
 def prefill_path(N, dtype, dk):
     """(traffic key, sources, label) of the kernels one kda_prefill call of this shape launches."""
-    if N == 1 and dtype == "bf16" and dk == 128:
-        return "prefill_2p", PREFILL_2P_SRC, PREFILL_2P_LABEL
+    if dtype == "bf16" and dk == 128:
+        if N == 1:
+            return "prefill_2p", PREFILL_2P_SRC, PREFILL_2P_LABEL
+        return "prefill_2p_multi", PREFILL_2P_SRC, PREFILL_2P_MULTI_LABEL
     return "prefill_tc", PREFILL_TC_SRC, PREFILL_TC_LABEL
 METRIC = "KDA prefill tokens/s (H=32,d=128); decode steps/s and state HBM GB/s vs peak"
 # what the bf16 prefill computes in: bf16 q/k/v in HBM, tensor-core products on fp16 and TF32 operands with

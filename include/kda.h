@@ -90,12 +90,14 @@ typedef enum {
 /*
  * Bytes of device workspace kda_prefill needs for this problem (0 is a valid
  * answer).  Pure host function; never fails (returns 0 for invalid sizes).
- *  - Several sequences: the longest-first schedule, 4 bytes per sequence.
- *  - One bf16 sequence with d_k = d_v = 128: the per-chunk records of the
- *    two-phase path (99,072 bytes per chunk and head, up to 1 GiB of them).
- *    kda_prefill also accepts less, down to the size returned for
- *    total_tokens = 64 (one chunk per window); it then walks the sequence in
- *    more windows, with identical results.
+ *  - bf16 with d_k = d_v = 128 (the two-phase path): the per-chunk records
+ *    (99,072 bytes per chunk and head, up to 1 GiB of them), preceded, for
+ *    several sequences, by their chunk offsets and their longest-first order
+ *    (4 (N + 1) and 4 N bytes, each rounded up to 256).  kda_prefill also
+ *    accepts less, down to one chunk's records after those offsets; it then
+ *    walks the chunks in more windows, with identical results.
+ *  - Other several-sequence calls: the longest-first schedule, 4 bytes per
+ *    sequence.
  */
 KDA_API size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                                   int32_t d_v, kda_dtype dt);
@@ -104,7 +106,8 @@ KDA_API size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens
  * Number of kernel launches a kda_prefill call with these arguments makes on the
  * current device (diagnostics: launch budgets, profiler capture ranges), or -1
  * for arguments kda_prefill would reject on the host.  The two-phase path makes
- * two launches per window of chunks, and its window count depends on
+ * two launches per window of chunks (plus two for the chunk offsets and the
+ * order of several sequences), and its window count depends on
  * workspace_bytes and on the device's SM count.  Calls cudaGetDevice and
  * cudaDeviceGetAttribute; enqueues nothing.
  */
@@ -161,9 +164,11 @@ KDA_API kda_status kda_prefill(const void* q, const void* k, const void* v, cons
  * snapshot_every) - 1 (a snapshot at len_n equals that sequence's
  * state_out).
  *
- * single_kernel (nonzero): one bf16 sequence with d_k = d_v = 128 runs the
- * single-kernel tensor-core path (TF32 / bf16 operands) instead of the
- * two-phase path, whose per-chunk records and state operand are fp16.  The
+ * single_kernel (nonzero): bf16 sequences with d_k = d_v = 128 run the
+ * single-kernel tensor-core path (TF32 / bf16 operands, one CTA per sequence,
+ * head and value slice; the workspace then needs only the longest-first order
+ * of several sequences) instead of the two-phase path, whose per-chunk records
+ * and state operand are fp16.  The
  * two-phase path keeps values and states of any magnitude inside fp16's range
  * with exact power-of-two scales (per chunk for v, per chunk and slice for the
  * state); only key-side products far outside O(1), which need keys far from
@@ -297,9 +302,10 @@ KDA_API kda_status kda_decode_step_ex(const void* q, const void* k, const void* 
  * host program that reaches this library only through the C ABI and has no
  * device allocator of its own.  Arguments, results and errors are those of
  * kda_prefill, except:
- *  - The one-sequence bf16 d = 128 case runs the single-kernel chunkwise path
- *    (kda_prefill's two-phase path needs its workspace for per-chunk records);
- *    results agree with kda_prefill within rounding.
+ *  - bf16 d = 128 runs the single-kernel chunkwise path (kda_prefill's
+ *    two-phase path needs its workspace for per-chunk records), as
+ *    kda_prefill_ex with single_kernel set; results agree with kda_prefill
+ *    within rounding.
  *  - The scratch kda_prefill takes as `workspace` for several sequences (their
  *    longest-first order) lives in a fixed static device array of
  *    KDA_NOALLOC_MAX_SEQS int32 entries (64 KiB), which every GPU that loads

@@ -96,8 +96,8 @@ const char* kda_status_string(kda_status s) {
 
 size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                                   int32_t d_v, kda_dtype dt) {
-    if (kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt))
-        return align_up(kda::prefill_2p_workspace(total_tokens, H), 256);   // per-chunk records
+    if (kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt))   // per-chunk records
+        return align_up(kda::prefill_2p_workspace(num_seqs, total_tokens, H), 256);
     if (num_seqs <= 1) return 0;
     // longest-first schedule of the sequences
     return align_up(sizeof(int32_t) * (size_t)num_seqs, 256);
@@ -109,14 +109,15 @@ int64_t kda_prefill_launch_count(int32_t num_seqs, int64_t total_tokens, int32_t
     if ((dt != KDA_DTYPE_F32 && dt != KDA_DTYPE_BF16) || !supported_head(d_k, d_v)) return -1;
     if (num_seqs == 0) return total_tokens == 0 ? 0 : -1;
     if (kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt)) {
-        if (workspace_bytes < kda::prefill_2p_min_workspace(H)) return -1;
+        if (workspace_bytes < kda::prefill_2p_min_workspace(num_seqs, H)) return -1;
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return -1;
-        const int64_t chunks = (total_tokens + kda::kChunk - 1) / kda::kChunk;
-        const kda::WindowPlan plan = kda::prefill_2p_plan(chunks, H, workspace_bytes, sms);
-        return 2 * ((chunks + plan.window - 1) / plan.window);
+        const int64_t chunks = kda::prefill_2p_max_chunks(num_seqs, total_tokens);
+        const kda::WindowPlan plan = kda::prefill_2p_plan(num_seqs, chunks, H, workspace_bytes, sms);
+        // several sequences: chunk offsets and longest-first order first
+        return (num_seqs > 1 ? 2 : 0) + 2 * ((chunks + plan.window - 1) / plan.window);
     }
     return num_seqs > 1 ? 2 : 1;                      // longest-first order, then the chunkwise kernel
 }
@@ -162,8 +163,9 @@ kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const flo
     const bool two_phase = kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt) &&
                            !(options && options->single_kernel);
     // the two-phase path takes any workspace down to one chunk's records and uses more windows
-    const size_t need = two_phase ? kda::prefill_2p_min_workspace(H)
-                                  : kda_prefill_workspace_size(num_seqs, total_tokens, H, d_k, d_v, dt);
+    const size_t need = two_phase ? kda::prefill_2p_min_workspace(num_seqs, H)
+                          : num_seqs > 1 ? align_up(sizeof(int32_t) * (size_t)num_seqs, 256)   // longest-first order
+                                         : 0;
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
         return KDA_ERR_WORKSPACE;
 
@@ -345,7 +347,10 @@ BwdLayout bwd_layout(int32_t N, int64_t T, int32_t H, int32_t d, kda_dtype dt) {
     L.gb = at; at = align_up(at + (size_t)(T / kda::kChunk) * H * dd, 256);
     L.o = at; at = align_up(at + (size_t)T * H * d * esize, 256);
     L.st = at; at = align_up(at + (size_t)N * H * dd, 256);
-    L.fwd = at; at = align_up(at + kda_prefill_workspace_size(N, T, H, d, d, dt), 256);
+    // the forward recompute: one sequence may take the two-phase path (records), several the single-kernel
+    // path (the longest-first order only)
+    L.fwd = at;
+    at = align_up(at + (N == 1 ? kda_prefill_workspace_size(1, T, H, d, d, dt) : align_up(4 * (size_t)N, 256)), 256);
     // per-CTA scratch of the chunk pass: the matrix form's matrices at d = 128, the token walk's states else
     L.scratch = at; at = align_up(at + ctas * (d == 128 ? kda::kBwdMatScratchBytes : (kda::kChunk - 1) * dd), 256);
     L.total = at;
@@ -403,6 +408,7 @@ kda_status kda_prefill_backward(const void* q, const void* k, const void* v, con
     opts.snapshot_every = kda::kChunk;
     opts.snapshots = snaps;
     opts.snapshot_offsets = off;
+    opts.single_kernel = num_seqs > 1 ? 1 : 0;        // several sequences: the single-kernel recompute
     const kda_status fs = kda_prefill_ex(q, k, v, beta, alpha, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, dt,
                                          scale, state_in, reinterpret_cast<float*>(ws + L.st), ws + L.o, ws + L.fwd,
                                          L.scratch - L.fwd, stream, &opts);
@@ -423,9 +429,9 @@ kda_status kda_prefill_backward(const void* q, const void* k, const void* v, con
         return KDA_ERR_CUDA;
     // one bf16 d=128 sequence whose forward recompute ran as one window: every chunk's record (Q', M,
     // Gamma_C) is still in the workspace, and the state-gradient chain walks chunks instead of tokens
-    if (kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt) && total_tokens > 0) {
+    if (num_seqs == 1 && kda::prefill_2p_supported(num_seqs, total_tokens, H, d_k, d_v, dt) && total_tokens > 0) {
         const int64_t chunks = (total_tokens + kda::kChunk - 1) / kda::kChunk;
-        const kda::WindowPlan plan = kda::prefill_2p_plan(chunks, H, L.scratch - L.fwd, sms);
+        const kda::WindowPlan plan = kda::prefill_2p_plan(1, chunks, H, L.scratch - L.fwd, sms);
         if (plan.window >= chunks) p.records = ws + L.fwd;
     }
     const int64_t units = bwd_max_units(num_seqs, total_tokens, H);

@@ -107,16 +107,17 @@ cudaError_t launch_prefill_cc(const PrefillParams& p, kda_dtype dt, cudaStream_t
 cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s);
 bool prefill_tc_supported(const PrefillParams& p, kda_dtype dt);
 int prefill_tc_slices(int32_t num_seqs, int32_t H, int32_t dv);
-// Two-phase single-sequence prefill (bf16, d_k = d_v = 128): per-chunk records in the workspace.
+// Two-phase prefill (bf16, d_k = d_v = 128): per-chunk records in the workspace, then the state chain.
 bool prefill_2p_supported(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
                           kda_dtype dt);
-size_t prefill_2p_workspace(int64_t total_tokens, int32_t H);   // recommended bytes (<= 512 MiB)
+size_t prefill_2p_workspace(int32_t num_seqs, int64_t total_tokens, int32_t H);   // recommended bytes
 struct WindowPlan {
     int64_t window;   // chunks per window
     int buffers;      // 2: phase 1 of the next window overlaps phase 2 of this one (side stream)
 };
-WindowPlan prefill_2p_plan(int64_t chunks, int32_t H, size_t workspace_bytes, int sms);
-size_t prefill_2p_min_workspace(int32_t H);                     // bytes for one chunk per window
+int64_t prefill_2p_max_chunks(int32_t num_seqs, int64_t total_tokens);
+WindowPlan prefill_2p_plan(int32_t num_seqs, int64_t chunks, int32_t H, size_t workspace_bytes, int sms);
+size_t prefill_2p_min_workspace(int32_t num_seqs, int32_t H);   // bytes for one chunk per window
 cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t workspace_bytes, cudaStream_t s);
 cudaError_t launch_order(const int32_t* cu_seqlens, int32_t num_seqs, int32_t* order, cudaStream_t s);
 cudaError_t launch_bwd_offsets(const int32_t* cu, int32_t N, int32_t T, int32_t* off, int32_t* choff, unsigned* err,

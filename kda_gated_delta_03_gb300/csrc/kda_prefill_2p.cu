@@ -135,27 +135,75 @@ __device__ __forceinline__ bool valid_single_sequence(const PrefillParams& p) {
     return p.num_seqs == 1 && p.cu_seqlens[0] == 0 && p.cu_seqlens[1] == p.total_tokens;
 }
 
+// Chunks of all sequences are numbered sequence by sequence: sequence n owns chunks [choff[n], choff[n+1])
+// (choff from kda_chunk_offsets_kernel; nullptr for one sequence, whose chunks are simply t / 64).
+// The sequence that owns chunk gc (the last n with choff[n] <= gc, which skips empty sequences).
+__device__ __forceinline__ int chunk_seq(const int32_t* choff, int32_t N, int64_t gc) {
+    int lo = 0, hi = N;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (choff[mid] <= gc) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+// First token of chunk gc and the end token of its sequence.
+__device__ __forceinline__ void chunk_span(const PrefillParams& p, const int32_t* choff, int64_t gc, int32_t& t0,
+                                           int32_t& t_end) {
+    if (!choff) {
+        t0 = (int32_t)(gc * C);
+        t_end = p.total_tokens;
+        return;
+    }
+    const int n = chunk_seq(choff, p.num_seqs, gc);
+    t0 = p.cu_seqlens[n] + (int32_t)(gc - choff[n]) * C;
+    t_end = p.cu_seqlens[n + 1];
+}
+
+// Chunk offsets of the sequences (chunks of 64 tokens, the last one partial) and the check of cu_seqlens;
+// with an inconsistent cu_seqlens every sequence counts as empty (nothing is computed, KDA_DEVERR_CU_SEQLENS).
+__global__ void kda_chunk_offsets_kernel(const int32_t* cu, int32_t N, int32_t T, int32_t* choff, unsigned* err) {
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    bool ok = cu[0] == 0 && cu[N] == T;
+    for (int n = 0; n < N && ok; ++n) ok = cu[n + 1] >= cu[n];
+    int32_t acc = 0;
+    choff[0] = 0;
+    for (int n = 0; n < N; ++n) {
+        acc += ok ? (cu[n + 1] - cu[n] + C - 1) / C : 0;
+        choff[n + 1] = acc;
+    }
+    if (!ok) atomicOr(err, KDA_DEVERR_CU_SEQLENS);
+}
+
 // ============================================================================================
 // Phase 1: persistent CTAs over the units (chunk-major: unit = window chunk * H + head) of the window
 // starting at chunk c_begin.  The raw tiles of a CTA's next unit are loaded while it stores the
 // current unit's record.
 // ============================================================================================
+// MULTI: several sequences (chunk offsets in choff); otherwise one sequence, whose chunk arithmetic is then
+// compiled without the lookups.
+template <bool MULTI>
 __global__ void __launch_bounds__(NT, 1)
     kda_prefill_prep_kernel(PrefillParams p, const __grid_constant__ PrepMaps maps, unsigned char* records,
-                            int c_begin, int n_units) {
+                            int c_begin, int n_units, const int32_t* choff_arg) {
+    const int32_t* choff = MULTI ? choff_arg : nullptr;
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const int quad = warp & 3, half = warp >> 2;
     const int ch = tid & (DK - 1), rh = tid >> 7;
     const int H = p.H;
-    if (!valid_single_sequence(p)) {
+    if (!choff && !valid_single_sequence(p)) {
         if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
         return;
     }
     if (saddr(sm) & 1023u) {
         if (tid == 0) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
         return;
+    }
+    {                                                // units that exist: chunks [c_begin, all chunks) x heads
+        const int64_t nc = choff ? (int64_t)choff[p.num_seqs] : ((int64_t)p.total_tokens + C - 1) / C;
+        const int64_t have = (nc - c_begin) * H;
+        if (have < n_units) n_units = have < 0 ? 0 : (int)have;
     }
 
     const __nv_bfloat16* vraw = reinterpret_cast<const __nv_bfloat16*>(sm + P_OFF_V);
@@ -212,7 +260,8 @@ __global__ void __launch_bounds__(NT, 1)
     // raw tiles of unit u by TMA (v with one 128-column box), in three groups
     auto unit_rows = [&](int u, int& hu, int32_t& tu) {
         hu = u % H;
-        tu = (int32_t)(c_begin + u / H) * C;
+        int32_t te;
+        chunk_span(p, choff, (int64_t)c_begin + u / H, tu, te);
     };
     auto issue_v = [&](int u) {                      // arms vkbar for v and k together
         if (tid == 32) {
@@ -300,10 +349,11 @@ __global__ void __launch_bounds__(NT, 1)
         issue_v(blockIdx.x);
         issue_k(blockIdx.x);
         issue_qa(blockIdx.x);
-        const int32_t tn = (int32_t)(c_begin + (int)blockIdx.x / H) * C;
+        int32_t tn, tn_end;
+        chunk_span(p, choff, (int64_t)c_begin + (int)blockIdx.x / H, tn, tn_end);
         if (tid < C) {
             const int64_t row = (int64_t)(tn + tid) * H + (int)blockIdx.x % H;
-            const bool in = tn + tid < p.total_tokens;
+            const bool in = tn + tid < tn_end;
             sbeta[tid] = in ? p.beta[row] : 0.f;
             sasc[tid] = per_head && in ? p.alpha[row] : 1.f;
         }
@@ -324,9 +374,9 @@ __global__ void __launch_bounds__(NT, 1)
 #endif
 
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const int cw = u / H;
-        const int32_t t0 = (int32_t)(c_begin + cw) * C;
-        const int L = min(C, p.total_tokens - t0);
+        int32_t t0, t_end;                              // the chunk's first token and its sequence's end
+        chunk_span(p, choff, (int64_t)c_begin + u / H, t0, t_end);
+        const int L = min(C, t_end - t0);
         unsigned char* rec = records + (size_t)u * REC_BYTES;
         const int un = u + (int)gridDim.x;                       // this CTA's next unit
         if (!mbar_wait(vkbar, vkph) || !mbar_wait(lbar, lph)) {
@@ -340,10 +390,11 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         if (*s_abort) break;
         if (tid < C && un < n_units) {                  // the next unit's beta (and alpha), used at this unit's end
-            const int32_t tn = (int32_t)(c_begin + un / H) * C;
+            int32_t tn, tn_end;
+            chunk_span(p, choff, (int64_t)c_begin + un / H, tn, tn_end);
             const int64_t row = (int64_t)(tn + tid) * H + un % H;
-            beta_next = tn + tid < p.total_tokens ? p.beta[row] : 0.f;
-            alpha_next = per_head && tn + tid < p.total_tokens ? p.alpha[row] : 1.f;
+            beta_next = tn + tid < tn_end ? p.beta[row] : 0.f;
+            alpha_next = per_head && tn + tid < tn_end ? p.alpha[row] : 1.f;
         }
         if (L < C) {                                    // rows past the sequence end read as zero
             for (int e = tid; e < (C - L) * 16; e += NT) {
@@ -800,7 +851,12 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ============================================================================================
-// Phase 2: one CTA per (head, 32 value columns), chunks [c_begin, c_begin + n_chunks) in order.
+// Phase 2: one CTA per (sequence, head, 32 value columns); it walks that sequence's chunks inside the window
+// [c_begin, c_begin + n_chunks) in order, from state_in where the sequence starts in the window and from
+// the state carried in state_out otherwise, and leaves its state in state_out.  With several sequences
+// (choff set) blockIdx enumerates (order[i], head, slice), longest sequences first; a CTA whose sequence
+// has no chunk in the window exits at once (a zero-length sequence copies state_in to state_out in the
+// first window).
 //
 // Warps 0-7 hold the state (thread = one key channel, 16 value columns) and run the fp32 update;
 // warp 8 issues the products, warp 9 the record loads; warps 12-13 (TMEM lanes 0..63: the chunk's 64
@@ -816,25 +872,51 @@ __global__ void __launch_bounds__(NT, 1)
 // can run at most one phase ahead of each of its waiters.  Warps 10-11 exist only so that the output
 // warps sit on TMEM lanes 0..63 (warp w reaches lanes 32 (w mod 4) .. +31).
 // ============================================================================================
+template <bool MULTI>
 __global__ void __launch_bounds__(C_NT, 1)
-    kda_prefill_chain_kernel(PrefillParams p, const unsigned char* records, int c_begin, int n_chunks,
-                             const float* state_in) {
+    kda_prefill_chain_kernel(PrefillParams p, const unsigned char* records, int c_begin, int n_window,
+                             const int32_t* choff_arg, const int32_t* order) {
+    const int32_t* choff = MULTI ? choff_arg : nullptr;
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = (warp >> 2) & 1;
     constexpr int CPT = SNV / 2;                      // value columns per epilogue thread
     const int H = p.H;
-    const int h = blockIdx.x / SLICES, slice = blockIdx.x % SLICES, j0 = slice * SNV;
-    if (!valid_single_sequence(p)) {
+    const int seq_i = blockIdx.x / (H * SLICES), hs = blockIdx.x % (H * SLICES);
+    const int h = hs / SLICES, slice = hs % SLICES, j0 = slice * SNV;
+    if (!choff && !valid_single_sequence(p)) {
         if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
         return;
     }
+    // this CTA's sequence, its tokens [s0, s0 + T) and its chunks inside the window [g0, g0 + n_chunks)
+    const int n = choff ? (order ? order[seq_i] : seq_i) : 0;
+    const int32_t s0 = choff ? p.cu_seqlens[n] : 0;
+    const int32_t T = choff ? (choff[n + 1] > choff[n] ? p.cu_seqlens[n + 1] - s0 : 0) : p.total_tokens;
+    const int64_t cseq = choff ? choff[n] : 0, cseq_end = choff ? choff[n + 1] : ((int64_t)T + C - 1) / C;
+    const int64_t g0 = cseq > c_begin ? cseq : c_begin;
+    const int64_t g1 = cseq_end < (int64_t)c_begin + n_window ? cseq_end : (int64_t)c_begin + n_window;
+    const int n_chunks = g1 > g0 ? (int)(g1 - g0) : 0;
+    const int64_t state_base = ((int64_t)n * H + h) * DK * (int64_t)p.dv;   // this (sequence, head)'s state
+    if (g0 == cseq && h == 0 && slice == 0 && tid == 0 && (n_chunks > 0 || c_begin == 0) &&
+        snapshot_offsets_bad(p, n, T))
+        atomicOr(p.err, KDA_DEVERR_SNAPSHOTS);
+    if (n_chunks == 0) {
+        if (cseq == cseq_end && c_begin == 0 && tid < 256) {      // an empty sequence: state_out = state_in
+            for (int e = tid; e < DK * SNV / 4; e += 256) {
+                const int64_t at = state_base + (int64_t)(e / (SNV / 4)) * p.dv + j0 + 4 * (e % (SNV / 4));
+                const float4 v4 = p.state_in ? *reinterpret_cast<const float4*>(p.state_in + at)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4*>(p.state_out + at) = v4;
+            }
+        }
+        return;
+    }
+    // the state this window starts from: state_in where the sequence starts here, else the carried state
+    const float* state_in = g0 == cseq ? p.state_in : p.state_out;
     if (saddr(sm) & 1023u) {
         if (tid == 0) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
         return;
     }
-    const int32_t T = p.total_tokens;
-    if (blockIdx.x == 0 && tid == 0 && c_begin == 0 && snapshot_offsets_bad(p, 0, T)) atomicOr(p.err, KDA_DEVERR_SNAPSHOTS);
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(p.o);
     unsigned char* misc = sm + C_OFF_MISC;
     volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 100);
@@ -871,7 +953,7 @@ __global__ void __launch_bounds__(C_NT, 1)
     if (warp < 8) {
         uint32_t m = 0u;
         if (state_in) {
-            const float* src = state_in + (((int64_t)h) * DK + 32 * quad + lane) * (int64_t)p.dv + j0 + (SNV / 2) * half;
+            const float* src = state_in + state_base + (int64_t)(32 * quad + lane) * p.dv + j0 + (SNV / 2) * half;
 #pragma unroll
             for (int j = 0; j < SNV / 2; j += 4) {
                 const float4 v4 = *reinterpret_cast<const float4*>(src + j);
@@ -955,7 +1037,7 @@ __global__ void __launch_bounds__(C_NT, 1)
             if (lane == 0) {
                 const uint32_t lb = lbar + 8 * (ci & 1);
                 mbar_expect_tx(lb, QM_BYTES);
-                bulk_g2s(saddr(sm + (ci & 1) * QM_BYTES), records + (size_t)(ci * H + h) * REC_BYTES + REC_QM,
+                bulk_g2s(saddr(sm + (ci & 1) * QM_BYTES), records + (size_t)((g0 - c_begin + ci) * H + h) * REC_BYTES + REC_QM,
                          QM_BYTES, lb);
             }
         };
@@ -978,7 +1060,7 @@ __global__ void __launch_bounds__(C_NT, 1)
         uint2 oq[SNV / 4];                             // raw fp16, converted where used
         int eo = 0;                                    // the chunk's value scale exponent
         auto fetch_o = [&](int ci) {                  // the chunk's P Utilde for this row and slice
-            const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
+            const unsigned char* rec = records + (size_t)((g0 - c_begin + ci) * H + h) * REC_BYTES;
 #pragma unroll
             for (int m = 0; m < SNV / 4; ++m)
                 oq[m] = __ldg(reinterpret_cast<const uint2*>(rec + REC_O + (((j0 + 4 * m) >> 2) * C + orow) * 8));
@@ -996,9 +1078,9 @@ __global__ void __launch_bounds__(C_NT, 1)
             tmem_ld32(tmem + tlane + TM_O + SNV * b, d);
             tc_fence_before();
             mbar_arrive(ofree + 8 * b);
-            const int32_t t0 = (c_begin + ci) * C;
+            const int32_t t0 = (int32_t)(g0 - cseq + ci) * C;   // within the sequence
             if (orow < min(C, T - t0)) {
-                __nv_bfloat16* dst = go + ((int64_t)(t0 + orow) * H + h) * p.dv + j0;
+                __nv_bfloat16* dst = go + ((int64_t)(s0 + t0 + orow) * H + h) * p.dv + j0;
                 const float fd = exp2i(E), fo = exp2i(eo);      // 1 unless values or the state are large
 #pragma unroll
                 for (int x = 0; x < SNV; x += 8) {
@@ -1017,7 +1099,7 @@ __global__ void __launch_bounds__(C_NT, 1)
         const uint32_t tlane = (uint32_t)(quad * 32) << 16;
         const int srow = 32 * quad + lane;            // state row (key channel)
         const int jc = j0 + CPT * half;               // first value column of this thread
-        const int64_t state_off = (((int64_t)h) * DK + srow) * (int64_t)p.dv + jc;
+        const int64_t state_off = state_base + (int64_t)srow * p.dv + jc;
         float S[CPT];                                 // the state divided by 2^E
         int E = E0;
         {
@@ -1060,7 +1142,7 @@ __global__ void __launch_bounds__(C_NT, 1)
         float gamC = 0.f;
         int eb = 0;                                    // the chunk's value scale exponent
         auto fetch_b = [&](int ci) {
-            const unsigned char* rec = records + (size_t)(ci * H + h) * REC_BYTES;
+            const unsigned char* rec = records + (size_t)((g0 - c_begin + ci) * H + h) * REC_BYTES;
 #pragma unroll
             for (int m = 0; m < CPT / 4; ++m)
                 bq[m] = __ldg(reinterpret_cast<const uint2*>(rec + REC_B + (((jc + 4 * m) >> 2) * DK + srow) * 8));
@@ -1070,7 +1152,7 @@ __global__ void __launch_bounds__(C_NT, 1)
         write_state_operand(0, absmax());
         if (n_chunks > 0) fetch_b(0);
         // the next snapshot point after the window start (never reached when there are no snapshots)
-        int32_t snap_next = p.snap_every > 0 ? (c_begin * C / p.snap_every + 1) * p.snap_every : -1;
+        int32_t snap_next = p.snap_every > 0 ? ((int32_t)(g0 - cseq) * C / p.snap_every + 1) * p.snap_every : -1;
         bool ok = true;
         for (int ci = 0; ci < n_chunks; ++ci) {
             const int b = ci & 1;
@@ -1115,7 +1197,7 @@ __global__ void __launch_bounds__(C_NT, 1)
                 for (int j = 0; j < CPT; ++j) S[j] *= r;
                 E = E_next;
             }
-            const int32_t t_done = min(T, (c_begin + ci + 1) * C);   // tokens of the sequence now in S
+            const int32_t t_done = min(T, (int32_t)(g0 - cseq + ci + 1) * C);   // tokens of the sequence now in S
             if (ci + 1 < n_chunks) {
                 // the operand buffer of S_{c+1} was last read by the products of chunk c-1; they were issued
                 // before chunk c's state products, whose commit (dbar, waited above) tracks every earlier
@@ -1130,7 +1212,7 @@ __global__ void __launch_bounds__(C_NT, 1)
             // a snapshot of the state after this chunk, if due (off the sequential path: after the operand
             // of the next chunk is out; the check is a compare against the next snapshot point)
             if (t_done == snap_next) {
-                const int64_t slot = snapshot_slot(p, 0, t_done, T);
+                const int64_t slot = snapshot_slot(p, n, t_done, T);
                 if (slot >= 0) {
                     float* dst = p.snapshots + ((slot * H + h) * DK + srow) * (int64_t)p.dv + jc;
                     const float f = exp2i(E);
@@ -1363,28 +1445,42 @@ cudaError_t side_stream(int dev, SideStream** out) {
 
 bool prefill_2p_supported(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
                           kda_dtype dt) {
-    return num_seqs == 1 && total_tokens > 0 && dt == KDA_DTYPE_BF16 && d_k == DK && d_v == DK && H > 0;
+    return num_seqs >= 1 && total_tokens > 0 && dt == KDA_DTYPE_BF16 && d_k == DK && d_v == DK && H > 0;
 }
 
-size_t prefill_2p_min_workspace(int32_t H) { return (size_t)H * REC_BYTES; }
+// Workspace of the two-phase path: with several sequences, their chunk offsets (N + 1 int32) and their
+// longest-first order (N int32), each 256-byte aligned; then the records of one window (or of two).
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+size_t prefill_2p_header(int32_t num_seqs) {
+    return num_seqs > 1 ? align256(4 * ((size_t)num_seqs + 1)) + align256(4 * (size_t)num_seqs) : 0;
+}
+int64_t prefill_2p_max_chunks(int32_t num_seqs, int64_t total_tokens) {   // chunks of all sequences, at most
+    return num_seqs > 1 ? total_tokens / C + num_seqs : (total_tokens + C - 1) / C;
+}
 
-size_t prefill_2p_workspace(int64_t total_tokens, int32_t H) {
-    const int64_t chunks = (total_tokens + C - 1) / C;
+size_t prefill_2p_min_workspace(int32_t num_seqs, int32_t H) {
+    return prefill_2p_header(num_seqs) + (size_t)H * REC_BYTES;
+}
+
+size_t prefill_2p_workspace(int32_t num_seqs, int64_t total_tokens, int32_t H) {
+    const int64_t chunks = prefill_2p_max_chunks(num_seqs, total_tokens);
     int64_t cap = (int64_t)(kOneWindowBudget / ((size_t)H * REC_BYTES));
-    if (cap < 2 * buffer_chunks(H)) cap = 2 * buffer_chunks(H);
-    return (size_t)(chunks < cap ? chunks : cap) * H * REC_BYTES;
+    if (num_seqs == 1 && cap < 2 * buffer_chunks(H)) cap = 2 * buffer_chunks(H);
+    return prefill_2p_header(num_seqs) + (size_t)(chunks < cap ? chunks : cap) * H * REC_BYTES;
 }
 
-WindowPlan prefill_2p_plan(int64_t chunks, int32_t H, size_t workspace_bytes, int sms) {
-    const int64_t cap = (int64_t)(workspace_bytes / prefill_2p_min_workspace(H));   // records that fit
+WindowPlan prefill_2p_plan(int32_t num_seqs, int64_t chunks, int32_t H, size_t workspace_bytes, int sms) {
+    const size_t hdr = prefill_2p_header(num_seqs);
+    const int64_t cap = workspace_bytes > hdr ? (int64_t)((workspace_bytes - hdr) / ((size_t)H * REC_BYTES)) : 0;
     const int64_t one = buffer_chunks(H);
-    const bool overlap_ok = 2 * H * SLICES <= sms;   // the chain leaves at least half the SMs to phase 1
+    const bool overlap_ok = num_seqs == 1 && 2 * H * SLICES <= sms;   // the chain leaves half the SMs to phase 1
     WindowPlan w;
     if (overlap_ok && chunks > one && cap >= 2) {
-        // few heads: phase 1 of the next window runs beside the chain of this one, on double buffers
+        // one sequence, few heads: phase 1 of the next window runs beside the chain of this one, on double
+        // buffers
         w.window = cap / 2 < one ? cap / 2 : one; w.buffers = 2;
     } else {
-        // many heads: the chain occupies most SMs, so the windows run back to back, as few as fit
+        // otherwise the windows run back to back, as few as fit
         w.window = chunks < cap ? chunks : cap; w.buffers = 1;
     }
     if (w.window < 1) w.window = 1;
@@ -1408,18 +1504,33 @@ cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t wo
                       CU_TENSOR_MAP_SWIZZLE_128B)) ||
         !encode_rows(enc, &maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, 2, p.dv, p.H, T, DK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(kda_prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+    const bool multi = p.num_seqs > 1;
+    cudaError_t e = cudaFuncSetAttribute(multi ? kda_prefill_prep_kernel<true> : kda_prefill_prep_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kda_prefill_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C_SMEM);
+    e = cudaFuncSetAttribute(multi ? kda_prefill_chain_kernel<true> : kda_prefill_chain_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C_SMEM);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const int64_t chunks = (T + C - 1) / C;
-    const WindowPlan plan = prefill_2p_plan(chunks, p.H, workspace_bytes, sms);
-    if ((size_t)plan.window * plan.buffers * prefill_2p_min_workspace(p.H) > workspace_bytes) return cudaErrorInvalidValue;
-    const int chain_ctas = p.H * SLICES;
-    const size_t buf_bytes = (size_t)plan.window * prefill_2p_min_workspace(p.H);
+    const int N = p.num_seqs;
+    const size_t hdr = prefill_2p_header(N);
+    const int64_t chunks = prefill_2p_max_chunks(N, T);
+    const WindowPlan plan = prefill_2p_plan(N, chunks, p.H, workspace_bytes, sms);
+    const size_t buf_bytes = (size_t)plan.window * p.H * REC_BYTES;
+    if (hdr + buf_bytes * plan.buffers > workspace_bytes) return cudaErrorInvalidValue;
+    // several sequences: their chunk offsets and their longest-first order head the workspace
+    int32_t* choff = nullptr;
+    int32_t* order = nullptr;
+    if (N > 1) {
+        choff = static_cast<int32_t*>(workspace);
+        order = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + align256(4 * ((size_t)N + 1)));
+        kda_chunk_offsets_kernel<<<1, 32, 0, s>>>(p.cu_seqlens, N, T, choff, p.err);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_order(p.cu_seqlens, N, order, s)) != cudaSuccess) return e;
+    }
+    const int chain_ctas = N * p.H * SLICES;
     SideStream* ss = nullptr;
     std::unique_lock<std::mutex> enqueue;             // concurrent callers must not interleave event records
     if (plan.buffers == 2) {
@@ -1433,20 +1544,27 @@ cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t wo
         const int64_t n = chunks - c0 < plan.window ? chunks - c0 : plan.window;
         const int units = (int)(n * p.H);
         const int buf = w % plan.buffers;
-        unsigned char* rec = static_cast<unsigned char*>(workspace) + buf * buf_bytes;
+        unsigned char* rec = static_cast<unsigned char*>(workspace) + hdr + buf * buf_bytes;
         cudaStream_t ps = ss ? ss->stream : s;
         // phase 1 shares the GPU with the previous window's chain when overlapped
-        int grid = (ss && w > 0) ? sms - chain_ctas : sms;
+        int grid = (ss && w > 0) ? sms - p.H * SLICES : sms;
         if (grid > units) grid = units;
         if (ss && w >= 2 && (e = cudaStreamWaitEvent(ps, ss->chain_done[buf], 0)) != cudaSuccess) return e;
-        kda_prefill_prep_kernel<<<(unsigned)grid, NT, P_SMEM, ps>>>(p, maps, rec, (int)c0, units);
+        if (multi)
+            kda_prefill_prep_kernel<true><<<(unsigned)grid, NT, P_SMEM, ps>>>(p, maps, rec, (int)c0, units, choff);
+        else
+            kda_prefill_prep_kernel<false><<<(unsigned)grid, NT, P_SMEM, ps>>>(p, maps, rec, (int)c0, units, nullptr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (ss) {
             if ((e = cudaEventRecord(ss->prep_done[buf], ps)) != cudaSuccess) return e;
             if ((e = cudaStreamWaitEvent(s, ss->prep_done[buf], 0)) != cudaSuccess) return e;
         }
-        kda_prefill_chain_kernel<<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n,
-                                                                            c0 == 0 ? p.state_in : p.state_out);
+        if (multi)
+            kda_prefill_chain_kernel<true><<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n, choff,
+                                                                                    order);
+        else
+            kda_prefill_chain_kernel<false><<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n,
+                                                                                     nullptr, nullptr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (ss && (e = cudaEventRecord(ss->chain_done[buf], s)) != cudaSuccess) return e;
     }

@@ -60,8 +60,16 @@ def test_workspace_size(lib):
     assert lib.kda_prefill_workspace_size(1, 65, 4, 128, 128, 1) == (2 * 4 * 99072 + 255) // 256 * 256
     assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 0) == 0      # fp32: single-kernel path
     assert lib.kda_prefill_workspace_size(1, 8192, 32, 64, 64, 1) == 0
-    assert lib.kda_prefill_workspace_size(64, 300000, 32, 128, 128, 1) == 256
-    assert lib.kda_prefill_workspace_size(65, 300000, 32, 128, 128, 1) == 512
+    # several bf16 d=128 sequences: their chunk offsets and longest-first order, then the records of at most
+    # T // 64 + N chunks (each sequence's last chunk may be partial), at most 1 GiB of them
+    up = lambda x: (x + 255) // 256 * 256
+    hdr = lambda n: up(4 * (n + 1)) + up(4 * n)
+    assert lib.kda_prefill_workspace_size(64, 300000, 32, 128, 128, 1) == up(hdr(64) + 338 * 32 * 99072)
+    assert lib.kda_prefill_workspace_size(65, 300000, 32, 128, 128, 1) == up(hdr(65) + 338 * 32 * 99072)
+    assert lib.kda_prefill_workspace_size(3, 700, 2, 128, 128, 1) == up(hdr(3) + (700 // 64 + 3) * 2 * 99072)
+    # other sequence batches: the longest-first order only
+    assert lib.kda_prefill_workspace_size(64, 300000, 32, 64, 64, 1) == 256
+    assert lib.kda_prefill_workspace_size(65, 300000, 32, 128, 128, 0) == 512
 
 
 def test_backward_workspace_size(lib):
@@ -75,8 +83,9 @@ def test_backward_workspace_size(lib):
     def expected(N, T, H, d, dt):
         dd, es = d * d * 4, 2 if dt == 1 else 4
         ctas = min((T // 64 + N) * H, 160)
-        parts = [(N + 1) * 8, (T // 64) * H * dd, (T // 64) * H * dd, T * H * d * es, N * H * dd,
-                 lib.kda_prefill_workspace_size(N, T, H, d, d, dt),
+        # the recompute: one sequence as kda_prefill, several on the single-kernel path (their order only)
+        fwd = lib.kda_prefill_workspace_size(N, T, H, d, d, dt) if N == 1 else 4 * N
+        parts = [(N + 1) * 8, (T // 64) * H * dd, (T // 64) * H * dd, T * H * d * es, N * H * dd, fwd,
                  ctas * (10 * 64 * 128 * 4 if d == 128 else 63 * dd)]
         return sum(up(x) for x in parts)
 

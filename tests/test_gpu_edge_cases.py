@@ -1,9 +1,11 @@
 """Edge cases of the method on every prefill path at d = 128, against the float64 oracle.
 
-Each case runs through the four kernels a kda_prefill call can take at d_k = d_v = 128:
+Each case runs through the paths a kda_prefill call can take at d_k = d_v = 128:
   - "two_phase":     one bf16 sequence (per-chunk records, then the state chain);
   - "single_kernel": one bf16 sequence with the single_kernel option (tcgen05 chunk kernel);
-  - "varlen":        several bf16 sequences (the same tcgen05 chunk kernel, longest-first order);
+  - "varlen":        several bf16 sequences (records of every sequence's chunks, one chain per sequence);
+  - "varlen_single": several bf16 sequences with the single_kernel option (the tcgen05 chunk kernel,
+                     longest-first order);
   - "fp32":          float32 inputs (the FFMA chunk kernel, 1e-4 tolerance).
 
 The cases ("Kimi K3, explained", section "The math" and "Check yourself"):
@@ -28,7 +30,8 @@ from kda_testutil import TOL, rel_frob, to_dev
 
 pytestmark = pytest.mark.gpu
 
-PATHS = ["two_phase", "single_kernel", "varlen", "fp32"]
+PATHS = ["two_phase", "single_kernel", "varlen", "varlen_single", "fp32"]
+SINGLE = ("single_kernel", "varlen_single")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -57,7 +60,7 @@ def path_inputs(path, seqlens, H, seed, state="randn"):
     """Seeded inputs for one path: a single sequence for the one-sequence paths, the same tokens split
     into several sequences for "varlen"."""
     dtype = "f32" if path == "fp32" else "bf16"
-    if path == "varlen":
+    if path.startswith("varlen"):
         T = sum(seqlens)
         cuts = [T // 3, T // 3 + 1, T - T // 3 - (T // 3 + 1)]
         seqlens = [c for c in cuts if c > 0] + [0]
@@ -90,13 +93,13 @@ def test_worked_overwrite_example_at_d128(path, golden_dir):
     a = np.zeros(d)
     b = np.zeros(d)
     a[:4], b[:4] = g["a"], g["b"]
-    reps = 2 if path == "varlen" else 1                   # two identical sequences for the varlen kernel
+    reps = 2 if path.startswith("varlen") else 1          # two identical sequences for the batch paths
     q = np.stack([key, key] * reps)[:, None, :].copy()
     v = np.stack([I.to_storage(a, dtype), I.to_storage(b, dtype)] * reps)[:, None, :].copy()
     inp = dict(q=q, k=q.copy(), v=v, beta=np.ones((2 * reps, 1), np.float32),
                alpha=np.ones((2 * reps, 1, d), np.float32), cu_seqlens=I.cu_seqlens_of([2] * reps),
                state_in=None, dtype=dtype, H=1, dk=d, dv=d)
-    o, st = run_gpu(inp, single_kernel=path == "single_kernel")
+    o, st = run_gpu(inp, single_kernel=path in SINGLE)
     for r in range(reps):
         np.testing.assert_allclose(o[2 * r, 0, :4], g["a"], rtol=0, atol=1e-6)
         np.testing.assert_allclose(o[2 * r + 1, 0, :4], g["delta_read_after_both_writes"], rtol=0, atol=1e-6)
@@ -121,7 +124,7 @@ def test_unit_key_overwrites_any_state(path):
             inp["k"][t, h] = e
             inp["q"][t, h] = e
             inp["beta"][t, h] = 1.0
-    o, st = run_gpu(inp, single_kernel=path == "single_kernel")
+    o, st = run_gpu(inp, single_kernel=path in SINGLE)
     v = I.storage_to_f64(inp["v"], dtype)
     tol = 1e-4 if dtype == "f32" else 1e-2            # bf16: o is rounded to bf16 once
     for t in rows:
@@ -138,7 +141,7 @@ def test_beta_exactly_zero_and_one(path):
     u = rng.random(inp["beta"].shape)
     inp["beta"][u < 1 / 3] = 0.0
     inp["beta"][u > 2 / 3] = 1.0
-    o, st = run_gpu(inp, single_kernel=path == "single_kernel")
+    o, st = run_gpu(inp, single_kernel=path in SINGLE)
     check_oracle(inp, o, st)
 
 
@@ -152,5 +155,5 @@ def test_decay_below_the_clamp(path):
     mask = rng.random(inp["alpha"].shape) < 0.05
     inp["alpha"][mask] = 1e-8
     inp["alpha"][[5, 64, 130, 400]] = 1e-8
-    o, st = run_gpu(inp, single_kernel=path == "single_kernel")
+    o, st = run_gpu(inp, single_kernel=path in SINGLE)
     check_oracle(inp, o, st)

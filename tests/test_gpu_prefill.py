@@ -65,6 +65,61 @@ def test_many_units_wide_slices():
     check(inp)
 
 
+@pytest.mark.parametrize("seqlens,H", [([int(x) for x in np.random.default_rng(77).integers(1, 200, size=40)], 4),
+                                         ([1, 63, 64, 65, 0, 200], 3)])
+def test_single_kernel_path_for_several_sequences(seqlens, H):
+    """The single-kernel option runs several bf16 d=128 sequences on the tcgen05 chunk kernel (64-column
+    slices once sequences x heads >= 148, 32-column slices below), matching the oracle."""
+    import kda_gated_delta_03_gb300 as kda
+    inp = I.prefill_inputs(seqlens, H, 128, 128, "bf16", 78, decay="slow", state="randn")
+    args = [to_dev(inp[n], n in ("q", "k", "v")) for n in ("q", "k", "v", "beta", "alpha", "cu_seqlens")]
+    o, st = kda.kda_prefill(*args, to_dev(inp["state_in"]), single_kernel=True)
+    torch.cuda.synchronize()
+    o_ref, st_ref = O.prefill(inp)
+    assert rel_frob(o.double().cpu().numpy(), o_ref) <= 3e-3
+    assert rel_frob(st.double().cpu().numpy(), st_ref) <= 3e-3
+
+
+def test_records_path_for_several_sequences():
+    """Several bf16 d=128 sequences take the record-based path: every sequence's chunks get their records,
+    then one chain CTA per (sequence, head, value slice) walks its own chunks.  Each sequence's o and state
+    equal, bit for bit, a one-sequence call on it; a workspace of only a few chunks (many windows, sequences
+    split across windows, their state carried through state_out, also in place) gives identical results;
+    and the oracle agrees."""
+    import kda_gated_delta_03_gb300 as kda
+    seqlens = [300, 0, 65, 1, 700, 64, 129]
+    H = 2
+    inp = I.prefill_inputs(seqlens, H, 128, 128, "bf16", 41, decay="slow", state="randn")
+    cu = inp["cu_seqlens"]
+    args = [to_dev(inp[n], n in ("q", "k", "v")) for n in ("q", "k", "v", "beta", "alpha", "cu_seqlens")]
+    s0 = to_dev(inp["state_in"])
+    o, st = kda.kda_prefill(*args, s0)
+    torch.cuda.synchronize()
+    o_ref, st_ref = O.prefill(inp)
+    assert rel_frob(o.double().cpu().numpy(), o_ref) <= 3e-3
+    assert rel_frob(st.double().cpu().numpy(), st_ref) <= 3e-3
+    for n in range(len(seqlens)):
+        one = _sub_batch(inp, [n])
+        o1, st1 = kda.kda_prefill(*[to_dev(one[m], m in ("q", "k", "v")) for m in ("q", "k", "v", "beta", "alpha",
+                                                                                    "cu_seqlens")],
+                                  to_dev(one["state_in"]))
+        torch.cuda.synchronize()
+        assert torch.equal(o1.view(torch.int16), o[cu[n]:cu[n + 1]].view(torch.int16)), n
+        assert torch.equal(st1, st[n:n + 1]), n
+    up = lambda x: (x + 255) // 256 * 256
+    hdr = up(4 * (len(seqlens) + 1)) + up(4 * len(seqlens))
+    for chunks in (1, 3):
+        ws = torch.empty(hdr + chunks * H * 99072, dtype=torch.uint8, device="cuda:0")
+        o2, st2 = kda.kda_prefill(*args, s0, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(o2.view(torch.int16), o.view(torch.int16)) and torch.equal(st2, st), chunks
+    st3 = s0.clone()
+    ws = torch.empty(hdr + 2 * H * 99072, dtype=torch.uint8, device="cuda:0")
+    o3, _ = kda.kda_prefill(*args, st3, state_out=st3, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o3.view(torch.int16), o.view(torch.int16)) and torch.equal(st3, st)
+
+
 def test_scale_and_zero_state():
     inp = I.prefill_inputs([130, 7], 2, 64, 64, "f32", 8, decay="slow")
     check(inp, scale=0.125)

@@ -35,10 +35,10 @@ def _device_inputs(inp):
 
 @pytest.mark.gpu
 def test_noalloc_matches_prefill_on_two_calls_in_a_row():
-    """Several sequences: the no-alloc call runs the same kernels as kda_prefill; only the home of the
-    longest-first sequence order differs.  So its results must be bit-identical, on two calls in a row with
-    different sequence counts (an order left stale by the first call would skip or repeat sequences), and
-    within tolerance of the float64 oracle."""
+    """Several sequences: the no-alloc call runs the same kernels as kda_prefill with the single-kernel
+    option (no records); only the home of the longest-first sequence order differs.  So its results must be
+    bit-identical, on two calls in a row with different sequence counts (an order left stale by the first
+    call would skip or repeat sequences), and within tolerance of the float64 oracle."""
     build.build()
     binding.load()
     cases = [
@@ -58,8 +58,10 @@ def test_noalloc_matches_prefill_on_two_calls_in_a_row():
                                     o=o, state_out=st)
     torch.cuda.synchronize()
     for inp, d, (o, st) in zip(cases, devs, outs):
+        # bf16 d=128 batches take kda_prefill's record-based path by default; the single-kernel option selects
+        # the path the no-alloc call runs
         o_ref, st_ref = binding.kda_prefill(d["q"], d["k"], d["v"], d["beta"], d["alpha"], d["cu_seqlens"],
-                                            d["state_in"])
+                                            d["state_in"], single_kernel=inp["dtype"] == "bf16")
         torch.cuda.synchronize()
         assert torch.equal(o.view(torch.int16) if o.dtype == torch.bfloat16 else o,
                            o_ref.view(torch.int16) if o_ref.dtype == torch.bfloat16 else o_ref)
