@@ -13,7 +13,7 @@
 // operand.  Phase 2 walks the chunks in order, one CTA per (head, 32 value columns), bulk-loading each
 // record one chunk ahead; per chunk it issues a single batch of tensor-core products,
 //
-//   M S  and  [Q'; M_top] S              tcgen05 kind::f16 (fp16 record and state operands), M=128, N=32, K=128
+//   M S (M=128)  and  Q' S (M=64)       tcgen05 kind::f16 (fp16 record and state operands), N=32, K=128
 //
 // followed by the fp32 update S <- Gamma_C . S + B - M S and o = scale (Q' S + P Utilde).  Folding W
 // into M and Q' doubles phase 1's work on W but leaves one round trip through the tensor core on the
@@ -103,7 +103,7 @@ constexpr int C_OFF_MISC = C_OFF_S + 2 * SOP_BYTES;
 constexpr int CM_SMX0 = 128, CM_EBAR = 160, CM_ERING = 192, CM_SLOT = 208;
 constexpr int C_SMEM = C_OFF_MISC + 272;
 constexpr int C_NT = NT + 6 * 32;                  // 8 state warps, the MMA-issue warp, the record-loader warp,
-                                                   // 2 idle warps, 2 output warps (on TMEM lanes 0..63)
+                                                   // 4 output warps (one per TMEM lane quadrant)
 static_assert(C_OFF_S % 1024 == 0 && C_SMEM <= 232448, "phase-2 shared memory");
 
 struct PrepMaps {
@@ -859,18 +859,18 @@ __global__ void __launch_bounds__(NT, 1)
 // first window).
 //
 // Warps 0-7 hold the state (thread = one key channel, 16 value columns) and run the fp32 update;
-// warp 8 issues the products, warp 9 the record loads; warps 12-13 (TMEM lanes 0..63: the chunk's 64
-// output rows) run the output epilogue.  Per chunk c:
+// warp 8 issues the products, warp 9 the record loads; warps 10-13 run the output epilogue (the output
+// product is M=64, whose row 16 q + i sits at lane i of TMEM lane quadrant q, and warp w reaches quadrant
+// w mod 4).  Per chunk c:
 //   warp 8:      wait record c, sbar ("S_c written") and ofree (output of c-2 read); issue M S_c -> dbar,
-//                then [Q'; M_top] S_c -> obar (issued while the state warps update S)
+//                then Q' S_c -> obar (issued while the state warps update S)
 //   warp 9:      wait obar, load record c+2 into the freed buffer
 //   warps 0-7:   wait dbar; S_{c+1} = Gamma_C S_c + B - M S_c; write the S^T operand of c+1; arrive on sbar
-//   warps 12-13: wait obar; o = scale ([Q'; M_top] S_c + P Utilde) for rows 0..63; arrive on ofree
+//   warps 10-13: wait obar; o = scale (Q' S_c + P Utilde) for rows 0..63; arrive on ofree
 // so the output products and epilogue of one chunk overlap the state products of the next, and the
 // state warps' proxy fence never waits on output traffic.  The S^T operand and the output accumulator
 // are double-buffered; M S uses one accumulator (it is read before the arrival on sbar).  Every barrier
-// can run at most one phase ahead of each of its waiters.  Warps 10-11 exist only so that the output
-// warps sit on TMEM lanes 0..63 (warp w reaches lanes 32 (w mod 4) .. +31).
+// can run at most one phase ahead of each of its waiters.
 // ============================================================================================
 template <bool MULTI>
 __global__ void __launch_bounds__(C_NT, 1)
@@ -927,7 +927,7 @@ __global__ void __launch_bounds__(C_NT, 1)
     const uint32_t ebar = saddr(misc + CM_EBAR);
     volatile int* e_ring = reinterpret_cast<volatile int*>(misc + CM_ERING);
     uint32_t* smax = reinterpret_cast<uint32_t*>(misc + CM_SLOT);   // read only after an mbarrier acquire
-    constexpr uint32_t TM_S = 0, TM_O = 32;           // M S accumulator; two [Q'; M_top] S accumulators
+    constexpr uint32_t TM_S = 0, TM_O = 32;           // M S accumulator; two Q' S accumulators
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -937,7 +937,7 @@ __global__ void __launch_bounds__(C_NT, 1)
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sbar), "r"(NT) : "memory");
         for (int b = 0; b < 2; ++b)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(ofree + 8 * b), "r"(64) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(ofree + 8 * b), "r"(128) : "memory");
         for (int b = 0; b < 4; ++b)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(ebar + 8 * b) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -997,7 +997,7 @@ __global__ void __launch_bounds__(C_NT, 1)
 
     const uint32_t sop0 = saddr(sm + C_OFF_S);
     if (warp == 8) {
-        // ---------------- products: M S_c (sequential path), then [Q'; M_top] S_c ----------------
+        // ---------------- products: M S_c (sequential path), then Q' S_c ----------------
         const uint64_t a_s0 = op_desc_h(saddr(sm) + C * DK * 2, DK), a_o0 = op_desc_h(saddr(sm), DK);
         const uint64_t b_s0 = desc_sw128(sop0);
         int issued = 0;                               // chunks whose products were issued
@@ -1022,7 +1022,7 @@ __global__ void __launch_bounds__(C_NT, 1)
 #pragma unroll
                 for (int ks = 0; ks < DK / 16; ++ks)
                     umma_f16_1(tmem + TM_O + SNV * b, ao + (uint64_t)(ks * 16),
-                               bs + (uint64_t)(((ks >> 2) * (SNV * 128) + (ks & 3) * 32) >> 4), idesc_f16(128, SNV),
+                               bs + (uint64_t)(((ks >> 2) * (SNV * 128) + (ks & 3) * 32) >> 4), idesc_f16(64, SNV),
                                ks > 0 ? 1u : 0u);
                 umma_commit(obar + 8 * b);
             }
@@ -1053,17 +1053,18 @@ __global__ void __launch_bounds__(C_NT, 1)
         // never leave copies in flight: every issued load completes (bounded waits)
         for (int ci = loaded - 2 < 0 ? 0 : loaded - 2; ci < loaded; ++ci)
             mbar_wait(lbar + 8 * (ci & 1), (uint32_t)(ci >> 1) & 1u);
-    } else if (warp >= 12) {
-        // ---------------- output warps: rows 0..63 of chunk c ----------------
-        const int orow = 32 * (warp - 12) + lane;
-        const uint32_t tlane = (uint32_t)(32 * (warp - 12)) << 16;
+    } else if (warp >= 10) {
+        // ---------------- output warps: rows 0..63 of chunk c (M=64: row 16 q + i at lane i of quadrant q) ----------------
+        const int orow = 16 * quad + (lane & 15);
+        const uint32_t tlane = (uint32_t)(32 * quad) << 16;
         uint2 oq[SNV / 4];                             // raw fp16, converted where used
         int eo = 0;                                    // the chunk's value scale exponent
         auto fetch_o = [&](int ci) {                  // the chunk's P Utilde for this row and slice
             const unsigned char* rec = records + (size_t)((g0 - c_begin + ci) * H + h) * REC_BYTES;
 #pragma unroll
             for (int m = 0; m < SNV / 4; ++m)
-                oq[m] = __ldg(reinterpret_cast<const uint2*>(rec + REC_O + (((j0 + 4 * m) >> 2) * C + orow) * 8));
+                oq[m] = lane < 16 ? __ldg(reinterpret_cast<const uint2*>(rec + REC_O + (((j0 + 4 * m) >> 2) * C + orow) * 8))
+                                  : make_uint2(0u, 0u);
             eo = __ldg(reinterpret_cast<const int*>(rec + REC_E));
         };
         if (n_chunks > 0) fetch_o(0);
@@ -1079,7 +1080,7 @@ __global__ void __launch_bounds__(C_NT, 1)
             tc_fence_before();
             mbar_arrive(ofree + 8 * b);
             const int32_t t0 = (int32_t)(g0 - cseq + ci) * C;   // within the sequence
-            if (orow < min(C, T - t0)) {
+            if (lane < 16 && orow < min(C, T - t0)) {
                 __nv_bfloat16* dst = go + ((int64_t)(s0 + t0 + orow) * H + h) * p.dv + j0;
                 const float fd = exp2i(E), fo = exp2i(eo);      // 1 unless values or the state are large
 #pragma unroll
