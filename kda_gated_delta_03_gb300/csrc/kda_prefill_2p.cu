@@ -1,4 +1,4 @@
-// Two-phase chunkwise prefill for a single long sequence: bf16 q/k/v, d_k = d_v = 128.
+// Two-phase chunkwise prefill: bf16 q/k/v, d_k = d_v = 128, one sequence or several.
 //
 // The chunk algebra is that of the single-kernel path ("Kimi K3, explained", section "Training in
 // chunks": WY form inside a chunk, only the state carried across chunks).  With U = Utilde - W S the
@@ -20,7 +20,10 @@
 // sequential path instead of two, and no U tile to build between them.
 //
 // Long sequences are processed in windows of chunks so that the workspace stays bounded; the state
-// passes between windows through state_out.  Every wait is bounded (KDA_DEVERR_TIMEOUT on expiry).
+// passes between windows through state_out.  Several sequences number their chunks one after the other
+// (chunk offsets computed on the device from cu_seqlens), phase 1 runs over every chunk of the window
+// whatever its sequence, and phase 2 runs one CTA per (sequence, head, slice), longest sequences first.
+// Every wait is bounded (KDA_DEVERR_TIMEOUT on expiry).
 
 #include "kda_tc_util.cuh"
 
