@@ -69,6 +69,7 @@ __device__ __forceinline__ int scale_exp_f32_at(uint32_t mag_bits, int E) {
     return e >= kScaleFromExp ? min(e, 126) : 0;
 }
 constexpr int SNV = 32;            // value columns per chain CTA
+constexpr int kPrefetchAhead = 4;  // chunks between the chain's L2 prefetch of a record's B and its use
 constexpr int SLICES = DK / SNV;
 constexpr size_t kBufBudget = size_t(128) << 20;      // record bytes per buffer of the overlapped schedule
                                                       // (about 170 chunks at H = 8: short enough that the
@@ -76,6 +77,9 @@ constexpr size_t kBufBudget = size_t(128) << 20;      // record bytes per buffer
                                                       // short; long enough to amortise the launches)
 constexpr size_t kOneWindowBudget = size_t(1) << 30;  // record bytes of the workspace, at most
 static_assert(QM_BYTES == REC_B && REC_B + DK * DK * 2 == REC_O && REC_O + C * DK * 2 == REC_G, "record layout");
+static_assert(REC_B % 16 == 0 && REC_O % 16 == 0 && REC_G % 16 == 0 && (REC_BYTES - REC_G) % 16 == 0 &&
+                  REC_BYTES % 256 == 0 && (SNV / 4) * C * 8 % 16 == 0,
+              "bulk copies and L2 prefetches of record pieces: 16-byte aligned, multiples of 16 bytes");
 
 // ---- phase 1 shared memory ----
 constexpr int P_OFF_V = OFF_V;                     // v tile, dense 64 x 128 bf16
@@ -117,6 +121,27 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(mbar)
                  : "memory");
+}
+
+// an L2 prefetch of global bytes (16-byte aligned, a multiple of 16 bytes); nothing to wait for
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// mbar_wait for a waiter off the critical path: it sleeps between polls, leaving issue slots to the warps
+// that share its scheduler (bounded like mbar_wait)
+__device__ __forceinline__ bool mbar_wait_lazy(uint32_t mbar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (true) {
+        uint32_t done;
+        asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(done)
+                     : "r"(mbar), "r"(parity)
+                     : "memory");
+        if (done) return true;
+        if (clock64() - t0 > kWaitLimit) return false;
+        __nanosleep(200);
+    }
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
@@ -867,7 +892,7 @@ __global__ void __launch_bounds__(NT, 1)
 // w mod 4).  Per chunk c:
 //   warp 8:      wait record c, sbar ("S_c written") and ofree (output of c-2 read); issue M S_c -> dbar,
 //                then Q' S_c -> obar (issued while the state warps update S)
-//   warp 9:      wait obar, load record c+2 into the freed buffer
+//   warp 9:      wait obar, load record c+2 into the freed buffer; prefetch B and P Utilde of c+4 into L2
 //   warps 0-7:   wait dbar; S_{c+1} = Gamma_C S_c + B - M S_c; write the S^T operand of c+1; arrive on sbar
 //   warps 10-13: wait obar; o = scale (Q' S_c + P Utilde) for rows 0..63; arrive on ofree
 // so the output products and epilogue of one chunk overlap the state products of the next, and the
@@ -1044,13 +1069,26 @@ __global__ void __launch_bounds__(C_NT, 1)
                          QM_BYTES, lb);
             }
         };
+        // this slice's B and P Utilde and the chunk's Gamma_C, pulled into L2 kPrefetchAhead chunks before the
+        // state and output warps read them (the records were written long before and are no longer in L2;
+        // a load from DRAM one chunk ahead was still in flight at the state update)
+        auto prefetch = [&](int ci) {
+            if (lane == 0 && ci < n_chunks) {
+                const unsigned char* rec = records + (size_t)((g0 - c_begin + ci) * H + h) * REC_BYTES;
+                prefetch_l2(rec + REC_B + (size_t)(j0 >> 2) * DK * 8, (SNV / 4) * DK * 8);
+                prefetch_l2(rec + REC_O + (size_t)(j0 >> 2) * C * 8, (SNV / 4) * C * 8);
+                prefetch_l2(rec + REC_G, REC_BYTES - REC_G);
+            }
+        };
+        for (int c = 1; c < kPrefetchAhead; ++c) prefetch(c);
         if (n_chunks > 0) load(0);
         if (n_chunks > 1) load(1);
         int loaded = n_chunks < 2 ? n_chunks : 2;
         for (int ci = 0; ci + 2 < n_chunks; ++ci) {
             if (*s_abort) break;
-            if (!mbar_wait(obar + 8 * (ci & 1), (uint32_t)(ci >> 1) & 1u)) { fail(); break; }
+            if (!mbar_wait_lazy(obar + 8 * (ci & 1), (uint32_t)(ci >> 1) & 1u)) { fail(); break; }
             load(ci + 2);
+            prefetch(ci + kPrefetchAhead);
             loaded = ci + 3;
         }
         // never leave copies in flight: every issued load completes (bounded waits)
@@ -1120,11 +1158,11 @@ __global__ void __launch_bounds__(C_NT, 1)
         // computed where S is) for the choice of the next scale
         auto write_state_operand = [&](int c, float m) {
             unsigned char* sop = sm + C_OFF_S + (c & 1) * SOP_BYTES;
+            const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));   // its latency under the stores
 #pragma unroll
             for (int j = 0; j < CPT; ++j)
                 *reinterpret_cast<__half*>(sop + sw128_off_h(CPT * half + j, srow, SNV)) = __float2half_rn(S[j]);
             big |= m > kF16Max;
-            const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
             if (lane == 0) smax[(c & 1) * 8 + warp] = mw;
             fence_async_smem();
             tc_fence_before();
