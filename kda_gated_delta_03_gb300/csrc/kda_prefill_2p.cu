@@ -335,10 +335,12 @@ __global__ void __launch_bounds__(NT, 1)
             tmem_ld32(tmem + tlane + (piece >= 2 ? DK : 0) + c0, v);
             if (piece < 2) {
 #pragma unroll
-                for (int x = 0; x < 32; x += 4) {
-                    big |= fmaxf(fmaxf(fabsf(v[x]), fabsf(v[x + 1])), fmaxf(fabsf(v[x + 2]), fabsf(v[x + 3]))) > kF16Max;
-                    *reinterpret_cast<uint2*>(rec_prev + REC_QM + op_off_h(C + mi, c0 + x, DK)) =
-                        make_uint2(pack_half2(v[x], v[x + 1]), pack_half2(v[x + 2], v[x + 3]));
+                for (int x = 0; x < 32; x += 8) {                // one 16-byte core-matrix row per store
+                    big |= fmaxf(fmaxf(fmaxf(fabsf(v[x]), fabsf(v[x + 1])), fmaxf(fabsf(v[x + 2]), fabsf(v[x + 3]))),
+                                 fmaxf(fmaxf(fabsf(v[x + 4]), fabsf(v[x + 5])), fmaxf(fabsf(v[x + 6]), fabsf(v[x + 7])))) > kF16Max;
+                    *reinterpret_cast<uint4*>(rec_prev + REC_QM + op_off_h(C + mi, c0 + x, DK)) =
+                        make_uint4(pack_half2(v[x], v[x + 1]), pack_half2(v[x + 2], v[x + 3]),
+                                   pack_half2(v[x + 4], v[x + 5]), pack_half2(v[x + 6], v[x + 7]));
                 }
             } else {
 #pragma unroll
@@ -698,30 +700,39 @@ __global__ void __launch_bounds__(NT, 1)
         }
         // T' = T Diag(beta) -> fp16 operand (M=64, K=64); the operands of steps 4 and 6 are fp16 (the same
         // 10-bit significand as TF32; their values are O(1) for unit-norm keys, and v and T' are checked)
-        for (int e = tid; e < C * 16; e += NT) {
-            const int r = ((e >> 7) << 3) | (e & 7), m0 = 4 * ((e >> 3) & 15);
-            float4 v;
-            v.x = m0 + 0 <= r ? Tb[r * AT_LD + m0 + 0] * sbeta[m0 + 0] : 0.f;
-            v.y = m0 + 1 <= r ? Tb[r * AT_LD + m0 + 1] * sbeta[m0 + 1] : 0.f;
-            v.z = m0 + 2 <= r ? Tb[r * AT_LD + m0 + 2] * sbeta[m0 + 2] : 0.f;
-            v.w = m0 + 3 <= r ? Tb[r * AT_LD + m0 + 3] * sbeta[m0 + 3] : 0.f;
-            big |= fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) > kF16Max;
-            *reinterpret_cast<uint2*>(X + PS_OPT + op_off_h(r, m0, C)) =
-                make_uint2(pack_half2(v.x, v.y), pack_half2(v.z, v.w));
+        for (int e = tid; e < C * 8; e += NT) {                    // row r, columns m0 .. m0 + 7 per thread
+            const int r = (e & 7) | (((e >> 6) & 7) << 3), m0 = 8 * ((e >> 3) & 7);
+            const float4 t0 = *reinterpret_cast<const float4*>(Tb + r * AT_LD + m0);
+            const float4 t1 = *reinterpret_cast<const float4*>(Tb + r * AT_LD + m0 + 4);
+            const float4 b0 = *reinterpret_cast<const float4*>(sbeta + m0);
+            const float4 b1 = *reinterpret_cast<const float4*>(sbeta + m0 + 4);
+            float v[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w, t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
+#pragma unroll
+            for (int x = 0; x < 8; ++x) v[x] = m0 + x <= r ? v[x] : 0.f;
+            big |= fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                         fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7])))) > kF16Max;
+            *reinterpret_cast<uint4*>(X + PS_OPT + op_off_h(r, m0, C)) =
+                make_uint4(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]), pack_half2(v[6], v[7]));
         }
         // [Gamma.K | V]^T -> fp16 operand (N=256 rows, K=64 time), v scaled by 2^-e_c
-        for (int e = tid; e < DK * 16; e += NT) {
-            const int i = e & (DK - 1), m0 = 4 * (e >> 7);
-            float gg[4], kk4[4];
+        // 8 time rows of channel i per thread, one 16-byte core-matrix row per store: a warp's four 8-row
+        // groups lie 1 KiB apart (the same banks), so 8-byte stores took as many wavefronts for half the bytes
+        for (int e = tid; e < DK * 8; e += NT) {
+            const int i = e & (DK - 1), m0 = 8 * (e >> 7);
+            float gk[8], vv[8];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) { gg[x] = Gat(m0 + x, i); kk4[x] = kat(m0 + x, i); }
-            *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(i, m0, C)) =
-                make_uint2(pack_half2(ex2f(gg[0]) * kk4[0], ex2f(gg[1]) * kk4[1]),
-                           pack_half2(ex2f(gg[2]) * kk4[2], ex2f(gg[3]) * kk4[3]));
-            const float v0 = vscale * bf(vraw + (m0 + 0) * DK + i), v1 = vscale * bf(vraw + (m0 + 1) * DK + i);
-            const float v2 = vscale * bf(vraw + (m0 + 2) * DK + i), v3 = vscale * bf(vraw + (m0 + 3) * DK + i);
-            big |= fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))) > kF16Max;
-            *reinterpret_cast<uint2*>(X + PS_KV + op_off_h(DK + i, m0, C)) = make_uint2(pack_half2(v0, v1), pack_half2(v2, v3));
+            for (int x = 0; x < 8; ++x) {
+                gk[x] = ex2f(Gat(m0 + x, i)) * kat(m0 + x, i);
+                vv[x] = vscale * bf(vraw + (m0 + x) * DK + i);
+            }
+            *reinterpret_cast<uint4*>(X + PS_KV + op_off_h(i, m0, C)) =
+                make_uint4(pack_half2(gk[0], gk[1]), pack_half2(gk[2], gk[3]), pack_half2(gk[4], gk[5]),
+                           pack_half2(gk[6], gk[7]));
+            big |= fmaxf(fmaxf(fmaxf(fabsf(vv[0]), fabsf(vv[1])), fmaxf(fabsf(vv[2]), fabsf(vv[3]))),
+                         fmaxf(fmaxf(fabsf(vv[4]), fabsf(vv[5])), fmaxf(fabsf(vv[6]), fabsf(vv[7])))) > kF16Max;
+            *reinterpret_cast<uint4*>(X + PS_KV + op_off_h(DK + i, m0, C)) =
+                make_uint4(pack_half2(vv[0], vv[1]), pack_half2(vv[2], vv[3]), pack_half2(vv[4], vv[5]),
+                           pack_half2(vv[6], vv[7]));
         }
         fence_async_smem();
         tc_fence_before();
@@ -759,22 +770,24 @@ __global__ void __launch_bounds__(NT, 1)
             for (int cb = 0; cb < 2; ++cb) {
                 tmem_ld32(tmem + tlane + TM_W + C * half + 32 * cb, v);
 #pragma unroll
-                for (int x = 0; x < 32; x += 4) {
-                    big |= fmaxf(fmaxf(fabsf(v[x]), fabsf(v[x + 1])), fmaxf(fabsf(v[x + 2]), fabsf(v[x + 3]))) > kF16Max;
-                    *reinterpret_cast<uint2*>(opWU + op_off_h(n, 32 * cb + x, C)) =
-                        make_uint2(pack_half2(v[x], v[x + 1]), pack_half2(v[x + 2], v[x + 3]));
+                for (int x = 0; x < 32; x += 8) {
+                    big |= fmaxf(fmaxf(fmaxf(fabsf(v[x]), fabsf(v[x + 1])), fmaxf(fabsf(v[x + 2]), fabsf(v[x + 3]))),
+                                 fmaxf(fmaxf(fabsf(v[x + 4]), fabsf(v[x + 5])), fmaxf(fabsf(v[x + 6]), fabsf(v[x + 7])))) > kF16Max;
+                    *reinterpret_cast<uint4*>(opWU + op_off_h(n, 32 * cb + x, C)) =
+                        make_uint4(pack_half2(v[x], v[x + 1]), pack_half2(v[x + 2], v[x + 3]),
+                                   pack_half2(v[x + 4], v[x + 5]), pack_half2(v[x + 6], v[x + 7]));
                 }
             }
         }
-        for (int e = tid; e < DK * 16; e += NT) {
-            const int i = e & (DK - 1), s0 = 4 * (e >> 7);
+        for (int e = tid; e < DK * 8; e += NT) {                  // 8 time rows of channel i per thread
+            const int i = e & (DK - 1), s0 = 8 * (e >> 7);
             const float gl = Gat(C - 1, i);
-            float gg[4], kk4[4];
+            float kh[8];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) { gg[x] = Gat(s0 + x, i); kk4[x] = kat(s0 + x, i); }
-            *reinterpret_cast<uint2*>(opKH + op_off_h(i, s0, C)) =
-                make_uint2(pack_half2(ex2f(gl - gg[0]) * kk4[0], ex2f(gl - gg[1]) * kk4[1]),
-                           pack_half2(ex2f(gl - gg[2]) * kk4[2], ex2f(gl - gg[3]) * kk4[3]));
+            for (int x = 0; x < 8; ++x) kh[x] = ex2f(gl - Gat(s0 + x, i)) * kat(s0 + x, i);
+            *reinterpret_cast<uint4*>(opKH + op_off_h(i, s0, C)) =
+                make_uint4(pack_half2(kh[0], kh[1]), pack_half2(kh[2], kh[3]), pack_half2(kh[4], kh[5]),
+                           pack_half2(kh[6], kh[7]));
         }
         drain(4);                                       // the last piece, before step 6 writes its columns
         rec_prev = nullptr;
@@ -841,11 +854,12 @@ __global__ void __launch_bounds__(NT, 1)
             tmem_ld32(tmem + tlane + 2 * DK + c0, v);
             if (lane < 16) {
 #pragma unroll
-                for (int x = 0; x < 32; x += 4) {
-                    const float a0 = -v[x], a1 = -v[x + 1], a2 = -v[x + 2], a3 = -v[x + 3];
-                    big |= fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))) > kF16Max;
-                    *reinterpret_cast<uint2*>(rec + REC_QM + op_off_h(mr, c0 + x, DK)) =
-                        make_uint2(pack_half2(a0, a1), pack_half2(a2, a3));
+                for (int x = 0; x < 32; x += 8) {                // one 16-byte core-matrix row per store
+                    big |= fmaxf(fmaxf(fmaxf(fabsf(v[x]), fabsf(v[x + 1])), fmaxf(fabsf(v[x + 2]), fabsf(v[x + 3]))),
+                                 fmaxf(fmaxf(fabsf(v[x + 4]), fabsf(v[x + 5])), fmaxf(fabsf(v[x + 6]), fabsf(v[x + 7])))) > kF16Max;
+                    *reinterpret_cast<uint4*>(rec + REC_QM + op_off_h(mr, c0 + x, DK)) =
+                        make_uint4(pack_half2(-v[x], -v[x + 1]), pack_half2(-v[x + 2], -v[x + 3]),
+                                   pack_half2(-v[x + 4], -v[x + 5]), pack_half2(-v[x + 6], -v[x + 7]));
                 }
             }
         }
