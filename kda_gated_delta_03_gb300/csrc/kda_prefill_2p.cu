@@ -101,7 +101,7 @@ static_assert(PS_KH + DK * C * 4 <= PS_P, "phase-1 fold operands");
 static_assert(P_SMEM <= 232448, "phase-1 shared memory");
 
 // ---- phase 2 shared memory and threads ----
-constexpr int SOP_BYTES = SNV * DK * 2;            // S^T operand: fp16 32 x 128, 128-byte swizzle
+constexpr int SOP_BYTES = SNV * DK * 2;            // S^T operand: fp16 NV x 128 (NV <= 32), 128-byte swizzle
 constexpr int C_OFF_S = 2 * QM_BYTES;              // two record buffers, then two S^T operands
 constexpr int C_OFF_MISC = C_OFF_S + 2 * SOP_BYTES;
 // misc: 0 lbar[2], 16 dbar[2], 32 obar[2], 48 sbar, 64 ofree[2], 96 TMEM address, 100 abort flag,
@@ -914,7 +914,7 @@ __global__ void __launch_bounds__(NT, 1)
 // are double-buffered; M S uses one accumulator (it is read before the arrival on sbar).  Every barrier
 // can run at most one phase ahead of each of its waiters.
 // ============================================================================================
-template <bool MULTI>
+template <bool MULTI, int NV>
 __global__ void __launch_bounds__(C_NT, 1)
     kda_prefill_chain_kernel(PrefillParams p, const unsigned char* records, int c_begin, int n_window,
                              const int32_t* choff_arg, const int32_t* order) {
@@ -922,10 +922,12 @@ __global__ void __launch_bounds__(C_NT, 1)
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = (warp >> 2) & 1;
-    constexpr int CPT = SNV / 2;                      // value columns per epilogue thread
+    static_assert(NV == 16 || NV == 32, "16 or 32 value columns per CTA");
+    constexpr int CPT = NV / 2;                       // value columns per state thread
+    constexpr int NSL = DK / NV;                      // slices of a head
     const int H = p.H;
-    const int seq_i = blockIdx.x / (H * SLICES), hs = blockIdx.x % (H * SLICES);
-    const int h = hs / SLICES, slice = hs % SLICES, j0 = slice * SNV;
+    const int seq_i = blockIdx.x / (H * NSL), hs = blockIdx.x % (H * NSL);
+    const int h = hs / NSL, slice = hs % NSL, j0 = slice * NV;
     if (!choff && !valid_single_sequence(p)) {
         if (tid == 0) atomicOr(p.err, KDA_DEVERR_CU_SEQLENS);
         return;
@@ -944,8 +946,8 @@ __global__ void __launch_bounds__(C_NT, 1)
         atomicOr(p.err, KDA_DEVERR_SNAPSHOTS);
     if (n_chunks == 0) {
         if (cseq == cseq_end && c_begin == 0 && tid < 256) {      // an empty sequence: state_out = state_in
-            for (int e = tid; e < DK * SNV / 4; e += 256) {
-                const int64_t at = state_base + (int64_t)(e / (SNV / 4)) * p.dv + j0 + 4 * (e % (SNV / 4));
+            for (int e = tid; e < DK * NV / 4; e += 256) {
+                const int64_t at = state_base + (int64_t)(e / (NV / 4)) * p.dv + j0 + 4 * (e % (NV / 4));
                 const float4 v4 = p.state_in ? *reinterpret_cast<const float4*>(p.state_in + at)
                                              : make_float4(0.f, 0.f, 0.f, 0.f);
                 *reinterpret_cast<float4*>(p.state_out + at) = v4;
@@ -995,9 +997,9 @@ __global__ void __launch_bounds__(C_NT, 1)
     if (warp < 8) {
         uint32_t m = 0u;
         if (state_in) {
-            const float* src = state_in + state_base + (int64_t)(32 * quad + lane) * p.dv + j0 + (SNV / 2) * half;
+            const float* src = state_in + state_base + (int64_t)(32 * quad + lane) * p.dv + j0 + CPT * half;
 #pragma unroll
-            for (int j = 0; j < SNV / 2; j += 4) {
+            for (int j = 0; j < CPT; j += 4) {
                 const float4 v4 = *reinterpret_cast<const float4*>(src + j);
                 m = max(m, max(max(__float_as_uint(fabsf(v4.x)), __float_as_uint(fabsf(v4.y))),
                                max(__float_as_uint(fabsf(v4.z)), __float_as_uint(fabsf(v4.w)))));
@@ -1058,13 +1060,13 @@ __global__ void __launch_bounds__(C_NT, 1)
 #pragma unroll
                 for (int ks = 0; ks < DK / 16; ++ks)           // 16 fp16 = 32 bytes of K per step
                     umma_f16_1(tmem + TM_S, as + (uint64_t)(ks * 16),
-                               bs + (uint64_t)(((ks >> 2) * (SNV * 128) + (ks & 3) * 32) >> 4), idesc_f16(128, SNV),
+                               bs + (uint64_t)(((ks >> 2) * (NV * 128) + (ks & 3) * 32) >> 4), idesc_f16(128, NV),
                                ks > 0 ? 1u : 0u);
                 umma_commit(dbar + 8 * b);
 #pragma unroll
                 for (int ks = 0; ks < DK / 16; ++ks)
-                    umma_f16_1(tmem + TM_O + SNV * b, ao + (uint64_t)(ks * 16),
-                               bs + (uint64_t)(((ks >> 2) * (SNV * 128) + (ks & 3) * 32) >> 4), idesc_f16(64, SNV),
+                    umma_f16_1(tmem + TM_O + NV * b, ao + (uint64_t)(ks * 16),
+                               bs + (uint64_t)(((ks >> 2) * (NV * 128) + (ks & 3) * 32) >> 4), idesc_f16(64, NV),
                                ks > 0 ? 1u : 0u);
                 umma_commit(obar + 8 * b);
             }
@@ -1089,8 +1091,8 @@ __global__ void __launch_bounds__(C_NT, 1)
         auto prefetch = [&](int ci) {
             if (lane == 0 && ci < n_chunks) {
                 const unsigned char* rec = records + (size_t)((g0 - c_begin + ci) * H + h) * REC_BYTES;
-                prefetch_l2(rec + REC_B + (size_t)(j0 >> 2) * DK * 8, (SNV / 4) * DK * 8);
-                prefetch_l2(rec + REC_O + (size_t)(j0 >> 2) * C * 8, (SNV / 4) * C * 8);
+                prefetch_l2(rec + REC_B + (size_t)(j0 >> 2) * DK * 8, (NV / 4) * DK * 8);
+                prefetch_l2(rec + REC_O + (size_t)(j0 >> 2) * C * 8, (NV / 4) * C * 8);
                 prefetch_l2(rec + REC_G, REC_BYTES - REC_G);
             }
         };
@@ -1112,12 +1114,12 @@ __global__ void __launch_bounds__(C_NT, 1)
         // ---------------- output warps: rows 0..63 of chunk c (M=64: row 16 q + i at lane i of quadrant q) ----------------
         const int orow = 16 * quad + (lane & 15);
         const uint32_t tlane = (uint32_t)(32 * quad) << 16;
-        uint2 oq[SNV / 4];                             // raw fp16, converted where used
+        uint2 oq[NV / 4];                              // raw fp16, converted where used
         int eo = 0;                                    // the chunk's value scale exponent
         auto fetch_o = [&](int ci) {                  // the chunk's P Utilde for this row and slice
             const unsigned char* rec = records + (size_t)((g0 - c_begin + ci) * H + h) * REC_BYTES;
 #pragma unroll
-            for (int m = 0; m < SNV / 4; ++m)
+            for (int m = 0; m < NV / 4; ++m)
                 oq[m] = lane < 16 ? __ldg(reinterpret_cast<const uint2*>(rec + REC_O + (((j0 + 4 * m) >> 2) * C + orow) * 8))
                                   : make_uint2(0u, 0u);
             eo = __ldg(reinterpret_cast<const int*>(rec + REC_E));
@@ -1130,8 +1132,8 @@ __global__ void __launch_bounds__(C_NT, 1)
             if (!mbar_wait(ebar + 8 * (ci & 3), (uint32_t)(ci >> 2) & 1u)) { fail(); break; }
             const int E = e_ring[ci & 3];               // the scale of the chunk's state operand
             tc_fence_after();
-            float d[SNV];
-            tmem_ld32(tmem + tlane + TM_O + SNV * b, d);
+            float d[NV];
+            tmem_ld<NV>(tmem + tlane + TM_O + NV * b, d);
             tc_fence_before();
             mbar_arrive(ofree + 8 * b);
             const int32_t t0 = (int32_t)(g0 - cseq + ci) * C;   // within the sequence
@@ -1139,7 +1141,7 @@ __global__ void __launch_bounds__(C_NT, 1)
                 __nv_bfloat16* dst = go + ((int64_t)(s0 + t0 + orow) * H + h) * p.dv + j0;
                 const float fd = exp2i(E), fo = exp2i(eo);      // 1 unless values or the state are large
 #pragma unroll
-                for (int x = 0; x < SNV; x += 8) {
+                for (int x = 0; x < NV; x += 8) {
                     const float4 o0 = half4_to_float4(oq[x / 4]), o1 = half4_to_float4(oq[x / 4 + 1]);
                     *reinterpret_cast<uint4*>(dst + x) = make_uint4(
                         pack_bf16x2(p.scale * (fd * d[x] + fo * o0.x), p.scale * (fd * d[x + 1] + fo * o0.y)),
@@ -1175,7 +1177,7 @@ __global__ void __launch_bounds__(C_NT, 1)
             const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));   // its latency under the stores
 #pragma unroll
             for (int j = 0; j < CPT; ++j)
-                *reinterpret_cast<__half*>(sop + sw128_off_h(CPT * half + j, srow, SNV)) = __float2half_rn(S[j]);
+                *reinterpret_cast<__half*>(sop + sw128_off_h(CPT * half + j, srow, NV)) = __float2half_rn(S[j]);
             big |= m > kF16Max;
             if (lane == 0) smax[(c & 1) * 8 + warp] = mw;
             fence_async_smem();
@@ -1224,7 +1226,7 @@ __global__ void __launch_bounds__(C_NT, 1)
             if (!mbar_wait(dbar + 8 * b, par)) { fail(); ok = false; break; }
             tc_fence_after();
             float d[CPT];
-            tmem_ld16(tmem + tlane + TM_S + CPT * half, d);
+            tmem_ld<CPT>(tmem + tlane + TM_S + CPT * half, d);
             if (eb == E) {                             // the record's B is at the state's scale (always when nothing is scaled)
 #pragma unroll
                 for (int m = 0; m < CPT / 4; ++m) {
@@ -1525,6 +1527,13 @@ size_t prefill_2p_workspace(int32_t num_seqs, int64_t total_tokens, int32_t H) {
     return prefill_2p_header(num_seqs) + (size_t)(chunks < cap ? chunks : cap) * H * REC_BYTES;
 }
 
+// Value columns per chain CTA: 16 for one sequence whose 16-column chain still leaves half the SMs to phase 1
+// (few heads: there the chain's per-chunk latency sets the time, and half the columns halve the state warps'
+// update and operand write), otherwise 32.
+static int chain_columns(int32_t num_seqs, int32_t H, int sms) {
+    return num_seqs == 1 && 2 * H * (DK / 16) <= sms ? 16 : 32;
+}
+
 WindowPlan prefill_2p_plan(int32_t num_seqs, int64_t chunks, int32_t H, size_t workspace_bytes, int sms) {
     const size_t hdr = prefill_2p_header(num_seqs);
     const int64_t cap = workspace_bytes > hdr ? (int64_t)((workspace_bytes - hdr) / ((size_t)H * REC_BYTES)) : 0;
@@ -1564,12 +1573,14 @@ cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t wo
     cudaError_t e = cudaFuncSetAttribute(multi ? kda_prefill_prep_kernel<true> : kda_prefill_prep_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(multi ? kda_prefill_chain_kernel<true> : kda_prefill_chain_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C_SMEM);
-    if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int nv = chain_columns(p.num_seqs, p.H, sms);
+    e = cudaFuncSetAttribute(multi ? kda_prefill_chain_kernel<true, 32>
+                                   : (nv == 16 ? kda_prefill_chain_kernel<false, 16> : kda_prefill_chain_kernel<false, 32>),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C_SMEM);
+    if (e != cudaSuccess) return e;
     const int N = p.num_seqs;
     const size_t hdr = prefill_2p_header(N);
     const int64_t chunks = prefill_2p_max_chunks(N, T);
@@ -1586,7 +1597,7 @@ cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t wo
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = launch_order(p.cu_seqlens, N, order, s)) != cudaSuccess) return e;
     }
-    const int chain_ctas = N * p.H * SLICES;
+    const int chain_ctas = N * p.H * (DK / nv);
     SideStream* ss = nullptr;
     std::unique_lock<std::mutex> enqueue;             // concurrent callers must not interleave event records
     if (plan.buffers == 2) {
@@ -1603,7 +1614,7 @@ cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t wo
         unsigned char* rec = static_cast<unsigned char*>(workspace) + hdr + buf * buf_bytes;
         cudaStream_t ps = ss ? ss->stream : s;
         // phase 1 shares the GPU with the previous window's chain when overlapped
-        int grid = (ss && w > 0) ? sms - p.H * SLICES : sms;
+        int grid = (ss && w > 0) ? sms - chain_ctas : sms;
         if (grid > units) grid = units;
         if (ss && w >= 2 && (e = cudaStreamWaitEvent(ps, ss->chain_done[buf], 0)) != cudaSuccess) return e;
         if (multi)
@@ -1616,11 +1627,14 @@ cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t wo
             if ((e = cudaStreamWaitEvent(s, ss->prep_done[buf], 0)) != cudaSuccess) return e;
         }
         if (multi)
-            kda_prefill_chain_kernel<true><<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n, choff,
-                                                                                    order);
+            kda_prefill_chain_kernel<true, 32><<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n, choff,
+                                                                                        order);
+        else if (nv == 16)
+            kda_prefill_chain_kernel<false, 16><<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n,
+                                                                                         nullptr, nullptr);
         else
-            kda_prefill_chain_kernel<false><<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n,
-                                                                                     nullptr, nullptr);
+            kda_prefill_chain_kernel<false, 32><<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n,
+                                                                                         nullptr, nullptr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (ss && (e = cudaEventRecord(ss->chain_done[buf], s)) != cudaSuccess) return e;
     }

@@ -250,12 +250,27 @@ __device__ __forceinline__ float lg2f(float x) {
     return y;
 }
 
+// 8 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v) {
-    if constexpr (N == 16) {
+    if constexpr (N == 8) {
+        tmem_ld8(taddr, v);
+    } else if constexpr (N == 16) {
         tmem_ld16(taddr, v);
     } else {
-        static_assert(N == 32, "16 or 32 columns");
+        static_assert(N == 32, "8, 16 or 32 columns");
         tmem_ld32(taddr, v);
     }
 }
