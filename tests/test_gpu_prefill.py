@@ -168,6 +168,11 @@ def test_packing_independence(dtype, d):
         assert np.array_equal(st1, st[list(pair)])
 
 
+# One sequence with few heads runs the chain on 16-column slices, with more heads on 32-column slices (the
+# chain of 16-column slices must leave half of the GB300's 152 SMs to phase 1: H <= 9); H = 12 takes the latter.
+CHAIN_WIDTHS = [2, 12]
+
+
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 700])
 @pytest.mark.parametrize("decay", ["config", "slow", "one", "scalar"])
 def test_single_sequence_two_phase(T, decay):
@@ -176,15 +181,23 @@ def test_single_sequence_two_phase(T, decay):
     check(inp)
 
 
-def test_two_phase_windows_give_identical_results():
+@pytest.mark.parametrize("T", [65, 700])
+def test_single_sequence_two_phase_wide_chain(T):
+    """The same with twelve heads, whose chain runs on 32-column slices."""
+    inp = I.prefill_inputs([T], 12, 128, 128, "bf16", 400 + T, decay="config", state="randn")
+    check(inp)
+
+
+@pytest.mark.parametrize("H", CHAIN_WIDTHS)
+def test_two_phase_windows_give_identical_results(H):
     """A workspace smaller than the recommended size walks the sequence in more windows of chunks, the
     state passing between windows through state_out; the results are bit-identical, in place too."""
     import kda_gated_delta_03_gb300 as kda
-    inp = I.prefill_inputs([1000], 2, 128, 128, "bf16", 15, decay="slow", state="randn")
+    inp = I.prefill_inputs([1000], H, 128, 128, "bf16", 15, decay="slow", state="randn")
     args = [to_dev(inp[n], n in ("q", "k", "v")) for n in ("q", "k", "v", "beta", "alpha", "cu_seqlens")]
     s0 = to_dev(inp["state_in"])
-    rec = 2 * 99072                                           # one chunk of records for H = 2
-    assert kda.kda_prefill_workspace_size(1, 1000, 2, 128, 128, torch.bfloat16) == 16 * rec
+    rec = H * 99072                                           # one chunk of records
+    assert kda.kda_prefill_workspace_size(1, 1000, H, 128, 128, torch.bfloat16) == 16 * rec
     runs = []
     for chunks in (16, 5, 1):
         ws = torch.empty(chunks * rec, dtype=torch.uint8, device="cuda:0")
@@ -277,7 +290,8 @@ def _scaled_v(inp, factor, rows=slice(None)):
     return I.f32_to_bf16_bits(v)
 
 
-def test_large_values_and_states_on_the_two_phase_path():
+@pytest.mark.parametrize("H", CHAIN_WIDTHS)
+def test_large_values_and_states_on_the_two_phase_path(H):
     """The two-phase path keeps its per-chunk records and its state operand in fp16 (range 65,504) and
     holds large magnitudes inside that range with exact power-of-two scales: per chunk for v, and for the
     carried state a scale chosen before every chunk from the largest state entry.  With v and the initial
@@ -286,8 +300,8 @@ def test_large_values_and_states_on_the_two_phase_path():
     matches the float64 oracle (over the first and the later tokens separately, so that the large part
     does not hide the small one) and reports nothing; the single-kernel path agrees too."""
     import kda_gated_delta_03_gb300 as kda
-    base = I.prefill_inputs([700], 2, 128, 128, "bf16", 95, decay="slow", state="randn")
-    fast = I.prefill_inputs([700], 2, 128, 128, "bf16", 96, decay="config", state="randn")
+    base = I.prefill_inputs([700], H, 128, 128, "bf16", 95, decay="slow", state="randn")
+    fast = I.prefill_inputs([700], H, 128, 128, "bf16", 96, decay="config", state="randn")
     cases = {
         "all_x1e6": dict(base, v=_scaled_v(base, 1e6), state_in=base["state_in"] * 1e6),
         "just_above": dict(base, v=_scaled_v(base, 70.0)),
@@ -313,3 +327,20 @@ def test_single_kernel_option_matches_the_oracle():
     o1, s1 = _run_one(inp, True)
     assert kda.kda_get_device_error() == 0
     assert rel_frob(o1, o_ref) <= 3e-3 and rel_frob(s1, s_ref) <= 3e-3
+
+
+def test_chain_widths_agree_bit_for_bit():
+    """Heads are independent, so two heads taken out of a twelve-head sequence (chain on 32-column slices)
+    and run on their own (chain on 16-column slices) give the same bits: the slice width changes only how
+    the value columns are split over CTAs, not the arithmetic of any element."""
+    import kda_gated_delta_03_gb300 as kda
+    inp = I.prefill_inputs([700], 12, 128, 128, "bf16", 97, decay="config", state="randn")
+    names = ("q", "k", "v", "beta", "alpha")
+    full = [to_dev(inp[n], n in ("q", "k", "v")) for n in names] + [to_dev(inp["cu_seqlens"])]
+    o12, st12 = kda.kda_prefill(*full, to_dev(inp["state_in"]))
+    heads = slice(5, 7)
+    part = [to_dev(np.ascontiguousarray(inp[n][:, heads]), n in ("q", "k", "v")) for n in names]
+    o2, st2 = kda.kda_prefill(*part, to_dev(inp["cu_seqlens"]), to_dev(np.ascontiguousarray(inp["state_in"][:, heads])))
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_error() == 0
+    assert torch.equal(o2, o12[:, heads]) and torch.equal(st2, st12[:, heads])

@@ -30,9 +30,10 @@ def run(inp, every, workspace_chunks=None):
     return o.double().cpu().numpy(), st.double().cpu().numpy(), snaps.double().cpu().numpy()[:len(ref)], ref
 
 
-@pytest.mark.parametrize("workspace_chunks", [None, 3])
-def test_snapshots_two_phase(workspace_chunks):
-    inp = I.prefill_inputs([700], 2, 128, 128, "bf16", 90, decay="slow", state="randn")
+@pytest.mark.parametrize("workspace_chunks,H", [(None, 2), (3, 2), (3, 12)])
+def test_snapshots_two_phase(workspace_chunks, H):
+    """H = 2 runs the chain on 16-column slices, H = 12 on 32-column slices."""
+    inp = I.prefill_inputs([700], H, 128, 128, "bf16", 90, decay="slow", state="randn")
     o, st, snaps, ref = run(inp, 128, workspace_chunks)
     assert ref.shape[0] == 5
     assert rel_frob(snaps, ref) <= TOL["bf16"]
