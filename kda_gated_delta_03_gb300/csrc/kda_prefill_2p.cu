@@ -908,7 +908,8 @@ __global__ void __launch_bounds__(NT, 1)
 //                then Q' S_c -> obar (issued while the state warps update S)
 //   warp 9:      wait obar, load record c+2 into the freed buffer; prefetch B and P Utilde of c+4 into L2
 //   warps 0-7:   wait dbar; S_{c+1} = Gamma_C S_c + B - M S_c; write the S^T operand of c+1; arrive on sbar
-//   warps 10-13: wait obar; o = scale (Q' S_c + P Utilde) for rows 0..63; arrive on ofree
+//   warps 10-13: wait obar and the end of chunk c's state update (state warp 0 publishes E of c+1);
+//                o = scale (Q' S_c + P Utilde) for rows 0..63; arrive on ofree
 // so the output products and epilogue of one chunk overlap the state products of the next, and the
 // state warps' proxy fence never waits on output traffic.  The S^T operand and the output accumulator
 // are double-buffered; M S uses one accumulator (it is read before the arrival on sbar).  Every barrier
@@ -1130,6 +1131,10 @@ __global__ void __launch_bounds__(C_NT, 1)
             if (*s_abort) break;
             if (!mbar_wait(obar + 8 * b, (uint32_t)(ci >> 1) & 1u)) { fail(); break; }
             if (!mbar_wait(ebar + 8 * (ci & 3), (uint32_t)(ci >> 2) & 1u)) { fail(); break; }
+            // start the epilogue once state warp 0 has finished this chunk's update (it publishes the next
+            // chunk's E), so that it runs under the next round trip through the tensor core instead of
+            // taking issue slots from the update
+            if (ci + 1 < n_chunks && !mbar_wait(ebar + 8 * ((ci + 1) & 3), (uint32_t)((ci + 1) >> 2) & 1u)) { fail(); break; }
             const int E = e_ring[ci & 3];               // the scale of the chunk's state operand
             tc_fence_after();
             float d[NV];
