@@ -95,7 +95,9 @@ constexpr int PS_P = 122880;                                               // P 
 constexpr int PS_WU = 0, PS_KH = 65536;                                    // fold operands, after [W | Utilde]
 constexpr int ONE_L_OFF = C * DK * 4;                                     // one-reference A/P: R, then L
 constexpr float kOneRefMax = 125.f;                                        // log2 of the largest factor
-constexpr int P_SMEM = P_OFF_S + G1_BYTES;
+constexpr int P_OFF_CS = P_OFF_S + G1_BYTES;               // several sequences: chunk offsets and cu_seqlens
+constexpr int CS_MAX = 128;                                 // (N + 1 <= CS_MAX entries each) cached for the lookups
+constexpr int P_SMEM = P_OFF_CS + 2 * CS_MAX * 4;
 static_assert(PS_KV + (DK + DK) * 256 <= PS_P && PS_P + 16384 <= G1_BYTES, "phase-1 scratch");
 static_assert(PS_KH + DK * C * 4 <= PS_P, "phase-1 fold operands");
 static_assert(P_SMEM <= 232448, "phase-1 shared memory");
@@ -186,15 +188,16 @@ __device__ __forceinline__ int chunk_seq(const int32_t* choff, int32_t N, int64_
 }
 // First token of chunk gc and the end token of its sequence.
 __device__ __forceinline__ void chunk_span(const PrefillParams& p, const int32_t* choff, int64_t gc, int32_t& t0,
-                                           int32_t& t_end) {
+                                           int32_t& t_end, const int32_t* cu = nullptr) {
     if (!choff) {
         t0 = (int32_t)(gc * C);
         t_end = p.total_tokens;
         return;
     }
+    if (!cu) cu = p.cu_seqlens;
     const int n = chunk_seq(choff, p.num_seqs, gc);
-    t0 = p.cu_seqlens[n] + (int32_t)(gc - choff[n]) * C;
-    t_end = p.cu_seqlens[n + 1];
+    t0 = cu[n] + (int32_t)(gc - choff[n]) * C;
+    t_end = cu[n + 1];
 }
 
 // Chunk offsets of the sequences (chunks of 64 tokens, the last one partial) and the check of cu_seqlens;
@@ -224,6 +227,7 @@ __global__ void __launch_bounds__(NT, 1)
     kda_prefill_prep_kernel(PrefillParams p, const __grid_constant__ PrepMaps maps, unsigned char* records,
                             int c_begin, int n_units, const int32_t* choff_arg) {
     const int32_t* choff = MULTI ? choff_arg : nullptr;
+    const int32_t* cu = nullptr;                     // cu_seqlens for the chunk lookups (global unless cached)
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
@@ -265,6 +269,15 @@ __global__ void __launch_bounds__(NT, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *s_abort = 0;
     }
+    if (MULTI && p.num_seqs + 1 <= CS_MAX) {         // the lookups of every unit read shared memory
+        int32_t* cs = reinterpret_cast<int32_t*>(sm + P_OFF_CS);
+        for (int e = tid; e <= p.num_seqs; e += NT) {
+            cs[e] = choff_arg[e];
+            cs[CS_MAX + e] = p.cu_seqlens[e];
+        }
+        choff = cs;
+        cu = cs + CS_MAX;
+    }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(s_tmem)), "r"(512)
                      : "memory");
@@ -299,7 +312,7 @@ __global__ void __launch_bounds__(NT, 1)
     auto unit_rows = [&](int u, int& hu, int32_t& tu) {
         hu = u % H;
         int32_t te;
-        chunk_span(p, choff, (int64_t)c_begin + u / H, tu, te);
+        chunk_span(p, choff, (int64_t)c_begin + u / H, tu, te, cu);
     };
     auto issue_v = [&](int u) {                      // arms vkbar for v and k together
         if (tid == 32) {
@@ -390,7 +403,7 @@ __global__ void __launch_bounds__(NT, 1)
         issue_k(blockIdx.x);
         issue_qa(blockIdx.x);
         int32_t tn, tn_end;
-        chunk_span(p, choff, (int64_t)c_begin + (int)blockIdx.x / H, tn, tn_end);
+        chunk_span(p, choff, (int64_t)c_begin + (int)blockIdx.x / H, tn, tn_end, cu);
         if (tid < C) {
             const int64_t row = (int64_t)(tn + tid) * H + (int)blockIdx.x % H;
             const bool in = tn + tid < tn_end;
@@ -415,7 +428,7 @@ __global__ void __launch_bounds__(NT, 1)
 
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         int32_t t0, t_end;                              // the chunk's first token and its sequence's end
-        chunk_span(p, choff, (int64_t)c_begin + u / H, t0, t_end);
+        chunk_span(p, choff, (int64_t)c_begin + u / H, t0, t_end, cu);
         const int L = min(C, t_end - t0);
         unsigned char* rec = records + (size_t)u * REC_BYTES;
         const int un = u + (int)gridDim.x;                       // this CTA's next unit
@@ -431,7 +444,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (*s_abort) break;
         if (tid < C && un < n_units) {                  // the next unit's beta (and alpha), used at this unit's end
             int32_t tn, tn_end;
-            chunk_span(p, choff, (int64_t)c_begin + un / H, tn, tn_end);
+            chunk_span(p, choff, (int64_t)c_begin + un / H, tn, tn_end, cu);
             const int64_t row = (int64_t)(tn + tid) * H + un % H;
             beta_next = tn + tid < tn_end ? p.beta[row] : 0.f;
             alpha_next = per_head && tn + tid < tn_end ? p.alpha[row] : 1.f;
