@@ -91,11 +91,13 @@ typedef enum {
  * Bytes of device workspace kda_prefill needs for this problem (0 is a valid
  * answer).  Pure host function; never fails (returns 0 for invalid sizes).
  *  - bf16 with d_k = d_v = 128 (the two-phase path): the per-chunk records
- *    (99,072 bytes per chunk and head, up to 1 GiB of them), preceded, for
- *    several sequences, by their chunk offsets and their longest-first order
- *    (4 (N + 1) and 4 N bytes, each rounded up to 256).  kda_prefill also
- *    accepts less, down to one chunk's records after those offsets; it then
- *    walks the chunks in more windows, with identical results.
+ *    (99,072 bytes per chunk and head; up to 1 GiB of them for one sequence,
+ *    up to 16 GiB for several, so that all chunks of a batch of sequences fit
+ *    one window), preceded, for several sequences, by their chunk offsets and
+ *    their longest-first order (4 (N + 1) and 4 N bytes, each rounded up to
+ *    256).  kda_prefill also accepts less, down to one chunk's records after
+ *    those offsets; it then walks the chunks in more windows, with identical
+ *    results.
  *  - Other several-sequence calls: the longest-first schedule, 4 bytes per
  *    sequence.
  */

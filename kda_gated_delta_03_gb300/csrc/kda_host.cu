@@ -126,9 +126,13 @@ HostLayout host_layout(int32_t N, int64_t T, int32_t H, int32_t dk, int32_t dv, 
     // a segment holds at most N sequences and T tokens; one sequence is cut into segments of at most
     // single_sequence_cut(T) tokens, and a group of several may hold a single sequence (whose path, for
     // bf16 d=128, needs the per-chunk records)
+    // (for several sequences the records are held to the one-sequence budget of 1 GiB: a segment is short,
+    // and more windows only lengthen the walk, not the results)
+    const size_t ws_multi = kda::prefill_2p_supported(N, T, H, dk, dv, dt)
+                                ? a256(kda::prefill_2p_workspace(N, T, H, size_t(1) << 30))
+                                : kda_prefill_workspace_size(N, T, H, dk, dv, dt);
     L.ws_bytes = N == 1 ? kda_prefill_workspace_size(1, std::min<int64_t>(T, single_sequence_cut(T)), H, dk, dv, dt)
-                        : std::max(kda_prefill_workspace_size(N, T, H, dk, dv, dt),
-                                   kda_prefill_workspace_size(1, T, H, dk, dv, dt));
+                        : std::max(ws_multi, kda_prefill_workspace_size(1, T, H, dk, dv, dt));
     L.ws = at; at = a256(at + L.ws_bytes);
     L.total = at;
     return L;

@@ -110,7 +110,8 @@ int prefill_tc_slices(int32_t num_seqs, int32_t H, int32_t dv);
 // Two-phase prefill (bf16, d_k = d_v = 128): per-chunk records in the workspace, then the state chain.
 bool prefill_2p_supported(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
                           kda_dtype dt);
-size_t prefill_2p_workspace(int32_t num_seqs, int64_t total_tokens, int32_t H);   // recommended bytes
+// recommended bytes; record_budget caps the records (0: 1 GiB for one sequence, 16 GiB for several)
+size_t prefill_2p_workspace(int32_t num_seqs, int64_t total_tokens, int32_t H, size_t record_budget = 0);
 struct WindowPlan {
     int64_t window;   // chunks per window
     int buffers;      // 2: phase 1 of the next window overlaps phase 2 of this one (side stream)

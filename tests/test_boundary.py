@@ -61,11 +61,13 @@ def test_workspace_size(lib):
     assert lib.kda_prefill_workspace_size(1, 8192, 32, 128, 128, 0) == 0      # fp32: single-kernel path
     assert lib.kda_prefill_workspace_size(1, 8192, 32, 64, 64, 1) == 0
     # several bf16 d=128 sequences: their chunk offsets and longest-first order, then the records of at most
-    # T // 64 + N chunks (each sequence's last chunk may be partial), at most 1 GiB of them
+    # T // 64 + N chunks (each sequence's last chunk may be partial), at most 16 GiB of them
     up = lambda x: (x + 255) // 256 * 256
     hdr = lambda n: up(4 * (n + 1)) + up(4 * n)
-    assert lib.kda_prefill_workspace_size(64, 300000, 32, 128, 128, 1) == up(hdr(64) + 338 * 32 * 99072)
-    assert lib.kda_prefill_workspace_size(65, 300000, 32, 128, 128, 1) == up(hdr(65) + 338 * 32 * 99072)
+    assert lib.kda_prefill_workspace_size(64, 300000, 32, 128, 128, 1) == up(hdr(64) + (300000 // 64 + 64) * 32 * 99072)
+    assert lib.kda_prefill_workspace_size(65, 300000, 32, 128, 128, 1) == up(hdr(65) + (300000 // 64 + 65) * 32 * 99072)
+    cap = (16 << 30) // (32 * 99072)
+    assert lib.kda_prefill_workspace_size(64, 1 << 20, 32, 128, 128, 1) == up(hdr(64) + cap * 32 * 99072)
     assert lib.kda_prefill_workspace_size(3, 700, 2, 128, 128, 1) == up(hdr(3) + (700 // 64 + 3) * 2 * 99072)
     # other sequence batches: the longest-first order only
     assert lib.kda_prefill_workspace_size(64, 300000, 32, 64, 64, 1) == 256
