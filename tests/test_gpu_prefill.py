@@ -120,6 +120,33 @@ def test_records_path_for_several_sequences():
     assert torch.equal(o3.view(torch.int16), o.view(torch.int16)) and torch.equal(st3, st)
 
 
+@pytest.mark.parametrize("N", [127, 128, 200])
+def test_records_path_for_many_sequences(N):
+    """Up to 127 sequences, phase 1 looks chunks up in copies of the chunk offsets and cu_seqlens in shared
+    memory; beyond that, in global memory.  Both sides of that limit match the oracle, with short and
+    empty sequences mixed in, and a workspace of a few chunks (many windows) gives the same bits."""
+    import kda_gated_delta_03_gb300 as kda
+    rng = np.random.default_rng(700 + N)
+    seqlens = [int(x) for x in rng.integers(0, 90, N)]
+    seqlens[3] = 0
+    seqlens[N - 1] = 129
+    H = 2
+    inp = I.prefill_inputs(seqlens, H, 128, 128, "bf16", 42, decay="config", state="randn")
+    args = [to_dev(inp[n], n in ("q", "k", "v")) for n in ("q", "k", "v", "beta", "alpha", "cu_seqlens")]
+    s0 = to_dev(inp["state_in"])
+    o, st = kda.kda_prefill(*args, s0)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_error() == 0
+    o_ref, st_ref = O.prefill(inp)
+    assert rel_frob(o.double().cpu().numpy(), o_ref) <= 3e-3
+    assert rel_frob(st.double().cpu().numpy(), st_ref) <= 3e-3
+    up = lambda x: (x + 255) // 256 * 256
+    ws = torch.empty(up(4 * (N + 1)) + up(4 * N) + 5 * H * 99072, dtype=torch.uint8, device="cuda:0")
+    o2, st2 = kda.kda_prefill(*args, s0, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o2.view(torch.int16), o.view(torch.int16)) and torch.equal(st2, st)
+
+
 def test_scale_and_zero_state():
     inp = I.prefill_inputs([130, 7], 2, 64, 64, "f32", 8, decay="slow")
     check(inp, scale=0.125)
