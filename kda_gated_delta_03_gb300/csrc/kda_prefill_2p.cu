@@ -10,10 +10,11 @@
 // Phase 1 computes, for every (head, chunk) of a window in parallel, everything that does not depend
 // on S -- g, A and P, T' = (I + A)^-1 Diag(beta), [W | Utilde], and from them Q', M, B and P Utilde --
 // and stores it as a record in the workspace, Q' and M already in the byte layout of a tensor-core
-// operand.  Phase 2 walks the chunks in order, one CTA per (head, 32 value columns), bulk-loading each
-// record one chunk ahead; per chunk it issues a single batch of tensor-core products,
+// operand.  Phase 2 walks the chunks in order, one CTA per (head, NV value columns: 32, or 16 for one
+// sequence with few heads), bulk-loading each record one chunk ahead; per chunk it issues a single batch
+// of tensor-core products,
 //
-//   M S (M=128)  and  Q' S (M=64)       tcgen05 kind::f16 (fp16 record and state operands), N=32, K=128
+//   M S (M=128)  and  Q' S (M=64)       tcgen05 kind::f16 (fp16 record and state operands), N=NV, K=128
 //
 // followed by the fp32 update S <- Gamma_C . S + B - M S and o = scale (Q' S + P Utilde).  Folding W
 // into M and Q' doubles phase 1's work on W but leaves one round trip through the tensor core on the
@@ -920,14 +921,14 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ============================================================================================
-// Phase 2: one CTA per (sequence, head, 32 value columns); it walks that sequence's chunks inside the window
+// Phase 2: one CTA per (sequence, head, NV value columns); it walks that sequence's chunks inside the window
 // [c_begin, c_begin + n_chunks) in order, from state_in where the sequence starts in the window and from
 // the state carried in state_out otherwise, and leaves its state in state_out.  With several sequences
 // (choff set) blockIdx enumerates (order[i], head, slice), longest sequences first; a CTA whose sequence
 // has no chunk in the window exits at once (a zero-length sequence copies state_in to state_out in the
 // first window).
 //
-// Warps 0-7 hold the state (thread = one key channel, 16 value columns) and run the fp32 update;
+// Warps 0-7 hold the state (thread = one key channel, NV/2 value columns) and run the fp32 update;
 // warp 8 issues the products, warp 9 the record loads; warps 10-13 run the output epilogue (the output
 // product is M=64, whose row 16 q + i sits at lane i of TMEM lane quadrant q, and warp w reaches quadrant
 // w mod 4).  Per chunk c:
