@@ -50,10 +50,11 @@ constexpr int MAT = MC * MD;           // floats per scratch matrix
 // shared memory (floats)
 constexpr int F_P = 0;                             // P
 constexpr int F_T = F_P + MC * LD64;               // T
-constexpr int F_DP = F_T + MC * LD64;              // dP
-constexpr int F_DA = F_DP + MC * LD64;             // dA, then dBt
-constexpr int F_BT = F_DA + MC * LD64;             // Bt
-constexpr int F_Y = F_BT + MC * LD64;              // scaled operands [64][LDY]; dT and X [64][LD64] each
+constexpr int F_BT = F_T + MC * LD64;              // Bt
+constexpr int F_DP = F_BT + MC * LD64;             // dP  } dP, dA, Y and the staging area are contiguous: the
+constexpr int F_DA = F_DP + MC * LD64;             // dA  } products before dP (or dA) is written run their
+constexpr int F_Y = F_DA + MC * LD64;              //     } cp.async ring over them, with more stages in flight
+                                                   // scaled operands [64][LDY]; dT and X [64][LD64] each
 constexpr int F_STG = F_Y + 2 * MC * LD64;         // product staging: A [16][LD64], B [16][LDY]; also 2 x [16][LDY]
 constexpr int F_VEC = F_STG + 2 * 16 * LDY;        // beta [64], G_C [128], row sums [128], column sums [2][128], 2 x [64]
 constexpr int F_K = F_VEC + 64 + 128 + 128 + 256 + 64 + 64;   // k [64][128]
@@ -184,6 +185,8 @@ __device__ __forceinline__ int mcol(int j) {
 constexpr int LDA = 72;                               // staged A row (k-major): conflict-free fragment loads
 static_assert(16 * LDA + 16 * (128 + 8) <= 2 * 16 * LDY, "staging area");
 static_assert(3 * (64 * 20 + 128 * 20) <= 2 * MC * LD64 + 2 * 16 * LDY, "product ring (scaled-operand and staging areas)");
+static_assert(5 * (64 * 20 + 128 * 20) <= 4 * MC * LD64 + 2 * 16 * LDY, "five-stage ring from dP on");
+static_assert(4 * (64 * 20 + 128 * 20) <= 3 * MC * LD64 + 2 * 16 * LDY, "four-stage ring from dA on");
 template <int NN, int KK>
 __device__ __forceinline__ void mm(const float* A, int am, int ak, const float* B, int bk, int bn, float* stage,
                                    float (&acc)[4][NN / 16]) {
@@ -265,15 +268,16 @@ __device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.w
 // stored so that the fragment loads are free of bank conflicts (k-contiguous rows of 20 floats, or
 // k-major rows of 72 / NN + 8).  Operands are rounded to TF32 (nearest) as their fragments are loaded.
 constexpr int RING_STAGE = 64 * 20 + 128 * 20;     // floats per stage: A 64 x 20, B up to 128 x 20
-template <int NN, int KK, bool AS, bool AT, bool BS, bool BT>
+template <int NN, int KK, bool AS, bool AT, bool BS, bool BT, int NRS>
 __device__ __forceinline__ void mm_tc(const float* A, int lda, const float* B, int ldb, float* ring,
                                       float (&acc)[4][NN / 16]) {
     constexpr int NST = KK / 16;
+    static_assert(NRS >= 3 && NRS <= 5, "ring stages");
     constexpr int LAR = 20, LAT = 72, LBR = NN + 8, LBT = 20;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, g = lane >> 2, t = lane & 3;
     const int m0 = 32 * (w & 1), n0 = (NN / 4) * (w >> 1);
     auto issue = [&](int st) {
-        float* sa = ring + (st % 3) * RING_STAGE;
+        float* sa = ring + (st % NRS) * RING_STAGE;
         float* sb = sa + 64 * 20;
         const int k0 = 16 * st;
         if constexpr (!AS) {
@@ -300,15 +304,19 @@ __device__ __forceinline__ void mm_tc(const float* A, int lda, const float* B, i
         }
         cp_async_commit_group();
     };
-    issue(0);
-    if (NST > 1) issue(1);
+#pragma unroll
+    for (int j = 0; j < NRS - 1; ++j)
+        if (j < NST) issue(j);
 #pragma unroll 1
     for (int st = 0; st < NST; ++st) {
-        if (st + 1 < NST) cp_async_wait_group<1>();
+        const int ahead = min(NST - 1 - st, NRS - 2);  // stages committed after st
+        if (ahead >= 3) cp_async_wait_group<3>();
+        else if (ahead == 2) cp_async_wait_group<2>();
+        else if (ahead == 1) cp_async_wait_group<1>();
         else cp_async_wait_group<0>();
         __syncthreads();                               // stage st landed for every thread; stage st - 1 is read
-        if (st + 2 < NST) issue(st + 2);               // into the slot of stage st - 1
-        const float* sa = ring + (st % 3) * RING_STAGE;
+        if (st + NRS - 1 < NST) issue(st + NRS - 1);   // into the slot of stage st - 1
+        const float* sa = ring + (st % NRS) * RING_STAGE;
         const float* sb = sa + 64 * 20;
         const int k0 = 16 * st;
         auto fa = [&](int m, int kl) -> float {        // kl: k within the stage
@@ -351,10 +359,10 @@ __device__ __forceinline__ void mm_tc(const float* A, int lda, const float* B, i
 }
 
 // One product of the chunk: on the tensor cores (TC) or in fp32 on the CUDA cores.
-template <bool TC, int NN, int KK, bool AS, bool AT, bool BS, bool BT>
+template <bool TC, int NN, int KK, bool AS, bool AT, bool BS, bool BT, int NRS = 3>
 __device__ __forceinline__ void prod(const float* A, int lda, const float* B, int ldb, float* ring, float* stage,
                                      float (&acc)[4][NN / 16]) {
-    if constexpr (TC) mm_tc<NN, KK, AS, AT, BS, BT>(A, lda, B, ldb, ring, acc);
+    if constexpr (TC) mm_tc<NN, KK, AS, AT, BS, BT, NRS>(A, lda, B, ldb, ring, acc);
     else mm<NN, KK>(A, AT ? 1 : lda, AT ? lda : 1, B, BT ? 1 : ldb, BT ? ldb : 1, stage, acc);
 }
 
@@ -390,6 +398,8 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
     float* sBT = fsm + F_BT;
     float* sY = fsm + F_Y;
     float* stg = fsm + F_STG;
+    float* ring5 = fsm + F_DP;                         // product rings while dP (ring5) or dA (ring4) is free
+    float* ring4 = fsm + F_DA;
     float* sbeta = fsm + F_VEC;
     float* sgc = sbeta + 64;                           // G of the chunk's last row, per key channel
     float* srow = sgc + 128;                           // sum_j dS_1[i][j] S_0[i][j], per key channel i
@@ -636,15 +646,15 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         float acc[4][8];
         // W = T (beta Gamma K);  Utilde = T (beta V);  U = Utilde - W S_0
         zero<128>(acc);
-        prod<TC, 128, 64, true, false, false, false>(sT, LD64, M(XKTB), MD, sY, stg, acc);
+        prod<TC, 128, 64, true, false, false, false, 5>(sT, LD64, M(XKTB), MD, ring5, stg, acc);
         put128<TC>(M(XW), acc);
         zero<128>(acc);
-        prod<TC, 128, 64, true, false, false, false>(sT, LD64, M(XVB), MD, sY, stg, acc);
+        prod<TC, 128, 64, true, false, false, false, 5>(sT, LD64, M(XVB), MD, ring5, stg, acc);
         __syncthreads();                               // W is written
         if (S0) {
             float ws[4][8];
             zero<128>(ws);
-            prod<TC, 128, 128, false, false, false, false>(M(XW), MD, S0, MD, sY, stg, ws);
+            prod<TC, 128, 128, false, false, false, false, 5>(M(XW), MD, S0, MD, ring5, stg, ws);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -654,14 +664,14 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         __syncthreads();
         // dU = P^T dO + Khat dS_1
         zero<128>(acc);
-        prod<TC, 128, 64, true, true, false, false>(sP, LD64, M(XDO), MD, sY, stg, acc);
-        if (dS1) prod<TC, 128, 128, false, false, false, false>(M(XKH), MD, dS1, MD, sY, stg, acc);
+        prod<TC, 128, 64, true, true, false, false, 5>(sP, LD64, M(XDO), MD, ring5, stg, acc);
+        if (dS1) prod<TC, 128, 128, false, false, false, false, 5>(M(XKH), MD, dS1, MD, ring5, stg, acc);
         put128<TC>(M(XDU), acc);
         // dP = dO U^T on s <= r
         {
             float a64[4][4];
             zero<64>(a64);
-            prod<TC, 64, 128, false, false, false, true>(M(XDO), MD, M(XU), MD, sY, stg, a64);
+            prod<TC, 64, 128, false, false, false, true, 5>(M(XDO), MD, M(XU), MD, ring5, stg, a64);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -673,13 +683,13 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         __syncthreads();
         // dQs = dO S_0^T;  dKhat = U dS_1^T;  dW = -dU S_0^T
         zero<128>(acc);
-        if (S0) prod<TC, 128, 128, false, false, false, true>(M(XDO), MD, S0, MD, sY, stg, acc);
+        if (S0) prod<TC, 128, 128, false, false, false, true, 4>(M(XDO), MD, S0, MD, ring4, stg, acc);
         put128<TC>(M(XDQS), acc);
         zero<128>(acc);
-        if (dS1) prod<TC, 128, 128, false, false, false, true>(M(XU), MD, dS1, MD, sY, stg, acc);
+        if (dS1) prod<TC, 128, 128, false, false, false, true, 4>(M(XU), MD, dS1, MD, ring4, stg, acc);
         put128<TC>(M(XDKH), acc);
         zero<128>(acc);
-        if (S0) prod<TC, 128, 128, false, false, false, true>(M(XDU), MD, S0, MD, sY, stg, acc);
+        if (S0) prod<TC, 128, 128, false, false, false, true, 4>(M(XDU), MD, S0, MD, ring4, stg, acc);
         put128<TC>(M(XDW), acc, -1.f);
         __syncthreads();
         // dT = dW (beta Gamma K)^T + dU (beta V)^T, kept on a > b (the only part T^T dT T^T reads below
@@ -689,8 +699,8 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         {
             float a64[4][4];
             zero<64>(a64);
-            prod<TC, 64, 128, false, false, false, true>(M(XDW), MD, M(XKTB), MD, sY, stg, a64);
-            prod<TC, 64, 128, false, false, false, true>(M(XDU), MD, M(XVB), MD, sY, stg, a64);
+            prod<TC, 64, 128, false, false, false, true, 4>(M(XDW), MD, M(XKTB), MD, ring4, stg, a64);
+            prod<TC, 64, 128, false, false, false, true, 4>(M(XDU), MD, M(XVB), MD, ring4, stg, a64);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
