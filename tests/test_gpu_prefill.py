@@ -240,6 +240,14 @@ def test_two_phase_windows_give_identical_results(H):
     assert rel_frob(runs[0][1].double().cpu().numpy(), s_ref) <= 3e-3
 
 
+@pytest.mark.parametrize("H,T", [(1, 200), (48, 300)])
+def test_single_sequence_two_phase_head_counts(H, T):
+    """One head (eight 16-column chain CTAs) and 48 heads (192 chain CTAs of 32 columns: more than the
+    GB300's 152 SMs, so the chain runs in two waves)."""
+    inp = I.prefill_inputs([T], H, 128, 128, "bf16", 500 + H, decay="config", state="randn")
+    check(inp)
+
+
 def test_two_phase_bad_cu_seqlens_is_reported():
     import kda_gated_delta_03_gb300 as kda
     inp = I.prefill_inputs([100], 2, 128, 128, "bf16", 16)
