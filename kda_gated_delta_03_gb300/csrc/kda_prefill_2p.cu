@@ -822,27 +822,24 @@ __global__ void __launch_bounds__(NT, 1)
         {
             // -Gamma.Q into the PW half of step 6's M=64 accumulator (row r at lane r % 16 of quadrant r / 16,
             // columns 2 DK + c) and zeros into its P Utilde half, so that step 6 accumulates PW - Gamma.Q = -Q'
-            // and q and alpha are free from here on; each warp writes the columns of its own quadrant that it
-            // has just read the [W | Utilde]^T accumulator from
-            const int gr = mr & (C - 1);                // lanes 16..31 repeat rows into lanes the MMA does not use
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                const int c0 = 64 * half + 16 * cb;
-                float v[16];
+            // and q and alpha are free from here on; each warp writes the 64 columns of its own quadrant that
+            // it has just read the [W | Utilde]^T accumulator from, lane (g, t) rows 16 quad + g (+ 8) and
+            // column pairs 8 j + 2 t (16x256b shape: every lane carries rows the products use)
+            float v[32];
 #pragma unroll
-                for (int x = 0; x < 16; x += 4) {
-                    const float4 gg = *reinterpret_cast<const float4*>(sm + OFF_G + g_off(gr, c0 + x));
-                    const uint2 qq = *reinterpret_cast<const uint2*>(sm + OFF_Q + kq_off(gr, c0 + x));
-                    const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qq);
-                    v[x] = -ex2f(gg.x) * __low2float(q2[0]);
-                    v[x + 1] = -ex2f(gg.y) * __high2float(q2[0]);
-                    v[x + 2] = -ex2f(gg.z) * __low2float(q2[1]);
-                    v[x + 3] = -ex2f(gg.w) * __high2float(q2[1]);
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = 16 * quad + gid + 8 * h, c = 64 * half + 8 * j + 2 * tig;
+                    const float2 gg = *reinterpret_cast<const float2*>(sm + OFF_G + g_off(r, c));
+                    const __nv_bfloat162 q2 = *reinterpret_cast<const __nv_bfloat162*>(sm + OFF_Q + kq_off(r, c));
+                    v[4 * j + 2 * h] = -ex2f(gg.x) * __low2float(q2);
+                    v[4 * j + 2 * h + 1] = -ex2f(gg.y) * __high2float(q2);
                 }
-                tmem_st16(tmem + tlane + 2 * DK + c0, v);
-                const float zero[16] = {};
-                tmem_st16(tmem + tlane + 3 * DK + c0, zero);
-            }
+            tmem_st16x256b_x8(tmem + tlane + 2 * DK + 64 * half, v);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) v[x] = 0.f;
+            tmem_st16x256b_x8(tmem + tlane + 3 * DK + 64 * half, v);
             tmem_wait_st();
         }
         fence_async_smem();
