@@ -802,62 +802,84 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         }
         // ---- column-side decayed sums for block b of s: sum_{r >= s} X_rs y_r E_rs
         //      = 2^(G_ref - G_s) sum_r X_rs (y_r 2^(G_r - G_ref)), y = q with X = dP, y = k with X = dBt ----
-        for (int b = 0; b < 4; ++b) {
-            const int ref = 16 * b + 7, r0 = 16 * b;
-            for (int pass = 0; pass < 2; ++pass) {
-                const float* src = pass == 0 ? M(XQ) : sK;
-                const float* xs = pass == 0 ? sDP : sDA;
+        if constexpr (TC) {
+            // both passes of block b share the factors 2^(G_r - G_ref) and 2^(G_ref - G_s): one build writes
+            // Y_q (q rows, in sY) and Y_k (k rows, in the P and T area, free since the products), then the two
+            // split-TF32 products, X^T (16 x (64 - r0), the block's columns s) times Y ((64 - r0) x 128)
+            float* sYk = sP;                           // [64][LDY] over P and T
+            const int g = lane >> 2, t = lane & 3;
+            for (int b = 0; b < 4; ++b) {
+                const int ref = 16 * b + 7, r0 = 16 * b;
 #pragma unroll 1
-                for (int e0 = r0 * MD + tid; e0 < MAT; e0 += 8 * MNT) {      // (64 - r0) x 128 = 2048 multiples
+                for (int e0 = r0 * MD + tid; e0 < MAT; e0 += 8 * MNT) {
                     float yv[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) yv[u] = src[e0 + MNT * u];
+                    for (int u = 0; u < 8; ++u) yv[u] = M(XQ)[e0 + MNT * u];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         const int e = e0 + MNT * u, r = e >> 7, i = e & 127;
-                        sY[(r - r0) * LDY + i] = yv[u] * exp2f(G[e] - G[ref * MD + i]);
+                        const float f = exp2f(G[e] - G[ref * MD + i]);
+                        sY[(r - r0) * LDY + i] = yv[u] * f;
+                        sYk[(r - r0) * LDY + i] = sK[e] * f;
                     }
                 }
                 __syncthreads();
-                if constexpr (TC) {
-                    // X^T (16 x (64 - r0), the block's columns s) times Y ((64 - r0) x 128), split TF32
-                    const int g = lane >> 2, t = lane & 3;
-                    float* out = M(pass == 0 ? XCP : XCK);
-                    float d[1][2][4] = {};
-                    tiles_mma3<1, 2>(d, (MC - r0) / 8, [&](int, int m, int k) { return xs[(r0 + k) * LD64 + r0 + m]; },
-                                     [&](int nb, int k, int n) { return sY[k * LDY + 8 * (warp + 8 * nb) + n]; });
+                float dp[1][2][4] = {}, dk[1][2][4] = {};
+                tiles_mma3<1, 2>(dp, (MC - r0) / 8, [&](int, int m, int k) { return sDP[(r0 + k) * LD64 + r0 + m]; },
+                                 [&](int nb, int k, int n) { return sY[k * LDY + 8 * (warp + 8 * nb) + n]; });
+                tiles_mma3<1, 2>(dk, (MC - r0) / 8, [&](int, int m, int k) { return sDA[(r0 + k) * LD64 + r0 + m]; },
+                                 [&](int nb, int k, int n) { return sYk[k * LDY + 8 * (warp + 8 * nb) + n]; });
 #pragma unroll
-                    for (int nb = 0; nb < 2; ++nb)
+                for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int sr = r0 + g + 8 * (q >> 1), i = 8 * (warp + 8 * nb) + 2 * t + (q & 1);
-                            out[sr * MD + i] = exp2f(G[ref * MD + i] - G[sr * MD + i]) * d[0][nb][q];
-                        }
-                    __syncthreads();
-                    continue;
-                }
-                const int s = r0 + tr;
-                float a8[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) a8[j] = 0.f;
-                for (int r = r0; r < MC; ++r) {
-                    const float x = xs[r * LD64 + s];
-                    const float4 y0 = *reinterpret_cast<const float4*>(sY + (r - r0) * LDY + 4 * tc);
-                    const float4 y1 = *reinterpret_cast<const float4*>(sY + (r - r0) * LDY + 64 + 4 * tc);
-                    const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) a8[j] = fmaf(x, yv[j], a8[j]);
-                }
-                float* out = M(pass == 0 ? XCP : XCK);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int i = col8(j);
-                    out[s * MD + i] = exp2f(G[ref * MD + i] - G[s * MD + i]) * a8[j];
-                }
+                    for (int q = 0; q < 4; ++q) {
+                        const int sr = r0 + g + 8 * (q >> 1), i = 8 * (warp + 8 * nb) + 2 * t + (q & 1);
+                        const float f = exp2f(G[ref * MD + i] - G[sr * MD + i]);
+                        M(XCP)[sr * MD + i] = f * dp[0][nb][q];
+                        M(XCK)[sr * MD + i] = f * dk[0][nb][q];
+                    }
                 __syncthreads();
             }
+        } else {
+            for (int b = 0; b < 4; ++b) {
+                const int ref = 16 * b + 7, r0 = 16 * b;
+                for (int pass = 0; pass < 2; ++pass) {
+                    const float* src = pass == 0 ? M(XQ) : sK;
+                    const float* xs = pass == 0 ? sDP : sDA;
+#pragma unroll 1
+                    for (int e0 = r0 * MD + tid; e0 < MAT; e0 += 8 * MNT) {      // (64 - r0) x 128 = 2048 multiples
+                        float yv[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) yv[u] = src[e0 + MNT * u];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int e = e0 + MNT * u, r = e >> 7, i = e & 127;
+                            sY[(r - r0) * LDY + i] = yv[u] * exp2f(G[e] - G[ref * MD + i]);
+                        }
+                    }
+                    __syncthreads();
+                    const int s = r0 + tr;
+                    float a8[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) a8[j] = 0.f;
+                    for (int r = r0; r < MC; ++r) {
+                        const float x = xs[r * LD64 + s];
+                        const float4 y0 = *reinterpret_cast<const float4*>(sY + (r - r0) * LDY + 4 * tc);
+                        const float4 y1 = *reinterpret_cast<const float4*>(sY + (r - r0) * LDY + 64 + 4 * tc);
+                        const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) a8[j] = fmaf(x, yv[j], a8[j]);
+                    }
+                    float* out = M(pass == 0 ? XCP : XCK);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int i = col8(j);
+                        out[s * MD + i] = exp2f(G[ref * MD + i] - G[s * MD + i]) * a8[j];
+                    }
+                    __syncthreads();
+                }
+            }
         }
-
         // ---- dq, dk, dv; dg into the dq_p scratch (dq_p is used only here); the rest of dbeta (row sums of
         //      Gamma k . T^T dW + v . T^T dU) and the column sums of dKhat . Khat on the way.  Element x =
         //      tid + 256 u keeps the key channel i = tid % 128; 8 elements at a time, their loads issued
