@@ -69,6 +69,13 @@ enum : int { XQ = 0, XV, XDO, XKTB, XVB, XW, XU, XKH, XDU, XDW, X_COUNT,
              XTDW = XDO, XRQ = XKTB, XRK = XVB, XDQS = XW, XCP = XU, XDKH = XKH, XCK = XDU, XTDU = XDW };
 static_assert((size_t)X_COUNT * MAT * 4 <= kBwdMatScratchBytes, "per-CTA scratch");
 
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error about 2^-22, results below 2^-126
+// flushed to zero, which only drops decay factors far below every other term)
+__device__ __forceinline__ float ex2a(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
 // 16 bytes of a token row as floats
 __device__ __forceinline__ void ld16f(const float* p, float* o) {
@@ -523,7 +530,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             float* sQB = stg + 16 * LDY;               // [16][LDY]: q_r 2^(G_r - G_ref)
             for (int e = tid; e < ns * MD; e += MNT) {
                 const int s = e >> 7, i = e & 127;
-                sY[s * LDY + i] = cv(sK[e] * exp2f(G[ref * MD + i] - G[e]));
+                sY[s * LDY + i] = cv(sK[e] * ex2a(G[ref * MD + i] - G[e]));
             }
             {
                 float qv[16 * MD / MNT];
@@ -532,7 +539,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
 #pragma unroll
                 for (int u = 0; u < 16 * MD / MNT; ++u) {
                     const int e = tid + MNT * u, r = e >> 7, i = e & 127, x = 16 * b * MD + e;
-                    const float f = exp2f(G[x] - G[ref * MD + i]);
+                    const float f = ex2a(G[x] - G[ref * MD + i]);
                     sKB[r * LDY + i] = cv(sK[x] * f);
                     sQB[r * LDY + i] = cv(qv[u] * f);
                 }
@@ -636,9 +643,9 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             for (int u = 0; u < 8; ++u) {
                 const int e = e0 + MNT * u, r = e >> 7, i = e & 127;
                 const float kk = sK[e], g = G[e];
-                M(XKTB)[e] = sbeta[r] * kk * exp2f(g);
+                M(XKTB)[e] = sbeta[r] * kk * ex2a(g);
                 M(XVB)[e] = sbeta[r] * vv[u];
-                M(XKH)[e] = kk * exp2f(sgc[i] - g);
+                M(XKH)[e] = kk * ex2a(sgc[i] - g);
             }
         }
         __syncthreads();
@@ -750,7 +757,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
             const int ref = 16 * b + 7, ns = 16 * (b + 1);
             for (int e = tid; e < ns * MD; e += MNT) {
                 const int s = e >> 7, i = e & 127;
-                sY[s * LDY + i] = sK[e] * exp2f(G[ref * MD + i] - G[e]);
+                sY[s * LDY + i] = sK[e] * ex2a(G[ref * MD + i] - G[e]);
             }
             __syncthreads();
             if constexpr (TC) {
@@ -770,7 +777,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const int r = 16 * b + g + 8 * (q >> 1), i = 8 * (warp + 8 * nb) + 2 * t + (q & 1);
-                            out[r * MD + i] = exp2f(G[r * MD + i] - G[ref * MD + i]) * d[ma][nb][q];
+                            out[r * MD + i] = ex2a(G[r * MD + i] - G[ref * MD + i]) * d[ma][nb][q];
                         }
                 }
                 __syncthreads();
@@ -794,7 +801,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = col8(j);
-                const float f = exp2f(G[r * MD + i] - G[ref * MD + i]);
+                const float f = ex2a(G[r * MD + i] - G[ref * MD + i]);
                 M(XRQ)[r * MD + i] = f * aq[j];
                 M(XRK)[r * MD + i] = f * ak[j];
             }
@@ -818,7 +825,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         const int e = e0 + MNT * u, r = e >> 7, i = e & 127;
-                        const float f = exp2f(G[e] - G[ref * MD + i]);
+                        const float f = ex2a(G[e] - G[ref * MD + i]);
                         sY[(r - r0) * LDY + i] = yv[u] * f;
                         sYk[(r - r0) * LDY + i] = sK[e] * f;
                     }
@@ -834,7 +841,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int sr = r0 + g + 8 * (q >> 1), i = 8 * (warp + 8 * nb) + 2 * t + (q & 1);
-                        const float f = exp2f(G[ref * MD + i] - G[sr * MD + i]);
+                        const float f = ex2a(G[ref * MD + i] - G[sr * MD + i]);
                         M(XCP)[sr * MD + i] = f * dp[0][nb][q];
                         M(XCK)[sr * MD + i] = f * dk[0][nb][q];
                     }
@@ -854,7 +861,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
                             const int e = e0 + MNT * u, r = e >> 7, i = e & 127;
-                            sY[(r - r0) * LDY + i] = yv[u] * exp2f(G[e] - G[ref * MD + i]);
+                            sY[(r - r0) * LDY + i] = yv[u] * ex2a(G[e] - G[ref * MD + i]);
                         }
                     }
                     __syncthreads();
@@ -874,7 +881,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int i = col8(j);
-                        out[s * MD + i] = exp2f(G[ref * MD + i] - G[s * MD + i]) * a8[j];
+                        out[s * MD + i] = ex2a(G[ref * MD + i] - G[s * MD + i]) * a8[j];
                     }
                     __syncthreads();
                 }
@@ -900,7 +907,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int x = x0 + MNT * u, r = x >> 7, i = x & 127;
-                const float gam = exp2f(G[x]), kh = exp2f(sgc[i] - G[x]);
+                const float gam = ex2a(G[x]), kh = ex2a(sgc[i] - G[x]);
                 const float kv = sK[x], be = sbeta[r];
                 const float d = qv[u] * rq[u] - kv * cp[u] + kv * rk[u] - kv * ck[u] + dqs[u] * qv[u] * gam +
                                 be * tdw[u] * kv * gam - dkh[u] * kv * kh;
@@ -925,7 +932,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         {
             const int i = tid & 127, half = tid >> 7;
             // the last row's own term: sum_s dKhat . Khat + Gamma_L . rowsum(dS_1 . S_0)
-            const float extra = scol[i] + scol[128 + i] + exp2f(sgc[i]) * srow[i];
+            const float extra = scol[i] + scol[128 + i] + ex2a(sgc[i]) * srow[i];
             float dg[32], al[32], tot = 0.f;
 #pragma unroll
             for (int rr = 0; rr < 32; ++rr) {
