@@ -56,8 +56,8 @@ constexpr int F_DA = F_DP + MC * LD64;             // dA  } products before dP (
 constexpr int F_Y = F_DA + MC * LD64;              //     } cp.async ring over them, with more stages in flight
                                                    // scaled operands [64][LDY]; dT and X [64][LD64] each
 constexpr int F_STG = F_Y + 2 * MC * LD64;         // product staging: A [16][LD64], B [16][LDY]; also 2 x [16][LDY]
-constexpr int F_VEC = F_STG + 2 * 16 * LDY;        // beta [64], G_C [128], row sums [128], column sums [2][128], 2 x [64]
-constexpr int F_K = F_VEC + 64 + 128 + 128 + 256 + 64 + 64;   // k [64][128]
+constexpr int F_VEC = F_STG + 2 * 16 * LDY;        // beta [64], G_C [128], row sums [128], column sums [2][128], [64]
+constexpr int F_K = F_VEC + 64 + 128 + 128 + 256 + 64;        // k [64][128]
 constexpr int F_G = F_K + MC * MD;                 // G [64][128]
 constexpr int MAT_SMEM_FLOATS = F_G + MC * MD;
 static_assert(2 * MC * LD64 >= MC * LDY, "scaled operand area");
@@ -161,6 +161,45 @@ __device__ __forceinline__ void tiles_mma3(float (&d)[MA][NB][4], int ksteps, FA
         for (int ma = 0; ma < MA; ++ma)
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) mma_tf32(d[ma][nb], ah[ma], bh[nb][0], bh[nb][1]);
+    }
+}
+// The same for MA products that share no operand, d[ma] += A_ma B_ma (B fragments per ma), in one k-loop so
+// that their MMA chains interleave.
+template <int MA, int NB, class FA, class FB>
+__device__ __forceinline__ void tiles_mma3_sep(float (&d)[MA][NB][4], int ksteps, FA fa, FB fb) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    auto split = [](float x, uint32_t& hi, uint32_t& lo) {
+        hi = tf32_bits(x);
+        lo = tf32_bits(x - __uint_as_float(hi));
+    };
+#pragma unroll 1
+    for (int ks = 0; ks < ksteps; ++ks) {
+        const int k0 = 8 * ks;
+        uint32_t ah[MA][4], al[MA][4], bh[MA][NB][2], bl[MA][NB][2];
+#pragma unroll
+        for (int ma = 0; ma < MA; ++ma) {
+            split(fa(ma, g, k0 + t), ah[ma][0], al[ma][0]);
+            split(fa(ma, g + 8, k0 + t), ah[ma][1], al[ma][1]);
+            split(fa(ma, g, k0 + t + 4), ah[ma][2], al[ma][2]);
+            split(fa(ma, g + 8, k0 + t + 4), ah[ma][3], al[ma][3]);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                split(fb(ma, nb, k0 + t, g), bh[ma][nb][0], bl[ma][nb][0]);
+                split(fb(ma, nb, k0 + t + 4, g), bh[ma][nb][1], bl[ma][nb][1]);
+            }
+        }
+#pragma unroll
+        for (int ma = 0; ma < MA; ++ma)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_tf32(d[ma][nb], al[ma], bh[ma][nb][0], bh[ma][nb][1]);
+#pragma unroll
+        for (int ma = 0; ma < MA; ++ma)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_tf32(d[ma][nb], ah[ma], bl[ma][nb][0], bl[ma][nb][1]);
+#pragma unroll
+        for (int ma = 0; ma < MA; ++ma)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_tf32(d[ma][nb], ah[ma], bh[ma][nb][0], bh[ma][nb][1]);
     }
 }
 // outputs written once: streaming stores, so that they do not push the scratch out of L2
@@ -412,7 +451,6 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
     float* srow = sgc + 128;                           // sum_j dS_1[i][j] S_0[i][j], per key channel i
     float* scol = srow + 128;                          // [2][128] column partial sums
     float* sdb = scol + 256;                           // [64] sum_s dA_rs Bt_rs
-    float* sdb2 = sdb + 64;                            // [64] the rest of dbeta, by row
     float* sK = fsm + F_K;
     float* sG = fsm + F_G;
     const float* G = sG;
@@ -831,19 +869,20 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
                     }
                 }
                 __syncthreads();
-                float dp[1][2][4] = {}, dk[1][2][4] = {};
-                tiles_mma3<1, 2>(dp, (MC - r0) / 8, [&](int, int m, int k) { return sDP[(r0 + k) * LD64 + r0 + m]; },
-                                 [&](int nb, int k, int n) { return sY[k * LDY + 8 * (warp + 8 * nb) + n]; });
-                tiles_mma3<1, 2>(dk, (MC - r0) / 8, [&](int, int m, int k) { return sDA[(r0 + k) * LD64 + r0 + m]; },
-                                 [&](int nb, int k, int n) { return sYk[k * LDY + 8 * (warp + 8 * nb) + n]; });
+                float dd[2][2][4] = {};                    // [0]: X = dP, Y = Y_q; [1]: X = dBt, Y = Y_k
+                tiles_mma3_sep<2, 2>(dd, (MC - r0) / 8,
+                                     [&](int ma, int m, int k) { return (ma ? sDA : sDP)[(r0 + k) * LD64 + r0 + m]; },
+                                     [&](int ma, int nb, int k, int n) {
+                                         return (ma ? sYk : sY)[k * LDY + 8 * (warp + 8 * nb) + n];
+                                     });
 #pragma unroll
                 for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int sr = r0 + g + 8 * (q >> 1), i = 8 * (warp + 8 * nb) + 2 * t + (q & 1);
                         const float f = ex2a(G[ref * MD + i] - G[sr * MD + i]);
-                        M(XCP)[sr * MD + i] = f * dp[0][nb][q];
-                        M(XCK)[sr * MD + i] = f * dk[0][nb][q];
+                        M(XCP)[sr * MD + i] = f * dd[0][nb][q];
+                        M(XCK)[sr * MD + i] = f * dd[1][nb][q];
                     }
                 __syncthreads();
             }
@@ -891,8 +930,6 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         //      Gamma k . T^T dW + v . T^T dU) and the column sums of dKhat . Khat on the way.  Element x =
         //      tid + 256 u keeps the key channel i = tid % 128; 8 elements at a time, their loads issued
         //      before any store ----
-        if (tid < MC) sdb2[tid] = 0.f;
-        __syncthreads();
         float colp = 0.f;
 #pragma unroll 1
         for (int x0 = tid; x0 < MAT; x0 += 8 * MNT) {
@@ -912,10 +949,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
                 const float d = qv[u] * rq[u] - kv * cp[u] + kv * rk[u] - kv * ck[u] + dqs[u] * qv[u] * gam +
                                 be * tdw[u] * kv * gam - dkh[u] * kv * kh;
                 colp = fmaf(dkh[u], kv * kh, colp);
-                float db = fmaf(kv * gam, tdw[u], vv[u] * tdu[u]);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) db += __shfl_xor_sync(0xffffffffu, db, o);
-                if (lane == 0) atomicAdd(&sdb2[r], db);
+                sY[r * LDY + i] = fmaf(kv * gam, tdw[u], vv[u] * tdu[u]);     // summed by rows below
                 M(XRQ)[x] = r < L ? d : 0.f;
                 if (r < L) {
                     const int64_t o = ((int64_t)(t0 + r) * H + h) * MD + i;
@@ -927,7 +961,18 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         }
         scol[(tid >> 7) * 128 + (tid & 127)] = colp;
         __syncthreads();
-        if (tid < L) p.d_beta[(int64_t)(t0 + tid) * H + h] = sdb[tid] + sdb2[tid];
+        {                                              // row sums of the dbeta terms: four threads per row
+            const int r = tid >> 2, q4 = tid & 3;
+            float db = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float4 v4 = *reinterpret_cast<const float4*>(sY + r * LDY + 32 * q4 + j);
+                db += (v4.x + v4.y) + (v4.z + v4.w);
+            }
+            db += __shfl_xor_sync(0xffffffffu, db, 1);
+            db += __shfl_xor_sync(0xffffffffu, db, 2);
+            if (q4 == 0 && r < L) p.d_beta[(int64_t)(t0 + r) * H + h] = sdb[r] + db;
+        }
         // ---- d ln alpha = running sum of dg from the last row up; dalpha = d ln alpha / alpha ----
         {
             const int i = tid & 127, half = tid >> 7;
