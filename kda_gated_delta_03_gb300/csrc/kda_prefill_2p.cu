@@ -231,6 +231,9 @@ template <bool MULTI>
 __global__ void __launch_bounds__(NT, 1)
     kda_prefill_prep_kernel(PrefillParams p, const __grid_constant__ PrepMaps maps, unsigned char* records,
                             int c_begin, int n_units, const int32_t* choff_arg) {
+    // the chain kernel after this one may be scheduled at once: its CTAs take SMs as this kernel's leave
+    // (neither fits beside the other) and wait for its completion before reading a record
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int32_t* choff = MULTI ? choff_arg : nullptr;
     const int32_t* cu = nullptr;                     // cu_seqlens for the chunk lookups (global unless cached)
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -1034,6 +1037,9 @@ __global__ void __launch_bounds__(C_NT, 1)
         m = __reduce_max_sync(0xffffffffu, m);
         if (lane == 0) s_smx[warp] = m;
     }
+    // launched as phase 1's programmatic dependent (one stream): everything above reads only what was
+    // written before phase 1 started; the records are read below, once phase 1 has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1657,15 +1663,30 @@ cudaError_t launch_prefill_2p(const PrefillParams& p, void* workspace, size_t wo
             if ((e = cudaEventRecord(ss->prep_done[buf], ps)) != cudaSuccess) return e;
             if ((e = cudaStreamWaitEvent(s, ss->prep_done[buf], 0)) != cudaSuccess) return e;
         }
+        // on one stream the chain is phase 1's programmatic dependent: its launch and prologue overlap phase
+        // 1's last units (it waits for phase 1's completion before its first record read)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)chain_ctas);
+        cfg.blockDim = dim3(C_NT);
+        cfg.dynamicSmemBytes = C_SMEM;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = ss ? 0 : 1;
+        const unsigned char* crec = rec;
+        const int cb = (int)c0, cn = (int)n;
         if (multi)
-            kda_prefill_chain_kernel<true, 32><<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n, choff,
-                                                                                        order);
+            e = cudaLaunchKernelEx(&cfg, kda_prefill_chain_kernel<true, 32>, p, crec, cb, cn,
+                                   static_cast<const int32_t*>(choff), static_cast<const int32_t*>(order));
         else if (nv == 16)
-            kda_prefill_chain_kernel<false, 16><<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n,
-                                                                                         nullptr, nullptr);
+            e = cudaLaunchKernelEx(&cfg, kda_prefill_chain_kernel<false, 16>, p, crec, cb, cn,
+                                   static_cast<const int32_t*>(nullptr), static_cast<const int32_t*>(nullptr));
         else
-            kda_prefill_chain_kernel<false, 32><<<(unsigned)chain_ctas, C_NT, C_SMEM, s>>>(p, rec, (int)c0, (int)n,
-                                                                                         nullptr, nullptr);
+            e = cudaLaunchKernelEx(&cfg, kda_prefill_chain_kernel<false, 32>, p, crec, cb, cn,
+                                   static_cast<const int32_t*>(nullptr), static_cast<const int32_t*>(nullptr));
+        if (e != cudaSuccess) return e;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (ss && (e = cudaEventRecord(ss->chain_done[buf], s)) != cudaSuccess) return e;
     }
