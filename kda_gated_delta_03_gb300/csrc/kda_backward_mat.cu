@@ -636,17 +636,18 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
         //      (a thread per column), then T_bc = -T_bb sum_{m = c}^{b - 1} A_bm T_mc in order of b - c ----
         for (int e = tid; e < MC * MC; e += MNT) sT[(e >> 6) * LD64 + (e & 63)] = 0.f;
         __syncthreads();
-        if (tid < MC) {
+        if (tid < MC) {                                // a thread per column c of diagonal block b
             const int b = tid >> 4, c = tid & 15;
-            float t[16];
+            // right-looking: once t[m] is known it enters every later row's sum (the same FMAs in the same
+            // order per sum as row by row, with a dependent path of one FMA per row)
+            float t[16], z[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) t[r] = r == c ? 1.f : 0.f;
+            for (int r = 0; r < 16; ++r) z[r] = 0.f;
 #pragma unroll
-            for (int r = 1; r < 16; ++r) {
-                float z = 0.f;
+            for (int m = 0; m < 16; ++m) {
+                t[m] = m == c ? 1.f : (m > c ? -sbeta[16 * b + m] * z[m] : 0.f);
 #pragma unroll
-                for (int m = 0; m < r; ++m) z = fmaf(sBT[(16 * b + r) * LD64 + 16 * b + m], t[m], z);
-                if (r > c) t[r] = -sbeta[16 * b + r] * z;
+                for (int r = m + 1; r < 16; ++r) z[r] = fmaf(sBT[(16 * b + r) * LD64 + 16 * b + m], t[m], z[r]);
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) sT[(16 * b + r) * LD64 + 16 * b + c] = t[r];
