@@ -927,10 +927,11 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
                 }
             }
         }
-        // ---- dq, dk, dv; dg into the dq_p scratch (dq_p is used only here); the rest of dbeta (row sums of
-        //      Gamma k . T^T dW + v . T^T dU) and the column sums of dKhat . Khat on the way.  Element x =
-        //      tid + 256 u keeps the key channel i = tid % 128; 8 elements at a time, their loads issued
-        //      before any store ----
+        // ---- dq, dk, dv; dg into shared memory (the P and T area, free since the column-side sums); the
+        //      rest of dbeta (row sums of Gamma k . T^T dW + v . T^T dU) and the column sums of dKhat . Khat
+        //      on the way.  Element x = tid + 256 u keeps the key channel i = tid % 128; 8 elements at a
+        //      time, their loads issued before any store ----
+        float* sDG = sP;                               // [64][128]
         float colp = 0.f;
 #pragma unroll 1
         for (int x0 = tid; x0 < MAT; x0 += 8 * MNT) {
@@ -951,7 +952,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
                                 be * tdw[u] * kv * gam - dkh[u] * kv * kh;
                 colp = fmaf(dkh[u], kv * kh, colp);
                 sY[r * LDY + i] = fmaf(kv * gam, tdw[u], vv[u] * tdu[u]);     // summed by rows below
-                M(XRQ)[x] = r < L ? d : 0.f;
+                sDG[x] = r < L ? d : 0.f;
                 if (r < L) {
                     const int64_t o = ((int64_t)(t0 + r) * H + h) * MD + i;
                     st_out(gdq, o, rq[u] + dqs[u] * gam);
@@ -983,7 +984,7 @@ __global__ void __launch_bounds__(MNT, 1) kda_bwd_chunk_mat_kernel(BwdParams p) 
 #pragma unroll
             for (int rr = 0; rr < 32; ++rr) {
                 const int r = 32 * half + rr;
-                dg[rr] = M(XRQ)[r * MD + i] + (r == L - 1 ? extra : 0.f);
+                dg[rr] = sDG[r * MD + i] + (r == L - 1 ? extra : 0.f);
                 al[rr] = r < L ? __ldg(p.alpha + ((int64_t)(t0 + r) * H + h) * MD + i) : 1.f;
                 tot += dg[rr];
             }
