@@ -685,6 +685,22 @@ def run_append(args, w, dev, peaks, line, world, local_rank):
     return line
 
 
+def workload_config(name, world):
+    """The `config` object of a workload's bench line: the workload itself (the GPU arm's keys), whatever
+    sample of it an arm times."""
+    if name.startswith("decode_512x32"):
+        w = I.workload("decode_512x32")
+        bf = name.endswith("bf16_state")
+        return {"workload": name, "B": w["B"], "H": w["H"], "d": w["dk"], "qkv": w["dtype"],
+                "state": "bf16" if bf else "f32", "l2": f"state pool ({'0.5' if bf else '1'} GiB) larger than L2"}
+    w = I.workload(name)
+    if name == "append_1m":
+        return {"workload": name, "prefill_tokens": int(sum(w["seqlens"])), "append_tokens": int(w["append"]),
+                "H": w["H"], "d": w["dk"], "l2": "inputs larger than L2 (no flush)"}
+    return {"workload": name, "seqs": len(w["seqlens"]), "tokens": int(sum(w["seqlens"])), "H": w["H"], "d": w["dk"],
+            "qkv": w["dtype"], "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{world}"}
+
+
 def run_reference(args, rank, world):
     """The float64 CPU oracle on the host cores, one bounded sample of the workload per step."""
     if rank != 0:
@@ -738,7 +754,7 @@ def run_reference(args, rank, world):
     return {"impl": "reference", "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": name},
+            "config": workload_config(name, world),
             "cpu_baseline": {"value": round(value, 3), "unit": unit, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 3), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
