@@ -520,9 +520,7 @@ def run_ours(args, rank, world, local_rank):
         line.update(metric="KDA decode steps/s (512 seqs x 32 heads, d=128)", value=round(steps_s, 2),
                     unit="steps/s", ms_per_step=round(ms, 4),
                     dtype=DECODE_DTYPE if sdt == "f32" else "bf16 q/k/v and state; fp32 arithmetic",
-                    config={"workload": name, "B": w["B"], "H": w["H"], "d": w["dk"], "qkv": w["dtype"],
-                            "state": "bf16" if sdt == "bf16" else "f32",
-                            "l2": f"state pool ({'0.5' if sdt == 'bf16' else '1'} GiB) larger than L2"},
+                    config=workload_config(name, world),
                     roofline=roofline_obj(r["bytes_per_step"], r["kernel_ms"], peaks,
                                           "decode_bf16" if sdt == "bf16" else "decode",
                                           DECODE_BF16S_SRC if sdt == "bf16" else DECODE_KERNEL_SRC,
@@ -545,8 +543,7 @@ def run_ours(args, rank, world, local_rank):
     alg = prefill_bytes(tokens, r["H"], inp["dk"], inp["dv"], esize, 0 if inp["state_in"] is None else r["N"], r["N"])
     line.update(value=round(world * tokens * 1e3 / ms, 1), unit="tokens/s", ms_per_step=round(ms, 4),
                 dtype=PREFILL_DTYPE if inp["dtype"] == "bf16" else "f32",
-                config={"workload": name, "seqs": r["N"], "tokens": tokens, "H": r["H"], "d": inp["dk"],
-                        "qkv": inp["dtype"], "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{world}"},
+                config=workload_config(name, world),
                 roofline=roofline_obj(alg, r["kernel_ms"], peaks, *prefill_path(r["N"], inp["dtype"], inp["dk"]), name),
                 e2e={"value": round(world * tokens * 1e3 / e2e_ms, 1), "unit": "tokens/s",
                      "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
@@ -672,8 +669,7 @@ def run_append(args, w, dev, peaks, line, world, local_rank):
     line.update(metric="KDA append-prefill tokens/s (H=8, d=128): 1,032,192-token prefill",
                 value=round(world * T1 * 1e3 / a["ms1"], 1), unit="tokens/s", ms_per_step=round(a["ms1"], 4),
                 dtype=PREFILL_DTYPE,
-                config={"workload": "append_1m", "prefill_tokens": T1, "append_tokens": T2, "H": w["H"],
-                        "d": w["dk"], "l2": "inputs larger than L2 (no flush)"},
+                config=workload_config("append_1m", world),
                 roofline=a["roof1"],
                 e2e={"value": round(world * T1 * 1e3 / r1["e2e_ms"], 1), "unit": "tokens/s",
                      "h2d_bytes_per_step": r1["h2d"], "d2h_bytes_per_step": r1["d2h"]},
