@@ -316,11 +316,19 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_after();
         return true;
     };
+    // several sequences: the span of this CTA's next unit, found once per unit (with its beta) and kept in
+    // shared memory for that unit's tile fetches and its own start
+    int32_t* s_span = reinterpret_cast<int32_t*>(sm + P_OFF_MISC + 48);
+    int span_unit = -1;                               // the unit s_span holds (block-uniform)
     // raw tiles of unit u by TMA (v with one 128-column box), in three groups
     auto unit_rows = [&](int u, int& hu, int32_t& tu) {
         hu = u % H;
-        int32_t te;
-        chunk_span(p, choff, (int64_t)c_begin + u / H, tu, te, cu);
+        if (MULTI && u == span_unit) {
+            tu = s_span[0];
+        } else {
+            int32_t te;
+            chunk_span(p, choff, (int64_t)c_begin + u / H, tu, te, cu);
+        }
     };
     auto issue_v = [&](int u) {                      // arms vkbar for v and k together
         if (tid == 32) {
@@ -436,7 +444,12 @@ __global__ void __launch_bounds__(NT, 1)
 
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         int32_t t0, t_end;                              // the chunk's first token and its sequence's end
-        chunk_span(p, choff, (int64_t)c_begin + u / H, t0, t_end, cu);
+        if (MULTI && u == span_unit) {
+            t0 = s_span[0];
+            t_end = s_span[1];
+        } else {
+            chunk_span(p, choff, (int64_t)c_begin + u / H, t0, t_end, cu);
+        }
         const int L = min(C, t_end - t0);
         unsigned char* rec = records + (size_t)u * REC_BYTES;
         const int un = u + (int)gridDim.x;                       // this CTA's next unit
@@ -456,7 +469,14 @@ __global__ void __launch_bounds__(NT, 1)
             const int64_t row = (int64_t)(tn + tid) * H + un % H;
             beta_next = tn + tid < tn_end ? p.beta[row] : 0.f;
             alpha_next = per_head && tn + tid < tn_end ? p.alpha[row] : 1.f;
+            if (MULTI && tid == 0) {
+                s_span[0] = tn;
+                s_span[1] = tn_end;
+            }
         }
+        // s_span is read (tile fetches of unit un, the start of the next iteration) only after this unit's
+        // next barrier
+        if (MULTI) span_unit = un < n_units ? un : -1;
         if (L < C) {                                    // rows past the sequence end read as zero
             for (int e = tid; e < (C - L) * 16; e += NT) {
                 const int r = L + (e >> 4), c = e & 15;
